@@ -1,0 +1,204 @@
+/*
+ * Reference oracle for causal kernelized linear attention — TEST INFRASTRUCTURE.
+ *
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+ * load this file's library.  It shares no code, header, table or helper with the
+ * CUDA library; it is a plain, slow, fp64 transcription of the method so that a
+ * reader can check it against the pages by eye.
+ *
+ * Sources (cited by page title and equation):
+ *   [ET-II]  "Efficient Transformers II" (blog-8pb.pages.dev, .../efficient2/),
+ *            §2.2 Linear Attention, eq (6)–(11).
+ *   [ET-I]   "Efficient Transformers I" (blog-8pb.pages.dev, .../efficient1/),
+ *            kernelized attention, eq (22)–(27).
+ *   [LAR]    "Linear Attention Research 2026" (guijiagi.com), sections
+ *            "Performer random features" and "Linear Transformer".
+ *
+ * Conventions: row vectors; q_j, k_j, v_j in R^{1×d}; φ: R^d → R^{d'}; the
+ * state μ is d'×d (row i = feature i, column c = value column c), ν is d'.
+ * Tensors are dense row-major [B, H, n, d] (d innermost); μ is [B, H, d', d],
+ * ν is [B, H, d'].  Everything is double precision.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - elu uses α = 1, so φ(x) = x + 1 for x > 0 and e^x otherwise [LAR].
+ *   - a == 1 means the plain running sums of eq (7)–(8) (weight w = 1); any
+ *     other a uses eq (10)–(11) with w = 1 − a [ET-II].
+ *   - The causal readout uses μ_j, ν_j, i.e. token j itself is included
+ *     ([ET-II] the causal form stated after eq (9)).
+ *   - No ε is added to the normalizer.
+ *   - Non-causal mode is eq (6)/(9) with μ_n, ν_n and no decay.
+ *
+ * parity pins: every function here is pinned by the CPU tests (quadratic form
+ * of [ET-I] eq (25)–(26) by brute force and in exact rationals, the a = 0
+ * closed form, eq (6) as dense products, positivity and convexity, the
+ * Performer expectation, ω = 0 and single-entry ω closed forms).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_FM_ELU1 = 0, OR_FM_PERFORMER = 1 };
+
+/* φ(x) = elu(x) + 1, α = 1  ([LAR] "Linear Transformer"). */
+static double phi_elu1_scalar(double x) { return x > 0.0 ? x + 1.0 : exp(x); }
+
+/* Performer positive random features ([LAR] "Performer random features"):
+ *   φ(x)_i = exp(x·ω_i − ½‖x‖²) / √m,
+ * where ω is stored d×m row-major and ω_i is its i-th column. */
+static void phi_performer_vec(const double* x, int64_t d, const double* omega,
+                              int64_t m, double* out) {
+  double sq = 0.0;
+  for (int64_t c = 0; c < d; ++c) sq += x[c] * x[c];
+  const double inv_sqrt_m = 1.0 / sqrt((double)m);
+  for (int64_t i = 0; i < m; ++i) {
+    double u = 0.0;
+    for (int64_t c = 0; c < d; ++c) u += x[c] * omega[c * m + i];
+    out[i] = exp(u - 0.5 * sq) * inv_sqrt_m;
+  }
+}
+
+/* φ applied to one row x ∈ R^d, result in R^{d'}. */
+static void phi_row(int fm, const double* x, int64_t d, const double* omega,
+                    int64_t m, double* out) {
+  if (fm == OR_FM_ELU1) {
+    for (int64_t c = 0; c < d; ++c) out[c] = phi_elu1_scalar(x[c]);
+  } else {
+    phi_performer_vec(x, d, omega, m, out);
+  }
+}
+
+/* Feature dimension d' of the map: d for elu+1, m for Performer. */
+static int64_t feature_dim(int fm, int64_t d, int64_t m) {
+  return fm == OR_FM_ELU1 ? d : m;
+}
+
+/* Public: φ on a batch of rows, x [rows, d] → out [rows, d']. */
+int oracle_features(int64_t rows, int64_t d, int fm, int64_t m,
+                    const double* x, const double* omega, double* out) {
+  if (fm != OR_FM_ELU1 && fm != OR_FM_PERFORMER) return 1;
+  if (fm == OR_FM_PERFORMER && (omega == NULL || m <= 0)) return 1;
+  const int64_t dp = feature_dim(fm, d, m);
+  for (int64_t r = 0; r < rows; ++r) phi_row(fm, x + r * d, d, omega, m, out + r * dp);
+  return 0;
+}
+
+/*
+ * One (b, h) head of the method.
+ *
+ * Causal ([ET-II] eq (7)–(11) and the causal readout after eq (9)): for each
+ * token j in order
+ *     k' = φ(k_j);  μ ← a·μ + w·k'^T v_j;  ν ← a·ν + w·k'^T;
+ *     q' = φ(q_j);  o_j = (q'·μ) / (q'·ν).
+ * Non-causal ([ET-II] eq (6) read as eq (9)): run the same sums over all n
+ * tokens (a = 1), then o_j = (q'_j·μ_n) / (q'_j·ν_n) for every j.
+ */
+static void one_head(int64_t n, int64_t d, int64_t dp, int fm, int64_t m,
+                     const double* q, const double* k, const double* v,
+                     double a, const double* omega, int causal,
+                     double* mu, double* nu, double* out,
+                     double* kf, double* qf) {
+  const double w = (a == 1.0) ? 1.0 : (1.0 - a);
+  for (int64_t j = 0; j < n; ++j) {
+    const double* kj = k + j * d;
+    const double* vj = v + j * d;
+    phi_row(fm, kj, d, omega, m, kf);
+    for (int64_t i = 0; i < dp; ++i) {
+      for (int64_t c = 0; c < d; ++c) {
+        mu[i * d + c] = a * mu[i * d + c] + w * kf[i] * vj[c];
+      }
+      nu[i] = a * nu[i] + w * kf[i];
+    }
+    if (causal) {
+      phi_row(fm, q + j * d, d, omega, m, qf);
+      double den = 0.0;
+      for (int64_t i = 0; i < dp; ++i) den += qf[i] * nu[i];
+      for (int64_t c = 0; c < d; ++c) {
+        double num = 0.0;
+        for (int64_t i = 0; i < dp; ++i) num += qf[i] * mu[i * d + c];
+        out[j * d + c] = num / den;
+      }
+    }
+  }
+  if (!causal) {
+    for (int64_t j = 0; j < n; ++j) {
+      phi_row(fm, q + j * d, d, omega, m, qf);
+      double den = 0.0;
+      for (int64_t i = 0; i < dp; ++i) den += qf[i] * nu[i];
+      for (int64_t c = 0; c < d; ++c) {
+        double num = 0.0;
+        for (int64_t i = 0; i < dp; ++i) num += qf[i] * mu[i * d + c];
+        out[j * d + c] = num / den;
+      }
+    }
+  }
+}
+
+/*
+ * Forward over B·H independent heads.
+ *   q, k, v   [B,H,n,d]
+ *   a         [H] per-head decay, or NULL for a = 1 (eq (7)–(8))
+ *   omega     [d,m] for Performer, else NULL
+ *   mu0, nu0  initial state [B,H,d',d], [B,H,d'], or NULL for zero
+ *   out       [B,H,n,d]
+ *   mu_out, nu_out  final state, or NULL
+ * Returns 0 on success, 1 on invalid arguments (non-causal with a decay,
+ * unknown feature map, missing ω, or a decay outside [0, 1]).
+ * Heads run in parallel with OpenMP when the library is built with it.
+ */
+int oracle_forward(int64_t B, int64_t H, int64_t n, int64_t d, int fm, int64_t m,
+                   const double* q, const double* k, const double* v,
+                   const double* a, const double* omega, int causal,
+                   const double* mu0, const double* nu0,
+                   double* out, double* mu_out, double* nu_out) {
+  if (fm != OR_FM_ELU1 && fm != OR_FM_PERFORMER) return 1;
+  if (fm == OR_FM_PERFORMER && (omega == NULL || m <= 0)) return 1;
+  if (!causal && a != NULL) return 1;
+  if (a != NULL) {
+    for (int64_t h = 0; h < H; ++h) {
+      if (!(a[h] >= 0.0 && a[h] <= 1.0)) return 1;
+    }
+  }
+  const int64_t dp = feature_dim(fm, d, m);
+  int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bh = 0; bh < B * H; ++bh) {
+    const int64_t h = bh % H;
+    double* mu = (double*)malloc((size_t)(dp * d) * sizeof(double));
+    double* nu = (double*)malloc((size_t)dp * sizeof(double));
+    double* kf = (double*)malloc((size_t)dp * sizeof(double));
+    double* qf = (double*)malloc((size_t)dp * sizeof(double));
+    if (!mu || !nu || !kf || !qf) {
+      failed = 1;
+    } else {
+      if (mu0) memcpy(mu, mu0 + bh * dp * d, (size_t)(dp * d) * sizeof(double));
+      else memset(mu, 0, (size_t)(dp * d) * sizeof(double));
+      if (nu0) memcpy(nu, nu0 + bh * dp, (size_t)dp * sizeof(double));
+      else memset(nu, 0, (size_t)dp * sizeof(double));
+      const double ah = a ? a[h] : 1.0;
+      one_head(n, d, dp, fm, m, q + bh * n * d, k + bh * n * d, v + bh * n * d,
+               ah, omega, causal, mu, nu, out + bh * n * d, kf, qf);
+      if (mu_out) memcpy(mu_out + bh * dp * d, mu, (size_t)(dp * d) * sizeof(double));
+      if (nu_out) memcpy(nu_out + bh * dp, nu, (size_t)dp * sizeof(double));
+    }
+    free(mu);
+    free(nu);
+    free(kf);
+    free(qf);
+  }
+  return failed ? 2 : 0;
+}
+
+/*
+ * One recurrent decode step ([ET-II] eq (10)–(11), then the causal readout):
+ * the state (μ, ν) of every head is advanced in place by one token with the
+ * elu+1 map and the head's decay, and o = q'μ / q'ν is written.
+ *   mu [B,H,d,d], nu [B,H,d], q/k/v/out [B,H,d], a [H] or NULL.
+ */
+int oracle_decode_step(int64_t B, int64_t H, int64_t d, double* mu, double* nu,
+                       const double* q, const double* k, const double* v,
+                       const double* a, double* out) {
+  return oracle_forward(B, H, 1, d, OR_FM_ELU1, 0, q, k, v, a, NULL, 1, mu, nu,
+                        out, mu, nu);
+}

@@ -1,0 +1,128 @@
+"""Seeded synthetic inputs for causal kernelized linear attention.
+
+This module is shared by the tests, the benchmark and the smoke check, on
+both sides of every parity comparison (the CUDA library and the fp64 oracle).
+It holds shapes and random draws only — none of the method's arithmetic.
+
+Every draw uses a torch CPU ``Generator`` so that the values do not depend on
+the device.  Draw order per forward workload: q, k, v, a, ω.  Values that the
+workload stores in bf16 are rounded with round-to-nearest-even by the dtype
+cast.  The workloads mirror the shapes and value distributions of the method
+description ("Efficient Transformers II" §2.2 eq (6)–(11); "Linear Attention
+Research 2026", Performer and elu+1 sections); no public dataset is involved.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional, Tuple
+
+import torch
+
+
+@dataclass(frozen=True)
+class ForwardWorkload:
+    name: str
+    B: int
+    H: int
+    n: int
+    d: int
+    dtype: str                 # "bf16" or "f32"
+    feature_map: str           # "elu1" or "performer"
+    m: int = 0                 # Performer feature count (d' = m)
+    decay: Optional[Tuple[float, float]] = None  # a_h ~ U[lo, hi], None => a = 1
+    seed: int = 0
+    qk_scale: float = 1.0      # multiplies q and k before rounding
+    omega_std: Optional[float] = None  # ω ~ N(0, omega_std²); None => d^-1/2
+    modes: Tuple[str, ...] = ("causal",)
+
+    @property
+    def dprime(self) -> int:
+        return self.d if self.feature_map == "elu1" else self.m
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.n
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    B: int
+    H: int
+    d: int
+    prefill: int
+    steps: int
+    decay: Tuple[float, float]
+    seed: int
+
+
+# The five workloads of the method's evaluation plan.
+TINY_FP32 = ForwardWorkload("tiny_fp32_B1_H1_n256_d32", 1, 1, 256, 32, "f32", "elu1",
+                            seed=0, modes=("causal", "noncausal"))
+ELU1_DECAY = ForwardWorkload("elu1_decay_B4_H8_n2048_d64", 4, 8, 2048, 64, "bf16", "elu1",
+                             decay=(0.9, 0.999), seed=1)
+PERFORMER = ForwardWorkload("performer_B2_H8_n4096_d64_m256", 2, 8, 4096, 64, "bf16",
+                            "performer", m=256, seed=2, qk_scale=64 ** -0.25,
+                            modes=("noncausal", "causal"))
+LONG = ForwardWorkload("long_B1_H16_n65536_d128", 1, 16, 65536, 128, "bf16", "elu1",
+                       decay=(0.95, 0.9999), seed=3)
+DECODE = DecodeWorkload("decode_B256_H32_d128", 256, 32, 128, prefill=512, steps=1024,
+                        decay=(0.9, 0.999), seed=4)
+
+FORWARD_WORKLOADS = {w.name: w for w in (TINY_FP32, ELU1_DECAY, PERFORMER, LONG)}
+
+_TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def torch_dtype(name: str) -> torch.dtype:
+    return _TORCH_DTYPE[name]
+
+
+def make_forward_inputs(B, H, n, d, dtype="bf16", feature_map="elu1", m=0,
+                        decay=None, seed=0, qk_scale=1.0, omega_std=None):
+    """Return a dict of CPU tensors: q, k, v [B,H,n,d] in ``dtype``,
+    a [H] fp32 or None, omega [d,m] in ``dtype`` or None."""
+    g = torch.Generator().manual_seed(int(seed))
+    dt = _TORCH_DTYPE[dtype]
+    q = torch.randn(B, H, n, d, generator=g)
+    k = torch.randn(B, H, n, d, generator=g)
+    v = torch.randn(B, H, n, d, generator=g)
+    if qk_scale != 1.0:
+        q = q * qk_scale
+        k = k * qk_scale
+    a = None
+    if decay is not None:
+        lo, hi = decay
+        a = (torch.rand(H, generator=g, dtype=torch.float64) * (hi - lo) + lo).float()
+    omega = None
+    if feature_map == "performer":
+        std = (d ** -0.5) if omega_std is None else omega_std
+        omega = (torch.randn(d, m, generator=g) * std).to(dt)
+    return {"q": q.to(dt), "k": k.to(dt), "v": v.to(dt), "a": a, "omega": omega}
+
+
+def forward_inputs(w: ForwardWorkload, n: Optional[int] = None, B: Optional[int] = None,
+                   H: Optional[int] = None):
+    """Inputs of a named workload (optionally with fewer tokens/heads for a
+    quick case drawn the same way)."""
+    return make_forward_inputs(B or w.B, H or w.H, n or w.n, w.d, w.dtype, w.feature_map,
+                               w.m, w.decay, w.seed, w.qk_scale, w.omega_std)
+
+
+def decode_prefill_inputs(w: DecodeWorkload, B: Optional[int] = None, H: Optional[int] = None):
+    """Prefill q, k, v [B,H,prefill,d] bf16 and the per-head decay a [H] fp32."""
+    return make_forward_inputs(B or w.B, H or w.H, w.prefill, w.d, "bf16", "elu1",
+                               decay=w.decay, seed=w.seed)
+
+
+def decode_step_inputs(w: DecodeWorkload, step: int, B: Optional[int] = None,
+                       H: Optional[int] = None):
+    """Fresh bf16 q, k, v [B,H,d] for one decode step; each step has its own
+    seed so that any step can be regenerated on its own."""
+    g = torch.Generator().manual_seed(int(w.seed) * 1_000_003 + 7919 * (int(step) + 1))
+    B = B or w.B
+    H = H or w.H
+    q = torch.randn(B, H, w.d, generator=g)
+    k = torch.randn(B, H, w.d, generator=g)
+    v = torch.randn(B, H, w.d, generator=g)
+    return {"q": q.bfloat16(), "k": k.bfloat16(), "v": v.bfloat16()}
