@@ -1,0 +1,21 @@
+"""Causal kernelized linear attention for GB300 (sm_103a).
+
+Python face of liblinattn (C ABI in include/linattn.h).  The method
+("Efficient Transformers II" §2.2 eq (6)–(11); "Linear Attention Research
+2026", elu+1 and Performer feature maps):
+
+* ``forward`` — o_j = q'_j·μ_j / q'_j·ν_j with μ_j = a·μ_{j−1} + (1−a)·k'_jᵀv_j,
+  ν_j = a·ν_{j−1} + (1−a)·k'_jᵀ (plain sums for a = 1), or the non-causal
+  D⁻¹(Q'(K'ᵀV)) of eq (6);
+* ``forward_with_state`` — the same, also returning the final (μ, ν);
+* ``decode_step`` — one recurrent token for many heads, state updated in place.
+
+All work runs in the library's CUDA kernels; PyTorch only allocates device
+memory and provides the stream.
+"""
+from ._binding import (EXPORTED, LinAttnError, decode_step, forward, forward_with_state,
+                       last_device_status, launch_count, library_path, load, status_string)
+from .build import build
+
+__all__ = ["forward", "forward_with_state", "decode_step", "last_device_status", "status_string",
+           "LinAttnError", "build", "load", "library_path", "launch_count", "EXPORTED"]

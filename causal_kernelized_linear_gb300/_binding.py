@@ -1,0 +1,218 @@
+"""ctypes binding of liblinattn (C ABI in include/linattn.h).
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+layout, outputs are allocated with PyTorch, and every arithmetic step runs in
+the library's CUDA kernels on the current PyTorch stream.  There is no CPU or
+PyTorch fallback: if the library is missing or fails, a call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+LA_OK = 0
+LA_ERR_INVALID_ARG = 1
+LA_ERR_UNSUPPORTED = 2
+LA_ERR_CUDA = 3
+LA_ERR_TIMEOUT = 4
+LA_ERR_OUT_OF_MEMORY = 5
+
+LA_BF16 = 0
+LA_F32 = 1
+LA_FM_ELU1 = 0
+LA_FM_PERFORMER = 1
+
+_FM = {"elu1": LA_FM_ELU1, "performer": LA_FM_PERFORMER}
+_DT = {torch.bfloat16: LA_BF16, torch.float32: LA_F32}
+
+EXPORTED = ("la_forward", "la_forward_with_state", "la_decode_step", "la_status_string",
+            "la_get_last_device_status", "la_launch_count")
+
+
+class LinAttnError(RuntimeError):
+    """A liblinattn call returned a non-OK status."""
+
+    def __init__(self, fn: str, status: int, name: str):
+        super().__init__(f"{fn} failed: {name} ({status})")
+        self.status = status
+        self.status_name = name
+
+
+class LaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int), ("B", ctypes.c_int64),
+                ("H", ctypes.c_int64), ("n", ctypes.c_int64), ("d", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load liblinattn.so (built in-tree by ``causal_kernelized_linear_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"liblinattn.so is not built ({path}); run "
+                               "`python -m causal_kernelized_linear_gb300.build`")
+        lib = ctypes.CDLL(path)
+        P = ctypes.POINTER(LaTensor)
+        vp = ctypes.c_void_p
+        lib.la_forward.argtypes = [P, P, P, vp, ctypes.c_int, P, ctypes.c_int, P, vp]
+        lib.la_forward.restype = ctypes.c_int
+        lib.la_forward_with_state.argtypes = [P, P, P, vp, ctypes.c_int, P, ctypes.c_int, P,
+                                              vp, vp, vp]
+        lib.la_forward_with_state.restype = ctypes.c_int
+        lib.la_decode_step.argtypes = [vp, vp, P, P, P, vp, P, vp]
+        lib.la_decode_step.restype = ctypes.c_int
+        lib.la_status_string.argtypes = [ctypes.c_int]
+        lib.la_status_string.restype = ctypes.c_char_p
+        lib.la_get_last_device_status.argtypes = [vp]
+        lib.la_get_last_device_status.restype = ctypes.c_int
+        lib.la_launch_count.argtypes = []
+        lib.la_launch_count.restype = ctypes.c_uint64
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().la_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != LA_OK:
+        raise LinAttnError(fn, status, status_string(status))
+
+
+def _desc(t: torch.Tensor, shape4) -> LaTensor:
+    return LaTensor(t.data_ptr(), _DT[t.dtype], *[int(s) for s in shape4])
+
+
+def _need_cuda(name: str, t: torch.Tensor, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    if t.dtype not in _DT:
+        raise ValueError(f"{name}: unsupported dtype {t.dtype}")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _forward_args(q, k, v, decay_a, feature_map, omega, out):
+    for nm, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(nm, t)
+    if q.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, n, d]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda("out", out)
+    fm = _FM[feature_map] if isinstance(feature_map, str) else int(feature_map)
+    dptr = None
+    if decay_a is not None:
+        _need_cuda("decay_a", decay_a, torch.float32)
+        dptr = decay_a.data_ptr()
+    om = None
+    if omega is not None:
+        _need_cuda("omega", omega)
+        if omega.dim() != 2:
+            raise ValueError("omega must be [d, m]")
+        om = _desc(omega, (1, 1, omega.shape[0], omega.shape[1]))
+    qd, kd, vd = (_desc(t, t.shape) for t in (q, k, v))
+    od = _desc(out, out.shape)
+    return out, fm, dptr, om, qd, kd, vd, od
+
+
+def forward(q, k, v, decay_a=None, feature_map="elu1", omega=None, causal=True, out=None,
+            stream=None):
+    """la_forward: q, k, v [B,H,n,d] (bf16 or fp32, CUDA, contiguous); decay_a [H]
+    fp32 or None; omega [d, m] for feature_map="performer".  Returns out."""
+    out, fm, dptr, om, qd, kd, vd, od = _forward_args(q, k, v, decay_a, feature_map, omega, out)
+    st = load().la_forward(ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), dptr, fm,
+                           ctypes.byref(om) if om is not None else None, int(bool(causal)),
+                           ctypes.byref(od), _stream_handle(stream))
+    _check("la_forward", st)
+    return out
+
+
+def forward_with_state(q, k, v, decay_a=None, feature_map="elu1", omega=None, causal=True,
+                       out=None, mu_out=None, nu_out=None, stream=None):
+    """la_forward_with_state: returns (out, μ [B,H,d',d] fp32, ν [B,H,d'] fp32)."""
+    out, fm, dptr, om, qd, kd, vd, od = _forward_args(q, k, v, decay_a, feature_map, omega, out)
+    B, H, _, d = q.shape
+    dp = d if fm == LA_FM_ELU1 else omega.shape[1]
+    if mu_out is None:
+        mu_out = torch.empty(B, H, dp, d, device=q.device, dtype=torch.float32)
+    if nu_out is None:
+        nu_out = torch.empty(B, H, dp, device=q.device, dtype=torch.float32)
+    _need_cuda("mu_out", mu_out, torch.float32)
+    _need_cuda("nu_out", nu_out, torch.float32)
+    if tuple(mu_out.shape) != (B, H, dp, d) or tuple(nu_out.shape) != (B, H, dp):
+        raise ValueError("mu_out must be [B,H,d',d] and nu_out [B,H,d']")
+    st = load().la_forward_with_state(ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), dptr,
+                                      fm, ctypes.byref(om) if om is not None else None,
+                                      int(bool(causal)), ctypes.byref(od), mu_out.data_ptr(),
+                                      nu_out.data_ptr(), _stream_handle(stream))
+    _check("la_forward_with_state", st)
+    return out, mu_out, nu_out
+
+
+def decode_step(mu, nu, q, k, v, decay_a=None, out=None, stream=None):
+    """la_decode_step: μ [B,H,d,d], ν [B,H,d] fp32 updated in place; q, k, v
+    [B,H,d] or [B,H,1,d].  Returns out (same shape as q)."""
+    _need_cuda("mu", mu, torch.float32)
+    _need_cuda("nu", nu, torch.float32)
+    for nm, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(nm, t)
+    if q.dim() == 3:
+        shape4 = (q.shape[0], q.shape[1], 1, q.shape[2])
+    elif q.dim() == 4:
+        shape4 = tuple(q.shape)
+    else:
+        raise ValueError("q must be [B,H,d] or [B,H,1,d]")
+    B, H, _, d = shape4
+    if tuple(mu.shape) != (B, H, d, d) or tuple(nu.shape) != (B, H, d):
+        raise ValueError("mu must be [B,H,d,d] and nu [B,H,d]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda("out", out)
+    dptr = None
+    if decay_a is not None:
+        _need_cuda("decay_a", decay_a, torch.float32)
+        dptr = decay_a.data_ptr()
+    qd, kd, vd = (_desc(t, shape4) for t in (q, k, v))
+    od = _desc(out, shape4)
+    st = load().la_decode_step(mu.data_ptr(), nu.data_ptr(), ctypes.byref(qd), ctypes.byref(kd),
+                               ctypes.byref(vd), dptr, ctypes.byref(od), _stream_handle(stream))
+    _check("la_decode_step", st)
+    return out
+
+
+def last_device_status(stream=None) -> int:
+    """la_get_last_device_status: synchronises the stream and returns (and
+    clears) the device status word."""
+    return int(load().la_get_last_device_status(_stream_handle(stream)))
+
+
+def launch_count() -> int:
+    """la_launch_count: kernels queued by the library in this process so far."""
+    return int(load().la_launch_count())

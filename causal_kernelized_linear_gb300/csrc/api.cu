@@ -1,0 +1,282 @@
+// C ABI of liblinattn (declared in include/linattn.h): argument validation,
+// path selection, segment planning and workspace, device status word.
+#include "linattn.h"
+
+#include "internal.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+namespace la {
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void count_launches(int k) { g_launches.fetch_add((uint64_t)k, std::memory_order_relaxed); }
+
+namespace {
+
+// Per-device status word written by kernels whose bounded waits expire.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  int* status = nullptr;  // device address of g_device_status
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+la_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return LA_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return LA_ERR_CUDA;
+    di.num_sms = sms;
+    di.status = static_cast<int*>(p);
+    di.ready = true;
+  }
+  *out = di;
+  return LA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dtype(la_dtype t) { return t == LA_BF16 || t == LA_F32; }
+
+bool same_shape(const la_tensor* a, const la_tensor* b) {
+  return a->B == b->B && a->H == b->H && a->n == b->n && a->d == b->d;
+}
+
+bool supported_width(int64_t d) { return d == 32 || d == 64 || d == 128; }
+
+bool supported_features(int64_t m) { return m == 64 || m == 128 || m == 256; }
+
+// Checks shared by la_forward and la_forward_with_state; fills `a`.
+la_status validate_forward(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                           const float* decay_a, la_feature_map fm, const la_tensor* omega,
+                           int causal, la_tensor* out, FwdArgs* a) {
+  if (!q || !k || !v || !out) return LA_ERR_INVALID_ARG;
+  if (!valid_dtype(q->dtype) || k->dtype != q->dtype || v->dtype != q->dtype ||
+      out->dtype != q->dtype)
+    return LA_ERR_INVALID_ARG;
+  if (!same_shape(q, k) || !same_shape(q, v) || !same_shape(q, out)) return LA_ERR_INVALID_ARG;
+  if (q->B < 1 || q->H < 1 || q->n < 0 || q->d < 1) return LA_ERR_INVALID_ARG;
+  if (q->B > (int64_t)1 << 24 || q->H > (int64_t)1 << 16 || q->n > (int64_t)1 << 31)
+    return LA_ERR_UNSUPPORTED;
+  if (!supported_width(q->d)) return LA_ERR_UNSUPPORTED;
+  if (fm != LA_FM_ELU1 && fm != LA_FM_PERFORMER) return LA_ERR_INVALID_ARG;
+  if (!causal && decay_a) return LA_ERR_UNSUPPORTED;  // eq (6) carries no decay
+  const int64_t elems = q->B * q->H * q->n * q->d;
+  if (elems > 0) {
+    if (!q->data || !k->data || !v->data || !out->data) return LA_ERR_INVALID_ARG;
+    if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(v->data) ||
+        !aligned16(out->data))
+      return LA_ERR_INVALID_ARG;
+  }
+  if (decay_a && (reinterpret_cast<uintptr_t>(decay_a) & 3u)) return LA_ERR_INVALID_ARG;
+  int m = 0;
+  if (fm == LA_FM_PERFORMER) {
+    if (!omega || !omega->data) return LA_ERR_INVALID_ARG;
+    if (omega->dtype != q->dtype || omega->B != 1 || omega->H != 1 || omega->n != q->d)
+      return LA_ERR_INVALID_ARG;
+    if (!aligned16(omega->data)) return LA_ERR_INVALID_ARG;
+    if (!supported_features(omega->d)) return LA_ERR_UNSUPPORTED;
+    m = (int)omega->d;
+  } else if (omega) {
+    return LA_ERR_INVALID_ARG;
+  }
+  a->q = q->data;
+  a->k = k->data;
+  a->v = v->data;
+  a->out = out->data;
+  a->decay = decay_a;
+  a->omega = omega ? omega->data : nullptr;
+  a->B = q->B;
+  a->H = q->H;
+  a->n = q->n;
+  a->d = (int)q->d;
+  a->m = m;
+  a->dp = fm == LA_FM_PERFORMER ? m : (int)q->d;
+  a->bf16 = q->dtype == LA_BF16;
+  a->performer = fm == LA_FM_PERFORMER;
+  a->causal = causal != 0;
+  a->mu_out = nullptr;
+  a->nu_out = nullptr;
+  return LA_OK;
+}
+
+// Cut every head into segments so that the grid covers the GPU a few times over.
+SegmentPlan plan_segments(int64_t BH, int64_t n, int num_sms, int64_t granule,
+                          int ctas_per_sm) {
+  SegmentPlan p;
+  const int64_t target = (int64_t)num_sms * ctas_per_sm;
+  int64_t g = (target + BH - 1) / BH;
+  const int64_t max_g = std::max<int64_t>(1, (n + granule - 1) / granule);
+  g = std::max<int64_t>(1, std::min(g, max_g));
+  int64_t len = (n + g - 1) / g;
+  len = ((len + granule - 1) / granule) * granule;
+  p.seg_len = std::max<int64_t>(len, granule);
+  p.nseg = (int)std::max<int64_t>(1, (n + p.seg_len - 1) / p.seg_len);
+  return p;
+}
+
+la_status to_status(cudaError_t e) {
+  if (e == cudaSuccess) return LA_OK;
+  if (e == cudaErrorMemoryAllocation) return LA_ERR_OUT_OF_MEMORY;
+  return LA_ERR_CUDA;
+}
+
+la_status run_forward(FwdArgs& a, cudaStream_t stream) {
+  DeviceInfo di;
+  la_status st = device_info(&di);
+  if (st != LA_OK) return st;
+  a.status = di.status;
+  a.num_sms = di.num_sms;
+  const int64_t BH = a.B * a.H;
+  const size_t state_elems = (size_t)a.dp * a.d;
+  if (a.n == 0) {
+    // empty sequence: nothing to write but the (zero) state
+    if (a.mu_out && cudaMemsetAsync(a.mu_out, 0, BH * state_elems * sizeof(float), stream) != cudaSuccess)
+      return LA_ERR_CUDA;
+    if (a.nu_out && cudaMemsetAsync(a.nu_out, 0, BH * a.dp * sizeof(float), stream) != cudaSuccess)
+      return LA_ERR_CUDA;
+    return LA_OK;
+  }
+  const SegmentPlan plan = plan_segments(BH, a.n, a.num_sms, 32, 2);
+  const bool need_ws = !a.causal || plan.nseg > 1;
+  const bool need_tot = need_ws && (a.mu_out == nullptr);
+  size_t ws_floats = 0;
+  if (need_ws) ws_floats += (size_t)BH * plan.nseg * (state_elems + a.dp);
+  if (need_tot) ws_floats += (size_t)BH * (state_elems + a.dp);
+  float* ws = nullptr;
+  if (ws_floats) {
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_floats * sizeof(float), stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return e == cudaErrorMemoryAllocation ? LA_ERR_OUT_OF_MEMORY : LA_ERR_CUDA;
+    }
+  }
+  float* ws_state = ws;
+  float* ws_z = ws ? ws + (size_t)BH * plan.nseg * state_elems : nullptr;
+  float* tot_state = a.mu_out;
+  float* tot_z = a.nu_out;
+  if (need_tot) {
+    tot_state = ws + (size_t)BH * plan.nseg * (state_elems + a.dp);
+    tot_z = tot_state + (size_t)BH * state_elems;
+  }
+  cudaError_t e = simt_forward(a, stream, ws_state, ws_z, tot_state, tot_z, plan);
+  if (ws) {
+    cudaError_t f = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = f;
+  }
+  return to_status(e);
+}
+
+}  // namespace
+}  // namespace la
+
+extern "C" {
+
+la_status la_forward(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                     const float* decay_a, la_feature_map feature_map,
+                     const la_tensor* omega, int causal, la_tensor* out, la_stream stream) {
+  la::FwdArgs a;
+  la_status st = la::validate_forward(q, k, v, decay_a, feature_map, omega, causal, out, &a);
+  if (st != LA_OK) return st;
+  return la::run_forward(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+la_status la_forward_with_state(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                                const float* decay_a, la_feature_map feature_map,
+                                const la_tensor* omega, int causal, la_tensor* out,
+                                float* mu_out, float* nu_out, la_stream stream) {
+  la::FwdArgs a;
+  la_status st = la::validate_forward(q, k, v, decay_a, feature_map, omega, causal, out, &a);
+  if (st != LA_OK) return st;
+  if (!mu_out || !nu_out || !la::aligned16(mu_out) || !la::aligned16(nu_out))
+    return LA_ERR_INVALID_ARG;
+  a.mu_out = mu_out;
+  a.nu_out = nu_out;
+  return la::run_forward(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+la_status la_decode_step(float* mu, float* nu, const la_tensor* q, const la_tensor* k,
+                         const la_tensor* v, const float* decay_a, la_tensor* out,
+                         la_stream stream) {
+  if (!mu || !nu || !q || !k || !v || !out) return LA_ERR_INVALID_ARG;
+  if (!la::valid_dtype(q->dtype) || k->dtype != q->dtype || v->dtype != q->dtype ||
+      out->dtype != q->dtype)
+    return LA_ERR_INVALID_ARG;
+  if (!la::same_shape(q, k) || !la::same_shape(q, v) || !la::same_shape(q, out))
+    return LA_ERR_INVALID_ARG;
+  if (q->B < 1 || q->H < 1 || q->n != 1) return LA_ERR_INVALID_ARG;
+  if (q->B * q->H > ((int64_t)1 << 31) - 1) return LA_ERR_UNSUPPORTED;
+  if (!la::supported_width(q->d)) return LA_ERR_UNSUPPORTED;
+  if (!q->data || !k->data || !v->data || !out->data) return LA_ERR_INVALID_ARG;
+  if (!la::aligned16(mu) || !la::aligned16(nu) || !la::aligned16(q->data) ||
+      !la::aligned16(k->data) || !la::aligned16(v->data) || !la::aligned16(out->data))
+    return LA_ERR_INVALID_ARG;
+  if (decay_a && (reinterpret_cast<uintptr_t>(decay_a) & 3u)) return LA_ERR_INVALID_ARG;
+  la::DecodeArgs a;
+  a.mu = mu;
+  a.nu = nu;
+  a.q = q->data;
+  a.k = k->data;
+  a.v = v->data;
+  a.out = out->data;
+  a.decay = decay_a;
+  a.B = q->B;
+  a.H = q->H;
+  a.d = (int)q->d;
+  a.bf16 = q->dtype == LA_BF16;
+  return la::to_status(la::decode_step(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* la_status_string(la_status status) {
+  switch (status) {
+    case LA_OK: return "LA_OK";
+    case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG";
+    case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED";
+    case LA_ERR_CUDA: return "LA_ERR_CUDA";
+    case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT";
+    case LA_ERR_OUT_OF_MEMORY: return "LA_ERR_OUT_OF_MEMORY";
+  }
+  return "LA_ERR_UNKNOWN";
+}
+
+uint64_t la_launch_count(void) { return la::g_launches.load(std::memory_order_relaxed); }
+
+la_status la_get_last_device_status(la_stream stream) {
+  la::DeviceInfo di;
+  la_status st = la::device_info(&di);
+  if (st != LA_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return LA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, di.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return LA_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(di.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return LA_ERR_CUDA;
+    return static_cast<la_status>(word);
+  }
+  return LA_OK;
+}
+
+}  // extern "C"

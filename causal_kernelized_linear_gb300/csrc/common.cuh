@@ -1,0 +1,32 @@
+// Device helpers shared by the kernels of liblinattn.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace la {
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// φ(x) = elu(x) + 1 with α = 1 ("Linear Attention Research 2026", Linear
+// Transformer): x + 1 for x > 0, e^x otherwise.
+__device__ __forceinline__ float elu1(float x) { return x > 0.f ? x + 1.f : expf(x); }
+
+// Weight of the newest token in eq (10)–(11): 1 − a, except a = 1 which is
+// the plain running sum of eq (7)–(8).
+__device__ __forceinline__ float new_token_weight(float a) { return a == 1.f ? 1.f : 1.f - a; }
+
+// a^k for integer k ≥ 0 with 0^0 = 1.
+__device__ __forceinline__ float decay_pow(float a, int64_t k) {
+  return k == 0 ? 1.f : powf(a, (float)k);
+}
+
+}  // namespace la

@@ -1,0 +1,136 @@
+// Recurrent decode step ("Efficient Transformers II" §2.2, eq (10)–(11) and
+// the causal readout of eq (9)) for B·H independent heads, elu+1 map (d' = d):
+//   k' = φ(k), q' = φ(q);  μ ← a·μ + w·k'ᵀv;  ν ← a·ν + w·k';  o = q'μ / q'ν.
+//
+// The step is bound by HBM: every head streams its d×d fp32 μ in and out once
+// (128 KiB of traffic at d = 128) against ~5·d² flops.  One CTA per head; each
+// thread owns a float4 column group and a strided set of rows, so that a warp
+// touches one contiguous 512-byte row segment per access (128-bit, coalesced).
+// All μ loads of a thread are issued before any arithmetic to keep enough
+// bytes in flight; loads and stores use the streaming (evict-first) hints
+// because μ is touched once per step.  q'·μ is reduced over rows through
+// shared memory and q'·ν with warp shuffles.
+#include "common.cuh"
+#include "internal.h"
+
+namespace la {
+namespace {
+
+constexpr int kDecThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float load_elem(const T* p, int64_t i) { return to_f32(p[i]); }
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kDecThreads)
+decode_step_kernel(float* __restrict__ mu, float* __restrict__ nu, const T* __restrict__ q,
+                   const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ out,
+                   const float* __restrict__ decay, int64_t H) {
+  constexpr int CG = D / 4;                 // float4 column groups per row
+  constexpr int RG = kDecThreads / CG;      // row groups
+  constexpr int RPT = D / RG;               // rows per thread
+  static_assert(RPT >= 1 && D % RG == 0, "decode layout");
+  __shared__ float qf[D], kf[D], vv[D];
+  __shared__ float4 part[RG][CG];
+  __shared__ float red[kDecThreads / 32];
+
+  const int64_t bh = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int cg = tid % CG;
+  const int rg = tid / CG;
+  float4* mrow = reinterpret_cast<float4*>(mu + bh * (int64_t)(D * D));
+
+  // issue every μ load of this thread first (rows rg, rg+RG, ...)
+  float4 m[RPT];
+#pragma unroll
+  for (int r = 0; r < RPT; ++r) m[r] = __ldcs(mrow + (int64_t)(rg + r * RG) * CG + cg);
+
+  const float a = decay ? decay[bh % H] : 1.f;
+  const float w = new_token_weight(a);
+  for (int i = tid; i < D; i += kDecThreads) {
+    qf[i] = elu1(load_elem(q, bh * D + i));
+    kf[i] = elu1(load_elem(k, bh * D + i));
+    vv[i] = load_elem(v, bh * D + i);
+  }
+  __syncthreads();
+
+  const float4 vc = make_float4(vv[4 * cg], vv[4 * cg + 1], vv[4 * cg + 2], vv[4 * cg + 3]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int r = 0; r < RPT; ++r) {
+    const int i = rg + r * RG;
+    const float wk = w * kf[i];
+    float4 x = m[r];
+    x.x = a * x.x + wk * vc.x;
+    x.y = a * x.y + wk * vc.y;
+    x.z = a * x.z + wk * vc.z;
+    x.w = a * x.w + wk * vc.w;
+    __stcs(mrow + (int64_t)i * CG + cg, x);
+    const float qi = qf[i];
+    acc.x += qi * x.x;
+    acc.y += qi * x.y;
+    acc.z += qi * x.z;
+    acc.w += qi * x.w;
+  }
+  part[rg][cg] = acc;
+
+  // ν update and q'·ν (first D threads, then a block reduction)
+  float dpart = 0.f;
+  if (tid < D) {
+    float* nb = nu + bh * D;
+    const float x = a * nb[tid] + w * kf[tid];
+    nb[tid] = x;
+    dpart = qf[tid] * x;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) dpart += __shfl_xor_sync(0xffffffffu, dpart, off);
+  if ((tid & 31) == 0) red[tid >> 5] = dpart;
+  __syncthreads();
+
+  if (tid < D) {
+    float den = 0.f;
+#pragma unroll
+    for (int wv = 0; wv < kDecThreads / 32; ++wv) den += red[wv];
+    const int c = tid;
+    float num = 0.f;
+#pragma unroll 8
+    for (int g = 0; g < RG; ++g) {
+      const float4 pv = part[g][c / 4];
+      num += (c % 4 == 0) ? pv.x : (c % 4 == 1) ? pv.y : (c % 4 == 2) ? pv.z : pv.w;
+    }
+    out[bh * D + c] = from_f32<T>(num / den);
+  }
+}
+
+template <typename T>
+cudaError_t run_decode(const DecodeArgs& a, cudaStream_t s) {
+  const unsigned grid = (unsigned)(a.B * a.H);
+  const T* q = static_cast<const T*>(a.q);
+  const T* k = static_cast<const T*>(a.k);
+  const T* v = static_cast<const T*>(a.v);
+  T* o = static_cast<T*>(a.out);
+  switch (a.d) {
+    case 32:
+      decode_step_kernel<T, 32><<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, a.decay, a.H);
+      break;
+    case 64:
+      decode_step_kernel<T, 64><<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, a.decay, a.H);
+      break;
+    case 128:
+      decode_step_kernel<T, 128><<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, a.decay, a.H);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t decode_step(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.bf16) return run_decode<__nv_bfloat16>(a, stream);
+  return run_decode<float>(a, stream);
+}
+
+}  // namespace la

@@ -1,0 +1,420 @@
+// fp32 CUDA-core chunked forward of causal / non-causal kernelized linear
+// attention, and the decayed segment scan.
+//
+// Method ("Efficient Transformers II" §2.2, eq (6)–(11)): per head, with the
+// state (μ, ν) at the start of a chunk of cs tokens (local positions t, s):
+//   o_t = [ Σ_{s≤t} w·a^{t−s}(q'_t·k'_s) v_s + a^{t+1} q'_t μ ]
+//       / [ Σ_{s≤t} w·a^{t−s}(q'_t·k'_s)     + a^{t+1} q'_t ν ]
+//   μ ← a^{cs} μ + Σ_s w·a^{cs−1−s} k'_sᵀ v_s,   ν ← a^{cs} ν + Σ_s w·a^{cs−1−s} k'_sᵀ
+// which is eq (10)–(11) unrolled over the chunk (eq (7)–(8) when a = 1, w = 1),
+// with the causal readout of eq (9) that includes token t.  The intra-chunk part
+// is the quadratic form of "Efficient Transformers I" eq (25)–(26) restricted to
+// the chunk.  Everything is computed in fp32 on CUDA cores: this is the path
+// for fp32 inputs, where the parity bound (1e-4) rules out bf16 tensor-core
+// operands.
+//
+// Long sequences are cut into segments (one CTA per (segment, head)).  Pass 1
+// computes each segment's own decayed aggregate, segment_scan turns them into
+// exclusive prefixes (the state entering each segment), pass 2 produces the
+// outputs.  Non-causal mode: pass 1 + scan give μ_n, ν_n, then a readout pass.
+#include "common.cuh"
+#include "internal.h"
+
+#include <algorithm>
+
+namespace la {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int D, int DP, bool PERF>
+struct SimtCfg {
+  // tokens per chunk: 32 unless the fp32 state plus chunk buffers would not fit
+  static constexpr int CS = (DP * D >= 256 * 128) ? 16 : 32;
+  static constexpr int FS = DP + 1;  // padded row stride of feature tiles
+  // shared-memory layout (floats)
+  static constexpr int oS = 0;                      // μ  [DP][D]
+  static constexpr int oZ = oS + DP * D;            // ν  [DP]
+  static constexpr int oQF = oZ + DP;               // q' [CS][FS]
+  static constexpr int oKF = oQF + CS * FS;         // k' [CS][FS]
+  static constexpr int oV = oKF + CS * FS;          // v  [CS][D]
+  static constexpr int oX = oV + CS * D;            // raw rows for Performer [CS][D]
+  static constexpr int oP = oX + (PERF ? CS * D : 0);  // masked weights [CS][CS]
+  static constexpr int oPW = oP + CS * CS;          // a^k, k = 0..CS
+  static constexpr int oSQ = oPW + CS + 1;          // ½‖x‖² per row (Performer)
+  static constexpr int oDEN = oSQ + CS;             // denominators [CS]
+  static constexpr int total = oDEN + CS;
+  static constexpr size_t bytes = size_t(total) * sizeof(float);
+};
+
+// Loads rows [row0, row0+cs) of one head (zero beyond cs) and applies φ.
+// f receives φ(x) with row stride FS.  For the Performer map ω is [D, DP]
+// row-major in global memory and φ(x)_i = exp(x·ω_i − ½‖x‖²)/√m.
+template <typename T, int D, int DP, bool PERF, int CS, int FS>
+__device__ void load_features(const T* __restrict__ x, int cs, float* f, float* xraw,
+                              float* halfsq, const T* __restrict__ omega) {
+  if constexpr (!PERF) {
+    for (int e = threadIdx.x; e < CS * D; e += kThreads) {
+      const int t = e / D, c = e % D;
+      f[t * FS + c] = (t < cs) ? elu1(to_f32(x[(int64_t)t * D + c])) : 0.f;
+    }
+  } else {
+    for (int e = threadIdx.x; e < CS * D; e += kThreads) {
+      const int t = e / D;
+      xraw[e] = (t < cs) ? to_f32(x[(int64_t)t * D + (e % D)]) : 0.f;
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < CS; t += kThreads) {
+      float s = 0.f;
+      for (int c = 0; c < D; ++c) s += xraw[t * D + c] * xraw[t * D + c];
+      halfsq[t] = 0.5f * s;
+    }
+    __syncthreads();
+    const float inv_sqrt_m = rsqrtf((float)DP);
+    for (int e = threadIdx.x; e < CS * DP; e += kThreads) {
+      const int t = e / DP, i = e % DP;
+      float u = 0.f;
+      for (int c = 0; c < D; ++c) u += xraw[t * D + c] * to_f32(omega[c * DP + i]);
+      f[t * FS + i] = (t < cs) ? expf(u - halfsq[t]) * inv_sqrt_m : 0.f;
+    }
+  }
+}
+
+template <typename T, int D, int CS>
+__device__ void load_values(const T* __restrict__ v, int cs, float* vv) {
+  for (int e = threadIdx.x; e < CS * D; e += kThreads) {
+    const int t = e / D;
+    vv[e] = (t < cs) ? to_f32(v[(int64_t)t * D + (e % D)]) : 0.f;
+  }
+}
+
+// μ ← a^{cs} μ + Σ_s w·a^{cs−1−s} k'_sᵀ v_s ; ν likewise (eq (10)–(11) over a chunk).
+template <int D, int DP, int CS, int FS>
+__device__ void update_state(float* S, float* z, const float* kf, const float* vv,
+                             const float* pw, float w, int cs) {
+  const float acs = pw[cs];
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) {
+    const int i = e / D, c = e % D;
+    float acc = 0.f;
+    for (int s = 0; s < cs; ++s) acc += (w * pw[cs - 1 - s]) * kf[s * FS + i] * vv[s * D + c];
+    S[e] = acs * S[e] + acc;
+  }
+  for (int i = threadIdx.x; i < DP; i += kThreads) {
+    float acc = 0.f;
+    for (int s = 0; s < cs; ++s) acc += (w * pw[cs - 1 - s]) * kf[s * FS + i];
+    z[i] = acs * z[i] + acc;
+  }
+}
+
+struct SimtParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const float* decay;
+  const void* omega;
+  int64_t H, n, seg_len;
+  int nseg;
+  float* ws_state;   // [BH][nseg][DP*D]
+  float* ws_z;       // [BH][nseg][DP]
+  const float* tot_state;  // non-causal: [BH][DP*D]
+  const float* tot_z;
+  float* fin_state;  // causal single-segment: final state out (or nullptr)
+  float* fin_z;
+};
+
+// Pass 1: the decayed aggregate of one segment, starting from zero state.
+template <typename T, int D, int DP, bool PERF>
+__global__ void __launch_bounds__(kThreads)
+simt_segment_state(SimtParams p) {
+  using C = SimtCfg<D, DP, PERF>;
+  constexpr int CS = C::CS, FS = C::FS;
+  extern __shared__ float sm[];
+  float* S = sm + C::oS;
+  float* z = sm + C::oZ;
+  float* kf = sm + C::oKF;
+  float* vv = sm + C::oV;
+  float* xr = sm + C::oX;
+  float* pw = sm + C::oPW;
+  float* hs = sm + C::oSQ;
+  const int g = blockIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int64_t t_begin = (int64_t)g * p.seg_len;
+  const int64_t t_end = min(p.n, t_begin + p.seg_len);
+  const float a = p.decay ? p.decay[bh % p.H] : 1.f;
+  const float w = new_token_weight(a);
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) S[e] = 0.f;
+  for (int i = threadIdx.x; i < DP; i += kThreads) z[i] = 0.f;
+  for (int kk = threadIdx.x; kk <= CS; kk += kThreads) pw[kk] = decay_pow(a, kk);
+  const T* kb = static_cast<const T*>(p.k) + bh * p.n * D;
+  const T* vb = static_cast<const T*>(p.v) + bh * p.n * D;
+  const T* om = static_cast<const T*>(p.omega);
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += CS) {
+    const int cs = (int)min((int64_t)CS, t_end - t0);
+    __syncthreads();
+    load_features<T, D, DP, PERF, CS, FS>(kb + t0 * D, cs, kf, xr, hs, om);
+    load_values<T, D, CS>(vb + t0 * D, cs, vv);
+    __syncthreads();
+    update_state<D, DP, CS, FS>(S, z, kf, vv, pw, w, cs);
+  }
+  __syncthreads();
+  float* dS = p.ws_state + (bh * p.nseg + g) * (int64_t)(DP * D);
+  float* dz = p.ws_z + (bh * p.nseg + g) * (int64_t)DP;
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) dS[e] = S[e];
+  for (int i = threadIdx.x; i < DP; i += kThreads) dz[i] = z[i];
+}
+
+// Pass 2 (causal): outputs of one segment from the state entering it.
+template <typename T, int D, int DP, bool PERF>
+__global__ void __launch_bounds__(kThreads)
+simt_causal_output(SimtParams p) {
+  using C = SimtCfg<D, DP, PERF>;
+  constexpr int CS = C::CS, FS = C::FS;
+  extern __shared__ float sm[];
+  float* S = sm + C::oS;
+  float* z = sm + C::oZ;
+  float* qf = sm + C::oQF;
+  float* kf = sm + C::oKF;
+  float* vv = sm + C::oV;
+  float* xr = sm + C::oX;
+  float* P = sm + C::oP;
+  float* pw = sm + C::oPW;
+  float* hs = sm + C::oSQ;
+  float* den = sm + C::oDEN;
+  const int g = blockIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int64_t t_begin = (int64_t)g * p.seg_len;
+  const int64_t t_end = min(p.n, t_begin + p.seg_len);
+  const float a = p.decay ? p.decay[bh % p.H] : 1.f;
+  const float w = new_token_weight(a);
+  if (p.nseg > 1) {
+    const float* sS = p.ws_state + (bh * p.nseg + g) * (int64_t)(DP * D);
+    const float* sz = p.ws_z + (bh * p.nseg + g) * (int64_t)DP;
+    for (int e = threadIdx.x; e < DP * D; e += kThreads) S[e] = sS[e];
+    for (int i = threadIdx.x; i < DP; i += kThreads) z[i] = sz[i];
+  } else {
+    for (int e = threadIdx.x; e < DP * D; e += kThreads) S[e] = 0.f;
+    for (int i = threadIdx.x; i < DP; i += kThreads) z[i] = 0.f;
+  }
+  for (int kk = threadIdx.x; kk <= CS; kk += kThreads) pw[kk] = decay_pow(a, kk);
+  const T* qb = static_cast<const T*>(p.q) + bh * p.n * D;
+  const T* kb = static_cast<const T*>(p.k) + bh * p.n * D;
+  const T* vb = static_cast<const T*>(p.v) + bh * p.n * D;
+  T* ob = static_cast<T*>(p.out) + bh * p.n * D;
+  const T* om = static_cast<const T*>(p.omega);
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += CS) {
+    const int cs = (int)min((int64_t)CS, t_end - t0);
+    __syncthreads();
+    load_features<T, D, DP, PERF, CS, FS>(kb + t0 * D, cs, kf, xr, hs, om);
+    __syncthreads();
+    load_features<T, D, DP, PERF, CS, FS>(qb + t0 * D, cs, qf, xr, hs, om);
+    load_values<T, D, CS>(vb + t0 * D, cs, vv);
+    __syncthreads();
+    // masked, decayed weights P[t][s] = w·a^{t−s}(q'_t·k'_s), s ≤ t
+    for (int e = threadIdx.x; e < CS * CS; e += kThreads) {
+      const int t = e / CS, s = e % CS;
+      float acc = 0.f;
+      if (s <= t) {
+        for (int i = 0; i < DP; ++i) acc += qf[t * FS + i] * kf[s * FS + i];
+        acc *= w * pw[t - s];
+      }
+      P[e] = acc;
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < CS; t += kThreads) {
+      float intra = 0.f, inter = 0.f;
+      for (int s = 0; s <= t; ++s) intra += P[t * CS + s];
+      for (int i = 0; i < DP; ++i) inter += qf[t * FS + i] * z[i];
+      den[t] = intra + pw[t + 1] * inter;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < CS * D; e += kThreads) {
+      const int t = e / D, c = e % D;
+      if (t < cs) {
+        float intra = 0.f, inter = 0.f;
+        for (int s = 0; s <= t; ++s) intra += P[t * CS + s] * vv[s * D + c];
+        for (int i = 0; i < DP; ++i) inter += qf[t * FS + i] * S[i * D + c];
+        const float num = intra + pw[t + 1] * inter;
+        ob[(t0 + t) * D + c] = from_f32<T>(num / den[t]);
+      }
+    }
+    __syncthreads();
+    update_state<D, DP, CS, FS>(S, z, kf, vv, pw, w, cs);
+  }
+  if (p.fin_state) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < DP * D; e += kThreads) p.fin_state[bh * (DP * D) + e] = S[e];
+    for (int i = threadIdx.x; i < DP; i += kThreads) p.fin_z[bh * DP + i] = z[i];
+  }
+}
+
+// Non-causal readout: o_j = q'_j μ_n / q'_j ν_n (eq (6) / eq (9)).
+template <typename T, int D, int DP, bool PERF>
+__global__ void __launch_bounds__(kThreads)
+simt_noncausal_readout(SimtParams p) {
+  using C = SimtCfg<D, DP, PERF>;
+  constexpr int CS = C::CS, FS = C::FS;
+  extern __shared__ float sm[];
+  float* S = sm + C::oS;
+  float* z = sm + C::oZ;
+  float* qf = sm + C::oQF;
+  float* xr = sm + C::oX;
+  float* hs = sm + C::oSQ;
+  float* den = sm + C::oDEN;
+  const int g = blockIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int64_t t_begin = (int64_t)g * p.seg_len;
+  const int64_t t_end = min(p.n, t_begin + p.seg_len);
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) S[e] = p.tot_state[bh * (DP * D) + e];
+  for (int i = threadIdx.x; i < DP; i += kThreads) z[i] = p.tot_z[bh * DP + i];
+  const T* qb = static_cast<const T*>(p.q) + bh * p.n * D;
+  T* ob = static_cast<T*>(p.out) + bh * p.n * D;
+  const T* om = static_cast<const T*>(p.omega);
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += CS) {
+    const int cs = (int)min((int64_t)CS, t_end - t0);
+    __syncthreads();
+    load_features<T, D, DP, PERF, CS, FS>(qb + t0 * D, cs, qf, xr, hs, om);
+    __syncthreads();
+    for (int t = threadIdx.x; t < CS; t += kThreads) {
+      float acc = 0.f;
+      for (int i = 0; i < DP; ++i) acc += qf[t * FS + i] * z[i];
+      den[t] = acc;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < CS * D; e += kThreads) {
+      const int t = e / D, c = e % D;
+      if (t < cs) {
+        float acc = 0.f;
+        for (int i = 0; i < DP; ++i) acc += qf[t * FS + i] * S[i * D + c];
+        ob[(t0 + t) * D + c] = from_f32<T>(acc / den[t]);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256)
+segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z, int64_t H,
+                    int nseg, int64_t seg_len, int64_t n, int dpd, int dp,
+                    const float* decay) {
+  const int64_t bh = blockIdx.x;
+  const int e = blockIdx.y * 256 + threadIdx.x;
+  if (e >= dpd + dp) return;
+  const float a = decay ? decay[bh % H] : 1.f;
+  float* base;
+  int64_t stride;
+  if (e < dpd) {
+    base = ws_state + bh * nseg * (int64_t)dpd + e;
+    stride = dpd;
+  } else {
+    base = ws_z + bh * nseg * (int64_t)dp + (e - dpd);
+    stride = dp;
+  }
+  float acc = 0.f;  // state entering segment g
+  for (int g = 0; g < nseg; ++g) {
+    const float agg = base[g * stride];
+    base[g * stride] = acc;
+    const int64_t len = min(seg_len, n - (int64_t)g * seg_len);
+    acc = decay_pow(a, len) * acc + agg;
+  }
+  if (tot_state) {
+    if (e < dpd) tot_state[bh * dpd + e] = acc;
+    else tot_z[bh * dp + (e - dpd)] = acc;
+  }
+}
+
+template <typename T, int D, int DP, bool PERF>
+cudaError_t run_simt(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                     float* tot_state, float* tot_z, const SegmentPlan& plan) {
+  using C = SimtCfg<D, DP, PERF>;
+  static_assert(C::bytes <= 227 * 1024, "SIMT chunk buffers exceed shared memory");
+  const size_t smem = C::bytes;
+  cudaError_t err;
+  err = cudaFuncSetAttribute(simt_segment_state<T, D, DP, PERF>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(simt_causal_output<T, D, DP, PERF>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(simt_noncausal_readout<T, D, DP, PERF>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+
+  SimtParams p{};
+  p.q = a.q;
+  p.k = a.k;
+  p.v = a.v;
+  p.out = a.out;
+  p.decay = a.decay;
+  p.omega = a.omega;
+  p.H = a.H;
+  p.n = a.n;
+  p.seg_len = plan.seg_len;
+  p.nseg = plan.nseg;
+  p.ws_state = ws_state;
+  p.ws_z = ws_z;
+  const int64_t BH = a.B * a.H;
+  const dim3 grid((unsigned)plan.nseg, (unsigned)BH);
+  const bool need_scan = !a.causal || plan.nseg > 1;
+  if (need_scan) {
+    simt_segment_state<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
+    count_launches(1);
+    err = segment_scan(ws_state, ws_z, tot_state, tot_z, BH, a.H, plan.nseg, plan.seg_len,
+                       a.n, DP, D, a.decay, stream);
+    if (err != cudaSuccess) return err;
+  }
+  if (a.causal) {
+    if (plan.nseg == 1) {
+      p.fin_state = a.mu_out;
+      p.fin_z = a.nu_out;
+    }
+    simt_causal_output<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
+    count_launches(1);
+  } else {
+    p.tot_state = tot_state;
+    p.tot_z = tot_z;
+    simt_noncausal_readout<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
+    count_launches(1);
+  }
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_simt(const FwdArgs& a, cudaStream_t s, float* ws, float* wz, float* ts,
+                          float* tz, const SegmentPlan& pl) {
+  if (!a.performer) {
+    switch (a.d) {
+      case 32: return run_simt<T, 32, 32, false>(a, s, ws, wz, ts, tz, pl);
+      case 64: return run_simt<T, 64, 64, false>(a, s, ws, wz, ts, tz, pl);
+      case 128: return run_simt<T, 128, 128, false>(a, s, ws, wz, ts, tz, pl);
+    }
+    return cudaErrorInvalidValue;
+  }
+#define LA_PERF_CASE(DD, MM) \
+  if (a.d == DD && a.m == MM) return run_simt<T, DD, MM, true>(a, s, ws, wz, ts, tz, pl);
+  LA_PERF_CASE(32, 64) LA_PERF_CASE(32, 128) LA_PERF_CASE(32, 256)
+  LA_PERF_CASE(64, 64) LA_PERF_CASE(64, 128) LA_PERF_CASE(64, 256)
+  LA_PERF_CASE(128, 64) LA_PERF_CASE(128, 128) LA_PERF_CASE(128, 256)
+#undef LA_PERF_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* tot_z,
+                         int64_t BH, int64_t H, int nseg, int64_t seg_len, int64_t n, int dp,
+                         int d, const float* decay, cudaStream_t stream) {
+  const int dpd = dp * d;
+  const dim3 grid((unsigned)BH, (unsigned)((dpd + dp + 255) / 256));
+  segment_scan_kernel<<<grid, 256, 0, stream>>>(ws_state, ws_z, tot_state, tot_z, H, nseg,
+                                                seg_len, n, dpd, dp, decay);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t simt_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                         float* tot_state, float* tot_z, const SegmentPlan& plan) {
+  if (a.bf16) return dispatch_simt<__nv_bfloat16>(a, stream, ws_state, ws_z, tot_state, tot_z, plan);
+  return dispatch_simt<float>(a, stream, ws_state, ws_z, tot_state, tot_z, plan);
+}
+
+}  // namespace la

@@ -1,0 +1,69 @@
+// Internal host-side interfaces between the translation units of liblinattn.
+// Not part of the public ABI (include/linattn.h is).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace la {
+
+// Everything a forward launcher needs, already validated by the API layer.
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const float* decay;   // device [H] or nullptr (a = 1)
+  const void* omega;    // device [d, m] (Performer) or nullptr
+  int64_t B, H, n;
+  int d;                // value / input width
+  int m;                // Performer feature count (0 for elu+1)
+  int dp;               // feature width d' (d for elu+1, m for Performer)
+  bool bf16;            // element type of q, k, v, out, omega
+  bool performer;
+  bool causal;
+  float* mu_out;        // optional final state [B,H,dp,d]
+  float* nu_out;        // optional final state [B,H,dp]
+  int* status;          // device status word (bounded waits report here)
+  int num_sms;
+};
+
+struct DecodeArgs {
+  float* mu;
+  float* nu;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const float* decay;
+  int64_t B, H;
+  int d;
+  bool bf16;
+};
+
+// Segment plan shared by the forward paths: the sequence of every head is cut
+// into nseg segments of seg_len tokens (the last one ragged); per-segment
+// states are combined by segment_scan.
+struct SegmentPlan {
+  int nseg;
+  int64_t seg_len;
+};
+
+// fp32 CUDA-core chunked forward (fp32 or bf16 inputs).
+cudaError_t simt_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state,
+                         float* ws_z, float* tot_state, float* tot_z,
+                         const SegmentPlan& plan);
+
+// Exclusive decayed prefix over the per-segment aggregates of every head, in
+// place, plus the inclusive total (final state) when tot_state != nullptr.
+cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* tot_z,
+                         int64_t BH, int64_t H, int nseg, int64_t seg_len, int64_t n,
+                         int dp, int d, const float* decay, cudaStream_t stream);
+
+// Records `k` kernel launches in the process-wide launch counter.
+void count_launches(int k);
+
+// Memory-bound recurrent decode step.
+cudaError_t decode_step(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace la

@@ -1,0 +1,163 @@
+/*
+ * linattn.h — C ABI of the GB300 (sm_103a) causal kernelized linear attention
+ * library (liblinattn.so).
+ *
+ * The method (cited by page title and equation):
+ *   "Efficient Transformers II", §2.2 Linear Attention:
+ *     eq (6)   Att = D⁻¹(Q'(K'ᵀV)),  Q' = φ(Q), K' = φ(K) ∈ R^{n×d'}
+ *     eq (7)   μ_j = μ_{j−1} + k'_jᵀ v_j          (μ ∈ R^{d'×d})
+ *     eq (8)   ν_j = ν_{j−1} + k'_jᵀ              (ν ∈ R^{d'})
+ *     eq (9)   o_j = q'_j·μ / q'_j·ν  — μ_n, ν_n non-causal; μ_j, ν_j causal
+ *     eq (10)  μ_j = a·μ_{j−1} + (1−a)·k'_jᵀ v_j
+ *     eq (11)  ν_j = a·ν_{j−1} + (1−a)·k'_jᵀ
+ *   "Linear Attention Research 2026", "Linear Transformer": φ(x) = elu(x)+1
+ *     (α = 1), and "Performer random features": φ(x) = exp(xω − ½‖x‖²)/√m.
+ *   "Efficient Transformers I", kernelized attention eq (25)–(27): the same
+ *     output written as normalized weights (the quadratic form).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are dense, row-major [B, H, n, d] with d innermost and no
+ *     padding (element (b,h,t,c) at ((b·H + h)·n + t)·d + c).
+ *   - All tensor data, decay values and state buffers are DEVICE pointers on
+ *     the current CUDA device, owned by the caller.  The library never frees
+ *     or retains them after a call returns.
+ *   - A decay a = 1 (or decay_a == NULL) selects the plain sums of eq (7)–(8)
+ *     (weight 1 on the new token); any other a ∈ [0, 1] selects eq (10)–(11)
+ *     with weight (1 − a).  Values are read on the device only; values outside
+ *     [0, 1] give unspecified (but finite-time, fault-free) results.
+ *   - The exported state is μ [B, H, d', d] and ν [B, H, d'] in fp32,
+ *     row i of μ being feature i of φ.
+ *   - Work is queued on `stream` and the call returns without synchronising.
+ *     Arguments are validated on the host before anything is queued: a call
+ *     that returns an error queued no kernel and wrote nothing.
+ *   - Temporary device workspace (per-segment states of long sequences) is
+ *     taken with cudaMallocAsync / cudaFreeAsync on `stream`.
+ *   - The library keeps per-device state only for cached device attributes,
+ *     the device status word and cached kernel attributes.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  LA_ERR_CUDA carries a CUDA runtime error from a launch or an
+ * allocation; LA_ERR_TIMEOUT reports a bounded device-side wait that gave up. */
+typedef enum {
+  LA_OK = 0,
+  LA_ERR_INVALID_ARG = 1,   /* null pointer, shape or dtype mismatch, misalignment */
+  LA_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels implement */
+  LA_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+  LA_ERR_TIMEOUT = 4,       /* a device-side bounded wait expired (see la_get_last_device_status) */
+  LA_ERR_OUT_OF_MEMORY = 5  /* workspace allocation failed */
+} la_status;
+
+typedef enum { LA_BF16 = 0, LA_F32 = 1 } la_dtype;
+
+/* φ: elu(x)+1 ("Linear Transformer", d' = d) or Performer positive random
+ * features ("Performer random features", d' = m). */
+typedef enum { LA_FM_ELU1 = 0, LA_FM_PERFORMER = 1 } la_feature_map;
+
+/* A dense [B, H, n, d] tensor (see conventions above).  `data` must be
+ * 16-byte aligned. */
+typedef struct {
+  void* data;
+  la_dtype dtype;
+  int64_t B, H, n, d;
+} la_tensor;
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* la_stream;
+
+/*
+ * la_forward — prefill / training forward of the whole sequence.
+ *
+ * Computes, for every (b, h) head independently:
+ *   causal != 0 : o_j = q'_j·μ_j / q'_j·ν_j with μ, ν from eq (7)–(8) (a = 1)
+ *                 or eq (10)–(11) (per-head a), starting from zero state and
+ *                 including token j itself;
+ *   causal == 0 : eq (6), o_j = q'_j·μ_n / q'_j·ν_n (no decay).
+ *
+ *   q, k, v      [B, H, n, d], same shape and dtype (LA_BF16 or LA_F32);
+ *                d ∈ {32, 64, 128}; n ≥ 0 (n = 0 is a no-op).
+ *   decay_a      device [H] fp32, or NULL for a = 1.  Must be NULL when
+ *                causal == 0 (eq (6) has no decay) → LA_ERR_UNSUPPORTED.
+ *   feature_map  LA_FM_ELU1 (omega must be NULL) or LA_FM_PERFORMER.
+ *   omega        Performer only: tensor with B = H = 1, n = d, d = m,
+ *                i.e. ω stored [d, m] row-major, same dtype as q;
+ *                m ∈ {64, 128, 256}.  Column i of ω is the i-th random
+ *                direction.  Scaling of ω (e.g. N(0, 1/d)) is the caller's.
+ *   causal       non-zero for the causal (autoregressive) form.
+ *   out          [B, H, n, d], same dtype as q.  Written in full.
+ *   stream       CUDA stream for all work.
+ *
+ * bf16 inputs run on the tcgen05 tensor-core path with fp32 state; fp32
+ * inputs run on an fp32 CUDA-core path.
+ * Errors: LA_ERR_INVALID_ARG (null/shape/dtype/alignment), LA_ERR_UNSUPPORTED
+ * (d, m, or decay with causal == 0), LA_ERR_OUT_OF_MEMORY, LA_ERR_CUDA.
+ */
+la_status la_forward(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                     const float* decay_a, la_feature_map feature_map,
+                     const la_tensor* omega, int causal, la_tensor* out,
+                     la_stream stream);
+
+/*
+ * la_forward_with_state — la_forward that also exports the final state
+ * (μ_n, ν_n) of eq (7)–(11) for every head, e.g. to continue with
+ * la_decode_step ("Efficient Transformers II" §2.2: μ and ν are the fixed-size
+ * memory of the sequence).
+ *   mu_out  device fp32 [B, H, d', d], 16-byte aligned, written in full.
+ *   nu_out  device fp32 [B, H, d'], 16-byte aligned, written in full.
+ * Other arguments and errors as la_forward.
+ */
+la_status la_forward_with_state(const la_tensor* q, const la_tensor* k,
+                                const la_tensor* v, const float* decay_a,
+                                la_feature_map feature_map, const la_tensor* omega,
+                                int causal, la_tensor* out, float* mu_out,
+                                float* nu_out, la_stream stream);
+
+/*
+ * la_decode_step — one recurrent step for B·H heads ("Efficient Transformers
+ * II" eq (10)–(11) followed by the causal readout of eq (9)), elu+1 map:
+ *   k' = φ(k), μ ← a·μ + w·k'ᵀv, ν ← a·ν + w·k', o = q'μ / q'ν,
+ * with w = 1 − a (w = 1 when a = 1 or decay_a == NULL).
+ *   mu      device fp32 [B, H, d, d], updated in place (d' = d).
+ *   nu      device fp32 [B, H, d], updated in place.
+ *   q, k, v [B, H, 1, d] LA_BF16 or LA_F32 (all the same dtype), d ∈ {32, 64, 128}.
+ *   decay_a device [H] fp32 or NULL.
+ *   out     [B, H, 1, d], same dtype as q.
+ * Errors: LA_ERR_INVALID_ARG (null/shape/dtype/alignment, mu/nu not 16-byte
+ * aligned), LA_ERR_UNSUPPORTED (d), LA_ERR_CUDA.
+ */
+la_status la_decode_step(float* mu, float* nu, const la_tensor* q,
+                         const la_tensor* k, const la_tensor* v,
+                         const float* decay_a, la_tensor* out, la_stream stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* la_status_string(la_status status);
+
+/*
+ * la_get_last_device_status — synchronises `stream`, then reports and clears
+ * the current device's status word, which kernels set when a bounded wait on
+ * another CTA or on the tensor-core/TMA pipeline expires (LA_ERR_TIMEOUT).
+ * Returns LA_ERR_CUDA if the synchronisation itself fails.
+ */
+la_status la_get_last_device_status(la_stream stream);
+
+/*
+ * la_launch_count — instrumentation: the number of CUDA kernels this process
+ * has queued through the library so far (all devices, all entry points).
+ * The difference across a region counts the library's own launches in it.
+ * Host-only; never fails.  No counterpart on the pages: it exists so that
+ * benchmarks can report how many of this library's kernels they timed.
+ */
+uint64_t la_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H */

@@ -1,0 +1,125 @@
+"""C-ABI library checks that need no GPU: it builds for sm_103a, loads, exports
+every function that include/*.h declares, and rejects invalid arguments on
+the host before touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import causal_kernelized_linear_gb300 as cl
+from causal_kernelized_linear_gb300 import _binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cl.build()
+    return cl.load()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?\w+\s*\*?\s*(la_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    assert set(B.EXPORTED) <= names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert cl.status_string(0) == "LA_OK"
+    assert cl.status_string(2) == "LA_ERR_UNSUPPORTED"
+    assert cl.status_string(4) == "LA_ERR_TIMEOUT"
+    assert cl.status_string(99) == "LA_ERR_UNKNOWN"
+
+
+def _t(ptr=0x10000, dtype=B.LA_BF16, shape=(1, 2, 8, 64)):
+    return B.LaTensor(ptr, dtype, *shape)
+
+
+def _fwd(lib, q, k, v, decay=None, fm=B.LA_FM_ELU1, omega=None, causal=1, out=None):
+    out = out or _t()
+    return lib.la_forward(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), decay, fm,
+                          ctypes.byref(omega) if omega else None, causal, ctypes.byref(out), None)
+
+
+def test_host_validation_rejects_before_any_launch(lib):
+    ok = _t()
+    # null tensor descriptor
+    assert lib.la_forward(None, ctypes.byref(ok), ctypes.byref(ok), None, 0, None, 1,
+                          ctypes.byref(ok), None) == B.LA_ERR_INVALID_ARG
+    # shape mismatch
+    assert _fwd(lib, ok, _t(shape=(1, 2, 9, 64)), ok) == B.LA_ERR_INVALID_ARG
+    # dtype mismatch
+    assert _fwd(lib, ok, _t(dtype=B.LA_F32), ok) == B.LA_ERR_INVALID_ARG
+    # unsupported head width
+    w = _t(shape=(1, 2, 8, 48))
+    assert _fwd(lib, w, w, w, out=w) == B.LA_ERR_UNSUPPORTED
+    # misaligned data pointer
+    bad = _t(ptr=0x10008)
+    assert _fwd(lib, bad, ok, ok) == B.LA_ERR_INVALID_ARG
+    # null data with elements
+    assert _fwd(lib, _t(ptr=0), ok, ok) == B.LA_ERR_INVALID_ARG
+    # eq (6) has no decay: non-causal with decay_a
+    assert _fwd(lib, ok, ok, ok, decay=0x20000, causal=0) == B.LA_ERR_UNSUPPORTED
+    # elu+1 with an omega, Performer without one, Performer with unsupported m
+    om = _t(shape=(1, 1, 64, 256))
+    assert _fwd(lib, ok, ok, ok, omega=om) == B.LA_ERR_INVALID_ARG
+    assert _fwd(lib, ok, ok, ok, fm=B.LA_FM_PERFORMER) == B.LA_ERR_INVALID_ARG
+    assert _fwd(lib, ok, ok, ok, fm=B.LA_FM_PERFORMER,
+                omega=_t(shape=(1, 1, 64, 96))) == B.LA_ERR_UNSUPPORTED
+    # ω rows must equal d
+    assert _fwd(lib, ok, ok, ok, fm=B.LA_FM_PERFORMER,
+                omega=_t(shape=(1, 1, 32, 256))) == B.LA_ERR_INVALID_ARG
+    # unknown feature map
+    assert _fwd(lib, ok, ok, ok, fm=7) == B.LA_ERR_INVALID_ARG
+
+
+def test_forward_with_state_needs_state_buffers(lib):
+    ok = _t()
+    st = lib.la_forward_with_state(ctypes.byref(ok), ctypes.byref(ok), ctypes.byref(ok), None, 0,
+                                   None, 1, ctypes.byref(ok), None, 0x20000, None)
+    assert st == B.LA_ERR_INVALID_ARG
+    st = lib.la_forward_with_state(ctypes.byref(ok), ctypes.byref(ok), ctypes.byref(ok), None, 0,
+                                   None, 1, ctypes.byref(ok), 0x20004, 0x20000, None)
+    assert st == B.LA_ERR_INVALID_ARG
+
+
+def test_decode_validation(lib):
+    q = _t(shape=(4, 2, 1, 128))
+    ok_state = 0x40000
+    call = lambda mu, nu, qq, out=None: lib.la_decode_step(
+        mu, nu, ctypes.byref(qq), ctypes.byref(qq), ctypes.byref(qq), None,
+        ctypes.byref(out or qq), None)
+    assert call(None, ok_state, q) == B.LA_ERR_INVALID_ARG
+    assert call(ok_state + 4, ok_state, q) == B.LA_ERR_INVALID_ARG
+    assert call(ok_state, ok_state, _t(shape=(4, 2, 2, 128))) == B.LA_ERR_INVALID_ARG
+    assert call(ok_state, ok_state, _t(shape=(4, 2, 1, 96))) == B.LA_ERR_UNSUPPORTED
+    assert call(ok_state, ok_state, q, _t(shape=(4, 2, 1, 128), dtype=B.LA_F32)) == \
+        B.LA_ERR_INVALID_ARG
+
+
+def test_product_path_has_no_oracle_or_cpu_fallback():
+    pkg = os.path.join(ROOT, "causal_kernelized_linear_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*"), recursive=True):
+        if not os.path.isfile(path) or "_build" in path:
+            continue
+        if not path.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cc")):
+            continue
+        text = open(path, encoding="utf-8").read()
+        assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), path
+        assert "linattn_oracle" not in text and "liboracle" not in text, path
