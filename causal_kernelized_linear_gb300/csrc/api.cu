@@ -188,6 +188,59 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+// Forward into a workspace of `ws_floats` floats obtained from `get_ws`
+// after validation (no allocation).  Segments are planned as for la_forward,
+// then reduced until the per-segment states fit; a request whose smallest
+// plan does not fit is rejected with LA_ERR_UNSUPPORTED before anything is
+// queued.
+la_status forward_in_workspace(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                               const float* decay_a, la_feature_map feature_map,
+                               const la_tensor* omega, int causal, la_tensor* out,
+                               la_status (*get_ws)(float**), size_t ws_floats,
+                               cudaStream_t stream) {
+  FwdArgs a;
+  la_status st = validate_forward(q, k, v, decay_a, feature_map, omega, causal, out, &a);
+  if (st != LA_OK) return st;
+  DeviceInfo di;
+  st = device_info(&di);
+  if (st != LA_OK) return st;
+  a.status = di.status;
+  a.num_sms = di.num_sms;
+  if (a.n == 0) return LA_OK;
+  const int64_t BH = a.B * a.H;
+  const size_t per_state = (size_t)a.dp * a.d + a.dp;
+  SegmentPlan plan = plan_segments(BH, a.n, a.num_sms, 32, 2);
+  auto need = [&](const SegmentPlan& p) -> size_t {
+    const bool use_ws = !a.causal || p.nseg > 1;
+    if (!use_ws) return 0;
+    return (size_t)BH * per_state * (size_t)p.nseg + (a.causal ? 0 : (size_t)BH * per_state);
+  };
+  while (need(plan) > ws_floats && plan.nseg > 1) {
+    const int g = plan.nseg - 1;
+    int64_t len = (a.n + g - 1) / g;
+    len = ((len + 31) / 32) * 32;
+    plan.seg_len = len;
+    plan.nseg = (int)((a.n + len - 1) / len);
+  }
+  if (need(plan) > ws_floats) return LA_ERR_UNSUPPORTED;
+  float* ws = nullptr;
+  if (need(plan) > 0) {
+    st = get_ws(&ws);
+    if (st != LA_OK) return st;
+  }
+  const size_t state_elems = (size_t)a.dp * a.d;
+  float* ws_state = ws;
+  float* ws_z = ws ? ws + (size_t)BH * plan.nseg * state_elems : nullptr;
+  float* tot_state = nullptr;
+  float* tot_z = nullptr;
+  if (!a.causal) {
+    tot_state = ws + (size_t)BH * plan.nseg * per_state;
+    tot_z = tot_state + (size_t)BH * state_elems;
+  }
+  return to_status(simt_forward(a, stream, ws_state, ws_z, tot_state, tot_z, plan));
+}
+
 }  // namespace la
 
 extern "C" {

@@ -2,8 +2,11 @@
 // Not part of the public ABI (include/linattn.h is).
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+
+#include "linattn.h"
 
 namespace la {
 
@@ -59,6 +62,15 @@ cudaError_t simt_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state,
 cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* tot_z,
                          int64_t BH, int64_t H, int nseg, int64_t seg_len, int64_t n,
                          int dp, int d, const float* decay, cudaStream_t stream);
+
+// la_forward with a fixed workspace of ws_floats floats, fetched through
+// get_ws only when the plan needs it, instead of stream-ordered allocations
+// (see la_forward_noalloc).
+la_status forward_in_workspace(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                               const float* decay_a, la_feature_map feature_map,
+                               const la_tensor* omega, int causal, la_tensor* out,
+                               la_status (*get_ws)(float**), size_t ws_floats,
+                               cudaStream_t stream);
 
 // Records `k` kernel launches in the process-wide launch counter.
 void count_launches(int k);

@@ -148,6 +148,36 @@ const char* la_status_string(la_status status);
 la_status la_get_last_device_status(la_stream stream);
 
 /*
+ * la_forward_noalloc — la_forward for callers that cannot allocate device
+ * memory during the call: code running inside an allocator or out-of-memory
+ * handler, under a memory pool whose policy forbids growth, or in a setting
+ * where cudaMalloc / cudaMallocAsync would deadlock or be refused.  It
+ * allocates nothing: the per-segment states that la_forward takes with
+ * cudaMallocAsync live in a fixed scratch array of 4 Mi floats (16 MiB),
+ * which every GPU that loads the library holds until the process exits.
+ * The method is the same as la_forward; the pages have no counterpart of
+ * this entry point, it only changes where the temporary states live.
+ *
+ *   Arguments, output and validation are those of la_forward.
+ *   Segments are planned as for la_forward, then merged (fewer, longer
+ *   segments, so less parallelism) until their states fit the scratch.  A
+ *   request whose states do not fit even as one segment per head (a
+ *   non-causal call with B·H·2·(d'·d + d') > 4 Mi floats) returns
+ *   LA_ERR_UNSUPPORTED and queues nothing.  Causal requests that fit in one
+ *   segment per head use no scratch at all.
+ *   The first call on a device looks up the scratch array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call overwrites the part of the scratch it uses and nothing needs
+ *   to be zeroed, but all calls share the one array: calls that overlap on
+ *   the GPU (e.g. on two streams) race on it and give wrong results.
+ *   Serialise them (one stream, or events).
+ */
+la_status la_forward_noalloc(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                             const float* decay_a, la_feature_map feature_map,
+                             const la_tensor* omega, int causal, la_tensor* out,
+                             la_stream stream);
+
+/*
  * la_launch_count — instrumentation: the number of CUDA kernels this process
  * has queued through the library so far (all devices, all entry points).
  * The difference across a region counts the library's own launches in it.
