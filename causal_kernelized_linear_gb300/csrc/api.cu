@@ -120,12 +120,13 @@ la_status validate_forward(const la_tensor* q, const la_tensor* k, const la_tens
   return LA_OK;
 }
 
-// Cut every head into segments so that the grid covers the GPU a few times over.
+// Cut every head into segments so that all CTAs fit in one wave
+// (num_sms · ctas_per_sm); with more heads than that, one segment per head.
 SegmentPlan plan_segments(int64_t BH, int64_t n, int num_sms, int64_t granule,
                           int ctas_per_sm) {
   SegmentPlan p;
   const int64_t target = (int64_t)num_sms * ctas_per_sm;
-  int64_t g = (target + BH - 1) / BH;
+  int64_t g = target / BH;
   const int64_t max_g = std::max<int64_t>(1, (n + granule - 1) / granule);
   g = std::max<int64_t>(1, std::min(g, max_g));
   int64_t len = (n + g - 1) / g;
@@ -139,6 +140,30 @@ la_status to_status(cudaError_t e) {
   if (e == cudaSuccess) return LA_OK;
   if (e == cudaErrorMemoryAllocation) return LA_ERR_OUT_OF_MEMORY;
   return LA_ERR_CUDA;
+}
+
+// Kernel family for a validated request and its segment plan: the tcgen05
+// path for what it supports, the fp32 CUDA-core path otherwise.
+struct PathPlan {
+  bool tensor_cores;
+  SegmentPlan plan;
+  int64_t granule;
+};
+
+PathPlan choose_path(const FwdArgs& a) {
+  PathPlan pp;
+  pp.tensor_cores = tc_forward_supported(a);
+  // tcgen05 path: one 512-thread CTA per SM, 128-token chunks; CUDA-core
+  // path: two CTAs per SM, 32-token chunks
+  pp.granule = pp.tensor_cores ? tc_segment_granule() : 32;
+  pp.plan = plan_segments(a.B * a.H, a.n, a.num_sms, pp.granule, pp.tensor_cores ? 1 : 2);
+  return pp;
+}
+
+cudaError_t dispatch_forward(const FwdArgs& a, const PathPlan& pp, cudaStream_t stream,
+                             float* ws_state, float* ws_z, float* tot_state, float* tot_z) {
+  if (pp.tensor_cores) return tc_forward(a, stream, ws_state, ws_z, tot_state, tot_z, pp.plan);
+  return simt_forward(a, stream, ws_state, ws_z, tot_state, tot_z, pp.plan);
 }
 
 la_status run_forward(FwdArgs& a, cudaStream_t stream) {
@@ -157,7 +182,8 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
       return LA_ERR_CUDA;
     return LA_OK;
   }
-  const SegmentPlan plan = plan_segments(BH, a.n, a.num_sms, 32, 2);
+  const PathPlan pp = choose_path(a);
+  const SegmentPlan& plan = pp.plan;
   const bool need_ws = !a.causal || plan.nseg > 1;
   const bool need_tot = need_ws && (a.mu_out == nullptr);
   size_t ws_floats = 0;
@@ -179,7 +205,7 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
     tot_state = ws + (size_t)BH * plan.nseg * (state_elems + a.dp);
     tot_z = tot_state + (size_t)BH * state_elems;
   }
-  cudaError_t e = simt_forward(a, stream, ws_state, ws_z, tot_state, tot_z, plan);
+  cudaError_t e = dispatch_forward(a, pp, stream, ws_state, ws_z, tot_state, tot_z);
   if (ws) {
     cudaError_t f = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess) e = f;
@@ -210,7 +236,8 @@ la_status forward_in_workspace(const la_tensor* q, const la_tensor* k, const la_
   if (a.n == 0) return LA_OK;
   const int64_t BH = a.B * a.H;
   const size_t per_state = (size_t)a.dp * a.d + a.dp;
-  SegmentPlan plan = plan_segments(BH, a.n, a.num_sms, 32, 2);
+  PathPlan pp = choose_path(a);
+  SegmentPlan& plan = pp.plan;
   auto need = [&](const SegmentPlan& p) -> size_t {
     const bool use_ws = !a.causal || p.nseg > 1;
     if (!use_ws) return 0;
@@ -219,7 +246,7 @@ la_status forward_in_workspace(const la_tensor* q, const la_tensor* k, const la_
   while (need(plan) > ws_floats && plan.nseg > 1) {
     const int g = plan.nseg - 1;
     int64_t len = (a.n + g - 1) / g;
-    len = ((len + 31) / 32) * 32;
+    len = ((len + pp.granule - 1) / pp.granule) * pp.granule;
     plan.seg_len = len;
     plan.nseg = (int)((a.n + len - 1) / len);
   }
@@ -238,7 +265,7 @@ la_status forward_in_workspace(const la_tensor* q, const la_tensor* k, const la_
     tot_state = ws + (size_t)BH * plan.nseg * per_state;
     tot_z = tot_state + (size_t)BH * state_elems;
   }
-  return to_status(simt_forward(a, stream, ws_state, ws_z, tot_state, tot_z, plan));
+  return to_status(dispatch_forward(a, pp, stream, ws_state, ws_z, tot_state, tot_z));
 }
 
 }  // namespace la

@@ -296,10 +296,12 @@ __global__ void __launch_bounds__(256)
 segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z, int64_t H,
                     int nseg, int64_t seg_len, int64_t n, int dpd, int dp,
                     const float* decay) {
+  constexpr int kBatch = 8;  // aggregates loaded together to keep loads in flight
   const int64_t bh = blockIdx.x;
   const int e = blockIdx.y * 256 + threadIdx.x;
   if (e >= dpd + dp) return;
   const float a = decay ? decay[bh % H] : 1.f;
+  const float a_full = decay_pow(a, seg_len);  // every segment but the last is full
   float* base;
   int64_t stride;
   if (e < dpd) {
@@ -310,11 +312,19 @@ segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z
     stride = dp;
   }
   float acc = 0.f;  // state entering segment g
-  for (int g = 0; g < nseg; ++g) {
-    const float agg = base[g * stride];
-    base[g * stride] = acc;
-    const int64_t len = min(seg_len, n - (int64_t)g * seg_len);
-    acc = decay_pow(a, len) * acc + agg;
+  for (int g0 = 0; g0 < nseg; g0 += kBatch) {
+    float agg[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) agg[j] = (g0 + j < nseg) ? base[(g0 + j) * stride] : 0.f;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int g = g0 + j;
+      if (g < nseg) {
+        base[g * stride] = acc;
+        const int64_t len = min(seg_len, n - (int64_t)g * seg_len);
+        acc = (len == seg_len ? a_full : decay_pow(a, len)) * acc + agg[j];
+      }
+    }
   }
   if (tot_state) {
     if (e < dpd) tot_state[bh * dpd + e] = acc;

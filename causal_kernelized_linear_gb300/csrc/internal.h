@@ -57,6 +57,12 @@ cudaError_t simt_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state,
                          float* ws_z, float* tot_state, float* tot_z,
                          const SegmentPlan& plan);
 
+// tcgen05/TMA chunked forward (bf16, elu+1, causal, d ∈ {64, 128}, n ≥ 128).
+bool tc_forward_supported(const FwdArgs& a);
+int64_t tc_segment_granule();
+cudaError_t tc_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                       float* tot_state, float* tot_z, const SegmentPlan& plan);
+
 // Exclusive decayed prefix over the per-segment aggregates of every head, in
 // place, plus the inclusive total (final state) when tot_state != nullptr.
 cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* tot_z,

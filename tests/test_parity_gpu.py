@@ -116,6 +116,13 @@ CASES = [
     ("bf16", 64, "performer", 128, (0.95, 0.99), 700, True),
     ("bf16", 32, "performer", 256, None, 259, False),
     ("bf16", 128, "performer", 256, (0.9, 0.99), 200, True),
+    # tensor-core path (bf16, elu+1, causal, d ∈ {64, 128}, n ≥ 128)
+    ("bf16", 64, "elu1", 0, (0.0, 0.0), 300, True),
+    ("bf16", 128, "elu1", 0, (0.5, 0.9), 128, True),
+    ("bf16", 128, "elu1", 0, (0.99, 0.9999), 129, True),
+    ("bf16", 64, "elu1", 0, None, 20000, True),
+    ("bf16", 128, "elu1", 0, (0.3, 0.7), 4097, True),
+    ("bf16", 64, "elu1", 0, (1.0, 1.0), 2560, True),
     ("f32", 32, "elu1", 0, (0.9, 0.999), 1111, True),
     ("f32", 64, "elu1", 0, None, 517, False),
     ("f32", 128, "elu1", 0, (0.0, 1.0), 129, True),
