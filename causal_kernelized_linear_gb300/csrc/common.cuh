@@ -17,8 +17,10 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 }
 
 // φ(x) = elu(x) + 1 with α = 1 ("Linear Attention Research 2026", Linear
-// Transformer): x + 1 for x > 0, e^x otherwise.
-__device__ __forceinline__ float elu1(float x) { return x > 0.f ? x + 1.f : expf(x); }
+// Transformer): x + 1 for x > 0, e^x otherwise — computed as
+// max(x, 0) + exp(min(x, 0)), which is the same value (exp(0) = 1 exactly)
+// without a data-dependent branch.
+__device__ __forceinline__ float elu1(float x) { return fmaxf(x, 0.f) + expf(fminf(x, 0.f)); }
 
 // Weight of the newest token in eq (10)–(11): 1 − a, except a = 1 which is
 // the plain running sum of eq (7)–(8).

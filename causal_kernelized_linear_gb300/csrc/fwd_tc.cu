@@ -2,26 +2,38 @@
 // linear attention, elu+1 feature map, bf16 inputs, fp32 state, d = d' ∈ {64, 128}.
 //
 // Method ("Efficient Transformers II" §2.2, eq (7)–(11) with the causal
-// readout of eq (9)); per head, a chunk of C = 128 tokens (local t, s) with
-// state (μ, ν) = (S, z) at its start:
-//   scores  A = Q'K'ᵀ                                  (tcgen05, fp32 in TMEM)
-//   P_ts    = w·a^{t−s}·A_ts for s ≤ t, else 0         (registers → bf16 in TMEM)
-//   num     = P·V + Q''·S,  Q'' = diag(a^{t+1})·Q'     (two tcgen05 MMAs, one accumulator)
-//   den     = Σ_s P_ts + q''_t·z                       (P·1 by tcgen05; q''·z in registers)
-//   o_t     = num_t / den_t                            (epilogue, bf16, TMA store)
-//   ΔS      = K''ᵀ·V, Δz = K''ᵀ·1, K'' = diag(w·a^{cs−1−s})·K'   (tcgen05)
-//   S ← a^{cs}·S + ΔS,  z ← a^{cs}·z + Δz              (fp32 registers)
+// readout of eq (9)); per head, a chunk of C = 128 tokens (local t, s), cs of
+// them valid, with state (μ, ν) = (S, z) at its start:
+//   P_ts  = w·a^{t−s}·(q'_t·k'_s) for s ≤ t, else 0
+//   num_t = Σ_s P_ts v_s + a^{t+1} q'_t·S,   den_t = Σ_s P_ts + a^{t+1} q'_t·z
+//   o_t   = num_t / den_t
+//   S ← a^{cs}·S + Σ_s w·a^{cs−1−s} k'_sᵀ v_s,   z likewise
 // i.e. eq (10)–(11) unrolled over the chunk; the intra-chunk part is the
 // quadratic form of "Efficient Transformers I" eq (25)–(26) on the chunk.
 //
+// The decay is folded into the bf16 tensor-core operands.  Two foldings:
+//   centered (a ≥ 0.5 or a = 1):  Q'' = a^{t−63}·q',  K'' = w·a^{63−s}·k'
+//       Q''K''ᵀ = w·a^{t−s}·Q'K'ᵀ, so P is the causally masked product itself;
+//       num = P·V + Q''·(a^{64}S);  ΔS'' = K''ᵀV,  S ← a^{cs}S + a^{cs−64}ΔS''.
+//       Every power stays within a^{±64}, inside bf16/fp32 range for a ≥ 0.5.
+//       Only Q'' (TMEM) and K'' (smem; the K-major view feeds Q''K''ᵀ, the
+//       MN-major view feeds K''ᵀV) are needed, so the raw Q/K tiles are
+//       released as soon as φ has read them.
+//   general (any a ∈ [0, 1]):  Q' (smem), Q'' = a^{t+1}q' (TMEM), K' (smem),
+//       K'' = w·a^{cs−1−s}k'; P = (w·a^{t−s}) ⊙ Q'K'ᵀ with a table of w·a^k;
+//       num = P·V + Q''·S;  S ← a^{cs}S + K''ᵀV.
+// Each CTA picks the folding for its head's a.
+//
 // One CTA per (segment, head), 16 warps:
-//   warp 0        TMA producer (Q, K, V tiles; one Q buffer, two K/V stages)
+//   warp 0        TMA producer
 //   warp 1        tcgen05 MMA issuer, TMEM owner
-//   warps 4–7     φ(Q) → Q' (smem) and Q'' (TMEM); masked decayed P; epilogue
-//   warps 8–15    φ(K) → K' and K''; fp32 state S (64 columns per warpgroup)
-// Long sequences are split into segments; a state-only launch of the same
-// kernel computes each segment's decayed aggregate, segment_scan turns them
-// into the states entering each segment, and the full launch produces o.
+//   warps 4–7     φ(Q) → Q'' (and Q'); masked P; epilogue o = num/den → TMA store
+//   warps 8–15    φ(K) → K'' (and K'); fp32 state S (64 columns per warpgroup)
+// tcgen05 products: scores = Q''K''ᵀ (or Q'K'ᵀ), ΔS = K''ᵀV, Δz = K''ᵀ1,
+// num = Q''S + P·V, Σ_s P = P·1 — fp32 accumulators in TMEM.
+// Long sequences are split into segments: a state-only launch of this kernel
+// computes each segment's decayed aggregate, segment_scan turns them into the
+// states entering each segment, and the full launch produces o.
 // Every wait is bounded in time: on expiry the kernel records LA_ERR_TIMEOUT
 // in the device status word, stops issuing work, drains what it issued and
 // frees its TMEM.
@@ -39,37 +51,36 @@ namespace {
 
 using namespace tc;
 
-constexpr int kC = 128;          // tokens per chunk (MMA M)
-constexpr int kThreadsTc = 512;  // 16 warps
+constexpr int kC = 128;                  // tokens per chunk (MMA M)
+constexpr int kThreadsTc = 512;          // 16 warps
+constexpr float kCenteredMinDecay = 0.5f;
 
 template <int D>
 struct TcCfg {
   static constexpr int HALVES = D / 64;          // 64-column (128-byte) swizzle atoms per row
   static constexpr int TILE = kC * D * 2;        // one [128 × D] bf16 tile
   static constexpr int STILE = D * D * 2;        // state tile [D × D] bf16
-  // shared memory (offsets from a 1024-aligned base)
-  static constexpr int oQ = 0;
-  static constexpr int oK0 = oQ + TILE;
-  static constexpr int oK1 = oK0 + TILE;
-  static constexpr int oKP = oK1 + TILE;
+  // shared memory (offsets from a 1024-aligned base): seven [128 × D] tiles
+  // (see Layout for their roles), the bf16 state operand and small tables.
+  static constexpr int oT0 = 0;
+  static constexpr int oT1 = oT0 + TILE;
+  static constexpr int oT2 = oT1 + TILE;
+  static constexpr int oKP = oT2 + TILE;
   static constexpr int oV0 = oKP + TILE;
   static constexpr int oV1 = oV0 + TILE;
-  static constexpr int oS = oV1 + TILE;
+  static constexpr int oS = oV1 + TILE;          // state operand, bf16 [D' × D]
   static constexpr int oONES = oS + STILE;       // 16×16 bf16 ones (512 B)
-  // z [D] fp32.  One copy suffices: φ(Q) of chunk c reads z_c before it
-  // signals q_ready(c), and z_{c+1} is written only after MMA3(c) — issued
-  // after MMA1(c), which waits for q_ready(c) — has completed.
-  static constexpr int oZ = oONES + 512;
-  static constexpr int oPW = oZ + D * 4;         // w·a^k, k = 0..127 (+pad)
+  static constexpr int oZ = oONES + 512;         // normalizer operand z [D] fp32
+  static constexpr int oPW = oZ + D * 4;         // w·a^k, k = 0..127 (general folding)
   static constexpr int oBAR = oPW + 132 * 4;     // mbarriers
-  static constexpr int NBAR = 24;  // ≥ B_COUNT
+  static constexpr int NBAR = 32;
   static constexpr int oMISC = oBAR + NBAR * 8;  // tmem slot, abort flag
   static constexpr int BYTES = oMISC + 16;
   // + alignment slack; at least half of the SM's shared memory so that one
   // CTA (which owns all 512 TMEM columns) runs per SM
   static constexpr int SMEM_ALLOC = (BYTES + 1024 > 118 * 1024) ? BYTES + 1024 : 118 * 1024;
   // tensor memory columns
-  static constexpr uint32_t TS = 0;              // scores (fp32) / P (bf16 pairs, cols 0..63)
+  static constexpr uint32_t TS = 0;              // scores (fp32) / P (bf16 pairs)
   static constexpr uint32_t TN = 128;            // numerator [128 × D]
   static constexpr uint32_t TD = TN + D;         // ΔS [D' × D] (lanes = feature)
   static constexpr uint32_t TZ = TD + D;         // Δz (16 columns, column 0 used)
@@ -80,11 +91,41 @@ struct TcCfg {
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
 
-// barrier indices
+// z needs one copy: φ(Q) of chunk c reads z_c before it signals q_ready(c),
+// and z_{c+1} is written only after MMA3(c) — issued after the scores MMA of
+// chunk c, which waits for q_ready(c) — has completed.
+
 enum {
-  B_QFULL = 0, B_QEMPTY, B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1, B_VFULL0, B_VFULL1,
-  B_VEMPTY0, B_VEMPTY1, B_QREADY, B_KREADY, B_KPEMPTY, B_SREADY, B_SEMPTY, B_SCORES,
-  B_PREADY, B_NUMFULL, B_NUMEMPTY, B_DSFULL, B_DSEMPTY, B_QPEMPTY, B_MMADONE, B_STAGED, B_COUNT
+  B_QFULL0 = 0, B_QFULL1, B_QEMPTY0, B_QEMPTY1,
+  B_KFULL0, B_KFULL1, B_KFULL2, B_KEMPTY0, B_KEMPTY1, B_KEMPTY2,
+  B_VFULL0, B_VFULL1, B_VFULL2, B_VEMPTY0, B_VEMPTY1, B_VEMPTY2,
+  B_KREADY0, B_KREADY1, B_KREADY2,   // one per K stage: φ(K) may run a chunk ahead
+  B_QREADY, B_KPEMPTY, B_SREADY, B_SEMPTY, B_SCORES, B_PREADY, B_NUMFULL, B_NUMEMPTY,
+  B_DSFULL, B_DSEMPTY, B_QPEMPTY, B_MMADONE, B_STAGED, B_COUNT
+};
+
+// Roles of the seven tiles T0, T1, T2, KP, V0, V1 (and S) per kernel mode:
+//   centered, full:  Q stages T0, T1 | K stages T2, KP (φ(K) writes K'' in place) | V V0, V1
+//   general, full:   Q T0 | K stages T1, T2 (K' in place) | K'' in KP | V V0, V1
+//   state-only:      K stages T0, T1, T2 (K'' in place) | V stages KP, V0, V1
+template <int D, bool FULL, bool CEN>
+struct Layout {
+  using Cfg = TcCfg<D>;
+  static constexpr int QST = (FULL && CEN) ? 2 : 1;
+  static constexpr int KST = FULL ? 2 : 3;
+  static constexpr int VST = FULL ? 2 : 3;
+  static constexpr bool K_IN_PLACE = !(FULL && !CEN);   // K'' overwrites the raw K tile
+  __device__ static int q_off(int s) { return s ? Cfg::oT1 : Cfg::oT0; }
+  __device__ static int k_off(int s) {
+    if (FULL && CEN) return s ? Cfg::oKP : Cfg::oT2;
+    if (FULL) return s ? Cfg::oT2 : Cfg::oT1;
+    return s == 0 ? Cfg::oT0 : (s == 1 ? Cfg::oT1 : Cfg::oT2);
+  }
+  __device__ static int kpp_off(int s) { return K_IN_PLACE ? k_off(s) : Cfg::oKP; }
+  __device__ static int v_off(int s) {
+    if (FULL) return s ? Cfg::oV1 : Cfg::oV0;
+    return s == 0 ? Cfg::oKP : (s == 1 ? Cfg::oV0 : Cfg::oV1);
+  }
 };
 
 struct TcParams {
@@ -98,14 +139,24 @@ struct TcParams {
   int* status;
 };
 
-// 16-byte chunk j (8 bf16, columns h*64 + 8j …) of row `row` in a swizzled tile.
+// 16-byte chunk j (8 bf16, columns h*64 + 8j …) of row `row` in a tile stored
+// as column halves of [rows × 64] with the 128-byte swizzle (TMA layout).
 __device__ __forceinline__ uint32_t sw_chunk(int rows, int row, int half, int j) {
   return (uint32_t)(half * rows * 128 + row * 128 + ((j ^ (row & 7)) << 4));
 }
 
-// φ(x) = elu(x) + 1 with the fast exponential: the result is rounded to bf16,
-// so the intrinsic's few-ulp error is far below the output precision.
-__device__ __forceinline__ float elu1_fast(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+// φ(x) = elu(x) + 1 = max(x, 0) + exp(min(x, 0)), written without a branch
+// (x + 1 for x > 0 since exp(0) = 1 exactly; e^x otherwise) so that warps do
+// not diverge on the sign of each element.  The fast exponential's few-ulp
+// error is far below the bf16 precision the result is rounded to.
+__device__ __forceinline__ float elu1_fast(float x) {
+  return fmaxf(x, 0.f) + __expf(fminf(x, 0.f));
+}
+
+// a^e for integer e of either sign (a > 0, or e ≥ 0).
+__device__ __forceinline__ float decay_pow_signed(float a, int e) {
+  return e == 0 ? 1.f : powf(a, (float)e);
+}
 
 // Every lane of the warp waits (bounded); the warp then agrees on the
 // outcome so that control flow — and the .sync.aligned tcgen05 operations
@@ -128,6 +179,491 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                     pack_bf16x2(f[6], f[7]));
 }
 
+struct Ctx {
+  uint8_t* sm;
+  uint32_t sbase;
+  uint64_t* bar;
+  volatile int* abort_flag;
+  float* zbuf;
+  float* pw;
+  uint32_t tmem;
+  int* status;
+  int64_t bh, t_begin, t_end;
+  int g, nchunks;
+  float a, w;
+};
+
+// ------------------------------------------------------------------ roles
+
+template <int D, bool FULL, bool CEN>
+__device__ __forceinline__ void role_producer(const Ctx& x, const CUtensorMap* map_q,
+                                              const CUtensorMap* map_k,
+                                              const CUtensorMap* map_v) {
+  using Cfg = TcCfg<D>;
+  using L = Layout<D, FULL, CEN>;
+  uint64_t* bar = x.bar;
+  int last_q = -1, last_k = -1, last_v = -1;
+  auto load = [&](const CUtensorMap* map, int off, uint64_t* b, int y) {
+    mbar_arrive_expect_tx(b, Cfg::TILE);
+    for (int h = 0; h < Cfg::HALVES; ++h)
+      tma_load_3d(x.sm + off + h * kC * 128, map, b, h * 64, y, (int)x.bh);
+  };
+  // Every wait below is for a chunk at least two behind, so the producer runs
+  // up to one full stage ring ahead of the consumers.
+  for (int c = 0; c < x.nchunks && !*x.abort_flag; ++c) {
+    const int y = (int)(x.t_begin + (int64_t)c * kC);
+    if (FULL) {
+      const int qs = c % L::QST;
+      if (c >= L::QST &&
+          !mbar_wait(&bar[B_QEMPTY0 + qs], ((c - L::QST) / L::QST) & 1, x.status, x.abort_flag))
+        break;
+      load(map_q, L::q_off(qs), &bar[B_QFULL0 + qs], y);
+      last_q = c;
+    }
+    const int ks = c % L::KST;
+    if (c >= L::KST &&
+        !mbar_wait(&bar[B_KEMPTY0 + ks], ((c - L::KST) / L::KST) & 1, x.status, x.abort_flag))
+      break;
+    load(map_k, L::k_off(ks), &bar[B_KFULL0 + ks], y);
+    last_k = c;
+    const int vs = c % L::VST;
+    if (c >= L::VST &&
+        !mbar_wait(&bar[B_VEMPTY0 + vs], ((c - L::VST) / L::VST) & 1, x.status, x.abort_flag))
+      break;
+    load(map_v, L::v_off(vs), &bar[B_VFULL0 + vs], y);
+    last_v = c;
+  }
+  if (*x.abort_flag) {
+    // drain the loads still in flight before the CTA's shared memory goes away
+    if (FULL)
+      for (int c = max(0, last_q - L::QST + 1); c <= last_q; ++c)
+        mbar_wait_drain(&bar[B_QFULL0 + c % L::QST], (c / L::QST) & 1);
+    for (int c = max(0, last_k - L::KST + 1); c <= last_k; ++c)
+      mbar_wait_drain(&bar[B_KFULL0 + c % L::KST], (c / L::KST) & 1);
+    for (int c = max(0, last_v - L::VST + 1); c <= last_v; ++c)
+      mbar_wait_drain(&bar[B_VFULL0 + c % L::VST], (c / L::VST) & 1);
+  }
+}
+
+template <int D, bool FULL, bool CEN>
+__device__ __forceinline__ void role_mma(const Ctx& x) {
+  using Cfg = TcCfg<D>;
+  using L = Layout<D, FULL, CEN>;
+  uint64_t* bar = x.bar;
+  const uint32_t tmem = x.tmem;
+  const uint32_t sS = x.sbase + Cfg::oS, sONES = x.sbase + Cfg::oONES;
+  constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);   // scores
+  constexpr uint32_t idD = idesc_bf16_f32(128, D, true, true);       // ΔS = K''ᵀ V
+  constexpr uint32_t idZ = idesc_bf16_f32(128, 16, true, false);     // Δz = K''ᵀ 1
+  constexpr uint32_t idN = idesc_bf16_f32(128, D, false, true);      // num (+)= A·{S, V}
+  constexpr uint32_t idR = idesc_bf16_f32(128, 16, false, false);    // Σ_s P = P·1
+  constexpr int KD = D / 16;                                         // K-steps over D'
+  const uint32_t lbo_kp = (D == 128) ? kC * 128 : 0;                 // M blocks of K''ᵀ
+  const uint64_t ones = smem_desc(sONES, 128, 256, kSwizzleNone);
+  int* st = x.status;
+  volatile int* ab = x.abort_flag;
+  for (int c = 0; c < x.nchunks; ++c) {
+    const int ks = c % L::KST, vs = c % L::VST;
+    const uint32_t sK = x.sbase + L::k_off(ks);
+    const uint32_t sKP = x.sbase + L::kpp_off(ks);
+    const uint32_t sV = x.sbase + L::v_off(vs);
+    if (!mbar_wait(&bar[B_KREADY0 + ks], (c / L::KST) & 1, st, ab)) break;
+    if (FULL) {
+      // scores = Q''K''ᵀ (centered) or Q'K'ᵀ (general)
+      if (!mbar_wait(&bar[B_QREADY], c & 1, st, ab)) break;
+      if (c >= 1 && !mbar_wait(&bar[B_NUMFULL], (c - 1) & 1, st, ab)) break;
+      tc_fence_after();
+      if (CEN) {
+        for (int k = 0; k < KD; ++k) {
+          const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
+          mma_ts(tmem + Cfg::TS, tmem + Cfg::TQ + k * 8,
+                 smem_desc(sKP + off, 16, 1024, kSwizzle128B), idS, k > 0);
+        }
+        mma_commit(&bar[B_SCORES]);
+      } else {
+        const uint32_t sQ = x.sbase + L::q_off(0);
+        for (int k = 0; k < KD; ++k) {
+          const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
+          mma_ss(tmem + Cfg::TS, smem_desc(sQ + off, 16, 1024, kSwizzle128B),
+                 smem_desc(sK + off, 16, 1024, kSwizzle128B), idS, k > 0);
+        }
+        mma_commit(&bar[B_SCORES]);
+        mma_commit(&bar[B_QEMPTY0]);
+        mma_commit(&bar[B_KEMPTY0 + ks]);            // K' was the last reader of the raw tile
+      }
+    } else {
+      tc_fence_after();
+    }
+    // ΔS = K''ᵀ V ; Δz = K''ᵀ 1
+    if (!mbar_wait(&bar[B_VFULL0 + vs], (c / L::VST) & 1, st, ab)) break;
+    if (c >= 1 && !mbar_wait(&bar[B_DSEMPTY], (c - 1) & 1, st, ab)) break;
+    tc_fence_after();
+    for (int k = 0; k < kC / 16; ++k) {
+      const uint64_t ad = smem_desc(sKP + k * 2048, lbo_kp, 1024, kSwizzle128B);
+      mma_ss(tmem + Cfg::TD, ad, smem_desc(sV + k * 2048, kC * 128, 1024, kSwizzle128B), idD, k > 0);
+      mma_ss(tmem + Cfg::TZ, ad, ones, idZ, k > 0);
+    }
+    mma_commit(&bar[B_DSFULL]);
+    if (L::K_IN_PLACE) mma_commit(&bar[B_KEMPTY0 + ks]);   // K'' tile free for the next load
+    else mma_commit(&bar[B_KPEMPTY]);
+    if (!FULL) {
+      mma_commit(&bar[B_VEMPTY0 + vs]);
+      continue;
+    }
+    // num = Q''·S
+    if (!mbar_wait(&bar[B_SREADY], c & 1, st, ab)) break;
+    if (c >= 1 && !mbar_wait(&bar[B_NUMEMPTY], (c - 1) & 1, st, ab)) break;
+    tc_fence_after();
+    for (int k = 0; k < KD; ++k)
+      mma_ts(tmem + Cfg::TN, tmem + Cfg::TQ + k * 8,
+             smem_desc(sS + k * 2048, D * 128, 1024, kSwizzle128B), idN, k > 0);
+    mma_commit(&bar[B_SEMPTY]);
+    mma_commit(&bar[B_QPEMPTY]);
+    // num += P·V ; Σ_s P
+    if (!mbar_wait(&bar[B_PREADY], c & 1, st, ab)) break;
+    tc_fence_after();
+    for (int k = 0; k < kC / 16; ++k) {
+      mma_ts(tmem + Cfg::TN, tmem + Cfg::TS + k * 8,
+             smem_desc(sV + k * 2048, kC * 128, 1024, kSwizzle128B), idN, 1);
+      mma_ts(tmem + Cfg::TR, tmem + Cfg::TS + k * 8, ones, idR, k > 0);
+    }
+    mma_commit(&bar[B_NUMFULL]);
+  }
+  // every issued MMA must finish before TMEM is released
+  mma_commit(&bar[B_MMADONE]);
+  mbar_wait_drain(&bar[B_MMADONE], 0);
+}
+
+// Warps 4–7: φ(Q), masked P, epilogue.  Thread r owns row / TMEM lane r.
+// Order per chunk c: P(c), then φ(Q) of chunk c+1 (so the next scores MMA can
+// start as soon as P·V of chunk c is done), then the epilogue of chunk c.
+template <int D, bool CEN>
+__device__ __forceinline__ void role_rows(const Ctx& x, const CUtensorMap* map_o, int warp,
+                                          int lane) {
+  using Cfg = TcCfg<D>;
+  using L = Layout<D, true, CEN>;
+  uint64_t* bar = x.bar;
+  const uint32_t tmem = x.tmem;
+  int* st = x.status;
+  volatile int* ab = x.abort_flag;
+  const int r = (warp - 4) * 32 + lane;
+  const int wq = warp - 4;                        // lane quarter
+  const uint32_t lane_base = (uint32_t)wq * 32;
+  const float a_row = CEN ? decay_pow_signed(x.a, r - 63) : decay_pow(x.a, r + 1);
+
+  // φ(Q) of chunk c: Q'' = a_row·φ(q) into TMEM and q''·z; the general folding
+  // also writes Q' back in place for the scores MMA.
+  auto phi_q = [&](int c, float& qz) -> bool {
+    const int qs = c % L::QST;
+    if (!warp_wait(&bar[B_QFULL0 + qs], (c / L::QST) & 1, st, ab)) return false;
+    if (c >= 1 && !warp_wait(&bar[B_QPEMPTY], (c - 1) & 1, st, ab)) return false;
+    if (!warp_wait(&bar[B_SREADY], c & 1, st, ab)) return false;
+    const float4* zc4 = reinterpret_cast<const float4*>(x.zbuf);
+    qz = 0.f;
+#pragma unroll
+    for (int h = 0; h < Cfg::HALVES; ++h) {
+      uint8_t* qt = x.sm + L::q_off(qs);
+      uint32_t packed[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float f[8];
+        uint4* qp = reinterpret_cast<uint4*>(qt + sw_chunk(kC, r, h, j));
+        unpack8(*qp, f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = elu1_fast(f[e]);
+        if (!CEN) *qp = pack8(f);
+        const float4 z0 = zc4[(h * 64 + j * 8) / 4];
+        const float4 z1 = zc4[(h * 64 + j * 8) / 4 + 1];
+        const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const uint32_t pr = pack_bf16x2(a_row * f[e], a_row * f[e + 1]);
+          packed[j * 4 + e / 2] = pr;
+          qz += bf16lo_to_f32(pr) * zz[e] + bf16hi_to_f32(pr) * zz[e + 1];
+        }
+      }
+      tmem_st32(tmem_addr(tmem, lane_base, Cfg::TQ + h * 32), packed);
+    }
+    tmem_st_wait();
+    if (!CEN) fence_proxy_async_smem();            // Q' is read by the tensor core
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&bar[B_QREADY]);
+      if (CEN) mbar_arrive(&bar[B_QEMPTY0 + qs]);  // raw Q tile no longer needed
+    }
+    return true;
+  };
+
+  float qz_next = 0.f;
+  bool ok = x.nchunks > 0 && phi_q(0, qz_next);
+  for (int c = 0; ok && c < x.nchunks; ++c) {
+    const int vs = c % L::VST;
+    const float qz = qz_next;
+    // ---- P: causal mask (and, general folding, the decay w·a^{t−s})
+    if (!warp_wait(&bar[B_SCORES], c & 1, st, ab)) break;
+    tc_fence_after();
+    // 32-column blocks b: b > wq lies above the diagonal for the whole warp
+    // (zeros, scores not read), b < wq below it (no mask), b == wq straddles it.
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      uint32_t pk[16];
+      if (b > wq) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = 0u;
+      } else {
+        uint32_t sc[32];
+        tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TS + b * 32), sc);
+        tmem_ld_wait();
+        if (CEN) {
+          if (b < wq) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2)
+              pk[j / 2] = pack_bf16x2(__uint_as_float(sc[j]), __uint_as_float(sc[j + 1]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const int s0 = b * 32 + j;
+              const float p0 = (s0 <= r) ? __uint_as_float(sc[j]) : 0.f;
+              const float p1 = (s0 + 1 <= r) ? __uint_as_float(sc[j + 1]) : 0.f;
+              pk[j / 2] = pack_bf16x2(p0, p1);
+            }
+          }
+        } else {
+          const float* wp = x.pw + (r - b * 32);   // wp[-j] = w·a^{r-(32b+j)}
+          if (b < wq) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2)
+              pk[j / 2] = pack_bf16x2(wp[-j] * __uint_as_float(sc[j]),
+                                      wp[-j - 1] * __uint_as_float(sc[j + 1]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const int s0 = b * 32 + j;
+              const float p0 = (s0 <= r) ? wp[-j] * __uint_as_float(sc[j]) : 0.f;
+              const float p1 = (s0 + 1 <= r) ? wp[-j - 1] * __uint_as_float(sc[j + 1]) : 0.f;
+              pk[j / 2] = pack_bf16x2(p0, p1);
+            }
+          }
+        }
+      }
+      tmem_st16(tmem_addr(tmem, lane_base, Cfg::TS + b * 16), pk);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_PREADY]);
+
+    // ---- φ(Q) of the next chunk
+    if (c + 1 < x.nchunks && !phi_q(c + 1, qz_next)) break;
+
+    // ---- epilogue: o = num / den → bf16 → staging (V tile of this chunk) → TMA store
+    if (!warp_wait(&bar[B_NUMFULL], c & 1, st, ab)) break;
+    tc_fence_after();
+    uint32_t rs = 0;
+    tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TR), rs);
+    tmem_ld_wait();
+    const float inv_den = 1.f / (__uint_as_float(rs) + qz);
+    uint8_t* stage = x.sm + L::v_off(vs);
+    const uint32_t stage_sa = x.sbase + L::v_off(vs);
+#pragma unroll
+    for (int j0 = 0; j0 < D; j0 += 32) {
+      uint32_t nv[32];
+      tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TN + j0), nv);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(nv[q8 * 8 + e]) * inv_den;
+        const int col = j0 + q8 * 8;
+        sts128(stage_sa + sw_chunk(kC, r, col >> 6, (col & 63) >> 3), pack8(f));
+      }
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&bar[B_NUMEMPTY]);
+      mbar_arrive(&bar[B_STAGED]);
+    }
+    if (r == 0) {
+      // all four warps staged their rows: store the tile, then release the buffer
+      if (mbar_wait(&bar[B_STAGED], c & 1, st, ab)) {
+        const int y = (int)(x.t_begin + (int64_t)c * kC);
+        for (int h = 0; h < Cfg::HALVES; ++h)
+          tma_store_3d(map_o, stage + h * kC * 128, h * 64, y, (int)x.bh);
+        tma_store_commit();
+        tma_store_wait_read0();
+        mbar_arrive(&bar[B_VEMPTY0 + vs]);
+      }
+    }
+    __syncwarp();
+  }
+  if (r == 0) tma_store_wait0();
+}
+
+// Warps 8–15: φ(K) and the fp32 state.  Thread r: token row r for φ(K)
+// (columns of its half), feature row r for the state (64 columns of its half).
+// φ(K) runs one chunk ahead of the state update.
+template <int D, bool FULL, bool CEN>
+__device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int warp, int lane) {
+  using Cfg = TcCfg<D>;
+  using L = Layout<D, FULL, CEN>;
+  uint64_t* bar = x.bar;
+  const uint32_t tmem = x.tmem;
+  int* st = x.status;
+  volatile int* ab = x.abort_flag;
+  const int half = (warp - 8) >> 2;
+  const int r = ((warp - 8) & 3) * 32 + lane;
+  const uint32_t lane_base = (uint32_t)((warp - 8) & 3) * 32;
+  const bool srow = r < D;
+  const float a = x.a, w = x.w;
+  // centered folding: the state operand is a^{64}·S and K'' rows carry w·a^{63−s}
+  const float s_scale = CEN ? decay_pow_signed(a, 64) : 1.f;
+  const float k_scale_cen = CEN ? w * decay_pow_signed(a, 63 - r) : 0.f;
+  float S[64];
+  float zr = 0.f;
+  if (FULL && p.nseg > 1 && srow) {
+    const float* src = p.ws_state + (x.bh * p.nseg + x.g) * (int64_t)(D * D) + r * D + half * 64;
+#pragma unroll
+    for (int j = 0; j < 64; j += 4) {
+      const float4 v4 = *reinterpret_cast<const float4*>(src + j);
+      S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
+    }
+    if (half == 0) zr = p.ws_z[(x.bh * p.nseg + x.g) * (int64_t)D + r];
+  } else {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) S[j] = 0.f;
+  }
+  const uint32_t stile = x.sbase + Cfg::oS;
+  auto write_state = [&]() {
+    if (srow) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = s_scale * S[j * 8 + e];
+        sts128(stile + sw_chunk(D, r, half, j), pack8(f));
+      }
+      if (half == 0) x.zbuf[r] = s_scale * zr;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_SREADY]);
+  };
+  auto chunk_len = [&](int c) {
+    return (int)min((int64_t)kC, x.t_end - (x.t_begin + (int64_t)c * kC));
+  };
+  // φ(K) of chunk c → K'' (rows ≥ cs zeroed), written in place into the K tile
+  // except for the general full kernel, which keeps K' in place and writes K''
+  // into its own tile.
+  auto phi_k = [&](int c) -> bool {
+    const int ks = c % L::KST;
+    const int cs = chunk_len(c);
+    if (!warp_wait(&bar[B_KFULL0 + ks], (c / L::KST) & 1, st, ab)) return false;
+    if (!L::K_IN_PLACE && c >= 1 && !warp_wait(&bar[B_KPEMPTY], (c - 1) & 1, st, ab)) return false;
+    const uint32_t ktile = x.sbase + L::k_off(ks);
+    const uint32_t kp = x.sbase + L::kpp_off(ks);
+    // Rows past the end of the sequence (TMA zero-fill) must contribute
+    // nothing: their weight gs is 0, and K' (general folding) is masked with
+    // m.  φ itself is computed for every row so that no per-element branch
+    // breaks the warp into divergent paths.
+    const bool live = r < cs;
+    const float m = live ? 1.f : 0.f;
+    const float gs = live ? (CEN ? k_scale_cen : x.pw[max(cs - 1 - r, 0)]) : 0.f;
+    uint8_t* kt = x.sm + L::k_off(ks);
+    uint8_t* kpp = x.sm + L::kpp_off(ks);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t off = sw_chunk(kC, r, half, j);
+      float f[8], f2[8];
+      unpack8(*reinterpret_cast<const uint4*>(kt + off), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        f[e] = elu1_fast(f[e]);
+        f2[e] = gs * f[e];
+        if (!L::K_IN_PLACE) f[e] *= m;
+      }
+      if (!L::K_IN_PLACE) *reinterpret_cast<uint4*>(kt + off) = pack8(f);
+      *reinterpret_cast<uint4*>(kpp + off) = pack8(f2);
+    }
+    (void)ktile;
+    (void)kp;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_KREADY0 + ks]);
+    return true;
+  };
+
+  if (FULL) write_state();
+  bool ok = x.nchunks > 0 && phi_k(0);
+  for (int c = 0; ok && c < x.nchunks; ++c) {
+    if (c + 1 < x.nchunks && !phi_k(c + 1)) break;
+    // ---- state update: S ← a^{cs} S + (a^{cs−64}) ΔS, z likewise
+    const int cs = chunk_len(c);
+    if (!warp_wait(&bar[B_DSFULL], c & 1, st, ab)) break;
+    tc_fence_after();
+    const float acs = decay_pow(a, cs);
+    const float dscale = CEN ? decay_pow_signed(a, cs - 64) : 1.f;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t dv[32];
+      tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TD + half * 64 + hh * 32), dv);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        S[hh * 32 + j] = acs * S[hh * 32 + j] + dscale * __uint_as_float(dv[j]);
+    }
+    uint32_t dz = 0;
+    tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TZ), dz);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_DSEMPTY]);
+    zr = acs * zr + dscale * __uint_as_float(dz);
+    if (FULL) {
+      if (!warp_wait(&bar[B_SEMPTY], c & 1, st, ab)) break;
+      write_state();
+    }
+  }
+  // ---- hand the state on
+  if (srow && !*ab) {
+    float* dS = nullptr;
+    float* dz = nullptr;
+    if (!FULL) {
+      dS = p.ws_state + (x.bh * p.nseg + x.g) * (int64_t)(D * D);
+      dz = p.ws_z + (x.bh * p.nseg + x.g) * (int64_t)D;
+    } else if (p.fin_state) {
+      dS = p.fin_state + x.bh * (int64_t)(D * D);
+      dz = p.fin_z + x.bh * (int64_t)D;
+    }
+    if (dS) {
+#pragma unroll
+      for (int j = 0; j < 64; j += 4)
+        *reinterpret_cast<float4*>(dS + r * D + half * 64 + j) =
+            make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+      if (half == 0) dz[r] = zr;
+    }
+  }
+}
+
+template <int D, bool FULL, bool CEN>
+__device__ __forceinline__ void run_roles(const Ctx& x, const TcParams& p, const CUtensorMap* mq,
+                                          const CUtensorMap* mk, const CUtensorMap* mv,
+                                          const CUtensorMap* mo, int warp, int lane) {
+  using Cfg = TcCfg<D>;
+  if (warp == 0) {
+    if (lane == 0) role_producer<D, FULL, CEN>(x, mq, mk, mv);
+  } else if (warp == 1) {
+    if (lane == 0) role_mma<D, FULL, CEN>(x);
+  } else if (warp >= 4 && warp < 8) {
+    if (FULL) role_rows<D, CEN>(x, mo, warp, lane);
+  } else if (warp >= 8 && warp < 8 + 4 * Cfg::HALVES) {
+    role_state<D, FULL, CEN>(x, p, warp, lane);
+  }
+}
+
 template <int D, bool FULL>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -136,34 +672,39 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   using Cfg = TcCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
-  uint8_t* sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
-  const uint32_t sbase = smem_u32(sm);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Cfg::oBAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Cfg::oMISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Cfg::oMISC + 4);
-  float* zbuf = reinterpret_cast<float*>(sm + Cfg::oZ);
-  float* pw = reinterpret_cast<float*>(sm + Cfg::oPW);
+  Ctx x;
+  x.sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+  x.sbase = smem_u32(x.sm);
+  x.bar = reinterpret_cast<uint64_t*>(x.sm + Cfg::oBAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x.sm + Cfg::oMISC);
+  x.abort_flag = reinterpret_cast<volatile int*>(x.sm + Cfg::oMISC + 4);
+  x.zbuf = reinterpret_cast<float*>(x.sm + Cfg::oZ);
+  x.pw = reinterpret_cast<float*>(x.sm + Cfg::oPW);
+  x.status = p.status;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int g = blockIdx.x;
-  const int64_t bh = blockIdx.y;
-  const int64_t t_begin = (int64_t)g * p.seg_len;
-  const int64_t t_end = min(p.n, t_begin + p.seg_len);
-  const int nchunks = (int)((t_end - t_begin + kC - 1) / kC);
-  const float a = p.decay ? p.decay[bh % p.H] : 1.f;
-  const float w = new_token_weight(a);
+  x.g = blockIdx.x;
+  x.bh = blockIdx.y;
+  x.t_begin = (int64_t)x.g * p.seg_len;
+  x.t_end = min(p.n, x.t_begin + p.seg_len);
+  x.nchunks = (int)((x.t_end - x.t_begin + kC - 1) / kC);
+  x.a = p.decay ? p.decay[x.bh % p.H] : 1.f;
+  x.w = new_token_weight(x.a);
+  const bool cen = (x.a == 1.f) || (x.a >= kCenteredMinDecay);
 
   if (tid == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_QREADY || i == B_PREADY || i == B_NUMEMPTY || i == B_STAGED) cnt = 4;  // WG1 warps
-      if (i == B_KREADY) cnt = 4 * Cfg::HALVES;                                // φK warps
-      if (i == B_SREADY || i == B_DSEMPTY) cnt = 4 * Cfg::HALVES;              // state warps
-      mbar_init(&bar[i], cnt);
+      if (i == B_QREADY || i == B_PREADY || i == B_NUMEMPTY || i == B_STAGED) cnt = 4;
+      if ((i >= B_KREADY0 && i <= B_KREADY2) || i == B_SREADY || i == B_DSEMPTY)
+        cnt = 4 * Cfg::HALVES;
+      // centered: raw Q tiles are released by the φ(Q) warps
+      if ((i == B_QEMPTY0 || i == B_QEMPTY1) && cen) cnt = 4;
+      mbar_init(&x.bar[i], cnt);
     }
-    *abort_flag = 0;
+    *x.abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -171,12 +712,12 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     tmem_relinquish();
   }
   if (warp == 2) {
-    uint32_t* ones = reinterpret_cast<uint32_t*>(sm + Cfg::oONES);
+    uint32_t* ones = reinterpret_cast<uint32_t*>(x.sm + Cfg::oONES);
     for (int i = lane; i < 128; i += 32) ones[i] = 0x3F803F80u;  // bf16 1.0 pairs
     fence_proxy_async_smem();
   }
   if (warp == 3) {
-    for (int k = lane; k < kC; k += 32) pw[k] = w * decay_pow(a, k);  // w·a^k
+    for (int k = lane; k < kC; k += 32) x.pw[k] = x.w * decay_pow(x.a, k);  // w·a^k
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_k);
@@ -189,359 +730,16 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  int* status = p.status;
+  x.tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int issued_q = -1, issued_kv = -1;
-      for (int c = 0; c < nchunks && !*abort_flag; ++c) {
-        const int st = c & 1;
-        const int y = (int)(t_begin + (int64_t)c * kC);
-        if (c >= 2 && !mbar_wait(&bar[B_KEMPTY0 + st], ((c - 2) >> 1) & 1, status, abort_flag)) break;
-        mbar_arrive_expect_tx(&bar[B_KFULL0 + st], Cfg::TILE);
-        for (int h = 0; h < Cfg::HALVES; ++h)
-          tma_load_3d(sm + (st ? Cfg::oK1 : Cfg::oK0) + h * kC * 128, &map_k, &bar[B_KFULL0 + st],
-                      h * 64, y, (int)bh);
-        if (c >= 2 && !mbar_wait(&bar[B_VEMPTY0 + st], ((c - 2) >> 1) & 1, status, abort_flag)) break;
-        mbar_arrive_expect_tx(&bar[B_VFULL0 + st], Cfg::TILE);
-        for (int h = 0; h < Cfg::HALVES; ++h)
-          tma_load_3d(sm + (st ? Cfg::oV1 : Cfg::oV0) + h * kC * 128, &map_v, &bar[B_VFULL0 + st],
-                      h * 64, y, (int)bh);
-        issued_kv = c;
-        if (FULL) {
-          if (c >= 1 && !mbar_wait(&bar[B_QEMPTY], (c - 1) & 1, status, abort_flag)) break;
-          mbar_arrive_expect_tx(&bar[B_QFULL], Cfg::TILE);
-          for (int h = 0; h < Cfg::HALVES; ++h)
-            tma_load_3d(sm + Cfg::oQ + h * kC * 128, &map_q, &bar[B_QFULL], h * 64, y, (int)bh);
-          issued_q = c;
-        }
-      }
-      if (*abort_flag) {
-        // drain the loads still in flight before the CTA's shared memory goes away
-        for (int c = max(0, issued_kv - 1); c <= issued_kv; ++c) {
-          mbar_wait_drain(&bar[B_KFULL0 + (c & 1)], (c >> 1) & 1);
-          mbar_wait_drain(&bar[B_VFULL0 + (c & 1)], (c >> 1) & 1);
-        }
-        if (issued_q >= 0) mbar_wait_drain(&bar[B_QFULL], issued_q & 1);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t sQ = sbase + Cfg::oQ, sKP = sbase + Cfg::oKP, sS = sbase + Cfg::oS;
-      const uint32_t sONES = sbase + Cfg::oONES;
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);   // scores
-      constexpr uint32_t idD = idesc_bf16_f32(128, D, true, true);       // ΔS = K''ᵀ V
-      constexpr uint32_t idZ = idesc_bf16_f32(128, 16, true, false);     // Δz = K''ᵀ 1
-      constexpr uint32_t idN = idesc_bf16_f32(128, D, false, true);      // num (+)= A·{S,V}
-      constexpr uint32_t idR = idesc_bf16_f32(128, 16, false, false);    // Σ_s P = P·1
-      constexpr int KD = D / 16;                                         // K-steps over D'
-      const uint32_t lbo_kp = (D == 128) ? 64 * 128 * 2 : 0;             // M blocks of K''ᵀ
-      for (int c = 0; c < nchunks; ++c) {
-        const int st = c & 1;
-        const uint32_t sK = sbase + (st ? Cfg::oK1 : Cfg::oK0);
-        const uint32_t sV = sbase + (st ? Cfg::oV1 : Cfg::oV0);
-        if (FULL) {
-          // scores = Q' K'ᵀ
-          if (!mbar_wait(&bar[B_QREADY], c & 1, status, abort_flag)) break;
-          if (!mbar_wait(&bar[B_KREADY], c & 1, status, abort_flag)) break;
-          if (c >= 1 && !mbar_wait(&bar[B_NUMFULL], (c - 1) & 1, status, abort_flag)) break;
-          tc_fence_after();
-          for (int k = 0; k < KD; ++k) {
-            const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
-            mma_ss(tmem + Cfg::TS, smem_desc(sQ + off, 16, 1024, kSwizzle128B),
-                   smem_desc(sK + off, 16, 1024, kSwizzle128B), idS, k > 0);
-          }
-          mma_commit(&bar[B_SCORES]);
-          mma_commit(&bar[B_QEMPTY]);
-        } else {
-          if (!mbar_wait(&bar[B_KREADY], c & 1, status, abort_flag)) break;
-        }
-        mma_commit(&bar[B_KEMPTY0 + st]);
-        // ΔS = K''ᵀ V ; Δz = K''ᵀ 1
-        if (!mbar_wait(&bar[B_VFULL0 + st], (c >> 1) & 1, status, abort_flag)) break;
-        if (c >= 1 && !mbar_wait(&bar[B_DSEMPTY], (c - 1) & 1, status, abort_flag)) break;
-        tc_fence_after();
-        for (int k = 0; k < kC / 16; ++k) {
-          const uint64_t ad = smem_desc(sKP + k * 2048, lbo_kp, 1024, kSwizzle128B);
-          mma_ss(tmem + Cfg::TD, ad, smem_desc(sV + k * 2048, kC * 128, 1024, kSwizzle128B), idD,
-                 k > 0);
-          mma_ss(tmem + Cfg::TZ, ad, smem_desc(sONES, 128, 256, kSwizzleNone), idZ, k > 0);
-        }
-        mma_commit(&bar[B_DSFULL]);
-        mma_commit(&bar[B_KPEMPTY]);
-        if (!FULL) {
-          mma_commit(&bar[B_VEMPTY0 + st]);
-          continue;
-        }
-        // num = Q'' S
-        if (!mbar_wait(&bar[B_SREADY], c & 1, status, abort_flag)) break;
-        if (c >= 1 && !mbar_wait(&bar[B_NUMEMPTY], (c - 1) & 1, status, abort_flag)) break;
-        tc_fence_after();
-        for (int k = 0; k < KD; ++k)
-          mma_ts(tmem + Cfg::TN, tmem + Cfg::TQ + k * 8,
-                 smem_desc(sS + k * 2048, D * 128, 1024, kSwizzle128B), idN, k > 0);
-        mma_commit(&bar[B_SEMPTY]);
-        mma_commit(&bar[B_QPEMPTY]);
-        // num += P V
-        if (!mbar_wait(&bar[B_PREADY], c & 1, status, abort_flag)) break;
-        tc_fence_after();
-        for (int k = 0; k < kC / 16; ++k) {
-          mma_ts(tmem + Cfg::TN, tmem + Cfg::TS + k * 8,
-                 smem_desc(sV + k * 2048, kC * 128, 1024, kSwizzle128B), idN, 1);
-          mma_ts(tmem + Cfg::TR, tmem + Cfg::TS + k * 8, smem_desc(sONES, 128, 256, kSwizzleNone),
-                 idR, k > 0);
-        }
-        mma_commit(&bar[B_NUMFULL]);
-      }
-      // every issued MMA must finish before TMEM is released
-      mma_commit(&bar[B_MMADONE]);
-      mbar_wait_drain(&bar[B_MMADONE], 0);
-    }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ WG1: φ(Q), P, epilogue
-    if (FULL) {
-      const int r = tid - 128;                       // row / TMEM lane
-      const uint32_t lane_base = (uint32_t)(warp - 4) * 32;
-      const float a_row = decay_pow(a, r + 1);       // a^{r+1}
-      const float* pwr = pw;
-      for (int c = 0; c < nchunks; ++c) {
-        const int st = c & 1;
-        // ---- φ(Q): Q' in place (smem), Q'' = a^{r+1} Q' into TMEM, q''·z
-        if (!warp_wait(&bar[B_QFULL], c & 1, status, abort_flag)) break;
-        if (c >= 1 && !warp_wait(&bar[B_QPEMPTY], (c - 1) & 1, status, abort_flag)) break;
-        if (!warp_wait(&bar[B_SREADY], c & 1, status, abort_flag)) break;
-        const float4* zc4 = reinterpret_cast<const float4*>(zbuf);
-        float qz = 0.f;
-        uint8_t* qtile = sm + Cfg::oQ;
-#pragma unroll
-        for (int h = 0; h < Cfg::HALVES; ++h) {
-          uint32_t packed[32];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint4* ptr = reinterpret_cast<uint4*>(qtile + sw_chunk(kC, r, h, j));
-            float f[8];
-            unpack8(*ptr, f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = elu1_fast(f[e]);
-            *ptr = pack8(f);
-            const float4 z0 = zc4[(h * 64 + j * 8) / 4];
-            const float4 z1 = zc4[(h * 64 + j * 8) / 4 + 1];
-            const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              const uint32_t pr = pack_bf16x2(a_row * f[e], a_row * f[e + 1]);
-              packed[j * 4 + e / 2] = pr;
-              qz += bf16lo_to_f32(pr) * zz[e] + bf16hi_to_f32(pr) * zz[e + 1];
-            }
-          }
-          tmem_st32(tmem_addr(tmem, lane_base, Cfg::TQ + h * 32), packed);
-        }
-        tmem_st_wait();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[B_QREADY]);
-
-        // ---- P = mask ⊙ w a^{t−s} ⊙ scores  (bf16 into TMEM columns 0..63)
-        if (!warp_wait(&bar[B_SCORES], c & 1, status, abort_flag)) break;
-        tc_fence_after();
-        // 32-column blocks b of row r (warp quarter wq = rows 32wq..32wq+31):
-        // b > wq lies above the diagonal for the whole warp (zeros, scores not
-        // read), b < wq below it (no mask), b == wq straddles it.
-        const int wq = warp - 4;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          uint32_t pk[16];
-          if (b > wq) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) pk[j] = 0u;
-          } else {
-            uint32_t sc[32];
-            tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TS + b * 32), sc);
-            tmem_ld_wait();
-            const float* wp = pwr + (r - b * 32);      // wp[-j] = w·a^{r-(32b+j)}
-            if (b < wq) {
-#pragma unroll
-              for (int j = 0; j < 32; j += 2)
-                pk[j / 2] = pack_bf16x2(wp[-j] * __uint_as_float(sc[j]),
-                                        wp[-j - 1] * __uint_as_float(sc[j + 1]));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; j += 2) {
-                const int s0 = b * 32 + j;
-                const float p0 = (s0 <= r) ? wp[-j] * __uint_as_float(sc[j]) : 0.f;
-                const float p1 = (s0 + 1 <= r) ? wp[-j - 1] * __uint_as_float(sc[j + 1]) : 0.f;
-                pk[j / 2] = pack_bf16x2(p0, p1);
-              }
-            }
-          }
-          tmem_st16(tmem_addr(tmem, lane_base, Cfg::TS + b * 16), pk);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[B_PREADY]);
-
-        // ---- epilogue: o = num / den → bf16 → staging (V buffer) → TMA store
-        if (!warp_wait(&bar[B_NUMFULL], c & 1, status, abort_flag)) break;
-        tc_fence_after();
-        uint32_t rs = 0;
-        tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TR), rs);
-        tmem_ld_wait();
-        const float inv_den = 1.f / (__uint_as_float(rs) + qz);
-        uint8_t* stage = sm + (st ? Cfg::oV1 : Cfg::oV0);
-#pragma unroll
-        for (int j0 = 0; j0 < D; j0 += 32) {
-          uint32_t nv[32];
-          tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TN + j0), nv);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(nv[q8 * 8 + e]) * inv_den;
-            const int col = j0 + q8 * 8;
-            *reinterpret_cast<uint4*>(stage + sw_chunk(kC, r, col >> 6, (col & 63) >> 3)) = pack8(f);
-          }
-        }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bar[B_NUMEMPTY]);
-          mbar_arrive(&bar[B_STAGED]);
-        }
-        if (r == 0) {
-          // all four warps staged their rows: store the tile, then release the buffer
-          if (mbar_wait(&bar[B_STAGED], c & 1, status, abort_flag)) {
-            const int y = (int)(t_begin + (int64_t)c * kC);
-            for (int h = 0; h < Cfg::HALVES; ++h)
-              tma_store_3d(&map_o, stage + h * kC * 128, h * 64, y, (int)bh);
-            tma_store_commit();
-            tma_store_wait_read0();
-            mbar_arrive(&bar[B_VEMPTY0 + st]);
-          }
-        }
-        __syncwarp();
-      }
-      if (r == 0) tma_store_wait0();
-    }
-  } else if (warp >= 8 && warp < 8 + 4 * Cfg::HALVES) {
-    // ------------------------------------------------------------ WG2/WG3: φ(K), state
-    const int half = (warp - 8) >> 2;              // which 64 state columns
-    const int r = tid - 128 * (2 + half);          // token row for φK; feature row for S
-    const uint32_t lane_base = (uint32_t)((warp - 8) & 3) * 32;
-    float S[64];
-    float zr = 0.f;
-    const bool srow = r < D;                       // this thread owns state row r
-    if (p.nseg > 1) {
-      const float* src = p.ws_state + (bh * p.nseg + g) * (int64_t)(D * D);
-#pragma unroll
-      for (int j = 0; j < 64; ++j) S[j] = (FULL && srow) ? src[r * D + half * 64 + j] : 0.f;
-      if (FULL && srow && half == 0) zr = p.ws_z[(bh * p.nseg + g) * (int64_t)D + r];
-    } else {
-#pragma unroll
-      for (int j = 0; j < 64; ++j) S[j] = 0.f;
-    }
-    uint8_t* stile = sm + Cfg::oS;
-    auto write_state = [&]() {
-      if (srow) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = S[j * 8 + e];
-          *reinterpret_cast<uint4*>(stile + sw_chunk(D, r, half, j)) = pack8(f);
-        }
-        if (half == 0) zbuf[r] = zr;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_SREADY]);
-    };
-    write_state();
-    for (int c = 0; c < nchunks; ++c) {
-      const int st = c & 1;
-      const int cs = (int)min((int64_t)kC, t_end - (t_begin + (int64_t)c * kC));
-      // ---- φ(K): K' in place, K'' = w a^{cs−1−s} K' (rows ≥ cs zeroed)
-      if (!warp_wait(&bar[B_KFULL0 + st], (c >> 1) & 1, status, abort_flag)) break;
-      if (c >= 1 && !warp_wait(&bar[B_KPEMPTY], (c - 1) & 1, status, abort_flag)) break;
-      {
-        uint8_t* ktile = sm + (st ? Cfg::oK1 : Cfg::oK0);
-        uint8_t* kp = sm + Cfg::oKP;
-        const bool live = r < cs;
-        const float gs = live ? pw[cs - 1 - r] : 0.f;   // w·a^{cs−1−s}
-        const int h = half;                          // D = 128: each warpgroup one half
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t off = sw_chunk(kC, r, h, j);
-          uint4* ptr = reinterpret_cast<uint4*>(ktile + off);
-          float f[8], f2[8];
-          unpack8(*ptr, f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            f[e] = live ? elu1_fast(f[e]) : 0.f;
-            f2[e] = gs * f[e];
-          }
-          if (FULL) *ptr = pack8(f);
-          *reinterpret_cast<uint4*>(kp + off) = pack8(f2);
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_KREADY]);
-      // ---- state update: S ← a^{cs} S + ΔS, z ← a^{cs} z + Δz
-      if (!warp_wait(&bar[B_DSFULL], c & 1, status, abort_flag)) break;
-      tc_fence_after();
-      const float acs = decay_pow(a, cs);
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t dv[32];
-        tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TD + half * 64 + hh * 32), dv);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) S[hh * 32 + j] = acs * S[hh * 32 + j] + __uint_as_float(dv[j]);
-      }
-      uint32_t dz = 0;
-      tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TZ), dz);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_DSEMPTY]);
-      zr = acs * zr + __uint_as_float(dz);
-      if (FULL) {
-        if (!warp_wait(&bar[B_SEMPTY], c & 1, status, abort_flag)) break;
-        write_state();
-      }
-    }
-    // ---- hand the state on
-    if (srow && !*abort_flag) {
-      float* dS = nullptr;
-      float* dz = nullptr;
-      if (!FULL) {
-        dS = p.ws_state + (bh * p.nseg + g) * (int64_t)(D * D);
-        dz = p.ws_z + (bh * p.nseg + g) * (int64_t)D;
-      } else if (p.fin_state) {
-        dS = p.fin_state + bh * (int64_t)(D * D);
-        dz = p.fin_z + bh * (int64_t)D;
-      }
-      if (dS) {
-#pragma unroll
-        for (int j = 0; j < 64; j += 4)
-          *reinterpret_cast<float4*>(dS + r * D + half * 64 + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-        if (half == 0) dz[r] = zr;
-      }
-    }
-  }
+  if (cen) run_roles<D, FULL, true>(x, p, &map_q, &map_k, &map_v, &map_o, warp, lane);
+  else run_roles<D, FULL, false>(x, p, &map_q, &map_k, &map_v, &map_o, warp, lane);
 
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    tmem_dealloc(x.tmem, Cfg::TMEM_COLS);
   }
 }
 
