@@ -69,11 +69,12 @@ struct TcCfg {
   static constexpr int oV0 = oKP + TILE;
   static constexpr int oV1 = oV0 + TILE;
   static constexpr int oS = oV1 + TILE;          // state operand, bf16 [D' × D]
-  static constexpr int oONES = oS + STILE;       // 16×16 bf16 ones (512 B)
-  static constexpr int oZ = oONES + 512;         // normalizer operand z [D] fp32
+  static constexpr int oONES = oS + STILE;       // 8×8 bf16 ones (128 B; every core matrix aliases it)
+  static constexpr int oQZ = oONES + 128;        // q''·z per row, [128] fp32 (summed by the φ(Q) warps)
+  static constexpr int oZ = oQZ + kC * 4;        // normalizer operand z [D] fp32
   static constexpr int oPW = oZ + D * 4;         // w·a^k, k = 0..127 (general folding)
   static constexpr int oBAR = oPW + 132 * 4;     // mbarriers
-  static constexpr int NBAR = 32;
+  static constexpr int NBAR = 34;
   static constexpr int oMISC = oBAR + NBAR * 8;  // tmem slot, abort flag
   static constexpr int BYTES = oMISC + 16;
   // + alignment slack; at least half of the SM's shared memory so that one
@@ -101,7 +102,7 @@ enum {
   B_VFULL0, B_VFULL1, B_VFULL2, B_VEMPTY0, B_VEMPTY1, B_VEMPTY2,
   B_KREADY0, B_KREADY1, B_KREADY2,   // one per K stage: φ(K) may run a chunk ahead
   B_QREADY, B_KPEMPTY, B_SREADY, B_SEMPTY, B_SCORES, B_PREADY, B_NUMFULL, B_NUMEMPTY,
-  B_DSFULL, B_DSEMPTY, B_QPEMPTY, B_MMADONE, B_STAGED, B_COUNT
+  B_DSFULL, B_DSEMPTY, B_QPEMPTY, B_MMADONE, B_STAGED, B_QZREADY, B_QZEMPTY, B_COUNT
 };
 
 // Roles of the seven tiles T0, T1, T2, KP, V0, V1 (and S) per kernel mode:
@@ -185,6 +186,7 @@ struct Ctx {
   uint64_t* bar;
   volatile int* abort_flag;
   float* zbuf;
+  float* qzbuf;
   float* pw;
   uint32_t tmem;
   int* status;
@@ -259,7 +261,7 @@ __device__ __forceinline__ void role_mma(const Ctx& x) {
   constexpr uint32_t idR = idesc_bf16_f32(128, 16, false, false);    // Σ_s P = P·1
   constexpr int KD = D / 16;                                         // K-steps over D'
   const uint32_t lbo_kp = (D == 128) ? kC * 128 : 0;                 // M blocks of K''ᵀ
-  const uint64_t ones = smem_desc(sONES, 128, 256, kSwizzleNone);
+  const uint64_t ones = smem_desc(sONES, 0, 0, kSwizzleNone);   // all core matrices alias
   int* st = x.status;
   volatile int* ab = x.abort_flag;
   for (int c = 0; c < x.nchunks; ++c) {
@@ -296,12 +298,12 @@ __device__ __forceinline__ void role_mma(const Ctx& x) {
     }
     // ΔS = K''ᵀ V ; Δz = K''ᵀ 1
     if (!mbar_wait(&bar[B_VFULL0 + vs], (c / L::VST) & 1, st, ab)) break;
-    if (c >= 1 && !mbar_wait(&bar[B_DSEMPTY], (c - 1) & 1, st, ab)) break;
+    if (!mbar_wait(&bar[B_DSEMPTY], c & 1, st, ab)) break;   // pre-scaled state in TMEM
     tc_fence_after();
     for (int k = 0; k < kC / 16; ++k) {
       const uint64_t ad = smem_desc(sKP + k * 2048, lbo_kp, 1024, kSwizzle128B);
-      mma_ss(tmem + Cfg::TD, ad, smem_desc(sV + k * 2048, kC * 128, 1024, kSwizzle128B), idD, k > 0);
-      mma_ss(tmem + Cfg::TZ, ad, ones, idZ, k > 0);
+      mma_ss(tmem + Cfg::TD, ad, smem_desc(sV + k * 2048, kC * 128, 1024, kSwizzle128B), idD, 1);
+      mma_ss(tmem + Cfg::TZ, ad, ones, idZ, 1);
     }
     mma_commit(&bar[B_DSFULL]);
     if (L::K_IN_PLACE) mma_commit(&bar[B_KEMPTY0 + ks]);   // K'' tile free for the next load
@@ -334,9 +336,64 @@ __device__ __forceinline__ void role_mma(const Ctx& x) {
   mbar_wait_drain(&bar[B_MMADONE], 0);
 }
 
-// Warps 4–7: φ(Q), masked P, epilogue.  Thread r owns row / TMEM lane r.
-// Order per chunk c: P(c), then φ(Q) of chunk c+1 (so the next scores MMA can
-// start as soon as P·V of chunk c is done), then the epilogue of chunk c.
+// φ(Q) of chunk c for the 64 columns of half h of row r (TMEM lane r):
+// Q'' = a_row·φ(q) into TMEM, the partial q''·z over those columns; the
+// general folding also writes Q' back in place for the scores MMA.  Signals
+// q_ready (the scores MMA may start), then adds the partial into the per-row
+// q''·z buffer once the epilogue of chunk c−1 has read it, and signals
+// qz_ready.  Returns false if a wait gave up.
+template <int D, bool CEN>
+__device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, int lane,
+                                           uint32_t lane_base, float a_row) {
+  using Cfg = TcCfg<D>;
+  using L = Layout<D, true, CEN>;
+  uint64_t* bar = x.bar;
+  int* st = x.status;
+  volatile int* ab = x.abort_flag;
+  const int qs = c % L::QST;
+  if (!warp_wait(&bar[B_QFULL0 + qs], (c / L::QST) & 1, st, ab)) return false;
+  if (c >= 1 && !warp_wait(&bar[B_QPEMPTY], (c - 1) & 1, st, ab)) return false;
+  if (!warp_wait(&bar[B_SREADY], c & 1, st, ab)) return false;
+  const float4* zc4 = reinterpret_cast<const float4*>(x.zbuf);
+  uint8_t* qt = x.sm + L::q_off(qs);
+  float qz = 0.f;
+  uint32_t packed[32];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float f[8];
+    uint4* qp = reinterpret_cast<uint4*>(qt + sw_chunk(kC, r, h, j));
+    unpack8(*qp, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = elu1_fast(f[e]);
+    if (!CEN) *qp = pack8(f);
+    const float4 z0 = zc4[(h * 64 + j * 8) / 4];
+    const float4 z1 = zc4[(h * 64 + j * 8) / 4 + 1];
+    const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const uint32_t pr = pack_bf16x2(a_row * f[e], a_row * f[e + 1]);
+      packed[j * 4 + e / 2] = pr;
+      qz += bf16lo_to_f32(pr) * zz[e] + bf16hi_to_f32(pr) * zz[e + 1];
+    }
+  }
+  tmem_st32(tmem_addr(x.tmem, lane_base, Cfg::TQ + h * 32), packed);
+  tmem_st_wait();
+  if (!CEN) fence_proxy_async_smem();            // Q' is read by the tensor core
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive(&bar[B_QREADY]);
+    if (CEN) mbar_arrive(&bar[B_QEMPTY0 + qs]);  // raw Q tile no longer needed
+  }
+  // publish the partial q''·z of this row
+  if (c >= 1 && !warp_wait(&bar[B_QZEMPTY], (c - 1) & 1, st, ab)) return false;
+  atomicAdd(&x.qzbuf[r], qz);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bar[B_QZREADY]);
+  return true;
+}
+
+// Warps 4–7: masked P and the epilogue.  Thread r owns row / TMEM lane r.
 template <int D, bool CEN>
 __device__ __forceinline__ void role_rows(const Ctx& x, const CUtensorMap* map_o, int warp,
                                           int lane) {
@@ -349,57 +406,8 @@ __device__ __forceinline__ void role_rows(const Ctx& x, const CUtensorMap* map_o
   const int r = (warp - 4) * 32 + lane;
   const int wq = warp - 4;                        // lane quarter
   const uint32_t lane_base = (uint32_t)wq * 32;
-  const float a_row = CEN ? decay_pow_signed(x.a, r - 63) : decay_pow(x.a, r + 1);
-
-  // φ(Q) of chunk c: Q'' = a_row·φ(q) into TMEM and q''·z; the general folding
-  // also writes Q' back in place for the scores MMA.
-  auto phi_q = [&](int c, float& qz) -> bool {
-    const int qs = c % L::QST;
-    if (!warp_wait(&bar[B_QFULL0 + qs], (c / L::QST) & 1, st, ab)) return false;
-    if (c >= 1 && !warp_wait(&bar[B_QPEMPTY], (c - 1) & 1, st, ab)) return false;
-    if (!warp_wait(&bar[B_SREADY], c & 1, st, ab)) return false;
-    const float4* zc4 = reinterpret_cast<const float4*>(x.zbuf);
-    qz = 0.f;
-#pragma unroll
-    for (int h = 0; h < Cfg::HALVES; ++h) {
-      uint8_t* qt = x.sm + L::q_off(qs);
-      uint32_t packed[32];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float f[8];
-        uint4* qp = reinterpret_cast<uint4*>(qt + sw_chunk(kC, r, h, j));
-        unpack8(*qp, f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = elu1_fast(f[e]);
-        if (!CEN) *qp = pack8(f);
-        const float4 z0 = zc4[(h * 64 + j * 8) / 4];
-        const float4 z1 = zc4[(h * 64 + j * 8) / 4 + 1];
-        const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const uint32_t pr = pack_bf16x2(a_row * f[e], a_row * f[e + 1]);
-          packed[j * 4 + e / 2] = pr;
-          qz += bf16lo_to_f32(pr) * zz[e] + bf16hi_to_f32(pr) * zz[e + 1];
-        }
-      }
-      tmem_st32(tmem_addr(tmem, lane_base, Cfg::TQ + h * 32), packed);
-    }
-    tmem_st_wait();
-    if (!CEN) fence_proxy_async_smem();            // Q' is read by the tensor core
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&bar[B_QREADY]);
-      if (CEN) mbar_arrive(&bar[B_QEMPTY0 + qs]);  // raw Q tile no longer needed
-    }
-    return true;
-  };
-
-  float qz_next = 0.f;
-  bool ok = x.nchunks > 0 && phi_q(0, qz_next);
-  for (int c = 0; ok && c < x.nchunks; ++c) {
+  for (int c = 0; c < x.nchunks; ++c) {
     const int vs = c % L::VST;
-    const float qz = qz_next;
     // ---- P: causal mask (and, general folding, the decay w·a^{t−s})
     if (!warp_wait(&bar[B_SCORES], c & 1, st, ab)) break;
     tc_fence_after();
@@ -454,12 +462,14 @@ __device__ __forceinline__ void role_rows(const Ctx& x, const CUtensorMap* map_o
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[B_PREADY]);
 
-    // ---- φ(Q) of the next chunk
-    if (c + 1 < x.nchunks && !phi_q(c + 1, qz_next)) break;
-
     // ---- epilogue: o = num / den → bf16 → staging (V tile of this chunk) → TMA store
     if (!warp_wait(&bar[B_NUMFULL], c & 1, st, ab)) break;
     tc_fence_after();
+    if (!warp_wait(&bar[B_QZREADY], c & 1, st, ab)) break;
+    const float qz = x.qzbuf[r];
+    x.qzbuf[r] = 0.f;                               // the φ(Q) warps accumulate into it
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_QZEMPTY]);
     uint32_t rs = 0;
     tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TR), rs);
     tmem_ld_wait();
@@ -503,9 +513,17 @@ __device__ __forceinline__ void role_rows(const Ctx& x, const CUtensorMap* map_o
   if (r == 0) tma_store_wait0();
 }
 
-// Warps 8–15: φ(K) and the fp32 state.  Thread r: token row r for φ(K)
-// (columns of its half), feature row r for the state (64 columns of its half).
-// φ(K) runs one chunk ahead of the state update.
+// Warps 8–15: φ(K), the fp32 state, and (D = 128) φ(Q).  Thread r: token row r
+// for φ(K) and φ(Q) (the columns of its half), feature row r / TMEM lane r
+// for the state (the 64 state columns of its half).
+//
+// The fp32 state lives in TMEM (columns TD, and TZ for z), pre-scaled so that
+// the state MMA accumulates onto it: before the MMA of chunk c it holds β·S_c,
+// and the bf16 operand tile of the inter-chunk MMA holds α·S:
+//   centered:  TMEM = a^{64}·S_c, so after the MMA v = a^{64}S_c + ΔS'' and
+//              a^{64}·S_{c+1} = a^{cs}·v feeds both TMEM and the tile;
+//   general:   TMEM = a^{cs}·S_c, so after the MMA v = S_{c+1}; the tile gets
+//              S_{c+1} and TMEM a^{cs'}·S_{c+1} for the next chunk (cs').
 template <int D, bool FULL, bool CEN>
 __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int warp, int lane) {
   using Cfg = TcCfg<D>;
@@ -519,52 +537,74 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   const uint32_t lane_base = (uint32_t)((warp - 8) & 3) * 32;
   const bool srow = r < D;
   const float a = x.a, w = x.w;
-  // centered folding: the state operand is a^{64}·S and K'' rows carry w·a^{63−s}
-  const float s_scale = CEN ? decay_pow_signed(a, 64) : 1.f;
   const float k_scale_cen = CEN ? w * decay_pow_signed(a, 63 - r) : 0.f;
-  float S[64];
-  float zr = 0.f;
-  if (FULL && p.nseg > 1 && srow) {
-    const float* src = p.ws_state + (x.bh * p.nseg + x.g) * (int64_t)(D * D) + r * D + half * 64;
-#pragma unroll
-    for (int j = 0; j < 64; j += 4) {
-      const float4 v4 = *reinterpret_cast<const float4*>(src + j);
-      S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
-    }
-    if (half == 0) zr = p.ws_z[(x.bh * p.nseg + x.g) * (int64_t)D + r];
-  } else {
-#pragma unroll
-    for (int j = 0; j < 64; ++j) S[j] = 0.f;
-  }
+  const uint32_t td = tmem_addr(tmem, lane_base, Cfg::TD + half * 64);
+  const uint32_t tz = tmem_addr(tmem, lane_base, Cfg::TZ);
   const uint32_t stile = x.sbase + Cfg::oS;
-  auto write_state = [&]() {
-    if (srow) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float f[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = s_scale * S[j * 8 + e];
-        sts128(stile + sw_chunk(D, r, half, j), pack8(f));
-      }
-      if (half == 0) x.zbuf[r] = s_scale * zr;
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bar[B_SREADY]);
-  };
   auto chunk_len = [&](int c) {
     return (int)min((int64_t)kC, x.t_end - (x.t_begin + (int64_t)c * kC));
   };
-  // φ(K) of chunk c → K'' (rows ≥ cs zeroed), written in place into the K tile
-  // except for the general full kernel, which keeps K' in place and writes K''
-  // into its own tile.
+  // final-state destination (state-only pass: the segment aggregate)
+  float* out_S = nullptr;
+  float* out_z = nullptr;
+  if (!FULL) {
+    out_S = p.ws_state + (x.bh * p.nseg + x.g) * (int64_t)(D * D);
+    out_z = p.ws_z + (x.bh * p.nseg + x.g) * (int64_t)D;
+  } else if (p.fin_state) {
+    out_S = p.fin_state + x.bh * (int64_t)(D * D);
+    out_z = p.fin_z + x.bh * (int64_t)D;
+  }
+
+  // Writes one state value v (this thread's 64 columns, in 32-column steps
+  // produced by `fetch`) as: TMEM ← β·v, tile ← α·v (full kernel), global ←
+  // γ·v (last chunk).  z is handled by the half-0 warps.
+  auto put_state = [&](auto fetch, float zv, float alpha, float beta, float gamma, bool tile,
+                       bool to_global) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float v[32];
+      fetch(hh, v);
+      if (tile && srow) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = alpha * v[q * 8 + e];
+          sts128(stile + sw_chunk(D, r, half, hh * 4 + q), pack8(f));
+        }
+      }
+      if (to_global && srow) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(out_S + r * D + half * 64 + hh * 32 + j) =
+              make_float4(gamma * v[j], gamma * v[j + 1], gamma * v[j + 2], gamma * v[j + 3]);
+      }
+      uint32_t o[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(beta * v[j]);
+      tmem_st32(td + hh * 32, o);
+    }
+    if (half == 0) {
+      uint32_t zo[1] = {__float_as_uint(beta * zv)};
+      asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tz), "r"(zo[0])
+                   : "memory");
+      if (srow && tile) x.zbuf[r] = alpha * zv;
+      if (srow && to_global) out_z[r] = gamma * zv;
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    if (tile) fence_proxy_async_smem();
+    __syncwarp();
+  };
+
+  // φ(K) of chunk c → K'' (rows ≥ cs zeroed by weight), written in place into
+  // the K tile except for the general full kernel, which keeps K' in place
+  // and writes K'' into its own tile.
   auto phi_k = [&](int c) -> bool {
     const int ks = c % L::KST;
     const int cs = chunk_len(c);
     if (!warp_wait(&bar[B_KFULL0 + ks], (c / L::KST) & 1, st, ab)) return false;
     if (!L::K_IN_PLACE && c >= 1 && !warp_wait(&bar[B_KPEMPTY], (c - 1) & 1, st, ab)) return false;
-    const uint32_t ktile = x.sbase + L::k_off(ks);
-    const uint32_t kp = x.sbase + L::kpp_off(ks);
     // Rows past the end of the sequence (TMA zero-fill) must contribute
     // nothing: their weight gs is 0, and K' (general folding) is masked with
     // m.  φ itself is computed for every row so that no per-element branch
@@ -588,63 +628,78 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
       if (!L::K_IN_PLACE) *reinterpret_cast<uint4*>(kt + off) = pack8(f);
       *reinterpret_cast<uint4*>(kpp + off) = pack8(f2);
     }
-    (void)ktile;
-    (void)kp;
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[B_KREADY0 + ks]);
     return true;
   };
 
-  if (FULL) write_state();
-  bool ok = x.nchunks > 0 && phi_k(0);
-  for (int c = 0; ok && c < x.nchunks; ++c) {
-    if (c + 1 < x.nchunks && !phi_k(c + 1)) break;
-    // ---- state update: S ← a^{cs} S + (a^{cs−64}) ΔS, z likewise
-    const int cs = chunk_len(c);
-    if (!warp_wait(&bar[B_DSFULL], c & 1, st, ab)) break;
-    tc_fence_after();
-    const float acs = decay_pow(a, cs);
-    const float dscale = CEN ? decay_pow_signed(a, cs - 64) : 1.f;
+  // ---- initial state (S_in from the segment scan, or zero)
+  {
+    const bool have_in = FULL && p.nseg > 1;
+    const float* src = have_in ? p.ws_state + (x.bh * p.nseg + x.g) * (int64_t)(D * D) +
+                                     (int64_t)(srow ? r : 0) * D + half * 64
+                               : nullptr;
+    const float zin = (have_in && srow && half == 0)
+                          ? p.ws_z[(x.bh * p.nseg + x.g) * (int64_t)D + r] : 0.f;
+    const float alpha0 = CEN ? decay_pow_signed(a, 64) : 1.f;
+    const float beta0 = CEN ? alpha0 : decay_pow(a, chunk_len(0));
+    put_state([&](int hh, float* v) {
+                if (have_in && srow) {
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      uint32_t dv[32];
-      tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TD + half * 64 + hh * 32), dv);
-      tmem_ld_wait();
+                  for (int j = 0; j < 32; j += 4) {
+                    const float4 t = *reinterpret_cast<const float4*>(src + hh * 32 + j);
+                    v[j] = t.x; v[j + 1] = t.y; v[j + 2] = t.z; v[j + 3] = t.w;
+                  }
+                } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        S[hh * 32 + j] = acs * S[hh * 32 + j] + dscale * __uint_as_float(dv[j]);
-    }
-    uint32_t dz = 0;
-    tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TZ), dz);
-    tmem_ld_wait();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bar[B_DSEMPTY]);
-    zr = acs * zr + dscale * __uint_as_float(dz);
-    if (FULL) {
-      if (!warp_wait(&bar[B_SEMPTY], c & 1, st, ab)) break;
-      write_state();
+                  for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                }
+              },
+              zin, alpha0, beta0, 1.f, FULL, false);
+    if (lane == 0) {
+      mbar_arrive(&bar[B_DSEMPTY]);                // TMEM state ready for the first MMA
+      if (FULL) mbar_arrive(&bar[B_SREADY]);       // operand tile ready
     }
   }
-  // ---- hand the state on
-  if (srow && !*ab) {
-    float* dS = nullptr;
-    float* dz = nullptr;
-    if (!FULL) {
-      dS = p.ws_state + (x.bh * p.nseg + x.g) * (int64_t)(D * D);
-      dz = p.ws_z + (x.bh * p.nseg + x.g) * (int64_t)D;
-    } else if (p.fin_state) {
-      dS = p.fin_state + x.bh * (int64_t)(D * D);
-      dz = p.fin_z + x.bh * (int64_t)D;
+
+  // D = 128: these warps also compute φ(Q) for their half of the columns
+  constexpr bool DO_Q = FULL && Cfg::HALVES == 2;
+  const float a_row = CEN ? decay_pow_signed(a, r - 63) : decay_pow(a, r + 1);
+  bool ok = x.nchunks > 0 && phi_k(0);
+  if (DO_Q && ok) ok = phi_q_half<D, CEN>(x, 0, half, r, lane, lane_base, a_row);
+  for (int c = 0; ok && c < x.nchunks; ++c) {
+    if (c + 1 < x.nchunks && !phi_k(c + 1)) break;
+    // ---- state update from the accumulated TMEM value v
+    const int cs = chunk_len(c);
+    const bool last = c + 1 == x.nchunks;
+    if (!warp_wait(&bar[B_DSFULL], c & 1, st, ab)) break;
+    if (FULL && !warp_wait(&bar[B_SEMPTY], c & 1, st, ab)) break;   // tile free
+    tc_fence_after();
+    const float acs = decay_pow(a, cs);
+    const float alpha = CEN ? acs : 1.f;
+    const float beta = CEN ? acs : (last ? 1.f : decay_pow(a, chunk_len(c + 1)));
+    const float gamma = CEN ? decay_pow_signed(a, cs - 64) : 1.f;
+    uint32_t zraw = 0;
+    if (half == 0) {
+      tmem_ld1(tz, zraw);
+      tmem_ld_wait();
     }
-    if (dS) {
+    put_state([&](int hh, float* v) {
+                uint32_t u[32];
+                tmem_ld32(td + hh * 32, u);
+                tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 64; j += 4)
-        *reinterpret_cast<float4*>(dS + r * D + half * 64 + j) =
-            make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-      if (half == 0) dz[r] = zr;
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
+              },
+              __uint_as_float(zraw), alpha, beta, gamma, FULL && !last, last && out_S != nullptr);
+    if (lane == 0) {
+      mbar_arrive(&bar[B_DSEMPTY]);
+      if (FULL && !last) mbar_arrive(&bar[B_SREADY]);
     }
+    if (DO_Q && c + 1 < x.nchunks &&
+        !phi_q_half<D, CEN>(x, c + 1, half, r, lane, lane_base, a_row))
+      break;
   }
 }
 
@@ -661,6 +716,12 @@ __device__ __forceinline__ void run_roles(const Ctx& x, const TcParams& p, const
     if (FULL) role_rows<D, CEN>(x, mo, warp, lane);
   } else if (warp >= 8 && warp < 8 + 4 * Cfg::HALVES) {
     role_state<D, FULL, CEN>(x, p, warp, lane);
+  } else if (FULL && Cfg::HALVES == 1 && warp >= 12) {
+    // D = 64: the fourth warpgroup computes φ(Q)
+    const int r = (warp - 12) * 32 + lane;
+    const float a_row = CEN ? decay_pow_signed(x.a, r - 63) : decay_pow(x.a, r + 1);
+    for (int c = 0; c < x.nchunks; ++c)
+      if (!phi_q_half<D, CEN>(x, c, 0, r, lane, (uint32_t)(warp - 12) * 32, a_row)) break;
   }
 }
 
@@ -679,6 +740,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x.sm + Cfg::oMISC);
   x.abort_flag = reinterpret_cast<volatile int*>(x.sm + Cfg::oMISC + 4);
   x.zbuf = reinterpret_cast<float*>(x.sm + Cfg::oZ);
+  x.qzbuf = reinterpret_cast<float*>(x.sm + Cfg::oQZ);
   x.pw = reinterpret_cast<float*>(x.sm + Cfg::oPW);
   x.status = p.status;
 
@@ -697,11 +759,13 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   if (tid == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_QREADY || i == B_PREADY || i == B_NUMEMPTY || i == B_STAGED) cnt = 4;
+      if (i == B_PREADY || i == B_NUMEMPTY || i == B_STAGED || i == B_QZEMPTY) cnt = 4;
       if ((i >= B_KREADY0 && i <= B_KREADY2) || i == B_SREADY || i == B_DSEMPTY)
         cnt = 4 * Cfg::HALVES;
+      // φ(Q) warps: 8 for D = 128 (the state warps), 4 for D = 64
+      if (i == B_QREADY || i == B_QZREADY) cnt = 4 * Cfg::HALVES;
       // centered: raw Q tiles are released by the φ(Q) warps
-      if ((i == B_QEMPTY0 || i == B_QEMPTY1) && cen) cnt = 4;
+      if ((i == B_QEMPTY0 || i == B_QEMPTY1) && cen) cnt = 4 * Cfg::HALVES;
       mbar_init(&x.bar[i], cnt);
     }
     *x.abort_flag = 0;
@@ -713,7 +777,9 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   }
   if (warp == 2) {
     uint32_t* ones = reinterpret_cast<uint32_t*>(x.sm + Cfg::oONES);
-    for (int i = lane; i < 128; i += 32) ones[i] = 0x3F803F80u;  // bf16 1.0 pairs
+    for (int i = lane; i < 32; i += 32) ones[i] = 0x3F803F80u;   // bf16 1.0 pairs
+    float* qzb = reinterpret_cast<float*>(x.sm + Cfg::oQZ);
+    for (int i = lane; i < kC; i += 32) qzb[i] = 0.f;
     fence_proxy_async_smem();
   }
   if (warp == 3) {
