@@ -27,8 +27,10 @@
 // One CTA per (segment, head), 16 warps:
 //   warp 0        TMA producer
 //   warp 1        tcgen05 MMA issuer, TMEM owner
-//   warps 4–7     φ(Q) → Q'' (and Q'); masked P; epilogue o = num/den → TMA store
-//   warps 8–15    φ(K) → K'' (and K'); fp32 state S (64 columns per warpgroup)
+//   warps 4–7     masked P; epilogue o = num/den stored row by row
+//   warps 8–15    φ(K) → K'' (and K'); the state update (fp32 state in TMEM);
+//                 φ(Q) → Q'' in TMEM (and Q'), one column half per warpgroup
+//                 (d = 64: warps 12–15 compute φ(Q))
 // tcgen05 products: scores = Q''K''ᵀ (or Q'K'ᵀ), ΔS = K''ᵀV, Δz = K''ᵀ1,
 // num = Q''S + P·V, Σ_s P = P·1 — fp32 accumulators in TMEM.
 // Long sequences are split into segments: a state-only launch of this kernel
@@ -74,7 +76,7 @@ struct TcCfg {
   static constexpr int oZ = oQZ + kC * 4;        // normalizer operand z [D] fp32
   static constexpr int oPW = oZ + D * 4;         // w·a^k, k = 0..127 (general folding)
   static constexpr int oBAR = oPW + 132 * 4;     // mbarriers
-  static constexpr int NBAR = 34;
+  static constexpr int NBAR = 33;
   static constexpr int oMISC = oBAR + NBAR * 8;  // tmem slot, abort flag
   static constexpr int BYTES = oMISC + 16;
   // + alignment slack; at least half of the SM's shared memory so that one
@@ -102,7 +104,7 @@ enum {
   B_VFULL0, B_VFULL1, B_VFULL2, B_VEMPTY0, B_VEMPTY1, B_VEMPTY2,
   B_KREADY0, B_KREADY1, B_KREADY2,   // one per K stage: φ(K) may run a chunk ahead
   B_QREADY, B_KPEMPTY, B_SREADY, B_SEMPTY, B_SCORES, B_PREADY, B_NUMFULL, B_NUMEMPTY,
-  B_DSFULL, B_DSEMPTY, B_QPEMPTY, B_MMADONE, B_STAGED, B_QZREADY, B_QZEMPTY, B_COUNT
+  B_DSFULL, B_DSEMPTY, B_QPEMPTY, B_MMADONE, B_QZREADY, B_QZEMPTY, B_COUNT
 };
 
 // Roles of the seven tiles T0, T1, T2, KP, V0, V1 (and S) per kernel mode:
@@ -130,6 +132,7 @@ struct Layout {
 };
 
 struct TcParams {
+  __nv_bfloat16* out;      // [BH, n, D]
   const float* decay;      // [H] or nullptr
   int64_t H, n, seg_len;
   int nseg;
@@ -330,6 +333,7 @@ __device__ __forceinline__ void role_mma(const Ctx& x) {
       mma_ts(tmem + Cfg::TR, tmem + Cfg::TS + k * 8, ones, idR, k > 0);
     }
     mma_commit(&bar[B_NUMFULL]);
+    mma_commit(&bar[B_VEMPTY0 + vs]);              // P·V was the last reader of the V tile
   }
   // every issued MMA must finish before TMEM is released
   mma_commit(&bar[B_MMADONE]);
@@ -395,7 +399,7 @@ __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, in
 
 // Warps 4–7: masked P and the epilogue.  Thread r owns row / TMEM lane r.
 template <int D, bool CEN>
-__device__ __forceinline__ void role_rows(const Ctx& x, const CUtensorMap* map_o, int warp,
+__device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int64_t p_n, int warp,
                                           int lane) {
   using Cfg = TcCfg<D>;
   using L = Layout<D, true, CEN>;
@@ -462,7 +466,7 @@ __device__ __forceinline__ void role_rows(const Ctx& x, const CUtensorMap* map_o
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[B_PREADY]);
 
-    // ---- epilogue: o = num / den → bf16 → staging (V tile of this chunk) → TMA store
+    // ---- epilogue: o = num / den → bf16, row r written straight to global memory
     if (!warp_wait(&bar[B_NUMFULL], c & 1, st, ab)) break;
     tc_fence_after();
     if (!warp_wait(&bar[B_QZREADY], c & 1, st, ab)) break;
@@ -474,8 +478,9 @@ __device__ __forceinline__ void role_rows(const Ctx& x, const CUtensorMap* map_o
     tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TR), rs);
     tmem_ld_wait();
     const float inv_den = 1.f / (__uint_as_float(rs) + qz);
-    uint8_t* stage = x.sm + L::v_off(vs);
-    const uint32_t stage_sa = x.sbase + L::v_off(vs);
+    const int64_t row = x.t_begin + (int64_t)c * kC + r;
+    const bool valid = row < x.t_end;
+    uint4* orow = reinterpret_cast<uint4*>(out + (x.bh * p_n + (valid ? row : 0)) * D);
 #pragma unroll
     for (int j0 = 0; j0 < D; j0 += 32) {
       uint32_t nv[32];
@@ -486,32 +491,15 @@ __device__ __forceinline__ void role_rows(const Ctx& x, const CUtensorMap* map_o
         float f[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(nv[q8 * 8 + e]) * inv_den;
-        const int col = j0 + q8 * 8;
-        sts128(stage_sa + sw_chunk(kC, r, col >> 6, (col & 63) >> 3), pack8(f));
+        if (valid) __stcs(orow + (j0 + q8 * 8) / 8, pack8(f));
       }
     }
     tc_fence_before();
-    fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&bar[B_NUMEMPTY]);
-      mbar_arrive(&bar[B_STAGED]);
-    }
-    if (r == 0) {
-      // all four warps staged their rows: store the tile, then release the buffer
-      if (mbar_wait(&bar[B_STAGED], c & 1, st, ab)) {
-        const int y = (int)(x.t_begin + (int64_t)c * kC);
-        for (int h = 0; h < Cfg::HALVES; ++h)
-          tma_store_3d(map_o, stage + h * kC * 128, h * 64, y, (int)x.bh);
-        tma_store_commit();
-        tma_store_wait_read0();
-        mbar_arrive(&bar[B_VEMPTY0 + vs]);
-      }
-    }
-    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_NUMEMPTY]);
   }
-  if (r == 0) tma_store_wait0();
 }
+
 
 // Warps 8–15: φ(K), the fp32 state, and (D = 128) φ(Q).  Thread r: token row r
 // for φ(K) and φ(Q) (the columns of its half), feature row r / TMEM lane r
@@ -705,15 +693,15 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
 
 template <int D, bool FULL, bool CEN>
 __device__ __forceinline__ void run_roles(const Ctx& x, const TcParams& p, const CUtensorMap* mq,
-                                          const CUtensorMap* mk, const CUtensorMap* mv,
-                                          const CUtensorMap* mo, int warp, int lane) {
+                                          const CUtensorMap* mk, const CUtensorMap* mv, int warp,
+                                          int lane) {
   using Cfg = TcCfg<D>;
   if (warp == 0) {
     if (lane == 0) role_producer<D, FULL, CEN>(x, mq, mk, mv);
   } else if (warp == 1) {
     if (lane == 0) role_mma<D, FULL, CEN>(x);
   } else if (warp >= 4 && warp < 8) {
-    if (FULL) role_rows<D, CEN>(x, mo, warp, lane);
+    if (FULL) role_rows<D, CEN>(x, p.out, p.n, warp, lane);
   } else if (warp >= 8 && warp < 8 + 4 * Cfg::HALVES) {
     role_state<D, FULL, CEN>(x, p, warp, lane);
   } else if (FULL && Cfg::HALVES == 1 && warp >= 12) {
@@ -728,8 +716,7 @@ __device__ __forceinline__ void run_roles(const Ctx& x, const TcParams& p, const
 template <int D, bool FULL>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
-                  const TcParams p) {
+                  const __grid_constant__ CUtensorMap map_v, const TcParams p) {
   using Cfg = TcCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -759,7 +746,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   if (tid == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_PREADY || i == B_NUMEMPTY || i == B_STAGED || i == B_QZEMPTY) cnt = 4;
+      if (i == B_PREADY || i == B_NUMEMPTY || i == B_QZEMPTY) cnt = 4;
       if ((i >= B_KREADY0 && i <= B_KREADY2) || i == B_SREADY || i == B_DSEMPTY)
         cnt = 4 * Cfg::HALVES;
       // φ(Q) warps: 8 for D = 128 (the state warps), 4 for D = 64
@@ -788,18 +775,15 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
-    if (FULL) {
-      tma_prefetch_desc(&map_q);
-      tma_prefetch_desc(&map_o);
-    }
+    if (FULL) tma_prefetch_desc(&map_q);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   x.tmem = *tmem_slot;
 
-  if (cen) run_roles<D, FULL, true>(x, p, &map_q, &map_k, &map_v, &map_o, warp, lane);
-  else run_roles<D, FULL, false>(x, p, &map_q, &map_k, &map_v, &map_o, warp, lane);
+  if (cen) run_roles<D, FULL, true>(x, p, &map_q, &map_k, &map_v, warp, lane);
+  else run_roles<D, FULL, false>(x, p, &map_q, &map_k, &map_v, warp, lane);
 
   tc_fence_before();
   __syncthreads();
@@ -827,7 +811,7 @@ cudaError_t get_encoder() {
 }
 
 // [BH, n, D] bf16 viewed as a 3-D tensor (D innermost), box 64 × 128 × 1 with
-// the 128-byte swizzle.  Rows past n read as zero and are not stored.
+// the 128-byte swizzle.  Rows past n read as zero.
 cudaError_t make_map(CUtensorMap* m, const void* base, int64_t BH, int64_t n, int D) {
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)n, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)n * D * 2};
@@ -846,11 +830,10 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return e;
   const int64_t BH = a.B * a.H;
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv;
   if ((e = make_map(&mq, a.q, BH, a.n, D)) != cudaSuccess) return e;
   if ((e = make_map(&mk, a.k, BH, a.n, D)) != cudaSuccess) return e;
   if ((e = make_map(&mv, a.v, BH, a.n, D)) != cudaSuccess) return e;
-  if ((e = make_map(&mo, a.out, BH, a.n, D)) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc_forward_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
@@ -858,6 +841,7 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
                            Cfg::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   TcParams p{};
+  p.out = static_cast<__nv_bfloat16*>(a.out);
   p.decay = a.decay;
   p.H = a.H;
   p.n = a.n;
@@ -868,7 +852,7 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
   p.status = a.status;
   const dim3 grid((unsigned)plan.nseg, (unsigned)BH);
   if (plan.nseg > 1) {
-    tc_forward_kernel<D, false><<<grid, kThreadsTc, Cfg::SMEM_ALLOC, stream>>>(mq, mk, mv, mo, p);
+    tc_forward_kernel<D, false><<<grid, kThreadsTc, Cfg::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
     count_launches(1);
     e = segment_scan(ws_state, ws_z, tot_state, tot_z, BH, a.H, plan.nseg, plan.seg_len, a.n, D, D,
                      a.decay, stream);
@@ -877,7 +861,7 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
     p.fin_state = a.mu_out;
     p.fin_z = a.nu_out;
   }
-  tc_forward_kernel<D, true><<<grid, kThreadsTc, Cfg::SMEM_ALLOC, stream>>>(mq, mk, mv, mo, p);
+  tc_forward_kernel<D, true><<<grid, kThreadsTc, Cfg::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
   count_launches(1);
   return cudaGetLastError();
 }
