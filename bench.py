@@ -419,6 +419,39 @@ def run_ours(args, rank, world, dist):
     return 0
 
 
+def run_profile_case(case):
+    """Small seeded cases for ncu captures: a few calls of one entry point,
+    sized so that a full capture ends in about a minute (inputs larger than
+    L2, a few hundred MB on the device)."""
+    import causal_kernelized_linear_gb300 as cl
+    cl.build()
+    cl.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if case == "forward-long-small":
+        w = W.LONG
+        inp = W.forward_inputs(w, n=32768)          # B1 H16 n32768 d128: 512 MiB of q, k, v, o
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        out = torch.empty_like(g["q"])
+        for _ in range(3):
+            cl.forward(g["q"], g["k"], g["v"], g["a"], "elu1", None, True, out=out)
+    elif case == "decode-small":
+        w = W.DECODE
+        B = 64                                       # B64 H32 d128: 128 MiB of state
+        pre = W.decode_prefill_inputs(w, B=B)
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in pre.items()}
+        _, mu, nu = cl.forward_with_state(g["q"], g["k"], g["v"], g["a"], "elu1")
+        for step in range(5):
+            st = {k: v.to(dev) for k, v in W.decode_step_inputs(w, step, B=B).items()}
+            cl.decode_step(mu, nu, st["q"], st["k"], st["v"], g["a"])
+    else:
+        raise SystemExit(f"unknown profile case {case}")
+    torch.cuda.synchronize()
+    status = cl.last_device_status()
+    print(json.dumps({"profile_case": case, "device_status": status}))
+    return 0 if status == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -429,7 +462,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile-case", choices=["forward-long-small", "decode-small"], default=None,
+                    help="run a small seeded case for an ncu capture and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args.profile_case)
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
