@@ -185,7 +185,9 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
   const PathPlan pp = choose_path(a);
   const SegmentPlan& plan = pp.plan;
   const bool need_ws = !a.causal || plan.nseg > 1;
-  const bool need_tot = need_ws && (a.mu_out == nullptr);
+  // the inclusive total is an input of the non-causal readout; the causal
+  // paths write the final state only when the caller asks for it
+  const bool need_tot = !a.causal && (a.mu_out == nullptr);
   size_t ws_floats = 0;
   if (need_ws) ws_floats += (size_t)BH * plan.nseg * (state_elems + a.dp);
   if (need_tot) ws_floats += (size_t)BH * (state_elems + a.dp);

@@ -294,7 +294,7 @@ simt_noncausal_readout(SimtParams p) {
 
 __global__ void __launch_bounds__(256)
 segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z, int64_t H,
-                    int nseg, int64_t seg_len, int64_t n, int dpd, int dp,
+                    int nseg, int nagg, int64_t seg_len, int64_t n, int dpd, int dp,
                     const float* decay) {
   constexpr int kBatch = 8;  // aggregates loaded together to keep loads in flight
   const int64_t bh = blockIdx.x;
@@ -315,7 +315,7 @@ segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z
   for (int g0 = 0; g0 < nseg; g0 += kBatch) {
     float agg[kBatch];
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) agg[j] = (g0 + j < nseg) ? base[(g0 + j) * stride] : 0.f;
+    for (int j = 0; j < kBatch; ++j) agg[j] = (g0 + j < nagg) ? base[(g0 + j) * stride] : 0.f;
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int g = g0 + j;
@@ -326,7 +326,7 @@ segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z
       }
     }
   }
-  if (tot_state) {
+  if (tot_state && nagg == nseg) {
     if (e < dpd) tot_state[bh * dpd + e] = acc;
     else tot_z[bh * dp + (e - dpd)] = acc;
   }
@@ -368,8 +368,8 @@ cudaError_t run_simt(const FwdArgs& a, cudaStream_t stream, float* ws_state, flo
   if (need_scan) {
     simt_segment_state<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
     count_launches(1);
-    err = segment_scan(ws_state, ws_z, tot_state, tot_z, BH, a.H, plan.nseg, plan.seg_len,
-                       a.n, DP, D, a.decay, stream);
+    err = segment_scan(ws_state, ws_z, tot_state, tot_z, BH, a.H, plan.nseg, plan.nseg,
+                       plan.seg_len, a.n, DP, D, a.decay, stream);
     if (err != cudaSuccess) return err;
   }
   if (a.causal) {
@@ -411,11 +411,11 @@ cudaError_t dispatch_simt(const FwdArgs& a, cudaStream_t s, float* ws, float* wz
 }  // namespace
 
 cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* tot_z,
-                         int64_t BH, int64_t H, int nseg, int64_t seg_len, int64_t n, int dp,
-                         int d, const float* decay, cudaStream_t stream) {
+                         int64_t BH, int64_t H, int nseg, int nagg, int64_t seg_len, int64_t n,
+                         int dp, int d, const float* decay, cudaStream_t stream) {
   const int dpd = dp * d;
   const dim3 grid((unsigned)BH, (unsigned)((dpd + dp + 255) / 256));
-  segment_scan_kernel<<<grid, 256, 0, stream>>>(ws_state, ws_z, tot_state, tot_z, H, nseg,
+  segment_scan_kernel<<<grid, 256, 0, stream>>>(ws_state, ws_z, tot_state, tot_z, H, nseg, nagg,
                                                 seg_len, n, dpd, dp, decay);
   count_launches(1);
   return cudaGetLastError();

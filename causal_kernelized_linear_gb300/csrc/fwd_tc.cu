@@ -28,14 +28,17 @@
 //   warp 0        TMA producer
 //   warp 1        tcgen05 MMA issuer, TMEM owner
 //   warps 4–7     masked P; epilogue o = num/den stored row by row
+//                 (state-only launch: a share of φ(K))
 //   warps 8–15    φ(K) → K'' (and K'); the state update (fp32 state in TMEM);
 //                 φ(Q) → Q'' in TMEM (and Q'), one column half per warpgroup
-//                 (d = 64: warps 12–15 compute φ(Q))
+//                 (d = 64: warps 12–15 compute φ(Q), or a share of φ(K))
 // tcgen05 products: scores = Q''K''ᵀ (or Q'K'ᵀ), ΔS = K''ᵀV, Δz = K''ᵀ1,
-// num = Q''S + P·V, Σ_s P = P·1 — fp32 accumulators in TMEM.
+// num = Q''S + P·V, den = Q''z + P·1 — fp32 accumulators in TMEM; S and z
+// enter the products as bf16 operands.
 // Long sequences are split into segments: a state-only launch of this kernel
-// computes each segment's decayed aggregate, segment_scan turns them into the
-// states entering each segment, and the full launch produces o.
+// computes the decayed aggregate of every segment but the last, segment_scan
+// turns them into the states entering each segment, and the full launch
+// produces o (and, from the last segment, the final state).
 // Every wait is bounded in time: on expiry the kernel records LA_ERR_TIMEOUT
 // in the device status word, stops issuing work, drains what it issued and
 // frees its TMEM.
@@ -72,9 +75,12 @@ struct TcCfg {
   static constexpr int oV1 = oV0 + TILE;
   static constexpr int oS = oV1 + TILE;          // state operand, bf16 [D' × D]
   static constexpr int oONES = oS + STILE;       // 8×8 bf16 ones (128 B; every core matrix aliases it)
-  static constexpr int oQZ = oONES + 128;        // q''·z per row, [128] fp32 (summed by the φ(Q) warps)
-  static constexpr int oZ = oQZ + kC * 4;        // normalizer operand z [D] fp32
-  static constexpr int oPW = oZ + D * 4;         // w·a^k, k = 0..127 (general folding)
+  // normalizer operand z, bf16 [D'] followed by 112 readable bytes: the B
+  // operand of den = Q''·z is K-major with its core matrices 16 bytes apart,
+  // so row 0 of each holds z and rows 1–7 (output columns never read) overlap
+  // the next ones
+  static constexpr int oZB = oONES + 128;
+  static constexpr int oPW = oZB + 2 * D + 128;  // w·a^k, k = 0..127 (general folding)
   static constexpr int oBAR = oPW + 132 * 4;     // mbarriers
   static constexpr int NBAR = 33;
   static constexpr int oMISC = oBAR + NBAR * 8;  // tmem slot, abort flag
@@ -87,16 +93,12 @@ struct TcCfg {
   static constexpr uint32_t TN = 128;            // numerator [128 × D]
   static constexpr uint32_t TD = TN + D;         // ΔS [D' × D] (lanes = feature)
   static constexpr uint32_t TZ = TD + D;         // Δz (16 columns, column 0 used)
-  static constexpr uint32_t TR = TZ + 16;        // Σ_s P_ts (16 columns, column 0 used)
+  static constexpr uint32_t TR = TZ + 16;        // q''·z + Σ_s P_ts (16 columns, column 0 used)
   static constexpr uint32_t TQ = (D == 128) ? 448 : 320;  // Q'' (bf16 pairs, D/2 columns)
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(TR + 16 <= TQ, "TMEM layout");
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
-
-// z needs one copy: φ(Q) of chunk c reads z_c before it signals q_ready(c),
-// and z_{c+1} is written only after MMA3(c) — issued after the scores MMA of
-// chunk c, which waits for q_ready(c) — has completed.
 
 enum {
   B_QFULL0 = 0, B_QFULL1, B_QEMPTY0, B_QEMPTY1,
@@ -104,8 +106,9 @@ enum {
   B_VFULL0, B_VFULL1, B_VFULL2, B_VEMPTY0, B_VEMPTY1, B_VEMPTY2,
   B_KREADY0, B_KREADY1, B_KREADY2,   // one per K stage: φ(K) may run a chunk ahead
   B_QREADY, B_KPEMPTY, B_SREADY, B_SEMPTY, B_SCORES, B_PREADY, B_NUMFULL, B_NUMEMPTY,
-  B_DSFULL, B_DSEMPTY, B_QPEMPTY, B_MMADONE, B_QZREADY, B_QZEMPTY, B_COUNT
+  B_DSFULL, B_DSEMPTY, B_QPEMPTY, B_MMADONE, B_COUNT
 };
+static_assert(B_COUNT <= TcCfg<64>::NBAR, "barrier slots");
 
 // Roles of the seven tiles T0, T1, T2, KP, V0, V1 (and S) per kernel mode:
 //   centered, full:  Q stages T0, T1 | K stages T2, KP (φ(K) writes K'' in place) | V V0, V1
@@ -157,6 +160,18 @@ __device__ __forceinline__ float elu1_fast(float x) {
   return fmaxf(x, 0.f) + __expf(fminf(x, 0.f));
 }
 
+// The same φ on a pair of bf16 values in packed bf16 arithmetic:
+// max(x, 0) + 2^(min(x, 0)·log2 e).  The result is bf16 (the precision the
+// tensor-core operand is rounded to anyway); the bf16 rounding of the
+// exponent argument and of log2 e adds an error of at most 1.3 % for
+// x ≥ −3 (3 % for x ≥ −6), on the small e^x branch only — the x + 1 branch
+// is rounded once, as before.
+__device__ __forceinline__ uint32_t elu1_bf16x2(uint32_t x) {
+  constexpr uint32_t kLog2e = 0x3FB93FB9u;   // bf16(log2 e) = 1.4453125, both lanes
+  const uint32_t e = ex2_bf16x2(mul_bf16x2(min_bf16x2(x, 0u), kLog2e));
+  return add_bf16x2(max_bf16x2(x, 0u), e);
+}
+
 // a^e for integer e of either sign (a > 0, or e ≥ 0).
 __device__ __forceinline__ float decay_pow_signed(float a, int e) {
   return e == 0 ? 1.f : powf(a, (float)e);
@@ -188,15 +203,23 @@ struct Ctx {
   uint32_t sbase;
   uint64_t* bar;
   volatile int* abort_flag;
-  float* zbuf;
-  float* qzbuf;
+  __nv_bfloat16* zb;
   float* pw;
   uint32_t tmem;
   int* status;
   int64_t bh, t_begin, t_end;
   int g, nchunks;
   float a, w;
+  float lg;    // log2 a (centered folding; 0 for a = 1)
+  int R;       // centered folding: the TMEM state is rescaled every R chunks
 };
+
+// Centered folding, lazy rescaling: K'' of chunk c carries σ_c = a^{−128·(c mod R)}
+// (all chunks but the last are full), so that the state MMA can keep
+// accumulating onto the TMEM state for R chunks before it is rescaled.
+__device__ __forceinline__ float lazy_sigma(const Ctx& x, int c) {
+  return exp2f(-128.f * (float)(c % x.R) * x.lg);
+}
 
 // ------------------------------------------------------------------ roles
 
@@ -250,21 +273,24 @@ __device__ __forceinline__ void role_producer(const Ctx& x, const CUtensorMap* m
   }
 }
 
-template <int D, bool FULL, bool CEN>
-__device__ __forceinline__ void role_mma(const Ctx& x) {
+// Two MMA issuers, each a single thread; tcgen05.commit tracks the
+// operations of the issuing thread, so each chain commits its own barriers.
+// Output chain (warp 1): scores, num = Q''·S and den = Q''·z, then
+// num += P·V and den += P·1.  State chain (warp 2): ΔS = K''ᵀV, Δz = K''ᵀ1.
+// Tiles read by both chains (K'' in the centered folding, V) are released
+// by a commit from each.
+template <int D, bool CEN>
+__device__ __forceinline__ void role_mma_out(const Ctx& x) {
   using Cfg = TcCfg<D>;
-  using L = Layout<D, FULL, CEN>;
+  using L = Layout<D, true, CEN>;
   uint64_t* bar = x.bar;
   const uint32_t tmem = x.tmem;
-  const uint32_t sS = x.sbase + Cfg::oS, sONES = x.sbase + Cfg::oONES;
+  const uint32_t sS = x.sbase + Cfg::oS, sONES = x.sbase + Cfg::oONES, sZB = x.sbase + Cfg::oZB;
   constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);   // scores
-  constexpr uint32_t idD = idesc_bf16_f32(128, D, true, true);       // ΔS = K''ᵀ V
-  constexpr uint32_t idZ = idesc_bf16_f32(128, 16, true, false);     // Δz = K''ᵀ 1
   constexpr uint32_t idN = idesc_bf16_f32(128, D, false, true);      // num (+)= A·{S, V}
-  constexpr uint32_t idR = idesc_bf16_f32(128, 16, false, false);    // Σ_s P = P·1
+  constexpr uint32_t idR = idesc_bf16_f32(128, 16, false, false);    // den: Q''·z, P·1
   constexpr int KD = D / 16;                                         // K-steps over D'
-  const uint32_t lbo_kp = (D == 128) ? kC * 128 : 0;                 // M blocks of K''ᵀ
-  const uint64_t ones = smem_desc(sONES, 0, 0, kSwizzleNone);   // all core matrices alias
+  const uint64_t ones = smem_desc(sONES, 0, 0, kSwizzleNone);        // all core matrices alias
   int* st = x.status;
   volatile int* ab = x.abort_flag;
   for (int c = 0; c < x.nchunks; ++c) {
@@ -272,36 +298,78 @@ __device__ __forceinline__ void role_mma(const Ctx& x) {
     const uint32_t sK = x.sbase + L::k_off(ks);
     const uint32_t sKP = x.sbase + L::kpp_off(ks);
     const uint32_t sV = x.sbase + L::v_off(vs);
+    // scores = Q''K''ᵀ (centered) or Q'K'ᵀ (general); P(c−1) in the same
+    // columns must have been consumed by P·V of chunk c−1
     if (!mbar_wait(&bar[B_KREADY0 + ks], (c / L::KST) & 1, st, ab)) break;
-    if (FULL) {
-      // scores = Q''K''ᵀ (centered) or Q'K'ᵀ (general)
-      if (!mbar_wait(&bar[B_QREADY], c & 1, st, ab)) break;
-      if (c >= 1 && !mbar_wait(&bar[B_NUMFULL], (c - 1) & 1, st, ab)) break;
-      tc_fence_after();
-      if (CEN) {
-        for (int k = 0; k < KD; ++k) {
-          const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
-          mma_ts(tmem + Cfg::TS, tmem + Cfg::TQ + k * 8,
-                 smem_desc(sKP + off, 16, 1024, kSwizzle128B), idS, k > 0);
-        }
-        mma_commit(&bar[B_SCORES]);
-      } else {
-        const uint32_t sQ = x.sbase + L::q_off(0);
-        for (int k = 0; k < KD; ++k) {
-          const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
-          mma_ss(tmem + Cfg::TS, smem_desc(sQ + off, 16, 1024, kSwizzle128B),
-                 smem_desc(sK + off, 16, 1024, kSwizzle128B), idS, k > 0);
-        }
-        mma_commit(&bar[B_SCORES]);
-        mma_commit(&bar[B_QEMPTY0]);
-        mma_commit(&bar[B_KEMPTY0 + ks]);            // K' was the last reader of the raw tile
+    if (!mbar_wait(&bar[B_QREADY], c & 1, st, ab)) break;
+    if (c >= 1 && !mbar_wait(&bar[B_NUMFULL], (c - 1) & 1, st, ab)) break;
+    tc_fence_after();
+    if (CEN) {
+      for (int k = 0; k < KD; ++k) {
+        const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
+        mma_ts(tmem + Cfg::TS, tmem + Cfg::TQ + k * 8,
+               smem_desc(sKP + off, 16, 1024, kSwizzle128B), idS, k > 0);
       }
+      mma_commit(&bar[B_SCORES]);
     } else {
-      tc_fence_after();
+      const uint32_t sQ = x.sbase + L::q_off(0);
+      for (int k = 0; k < KD; ++k) {
+        const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
+        mma_ss(tmem + Cfg::TS, smem_desc(sQ + off, 16, 1024, kSwizzle128B),
+               smem_desc(sK + off, 16, 1024, kSwizzle128B), idS, k > 0);
+      }
+      mma_commit(&bar[B_SCORES]);
+      mma_commit(&bar[B_QEMPTY0]);
     }
-    // ΔS = K''ᵀ V ; Δz = K''ᵀ 1
+    mma_commit(&bar[B_KEMPTY0 + ks]);
+    // num = Q''·S ; den = Q''·z
+    if (!mbar_wait(&bar[B_SREADY], c & 1, st, ab)) break;
+    if (c >= 1 && !mbar_wait(&bar[B_NUMEMPTY], (c - 1) & 1, st, ab)) break;
+    tc_fence_after();
+    for (int k = 0; k < KD; ++k) {
+      mma_ts(tmem + Cfg::TN, tmem + Cfg::TQ + k * 8,
+             smem_desc(sS + k * 2048, D * 128, 1024, kSwizzle128B), idN, k > 0);
+      mma_ts(tmem + Cfg::TR, tmem + Cfg::TQ + k * 8, smem_desc(sZB + k * 32, 16, 0, kSwizzleNone),
+             idR, k > 0);
+    }
+    mma_commit(&bar[B_SEMPTY]);
+    mma_commit(&bar[B_QPEMPTY]);
+    // num += P·V ; den += P·1
+    if (!mbar_wait(&bar[B_PREADY], c & 1, st, ab)) break;
     if (!mbar_wait(&bar[B_VFULL0 + vs], (c / L::VST) & 1, st, ab)) break;
-    if (!mbar_wait(&bar[B_DSEMPTY], c & 1, st, ab)) break;   // pre-scaled state in TMEM
+    tc_fence_after();
+    for (int k = 0; k < kC / 16; ++k) {
+      mma_ts(tmem + Cfg::TN, tmem + Cfg::TS + k * 8,
+             smem_desc(sV + k * 2048, kC * 128, 1024, kSwizzle128B), idN, 1);
+      mma_ts(tmem + Cfg::TR, tmem + Cfg::TS + k * 8, ones, idR, 1);
+    }
+    mma_commit(&bar[B_NUMFULL]);
+    mma_commit(&bar[B_VEMPTY0 + vs]);
+  }
+  // every issued MMA must finish before TMEM is released
+  mma_commit(&bar[B_MMADONE]);
+  mbar_wait_drain(&bar[B_MMADONE], 0);
+}
+
+template <int D, bool FULL, bool CEN>
+__device__ __forceinline__ void role_mma_state(const Ctx& x) {
+  using Cfg = TcCfg<D>;
+  using L = Layout<D, FULL, CEN>;
+  uint64_t* bar = x.bar;
+  const uint32_t tmem = x.tmem;
+  constexpr uint32_t idD = idesc_bf16_f32(128, D, true, true);       // ΔS = K''ᵀ V
+  constexpr uint32_t idZ = idesc_bf16_f32(128, 16, true, false);     // Δz = K''ᵀ 1
+  const uint32_t lbo_kp = (D == 128) ? kC * 128 : 0;                 // M blocks of K''ᵀ
+  const uint64_t ones = smem_desc(x.sbase + Cfg::oONES, 0, 0, kSwizzleNone);
+  int* st = x.status;
+  volatile int* ab = x.abort_flag;
+  for (int c = 0; c < x.nchunks; ++c) {
+    const int ks = c % L::KST, vs = c % L::VST;
+    const uint32_t sKP = x.sbase + L::kpp_off(ks);
+    const uint32_t sV = x.sbase + L::v_off(vs);
+    if (!mbar_wait(&bar[B_KREADY0 + ks], (c / L::KST) & 1, st, ab)) break;
+    if (!mbar_wait(&bar[B_VFULL0 + vs], (c / L::VST) & 1, st, ab)) break;
+    if (!mbar_wait(&bar[B_DSEMPTY], c & 1, st, ab)) break;   // state in TMEM read out
     tc_fence_after();
     for (int k = 0; k < kC / 16; ++k) {
       const uint64_t ad = smem_desc(sKP + k * 2048, lbo_kp, 1024, kSwizzle128B);
@@ -309,43 +377,17 @@ __device__ __forceinline__ void role_mma(const Ctx& x) {
       mma_ss(tmem + Cfg::TZ, ad, ones, idZ, 1);
     }
     mma_commit(&bar[B_DSFULL]);
-    if (L::K_IN_PLACE) mma_commit(&bar[B_KEMPTY0 + ks]);   // K'' tile free for the next load
-    else mma_commit(&bar[B_KPEMPTY]);
-    if (!FULL) {
-      mma_commit(&bar[B_VEMPTY0 + vs]);
-      continue;
-    }
-    // num = Q''·S
-    if (!mbar_wait(&bar[B_SREADY], c & 1, st, ab)) break;
-    if (c >= 1 && !mbar_wait(&bar[B_NUMEMPTY], (c - 1) & 1, st, ab)) break;
-    tc_fence_after();
-    for (int k = 0; k < KD; ++k)
-      mma_ts(tmem + Cfg::TN, tmem + Cfg::TQ + k * 8,
-             smem_desc(sS + k * 2048, D * 128, 1024, kSwizzle128B), idN, k > 0);
-    mma_commit(&bar[B_SEMPTY]);
-    mma_commit(&bar[B_QPEMPTY]);
-    // num += P·V ; Σ_s P
-    if (!mbar_wait(&bar[B_PREADY], c & 1, st, ab)) break;
-    tc_fence_after();
-    for (int k = 0; k < kC / 16; ++k) {
-      mma_ts(tmem + Cfg::TN, tmem + Cfg::TS + k * 8,
-             smem_desc(sV + k * 2048, kC * 128, 1024, kSwizzle128B), idN, 1);
-      mma_ts(tmem + Cfg::TR, tmem + Cfg::TS + k * 8, ones, idR, k > 0);
-    }
-    mma_commit(&bar[B_NUMFULL]);
-    mma_commit(&bar[B_VEMPTY0 + vs]);              // P·V was the last reader of the V tile
+    mma_commit(&bar[L::K_IN_PLACE ? B_KEMPTY0 + ks : B_KPEMPTY]);
+    mma_commit(&bar[B_VEMPTY0 + vs]);
   }
-  // every issued MMA must finish before TMEM is released
   mma_commit(&bar[B_MMADONE]);
   mbar_wait_drain(&bar[B_MMADONE], 0);
 }
 
 // φ(Q) of chunk c for the 64 columns of half h of row r (TMEM lane r):
-// Q'' = a_row·φ(q) into TMEM, the partial q''·z over those columns; the
-// general folding also writes Q' back in place for the scores MMA.  Signals
-// q_ready (the scores MMA may start), then adds the partial into the per-row
-// q''·z buffer once the epilogue of chunk c−1 has read it, and signals
-// qz_ready.  Returns false if a wait gave up.
+// Q'' = a_row·φ(q) into TMEM; the general folding also writes Q' back in
+// place for the scores MMA.  Signals q_ready (the scores MMA may start).
+// Returns false if a wait gave up.
 template <int D, bool CEN>
 __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, int lane,
                                            uint32_t lane_base, float a_row) {
@@ -357,28 +399,20 @@ __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, in
   const int qs = c % L::QST;
   if (!warp_wait(&bar[B_QFULL0 + qs], (c / L::QST) & 1, st, ab)) return false;
   if (c >= 1 && !warp_wait(&bar[B_QPEMPTY], (c - 1) & 1, st, ab)) return false;
-  if (!warp_wait(&bar[B_SREADY], c & 1, st, ab)) return false;
-  const float4* zc4 = reinterpret_cast<const float4*>(x.zbuf);
   uint8_t* qt = x.sm + L::q_off(qs);
-  float qz = 0.f;
+  const uint32_t a2 = splat_bf16x2(a_row);
   uint32_t packed[32];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    float f[8];
     uint4* qp = reinterpret_cast<uint4*>(qt + sw_chunk(kC, r, h, j));
-    unpack8(*qp, f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] = elu1_fast(f[e]);
-    if (!CEN) *qp = pack8(f);
-    const float4 z0 = zc4[(h * 64 + j * 8) / 4];
-    const float4 z1 = zc4[(h * 64 + j * 8) / 4 + 1];
-    const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      const uint32_t pr = pack_bf16x2(a_row * f[e], a_row * f[e + 1]);
-      packed[j * 4 + e / 2] = pr;
-      qz += bf16lo_to_f32(pr) * zz[e] + bf16hi_to_f32(pr) * zz[e + 1];
-    }
+    uint4 u = *qp;
+    u.x = elu1_bf16x2(u.x); u.y = elu1_bf16x2(u.y);
+    u.z = elu1_bf16x2(u.z); u.w = elu1_bf16x2(u.w);
+    if (!CEN) *qp = u;
+    packed[j * 4 + 0] = mul_bf16x2(u.x, a2);
+    packed[j * 4 + 1] = mul_bf16x2(u.y, a2);
+    packed[j * 4 + 2] = mul_bf16x2(u.z, a2);
+    packed[j * 4 + 3] = mul_bf16x2(u.w, a2);
   }
   tmem_st32(tmem_addr(x.tmem, lane_base, Cfg::TQ + h * 32), packed);
   tmem_st_wait();
@@ -389,11 +423,6 @@ __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, in
     mbar_arrive(&bar[B_QREADY]);
     if (CEN) mbar_arrive(&bar[B_QEMPTY0 + qs]);  // raw Q tile no longer needed
   }
-  // publish the partial q''·z of this row
-  if (c >= 1 && !warp_wait(&bar[B_QZEMPTY], (c - 1) & 1, st, ab)) return false;
-  atomicAdd(&x.qzbuf[r], qz);
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&bar[B_QZREADY]);
   return true;
 }
 
@@ -469,15 +498,10 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
     // ---- epilogue: o = num / den → bf16, row r written straight to global memory
     if (!warp_wait(&bar[B_NUMFULL], c & 1, st, ab)) break;
     tc_fence_after();
-    if (!warp_wait(&bar[B_QZREADY], c & 1, st, ab)) break;
-    const float qz = x.qzbuf[r];
-    x.qzbuf[r] = 0.f;                               // the φ(Q) warps accumulate into it
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bar[B_QZEMPTY]);
-    uint32_t rs = 0;
-    tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TR), rs);
+    uint32_t den = 0;
+    tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TR), den);
     tmem_ld_wait();
-    const float inv_den = 1.f / (__uint_as_float(rs) + qz);
+    const float inv_den = 1.f / __uint_as_float(den);
     const int64_t row = x.t_begin + (int64_t)c * kC + r;
     const bool valid = row < x.t_end;
     uint4* orow = reinterpret_cast<uint4*>(out + (x.bh * p_n + (valid ? row : 0)) * D);
@@ -501,15 +525,82 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
 }
 
 
+// φ(K) of chunk c for the 16-byte column chunks [j0, j1) of token row r →
+// K'' = gs·φ(k) (rows ≥ cs get weight 0), written in place into the K tile
+// except for the general full kernel, which keeps K' = m·φ(k) in place and
+// writes K'' into its own tile.  φ is computed for every row so that no
+// per-element branch splits the warp.  Signals k_ready for the warp.
+template <int D, bool FULL, bool CEN>
+__device__ __forceinline__ bool phi_k_chunk(const Ctx& x, int c, int r, int j0, int j1, int lane,
+                                            float k_scale_cen) {
+  using L = Layout<D, FULL, CEN>;
+  uint64_t* bar = x.bar;
+  int* st = x.status;
+  volatile int* ab = x.abort_flag;
+  const int ks = c % L::KST;
+  const int cs = (int)min((int64_t)kC, x.t_end - (x.t_begin + (int64_t)c * kC));
+  if (!warp_wait(&bar[B_KFULL0 + ks], (c / L::KST) & 1, st, ab)) return false;
+  if (!L::K_IN_PLACE && c >= 1 && !warp_wait(&bar[B_KPEMPTY], (c - 1) & 1, st, ab)) return false;
+  const bool live = r < cs;
+  const uint32_t m2 = live ? 0x3F803F80u : 0u;   // bf16 1.0 / 0.0 pairs
+  const uint32_t g2 =
+      live ? splat_bf16x2(CEN ? k_scale_cen * lazy_sigma(x, c) : x.pw[max(cs - 1 - r, 0)]) : 0u;
+  uint8_t* kt = x.sm + L::k_off(ks);
+  uint8_t* kpp = x.sm + L::kpp_off(ks);
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {            // ranges are at most 8 chunks long
+    const int jj = j0 + t;
+    if (jj >= j1) break;
+    const uint32_t off = sw_chunk(kC, r, jj >> 3, jj & 7);
+    uint4 u = *reinterpret_cast<const uint4*>(kt + off);
+    u.x = elu1_bf16x2(u.x); u.y = elu1_bf16x2(u.y);
+    u.z = elu1_bf16x2(u.z); u.w = elu1_bf16x2(u.w);
+    if (!L::K_IN_PLACE)
+      *reinterpret_cast<uint4*>(kt + off) =
+          make_uint4(mul_bf16x2(u.x, m2), mul_bf16x2(u.y, m2), mul_bf16x2(u.z, m2), mul_bf16x2(u.w, m2));
+    *reinterpret_cast<uint4*>(kpp + off) =
+        make_uint4(mul_bf16x2(u.x, g2), mul_bf16x2(u.y, g2), mul_bf16x2(u.z, g2), mul_bf16x2(u.w, g2));
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bar[B_KREADY0 + ks]);
+  return true;
+}
+
+// φ(K) column ranges (16-byte chunks of a row, 8 per 64 columns).  Full
+// launch: the state warpgroups split the columns by halves.  State-only
+// launch: the idle warpgroups take a share — d = 128: warps 4–7 chunks
+// 0–7, the state warpgroups 8–11 and 12–15; d = 64: warps 4–7 chunks 0–2,
+// warps 12–15 chunks 3–5, the state warps 6–7.
+template <int D, bool FULL>
+struct KSplit {
+  static constexpr int NJ = 8 * TcCfg<D>::HALVES;
+  __device__ static void range(int wg, int& j0, int& j1) {
+    if (FULL) {
+      j0 = (wg - 2) * 8; j1 = j0 + 8;
+    } else if (D == 128) {
+      j0 = wg == 1 ? 0 : (wg == 2 ? 8 : 12); j1 = wg == 1 ? 8 : (wg == 2 ? 12 : 16);
+    } else {
+      j0 = wg == 1 ? 0 : (wg == 3 ? 3 : 6); j1 = wg == 1 ? 3 : (wg == 3 ? 6 : 8);
+    }
+  }
+  static constexpr int ARRIVALS = FULL ? 4 * TcCfg<D>::HALVES : 12;
+};
+
 // Warps 8–15: φ(K), the fp32 state, and (D = 128) φ(Q).  Thread r: token row r
 // for φ(K) and φ(Q) (the columns of its half), feature row r / TMEM lane r
 // for the state (the 64 state columns of its half).
 //
-// The fp32 state lives in TMEM (columns TD, and TZ for z), pre-scaled so that
-// the state MMA accumulates onto it: before the MMA of chunk c it holds β·S_c,
-// and the bf16 operand tile of the inter-chunk MMA holds α·S:
-//   centered:  TMEM = a^{64}·S_c, so after the MMA v = a^{64}S_c + ΔS'' and
-//              a^{64}·S_{c+1} = a^{cs}·v feeds both TMEM and the tile;
+// The fp32 state lives in TMEM (columns TD, and TZ for z), scaled so that
+// the state MMA accumulates onto it:
+//   centered:  TMEM holds U_c with a^{64}·S_c = ρ_c·U_c, ρ_c = a^{128·(c mod R)}.
+//              K''_c carries σ_c = 1/ρ_c, so the MMA leaves U_{c+1} = U_c + σ_c·ΔS''
+//              and a^{64}S_{c+1} = a^{cs}(a^{64}S_c + ΔS'') = ρ_{c+1}U_{c+1}.
+//              Every output term of chunk c — P·V, P·1 (through K'') and the
+//              inter-chunk part — is then scaled by the same σ_c, which
+//              cancels in num/den, so the operand tile is U_c itself.  Every
+//              R chunks U is multiplied by a^{128R} (ρ back to 1); R keeps
+//              σ ≤ 2^{32}.  a = 1: ρ = σ = 1 throughout.
 //   general:   TMEM = a^{cs}·S_c, so after the MMA v = S_{c+1}; the tile gets
 //              S_{c+1} and TMEM a^{cs'}·S_{c+1} for the next chunk (cs').
 template <int D, bool FULL, bool CEN>
@@ -538,16 +629,17 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   if (!FULL) {
     out_S = p.ws_state + (x.bh * p.nseg + x.g) * (int64_t)(D * D);
     out_z = p.ws_z + (x.bh * p.nseg + x.g) * (int64_t)D;
-  } else if (p.fin_state) {
+  } else if (p.fin_state && x.g == p.nseg - 1) {
     out_S = p.fin_state + x.bh * (int64_t)(D * D);
     out_z = p.fin_z + x.bh * (int64_t)D;
   }
 
   // Writes one state value v (this thread's 64 columns, in 32-column steps
-  // produced by `fetch`) as: TMEM ← β·v, tile ← α·v (full kernel), global ←
-  // γ·v (last chunk).  z is handled by the half-0 warps.
+  // produced by `fetch`) as: tile ← α·v (full kernel), TMEM ← β·v (when
+  // to_tmem), global ← γ·v (last chunk).  z is handled by the half-0 warps.
+  // tile, to_tmem and to_global are warp-uniform.
   auto put_state = [&](auto fetch, float zv, float alpha, float beta, float gamma, bool tile,
-                       bool to_global) {
+                       bool to_tmem, bool to_global) {
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       float v[32];
@@ -567,60 +659,31 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
           *reinterpret_cast<float4*>(out_S + r * D + half * 64 + hh * 32 + j) =
               make_float4(gamma * v[j], gamma * v[j + 1], gamma * v[j + 2], gamma * v[j + 3]);
       }
-      uint32_t o[32];
+      if (to_tmem) {
+        uint32_t o[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(beta * v[j]);
-      tmem_st32(td + hh * 32, o);
+        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(beta * v[j]);
+        tmem_st32(td + hh * 32, o);
+      }
     }
     if (half == 0) {
-      uint32_t zo[1] = {__float_as_uint(beta * zv)};
-      asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tz), "r"(zo[0])
-                   : "memory");
-      if (srow && tile) x.zbuf[r] = alpha * zv;
+      if (to_tmem) {
+        const uint32_t zo = __float_as_uint(beta * zv);
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tz), "r"(zo)
+                     : "memory");
+      }
+      if (srow && tile) x.zb[r] = __float2bfloat16_rn(alpha * zv);
       if (srow && to_global) out_z[r] = gamma * zv;
     }
-    tmem_st_wait();
+    if (to_tmem) tmem_st_wait();
     tc_fence_before();
     if (tile) fence_proxy_async_smem();
     __syncwarp();
   };
 
-  // φ(K) of chunk c → K'' (rows ≥ cs zeroed by weight), written in place into
-  // the K tile except for the general full kernel, which keeps K' in place
-  // and writes K'' into its own tile.
-  auto phi_k = [&](int c) -> bool {
-    const int ks = c % L::KST;
-    const int cs = chunk_len(c);
-    if (!warp_wait(&bar[B_KFULL0 + ks], (c / L::KST) & 1, st, ab)) return false;
-    if (!L::K_IN_PLACE && c >= 1 && !warp_wait(&bar[B_KPEMPTY], (c - 1) & 1, st, ab)) return false;
-    // Rows past the end of the sequence (TMA zero-fill) must contribute
-    // nothing: their weight gs is 0, and K' (general folding) is masked with
-    // m.  φ itself is computed for every row so that no per-element branch
-    // breaks the warp into divergent paths.
-    const bool live = r < cs;
-    const float m = live ? 1.f : 0.f;
-    const float gs = live ? (CEN ? k_scale_cen : x.pw[max(cs - 1 - r, 0)]) : 0.f;
-    uint8_t* kt = x.sm + L::k_off(ks);
-    uint8_t* kpp = x.sm + L::kpp_off(ks);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t off = sw_chunk(kC, r, half, j);
-      float f[8], f2[8];
-      unpack8(*reinterpret_cast<const uint4*>(kt + off), f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        f[e] = elu1_fast(f[e]);
-        f2[e] = gs * f[e];
-        if (!L::K_IN_PLACE) f[e] *= m;
-      }
-      if (!L::K_IN_PLACE) *reinterpret_cast<uint4*>(kt + off) = pack8(f);
-      *reinterpret_cast<uint4*>(kpp + off) = pack8(f2);
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bar[B_KREADY0 + ks]);
-    return true;
-  };
+  int kj0, kj1;
+  KSplit<D, FULL>::range((warp - 8) / 4 + 2, kj0, kj1);
+  auto phi_k = [&](int c) { return phi_k_chunk<D, FULL, CEN>(x, c, r, kj0, kj1, lane, k_scale_cen); };
 
   // ---- initial state (S_in from the segment scan, or zero)
   {
@@ -644,7 +707,7 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
                   for (int j = 0; j < 32; ++j) v[j] = 0.f;
                 }
               },
-              zin, alpha0, beta0, 1.f, FULL, false);
+              zin, alpha0, beta0, 1.f, FULL, true, false);
     if (lane == 0) {
       mbar_arrive(&bar[B_DSEMPTY]);                // TMEM state ready for the first MMA
       if (FULL) mbar_arrive(&bar[B_SREADY]);       // operand tile ready
@@ -662,25 +725,39 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
     const int cs = chunk_len(c);
     const bool last = c + 1 == x.nchunks;
     if (!warp_wait(&bar[B_DSFULL], c & 1, st, ab)) break;
-    if (FULL && !warp_wait(&bar[B_SEMPTY], c & 1, st, ab)) break;   // tile free
+    if (FULL && !last && !warp_wait(&bar[B_SEMPTY], c & 1, st, ab)) break;   // tile free
     tc_fence_after();
-    const float acs = decay_pow(a, cs);
-    const float alpha = CEN ? acs : 1.f;
-    const float beta = CEN ? acs : (last ? 1.f : decay_pow(a, chunk_len(c + 1)));
-    const float gamma = CEN ? decay_pow_signed(a, cs - 64) : 1.f;
-    uint32_t zraw = 0;
-    if (half == 0) {
-      tmem_ld1(tz, zraw);
-      tmem_ld_wait();
+    float alpha, beta, gamma;
+    bool to_tmem;
+    if (CEN) {
+      const bool renorm = !last && (c + 1) % x.R == 0;
+      alpha = beta = renorm ? exp2f(128.f * (float)x.R * x.lg) : 1.f;
+      gamma = exp2f(x.lg * (float)(cs - 64 + 128 * (c % x.R)));   // a^{cs−64}·ρ_c
+      to_tmem = renorm;
+    } else {
+      alpha = 1.f;
+      beta = last ? 1.f : decay_pow(a, chunk_len(c + 1));
+      gamma = 1.f;
+      to_tmem = !last;
     }
-    put_state([&](int hh, float* v) {
-                uint32_t u[32];
-                tmem_ld32(td + hh * 32, u);
-                tmem_ld_wait();
+    const bool tile = FULL && !last;
+    const bool to_global = last && out_S != nullptr;
+    if (tile || to_tmem || to_global) {
+      uint32_t zraw = 0;
+      uint32_t u[64];
+      tmem_ld32(td, u);
+      tmem_ld32(td + 32, u + 32);
+      if (half == 0) tmem_ld1(tz, zraw);
+      tmem_ld_wait();
+      put_state([&](int hh, float* v) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
-              },
-              __uint_as_float(zraw), alpha, beta, gamma, FULL && !last, last && out_S != nullptr);
+                  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[hh * 32 + j]);
+                },
+                __uint_as_float(zraw), alpha, beta, gamma, tile, to_tmem, to_global);
+    } else {
+      tc_fence_before();
+      __syncwarp();
+    }
     if (lane == 0) {
       mbar_arrive(&bar[B_DSEMPTY]);
       if (FULL && !last) mbar_arrive(&bar[B_SREADY]);
@@ -699,11 +776,21 @@ __device__ __forceinline__ void run_roles(const Ctx& x, const TcParams& p, const
   if (warp == 0) {
     if (lane == 0) role_producer<D, FULL, CEN>(x, mq, mk, mv);
   } else if (warp == 1) {
-    if (lane == 0) role_mma<D, FULL, CEN>(x);
-  } else if (warp >= 4 && warp < 8) {
-    if (FULL) role_rows<D, CEN>(x, p.out, p.n, warp, lane);
+    if (FULL && lane == 0) role_mma_out<D, CEN>(x);
+  } else if (warp == 2) {
+    if (lane == 0) role_mma_state<D, FULL, CEN>(x);
+  } else if (warp >= 4 && warp < 8 && FULL) {
+    role_rows<D, CEN>(x, p.out, p.n, warp, lane);
   } else if (warp >= 8 && warp < 8 + 4 * Cfg::HALVES) {
     role_state<D, FULL, CEN>(x, p, warp, lane);
+  } else if (!FULL && warp >= 4) {
+    // state-only launch: a share of φ(K) on the otherwise idle warpgroups
+    const int r = (warp & 3) * 32 + lane;
+    const float k_scale_cen = CEN ? x.w * decay_pow_signed(x.a, 63 - r) : 0.f;
+    int j0, j1;
+    KSplit<D, false>::range(warp / 4, j0, j1);
+    for (int c = 0; c < x.nchunks; ++c)
+      if (!phi_k_chunk<D, false, CEN>(x, c, r, j0, j1, lane, k_scale_cen)) break;
   } else if (FULL && Cfg::HALVES == 1 && warp >= 12) {
     // D = 64: the fourth warpgroup computes φ(Q)
     const int r = (warp - 12) * 32 + lane;
@@ -726,8 +813,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   x.bar = reinterpret_cast<uint64_t*>(x.sm + Cfg::oBAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x.sm + Cfg::oMISC);
   x.abort_flag = reinterpret_cast<volatile int*>(x.sm + Cfg::oMISC + 4);
-  x.zbuf = reinterpret_cast<float*>(x.sm + Cfg::oZ);
-  x.qzbuf = reinterpret_cast<float*>(x.sm + Cfg::oQZ);
+  x.zb = reinterpret_cast<__nv_bfloat16*>(x.sm + Cfg::oZB);
   x.pw = reinterpret_cast<float*>(x.sm + Cfg::oPW);
   x.status = p.status;
 
@@ -742,15 +828,21 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   x.a = p.decay ? p.decay[x.bh % p.H] : 1.f;
   x.w = new_token_weight(x.a);
   const bool cen = (x.a == 1.f) || (x.a >= kCenteredMinDecay);
+  x.lg = (cen && x.a != 1.f) ? log2f(x.a) : 0.f;
+  // largest R with 128·(R−1)·|log2 a| ≤ 32 − 128·|log2 a|, at least 1
+  x.R = x.lg == 0.f ? (1 << 30) : max(1, (int)fminf(32.f / (128.f * -x.lg), 1e9f));
 
   if (tid == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_PREADY || i == B_NUMEMPTY || i == B_QZEMPTY) cnt = 4;
-      if ((i >= B_KREADY0 && i <= B_KREADY2) || i == B_SREADY || i == B_DSEMPTY)
-        cnt = 4 * Cfg::HALVES;
+      if (i == B_PREADY || i == B_NUMEMPTY) cnt = 4;
+      // released by both MMA chains: K'' (centered, full), V (full)
+      if (i >= B_KEMPTY0 && i <= B_KEMPTY2 && FULL && cen) cnt = 2;
+      if (((i >= B_VEMPTY0 && i <= B_VEMPTY2) || i == B_MMADONE) && FULL) cnt = 2;
+      if (i == B_SREADY || i == B_DSEMPTY) cnt = 4 * Cfg::HALVES;
+      if (i >= B_KREADY0 && i <= B_KREADY2) cnt = KSplit<D, FULL>::ARRIVALS;
       // φ(Q) warps: 8 for D = 128 (the state warps), 4 for D = 64
-      if (i == B_QREADY || i == B_QZREADY) cnt = 4 * Cfg::HALVES;
+      if (i == B_QREADY) cnt = 4 * Cfg::HALVES;
       // centered: raw Q tiles are released by the φ(Q) warps
       if ((i == B_QEMPTY0 || i == B_QEMPTY1) && cen) cnt = 4 * Cfg::HALVES;
       mbar_init(&x.bar[i], cnt);
@@ -765,8 +857,9 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   if (warp == 2) {
     uint32_t* ones = reinterpret_cast<uint32_t*>(x.sm + Cfg::oONES);
     for (int i = lane; i < 32; i += 32) ones[i] = 0x3F803F80u;   // bf16 1.0 pairs
-    float* qzb = reinterpret_cast<float*>(x.sm + Cfg::oQZ);
-    for (int i = lane; i < kC; i += 32) qzb[i] = 0.f;
+    // z operand and its read-past bytes (columns never read, kept finite)
+    uint32_t* zw = reinterpret_cast<uint32_t*>(x.sm + Cfg::oZB);
+    for (int i = lane; i < (2 * D + 128) / 4; i += 32) zw[i] = 0u;
     fence_proxy_async_smem();
   }
   if (warp == 3) {
@@ -825,7 +918,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int64_t BH, int64_t n, in
 
 template <int D>
 cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
-                   float* tot_state, float* tot_z, const SegmentPlan& plan) {
+                   const SegmentPlan& plan) {
   using Cfg = TcCfg<D>;
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return e;
@@ -850,17 +943,19 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
   p.ws_state = ws_state;
   p.ws_z = ws_z;
   p.status = a.status;
-  const dim3 grid((unsigned)plan.nseg, (unsigned)BH);
+  // the last segment's CTA of the full launch writes the final state
+  p.fin_state = a.mu_out;
+  p.fin_z = a.nu_out;
   if (plan.nseg > 1) {
-    tc_forward_kernel<D, false><<<grid, kThreadsTc, Cfg::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
+    // aggregates of segments 0 … nseg−2 (nothing follows the last one)
+    const dim3 grid_state((unsigned)(plan.nseg - 1), (unsigned)BH);
+    tc_forward_kernel<D, false><<<grid_state, kThreadsTc, Cfg::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
     count_launches(1);
-    e = segment_scan(ws_state, ws_z, tot_state, tot_z, BH, a.H, plan.nseg, plan.seg_len, a.n, D, D,
-                     a.decay, stream);
+    e = segment_scan(ws_state, ws_z, nullptr, nullptr, BH, a.H, plan.nseg, plan.nseg - 1,
+                     plan.seg_len, a.n, D, D, a.decay, stream);
     if (e != cudaSuccess) return e;
-  } else {
-    p.fin_state = a.mu_out;
-    p.fin_z = a.nu_out;
   }
+  const dim3 grid((unsigned)plan.nseg, (unsigned)BH);
   tc_forward_kernel<D, true><<<grid, kThreadsTc, Cfg::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
   count_launches(1);
   return cudaGetLastError();
@@ -876,8 +971,10 @@ int64_t tc_segment_granule() { return kC; }
 
 cudaError_t tc_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
                        float* tot_state, float* tot_z, const SegmentPlan& plan) {
-  if (a.d == 128) return run_tc<128>(a, stream, ws_state, ws_z, tot_state, tot_z, plan);
-  if (a.d == 64) return run_tc<64>(a, stream, ws_state, ws_z, tot_state, tot_z, plan);
+  (void)tot_state;   // causal only: the final state goes straight to a.mu_out
+  (void)tot_z;
+  if (a.d == 128) return run_tc<128>(a, stream, ws_state, ws_z, plan);
+  if (a.d == 64) return run_tc<64>(a, stream, ws_state, ws_z, plan);
   return cudaErrorInvalidValue;
 }
 

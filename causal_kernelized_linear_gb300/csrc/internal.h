@@ -64,9 +64,12 @@ cudaError_t tc_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state, f
                        float* tot_state, float* tot_z, const SegmentPlan& plan);
 
 // Exclusive decayed prefix over the per-segment aggregates of every head, in
-// place, plus the inclusive total (final state) when tot_state != nullptr.
+// place.  Only the first nagg aggregates are read (nagg = nseg − 1 when the
+// last segment's aggregate was not computed: the exclusive prefixes do not
+// need it); the inclusive total (final state) is written when tot_state !=
+// nullptr and nagg == nseg.
 cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* tot_z,
-                         int64_t BH, int64_t H, int nseg, int64_t seg_len, int64_t n,
+                         int64_t BH, int64_t H, int nseg, int nagg, int64_t seg_len, int64_t n,
                          int dp, int d, const float* decay, cudaStream_t stream);
 
 // la_forward with a fixed workspace of ws_floats floats, fetched through

@@ -170,6 +170,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
+// Prefetch of a 3-D tile into L2 (no shared memory, no completion
+// signal); out-of-range parts of the box are ignored.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // 2-D tiled load into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, uint64_t* bar, int x,
                                             int y) {
@@ -348,6 +356,36 @@ __device__ __forceinline__ float bf16lo_to_f32(uint32_t x) { return __uint_as_fl
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t x) {
   return __uint_as_float(x & 0xFFFF0000u);
 }
+
+// Packed bf16 pair arithmetic (two lanes per 32-bit register, round to nearest even).
+__device__ __forceinline__ uint32_t min_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// 2^x per lane (hardware approximation, subnormal results flushed to zero).
+__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t a) {
+  uint32_t d;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+// The same bf16 value in both lanes.
+__device__ __forceinline__ uint32_t splat_bf16x2(float x) { return pack_bf16x2(x, x); }
 
 }  // namespace tc
 }  // namespace la
