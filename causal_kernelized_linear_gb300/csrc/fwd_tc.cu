@@ -26,19 +26,24 @@
 //
 // One CTA per (segment, head), 16 warps:
 //   warp 0        TMA producer
-//   warp 1        tcgen05 MMA issuer, TMEM owner
+//   warp 1        tcgen05 MMA issuer for the output products, TMEM owner
+//   warp 2        tcgen05 MMA issuer for the state products
 //   warps 4–7     masked P; epilogue o = num/den stored row by row
 //                 (state-only launch: a share of φ(K))
-//   warps 8–15    φ(K) → K'' (and K'); the state update (fp32 state in TMEM);
-//                 φ(Q) → Q'' in TMEM (and Q'), one column half per warpgroup
-//                 (d = 64: warps 12–15 compute φ(Q), or a share of φ(K))
+//   warps 8–15    φ(K) → K'' (and K') one chunk ahead; the state update (fp32
+//                 state in TMEM); φ(Q) → Q'' in TMEM (and Q'); one column
+//                 half per warpgroup (d = 64: warps 8–11 all columns, warps
+//                 12–15 compute φ(Q), or in the state-only launch a share of φ(K))
 // tcgen05 products: scores = Q''K''ᵀ (or Q'K'ᵀ), ΔS = K''ᵀV, Δz = K''ᵀ1,
 // num = Q''S + P·V, den = Q''z + P·1 — fp32 accumulators in TMEM; S and z
 // enter the products as bf16 operands.
 // Long sequences are split into segments: a state-only launch of this kernel
-// computes the decayed aggregate of every segment but the last, segment_scan
-// turns them into the states entering each segment, and the full launch
-// produces o (and, from the last segment, the final state).
+// computes the decayed aggregate of every segment but the last; the full
+// launch combines the aggregates before each segment into its entering state
+// and produces o (and, from the last segment, the final state).  The full
+// launch is a programmatic dependent of the state-only one: it starts on the
+// SMs the state-only launch leaves free (and as its CTAs finish), and only
+// the reads of the aggregates wait for it to complete.
 // Every wait is bounded in time: on expiry the kernel records LA_ERR_TIMEOUT
 // in the device status word, stops issuing work, drains what it issued and
 // frees its TMEM.
@@ -152,16 +157,9 @@ __device__ __forceinline__ uint32_t sw_chunk(int rows, int row, int half, int j)
   return (uint32_t)(half * rows * 128 + row * 128 + ((j ^ (row & 7)) << 4));
 }
 
-// φ(x) = elu(x) + 1 = max(x, 0) + exp(min(x, 0)), written without a branch
-// (x + 1 for x > 0 since exp(0) = 1 exactly; e^x otherwise) so that warps do
-// not diverge on the sign of each element.  The fast exponential's few-ulp
-// error is far below the bf16 precision the result is rounded to.
-__device__ __forceinline__ float elu1_fast(float x) {
-  return fmaxf(x, 0.f) + __expf(fminf(x, 0.f));
-}
-
-// The same φ on a pair of bf16 values in packed bf16 arithmetic:
-// max(x, 0) + 2^(min(x, 0)·log2 e).  The result is bf16 (the precision the
+// φ(x) = elu(x) + 1 on a pair of bf16 values in packed bf16 arithmetic,
+// without a branch: max(x, 0) + 2^(min(x, 0)·log2 e) (x + 1 for x > 0 since
+// 2^0 = 1 exactly; e^x otherwise).  The result is bf16 (the precision the
 // tensor-core operand is rounded to anyway); the bf16 rounding of the
 // exponent argument and of log2 e adds an error of at most 1.3 % for
 // x ≥ −3 (3 % for x ≥ −6), on the small e^x branch only — the x + 1 branch
@@ -184,13 +182,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* s
                                           volatile int* abort_flag) {
   const bool ok = mbar_wait(bar, parity, status, abort_flag);
   return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
-  f[0] = bf16lo_to_f32(u.x); f[1] = bf16hi_to_f32(u.x);
-  f[2] = bf16lo_to_f32(u.y); f[3] = bf16hi_to_f32(u.y);
-  f[4] = bf16lo_to_f32(u.z); f[5] = bf16hi_to_f32(u.z);
-  f[6] = bf16lo_to_f32(u.w); f[7] = bf16hi_to_f32(u.w);
 }
 
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
@@ -426,7 +417,66 @@ __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, in
   return true;
 }
 
-// Warps 4–7: masked P and the epilogue.  Thread r owns row / TMEM lane r.
+// φ(K) of chunk c for the 16-byte column chunks [j0, j1) of token row r →
+// K'' = gs·φ(k) (rows ≥ cs get weight 0), written in place into the K tile
+// except for the general full kernel, which keeps K' = m·φ(k) in place and
+// writes K'' into its own tile.  φ is computed for every row so that no
+// per-element branch splits the warp.  Signals k_ready for the warp.
+template <int D, bool FULL, bool CEN>
+__device__ __forceinline__ bool phi_k_chunk(const Ctx& x, int c, int r, int j0, int j1, int lane,
+                                            float k_scale_cen) {
+  using L = Layout<D, FULL, CEN>;
+  uint64_t* bar = x.bar;
+  int* st = x.status;
+  volatile int* ab = x.abort_flag;
+  const int ks = c % L::KST;
+  const int cs = (int)min((int64_t)kC, x.t_end - (x.t_begin + (int64_t)c * kC));
+  if (!warp_wait(&bar[B_KFULL0 + ks], (c / L::KST) & 1, st, ab)) return false;
+  if (!L::K_IN_PLACE && c >= 1 && !warp_wait(&bar[B_KPEMPTY], (c - 1) & 1, st, ab)) return false;
+  const bool live = r < cs;
+  const uint32_t m2 = live ? 0x3F803F80u : 0u;   // bf16 1.0 / 0.0 pairs
+  const uint32_t g2 =
+      live ? splat_bf16x2(CEN ? k_scale_cen * lazy_sigma(x, c) : x.pw[max(cs - 1 - r, 0)]) : 0u;
+  uint8_t* kt = x.sm + L::k_off(ks);
+  uint8_t* kpp = x.sm + L::kpp_off(ks);
+#pragma unroll 4
+  for (int jj = j0; jj < j1; ++jj) {
+    const uint32_t off = sw_chunk(kC, r, jj >> 3, jj & 7);
+    uint4 u = *reinterpret_cast<const uint4*>(kt + off);
+    u.x = elu1_bf16x2(u.x); u.y = elu1_bf16x2(u.y);
+    u.z = elu1_bf16x2(u.z); u.w = elu1_bf16x2(u.w);
+    if (!L::K_IN_PLACE)
+      *reinterpret_cast<uint4*>(kt + off) =
+          make_uint4(mul_bf16x2(u.x, m2), mul_bf16x2(u.y, m2), mul_bf16x2(u.z, m2), mul_bf16x2(u.w, m2));
+    *reinterpret_cast<uint4*>(kpp + off) =
+        make_uint4(mul_bf16x2(u.x, g2), mul_bf16x2(u.y, g2), mul_bf16x2(u.z, g2), mul_bf16x2(u.w, g2));
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bar[B_KREADY0 + ks]);
+  return true;
+}
+
+// φ(K) column ranges (16-byte chunks of a row, 8 per 64 columns) per
+// warpgroup wg.  Full launch: the state warpgroups, one 64-column half each.
+// State-only launch: the otherwise idle warpgroups take a share — d = 128:
+// warps 4–7 chunks 0–7, the state warpgroups 8–11 and 12–15; d = 64: warps
+// 4–7 chunks 0–2, warps 12–15 chunks 3–5, the state warps 6–7.
+template <int D, bool FULL>
+struct KSplit {
+  __device__ static void range(int wg, int& j0, int& j1) {
+    if (FULL) {
+      j0 = (wg - 2) * 8; j1 = j0 + 8;
+    } else if (D == 128) {
+      j0 = wg == 1 ? 0 : (wg == 2 ? 8 : 12); j1 = wg == 1 ? 8 : (wg == 2 ? 12 : 16);
+    } else {
+      j0 = wg == 1 ? 0 : (wg == 3 ? 3 : 6); j1 = wg == 1 ? 3 : (wg == 3 ? 6 : 8);
+    }
+  }
+  static constexpr int ARRIVALS = FULL ? 4 * TcCfg<D>::HALVES : 12;
+};
+
+// Warps 4–7: masked P and the epilogue.  Thread r owns token row / TMEM lane r.
 template <int D, bool CEN>
 __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int64_t p_n, int warp,
                                           int lane) {
@@ -440,13 +490,14 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
   const int wq = warp - 4;                        // lane quarter
   const uint32_t lane_base = (uint32_t)wq * 32;
   for (int c = 0; c < x.nchunks; ++c) {
-    const int vs = c % L::VST;
     // ---- P: causal mask (and, general folding, the decay w·a^{t−s})
     if (!warp_wait(&bar[B_SCORES], c & 1, st, ab)) break;
     tc_fence_after();
     // 32-column blocks b: b > wq lies above the diagonal for the whole warp
     // (zeros, scores not read), b < wq below it (no mask), b == wq straddles it.
-#pragma unroll
+    // Loops over blocks and output columns stay rolled: the roles of this
+    // kernel share each SM's instruction cache.
+#pragma unroll 1
     for (int b = 0; b < 4; ++b) {
       uint32_t pk[16];
       if (b > wq) {
@@ -505,7 +556,7 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
     const int64_t row = x.t_begin + (int64_t)c * kC + r;
     const bool valid = row < x.t_end;
     uint4* orow = reinterpret_cast<uint4*>(out + (x.bh * p_n + (valid ? row : 0)) * D);
-#pragma unroll
+#pragma unroll 1
     for (int j0 = 0; j0 < D; j0 += 32) {
       uint32_t nv[32];
       tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TN + j0), nv);
@@ -525,71 +576,9 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
 }
 
 
-// φ(K) of chunk c for the 16-byte column chunks [j0, j1) of token row r →
-// K'' = gs·φ(k) (rows ≥ cs get weight 0), written in place into the K tile
-// except for the general full kernel, which keeps K' = m·φ(k) in place and
-// writes K'' into its own tile.  φ is computed for every row so that no
-// per-element branch splits the warp.  Signals k_ready for the warp.
-template <int D, bool FULL, bool CEN>
-__device__ __forceinline__ bool phi_k_chunk(const Ctx& x, int c, int r, int j0, int j1, int lane,
-                                            float k_scale_cen) {
-  using L = Layout<D, FULL, CEN>;
-  uint64_t* bar = x.bar;
-  int* st = x.status;
-  volatile int* ab = x.abort_flag;
-  const int ks = c % L::KST;
-  const int cs = (int)min((int64_t)kC, x.t_end - (x.t_begin + (int64_t)c * kC));
-  if (!warp_wait(&bar[B_KFULL0 + ks], (c / L::KST) & 1, st, ab)) return false;
-  if (!L::K_IN_PLACE && c >= 1 && !warp_wait(&bar[B_KPEMPTY], (c - 1) & 1, st, ab)) return false;
-  const bool live = r < cs;
-  const uint32_t m2 = live ? 0x3F803F80u : 0u;   // bf16 1.0 / 0.0 pairs
-  const uint32_t g2 =
-      live ? splat_bf16x2(CEN ? k_scale_cen * lazy_sigma(x, c) : x.pw[max(cs - 1 - r, 0)]) : 0u;
-  uint8_t* kt = x.sm + L::k_off(ks);
-  uint8_t* kpp = x.sm + L::kpp_off(ks);
-#pragma unroll
-  for (int t = 0; t < 8; ++t) {            // ranges are at most 8 chunks long
-    const int jj = j0 + t;
-    if (jj >= j1) break;
-    const uint32_t off = sw_chunk(kC, r, jj >> 3, jj & 7);
-    uint4 u = *reinterpret_cast<const uint4*>(kt + off);
-    u.x = elu1_bf16x2(u.x); u.y = elu1_bf16x2(u.y);
-    u.z = elu1_bf16x2(u.z); u.w = elu1_bf16x2(u.w);
-    if (!L::K_IN_PLACE)
-      *reinterpret_cast<uint4*>(kt + off) =
-          make_uint4(mul_bf16x2(u.x, m2), mul_bf16x2(u.y, m2), mul_bf16x2(u.z, m2), mul_bf16x2(u.w, m2));
-    *reinterpret_cast<uint4*>(kpp + off) =
-        make_uint4(mul_bf16x2(u.x, g2), mul_bf16x2(u.y, g2), mul_bf16x2(u.z, g2), mul_bf16x2(u.w, g2));
-  }
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&bar[B_KREADY0 + ks]);
-  return true;
-}
-
-// φ(K) column ranges (16-byte chunks of a row, 8 per 64 columns).  Full
-// launch: the state warpgroups split the columns by halves.  State-only
-// launch: the idle warpgroups take a share — d = 128: warps 4–7 chunks
-// 0–7, the state warpgroups 8–11 and 12–15; d = 64: warps 4–7 chunks 0–2,
-// warps 12–15 chunks 3–5, the state warps 6–7.
-template <int D, bool FULL>
-struct KSplit {
-  static constexpr int NJ = 8 * TcCfg<D>::HALVES;
-  __device__ static void range(int wg, int& j0, int& j1) {
-    if (FULL) {
-      j0 = (wg - 2) * 8; j1 = j0 + 8;
-    } else if (D == 128) {
-      j0 = wg == 1 ? 0 : (wg == 2 ? 8 : 12); j1 = wg == 1 ? 8 : (wg == 2 ? 12 : 16);
-    } else {
-      j0 = wg == 1 ? 0 : (wg == 3 ? 3 : 6); j1 = wg == 1 ? 3 : (wg == 3 ? 6 : 8);
-    }
-  }
-  static constexpr int ARRIVALS = FULL ? 4 * TcCfg<D>::HALVES : 12;
-};
-
-// Warps 8–15: φ(K), the fp32 state, and (D = 128) φ(Q).  Thread r: token row r
-// for φ(K) and φ(Q) (the columns of its half), feature row r / TMEM lane r
-// for the state (the 64 state columns of its half).
+// Warps 8–15: φ(K), the fp32 state, and (D = 128) φ(Q).  Thread r: token
+// row r for φ(K) and φ(Q) (the columns of its half), feature row r / TMEM
+// lane r for the state (the 64 state columns of its half).
 //
 // The fp32 state lives in TMEM (columns TD, and TZ for z), scaled so that
 // the state MMA accumulates onto it:
@@ -685,26 +674,43 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   KSplit<D, FULL>::range((warp - 8) / 4 + 2, kj0, kj1);
   auto phi_k = [&](int c) { return phi_k_chunk<D, FULL, CEN>(x, c, r, kj0, kj1, lane, k_scale_cen); };
 
-  // ---- initial state (S_in from the segment scan, or zero)
-  {
-    const bool have_in = FULL && p.nseg > 1;
-    const float* src = have_in ? p.ws_state + (x.bh * p.nseg + x.g) * (int64_t)(D * D) +
-                                     (int64_t)(srow ? r : 0) * D + half * 64
-                               : nullptr;
-    const float zin = (have_in && srow && half == 0)
-                          ? p.ws_z[(x.bh * p.nseg + x.g) * (int64_t)D + r] : 0.f;
+  // D = 128: these warps also compute φ(Q) for their half of the columns;
+  // φ(Q) of the first chunk does not depend on the state, so it goes first
+  constexpr bool DO_Q = FULL && Cfg::HALVES == 2;
+  const float a_row = CEN ? decay_pow_signed(a, r - 63) : decay_pow(a, r + 1);
+  bool ok = x.nchunks > 0 && phi_k(0);
+  if (DO_Q && ok) ok = phi_q_half<D, CEN>(x, 0, half, r, lane, lane_base, a_row);
+
+  // ---- initial state: S_in = Σ_{j<g} a^{L·(g−1−j)}·A_j over the aggregates
+  // A_j of the earlier segments of this head (all of length L), written by
+  // the state-only launch that precedes this one — zero for the first segment
+  if (ok) {
+    const bool have_in = FULL && x.g > 0;
+    if (have_in) grid_dependency_wait();
+    const float aL = have_in ? decay_pow(a, p.seg_len) : 0.f;
+    const int64_t agg0 = x.bh * p.nseg;
+    float zin = 0.f;
+    if (have_in && srow && half == 0)
+      for (int j = 0; j < x.g; ++j) zin = aL * zin + p.ws_z[(agg0 + j) * D + r];
     const float alpha0 = CEN ? decay_pow_signed(a, 64) : 1.f;
     const float beta0 = CEN ? alpha0 : decay_pow(a, chunk_len(0));
     put_state([&](int hh, float* v) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0.f;
                 if (have_in && srow) {
+                  const float* src = p.ws_state + agg0 * (int64_t)(D * D) + r * D + half * 64 + hh * 32;
+#pragma unroll 2
+                  for (int j = 0; j < x.g; ++j) {
+                    const float4* s4 = reinterpret_cast<const float4*>(src + j * (int64_t)(D * D));
 #pragma unroll
-                  for (int j = 0; j < 32; j += 4) {
-                    const float4 t = *reinterpret_cast<const float4*>(src + hh * 32 + j);
-                    v[j] = t.x; v[j + 1] = t.y; v[j + 2] = t.z; v[j + 3] = t.w;
+                    for (int e = 0; e < 8; ++e) {
+                      const float4 t = s4[e];
+                      v[4 * e] = aL * v[4 * e] + t.x;
+                      v[4 * e + 1] = aL * v[4 * e + 1] + t.y;
+                      v[4 * e + 2] = aL * v[4 * e + 2] + t.z;
+                      v[4 * e + 3] = aL * v[4 * e + 3] + t.w;
+                    }
                   }
-                } else {
-#pragma unroll
-                  for (int j = 0; j < 32; ++j) v[j] = 0.f;
                 }
               },
               zin, alpha0, beta0, 1.f, FULL, true, false);
@@ -714,11 +720,6 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
     }
   }
 
-  // D = 128: these warps also compute φ(Q) for their half of the columns
-  constexpr bool DO_Q = FULL && Cfg::HALVES == 2;
-  const float a_row = CEN ? decay_pow_signed(a, r - 63) : decay_pow(a, r + 1);
-  bool ok = x.nchunks > 0 && phi_k(0);
-  if (DO_Q && ok) ok = phi_q_half<D, CEN>(x, 0, half, r, lane, lane_base, a_row);
   for (int c = 0; ok && c < x.nchunks; ++c) {
     if (c + 1 < x.nchunks && !phi_k(c + 1)) break;
     // ---- state update from the accumulated TMEM value v
@@ -820,8 +821,12 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  x.g = blockIdx.x;
-  x.bh = blockIdx.y;
+  // the full launch that depends on this state-only one may start now
+  if (!FULL) grid_dependents_launch();
+  // grid (heads, segments): the CTAs of the first segments, which need no
+  // aggregate, come first in launch order
+  x.bh = blockIdx.x;
+  x.g = blockIdx.y;
   x.t_begin = (int64_t)x.g * p.seg_len;
   x.t_end = min(p.n, x.t_begin + p.seg_len);
   x.nchunks = (int)((x.t_end - x.t_begin + kC - 1) / kC);
@@ -884,6 +889,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     tc_fence_after();
     tmem_dealloc(x.tmem, Cfg::TMEM_COLS);
   }
+  // a dependent full launch completes only after the launch it depends on
+  if (FULL) grid_dependency_wait();
 }
 
 // ------------------------------------------------------------------ host side
@@ -948,17 +955,27 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
   p.fin_z = a.nu_out;
   if (plan.nseg > 1) {
     // aggregates of segments 0 … nseg−2 (nothing follows the last one)
-    const dim3 grid_state((unsigned)(plan.nseg - 1), (unsigned)BH);
+    const dim3 grid_state((unsigned)BH, (unsigned)(plan.nseg - 1));
     tc_forward_kernel<D, false><<<grid_state, kThreadsTc, Cfg::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
     count_launches(1);
-    e = segment_scan(ws_state, ws_z, nullptr, nullptr, BH, a.H, plan.nseg, plan.nseg - 1,
-                     plan.seg_len, a.n, D, D, a.decay, stream);
-    if (e != cudaSuccess) return e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  const dim3 grid((unsigned)plan.nseg, (unsigned)BH);
-  tc_forward_kernel<D, true><<<grid, kThreadsTc, Cfg::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
+  // The full launch overlaps the state-only one only when it directly
+  // follows it: it reads q, k, v before waiting, so it must never overlap a
+  // caller's kernel.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)BH, (unsigned)plan.nseg);
+  cfg.blockDim = dim3(kThreadsTc);
+  cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = plan.nseg > 1 ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, tc_forward_kernel<D, true>, mq, mk, mv, p);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace

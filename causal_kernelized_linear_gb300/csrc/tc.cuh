@@ -68,11 +68,11 @@ constexpr int kStatusTimeout = 4;
 // Bounded wait on the phase with the given parity.  Gives up after
 // `limit_ns` nanoseconds of wall time: records a timeout in *status (first
 // writer wins), sets *abort_flag for the CTA and returns false.  Returns
-// false immediately if the CTA is already aborting.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
-                                          volatile int* abort_flag,
-                                          uint64_t limit_ns = 2000000000ull) {
-  if (mbar_try_wait(bar, parity)) return true;
+// false immediately if the CTA is already aborting.  The polling loop is
+// kept out of line so that the many call sites stay small in the
+// instruction cache; only the first probe is inlined.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, int* status,
+                                                   volatile int* abort_flag, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -87,11 +87,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          volatile int* abort_flag,
+                                          uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, status, abort_flag, limit_ns);
+}
+
 // Waits for a phase without regard to the abort flag, for at most limit_ns:
 // used while draining copies and MMAs that are already in flight (they
 // complete on their own).  Returns false if the limit expired.
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
-                                                uint64_t limit_ns = 500000000ull) {
+static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
+                                                    uint64_t limit_ns = 500000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -168,6 +175,17 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+
+// Programmatic dependent launch: let the grid launched after this one (with
+// programmatic stream serialization) start, and wait until the grid this
+// one depends on has completed with its memory operations visible.  Both
+// are no-ops without such a launch relation.
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Prefetch of a 3-D tile into L2 (no shared memory, no completion
