@@ -52,9 +52,6 @@
 #include "tc.cuh"
 
 #include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
 
 namespace la {
 namespace {
@@ -151,12 +148,6 @@ struct TcParams {
   int* status;
 };
 
-// 16-byte chunk j (8 bf16, columns h*64 + 8j …) of row `row` in a tile stored
-// as column halves of [rows × 64] with the 128-byte swizzle (TMA layout).
-__device__ __forceinline__ uint32_t sw_chunk(int rows, int row, int half, int j) {
-  return (uint32_t)(half * rows * 128 + row * 128 + ((j ^ (row & 7)) << 4));
-}
-
 // φ(x) = elu(x) + 1 on a pair of bf16 values in packed bf16 arithmetic,
 // without a branch: max(x, 0) + 2^(min(x, 0)·log2 e) (x + 1 for x > 0 since
 // 2^0 = 1 exactly; e^x otherwise).  The result is bf16 (the precision the
@@ -173,20 +164,6 @@ __device__ __forceinline__ uint32_t elu1_bf16x2(uint32_t x) {
 // a^e for integer e of either sign (a > 0, or e ≥ 0).
 __device__ __forceinline__ float decay_pow_signed(float a, int e) {
   return e == 0 ? 1.f : powf(a, (float)e);
-}
-
-// Every lane of the warp waits (bounded); the warp then agrees on the
-// outcome so that control flow — and the .sync.aligned tcgen05 operations
-// after it — stays warp-uniform even if the limit expires mid-wait.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status,
-                                          volatile int* abort_flag) {
-  const bool ok = mbar_wait(bar, parity, status, abort_flag);
-  return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                    pack_bf16x2(f[6], f[7]));
 }
 
 struct Ctx {
@@ -895,45 +872,16 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-cudaError_t get_encoder() {
-  std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  return g_encode ? cudaSuccess : cudaErrorNotSupported;
-}
-
-// [BH, n, D] bf16 viewed as a 3-D tensor (D innermost), box 64 × 128 × 1 with
-// the 128-byte swizzle.  Rows past n read as zero.
-cudaError_t make_map(CUtensorMap* m, const void* base, int64_t BH, int64_t n, int D) {
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)n, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)n * D * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int D>
 cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
                    const SegmentPlan& plan) {
   using Cfg = TcCfg<D>;
-  cudaError_t e = get_encoder();
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   const int64_t BH = a.B * a.H;
   CUtensorMap mq, mk, mv;
-  if ((e = make_map(&mq, a.q, BH, a.n, D)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, a.k, BH, a.n, D)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, a.v, BH, a.n, D)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mq, a.q, BH, a.n, D, kC)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mk, a.k, BH, a.n, D, kC)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mv, a.v, BH, a.n, D, kC)) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc_forward_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_ALLOC);
   if (e != cudaSuccess) return e;

@@ -1,0 +1,740 @@
+// Tensor-core (tcgen05 + TMA + TMEM) chunked forward of kernelized linear
+// attention with the Performer positive random feature map, bf16 inputs,
+// fp32 state, d = 64, m ∈ {128, 256} features, no decay (a = 1).
+//
+// Method ("Efficient Transformers II" §2.1: φ(x) = exp(xω − ½‖x‖²)/√m;
+// "Efficient Transformers I" eq (6)–(9): the running sums μ, ν and the
+// causal readout o_j = q'_j·μ_j / q'_j·ν_j).  Per head and 128-token chunk
+// (local t, s; cs valid rows) with state (S, z) at the chunk start:
+//   U = X·ω (the projection, on the tensor core, X = the raw q or k rows)
+//   φ(x)_i = 2^(u_i·log2 e − ½‖x‖²·log2 e − ½·log2 m)       (fp32 exponent)
+//   causal:     P_ts = q'_t·k'_s for s ≤ t, else 0
+//               num_t = Σ_s P_ts v_s + q'_t·S,   den_t = Σ_s P_ts + q'_t·z
+//   non-causal: num_t = q'_t·S_n,   den_t = q'_t·z_n   (S_n, z_n: the sums
+//               over the whole sequence, eq (6) regrouped as eq (9))
+//   S ← S + Σ_s k'_sᵀ v_s,   z ← z + Σ_s k'_s
+//
+// Launch modes (one CTA per (head, segment), 16 warps):
+//   state    the aggregate (S, z) of one segment, from zero
+//   causal   o over one segment, starting from the sum of the aggregates of
+//            the segments before it (the last segment also writes the final
+//            state)
+//   readout  o = q'·S_n / q'·z_n over one segment, S_n the sum of all the
+//            aggregates (the first segment also writes S_n as the final state)
+// A causal or readout launch that follows a state launch is its programmatic
+// dependent: it starts while the state launch drains, and only the reads of
+// the aggregates wait for it.
+//
+// Roles:
+//   warp 0       TMA producer (ω once; raw q, k, v tiles in two-stage rings)
+//   warp 1       tcgen05 MMA issuer, TMEM owner
+//   warps 4–7    initial state; state operand tile per chunk; masked P;
+//                epilogue o = num/den stored row by row; final state
+//   warps 8–15   φ: each 64-feature projection block of U comes through one
+//                of two TMEM buffers; warps 8–11 take its first 32 features,
+//                warps 12–15 the other 32; φ(K) goes to shared memory (the
+//                operand of the scores and state products), φ(Q) to TMEM
+// tcgen05 products: U = X·ω (M 128, N 64, K 64), scores = φ(Q)·φ(K)ᵀ
+// (K = m), ΔS = φ(K)ᵀV and Δz = φ(K)ᵀ1 per 128-feature block, num = φ(Q)·S,
+// den = φ(Q)·z, num += P·V, den += P·1.  Every wait is bounded in time and
+// reports LA_ERR_TIMEOUT through the device status word.
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace la {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 128;        // tokens per chunk
+constexpr int kD = 64;         // input and value width
+constexpr int kThreads = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum Mode { kState = 0, kCausal = 1, kReadout = 2 };
+
+template <int DP>
+struct PCfg {
+  static constexpr int NB = DP / 64;             // 64-feature blocks
+  static constexpr int MB = DP / 128;            // 128-feature blocks (state lane blocks)
+  static constexpr int TILE = kC * kD * 2;       // [128 × 64] bf16 = 16 KB
+  static constexpr int WATOM = 64 * 128;         // ω block [64 (d) × 64 (features)] = 8 KB
+  // shared memory (offsets from a 1024-aligned base)
+  static constexpr int oW = 0;                   // ω, NB blocks
+  static constexpr int oQ0 = oW + NB * WATOM;    // raw q stages
+  static constexpr int oQ1 = oQ0 + TILE;
+  static constexpr int oK0 = oQ1 + TILE;         // raw k stages
+  static constexpr int oK1 = oK0 + TILE;
+  static constexpr int oV0 = oK1 + TILE;         // v stages
+  static constexpr int oV1 = oV0 + TILE;
+  static constexpr int oKP = oV1 + TILE;         // φ(K): NB column blocks of [128 × 64]
+  static constexpr int oS = oKP + NB * TILE;     // state operand, bf16 [DP × 64]
+  static constexpr int oONES = oS + DP * kD * 2; // 8×8 bf16 ones (every core matrix aliases it)
+  static constexpr int oZB = oONES + 128;        // z operand bf16 [DP] + 112 read-past bytes
+  static constexpr int oBAR = oZB + 2 * DP + 128;
+  static constexpr int NBAR = 32;
+  static constexpr int oMISC = oBAR + NBAR * 8;  // tmem slot, abort flag
+  static constexpr int BYTES = oMISC + 16;
+  static constexpr int SMEM_ALLOC = (BYTES + 1024 > 118 * 1024) ? BYTES + 1024 : 118 * 1024;
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  // tensor memory columns
+  static constexpr uint32_t TST = 0;             // S: MB blocks of 64 columns (lanes = features)
+  static constexpr uint32_t TZ = 128;            // z: MB blocks of 16 columns (column 0 used)
+  static constexpr uint32_t TN = 160;            // numerator [128 × 64]
+  static constexpr uint32_t TR = 224;            // denominator (16 columns, column 0 used)
+  static constexpr uint32_t TS = 256;            // scores / P; two 64-column projection buffers
+  static constexpr uint32_t TQ = 384;            // φ(Q) as bf16 pairs, DP/2 columns
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(TST + MB * 64 <= TZ && TZ + MB * 16 <= TN && TQ + DP / 2 <= TMEM_COLS, "TMEM");
+};
+
+enum {
+  B_W = 0,
+  B_QFULL0, B_QFULL1, B_QEMPTY0, B_QEMPTY1,
+  B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1,
+  B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1,
+  B_PJFULL0, B_PJFULL1, B_PJEMPTY0, B_PJEMPTY1,
+  B_KREADY, B_KPEMPTY, B_QREADY, B_QPEMPTY,
+  B_SCORES, B_PREADY, B_NUMFULL, B_NUMEMPTY,
+  B_DSFULL, B_SCONV, B_SREADY, B_SEMPTY, B_MMADONE, B_COUNT
+};
+static_assert(B_COUNT <= PCfg<128>::NBAR, "barrier slots");
+
+struct PParams {
+  __nv_bfloat16* out;      // [BH, n, 64]
+  int64_t n, seg_len;
+  int nseg;
+  float* ws_state;         // [BH][nseg][DP·64] segment aggregates
+  float* ws_z;             // [BH][nseg][DP]
+  float* fin_state;        // final state [BH][DP·64] or nullptr
+  float* fin_z;
+  float half_log2m;        // ½·log2 m
+  int* status;
+};
+
+struct PCtx {
+  uint8_t* sm;
+  uint32_t sbase;
+  uint64_t* bar;
+  volatile int* abort_flag;
+  uint32_t tmem;
+  int* status;
+  int64_t bh, t_begin, t_end;
+  int g, nchunks;
+};
+
+template <int MODE> struct Loads {
+  static constexpr bool Q = MODE != kState;
+  static constexpr bool K = MODE != kReadout;
+  static constexpr bool V = MODE != kReadout;
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------------ roles
+
+template <int DP, int MODE>
+__device__ __forceinline__ void role_producer(const PCtx& x, const CUtensorMap* mq,
+                                              const CUtensorMap* mk, const CUtensorMap* mv,
+                                              const CUtensorMap* mw) {
+  using Cfg = PCfg<DP>;
+  using LD = Loads<MODE>;
+  uint64_t* bar = x.bar;
+  mbar_arrive_expect_tx(&bar[B_W], Cfg::NB * Cfg::WATOM);
+  for (int f = 0; f < Cfg::NB; ++f) tma_load_2d(x.sm + Cfg::oW + f * Cfg::WATOM, mw, &bar[B_W], 64 * f, 0);
+  int last[3] = {-1, -1, -1};   // last chunk loaded per operand (k, q, v)
+  auto load = [&](const CUtensorMap* map, int off0, int off1, int full, int empty, int c, int y,
+                  int which) -> bool {
+    const int s = c & 1;
+    if (c >= 2 && !mbar_wait(&bar[empty + s], ((c - 2) >> 1) & 1, x.status, x.abort_flag))
+      return false;
+    mbar_arrive_expect_tx(&bar[full + s], Cfg::TILE);
+    tma_load_3d(x.sm + (s ? off1 : off0), map, &bar[full + s], 0, y, (int)x.bh);
+    last[which] = c;
+    return true;
+  };
+  for (int c = 0; c < x.nchunks && !*x.abort_flag; ++c) {
+    const int y = (int)(x.t_begin + (int64_t)c * kC);
+    if (LD::K && !load(mk, Cfg::oK0, Cfg::oK1, B_KFULL0, B_KEMPTY0, c, y, 0)) break;
+    if (LD::Q && !load(mq, Cfg::oQ0, Cfg::oQ1, B_QFULL0, B_QEMPTY0, c, y, 1)) break;
+    if (LD::V && !load(mv, Cfg::oV0, Cfg::oV1, B_VFULL0, B_VEMPTY0, c, y, 2)) break;
+  }
+  if (*x.abort_flag) {
+    // drain the loads still in flight before the CTA's shared memory goes away
+    mbar_wait_drain(&bar[B_W], 0);
+    const int full[3] = {B_KFULL0, B_QFULL0, B_VFULL0};
+    for (int w = 0; w < 3; ++w)
+      for (int c = max(0, last[w] - 1); c <= last[w]; ++c)
+        mbar_wait_drain(&bar[full[w] + (c & 1)], (c >> 1) & 1);
+  }
+}
+
+template <int DP, int MODE>
+__device__ __forceinline__ void role_mma(const PCtx& x) {
+  using Cfg = PCfg<DP>;
+  using LD = Loads<MODE>;
+  uint64_t* bar = x.bar;
+  const uint32_t tmem = x.tmem;
+  const uint32_t sb = x.sbase;
+  constexpr uint32_t idP = idesc_bf16_f32(128, 64, false, true);    // U = X·ω
+  constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);  // scores
+  constexpr uint32_t idD = idesc_bf16_f32(128, 64, true, true);     // ΔS block = φ(K)ᵀ V
+  constexpr uint32_t idZ = idesc_bf16_f32(128, 16, true, false);    // Δz block = φ(K)ᵀ 1
+  constexpr uint32_t idN = idesc_bf16_f32(128, 64, false, true);    // num (+)= A·{S, V}
+  constexpr uint32_t idR = idesc_bf16_f32(128, 16, false, false);   // den: φ(Q)·z, P·1
+  const uint64_t ones = smem_desc(sb + Cfg::oONES, 0, 0, kSwizzleNone);
+  int* st = x.status;
+  volatile int* ab = x.abort_flag;
+  bool ok = mbar_wait(&bar[B_W], 0, st, ab);
+  int pj = 0;   // projection steps issued
+  // U block f of the raw tile at sX → projection buffer pj & 1
+  auto project = [&](uint32_t sX, int f) -> bool {
+    const int b = pj & 1;
+    if (pj >= 2 && !mbar_wait(&bar[B_PJEMPTY0 + b], ((pj - 2) >> 1) & 1, st, ab)) return false;
+    tc_fence_after();
+    for (int k = 0; k < kD / 16; ++k)
+      mma_ss(tmem + Cfg::TS + 64 * b, smem_desc(sX + k * 32, 16, 1024, kSwizzle128B),
+             smem_desc(sb + Cfg::oW + f * Cfg::WATOM + k * 2048, Cfg::WATOM, 1024, kSwizzle128B),
+             idP, k > 0);
+    mma_commit(&bar[B_PJFULL0 + b]);
+    ++pj;
+    return true;
+  };
+  for (int c = 0; ok && c < x.nchunks; ++c) {
+    const int s = c & 1;
+    const uint32_t sQ = sb + (s ? Cfg::oQ1 : Cfg::oQ0);
+    const uint32_t sK = sb + (s ? Cfg::oK1 : Cfg::oK0);
+    const uint32_t sV = sb + (s ? Cfg::oV1 : Cfg::oV0);
+    const uint32_t sKP = sb + Cfg::oKP;
+    // the projection buffers alias the scores / P of the previous chunk
+    if (MODE == kCausal && c >= 1 && !mbar_wait(&bar[B_NUMFULL], (c - 1) & 1, st, ab)) break;
+    if (LD::K) {
+      if (!mbar_wait(&bar[B_KFULL0 + s], (c >> 1) & 1, st, ab)) break;
+      tc_fence_after();
+      for (int f = 0; ok && f < Cfg::NB; ++f) ok = project(sK, f);
+      if (!ok) break;
+      mma_commit(&bar[B_KEMPTY0 + s]);
+    }
+    if (LD::Q) {
+      if (!mbar_wait(&bar[B_QFULL0 + s], (c >> 1) & 1, st, ab)) break;
+      tc_fence_after();
+      for (int f = 0; ok && f < Cfg::NB; ++f) ok = project(sQ, f);
+      if (!ok) break;
+      mma_commit(&bar[B_QEMPTY0 + s]);
+    }
+    if (MODE == kCausal) {
+      // scores = φ(Q)·φ(K)ᵀ over the m features
+      if (!mbar_wait(&bar[B_KREADY], c & 1, st, ab)) break;
+      if (!mbar_wait(&bar[B_QREADY], c & 1, st, ab)) break;
+      tc_fence_after();
+      for (int k = 0; k < DP / 16; ++k) {
+        const uint32_t off = (k >> 2) * Cfg::TILE + (k & 3) * 32;
+        mma_ts(tmem + Cfg::TS, tmem + Cfg::TQ + k * 8,
+               smem_desc(sKP + off, 16, 1024, kSwizzle128B), idS, k > 0);
+      }
+      mma_commit(&bar[B_SCORES]);
+    }
+    if (LD::K) {
+      // ΔS = φ(K)ᵀV, Δz = φ(K)ᵀ1, accumulated onto the TMEM state
+      if (MODE != kCausal && !mbar_wait(&bar[B_KREADY], c & 1, st, ab)) break;
+      if (!mbar_wait(&bar[B_VFULL0 + s], (c >> 1) & 1, st, ab)) break;
+      if ((MODE == kCausal || c == 0) &&
+          !mbar_wait(&bar[B_SCONV], MODE == kCausal ? (c & 1) : 0, st, ab))
+        break;
+      tc_fence_after();
+      for (int mb = 0; mb < Cfg::MB; ++mb)
+        for (int k = 0; k < kC / 16; ++k) {
+          const uint64_t ad = smem_desc(sKP + mb * 2 * Cfg::TILE + k * 2048, Cfg::TILE, 1024,
+                                        kSwizzle128B);
+          mma_ss(tmem + Cfg::TST + 64 * mb, ad,
+                 smem_desc(sV + k * 2048, Cfg::TILE, 1024, kSwizzle128B), idD, 1);
+          mma_ss(tmem + Cfg::TZ + 16 * mb, ad, ones, idZ, 1);
+        }
+      mma_commit(&bar[B_DSFULL]);
+      mma_commit(&bar[B_KPEMPTY]);                 // φ(K) tile read by scores and ΔS
+      if (MODE == kState) mma_commit(&bar[B_VEMPTY0 + s]);
+    }
+    if (LD::Q) {
+      // num = φ(Q)·S ; den = φ(Q)·z
+      if ((MODE == kCausal || c == 0) &&
+          !mbar_wait(&bar[B_SREADY], MODE == kCausal ? (c & 1) : 0, st, ab))
+        break;
+      if (c >= 1 && !mbar_wait(&bar[B_NUMEMPTY], (c - 1) & 1, st, ab)) break;
+      tc_fence_after();
+      for (int k = 0; k < DP / 16; ++k) {
+        mma_ts(tmem + Cfg::TN, tmem + Cfg::TQ + k * 8,
+               smem_desc(sb + Cfg::oS + k * 2048, DP * 128, 1024, kSwizzle128B), idN, k > 0);
+        mma_ts(tmem + Cfg::TR, tmem + Cfg::TQ + k * 8,
+               smem_desc(sb + Cfg::oZB + k * 32, 16, 0, kSwizzleNone), idR, k > 0);
+      }
+      if (MODE == kCausal) mma_commit(&bar[B_SEMPTY]);
+      mma_commit(&bar[B_QPEMPTY]);                 // φ(Q) read by scores and num
+      if (MODE == kReadout) mma_commit(&bar[B_NUMFULL]);
+    }
+    if (MODE == kCausal) {
+      // num += P·V ; den += P·1
+      if (!mbar_wait(&bar[B_PREADY], c & 1, st, ab)) break;
+      tc_fence_after();
+      for (int k = 0; k < kC / 16; ++k) {
+        mma_ts(tmem + Cfg::TN, tmem + Cfg::TS + k * 8,
+               smem_desc(sV + k * 2048, Cfg::TILE, 1024, kSwizzle128B), idN, 1);
+        mma_ts(tmem + Cfg::TR, tmem + Cfg::TS + k * 8, ones, idR, 1);
+      }
+      mma_commit(&bar[B_NUMFULL]);
+      mma_commit(&bar[B_VEMPTY0 + s]);
+    }
+  }
+  // every issued MMA must finish before TMEM is released
+  mma_commit(&bar[B_MMADONE]);
+  mbar_wait_drain(&bar[B_MMADONE], 0);
+}
+
+// Warps 8–15: φ.  Thread r: token row / TMEM lane r; `half` selects 32 of
+// the 64 features of each projection block.
+template <int DP, int MODE>
+__device__ __forceinline__ void role_phi(const PCtx& x, const PParams& p, int warp, int lane) {
+  using Cfg = PCfg<DP>;
+  using LD = Loads<MODE>;
+  uint64_t* bar = x.bar;
+  int* st = x.status;
+  volatile int* ab = x.abort_flag;
+  const int half = (warp - 8) >> 2;
+  const int r = (warp & 3) * 32 + lane;
+  const uint32_t lane_base = (uint32_t)(warp & 3) * 32;
+  int pj = 0;
+  // ½‖x_r‖²·log2 e + ½·log2 m for row r of a raw tile (the exponent offset)
+  auto row_offset = [&](int off) -> float {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 u = lds128(x.sbase + off + sw_chunk(kC, r, 0, j));
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = bf16lo_to_f32(w[e]), hi = bf16hi_to_f32(w[e]);
+        ss = fmaf(lo, lo, ss);
+        ss = fmaf(hi, hi, ss);
+      }
+    }
+    return 0.5f * ss * kLog2e + p.half_log2m;
+  };
+  // one projection block: φ of 32 features of row r, zero for dead rows
+  auto step = [&](bool is_k, int f, float off, bool live) -> bool {
+    const int b = pj & 1;
+    if (!warp_wait(&bar[B_PJFULL0 + b], (pj >> 1) & 1, st, ab)) return false;
+    tc_fence_after();
+    uint32_t u[32];
+    tmem_ld32(tmem_addr(x.tmem, lane_base, Cfg::TS + 64 * b + 32 * half), u);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_PJEMPTY0 + b]);
+    ++pj;
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float a0 = ex2_approx(fmaf(__uint_as_float(u[2 * j]), kLog2e, -off));
+      const float a1 = ex2_approx(fmaf(__uint_as_float(u[2 * j + 1]), kLog2e, -off));
+      pk[j] = live ? pack_bf16x2(a0, a1) : 0u;
+    }
+    if (is_k) {
+      const uint32_t base = x.sbase + Cfg::oKP + f * Cfg::TILE;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        sts128(base + sw_chunk(kC, r, 0, 4 * half + q),
+               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
+    } else {
+      tmem_st16(tmem_addr(x.tmem, lane_base, Cfg::TQ + 32 * f + 16 * half), pk);
+    }
+    return true;
+  };
+  for (int c = 0; c < x.nchunks; ++c) {
+    const int s = c & 1;
+    const int cs = (int)min((int64_t)kC, x.t_end - (x.t_begin + (int64_t)c * kC));
+    if (LD::K) {
+      if (!warp_wait(&bar[B_KFULL0 + s], (c >> 1) & 1, st, ab)) return;
+      const float off = row_offset(s ? Cfg::oK1 : Cfg::oK0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_KEMPTY0 + s]);
+      // the φ(K) tile of the previous chunk must have been consumed
+      if (c >= 1 && !warp_wait(&bar[B_KPEMPTY], (c - 1) & 1, st, ab)) return;
+      for (int f = 0; f < Cfg::NB; ++f)
+        if (!step(true, f, off, r < cs)) return;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_KREADY]);
+    }
+    if (LD::Q) {
+      if (!warp_wait(&bar[B_QFULL0 + s], (c >> 1) & 1, st, ab)) return;
+      const float off = row_offset(s ? Cfg::oQ1 : Cfg::oQ0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_QEMPTY0 + s]);
+      if (c >= 1 && !warp_wait(&bar[B_QPEMPTY], (c - 1) & 1, st, ab)) return;
+      for (int f = 0; f < Cfg::NB; ++f)
+        if (!step(false, f, off, true)) return;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_QREADY]);
+    }
+  }
+}
+
+// Warps 4–7: thread r owns feature rows r and 128 + r of the state (TMEM
+// lane r of each 128-feature block) and token row / TMEM lane r of a chunk.
+template <int DP, int MODE>
+__device__ __forceinline__ void role_rows(const PCtx& x, const PParams& p, int warp, int lane) {
+  using Cfg = PCfg<DP>;
+  uint64_t* bar = x.bar;
+  const uint32_t tmem = x.tmem;
+  int* st = x.status;
+  volatile int* ab = x.abort_flag;
+  const int r = (warp - 4) * 32 + lane;
+  const int wq = warp - 4;
+  const uint32_t lane_base = (uint32_t)wq * 32;
+  const uint32_t stile = x.sbase + Cfg::oS;
+  __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(x.sm + Cfg::oZB);
+  const int64_t agg0 = x.bh * p.nseg;
+
+  // State row f = 128·mb + r is handled in two 32-column halves hh.
+  // bf16 operand: 32 values of state-tile row f (16-byte chunks 4hh … 4hh+3)
+  auto put_tile_half = [&](int f, int hh, const float* v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = v[8 * q + e];
+      sts128(stile + sw_chunk(DP, f, 0, 4 * hh + q), pack8(w));
+    }
+  };
+  auto write_half = [&](float* dst_S, int f, int hh, const float* v) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+      *reinterpret_cast<float4*>(dst_S + (int64_t)f * kD + 32 * hh + j) =
+          make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+  };
+  // the fp32 state of block mb from TMEM → `sink(f, hh, v)` per half; returns z
+  auto drain_state = [&](int mb, auto sink) -> float {
+    uint32_t zr = 0;
+    tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TZ + 16 * mb), zr);
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t u[32];
+      tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TST + 64 * mb + 32 * hh), u);
+      tmem_ld_wait();
+      sink(128 * mb + r, hh, reinterpret_cast<const float*>(u));
+    }
+    return __uint_as_float(zr);
+  };
+
+  // ---- initial state: the sum of the aggregates before this segment
+  // (causal), of all of them (readout), or zero (state)
+  {
+    const int nagg = MODE == kCausal ? x.g : (MODE == kReadout ? p.nseg : 0);
+    if (nagg > 0) grid_dependency_wait();
+    for (int mb = 0; mb < Cfg::MB; ++mb) {
+      const int f = 128 * mb + r;
+      float zf = 0.f;
+      for (int a = 0; a < nagg; ++a) zf += p.ws_z[(agg0 + a) * DP + f];
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        for (int a = 0; a < nagg; ++a) {
+          const float4* src = reinterpret_cast<const float4*>(
+              p.ws_state + (agg0 + a) * (int64_t)(DP * kD) + f * kD + 32 * hh);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 t = src[j];
+            v[4 * j] += t.x; v[4 * j + 1] += t.y; v[4 * j + 2] += t.z; v[4 * j + 3] += t.w;
+          }
+        }
+        if (MODE != kReadout)
+          tmem_st32(tmem_addr(tmem, lane_base, Cfg::TST + 64 * mb + 32 * hh),
+                    reinterpret_cast<const uint32_t*>(v));
+        if (MODE != kState) put_tile_half(f, hh, v);
+        if (MODE == kReadout && x.g == 0 && p.fin_state)
+          write_half(p.fin_state + x.bh * (int64_t)(DP * kD), f, hh, v);
+      }
+      if (MODE != kReadout) {
+        const uint32_t zo = __float_as_uint(zf);
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(
+                         tmem_addr(tmem, lane_base, Cfg::TZ + 16 * mb)),
+                     "r"(zo)
+                     : "memory");
+      }
+      if (MODE != kState) zb[f] = __float2bfloat16_rn(zf);
+      if (MODE == kReadout && x.g == 0 && p.fin_state) p.fin_z[x.bh * DP + f] = zf;
+    }
+    if (MODE != kReadout) tmem_st_wait();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&bar[B_SCONV]);
+      mbar_arrive(&bar[B_SREADY]);
+    }
+  }
+
+  if (MODE == kState) {
+    bool ok = true;
+    for (int c = 0; ok && c < x.nchunks; ++c) ok = warp_wait(&bar[B_DSFULL], c & 1, st, ab);
+    if (!ok) return;
+    tc_fence_after();
+    float* dS = p.ws_state + (agg0 + x.g) * (int64_t)(DP * kD);
+    for (int mb = 0; mb < Cfg::MB; ++mb) {
+      const float zf = drain_state(mb, [&](int f, int hh, const float* v) { write_half(dS, f, hh, v); });
+      p.ws_z[(agg0 + x.g) * DP + 128 * mb + r] = zf;
+    }
+    return;
+  }
+
+  for (int c = 0; c < x.nchunks; ++c) {
+    if (MODE == kCausal) {
+      if (c >= 1) {
+        // operand tile for chunk c: S_c, accumulated by ΔS of chunk c−1
+        if (!warp_wait(&bar[B_DSFULL], (c - 1) & 1, st, ab)) return;
+        if (!warp_wait(&bar[B_SEMPTY], (c - 1) & 1, st, ab)) return;
+        tc_fence_after();
+        for (int mb = 0; mb < Cfg::MB; ++mb) {
+          const float zf =
+              drain_state(mb, [&](int f, int hh, const float* v) { put_tile_half(f, hh, v); });
+          zb[128 * mb + r] = __float2bfloat16_rn(zf);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bar[B_SCONV]);
+          mbar_arrive(&bar[B_SREADY]);
+        }
+      }
+      // ---- P: causal mask of the scores
+      if (!warp_wait(&bar[B_SCORES], c & 1, st, ab)) return;
+      tc_fence_after();
+#pragma unroll 1
+      for (int b = 0; b < 4; ++b) {
+        uint32_t pk[16];
+        if (b > wq) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = 0u;
+        } else {
+          uint32_t sc[32];
+          tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TS + b * 32), sc);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int s0 = b * 32 + j;
+            const float p0 = (s0 <= r) ? __uint_as_float(sc[j]) : 0.f;
+            const float p1 = (s0 + 1 <= r) ? __uint_as_float(sc[j + 1]) : 0.f;
+            pk[j / 2] = pack_bf16x2(p0, p1);
+          }
+        }
+        tmem_st16(tmem_addr(tmem, lane_base, Cfg::TS + b * 16), pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_PREADY]);
+    }
+    // ---- epilogue: o = num / den → bf16, row r straight to global memory
+    if (!warp_wait(&bar[B_NUMFULL], c & 1, st, ab)) return;
+    tc_fence_after();
+    uint32_t den = 0;
+    tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TR), den);
+    tmem_ld_wait();
+    const float inv_den = 1.f / __uint_as_float(den);
+    const int64_t row = x.t_begin + (int64_t)c * kC + r;
+    const bool valid = row < x.t_end;
+    uint4* orow = reinterpret_cast<uint4*>(p.out + (x.bh * p.n + (valid ? row : 0)) * kD);
+#pragma unroll 1
+    for (int j0 = 0; j0 < kD; j0 += 32) {
+      uint32_t nv[32];
+      tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TN + j0), nv);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(nv[q8 * 8 + e]) * inv_den;
+        if (valid) __stcs(orow + (j0 + q8 * 8) / 8, pack8(f));
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_NUMEMPTY]);
+  }
+  // ---- final state of the sequence (causal, last segment)
+  if (MODE == kCausal && p.fin_state && x.g == p.nseg - 1) {
+    if (!warp_wait(&bar[B_DSFULL], (x.nchunks - 1) & 1, st, ab)) return;
+    tc_fence_after();
+    float* dS = p.fin_state + x.bh * (int64_t)(DP * kD);
+    for (int mb = 0; mb < Cfg::MB; ++mb) {
+      const float zf = drain_state(mb, [&](int f, int hh, const float* v) { write_half(dS, f, hh, v); });
+      p.fin_z[x.bh * DP + 128 * mb + r] = zf;
+    }
+  }
+}
+
+template <int DP, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+tcp_forward_kernel(const __grid_constant__ CUtensorMap map_q,
+                   const __grid_constant__ CUtensorMap map_k,
+                   const __grid_constant__ CUtensorMap map_v,
+                   const __grid_constant__ CUtensorMap map_w, const PParams p) {
+  using Cfg = PCfg<DP>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  PCtx x;
+  x.sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+  x.sbase = smem_u32(x.sm);
+  x.bar = reinterpret_cast<uint64_t*>(x.sm + Cfg::oBAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x.sm + Cfg::oMISC);
+  x.abort_flag = reinterpret_cast<volatile int*>(x.sm + Cfg::oMISC + 4);
+  x.status = p.status;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  // a launch that depends on this state launch may start now
+  if (MODE == kState) grid_dependents_launch();
+  // grid (heads, segments)
+  x.bh = blockIdx.x;
+  x.g = blockIdx.y;
+  x.t_begin = (int64_t)x.g * p.seg_len;
+  x.t_end = min(p.n, x.t_begin + p.seg_len);
+  x.nchunks = (int)((x.t_end - x.t_begin + kC - 1) / kC);
+
+  if (tid == 0) {
+    for (int i = 0; i < B_COUNT; ++i) {
+      uint32_t cnt = 1;
+      if (i == B_QEMPTY0 || i == B_QEMPTY1 || i == B_KEMPTY0 || i == B_KEMPTY1) cnt = 1 + 8;
+      if (i == B_PJEMPTY0 || i == B_PJEMPTY1 || i == B_KREADY || i == B_QREADY) cnt = 8;
+      if (i == B_PREADY || i == B_NUMEMPTY || i == B_SCONV || i == B_SREADY) cnt = 4;
+      mbar_init(&x.bar[i], cnt);
+    }
+    *x.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 2) {
+    uint32_t* ones = reinterpret_cast<uint32_t*>(x.sm + Cfg::oONES);
+    for (int i = lane; i < 32; i += 32) ones[i] = 0x3F803F80u;   // bf16 1.0 pairs
+    // z operand and its read-past bytes (columns never read, kept finite)
+    uint32_t* zw = reinterpret_cast<uint32_t*>(x.sm + Cfg::oZB);
+    for (int i = lane; i < (2 * DP + 128) / 4; i += 32) zw[i] = 0u;
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_w);
+    if (Loads<MODE>::Q) tma_prefetch_desc(&map_q);
+    if (Loads<MODE>::K) tma_prefetch_desc(&map_k);
+    if (Loads<MODE>::V) tma_prefetch_desc(&map_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  x.tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) role_producer<DP, MODE>(x, &map_q, &map_k, &map_v, &map_w);
+  } else if (warp == 1) {
+    if (lane == 0) role_mma<DP, MODE>(x);
+  } else if (warp >= 4 && warp < 8) {
+    role_rows<DP, MODE>(x, p, warp, lane);
+  } else if (warp >= 8) {
+    role_phi<DP, MODE>(x, p, warp, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(x.tmem, Cfg::TMEM_COLS);
+  }
+  // a dependent launch completes only after the launch it depends on
+  if (MODE != kState) grid_dependency_wait();
+}
+
+template <int DP, int MODE>
+cudaError_t launch(const PParams& p, dim3 grid, bool dependent, const CUtensorMap& mq,
+                   const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mw,
+                   cudaStream_t stream) {
+  using Cfg = PCfg<DP>;
+  cudaError_t e = cudaFuncSetAttribute(tcp_forward_kernel<DP, MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, tcp_forward_kernel<DP, MODE>, mq, mk, mv, mw, p);
+  count_launches(1);
+  return e;
+}
+
+template <int DP>
+cudaError_t run(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                const SegmentPlan& plan) {
+  const int64_t BH = a.B * a.H;
+  CUtensorMap mq, mk, mv, mw;
+  cudaError_t e;
+  if ((e = tmap_rows(&mq, a.q, BH, a.n, kD, kC)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mk, a.k, BH, a.n, kD, kC)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mv, a.v, BH, a.n, kD, kC)) != cudaSuccess) return e;
+  if ((e = tmap_matrix(&mw, a.omega, kD, DP, 64)) != cudaSuccess) return e;
+  PParams p{};
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.n = a.n;
+  p.seg_len = plan.seg_len;
+  p.nseg = plan.nseg;
+  p.ws_state = ws_state;
+  p.ws_z = ws_z;
+  p.fin_state = a.mu_out;
+  p.fin_z = a.nu_out;
+  p.half_log2m = 0.5f * log2f((float)DP);
+  p.status = a.status;
+  const unsigned ubh = (unsigned)BH;
+  if (a.causal) {
+    if (plan.nseg > 1) {
+      // aggregates of segments 0 … nseg−2 (nothing follows the last one)
+      e = launch<DP, kState>(p, dim3(ubh, (unsigned)(plan.nseg - 1)), false, mq, mk, mv, mw, stream);
+      if (e != cudaSuccess) return e;
+    }
+    return launch<DP, kCausal>(p, dim3(ubh, (unsigned)plan.nseg), plan.nseg > 1, mq, mk, mv, mw,
+                               stream);
+  }
+  e = launch<DP, kState>(p, dim3(ubh, (unsigned)plan.nseg), false, mq, mk, mv, mw, stream);
+  if (e != cudaSuccess) return e;
+  return launch<DP, kReadout>(p, dim3(ubh, (unsigned)plan.nseg), true, mq, mk, mv, mw, stream);
+}
+
+}  // namespace
+
+bool tc_performer_supported(const FwdArgs& a) {
+  return a.bf16 && a.performer && a.d == kD && (a.m == 128 || a.m == 256) && a.decay == nullptr &&
+         a.n >= kC;
+}
+
+cudaError_t tc_performer_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state,
+                                 float* ws_z, const SegmentPlan& plan) {
+  if (a.m == 256) return run<256>(a, stream, ws_state, ws_z, plan);
+  if (a.m == 128) return run<128>(a, stream, ws_state, ws_z, plan);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace la

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "linattn.h"
@@ -62,6 +63,19 @@ bool tc_forward_supported(const FwdArgs& a);
 int64_t tc_segment_granule();
 cudaError_t tc_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
                        float* tot_state, float* tot_z, const SegmentPlan& plan);
+
+// tcgen05/TMA chunked forward with the Performer feature map (bf16, d = 64,
+// m ∈ {128, 256}, no decay, n ≥ 128; causal and non-causal).
+bool tc_performer_supported(const FwdArgs& a);
+cudaError_t tc_performer_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state,
+                                 float* ws_z, const SegmentPlan& plan);
+
+// TMA tensor maps (bf16, 128-byte swizzle, boxes 64 elements wide):
+//   tmap_rows:   [BH, n, D] as a 3-D tensor, box 64 × rows × 1 (rows past n
+//                read as zero);
+//   tmap_matrix: a row-major [rows, cols] matrix, box 64 × box_rows.
+cudaError_t tmap_rows(CUtensorMap* m, const void* base, int64_t BH, int64_t n, int D, int rows);
+cudaError_t tmap_matrix(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows);
 
 // Exclusive decayed prefix over the per-segment aggregates of every head, in
 // place.  Only the first nagg aggregates are read (nagg = nseg − 1 when the

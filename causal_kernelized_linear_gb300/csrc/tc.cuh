@@ -375,6 +375,27 @@ __device__ __forceinline__ float bf16hi_to_f32(uint32_t x) {
   return __uint_as_float(x & 0xFFFF0000u);
 }
 
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// 16-byte chunk j (8 bf16, columns h*64 + 8j …) of row `row` in a tile stored
+// as column blocks of [rows × 64] bf16 with the 128-byte swizzle (the TMA
+// layout of a box 64 elements wide).
+__device__ __forceinline__ uint32_t sw_chunk(int rows, int row, int half, int j) {
+  return (uint32_t)(half * rows * 128 + row * 128 + ((j ^ (row & 7)) << 4));
+}
+
+// Every lane of the warp waits (bounded); the warp then agrees on the
+// outcome so that control flow — and the .sync.aligned tcgen05 operations
+// after it — stays warp-uniform even if the limit expires mid-wait.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, status, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Packed bf16 pair arithmetic (two lanes per 32-bit register, round to nearest even).
 __device__ __forceinline__ uint32_t min_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;

@@ -123,6 +123,14 @@ CASES = [
     ("bf16", 64, "elu1", 0, None, 20000, True),
     ("bf16", 128, "elu1", 0, (0.3, 0.7), 4097, True),
     ("bf16", 64, "elu1", 0, (1.0, 1.0), 2560, True),
+    # tensor-core Performer path (bf16, d = 64, m ∈ {128, 256}, no decay, n ≥ 128):
+    # one chunk, ragged tails, one and many segments, both modes
+    ("bf16", 64, "performer", 256, None, 128, True),
+    ("bf16", 64, "performer", 256, None, 129, False),
+    ("bf16", 64, "performer", 256, None, 1000, True),
+    ("bf16", 64, "performer", 128, None, 4097, True),
+    ("bf16", 64, "performer", 128, None, 300, False),
+    ("bf16", 64, "performer", 256, None, 6000, False),
     ("f32", 32, "elu1", 0, (0.9, 0.999), 1111, True),
     ("f32", 64, "elu1", 0, None, 517, False),
     ("f32", 128, "elu1", 0, (0.0, 1.0), 129, True),
@@ -160,6 +168,20 @@ def test_forward_with_state_matches_oracle_state(cuda_device, dtype, n):
     assert_parity(out, ref_o, tol, "out")
     assert_parity(mu, ref_mu, tol, "mu")
     assert_parity(nu.unsqueeze(-1), ref_nu[..., None], tol, "nu")
+
+
+@pytest.mark.parametrize("causal,n", [(True, 3000), (False, 3000), (True, 200)])
+def test_performer_state_matches_oracle_state(cuda_device, causal, n):
+    inp = W.make_forward_inputs(2, 2, n, 64, "bf16", "performer", 256, seed=13,
+                                qk_scale=64 ** -0.25)
+    g = to_cuda(inp, cuda_device)
+    out, mu, nu = cl.forward_with_state(g["q"], g["k"], g["v"], None, "performer", g["omega"],
+                                        causal=causal)
+    ref_o, ref_mu, ref_nu = oracle.forward(inp["q"], inp["k"], inp["v"], None, "performer",
+                                           inp["omega"], causal=causal, return_state=True)
+    assert_parity(out, ref_o, TOL_BF16, "out")
+    assert_parity(mu, ref_mu, TOL_BF16, "mu")
+    assert_parity(nu.unsqueeze(-1), ref_nu[..., None], TOL_BF16, "nu")
 
 
 def test_noncausal_state_is_full_sum(cuda_device):
