@@ -435,6 +435,14 @@ def run_profile_case(case):
         out = torch.empty_like(g["q"])
         for _ in range(3):
             cl.forward(g["q"], g["k"], g["v"], g["a"], "elu1", None, True, out=out)
+    elif case == "performer":
+        w = W.PERFORMER                              # B2 H8 n4096 d64 m256 (the workload itself)
+        inp = W.forward_inputs(w)
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        out = torch.empty_like(g["q"])
+        for causal in (True, False):
+            for _ in range(3):
+                cl.forward(g["q"], g["k"], g["v"], None, "performer", g["omega"], causal, out=out)
     elif case == "decode-small":
         w = W.DECODE
         B = 64                                       # B64 H32 d128: 128 MiB of state
@@ -462,7 +470,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile-case", choices=["forward-long-small", "decode-small"], default=None,
+    ap.add_argument("--profile-case", choices=["forward-long-small", "performer", "decode-small"],
+                    default=None,
                     help="run a small seeded case for an ncu capture and exit")
     args = ap.parse_args()
     if args.profile_case:
