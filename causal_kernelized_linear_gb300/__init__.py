@@ -14,8 +14,10 @@ All work runs in the library's CUDA kernels; PyTorch only allocates device
 memory and provides the stream.
 """
 from ._binding import (EXPORTED, LinAttnError, decode_step, forward, forward_with_state,
-                       last_device_status, launch_count, library_path, load, status_string)
+                       last_device_status, launch_count, library_path, load,
+                       selftest_wait_timeout, status_string)
 from .build import build
 
 __all__ = ["forward", "forward_with_state", "decode_step", "last_device_status", "status_string",
-           "LinAttnError", "build", "load", "library_path", "launch_count", "EXPORTED"]
+           "LinAttnError", "build", "load", "library_path", "launch_count",
+           "selftest_wait_timeout", "EXPORTED"]

@@ -31,7 +31,7 @@ _FM = {"elu1": LA_FM_ELU1, "performer": LA_FM_PERFORMER}
 _DT = {torch.bfloat16: LA_BF16, torch.float32: LA_F32}
 
 EXPORTED = ("la_forward", "la_forward_with_state", "la_decode_step", "la_status_string",
-            "la_get_last_device_status", "la_launch_count")
+            "la_get_last_device_status", "la_launch_count", "la_selftest_wait_timeout")
 
 
 class LinAttnError(RuntimeError):
@@ -82,6 +82,8 @@ def load():
         lib.la_get_last_device_status.restype = ctypes.c_int
         lib.la_launch_count.argtypes = []
         lib.la_launch_count.restype = ctypes.c_uint64
+        lib.la_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        lib.la_selftest_wait_timeout.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -211,6 +213,13 @@ def last_device_status(stream=None) -> int:
     """la_get_last_device_status: synchronises the stream and returns (and
     clears) the device status word."""
     return int(load().la_get_last_device_status(_stream_handle(stream)))
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    """la_selftest_wait_timeout: queue the bounded-wait self-test kernel; the
+    returned status is that of the launch (the timeout itself is reported by
+    last_device_status)."""
+    return int(load().la_selftest_wait_timeout(int(limit_ns), _stream_handle(stream)))
 
 
 def launch_count() -> int:

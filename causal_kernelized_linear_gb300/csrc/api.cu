@@ -344,6 +344,14 @@ const char* la_status_string(la_status status) {
 
 uint64_t la_launch_count(void) { return la::g_launches.load(std::memory_order_relaxed); }
 
+la_status la_selftest_wait_timeout(uint64_t limit_ns, la_stream stream) {
+  if (limit_ns < 1000ull || limit_ns > 100000000ull) return LA_ERR_INVALID_ARG;
+  la::DeviceInfo di;
+  la_status st = la::device_info(&di);
+  if (st != LA_OK) return st;
+  return la::to_status(la::selftest_wait(di.status, limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 la_status la_get_last_device_status(la_stream stream) {
   la::DeviceInfo di;
   la_status st = la::device_info(&di);

@@ -98,6 +98,9 @@ la_status forward_in_workspace(const la_tensor* q, const la_tensor* k, const la_
 // Records `k` kernel launches in the process-wide launch counter.
 void count_launches(int k);
 
+// One CTA of bounded waits on a barrier nothing signals (la_selftest_wait_timeout).
+cudaError_t selftest_wait(int* status, uint64_t limit_ns, cudaStream_t stream);
+
 // Memory-bound recurrent decode step.
 cudaError_t decode_step(const DecodeArgs& a, cudaStream_t stream);
 

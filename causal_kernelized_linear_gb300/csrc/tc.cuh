@@ -391,8 +391,9 @@ __device__ __forceinline__ uint32_t sw_chunk(int rows, int row, int half, int j)
 // outcome so that control flow — and the .sync.aligned tcgen05 operations
 // after it — stays warp-uniform even if the limit expires mid-wait.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status,
-                                          volatile int* abort_flag) {
-  const bool ok = mbar_wait(bar, parity, status, abort_flag);
+                                          volatile int* abort_flag,
+                                          uint64_t limit_ns = 2000000000ull) {
+  const bool ok = mbar_wait(bar, parity, status, abort_flag, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -186,6 +186,20 @@ la_status la_forward_noalloc(const la_tensor* q, const la_tensor* k, const la_te
  */
 uint64_t la_launch_count(void);
 
+/*
+ * la_selftest_wait_timeout — test hook for the failure path of the bounded
+ * waits.  Queues on `stream` one small kernel that runs the same bounded
+ * wait the tensor-core kernels use (single-thread and whole-warp forms) on a
+ * shared-memory barrier that nothing ever signals, with a limit of
+ * `limit_ns` nanoseconds (1 000 … 100 000 000).  The waits give up, record
+ * LA_ERR_TIMEOUT in the device status word and the kernel exits normally: no
+ * trap, no fault, no hang.  A following la_get_last_device_status(stream)
+ * returns LA_ERR_TIMEOUT (and clears the word).  Returns LA_ERR_INVALID_ARG
+ * for a limit outside the range (nothing queued), LA_ERR_CUDA if the launch
+ * fails, else LA_OK.  No counterpart on the pages.
+ */
+la_status la_selftest_wait_timeout(uint64_t limit_ns, la_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

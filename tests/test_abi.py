@@ -89,6 +89,12 @@ def test_host_validation_rejects_before_any_launch(lib):
     assert _fwd(lib, ok, ok, ok, fm=7) == B.LA_ERR_INVALID_ARG
 
 
+def test_selftest_hook_rejects_out_of_range_limits(lib):
+    # validated before any device call: nothing is queued
+    assert lib.la_selftest_wait_timeout(999, None) == B.LA_ERR_INVALID_ARG
+    assert lib.la_selftest_wait_timeout(100_000_001, None) == B.LA_ERR_INVALID_ARG
+
+
 def test_forward_with_state_needs_state_buffers(lib):
     ok = _t()
     st = lib.la_forward_with_state(ctypes.byref(ok), ctypes.byref(ok), ctypes.byref(ok), None, 0,
