@@ -416,8 +416,11 @@ __device__ __forceinline__ bool phi_k_chunk(const Ctx& x, int c, int r, int j0, 
       live ? splat_bf16x2(CEN ? k_scale_cen * lazy_sigma(x, c) : x.pw[max(cs - 1 - r, 0)]) : 0u;
   uint8_t* kt = x.sm + L::k_off(ks);
   uint8_t* kpp = x.sm + L::kpp_off(ks);
-#pragma unroll 4
-  for (int jj = j0; jj < j1; ++jj) {
+  // full launch: always 8 chunks (one 64-column half), fully unrolled so that
+  // all eight loads are in flight together
+  constexpr int UNROLL = FULL ? 8 : 4;
+#pragma unroll UNROLL
+  for (int jj = j0; jj < (FULL ? j0 + 8 : j1); ++jj) {
     const uint32_t off = sw_chunk(kC, r, jj >> 3, jj & 7);
     uint4 u = *reinterpret_cast<const uint4*>(kt + off);
     u.x = elu1_bf16x2(u.x); u.y = elu1_bf16x2(u.y);
