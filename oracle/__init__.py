@@ -72,6 +72,9 @@ def _load():
             lib.oracle_features.restype = ctypes.c_int
             lib.oracle_decode_step.argtypes = [i64, i64, i64, dp, dp, dp, dp, dp, dp, dp]
             lib.oracle_decode_step.restype = ctypes.c_int
+            lib.oracle_decode_step_fm.argtypes = [i64, i64, i64, ctypes.c_int, i64, dp, dp, dp,
+                                                  dp, dp, dp, dp, dp]
+            lib.oracle_decode_step_fm.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -148,17 +151,27 @@ def forward(q, k, v, decay_a=None, feature_map="elu1", omega=None, causal=True,
     return out
 
 
-def decode_step(mu, nu, q, k, v, decay_a=None):
-    """One recurrent step (elu+1): returns (out [B,H,d], μ', ν') without
-    modifying the inputs.  q, k, v: [B, H, d]."""
+def decode_step(mu, nu, q, k, v, decay_a=None, feature_map="elu1", omega=None):
+    """One recurrent step: returns (out [B,H,d], μ', ν') without modifying
+    the inputs.  q, k, v: [B, H, d]; μ [B,H,d',d], ν [B,H,d']; omega [d, m]
+    for the Performer map (d' = m), None for elu+1 (d' = d)."""
     mu = _f64(mu).copy()
     nu = _f64(nu).copy()
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, d = q.shape
     a = _f64(decay_a)
+    fm = _fm(feature_map)
+    omega = _f64(omega)
+    if fm == FM_PERFORMER and omega is None:
+        raise ValueError("the Performer map needs omega [d, m]")
+    m = omega.shape[1] if fm == FM_PERFORMER else 0
     out = np.empty((B, H, d), dtype=np.float64)
-    rc = _load().oracle_decode_step(B, H, d, _ptr(mu), _ptr(nu), _ptr(q), _ptr(k),
-                                    _ptr(v), _ptr(a), _ptr(out))
+    if fm == FM_ELU1:
+        rc = _load().oracle_decode_step(B, H, d, _ptr(mu), _ptr(nu), _ptr(q), _ptr(k),
+                                        _ptr(v), _ptr(a), _ptr(out))
+    else:
+        rc = _load().oracle_decode_step_fm(B, H, d, fm, m, _ptr(mu), _ptr(nu), _ptr(q), _ptr(k),
+                                           _ptr(v), _ptr(a), _ptr(omega), _ptr(out))
     if rc != 0:
         raise ValueError(f"oracle_decode_step rejected its arguments (rc={rc})")
     return out, mu, nu

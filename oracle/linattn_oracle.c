@@ -202,3 +202,14 @@ int oracle_decode_step(int64_t B, int64_t H, int64_t d, double* mu, double* nu,
   return oracle_forward(B, H, 1, d, OR_FM_ELU1, 0, q, k, v, a, NULL, 1, mu, nu,
                         out, mu, nu);
 }
+
+/*
+ * The same step with either feature map: fm = OR_FM_ELU1 (d' = d, omega
+ * NULL) or OR_FM_PERFORMER (d' = m, omega [d, m], φ of [LAR] "Performer
+ * random features").  mu [B,H,d',d], nu [B,H,d'] are advanced in place.
+ */
+int oracle_decode_step_fm(int64_t B, int64_t H, int64_t d, int fm, int64_t m, double* mu,
+                          double* nu, const double* q, const double* k, const double* v,
+                          const double* a, const double* omega, double* out) {
+  return oracle_forward(B, H, 1, d, fm, m, q, k, v, a, omega, 1, mu, nu, out, mu, nu);
+}

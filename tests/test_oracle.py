@@ -262,6 +262,22 @@ def test_state_handoff_forward_then_decode():
     np.testing.assert_allclose(tail, full[:, :, n1:], rtol=1e-12, atol=1e-13)
 
 
+@pytest.mark.parametrize("fm", ["elu1", "performer"])
+def test_decode_steps_follow_the_quadratic_form(fm):
+    # n1 tokens through the forward, the rest one decode step at a time: every
+    # decoded output is the quadratic form (brute force, "Efficient
+    # Transformers I" eq (25)–(26) with the decay mask) at that position.
+    q, k, v, a, omega = _rand_inputs(21, 1, 3, 20, 5, fm=fm, m=9, decay=[0.8, 0.97, 1.0],
+                                     scale=0.7)
+    ref = _quadratic_form(q, k, v, a, fm, omega)
+    n1 = 11
+    _, mu, nu = oracle.forward(q[:, :, :n1], k[:, :, :n1], v[:, :, :n1], a, fm, omega,
+                               return_state=True)
+    for j in range(n1, q.shape[2]):
+        o, mu, nu = oracle.decode_step(mu, nu, q[:, :, j], k[:, :, j], v[:, :, j], a, fm, omega)
+        np.testing.assert_allclose(o, ref[:, :, j], rtol=1e-10, atol=1e-12)
+
+
 # --- (e) Performer expectation -----------------------------------------------------------
 
 def _perf_closed_form(q, k, sigma2):
