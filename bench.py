@@ -251,7 +251,8 @@ def bench_decode(cl, w: W.DecodeWorkload, stream, steps=None, distinct=32):
     steps = steps or w.steps
     pre = W.decode_prefill_inputs(w)
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in pre.items()}
-    _, mu, nu = cl.forward_with_state(g["q"], g["k"], g["v"], g["a"], "elu1", stream=stream)
+    _, mu, nu = cl.forward_with_state(g["q"], g["k"], g["v"], g["a"], w.feature_map, g["omega"],
+                                      stream=stream)
     del g["q"], g["k"], g["v"]
     sets = []
     for s in range(distinct):
@@ -263,13 +264,16 @@ def bench_decode(cl, w: W.DecodeWorkload, stream, steps=None, distinct=32):
     def step():
         x = sets[it[0] % distinct]
         it[0] += 1
-        cl.decode_step(mu, nu, x["q"], x["k"], x["v"], g["a"], out=out, stream=stream)
+        cl.decode_step(mu, nu, x["q"], x["k"], x["v"], g["a"], out=out, stream=stream,
+                       feature_map=w.feature_map, omega=g["omega"])
 
     ms, launches = _time_steps(step, steps, 3, stream, None, cl.launch_count)
     heads = w.B * w.H
-    # algorithmic bytes per head-step: μ read+write 8·d², ν read+write 8·d,
-    # q, k, v read and o written in bf16 (8·d)
-    nbytes = heads * (8 * w.d * w.d + 8 * w.d + 8 * w.d)
+    # algorithmic bytes per head-step: μ read+write 8·d'·d, ν read+write 8·d',
+    # q, k, v read and o written in bf16 (8·d); ω (Performer) is shared by all
+    # heads and read once per step
+    dp = w.m if w.feature_map == "performer" else w.d
+    nbytes = heads * (8 * dp * w.d + 8 * dp + 8 * w.d) + 2 * w.d * w.m
     return {"ms": ms, "avg_ms": statistics.mean(ms), "bytes": nbytes, "tokens": w.B,
             "launches_timed": launches}
 
@@ -388,15 +392,16 @@ def run_ours(args, rank, world, dist):
                 "frac_bf16_peak": fl / peaks["bf16_tflops"], "gbs_alg": gbs,
                 "frac_hbm": gbs / peaks["hbm_gbs"], "l2": "flushed between steps",
                 "launches_per_step": r["launches_per_step"]})
-        d = bench_decode(cl, W.DECODE, stream)
-        secs = d["avg_ms"] / 1e3
-        gbs = d["bytes"] / secs / 1e9
-        secondary.append({
-            "workload": W.DECODE.name, "value": gbs, "unit": "GB/s",
-            "frac_hbm": gbs / peaks["hbm_gbs"], "tokens_per_s": d["tokens"] * W.DECODE.H / secs,
-            "ms_per_step": d["avg_ms"], "steps": len(d["ms"]),
-            "l2": "state (512 MiB) larger than L2",
-            "launches_per_step": 1})
+        for dw in (W.DECODE, W.PERFORMER_DECODE):
+            d = bench_decode(cl, dw, stream)
+            secs = d["avg_ms"] / 1e3
+            gbs = d["bytes"] / secs / 1e9
+            secondary.append({
+                "workload": dw.name, "value": gbs, "unit": "GB/s",
+                "frac_hbm": gbs / peaks["hbm_gbs"], "tokens_per_s": d["tokens"] * dw.H / secs,
+                "ms_per_step": d["avg_ms"], "steps": len(d["ms"]),
+                "l2": "state (512 MiB) larger than L2",
+                "launches_per_step": 1})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -31,7 +31,8 @@ _FM = {"elu1": LA_FM_ELU1, "performer": LA_FM_PERFORMER}
 _DT = {torch.bfloat16: LA_BF16, torch.float32: LA_F32}
 
 EXPORTED = ("la_forward", "la_forward_with_state", "la_decode_step", "la_status_string",
-            "la_get_last_device_status", "la_launch_count", "la_selftest_wait_timeout")
+            "la_get_last_device_status", "la_launch_count", "la_selftest_wait_timeout",
+            "la_decode_step_fm")
 
 
 class LinAttnError(RuntimeError):
@@ -76,6 +77,8 @@ def load():
         lib.la_forward_with_state.restype = ctypes.c_int
         lib.la_decode_step.argtypes = [vp, vp, P, P, P, vp, P, vp]
         lib.la_decode_step.restype = ctypes.c_int
+        lib.la_decode_step_fm.argtypes = [vp, vp, P, P, P, vp, ctypes.c_int, P, P, vp]
+        lib.la_decode_step_fm.restype = ctypes.c_int
         lib.la_status_string.argtypes = [ctypes.c_int]
         lib.la_status_string.restype = ctypes.c_char_p
         lib.la_get_last_device_status.argtypes = [vp]
@@ -178,9 +181,12 @@ def forward_with_state(q, k, v, decay_a=None, feature_map="elu1", omega=None, ca
     return out, mu_out, nu_out
 
 
-def decode_step(mu, nu, q, k, v, decay_a=None, out=None, stream=None):
-    """la_decode_step: μ [B,H,d,d], ν [B,H,d] fp32 updated in place; q, k, v
-    [B,H,d] or [B,H,1,d].  Returns out (same shape as q)."""
+def decode_step(mu, nu, q, k, v, decay_a=None, out=None, stream=None, feature_map="elu1",
+                omega=None):
+    """One recurrent step, state updated in place: la_decode_step (elu+1) or
+    la_decode_step_fm (Performer, omega [d, m]).  μ [B,H,d',d], ν [B,H,d']
+    fp32 (d' = d for elu+1, m for Performer); q, k, v [B,H,d] or [B,H,1,d].
+    Returns out (same shape as q)."""
     _need_cuda("mu", mu, torch.float32)
     _need_cuda("nu", nu, torch.float32)
     for nm, t in (("q", q), ("k", k), ("v", v)):
@@ -192,8 +198,17 @@ def decode_step(mu, nu, q, k, v, decay_a=None, out=None, stream=None):
     else:
         raise ValueError("q must be [B,H,d] or [B,H,1,d]")
     B, H, _, d = shape4
-    if tuple(mu.shape) != (B, H, d, d) or tuple(nu.shape) != (B, H, d):
-        raise ValueError("mu must be [B,H,d,d] and nu [B,H,d]")
+    fm = _FM[feature_map] if isinstance(feature_map, str) else int(feature_map)
+    dp = d
+    om = None
+    if omega is not None:
+        _need_cuda("omega", omega)
+        if omega.dim() != 2:
+            raise ValueError("omega must be [d, m]")
+        dp = int(omega.shape[1])
+        om = LaTensor(omega.data_ptr(), _DT[omega.dtype], 1, 1, int(omega.shape[0]), dp)
+    if tuple(mu.shape) != (B, H, dp, d) or tuple(nu.shape) != (B, H, dp):
+        raise ValueError("mu must be [B,H,d',d] and nu [B,H,d']")
     if out is None:
         out = torch.empty_like(q)
     _need_cuda("out", out)
@@ -203,9 +218,17 @@ def decode_step(mu, nu, q, k, v, decay_a=None, out=None, stream=None):
         dptr = decay_a.data_ptr()
     qd, kd, vd = (_desc(t, shape4) for t in (q, k, v))
     od = _desc(out, shape4)
-    st = load().la_decode_step(mu.data_ptr(), nu.data_ptr(), ctypes.byref(qd), ctypes.byref(kd),
-                               ctypes.byref(vd), dptr, ctypes.byref(od), _stream_handle(stream))
-    _check("la_decode_step", st)
+    if fm == LA_FM_ELU1 and om is None:
+        st = load().la_decode_step(mu.data_ptr(), nu.data_ptr(), ctypes.byref(qd),
+                                   ctypes.byref(kd), ctypes.byref(vd), dptr, ctypes.byref(od),
+                                   _stream_handle(stream))
+        _check("la_decode_step", st)
+    else:
+        st = load().la_decode_step_fm(mu.data_ptr(), nu.data_ptr(), ctypes.byref(qd),
+                                      ctypes.byref(kd), ctypes.byref(vd), dptr, fm,
+                                      ctypes.byref(om) if om is not None else None,
+                                      ctypes.byref(od), _stream_handle(stream))
+        _check("la_decode_step_fm", st)
     return out
 
 

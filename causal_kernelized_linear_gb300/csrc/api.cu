@@ -298,9 +298,9 @@ la_status la_forward_with_state(const la_tensor* q, const la_tensor* k, const la
   return la::run_forward(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
-la_status la_decode_step(float* mu, float* nu, const la_tensor* q, const la_tensor* k,
-                         const la_tensor* v, const float* decay_a, la_tensor* out,
-                         la_stream stream) {
+la_status la_decode_step_fm(float* mu, float* nu, const la_tensor* q, const la_tensor* k,
+                            const la_tensor* v, const float* decay_a, la_feature_map feature_map,
+                            const la_tensor* omega, la_tensor* out, la_stream stream) {
   if (!mu || !nu || !q || !k || !v || !out) return LA_ERR_INVALID_ARG;
   if (!la::valid_dtype(q->dtype) || k->dtype != q->dtype || v->dtype != q->dtype ||
       out->dtype != q->dtype)
@@ -315,6 +315,19 @@ la_status la_decode_step(float* mu, float* nu, const la_tensor* q, const la_tens
       !la::aligned16(k->data) || !la::aligned16(v->data) || !la::aligned16(out->data))
     return LA_ERR_INVALID_ARG;
   if (decay_a && (reinterpret_cast<uintptr_t>(decay_a) & 3u)) return LA_ERR_INVALID_ARG;
+  int m = 0;
+  if (feature_map == LA_FM_PERFORMER) {
+    if (!omega || !omega->data) return LA_ERR_INVALID_ARG;
+    if (omega->dtype != q->dtype || omega->B != 1 || omega->H != 1 || omega->n != q->d)
+      return LA_ERR_INVALID_ARG;
+    if (!la::aligned16(omega->data)) return LA_ERR_INVALID_ARG;
+    if (!la::supported_features(omega->d)) return LA_ERR_UNSUPPORTED;
+    m = (int)omega->d;
+  } else if (feature_map == LA_FM_ELU1) {
+    if (omega) return LA_ERR_INVALID_ARG;
+  } else {
+    return LA_ERR_INVALID_ARG;
+  }
   la::DecodeArgs a;
   a.mu = mu;
   a.nu = nu;
@@ -323,11 +336,20 @@ la_status la_decode_step(float* mu, float* nu, const la_tensor* q, const la_tens
   a.v = v->data;
   a.out = out->data;
   a.decay = decay_a;
+  a.omega = omega ? omega->data : nullptr;
   a.B = q->B;
   a.H = q->H;
   a.d = (int)q->d;
+  a.m = m;
   a.bf16 = q->dtype == LA_BF16;
+  a.performer = feature_map == LA_FM_PERFORMER;
   return la::to_status(la::decode_step(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+la_status la_decode_step(float* mu, float* nu, const la_tensor* q, const la_tensor* k,
+                         const la_tensor* v, const float* decay_a, la_tensor* out,
+                         la_stream stream) {
+  return la_decode_step_fm(mu, nu, q, k, v, decay_a, LA_FM_ELU1, nullptr, out, stream);
 }
 
 const char* la_status_string(la_status status) {

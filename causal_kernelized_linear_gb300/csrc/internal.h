@@ -33,16 +33,19 @@ struct FwdArgs {
 };
 
 struct DecodeArgs {
-  float* mu;
-  float* nu;
+  float* mu;            // [B,H,d',d]
+  float* nu;            // [B,H,d']
   const void* q;
   const void* k;
   const void* v;
   void* out;
   const float* decay;
+  const void* omega;    // Performer: [d, m]; else nullptr
   int64_t B, H;
   int d;
+  int m;                // Performer feature count (0 for elu+1)
   bool bf16;
+  bool performer;
 };
 
 // Segment plan shared by the forward paths: the sequence of every head is cut

@@ -136,6 +136,22 @@ la_status la_decode_step(float* mu, float* nu, const la_tensor* q,
                          const la_tensor* k, const la_tensor* v,
                          const float* decay_a, la_tensor* out, la_stream stream);
 
+/*
+ * la_decode_step_fm — la_decode_step with either feature map
+ * ("Linear Attention Research 2026"): feature_map = LA_FM_ELU1 (omega must be
+ * NULL; identical to la_decode_step) or LA_FM_PERFORMER, φ(x) =
+ * exp(x·ω − ½‖x‖²)/√m with omega a [1, 1, d, m] tensor of the same dtype as
+ * q (m ∈ {64, 128, 256}, 16-byte aligned).  The state is then mu [B, H, m, d]
+ * and nu [B, H, m] (fp32, updated in place); everything else — shapes,
+ * decay, readout o = q'·μ / q'·ν after the update, ownership, asynchrony and
+ * errors — is as for la_decode_step.  Invalid or unsupported arguments
+ * (unknown map, omega missing or with the wrong shape, dtype or alignment,
+ * omega given for elu+1) are rejected before any launch.
+ */
+la_status la_decode_step_fm(float* mu, float* nu, const la_tensor* q, const la_tensor* k,
+                            const la_tensor* v, const float* decay_a, la_feature_map feature_map,
+                            const la_tensor* omega, la_tensor* out, la_stream stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* la_status_string(la_status status);
 

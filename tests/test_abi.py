@@ -119,6 +119,24 @@ def test_decode_validation(lib):
         B.LA_ERR_INVALID_ARG
 
 
+def test_decode_fm_validation(lib):
+    q = _t(shape=(4, 2, 1, 64))
+    st = 0x40000
+    om = _t(shape=(1, 1, 64, 256))
+
+    def call(fm, omega):
+        return lib.la_decode_step_fm(st, st, ctypes.byref(q), ctypes.byref(q), ctypes.byref(q),
+                                     None, fm, ctypes.byref(omega) if omega is not None else None,
+                                     ctypes.byref(q), None)
+    assert call(B.LA_FM_ELU1, om) == B.LA_ERR_INVALID_ARG              # ω given for elu+1
+    assert call(B.LA_FM_PERFORMER, None) == B.LA_ERR_INVALID_ARG       # ω missing
+    assert call(B.LA_FM_PERFORMER, _t(shape=(1, 1, 64, 96))) == B.LA_ERR_UNSUPPORTED
+    assert call(B.LA_FM_PERFORMER, _t(shape=(1, 1, 32, 256))) == B.LA_ERR_INVALID_ARG
+    assert call(B.LA_FM_PERFORMER, _t(shape=(1, 1, 64, 256), dtype=B.LA_F32)) == \
+        B.LA_ERR_INVALID_ARG
+    assert call(5, None) == B.LA_ERR_INVALID_ARG
+
+
 def test_product_path_has_no_oracle_or_cpu_fallback():
     pkg = os.path.join(ROOT, "causal_kernelized_linear_gb300")
     for path in glob.glob(os.path.join(pkg, "**", "*"), recursive=True):

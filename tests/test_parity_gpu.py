@@ -101,6 +101,42 @@ def test_decode_workload_sampled_heads(cuda_device):
     assert_parity(sub(nu.cpu()).unsqueeze(-1), ref_nu[..., None], TOL_BF16, "final nu")
 
 
+def test_performer_decode_workload_sampled_heads(cuda_device):
+    """Full-size Performer decode (B=256, H=32, d=64, m=256): 512-token prefill
+    through la_forward_with_state, then 256 steps of la_decode_step_fm; the
+    oracle follows 32 seeded-random heads through the prefill and every step."""
+    w = W.PERFORMER_DECODE
+    pre = W.decode_prefill_inputs(w)
+    g = to_cuda(pre, cuda_device)
+    _, mu, nu = cl.forward_with_state(g["q"], g["k"], g["v"], g["a"], "performer", g["omega"])
+    BH = w.B * w.H
+    pick = np.sort(np.random.default_rng(321).choice(BH, size=32, replace=False))
+    pick_t = torch.from_numpy(pick)
+    hsel = pick % w.H
+
+    def sub(x):  # [B,H,...] -> [1, 32, ...]
+        return x.reshape(BH, *x.shape[2:])[pick_t].unsqueeze(0)
+
+    a_sub = pre["a"][torch.from_numpy(hsel)]
+    _, ref_mu, ref_nu = oracle.forward(sub(pre["q"]), sub(pre["k"]), sub(pre["v"]), a_sub,
+                                       "performer", pre["omega"], return_state=True)
+    assert_parity(sub(mu.cpu()), ref_mu, TOL_BF16, "prefill state mu")
+    out = torch.empty(w.B, w.H, w.d, device=cuda_device, dtype=torch.bfloat16)
+    for step in range(256):
+        st = W.decode_step_inputs(w, step)
+        gs = to_cuda(st, cuda_device)
+        cl.decode_step(mu, nu, gs["q"], gs["k"], gs["v"], g["a"], out=out,
+                       feature_map="performer", omega=g["omega"])
+        ref_o, ref_mu, ref_nu = oracle.decode_step(ref_mu, ref_nu, sub(st["q"]), sub(st["k"]),
+                                                   sub(st["v"]), a_sub, "performer", pre["omega"])
+        if step in (0, 1, 2, 127) or step % 64 == 63:
+            assert_parity(sub(out.cpu()).unsqueeze(2), ref_o[:, :, None], TOL_BF16,
+                          f"performer decode step {step}")
+    torch.cuda.synchronize()
+    assert_parity(sub(mu.cpu()), ref_mu, TOL_BF16, "final mu")
+    assert_parity(sub(nu.cpu()).unsqueeze(-1), ref_nu[..., None], TOL_BF16, "final nu")
+
+
 # --- sweeps over shapes, maps, decays, ragged lengths --------------------------------------
 
 CASES = [
@@ -231,6 +267,53 @@ def test_decode_small_against_oracle(cuda_device, dtype):
 
 
 # --- edge cases and error behaviour --------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("d,m", [(32, 64), (32, 256), (64, 128), (64, 256), (128, 64), (128, 256)])
+def test_performer_decode_small_against_oracle(cuda_device, dtype, d, m):
+    B, H, steps = 3, 4, 5
+    inp = W.make_forward_inputs(B, H, 7, d, dtype, "performer", m, decay=(0.7, 0.99),
+                                seed=31 + d + m, qk_scale=d ** -0.25)
+    g = to_cuda(inp, cuda_device)
+    _, mu, nu = cl.forward_with_state(g["q"], g["k"], g["v"], g["a"], "performer", g["omega"])
+    _, ref_mu, ref_nu = oracle.forward(inp["q"], inp["k"], inp["v"], inp["a"], "performer",
+                                       inp["omega"], return_state=True)
+    tol = TOL_F32 if dtype == "f32" else TOL_BF16
+    gen = torch.Generator().manual_seed(77 + d)
+    for s in range(steps):
+        q, k, v = (torch.randn(B, H, d, generator=gen) for _ in range(3))
+        q, k = q * d ** -0.25, k * d ** -0.25
+        q, k, v = (x.to(W.torch_dtype(dtype)) for x in (q, k, v))
+        o = cl.decode_step(mu, nu, q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
+                           g["a"], feature_map="performer", omega=g["omega"])
+        ref_o, ref_mu, ref_nu = oracle.decode_step(ref_mu, ref_nu, q, k, v, inp["a"],
+                                                   "performer", inp["omega"])
+        assert_parity(o.unsqueeze(2), ref_o[:, :, None], tol, f"step {s}")
+    assert_parity(mu, ref_mu, tol, "mu")
+    assert_parity(nu.unsqueeze(-1), ref_nu[..., None], tol, "nu")
+
+
+def test_performer_prefill_then_decode_equals_forward(cuda_device):
+    # forward over n1 tokens with the state, then decode steps, against the
+    # forward over all n1 + n2 tokens (tensor-core prefill: no decay)
+    n1, n2 = 300, 12
+    inp = W.make_forward_inputs(1, 4, n1 + n2, 64, "bf16", "performer", 256, seed=41,
+                                qk_scale=64 ** -0.25)
+    g = to_cuda(inp, cuda_device)
+    full = cl.forward(g["q"], g["k"], g["v"], None, "performer", g["omega"], True)
+    _, mu, nu = cl.forward_with_state(g["q"][:, :, :n1].contiguous(), g["k"][:, :, :n1].contiguous(),
+                                      g["v"][:, :, :n1].contiguous(), None, "performer", g["omega"])
+    outs = []
+    for j in range(n1, n1 + n2):
+        o = cl.decode_step(mu, nu, g["q"][:, :, j].contiguous(), g["k"][:, :, j].contiguous(),
+                           g["v"][:, :, j].contiguous(), None, feature_map="performer",
+                           omega=g["omega"])
+        outs.append(o.unsqueeze(2))
+    dec = torch.cat(outs, dim=2)
+    ref = oracle.forward(inp["q"], inp["k"], inp["v"], None, "performer", inp["omega"], True)
+    assert_parity(dec, ref[:, :, n1:], TOL_BF16, "decoded tail vs oracle")
+    assert_parity(full[:, :, n1:], ref[:, :, n1:], TOL_BF16, "forward tail vs oracle")
+
 
 def test_empty_sequence_is_a_noop(cuda_device):
     q = torch.empty(2, 3, 0, 64, device=cuda_device, dtype=torch.bfloat16)

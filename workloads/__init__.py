@@ -54,6 +54,9 @@ class DecodeWorkload:
     steps: int
     decay: Tuple[float, float]
     seed: int
+    feature_map: str = "elu1"
+    m: int = 0
+    qk_scale: float = 1.0
 
 
 # The five workloads of the method's evaluation plan.
@@ -68,6 +71,12 @@ LONG = ForwardWorkload("long_B1_H16_n65536_d128", 1, 16, 65536, 128, "bf16", "el
                        decay=(0.95, 0.9999), seed=3)
 DECODE = DecodeWorkload("decode_B256_H32_d128", 256, 32, 128, prefill=512, steps=1024,
                         decay=(0.9, 0.999), seed=4)
+# Decode with the Performer map (the recurrent counterpart of the Performer
+# workload: d = 64, m = 256, q and k scaled by d^{-1/4}; decay and state size
+# as in the decode workload: 8192 heads × 64 KiB of μ).
+PERFORMER_DECODE = DecodeWorkload("performer_decode_B256_H32_d64_m256", 256, 32, 64, prefill=512,
+                                  steps=1024, decay=(0.9, 0.999), seed=5, feature_map="performer",
+                                  m=256, qk_scale=64 ** -0.25)
 
 FORWARD_WORKLOADS = {w.name: w for w in (TINY_FP32, ELU1_DECAY, PERFORMER, LONG)}
 
@@ -110,9 +119,10 @@ def forward_inputs(w: ForwardWorkload, n: Optional[int] = None, B: Optional[int]
 
 
 def decode_prefill_inputs(w: DecodeWorkload, B: Optional[int] = None, H: Optional[int] = None):
-    """Prefill q, k, v [B,H,prefill,d] bf16 and the per-head decay a [H] fp32."""
-    return make_forward_inputs(B or w.B, H or w.H, w.prefill, w.d, "bf16", "elu1",
-                               decay=w.decay, seed=w.seed)
+    """Prefill q, k, v [B,H,prefill,d] bf16, the per-head decay a [H] fp32 and
+    (Performer) ω [d, m]."""
+    return make_forward_inputs(B or w.B, H or w.H, w.prefill, w.d, "bf16", w.feature_map, w.m,
+                               decay=w.decay, seed=w.seed, qk_scale=w.qk_scale)
 
 
 def decode_step_inputs(w: DecodeWorkload, step: int, B: Optional[int] = None,
@@ -122,7 +132,7 @@ def decode_step_inputs(w: DecodeWorkload, step: int, B: Optional[int] = None,
     g = torch.Generator().manual_seed(int(w.seed) * 1_000_003 + 7919 * (int(step) + 1))
     B = B or w.B
     H = H or w.H
-    q = torch.randn(B, H, w.d, generator=g)
-    k = torch.randn(B, H, w.d, generator=g)
+    q = torch.randn(B, H, w.d, generator=g) * w.qk_scale
+    k = torch.randn(B, H, w.d, generator=g) * w.qk_scale
     v = torch.randn(B, H, w.d, generator=g)
     return {"q": q.bfloat16(), "k": k.bfloat16(), "v": v.bfloat16()}
