@@ -253,7 +253,9 @@ __device__ __forceinline__ void role_mma_out(const Ctx& x) {
   using L = Layout<D, true, CEN>;
   uint64_t* bar = x.bar;
   const uint32_t tmem = x.tmem;
-  const uint32_t sS = x.sbase + Cfg::oS, sONES = x.sbase + Cfg::oONES, sZB = x.sbase + Cfg::oZB;
+  const uint32_t sONES = x.sbase + Cfg::oONES;
+  const uint64_t dS = smem_desc(x.sbase + Cfg::oS, D * 128, 1024, kSwizzle128B);
+  const uint64_t dZ = smem_desc(x.sbase + Cfg::oZB, 16, 0, kSwizzleNone);
   constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);   // scores
   constexpr uint32_t idN = idesc_bf16_f32(128, D, false, true);      // num (+)= A·{S, V}
   constexpr uint32_t idR = idesc_bf16_f32(128, 16, false, false);    // den: Q''·z, P·1
@@ -273,18 +275,19 @@ __device__ __forceinline__ void role_mma_out(const Ctx& x) {
     if (c >= 1 && !mbar_wait(&bar[B_NUMFULL], (c - 1) & 1, st, ab)) break;
     tc_fence_after();
     if (CEN) {
-      for (int k = 0; k < KD; ++k) {
-        const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
+      const uint64_t dKP = smem_desc(sKP, 16, 1024, kSwizzle128B);
+#pragma unroll
+      for (int k = 0; k < KD; ++k)
         mma_ts(tmem + Cfg::TS, tmem + Cfg::TQ + k * 8,
-               smem_desc(sKP + off, 16, 1024, kSwizzle128B), idS, k > 0);
-      }
+               desc_at(dKP, (k >> 2) * (kC * 128) + (k & 3) * 32), idS, k > 0);
       mma_commit(&bar[B_SCORES]);
     } else {
-      const uint32_t sQ = x.sbase + L::q_off(0);
+      const uint64_t dQ = smem_desc(x.sbase + L::q_off(0), 16, 1024, kSwizzle128B);
+      const uint64_t dK = smem_desc(sK, 16, 1024, kSwizzle128B);
+#pragma unroll
       for (int k = 0; k < KD; ++k) {
         const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
-        mma_ss(tmem + Cfg::TS, smem_desc(sQ + off, 16, 1024, kSwizzle128B),
-               smem_desc(sK + off, 16, 1024, kSwizzle128B), idS, k > 0);
+        mma_ss(tmem + Cfg::TS, desc_at(dQ, off), desc_at(dK, off), idS, k > 0);
       }
       mma_commit(&bar[B_SCORES]);
       mma_commit(&bar[B_QEMPTY0]);
@@ -294,11 +297,10 @@ __device__ __forceinline__ void role_mma_out(const Ctx& x) {
     if (!mbar_wait(&bar[B_SREADY], c & 1, st, ab)) break;
     if (c >= 1 && !mbar_wait(&bar[B_NUMEMPTY], (c - 1) & 1, st, ab)) break;
     tc_fence_after();
+#pragma unroll
     for (int k = 0; k < KD; ++k) {
-      mma_ts(tmem + Cfg::TN, tmem + Cfg::TQ + k * 8,
-             smem_desc(sS + k * 2048, D * 128, 1024, kSwizzle128B), idN, k > 0);
-      mma_ts(tmem + Cfg::TR, tmem + Cfg::TQ + k * 8, smem_desc(sZB + k * 32, 16, 0, kSwizzleNone),
-             idR, k > 0);
+      mma_ts(tmem + Cfg::TN, tmem + Cfg::TQ + k * 8, desc_at(dS, k * 2048), idN, k > 0);
+      mma_ts(tmem + Cfg::TR, tmem + Cfg::TQ + k * 8, desc_at(dZ, k * 32), idR, k > 0);
     }
     mma_commit(&bar[B_SEMPTY]);
     mma_commit(&bar[B_QPEMPTY]);
@@ -306,9 +308,10 @@ __device__ __forceinline__ void role_mma_out(const Ctx& x) {
     if (!mbar_wait(&bar[B_PREADY], c & 1, st, ab)) break;
     if (!mbar_wait(&bar[B_VFULL0 + vs], (c / L::VST) & 1, st, ab)) break;
     tc_fence_after();
+    const uint64_t dV = smem_desc(sV, kC * 128, 1024, kSwizzle128B);
+#pragma unroll
     for (int k = 0; k < kC / 16; ++k) {
-      mma_ts(tmem + Cfg::TN, tmem + Cfg::TS + k * 8,
-             smem_desc(sV + k * 2048, kC * 128, 1024, kSwizzle128B), idN, 1);
+      mma_ts(tmem + Cfg::TN, tmem + Cfg::TS + k * 8, desc_at(dV, k * 2048), idN, 1);
       mma_ts(tmem + Cfg::TR, tmem + Cfg::TS + k * 8, ones, idR, 1);
     }
     mma_commit(&bar[B_NUMFULL]);
@@ -339,9 +342,12 @@ __device__ __forceinline__ void role_mma_state(const Ctx& x) {
     if (!mbar_wait(&bar[B_VFULL0 + vs], (c / L::VST) & 1, st, ab)) break;
     if (!mbar_wait(&bar[B_DSEMPTY], c & 1, st, ab)) break;   // state in TMEM read out
     tc_fence_after();
+    const uint64_t dA = smem_desc(sKP, lbo_kp, 1024, kSwizzle128B);
+    const uint64_t dV = smem_desc(sV, kC * 128, 1024, kSwizzle128B);
+#pragma unroll
     for (int k = 0; k < kC / 16; ++k) {
-      const uint64_t ad = smem_desc(sKP + k * 2048, lbo_kp, 1024, kSwizzle128B);
-      mma_ss(tmem + Cfg::TD, ad, smem_desc(sV + k * 2048, kC * 128, 1024, kSwizzle128B), idD, 1);
+      const uint64_t ad = desc_at(dA, k * 2048);
+      mma_ss(tmem + Cfg::TD, ad, desc_at(dV, k * 2048), idD, 1);
       mma_ss(tmem + Cfg::TZ, ad, ones, idZ, 1);
     }
     mma_commit(&bar[B_DSFULL]);

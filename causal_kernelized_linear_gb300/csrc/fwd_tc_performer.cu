@@ -27,7 +27,8 @@
 //
 // Roles:
 //   warp 0       TMA producer (ω once; raw q, k, v tiles in two-stage rings)
-//   warp 1       tcgen05 MMA issuer, TMEM owner
+//   warps 1–3    tcgen05 MMA issuers: output products (warp 1, TMEM owner),
+//                state products (warp 2), projections (warp 3)
 //   warps 4–7    initial state; state operand tile per chunk; masked P;
 //                epilogue o = num/den stored row by row; final state
 //   warps 8–15   φ: each 64-feature projection block of U comes through one
@@ -174,122 +175,158 @@ __device__ __forceinline__ void role_producer(const PCtx& x, const CUtensorMap* 
   }
 }
 
+// Three MMA issuers, one thread each (tcgen05.commit tracks the MMAs of
+// the issuing thread, so each chain commits its own barriers; a tile read
+// by two chains is released by a commit from each):
+//   projections (warp 3):  U = X·ω per 64-feature block into the two TMEM
+//                          buffers (they alias the scores columns, so in the
+//                          causal mode chunk c + 1 waits for P·V of chunk c)
+//   state (warp 2):        ΔS = φ(K)ᵀV, Δz = φ(K)ᵀ1 onto the TMEM state
+//   output (warp 1):       scores = φ(Q)·φ(K)ᵀ; num = φ(Q)·S, den = φ(Q)·z;
+//                          num += P·V, den += P·1
+// Operand descriptors are built once per tile and advanced by address.
 template <int DP, int MODE>
-__device__ __forceinline__ void role_mma(const PCtx& x) {
+__device__ __forceinline__ void role_mma_proj(const PCtx& x) {
   using Cfg = PCfg<DP>;
   using LD = Loads<MODE>;
   uint64_t* bar = x.bar;
-  const uint32_t tmem = x.tmem;
   const uint32_t sb = x.sbase;
   constexpr uint32_t idP = idesc_bf16_f32(128, 64, false, true);    // U = X·ω
-  constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);  // scores
-  constexpr uint32_t idD = idesc_bf16_f32(128, 64, true, true);     // ΔS block = φ(K)ᵀ V
-  constexpr uint32_t idZ = idesc_bf16_f32(128, 16, true, false);    // Δz block = φ(K)ᵀ 1
-  constexpr uint32_t idN = idesc_bf16_f32(128, 64, false, true);    // num (+)= A·{S, V}
-  constexpr uint32_t idR = idesc_bf16_f32(128, 16, false, false);   // den: φ(Q)·z, P·1
-  const uint64_t ones = smem_desc(sb + Cfg::oONES, 0, 0, kSwizzleNone);
   int* st = x.status;
   volatile int* ab = x.abort_flag;
+  const uint64_t dW = smem_desc(sb + Cfg::oW, Cfg::WATOM, 1024, kSwizzle128B);
   bool ok = mbar_wait(&bar[B_W], 0, st, ab);
-  int pj = 0;   // projection steps issued
-  // U block f of the raw tile at sX → projection buffer pj & 1
+  int pj = 0;
   auto project = [&](uint32_t sX, int f) -> bool {
     const int b = pj & 1;
     if (pj >= 2 && !mbar_wait(&bar[B_PJEMPTY0 + b], ((pj - 2) >> 1) & 1, st, ab)) return false;
     tc_fence_after();
+    const uint64_t dX = smem_desc(sX, 16, 1024, kSwizzle128B);
+    const uint32_t d = x.tmem + Cfg::TS + 64 * b;
+#pragma unroll
     for (int k = 0; k < kD / 16; ++k)
-      mma_ss(tmem + Cfg::TS + 64 * b, smem_desc(sX + k * 32, 16, 1024, kSwizzle128B),
-             smem_desc(sb + Cfg::oW + f * Cfg::WATOM + k * 2048, Cfg::WATOM, 1024, kSwizzle128B),
-             idP, k > 0);
+      mma_ss(d, desc_at(dX, k * 32), desc_at(dW, f * Cfg::WATOM + k * 2048), idP, k > 0);
     mma_commit(&bar[B_PJFULL0 + b]);
     ++pj;
     return true;
   };
   for (int c = 0; ok && c < x.nchunks; ++c) {
     const int s = c & 1;
-    const uint32_t sQ = sb + (s ? Cfg::oQ1 : Cfg::oQ0);
-    const uint32_t sK = sb + (s ? Cfg::oK1 : Cfg::oK0);
-    const uint32_t sV = sb + (s ? Cfg::oV1 : Cfg::oV0);
-    const uint32_t sKP = sb + Cfg::oKP;
-    // the projection buffers alias the scores / P of the previous chunk
     if (MODE == kCausal && c >= 1 && !mbar_wait(&bar[B_NUMFULL], (c - 1) & 1, st, ab)) break;
     if (LD::K) {
       if (!mbar_wait(&bar[B_KFULL0 + s], (c >> 1) & 1, st, ab)) break;
-      tc_fence_after();
-      for (int f = 0; ok && f < Cfg::NB; ++f) ok = project(sK, f);
+      for (int f = 0; ok && f < Cfg::NB; ++f) ok = project(sb + (s ? Cfg::oK1 : Cfg::oK0), f);
       if (!ok) break;
       mma_commit(&bar[B_KEMPTY0 + s]);
     }
     if (LD::Q) {
       if (!mbar_wait(&bar[B_QFULL0 + s], (c >> 1) & 1, st, ab)) break;
-      tc_fence_after();
-      for (int f = 0; ok && f < Cfg::NB; ++f) ok = project(sQ, f);
+      for (int f = 0; ok && f < Cfg::NB; ++f) ok = project(sb + (s ? Cfg::oQ1 : Cfg::oQ0), f);
       if (!ok) break;
       mma_commit(&bar[B_QEMPTY0 + s]);
     }
+  }
+  mma_commit(&bar[B_MMADONE]);
+  mbar_wait_drain(&bar[B_MMADONE], 0);
+}
+
+template <int DP, int MODE>
+__device__ __forceinline__ void role_mma_state(const PCtx& x) {
+  using Cfg = PCfg<DP>;
+  uint64_t* bar = x.bar;
+  const uint32_t sb = x.sbase;
+  constexpr uint32_t idD = idesc_bf16_f32(128, 64, true, true);     // ΔS block = φ(K)ᵀ V
+  constexpr uint32_t idZ = idesc_bf16_f32(128, 16, true, false);    // Δz block = φ(K)ᵀ 1
+  const uint64_t ones = smem_desc(sb + Cfg::oONES, 0, 0, kSwizzleNone);
+  const uint64_t dKP = smem_desc(sb + Cfg::oKP, Cfg::TILE, 1024, kSwizzle128B);
+  int* st = x.status;
+  volatile int* ab = x.abort_flag;
+  for (int c = 0; c < x.nchunks; ++c) {
+    const int s = c & 1;
+    const uint64_t dV = smem_desc(sb + (s ? Cfg::oV1 : Cfg::oV0), Cfg::TILE, 1024, kSwizzle128B);
+    if (!mbar_wait(&bar[B_KREADY], c & 1, st, ab)) break;
+    if (!mbar_wait(&bar[B_VFULL0 + s], (c >> 1) & 1, st, ab)) break;
+    if ((MODE == kCausal || c == 0) &&
+        !mbar_wait(&bar[B_SCONV], MODE == kCausal ? (c & 1) : 0, st, ab))
+      break;
+    tc_fence_after();
+#pragma unroll
+    for (int mb = 0; mb < Cfg::MB; ++mb)
+#pragma unroll
+      for (int k = 0; k < kC / 16; ++k) {
+        const uint64_t ad = desc_at(dKP, mb * 2 * Cfg::TILE + k * 2048);
+        mma_ss(x.tmem + Cfg::TST + 64 * mb, ad, desc_at(dV, k * 2048), idD, 1);
+        mma_ss(x.tmem + Cfg::TZ + 16 * mb, ad, ones, idZ, 1);
+      }
+    mma_commit(&bar[B_DSFULL]);
+    mma_commit(&bar[B_KPEMPTY]);
+    mma_commit(&bar[B_VEMPTY0 + s]);
+  }
+  mma_commit(&bar[B_MMADONE]);
+  mbar_wait_drain(&bar[B_MMADONE], 0);
+}
+
+template <int DP, int MODE>
+__device__ __forceinline__ void role_mma_out(const PCtx& x) {
+  using Cfg = PCfg<DP>;
+  uint64_t* bar = x.bar;
+  const uint32_t tmem = x.tmem;
+  const uint32_t sb = x.sbase;
+  constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);  // scores
+  constexpr uint32_t idN = idesc_bf16_f32(128, 64, false, true);    // num (+)= A·{S, V}
+  constexpr uint32_t idR = idesc_bf16_f32(128, 16, false, false);   // den: φ(Q)·z, P·1
+  const uint64_t ones = smem_desc(sb + Cfg::oONES, 0, 0, kSwizzleNone);
+  const uint64_t dKP = smem_desc(sb + Cfg::oKP, 16, 1024, kSwizzle128B);
+  const uint64_t dS = smem_desc(sb + Cfg::oS, DP * 128, 1024, kSwizzle128B);
+  const uint64_t dZ = smem_desc(sb + Cfg::oZB, 16, 0, kSwizzleNone);
+  int* st = x.status;
+  volatile int* ab = x.abort_flag;
+  for (int c = 0; c < x.nchunks; ++c) {
+    const int s = c & 1;
     if (MODE == kCausal) {
       // scores = φ(Q)·φ(K)ᵀ over the m features
       if (!mbar_wait(&bar[B_KREADY], c & 1, st, ab)) break;
       if (!mbar_wait(&bar[B_QREADY], c & 1, st, ab)) break;
       tc_fence_after();
-      for (int k = 0; k < DP / 16; ++k) {
-        const uint32_t off = (k >> 2) * Cfg::TILE + (k & 3) * 32;
+#pragma unroll
+      for (int k = 0; k < DP / 16; ++k)
         mma_ts(tmem + Cfg::TS, tmem + Cfg::TQ + k * 8,
-               smem_desc(sKP + off, 16, 1024, kSwizzle128B), idS, k > 0);
-      }
+               desc_at(dKP, (k >> 2) * Cfg::TILE + (k & 3) * 32), idS, k > 0);
       mma_commit(&bar[B_SCORES]);
+      mma_commit(&bar[B_KPEMPTY]);                 // φ(K) also read by ΔS (state chain)
+    } else {
+      if (!mbar_wait(&bar[B_QREADY], c & 1, st, ab)) break;
     }
-    if (LD::K) {
-      // ΔS = φ(K)ᵀV, Δz = φ(K)ᵀ1, accumulated onto the TMEM state
-      if (MODE != kCausal && !mbar_wait(&bar[B_KREADY], c & 1, st, ab)) break;
-      if (!mbar_wait(&bar[B_VFULL0 + s], (c >> 1) & 1, st, ab)) break;
-      if ((MODE == kCausal || c == 0) &&
-          !mbar_wait(&bar[B_SCONV], MODE == kCausal ? (c & 1) : 0, st, ab))
-        break;
-      tc_fence_after();
-      for (int mb = 0; mb < Cfg::MB; ++mb)
-        for (int k = 0; k < kC / 16; ++k) {
-          const uint64_t ad = smem_desc(sKP + mb * 2 * Cfg::TILE + k * 2048, Cfg::TILE, 1024,
-                                        kSwizzle128B);
-          mma_ss(tmem + Cfg::TST + 64 * mb, ad,
-                 smem_desc(sV + k * 2048, Cfg::TILE, 1024, kSwizzle128B), idD, 1);
-          mma_ss(tmem + Cfg::TZ + 16 * mb, ad, ones, idZ, 1);
-        }
-      mma_commit(&bar[B_DSFULL]);
-      mma_commit(&bar[B_KPEMPTY]);                 // φ(K) tile read by scores and ΔS
-      if (MODE == kState) mma_commit(&bar[B_VEMPTY0 + s]);
+    // num = φ(Q)·S ; den = φ(Q)·z
+    if ((MODE == kCausal || c == 0) &&
+        !mbar_wait(&bar[B_SREADY], MODE == kCausal ? (c & 1) : 0, st, ab))
+      break;
+    if (c >= 1 && !mbar_wait(&bar[B_NUMEMPTY], (c - 1) & 1, st, ab)) break;
+    tc_fence_after();
+#pragma unroll
+    for (int k = 0; k < DP / 16; ++k) {
+      mma_ts(tmem + Cfg::TN, tmem + Cfg::TQ + k * 8, desc_at(dS, k * 2048), idN, k > 0);
+      mma_ts(tmem + Cfg::TR, tmem + Cfg::TQ + k * 8, desc_at(dZ, k * 32), idR, k > 0);
     }
-    if (LD::Q) {
-      // num = φ(Q)·S ; den = φ(Q)·z
-      if ((MODE == kCausal || c == 0) &&
-          !mbar_wait(&bar[B_SREADY], MODE == kCausal ? (c & 1) : 0, st, ab))
-        break;
-      if (c >= 1 && !mbar_wait(&bar[B_NUMEMPTY], (c - 1) & 1, st, ab)) break;
-      tc_fence_after();
-      for (int k = 0; k < DP / 16; ++k) {
-        mma_ts(tmem + Cfg::TN, tmem + Cfg::TQ + k * 8,
-               smem_desc(sb + Cfg::oS + k * 2048, DP * 128, 1024, kSwizzle128B), idN, k > 0);
-        mma_ts(tmem + Cfg::TR, tmem + Cfg::TQ + k * 8,
-               smem_desc(sb + Cfg::oZB + k * 32, 16, 0, kSwizzleNone), idR, k > 0);
-      }
-      if (MODE == kCausal) mma_commit(&bar[B_SEMPTY]);
-      mma_commit(&bar[B_QPEMPTY]);                 // φ(Q) read by scores and num
-      if (MODE == kReadout) mma_commit(&bar[B_NUMFULL]);
-    }
-    if (MODE == kCausal) {
-      // num += P·V ; den += P·1
-      if (!mbar_wait(&bar[B_PREADY], c & 1, st, ab)) break;
-      tc_fence_after();
-      for (int k = 0; k < kC / 16; ++k) {
-        mma_ts(tmem + Cfg::TN, tmem + Cfg::TS + k * 8,
-               smem_desc(sV + k * 2048, Cfg::TILE, 1024, kSwizzle128B), idN, 1);
-        mma_ts(tmem + Cfg::TR, tmem + Cfg::TS + k * 8, ones, idR, 1);
-      }
+    if (MODE == kCausal) mma_commit(&bar[B_SEMPTY]);
+    mma_commit(&bar[B_QPEMPTY]);                   // φ(Q) read by scores and num
+    if (MODE == kReadout) {
       mma_commit(&bar[B_NUMFULL]);
-      mma_commit(&bar[B_VEMPTY0 + s]);
+      continue;
     }
+    // num += P·V ; den += P·1
+    const uint64_t dV = smem_desc(sb + (s ? Cfg::oV1 : Cfg::oV0), Cfg::TILE, 1024, kSwizzle128B);
+    if (!mbar_wait(&bar[B_PREADY], c & 1, st, ab)) break;
+    if (!mbar_wait(&bar[B_VFULL0 + s], (c >> 1) & 1, st, ab)) break;
+    tc_fence_after();
+#pragma unroll
+    for (int k = 0; k < kC / 16; ++k) {
+      mma_ts(tmem + Cfg::TN, tmem + Cfg::TS + k * 8, desc_at(dV, k * 2048), idN, 1);
+      mma_ts(tmem + Cfg::TR, tmem + Cfg::TS + k * 8, ones, idR, 1);
+    }
+    mma_commit(&bar[B_NUMFULL]);
+    mma_commit(&bar[B_VEMPTY0 + s]);
   }
-  // every issued MMA must finish before TMEM is released
   mma_commit(&bar[B_MMADONE]);
   mbar_wait_drain(&bar[B_MMADONE], 0);
 }
@@ -616,6 +653,9 @@ tcp_forward_kernel(const __grid_constant__ CUtensorMap map_q,
       if (i == B_QEMPTY0 || i == B_QEMPTY1 || i == B_KEMPTY0 || i == B_KEMPTY1) cnt = 1 + 8;
       if (i == B_PJEMPTY0 || i == B_PJEMPTY1 || i == B_KREADY || i == B_QREADY) cnt = 8;
       if (i == B_PREADY || i == B_NUMEMPTY || i == B_SCONV || i == B_SREADY) cnt = 4;
+      // released by two MMA chains in the causal mode: φ(K) (scores, ΔS), V (ΔS, P·V)
+      if ((i == B_KPEMPTY || i == B_VEMPTY0 || i == B_VEMPTY1) && MODE == kCausal) cnt = 2;
+      if (i == B_MMADONE) cnt = MODE == kCausal ? 3 : 2;
       mbar_init(&x.bar[i], cnt);
     }
     *x.abort_flag = 0;
@@ -647,7 +687,11 @@ tcp_forward_kernel(const __grid_constant__ CUtensorMap map_q,
   if (warp == 0) {
     if (lane == 0) role_producer<DP, MODE>(x, &map_q, &map_k, &map_v, &map_w);
   } else if (warp == 1) {
-    if (lane == 0) role_mma<DP, MODE>(x);
+    if (MODE != kState && lane == 0) role_mma_out<DP, MODE>(x);
+  } else if (warp == 2) {
+    if (MODE != kReadout && lane == 0) role_mma_state<DP, MODE>(x);
+  } else if (warp == 3) {
+    if (lane == 0) role_mma_proj<DP, MODE>(x);
   } else if (warp >= 4 && warp < 8) {
     role_rows<DP, MODE>(x, p, warp, lane);
   } else if (warp >= 8) {

@@ -321,6 +321,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
+// The descriptor of the same operand `byte_off` bytes further on: only the
+// 14-bit start-address field (bits 0–13, address / 16) changes, and shared
+// addresses stay below 256 KB, so no carry leaves the field.
+__device__ __forceinline__ uint64_t desc_at(uint64_t desc, uint32_t byte_off) {
+  return desc + (uint64_t)(byte_off >> 4);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
 // a_mn / b_mn select MN-major (transposed) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn,
