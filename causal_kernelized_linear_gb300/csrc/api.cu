@@ -162,7 +162,8 @@ PathPlan choose_path(const FwdArgs& a) {
 
 cudaError_t dispatch_forward(const FwdArgs& a, const PathPlan& pp, cudaStream_t stream,
                              float* ws_state, float* ws_z, float* tot_state, float* tot_z) {
-  if (pp.tensor_cores && a.performer) return tc_performer_forward(a, stream, ws_state, ws_z, pp.plan);
+  if (pp.tensor_cores && a.performer)
+    return tc_performer_forward(a, stream, ws_state, ws_z, tot_state, tot_z, pp.plan);
   if (pp.tensor_cores) return tc_forward(a, stream, ws_state, ws_z, tot_state, tot_z, pp.plan);
   return simt_forward(a, stream, ws_state, ws_z, tot_state, tot_z, pp.plan);
 }

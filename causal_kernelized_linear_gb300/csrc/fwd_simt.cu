@@ -297,6 +297,11 @@ segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z
                     int nseg, int nagg, int64_t seg_len, int64_t n, int dpd, int dp,
                     const float* decay) {
   constexpr int kBatch = 8;  // aggregates loaded together to keep loads in flight
+  // launched as a programmatic dependent of the launch that wrote the
+  // aggregates (tensor-core paths): let the next launch start, then wait for
+  // the aggregates (both are no-ops in an ordinary launch)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t bh = blockIdx.x;
   const int e = blockIdx.y * 256 + threadIdx.x;
   if (e >= dpd + dp) return;
@@ -369,7 +374,7 @@ cudaError_t run_simt(const FwdArgs& a, cudaStream_t stream, float* ws_state, flo
     simt_segment_state<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
     count_launches(1);
     err = segment_scan(ws_state, ws_z, tot_state, tot_z, BH, a.H, plan.nseg, plan.nseg,
-                       plan.seg_len, a.n, DP, D, a.decay, stream);
+                       plan.seg_len, a.n, DP, D, a.decay, stream, false);
     if (err != cudaSuccess) return err;
   }
   if (a.causal) {
@@ -412,13 +417,21 @@ cudaError_t dispatch_simt(const FwdArgs& a, cudaStream_t s, float* ws, float* wz
 
 cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* tot_z,
                          int64_t BH, int64_t H, int nseg, int nagg, int64_t seg_len, int64_t n,
-                         int dp, int d, const float* decay, cudaStream_t stream) {
+                         int dp, int d, const float* decay, cudaStream_t stream, bool dependent) {
   const int dpd = dp * d;
-  const dim3 grid((unsigned)BH, (unsigned)((dpd + dp + 255) / 256));
-  segment_scan_kernel<<<grid, 256, 0, stream>>>(ws_state, ws_z, tot_state, tot_z, H, nseg, nagg,
-                                                seg_len, n, dpd, dp, decay);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)BH, (unsigned)((dpd + dp + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, segment_scan_kernel, ws_state, ws_z, tot_state, tot_z,
+                                     H, nseg, nagg, seg_len, n, dpd, dp, decay);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t simt_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,

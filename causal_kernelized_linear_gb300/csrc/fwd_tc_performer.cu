@@ -20,13 +20,15 @@
 //            the segments before it (the last segment also writes the final
 //            state)
 //   readout  o = q'·S_n / q'·z_n over one segment, S_n the sum of all the
-//            aggregates (the first segment also writes S_n as the final state)
-// A causal or readout launch that follows a state launch is its programmatic
-// dependent: it starts while the state launch drains, and only the reads of
-// the aggregates wait for it.
+//            aggregates
+// Between the state launch and the other one, segment_scan turns the
+// aggregates into those sums (exclusive prefixes, and the total, which is
+// also the non-causal final state).  The scan and the launch after it are
+// programmatic dependents: they start while the launch before drains, and
+// only the reads of its results wait for it.
 //
 // Roles:
-//   warp 0       TMA producer (ω once; raw q, k, v tiles in two-stage rings)
+//   warp 0       TMA producer (ω once; raw q and k tiles one stage each, v two)
 //   warps 1–3    tcgen05 MMA issuers: output products (warp 1, TMEM owner),
 //                state products (warp 2), projections (warp 3)
 //   warps 4–7    initial state; state operand tile per chunk; masked P;
@@ -58,36 +60,47 @@ enum Mode { kState = 0, kCausal = 1, kReadout = 2 };
 template <int DP>
 struct PCfg {
   static constexpr int NB = DP / 64;             // 64-feature blocks
+  static constexpr int NP = DP / 128;            // 128-feature projection steps per operand
   static constexpr int MB = DP / 128;            // 128-feature blocks (state lane blocks)
   static constexpr int TILE = kC * kD * 2;       // [128 × 64] bf16 = 16 KB
   static constexpr int WATOM = 64 * 128;         // ω block [64 (d) × 64 (features)] = 8 KB
   // shared memory (offsets from a 1024-aligned base)
   static constexpr int oW = 0;                   // ω, NB blocks
-  static constexpr int oQ0 = oW + NB * WATOM;    // raw q stages
-  static constexpr int oQ1 = oQ0 + TILE;
-  static constexpr int oK0 = oQ1 + TILE;         // raw k stages
-  static constexpr int oK1 = oK0 + TILE;
-  static constexpr int oV0 = oK1 + TILE;         // v stages
+  // raw q and k, one stage each: only the projection and the row norms read
+  // them, early in a chunk, so the next chunk's load has most of a chunk to land
+  static constexpr int oQ0 = oW + NB * WATOM;
+  static constexpr int oK0 = oQ0 + TILE;
+  static constexpr int oV0 = oK0 + TILE;         // v stages
   static constexpr int oV1 = oV0 + TILE;
-  static constexpr int oKP = oV1 + TILE;         // φ(K): NB column blocks of [128 × 64]
+  // an all-ones [128 × 64] block one descriptor stride after either v stage:
+  // the B operand [V | 1] (N = 80) gives Σ_s φ(k_s)ᵀ·1 next to ΔS and Σ_s P
+  // next to P·V, without separate N = 16 products
+  static constexpr int oVONE = oV1 + TILE;
+  static constexpr int oKP = oVONE + TILE;       // φ(K): NB column blocks of [128 × 64]
   static constexpr int oS = oKP + NB * TILE;     // state operand, bf16 [DP × 64]
-  static constexpr int oONES = oS + DP * kD * 2; // 8×8 bf16 ones (every core matrix aliases it)
-  static constexpr int oZB = oONES + 128;        // z operand bf16 [DP] + 112 read-past bytes
-  static constexpr int oBAR = oZB + 2 * DP + 128;
-  static constexpr int NBAR = 32;
+  static constexpr int oZF = oS + DP * kD * 2;   // z of the state operand, fp32 [DP]
+  static constexpr int oQZ = oZF + DP * 4;       // q'·z partials [chunk parity][half][128 rows]
+  static constexpr int oBAR = oQZ + 2 * 2 * kC * 4;
+  static constexpr int NBAR = 40;
   static constexpr int oMISC = oBAR + NBAR * 8;  // tmem slot, abort flag
   static constexpr int BYTES = oMISC + 16;
   static constexpr int SMEM_ALLOC = (BYTES + 1024 > 118 * 1024) ? BYTES + 1024 : 118 * 1024;
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
   // tensor memory columns
-  static constexpr uint32_t TST = 0;             // S: MB blocks of 64 columns (lanes = features)
-  static constexpr uint32_t TZ = 128;            // z: MB blocks of 16 columns (column 0 used)
-  static constexpr uint32_t TN = 160;            // numerator [128 × 64]
-  static constexpr uint32_t TR = 224;            // denominator (16 columns, column 0 used)
-  static constexpr uint32_t TS = 256;            // scores / P; two 64-column projection buffers
-  static constexpr uint32_t TQ = 384;            // φ(Q) as bf16 pairs, DP/2 columns
+  static constexpr uint32_t TST = 0;             // [S | z]: MB blocks of 80 columns (lanes =
+                                                 // features; z in column 64 of a block)
+  static constexpr uint32_t TN = 160;            // [num | Σ P]: 64 + 16 columns
+  static constexpr uint32_t TR = TN + 64;        // Σ_s P_ts (16 equal columns, zeroed by the row
+                                                 // warps before each chunk's products)
+  static constexpr uint32_t TS = 256;            // scores / P; the q projection buffer (128 columns)
+  static constexpr uint32_t TQ = 384;            // φ(Q) as bf16 pairs (DP/2 columns); the k
+                                                 // projection buffer (128 columns)
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(TST + MB * 64 <= TZ && TZ + MB * 16 <= TN && TQ + DP / 2 <= TMEM_COLS, "TMEM");
+  static_assert(TST + MB * 80 <= TN && TN + 80 <= TS && TQ + 128 <= TMEM_COLS, "TMEM");
+  __host__ __device__ static constexpr uint32_t tst(int mb) { return TST + 80 * mb; }
+  __host__ __device__ static constexpr uint32_t tz(int mb) { return TST + 80 * mb + 64; }
+  // [V | 1] descriptor stride for v stage s: the distance to the ones block
+  __host__ __device__ static constexpr int vone_lbo(int s) { return oVONE - (s ? oV1 : oV0); }
 };
 
 enum {
@@ -95,7 +108,8 @@ enum {
   B_QFULL0, B_QFULL1, B_QEMPTY0, B_QEMPTY1,
   B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1,
   B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1,
-  B_PJFULL0, B_PJFULL1, B_PJEMPTY0, B_PJEMPTY1,
+  B_PKFULL, B_PKEMPTY,     // projection buffer of k (in the φ(Q) columns)
+  B_PQFULL, B_PQEMPTY,     // projection buffer of q (in the scores columns)
   B_KREADY, B_KPEMPTY, B_QREADY, B_QPEMPTY,
   B_SCORES, B_PREADY, B_NUMFULL, B_NUMEMPTY,
   B_DSFULL, B_SCONV, B_SREADY, B_SEMPTY, B_MMADONE, B_COUNT
@@ -106,9 +120,11 @@ struct PParams {
   __nv_bfloat16* out;      // [BH, n, 64]
   int64_t n, seg_len;
   int nseg;
-  float* ws_state;         // [BH][nseg][DP·64] segment aggregates
+  float* ws_state;         // [BH][nseg][DP·64] segment aggregates → exclusive prefixes (scan)
   float* ws_z;             // [BH][nseg][DP]
-  float* fin_state;        // final state [BH][DP·64] or nullptr
+  float* tot_state;        // non-causal: the sum of all aggregates [BH][DP·64] (scan)
+  float* tot_z;
+  float* fin_state;        // causal: final state [BH][DP·64] or nullptr
   float* fin_z;
   float half_log2m;        // ½·log2 m
   int* status;
@@ -149,10 +165,12 @@ __device__ __forceinline__ void role_producer(const PCtx& x, const CUtensorMap* 
   mbar_arrive_expect_tx(&bar[B_W], Cfg::NB * Cfg::WATOM);
   for (int f = 0; f < Cfg::NB; ++f) tma_load_2d(x.sm + Cfg::oW + f * Cfg::WATOM, mw, &bar[B_W], 64 * f, 0);
   int last[3] = {-1, -1, -1};   // last chunk loaded per operand (k, q, v)
+  // ring of `stages` (1 or 2) buffers; stage s of chunk c = c % stages
   auto load = [&](const CUtensorMap* map, int off0, int off1, int full, int empty, int c, int y,
-                  int which) -> bool {
-    const int s = c & 1;
-    if (c >= 2 && !mbar_wait(&bar[empty + s], ((c - 2) >> 1) & 1, x.status, x.abort_flag))
+                  int which, int stages) -> bool {
+    const int s = stages == 2 ? (c & 1) : 0;
+    const int u = stages == 2 ? (c >> 1) : c;          // use index of the stage
+    if (c >= stages && !mbar_wait(&bar[empty + s], (u - 1) & 1, x.status, x.abort_flag))
       return false;
     mbar_arrive_expect_tx(&bar[full + s], Cfg::TILE);
     tma_load_3d(x.sm + (s ? off1 : off0), map, &bar[full + s], 0, y, (int)x.bh);
@@ -161,26 +179,30 @@ __device__ __forceinline__ void role_producer(const PCtx& x, const CUtensorMap* 
   };
   for (int c = 0; c < x.nchunks && !*x.abort_flag; ++c) {
     const int y = (int)(x.t_begin + (int64_t)c * kC);
-    if (LD::K && !load(mk, Cfg::oK0, Cfg::oK1, B_KFULL0, B_KEMPTY0, c, y, 0)) break;
-    if (LD::Q && !load(mq, Cfg::oQ0, Cfg::oQ1, B_QFULL0, B_QEMPTY0, c, y, 1)) break;
-    if (LD::V && !load(mv, Cfg::oV0, Cfg::oV1, B_VFULL0, B_VEMPTY0, c, y, 2)) break;
+    if (LD::K && !load(mk, Cfg::oK0, Cfg::oK0, B_KFULL0, B_KEMPTY0, c, y, 0, 1)) break;
+    if (LD::Q && !load(mq, Cfg::oQ0, Cfg::oQ0, B_QFULL0, B_QEMPTY0, c, y, 1, 1)) break;
+    if (LD::V && !load(mv, Cfg::oV0, Cfg::oV1, B_VFULL0, B_VEMPTY0, c, y, 2, 2)) break;
   }
   if (*x.abort_flag) {
     // drain the loads still in flight before the CTA's shared memory goes away
     mbar_wait_drain(&bar[B_W], 0);
     const int full[3] = {B_KFULL0, B_QFULL0, B_VFULL0};
+    const int stages[3] = {1, 1, 2};
     for (int w = 0; w < 3; ++w)
-      for (int c = max(0, last[w] - 1); c <= last[w]; ++c)
-        mbar_wait_drain(&bar[full[w] + (c & 1)], (c >> 1) & 1);
+      for (int c = max(0, last[w] - stages[w] + 1); c <= last[w]; ++c)
+        mbar_wait_drain(&bar[full[w] + (stages[w] == 2 ? (c & 1) : 0)],
+                        (stages[w] == 2 ? (c >> 1) : c) & 1);
   }
 }
 
 // Three MMA issuers, one thread each (tcgen05.commit tracks the MMAs of
 // the issuing thread, so each chain commits its own barriers; a tile read
 // by two chains is released by a commit from each):
-//   projections (warp 3):  U = X·ω per 64-feature block into the two TMEM
-//                          buffers (they alias the scores columns, so in the
-//                          causal mode chunk c + 1 waits for P·V of chunk c)
+//   projections (warp 3):  U = X·ω per 64-feature block into two TMEM
+//                          buffers per operand: k's in the φ(Q) columns (free
+//                          once φ(Q)·S of the previous chunk is done, so they
+//                          overlap its P mask and P·V), q's in the scores
+//                          columns (free once P·V of the previous chunk is done)
 //   state (warp 2):        ΔS = φ(K)ᵀV, Δz = φ(K)ᵀ1 onto the TMEM state
 //   output (warp 1):       scores = φ(Q)·φ(K)ᵀ; num = φ(Q)·S, den = φ(Q)·z;
 //                          num += P·V, den += P·1
@@ -191,39 +213,47 @@ __device__ __forceinline__ void role_mma_proj(const PCtx& x) {
   using LD = Loads<MODE>;
   uint64_t* bar = x.bar;
   const uint32_t sb = x.sbase;
-  constexpr uint32_t idP = idesc_bf16_f32(128, 64, false, true);    // U = X·ω
+  constexpr uint32_t idP = idesc_bf16_f32(128, 128, false, true);   // U = X·ω, 128 features
   int* st = x.status;
   volatile int* ab = x.abort_flag;
   const uint64_t dW = smem_desc(sb + Cfg::oW, Cfg::WATOM, 1024, kSwizzle128B);
   bool ok = mbar_wait(&bar[B_W], 0, st, ab);
-  int pj = 0;
-  auto project = [&](uint32_t sX, int f) -> bool {
-    const int b = pj & 1;
-    if (pj >= 2 && !mbar_wait(&bar[B_PJEMPTY0 + b], ((pj - 2) >> 1) & 1, st, ab)) return false;
+  int pk = 0, pq = 0;   // projection steps issued into the k / q buffer
+  // U for features 128·f … 128·f + 127 of the raw tile at sX into the k
+  // buffer (φ(Q) columns) or the q buffer (scores columns)
+  auto project = [&](uint32_t sX, int f, bool is_k) -> bool {
+    int& pj = is_k ? pk : pq;
+    if (pj >= 1 && !mbar_wait(&bar[is_k ? B_PKEMPTY : B_PQEMPTY], (pj - 1) & 1, st, ab))
+      return false;
     tc_fence_after();
     const uint64_t dX = smem_desc(sX, 16, 1024, kSwizzle128B);
-    const uint32_t d = x.tmem + Cfg::TS + 64 * b;
+    const uint32_t d = x.tmem + (is_k ? Cfg::TQ : Cfg::TS);
 #pragma unroll
     for (int k = 0; k < kD / 16; ++k)
-      mma_ss(d, desc_at(dX, k * 32), desc_at(dW, f * Cfg::WATOM + k * 2048), idP, k > 0);
-    mma_commit(&bar[B_PJFULL0 + b]);
+      mma_ss(d, desc_at(dX, k * 32), desc_at(dW, 2 * f * Cfg::WATOM + k * 2048), idP, k > 0);
+    mma_commit(&bar[is_k ? B_PKFULL : B_PQFULL]);
     ++pj;
     return true;
   };
   for (int c = 0; ok && c < x.nchunks; ++c) {
     const int s = c & 1;
-    if (MODE == kCausal && c >= 1 && !mbar_wait(&bar[B_NUMFULL], (c - 1) & 1, st, ab)) break;
     if (LD::K) {
-      if (!mbar_wait(&bar[B_KFULL0 + s], (c >> 1) & 1, st, ab)) break;
-      for (int f = 0; ok && f < Cfg::NB; ++f) ok = project(sb + (s ? Cfg::oK1 : Cfg::oK0), f);
+      // causal: the k buffers sit in the φ(Q) columns of chunk c − 1, free
+      // once φ(Q)·S of that chunk (after its scores) has completed
+      if (MODE == kCausal && c >= 1 && !mbar_wait(&bar[B_QPEMPTY], (c - 1) & 1, st, ab)) break;
+      if (!mbar_wait(&bar[B_KFULL0], c & 1, st, ab)) break;
+      for (int f = 0; ok && f < Cfg::NP; ++f) ok = project(sb + Cfg::oK0, f, true);
       if (!ok) break;
-      mma_commit(&bar[B_KEMPTY0 + s]);
+      mma_commit(&bar[B_KEMPTY0]);
     }
     if (LD::Q) {
-      if (!mbar_wait(&bar[B_QFULL0 + s], (c >> 1) & 1, st, ab)) break;
-      for (int f = 0; ok && f < Cfg::NB; ++f) ok = project(sb + (s ? Cfg::oQ1 : Cfg::oQ0), f);
+      // causal: the q buffers sit in the scores columns, free once P·V of
+      // chunk c − 1 has completed
+      if (MODE == kCausal && c >= 1 && !mbar_wait(&bar[B_NUMFULL], (c - 1) & 1, st, ab)) break;
+      if (!mbar_wait(&bar[B_QFULL0], c & 1, st, ab)) break;
+      for (int f = 0; ok && f < Cfg::NP; ++f) ok = project(sb + Cfg::oQ0, f, false);
       if (!ok) break;
-      mma_commit(&bar[B_QEMPTY0 + s]);
+      mma_commit(&bar[B_QEMPTY0]);
     }
   }
   mma_commit(&bar[B_MMADONE]);
@@ -235,15 +265,14 @@ __device__ __forceinline__ void role_mma_state(const PCtx& x) {
   using Cfg = PCfg<DP>;
   uint64_t* bar = x.bar;
   const uint32_t sb = x.sbase;
-  constexpr uint32_t idD = idesc_bf16_f32(128, 64, true, true);     // ΔS block = φ(K)ᵀ V
-  constexpr uint32_t idZ = idesc_bf16_f32(128, 16, true, false);    // Δz block = φ(K)ᵀ 1
-  const uint64_t ones = smem_desc(sb + Cfg::oONES, 0, 0, kSwizzleNone);
+  constexpr uint32_t idD = idesc_bf16_f32(128, 80, true, true);     // [ΔS | Δz] = φ(K)ᵀ [V | 1]
   const uint64_t dKP = smem_desc(sb + Cfg::oKP, Cfg::TILE, 1024, kSwizzle128B);
   int* st = x.status;
   volatile int* ab = x.abort_flag;
   for (int c = 0; c < x.nchunks; ++c) {
     const int s = c & 1;
-    const uint64_t dV = smem_desc(sb + (s ? Cfg::oV1 : Cfg::oV0), Cfg::TILE, 1024, kSwizzle128B);
+    const uint64_t dV =
+        smem_desc(sb + (s ? Cfg::oV1 : Cfg::oV0), Cfg::vone_lbo(s), 1024, kSwizzle128B);
     if (!mbar_wait(&bar[B_KREADY], c & 1, st, ab)) break;
     if (!mbar_wait(&bar[B_VFULL0 + s], (c >> 1) & 1, st, ab)) break;
     if ((MODE == kCausal || c == 0) &&
@@ -254,9 +283,8 @@ __device__ __forceinline__ void role_mma_state(const PCtx& x) {
     for (int mb = 0; mb < Cfg::MB; ++mb)
 #pragma unroll
       for (int k = 0; k < kC / 16; ++k) {
-        const uint64_t ad = desc_at(dKP, mb * 2 * Cfg::TILE + k * 2048);
-        mma_ss(x.tmem + Cfg::TST + 64 * mb, ad, desc_at(dV, k * 2048), idD, 1);
-        mma_ss(x.tmem + Cfg::TZ + 16 * mb, ad, ones, idZ, 1);
+        mma_ss(x.tmem + Cfg::tst(mb), desc_at(dKP, mb * 2 * Cfg::TILE + k * 2048),
+               desc_at(dV, k * 2048), idD, 1);
       }
     mma_commit(&bar[B_DSFULL]);
     mma_commit(&bar[B_KPEMPTY]);
@@ -274,11 +302,9 @@ __device__ __forceinline__ void role_mma_out(const PCtx& x) {
   const uint32_t sb = x.sbase;
   constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);  // scores
   constexpr uint32_t idN = idesc_bf16_f32(128, 64, false, true);    // num (+)= A·{S, V}
-  constexpr uint32_t idR = idesc_bf16_f32(128, 16, false, false);   // den: φ(Q)·z, P·1
-  const uint64_t ones = smem_desc(sb + Cfg::oONES, 0, 0, kSwizzleNone);
+  constexpr uint32_t idV = idesc_bf16_f32(128, 80, false, true);    // [num | den] += P·[V | 1]
   const uint64_t dKP = smem_desc(sb + Cfg::oKP, 16, 1024, kSwizzle128B);
   const uint64_t dS = smem_desc(sb + Cfg::oS, DP * 128, 1024, kSwizzle128B);
-  const uint64_t dZ = smem_desc(sb + Cfg::oZB, 16, 0, kSwizzleNone);
   int* st = x.status;
   volatile int* ab = x.abort_flag;
   for (int c = 0; c < x.nchunks; ++c) {
@@ -297,33 +323,30 @@ __device__ __forceinline__ void role_mma_out(const PCtx& x) {
     } else {
       if (!mbar_wait(&bar[B_QREADY], c & 1, st, ab)) break;
     }
-    // num = φ(Q)·S ; den = φ(Q)·z
+    // num = φ(Q)·S (φ(Q)·z is summed by the φ warps)
     if ((MODE == kCausal || c == 0) &&
         !mbar_wait(&bar[B_SREADY], MODE == kCausal ? (c & 1) : 0, st, ab))
       break;
     if (c >= 1 && !mbar_wait(&bar[B_NUMEMPTY], (c - 1) & 1, st, ab)) break;
     tc_fence_after();
 #pragma unroll
-    for (int k = 0; k < DP / 16; ++k) {
+    for (int k = 0; k < DP / 16; ++k)
       mma_ts(tmem + Cfg::TN, tmem + Cfg::TQ + k * 8, desc_at(dS, k * 2048), idN, k > 0);
-      mma_ts(tmem + Cfg::TR, tmem + Cfg::TQ + k * 8, desc_at(dZ, k * 32), idR, k > 0);
-    }
     if (MODE == kCausal) mma_commit(&bar[B_SEMPTY]);
     mma_commit(&bar[B_QPEMPTY]);                   // φ(Q) read by scores and num
     if (MODE == kReadout) {
       mma_commit(&bar[B_NUMFULL]);
       continue;
     }
-    // num += P·V ; den += P·1
-    const uint64_t dV = smem_desc(sb + (s ? Cfg::oV1 : Cfg::oV0), Cfg::TILE, 1024, kSwizzle128B);
+    // [num | den] += P·[V | 1]
+    const uint64_t dV =
+        smem_desc(sb + (s ? Cfg::oV1 : Cfg::oV0), Cfg::vone_lbo(s), 1024, kSwizzle128B);
     if (!mbar_wait(&bar[B_PREADY], c & 1, st, ab)) break;
     if (!mbar_wait(&bar[B_VFULL0 + s], (c >> 1) & 1, st, ab)) break;
     tc_fence_after();
 #pragma unroll
-    for (int k = 0; k < kC / 16; ++k) {
-      mma_ts(tmem + Cfg::TN, tmem + Cfg::TS + k * 8, desc_at(dV, k * 2048), idN, 1);
-      mma_ts(tmem + Cfg::TR, tmem + Cfg::TS + k * 8, ones, idR, 1);
-    }
+    for (int k = 0; k < kC / 16; ++k)
+      mma_ts(tmem + Cfg::TN, tmem + Cfg::TS + k * 8, desc_at(dV, k * 2048), idV, 1);
     mma_commit(&bar[B_NUMFULL]);
     mma_commit(&bar[B_VEMPTY0 + s]);
   }
@@ -331,8 +354,10 @@ __device__ __forceinline__ void role_mma_out(const PCtx& x) {
   mbar_wait_drain(&bar[B_MMADONE], 0);
 }
 
-// Warps 8–15: φ.  Thread r: token row / TMEM lane r; `half` selects 32 of
-// the 64 features of each projection block.
+// Warps 8–15: φ.  Thread r: token row / TMEM lane r; `half` selects 64 of
+// the 128 features of each projection step.  For q the warps also sum
+// φ(q_r)·z over their features (the q'·z term of the denominator) into a
+// per-row partial that the epilogue adds.
 template <int DP, int MODE>
 __device__ __forceinline__ void role_phi(const PCtx& x, const PParams& p, int warp, int lane) {
   using Cfg = PCfg<DP>;
@@ -343,7 +368,9 @@ __device__ __forceinline__ void role_phi(const PCtx& x, const PParams& p, int wa
   const int half = (warp - 8) >> 2;
   const int r = (warp & 3) * 32 + lane;
   const uint32_t lane_base = (uint32_t)(warp & 3) * 32;
-  int pj = 0;
+  const float* zf = reinterpret_cast<const float*>(x.sm + Cfg::oZF);
+  float* qzbuf = reinterpret_cast<float*>(x.sm + Cfg::oQZ);
+  int pk = 0, pq = 0;   // projection steps consumed from the k / q buffer
   // ½‖x_r‖²·log2 e + ½·log2 m for row r of a raw tile (the exponent offset)
   auto row_offset = [&](int off) -> float {
     float ss = 0.f;
@@ -360,33 +387,40 @@ __device__ __forceinline__ void role_phi(const PCtx& x, const PParams& p, int wa
     }
     return 0.5f * ss * kLog2e + p.half_log2m;
   };
-  // one projection block: φ of 32 features of row r, zero for dead rows
-  auto step = [&](bool is_k, int f, float off, bool live) -> bool {
-    const int b = pj & 1;
-    if (!warp_wait(&bar[B_PJFULL0 + b], (pj >> 1) & 1, st, ab)) return false;
+  // one projection step f: φ of features 128·f + 64·half … + 63 of row r
+  // (zero for dead rows); q also adds its features' φ·z to `qz`
+  auto step = [&](bool is_k, int f, float off, bool live, float& qz) -> bool {
+    int& pj = is_k ? pk : pq;
+    if (!warp_wait(&bar[is_k ? B_PKFULL : B_PQFULL], pj & 1, st, ab)) return false;
     tc_fence_after();
-    uint32_t u[32];
-    tmem_ld32(tmem_addr(x.tmem, lane_base, Cfg::TS + 64 * b + 32 * half), u);
+    uint32_t u[64];
+    const uint32_t src = tmem_addr(x.tmem, lane_base, (is_k ? Cfg::TQ : Cfg::TS) + 64 * half);
+    tmem_ld32(src, u);
+    tmem_ld32(src + 32, u + 32);
     tmem_ld_wait();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bar[B_PJEMPTY0 + b]);
+    if (lane == 0) mbar_arrive(&bar[is_k ? B_PKEMPTY : B_PQEMPTY]);
     ++pj;
-    uint32_t pk[16];
+    const int f0 = 128 * f + 64 * half;            // first feature of this thread's 64
+    uint32_t pkd[32];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < 32; ++j) {
       const float a0 = ex2_approx(fmaf(__uint_as_float(u[2 * j]), kLog2e, -off));
       const float a1 = ex2_approx(fmaf(__uint_as_float(u[2 * j + 1]), kLog2e, -off));
-      pk[j] = live ? pack_bf16x2(a0, a1) : 0u;
+      pkd[j] = live ? pack_bf16x2(a0, a1) : 0u;
+      // with the bf16 values the tensor core sees in φ(Q)·S
+      if (!is_k)
+        qz += bf16lo_to_f32(pkd[j]) * zf[f0 + 2 * j] + bf16hi_to_f32(pkd[j]) * zf[f0 + 2 * j + 1];
     }
     if (is_k) {
-      const uint32_t base = x.sbase + Cfg::oKP + f * Cfg::TILE;
+      const uint32_t base = x.sbase + Cfg::oKP + (2 * f + half) * Cfg::TILE;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        sts128(base + sw_chunk(kC, r, 0, 4 * half + q),
-               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
+      for (int q = 0; q < 8; ++q)
+        sts128(base + sw_chunk(kC, r, 0, q),
+               make_uint4(pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2], pkd[4 * q + 3]));
     } else {
-      tmem_st16(tmem_addr(x.tmem, lane_base, Cfg::TQ + 32 * f + 16 * half), pk);
+      tmem_st32(tmem_addr(x.tmem, lane_base, Cfg::TQ + 64 * f + 32 * half), pkd);
     }
     return true;
   };
@@ -394,26 +428,33 @@ __device__ __forceinline__ void role_phi(const PCtx& x, const PParams& p, int wa
     const int s = c & 1;
     const int cs = (int)min((int64_t)kC, x.t_end - (x.t_begin + (int64_t)c * kC));
     if (LD::K) {
-      if (!warp_wait(&bar[B_KFULL0 + s], (c >> 1) & 1, st, ab)) return;
-      const float off = row_offset(s ? Cfg::oK1 : Cfg::oK0);
+      if (!warp_wait(&bar[B_KFULL0], c & 1, st, ab)) return;
+      const float off = row_offset(Cfg::oK0);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_KEMPTY0 + s]);
+      if (lane == 0) mbar_arrive(&bar[B_KEMPTY0]);
       // the φ(K) tile of the previous chunk must have been consumed
       if (c >= 1 && !warp_wait(&bar[B_KPEMPTY], (c - 1) & 1, st, ab)) return;
-      for (int f = 0; f < Cfg::NB; ++f)
-        if (!step(true, f, off, r < cs)) return;
+      float unused = 0.f;
+      for (int f = 0; f < Cfg::NP; ++f)
+        if (!step(true, f, off, r < cs, unused)) return;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_KREADY]);
     }
     if (LD::Q) {
-      if (!warp_wait(&bar[B_QFULL0 + s], (c >> 1) & 1, st, ab)) return;
-      const float off = row_offset(s ? Cfg::oQ1 : Cfg::oQ0);
+      if (!warp_wait(&bar[B_QFULL0], c & 1, st, ab)) return;
+      const float off = row_offset(Cfg::oQ0);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_QEMPTY0 + s]);
+      if (lane == 0) mbar_arrive(&bar[B_QEMPTY0]);
       if (c >= 1 && !warp_wait(&bar[B_QPEMPTY], (c - 1) & 1, st, ab)) return;
-      for (int f = 0; f < Cfg::NB; ++f)
-        if (!step(false, f, off, true)) return;
+      // z of this chunk's state (written with the state operand)
+      if ((MODE == kCausal || c == 0) &&
+          !warp_wait(&bar[B_SREADY], MODE == kCausal ? (c & 1) : 0, st, ab))
+        return;
+      float qz = 0.f;
+      for (int f = 0; f < Cfg::NP; ++f)
+        if (!step(false, f, off, true, qz)) return;
+      qzbuf[((c & 1) * 2 + half) * kC + r] = qz;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -435,8 +476,16 @@ __device__ __forceinline__ void role_rows(const PCtx& x, const PParams& p, int w
   const int wq = warp - 4;
   const uint32_t lane_base = (uint32_t)wq * 32;
   const uint32_t stile = x.sbase + Cfg::oS;
-  __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(x.sm + Cfg::oZB);
+  float* zf = reinterpret_cast<float*>(x.sm + Cfg::oZF);
+  const float* qzbuf = reinterpret_cast<const float*>(x.sm + Cfg::oQZ);
   const int64_t agg0 = x.bh * p.nseg;
+  // zero the Σ P columns of the accumulator (P·[V | 1] accumulates into them)
+  auto zero_rowsum = [&]() {
+    uint32_t zz[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) zz[j] = 0u;
+    tmem_st16(tmem_addr(tmem, lane_base, Cfg::TR), zz);
+  };
 
   // State row f = 128·mb + r is handled in two 32-column halves hh.
   // bf16 operand: 32 values of state-tile row f (16-byte chunks 4hh … 4hh+3)
@@ -458,57 +507,62 @@ __device__ __forceinline__ void role_rows(const PCtx& x, const PParams& p, int w
   // the fp32 state of block mb from TMEM → `sink(f, hh, v)` per half; returns z
   auto drain_state = [&](int mb, auto sink) -> float {
     uint32_t zr = 0;
-    tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TZ + 16 * mb), zr);
+    tmem_ld1(tmem_addr(tmem, lane_base, Cfg::tz(mb)), zr);
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
       uint32_t u[32];
-      tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TST + 64 * mb + 32 * hh), u);
+      tmem_ld32(tmem_addr(tmem, lane_base, Cfg::tst(mb) + 32 * hh), u);
       tmem_ld_wait();
       sink(128 * mb + r, hh, reinterpret_cast<const float*>(u));
     }
     return __uint_as_float(zr);
   };
 
-  // ---- initial state: the sum of the aggregates before this segment
-  // (causal), of all of them (readout), or zero (state)
+  // ---- initial state: the prefix of the aggregates before this segment
+  // (causal, from the scan), the total (readout), or zero (state)
   {
-    const int nagg = MODE == kCausal ? x.g : (MODE == kReadout ? p.nseg : 0);
-    if (nagg > 0) grid_dependency_wait();
+    const float* srcS = nullptr;
+    const float* srcZ = nullptr;
+    if (MODE == kCausal && x.g > 0) {
+      srcS = p.ws_state + (agg0 + x.g) * (int64_t)(DP * kD);
+      srcZ = p.ws_z + (agg0 + x.g) * DP;
+    } else if (MODE == kReadout) {
+      srcS = p.tot_state + x.bh * (int64_t)(DP * kD);
+      srcZ = p.tot_z + x.bh * DP;
+    }
+    if (srcS) grid_dependency_wait();
     for (int mb = 0; mb < Cfg::MB; ++mb) {
       const int f = 128 * mb + r;
-      float zf = 0.f;
-      for (int a = 0; a < nagg; ++a) zf += p.ws_z[(agg0 + a) * DP + f];
+      const float zsum = srcS ? srcZ[f] : 0.f;
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0.f;
-        for (int a = 0; a < nagg; ++a) {
-          const float4* src = reinterpret_cast<const float4*>(
-              p.ws_state + (agg0 + a) * (int64_t)(DP * kD) + f * kD + 32 * hh);
+        if (srcS) {
+          const float4* src4 = reinterpret_cast<const float4*>(srcS + f * kD + 32 * hh);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float4 t = src[j];
-            v[4 * j] += t.x; v[4 * j + 1] += t.y; v[4 * j + 2] += t.z; v[4 * j + 3] += t.w;
+            const float4 t = src4[j];
+            v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
           }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
         if (MODE != kReadout)
-          tmem_st32(tmem_addr(tmem, lane_base, Cfg::TST + 64 * mb + 32 * hh),
+          tmem_st32(tmem_addr(tmem, lane_base, Cfg::tst(mb) + 32 * hh),
                     reinterpret_cast<const uint32_t*>(v));
         if (MODE != kState) put_tile_half(f, hh, v);
-        if (MODE == kReadout && x.g == 0 && p.fin_state)
-          write_half(p.fin_state + x.bh * (int64_t)(DP * kD), f, hh, v);
       }
       if (MODE != kReadout) {
-        const uint32_t zo = __float_as_uint(zf);
+        const uint32_t zo = __float_as_uint(zsum);
         asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(
-                         tmem_addr(tmem, lane_base, Cfg::TZ + 16 * mb)),
+                         tmem_addr(tmem, lane_base, Cfg::tz(mb))),
                      "r"(zo)
                      : "memory");
       }
-      if (MODE != kState) zb[f] = __float2bfloat16_rn(zf);
-      if (MODE == kReadout && x.g == 0 && p.fin_state) p.fin_z[x.bh * DP + f] = zf;
+      if (MODE != kState) zf[f] = zsum;
     }
+    if (MODE == kCausal) zero_rowsum();
     if (MODE != kReadout) tmem_st_wait();
     fence_proxy_async_smem();
     tc_fence_before();
@@ -526,8 +580,9 @@ __device__ __forceinline__ void role_rows(const PCtx& x, const PParams& p, int w
     tc_fence_after();
     float* dS = p.ws_state + (agg0 + x.g) * (int64_t)(DP * kD);
     for (int mb = 0; mb < Cfg::MB; ++mb) {
-      const float zf = drain_state(mb, [&](int f, int hh, const float* v) { write_half(dS, f, hh, v); });
-      p.ws_z[(agg0 + x.g) * DP + 128 * mb + r] = zf;
+      const float zsum =
+          drain_state(mb, [&](int f, int hh, const float* v) { write_half(dS, f, hh, v); });
+      p.ws_z[(agg0 + x.g) * DP + 128 * mb + r] = zsum;
     }
     return;
   }
@@ -540,9 +595,8 @@ __device__ __forceinline__ void role_rows(const PCtx& x, const PParams& p, int w
         if (!warp_wait(&bar[B_SEMPTY], (c - 1) & 1, st, ab)) return;
         tc_fence_after();
         for (int mb = 0; mb < Cfg::MB; ++mb) {
-          const float zf =
+          zf[128 * mb + r] =
               drain_state(mb, [&](int f, int hh, const float* v) { put_tile_half(f, hh, v); });
-          zb[128 * mb + r] = __float2bfloat16_rn(zf);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -583,10 +637,15 @@ __device__ __forceinline__ void role_rows(const PCtx& x, const PParams& p, int w
     // ---- epilogue: o = num / den → bf16, row r straight to global memory
     if (!warp_wait(&bar[B_NUMFULL], c & 1, st, ab)) return;
     tc_fence_after();
-    uint32_t den = 0;
-    tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TR), den);
-    tmem_ld_wait();
-    const float inv_den = 1.f / __uint_as_float(den);
+    uint32_t psum = 0;
+    if (MODE == kCausal) {
+      tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TR), psum);
+      tmem_ld_wait();
+    }
+    // q'·z: the φ warps' partials, published with q_ready of this chunk
+    if (!warp_wait(&bar[B_QREADY], c & 1, st, ab)) return;
+    const float qz = qzbuf[((c & 1) * 2) * kC + r] + qzbuf[((c & 1) * 2 + 1) * kC + r];
+    const float inv_den = 1.f / (__uint_as_float(psum) + qz);
     const int64_t row = x.t_begin + (int64_t)c * kC + r;
     const bool valid = row < x.t_end;
     uint4* orow = reinterpret_cast<uint4*>(p.out + (x.bh * p.n + (valid ? row : 0)) * kD);
@@ -603,6 +662,10 @@ __device__ __forceinline__ void role_rows(const PCtx& x, const PParams& p, int w
         if (valid) __stcs(orow + (j0 + q8 * 8) / 8, pack8(f));
       }
     }
+    if (MODE == kCausal) {
+      zero_rowsum();
+      tmem_st_wait();
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[B_NUMEMPTY]);
@@ -613,8 +676,9 @@ __device__ __forceinline__ void role_rows(const PCtx& x, const PParams& p, int w
     tc_fence_after();
     float* dS = p.fin_state + x.bh * (int64_t)(DP * kD);
     for (int mb = 0; mb < Cfg::MB; ++mb) {
-      const float zf = drain_state(mb, [&](int f, int hh, const float* v) { write_half(dS, f, hh, v); });
-      p.fin_z[x.bh * DP + 128 * mb + r] = zf;
+      const float zsum =
+          drain_state(mb, [&](int f, int hh, const float* v) { write_half(dS, f, hh, v); });
+      p.fin_z[x.bh * DP + 128 * mb + r] = zsum;
     }
   }
 }
@@ -651,7 +715,7 @@ tcp_forward_kernel(const __grid_constant__ CUtensorMap map_q,
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
       if (i == B_QEMPTY0 || i == B_QEMPTY1 || i == B_KEMPTY0 || i == B_KEMPTY1) cnt = 1 + 8;
-      if (i == B_PJEMPTY0 || i == B_PJEMPTY1 || i == B_KREADY || i == B_QREADY) cnt = 8;
+      if (i == B_PKEMPTY || i == B_PQEMPTY || i == B_KREADY || i == B_QREADY) cnt = 8;
       if (i == B_PREADY || i == B_NUMEMPTY || i == B_SCONV || i == B_SREADY) cnt = 4;
       // released by two MMA chains in the causal mode: φ(K) (scores, ΔS), V (ΔS, P·V)
       if ((i == B_KPEMPTY || i == B_VEMPTY0 || i == B_VEMPTY1) && MODE == kCausal) cnt = 2;
@@ -665,13 +729,10 @@ tcp_forward_kernel(const __grid_constant__ CUtensorMap map_q,
     tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 2) {
-    uint32_t* ones = reinterpret_cast<uint32_t*>(x.sm + Cfg::oONES);
-    for (int i = lane; i < 32; i += 32) ones[i] = 0x3F803F80u;   // bf16 1.0 pairs
-    // z operand and its read-past bytes (columns never read, kept finite)
-    uint32_t* zw = reinterpret_cast<uint32_t*>(x.sm + Cfg::oZB);
-    for (int i = lane; i < (2 * DP + 128) / 4; i += 32) zw[i] = 0u;
-    fence_proxy_async_smem();
+  {
+    uint32_t* vone = reinterpret_cast<uint32_t*>(x.sm + Cfg::oVONE);
+    for (int i = tid; i < Cfg::TILE / 4; i += kThreads) vone[i] = 0x3F803F80u;   // bf16 1.0 pairs
+    fence_proxy_async_smem();                     // read by the tensor core
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_w);
@@ -733,7 +794,7 @@ cudaError_t launch(const PParams& p, dim3 grid, bool dependent, const CUtensorMa
 
 template <int DP>
 cudaError_t run(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
-                const SegmentPlan& plan) {
+                float* tot_state, float* tot_z, const SegmentPlan& plan) {
   const int64_t BH = a.B * a.H;
   CUtensorMap mq, mk, mv, mw;
   cudaError_t e;
@@ -748,6 +809,8 @@ cudaError_t run(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* w
   p.nseg = plan.nseg;
   p.ws_state = ws_state;
   p.ws_z = ws_z;
+  p.tot_state = tot_state;
+  p.tot_z = tot_z;
   p.fin_state = a.mu_out;
   p.fin_z = a.nu_out;
   p.half_log2m = 0.5f * log2f((float)DP);
@@ -755,14 +818,22 @@ cudaError_t run(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* w
   const unsigned ubh = (unsigned)BH;
   if (a.causal) {
     if (plan.nseg > 1) {
-      // aggregates of segments 0 … nseg−2 (nothing follows the last one)
+      // aggregates of segments 0 … nseg−2 (nothing follows the last one),
+      // then their exclusive prefixes in place
       e = launch<DP, kState>(p, dim3(ubh, (unsigned)(plan.nseg - 1)), false, mq, mk, mv, mw, stream);
+      if (e != cudaSuccess) return e;
+      e = segment_scan(ws_state, ws_z, nullptr, nullptr, a.B * a.H, a.H, plan.nseg, plan.nseg - 1,
+                       plan.seg_len, a.n, DP, kD, nullptr, stream, true);
       if (e != cudaSuccess) return e;
     }
     return launch<DP, kCausal>(p, dim3(ubh, (unsigned)plan.nseg), plan.nseg > 1, mq, mk, mv, mw,
                                stream);
   }
+  // non-causal: all the aggregates, their total (the final state) by the scan
   e = launch<DP, kState>(p, dim3(ubh, (unsigned)plan.nseg), false, mq, mk, mv, mw, stream);
+  if (e != cudaSuccess) return e;
+  e = segment_scan(ws_state, ws_z, tot_state, tot_z, a.B * a.H, a.H, plan.nseg, plan.nseg,
+                   plan.seg_len, a.n, DP, kD, nullptr, stream, true);
   if (e != cudaSuccess) return e;
   return launch<DP, kReadout>(p, dim3(ubh, (unsigned)plan.nseg), true, mq, mk, mv, mw, stream);
 }
@@ -775,9 +846,10 @@ bool tc_performer_supported(const FwdArgs& a) {
 }
 
 cudaError_t tc_performer_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state,
-                                 float* ws_z, const SegmentPlan& plan) {
-  if (a.m == 256) return run<256>(a, stream, ws_state, ws_z, plan);
-  if (a.m == 128) return run<128>(a, stream, ws_state, ws_z, plan);
+                                 float* ws_z, float* tot_state, float* tot_z,
+                                 const SegmentPlan& plan) {
+  if (a.m == 256) return run<256>(a, stream, ws_state, ws_z, tot_state, tot_z, plan);
+  if (a.m == 128) return run<128>(a, stream, ws_state, ws_z, tot_state, tot_z, plan);
   return cudaErrorInvalidValue;
 }
 

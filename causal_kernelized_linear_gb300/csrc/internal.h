@@ -71,7 +71,8 @@ cudaError_t tc_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state, f
 // m ∈ {128, 256}, no decay, n ≥ 128; causal and non-causal).
 bool tc_performer_supported(const FwdArgs& a);
 cudaError_t tc_performer_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state,
-                                 float* ws_z, const SegmentPlan& plan);
+                                 float* ws_z, float* tot_state, float* tot_z,
+                                 const SegmentPlan& plan);
 
 // TMA tensor maps (bf16, 128-byte swizzle, boxes 64 elements wide):
 //   tmap_rows:   [BH, n, D] as a 3-D tensor, box 64 × rows × 1 (rows past n
@@ -84,10 +85,12 @@ cudaError_t tmap_matrix(CUtensorMap* m, const void* base, int64_t rows, int64_t 
 // place.  Only the first nagg aggregates are read (nagg = nseg − 1 when the
 // last segment's aggregate was not computed: the exclusive prefixes do not
 // need it); the inclusive total (final state) is written when tot_state !=
-// nullptr and nagg == nseg.
+// nullptr and nagg == nseg.  `dependent` launches it as a programmatic
+// dependent of the preceding launch (which must be this library's kernel
+// that wrote the aggregates); the launch after it may then start early too.
 cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* tot_z,
                          int64_t BH, int64_t H, int nseg, int nagg, int64_t seg_len, int64_t n,
-                         int dp, int d, const float* decay, cudaStream_t stream);
+                         int dp, int d, const float* decay, cudaStream_t stream, bool dependent);
 
 // la_forward with a fixed workspace of ws_floats floats, fetched through
 // get_ws only when the plan needs it, instead of stream-ordered allocations
