@@ -448,6 +448,16 @@ def run_profile_case(case):
         for causal in (True, False):
             for _ in range(3):
                 cl.forward(g["q"], g["k"], g["v"], None, "performer", g["omega"], causal, out=out)
+    elif case == "performer-decode-small":
+        w = W.PERFORMER_DECODE
+        B = 64                                       # B64 H32 d64 m256: 128 MiB of state
+        pre = W.decode_prefill_inputs(w, B=B)
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in pre.items()}
+        _, mu, nu = cl.forward_with_state(g["q"], g["k"], g["v"], g["a"], "performer", g["omega"])
+        for step in range(5):
+            st = {k: v.to(dev) for k, v in W.decode_step_inputs(w, step, B=B).items()}
+            cl.decode_step(mu, nu, st["q"], st["k"], st["v"], g["a"], feature_map="performer",
+                           omega=g["omega"])
     elif case == "decode-small":
         w = W.DECODE
         B = 64                                       # B64 H32 d128: 128 MiB of state
@@ -475,7 +485,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile-case", choices=["forward-long-small", "performer", "decode-small"],
+    ap.add_argument("--profile-case", choices=["forward-long-small", "performer", "decode-small",
+                                               "performer-decode-small"],
                     default=None,
                     help="run a small seeded case for an ncu capture and exit")
     args = ap.parse_args()
