@@ -13,13 +13,20 @@ converts numpy arrays.  Sources, cited by page title and equation:
   readout o_j = q'_j·μ_j / q'_j·ν_j (causal) or with μ_n, ν_n (non-causal).
 * "Linear Attention Research 2026", "Linear Transformer": φ(x) = elu(x)+1;
   "Performer random features": φ(x) = exp(xω − ½‖x‖²)/√m.
+* Per-token decay: "Efficient Transformers II" eq (4), z_i = a·z_{i−1} + b·s_i,
+  with a and b indexed by the token (the input-dependent step of the Mamba
+  section of "Linear Attention Research 2026"): μ_i = a_i μ_{i−1} + b_i k'_iᵀv_i,
+  b_i = 1 − a_i unless given.
 
 Parity pins (tests/test_oracle.py): brute-force quadratic form of
 "Efficient Transformers I" eq (25)–(26) with the causal decay mask, also in
 exact rational arithmetic; a = 0 ⇒ o_j = v_j; eq (6) as dense matrix
 products; ν_j > 0 and convex-combination bounds; the Performer expectation
 closed form and its m^{-1/2} convergence; ω = 0 and single-entry ω closed
-forms; the exported state against Σ_i a^{n−i}(1−a) k'_iᵀ v_i.
+forms; the exported state against Σ_i a^{n−i}(1−a) k'_iᵀ v_i.  Per-token decay:
+the quadratic form with weights b_s·Π_{s<j≤t} a_j by brute force and in exact
+rationals, reduction to the per-head oracle for constant a, the reset at
+a_i = 0, a single weighted token, and the state closed form.
 """
 from __future__ import annotations
 
@@ -75,6 +82,10 @@ def _load():
             lib.oracle_decode_step_fm.argtypes = [i64, i64, i64, ctypes.c_int, i64, dp, dp, dp,
                                                   dp, dp, dp, dp, dp]
             lib.oracle_decode_step_fm.restype = ctypes.c_int
+            lib.oracle_forward_token_decay.argtypes = [i64, i64, i64, i64, ctypes.c_int, i64,
+                                                       dp, dp, dp, dp, dp, dp, dp, dp,
+                                                       dp, dp, dp]
+            lib.oracle_forward_token_decay.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -175,3 +186,60 @@ def decode_step(mu, nu, q, k, v, decay_a=None, feature_map="elu1", omega=None):
     if rc != 0:
         raise ValueError(f"oracle_decode_step rejected its arguments (rc={rc})")
     return out, mu, nu
+
+
+def forward_token_decay(q, k, v, decay_a, weight_b=None, feature_map="elu1", omega=None,
+                        mu0=None, nu0=None, return_state=False):
+    """Causal recurrence with a per-token decay in fp64.
+
+    q, k, v: [B, H, n, d]; decay_a: [B, H, n] with values in [0, 1];
+    weight_b: [B, H, n] (≥ 0) or None for b_i = 1 − a_i; omega [d, m] for the
+    Performer map.  Returns out [B, H, n, d] and, with ``return_state``, the
+    final (μ [B, H, d', d], ν [B, H, d']).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, n, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share the shape [B, H, n, d]")
+    a = _f64(decay_a)
+    b = _f64(weight_b)
+    if a is None or a.shape != (B, H, n):
+        raise ValueError("decay_a must have the shape [B, H, n]")
+    if b is not None and b.shape != (B, H, n):
+        raise ValueError("weight_b must have the shape [B, H, n]")
+    fm = _fm(feature_map)
+    omega = _f64(omega)
+    if fm == FM_PERFORMER and omega is None:
+        raise ValueError("the Performer map needs omega [d, m]")
+    m = omega.shape[1] if fm == FM_PERFORMER else 0
+    dp = d if fm == FM_ELU1 else m
+    mu0 = _f64(mu0)
+    nu0 = _f64(nu0)
+    out = np.empty((B, H, n, d), dtype=np.float64)
+    mu = np.empty((B, H, dp, d), dtype=np.float64)
+    nu = np.empty((B, H, dp), dtype=np.float64)
+    rc = _load().oracle_forward_token_decay(B, H, n, d, fm, m, _ptr(q), _ptr(k), _ptr(v),
+                                            _ptr(a), _ptr(b), _ptr(omega), _ptr(mu0),
+                                            _ptr(nu0), _ptr(out), _ptr(mu), _ptr(nu))
+    if rc != 0:
+        raise ValueError(f"oracle_forward_token_decay rejected its arguments (rc={rc})")
+    if return_state:
+        return out, mu, nu
+    return out
+
+
+def decode_step_token_decay(mu, nu, q, k, v, decay_a, weight_b=None, feature_map="elu1",
+                            omega=None):
+    """One recurrent step with this token's decay a [B, H] (and weight b
+    [B, H], default 1 − a): returns (out [B,H,d], μ', ν') without modifying
+    the inputs."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, d = q.shape
+    a = _f64(decay_a)
+    b = _f64(weight_b)
+    out, mu2, nu2 = forward_token_decay(
+        q[:, :, None, :], k[:, :, None, :], v[:, :, None, :],
+        None if a is None else a.reshape(B, H, 1),
+        None if b is None else b.reshape(B, H, 1),
+        feature_map, omega, mu0=mu, nu0=nu, return_state=True)
+    return out[:, :, 0, :], mu2, nu2

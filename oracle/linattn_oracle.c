@@ -12,7 +12,8 @@
  *   [ET-I]   "Efficient Transformers I" (blog-8pb.pages.dev, .../efficient1/),
  *            kernelized attention, eq (22)–(27).
  *   [LAR]    "Linear Attention Research 2026" (guijiagi.com), sections
- *            "Performer random features" and "Linear Transformer".
+ *            "Performer random features" and "Linear Transformer"; the
+ *            selective (input-dependent) state update of its Mamba section.
  *
  * Conventions: row vectors; q_j, k_j, v_j in R^{1×d}; φ: R^d → R^{d'}; the
  * state μ is d'×d (row i = feature i, column c = value column c), ν is d'.
@@ -27,6 +28,12 @@
  *     ([ET-II] the causal form stated after eq (9)).
  *   - No ε is added to the normalizer.
  *   - Non-causal mode is eq (6)/(9) with μ_n, ν_n and no decay.
+ *   - Per-token decay: [ET-II] eq (4), z_i = a·z_{i−1} + b·s_i, with a and b
+ *     indexed by the token (the input-dependent step of [LAR]'s Mamba
+ *     section) and s_i = k'_iᵀv_i (resp. k'_iᵀ): μ_i = a_i μ_{i−1} + b_i k'_iᵀv_i.
+ *     When b is not given, b_i = 1 − a_i (eq (10)–(11) per token), with no
+ *     special case at a_i = 1: such a token is skipped, it does not restart
+ *     the plain running sum.
  *
  * parity pins: every function here is pinned by the CPU tests (quadratic form
  * of [ET-I] eq (25)–(26) by brute force and in exact rationals, the a = 0
@@ -212,4 +219,88 @@ int oracle_decode_step_fm(int64_t B, int64_t H, int64_t d, int fm, int64_t m, do
                           double* nu, const double* q, const double* k, const double* v,
                           const double* a, const double* omega, double* out) {
   return oracle_forward(B, H, 1, d, fm, m, q, k, v, a, omega, 1, mu, nu, out, mu, nu);
+}
+
+/*
+ * One head with a per-token decay a_i and input weight b_i ([ET-II] eq (4)
+ * with a, b indexed by the token; the readout after eq (9)):
+ *     k' = φ(k_i);  μ ← a_i·μ + b_i·k'^T v_i;  ν ← a_i·ν + b_i·k'^T;
+ *     q' = φ(q_i);  o_i = (q'·μ) / (q'·ν).
+ * a, b point at this head's n values; b == NULL means b_i = 1 − a_i.
+ */
+static void one_head_token(int64_t n, int64_t d, int64_t dp, int fm, int64_t m,
+                           const double* q, const double* k, const double* v,
+                           const double* a, const double* b, const double* omega,
+                           double* mu, double* nu, double* out, double* kf, double* qf) {
+  for (int64_t j = 0; j < n; ++j) {
+    const double aj = a[j];
+    const double bj = b ? b[j] : 1.0 - aj;
+    phi_row(fm, k + j * d, d, omega, m, kf);
+    for (int64_t i = 0; i < dp; ++i) {
+      for (int64_t c = 0; c < d; ++c) {
+        mu[i * d + c] = aj * mu[i * d + c] + bj * kf[i] * v[j * d + c];
+      }
+      nu[i] = aj * nu[i] + bj * kf[i];
+    }
+    phi_row(fm, q + j * d, d, omega, m, qf);
+    double den = 0.0;
+    for (int64_t i = 0; i < dp; ++i) den += qf[i] * nu[i];
+    for (int64_t c = 0; c < d; ++c) {
+      double num = 0.0;
+      for (int64_t i = 0; i < dp; ++i) num += qf[i] * mu[i * d + c];
+      out[j * d + c] = num / den;
+    }
+  }
+}
+
+/*
+ * Causal forward with a per-token decay over B·H independent heads.
+ *   q, k, v   [B,H,n,d]
+ *   a         [B,H,n] decays a_i ∈ [0, 1]
+ *   b         [B,H,n] input weights b_i ≥ 0, or NULL for b_i = 1 − a_i
+ *   omega     [d,m] for Performer, else NULL
+ *   mu0, nu0  initial state [B,H,d',d], [B,H,d'], or NULL for zero
+ *   out       [B,H,n,d];  mu_out, nu_out  final state, or NULL
+ * Returns 0 on success, 1 on invalid arguments (unknown feature map, missing
+ * ω, a missing a, a decay outside [0, 1] or a negative or non-finite weight).
+ */
+int oracle_forward_token_decay(int64_t B, int64_t H, int64_t n, int64_t d, int fm, int64_t m,
+                               const double* q, const double* k, const double* v,
+                               const double* a, const double* b, const double* omega,
+                               const double* mu0, const double* nu0,
+                               double* out, double* mu_out, double* nu_out) {
+  if (fm != OR_FM_ELU1 && fm != OR_FM_PERFORMER) return 1;
+  if (fm == OR_FM_PERFORMER && (omega == NULL || m <= 0)) return 1;
+  if (a == NULL) return 1;
+  for (int64_t i = 0; i < B * H * n; ++i) {
+    if (!(a[i] >= 0.0 && a[i] <= 1.0)) return 1;
+    if (b && !(b[i] >= 0.0 && isfinite(b[i]))) return 1;
+  }
+  const int64_t dp = feature_dim(fm, d, m);
+  int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bh = 0; bh < B * H; ++bh) {
+    double* mu = (double*)malloc((size_t)(dp * d) * sizeof(double));
+    double* nu = (double*)malloc((size_t)dp * sizeof(double));
+    double* kf = (double*)malloc((size_t)dp * sizeof(double));
+    double* qf = (double*)malloc((size_t)dp * sizeof(double));
+    if (!mu || !nu || !kf || !qf) {
+      failed = 1;
+    } else {
+      if (mu0) memcpy(mu, mu0 + bh * dp * d, (size_t)(dp * d) * sizeof(double));
+      else memset(mu, 0, (size_t)(dp * d) * sizeof(double));
+      if (nu0) memcpy(nu, nu0 + bh * dp, (size_t)dp * sizeof(double));
+      else memset(nu, 0, (size_t)dp * sizeof(double));
+      one_head_token(n, d, dp, fm, m, q + bh * n * d, k + bh * n * d, v + bh * n * d,
+                     a + bh * n, b ? b + bh * n : NULL, omega, mu, nu, out + bh * n * d,
+                     kf, qf);
+      if (mu_out) memcpy(mu_out + bh * dp * d, mu, (size_t)(dp * d) * sizeof(double));
+      if (nu_out) memcpy(nu_out + bh * dp, nu, (size_t)dp * sizeof(double));
+    }
+    free(mu);
+    free(nu);
+    free(kf);
+    free(qf);
+  }
+  return failed ? 2 : 0;
 }
