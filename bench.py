@@ -6,7 +6,8 @@ a ~ U[0.95, 0.9999], fp32 state) — the n ≥ 16K configuration at which the
 forward metric is quoted.  A step is one la_forward over the whole batch.
 Secondary lines (same JSON object, key "secondary") time the other
 workloads: elu+1 with decay at n=2048, Performer (m=256) causal and
-non-causal, and the recurrent decode step (B=256, H=32, d=128).
+non-causal, the long shape with a per-token decay and input weight, and the
+recurrent decode step (B=256, H=32, d=128; and Performer, d=64, m=256).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -219,6 +220,28 @@ def bench_forward(cl, w, causal, steps, warmup, stream, flush_l2, peaks, want_e2
     return res
 
 
+def bench_token_decay(cl, tw: W.TokenDecayWorkload, steps, warmup, stream):
+    """la_forward_token_decay over the whole batch: per-token a and b [B,H,n]
+    fp32.  Algorithmic bytes: q, k, v read and o written (bf16) plus a and b
+    read (fp32) per token-head."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = W.token_decay_inputs(tw)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out = torch.empty_like(g["q"])
+    w = tw.base
+
+    def step():
+        cl.forward_token_decay(g["q"], g["k"], g["v"], g["a_tok"], g["b_tok"], "elu1", None,
+                               out=out, stream=stream)
+
+    ms, launches = _time_steps(step, steps, warmup, stream, None, cl.launch_count)
+    th = w.B * w.H * w.n
+    flops, nbytes = _fwd_alg(w)
+    nbytes += th * 4 * (2 if tw.weight else 1)
+    return {"ms": ms, "avg_ms": statistics.mean(ms), "flops": flops, "bytes": nbytes,
+            "launches_per_step": launches / steps, "tokens": w.B * w.n}
+
+
 def bench_forward_e2e(cl, w, causal, inp, steps, warmup, stream):
     """Same forward through the public API with host buffers: every step copies
     q, k, v from pinned host memory, runs la_forward and copies o back."""
@@ -392,6 +415,19 @@ def run_ours(args, rank, world, dist):
                 "frac_bf16_peak": fl / peaks["bf16_tflops"], "gbs_alg": gbs,
                 "frac_hbm": gbs / peaks["hbm_gbs"], "l2": "flushed between steps",
                 "launches_per_step": r["launches_per_step"]})
+        tw = W.TOKEN_DECAY_LONG
+        r = bench_token_decay(cl, tw, max(args.steps, 20), max(args.warmup, 3), stream)
+        secs = r["avg_ms"] / 1e3
+        gbs = r["bytes"] / secs / 1e9
+        fl = r["flops"] / secs / 1e12
+        secondary.append({
+            "workload": tw.name, "causal": True, "value": r["tokens"] / secs, "unit": "tokens/s",
+            "ms_per_step": r["avg_ms"], "tflops_alg": fl,
+            "frac_bf16_peak": fl / peaks["bf16_tflops"], "gbs_alg": gbs,
+            "frac_hbm": gbs / peaks["hbm_gbs"],
+            "decay": "per token: a = exp(-A_h*softplus(z-4)), b = softplus(z-4)",
+            "l2": "inputs (776 MiB) larger than L2; no flush",
+            "launches_per_step": r["launches_per_step"]})
         for dw in (W.DECODE, W.PERFORMER_DECODE):
             d = bench_decode(cl, dw, stream)
             secs = d["avg_ms"] / 1e3
@@ -458,6 +494,14 @@ def run_profile_case(case):
             st = {k: v.to(dev) for k, v in W.decode_step_inputs(w, step, B=B).items()}
             cl.decode_step(mu, nu, st["q"], st["k"], st["v"], g["a"], feature_map="performer",
                            omega=g["omega"])
+    elif case == "token-decay-small":
+        tw = W.TOKEN_DECAY_LONG
+        inp = W.token_decay_inputs(tw, n=32768)     # B1 H16 n32768 d128 + a, b: 516 MiB
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        out = torch.empty_like(g["q"])
+        for _ in range(3):
+            cl.forward_token_decay(g["q"], g["k"], g["v"], g["a_tok"], g["b_tok"], "elu1", None,
+                                   out=out)
     elif case == "decode-small":
         w = W.DECODE
         B = 64                                       # B64 H32 d128: 128 MiB of state
@@ -486,7 +530,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile-case", choices=["forward-long-small", "performer", "decode-small",
-                                               "performer-decode-small"],
+                                               "performer-decode-small", "token-decay-small"],
                     default=None,
                     help="run a small seeded case for an ncu capture and exit")
     args = ap.parse_args()

@@ -32,7 +32,7 @@ _DT = {torch.bfloat16: LA_BF16, torch.float32: LA_F32}
 
 EXPORTED = ("la_forward", "la_forward_with_state", "la_decode_step", "la_status_string",
             "la_get_last_device_status", "la_launch_count", "la_selftest_wait_timeout",
-            "la_decode_step_fm")
+            "la_decode_step_fm", "la_forward_token_decay", "la_decode_step_token_decay")
 
 
 class LinAttnError(RuntimeError):
@@ -79,6 +79,11 @@ def load():
         lib.la_decode_step.restype = ctypes.c_int
         lib.la_decode_step_fm.argtypes = [vp, vp, P, P, P, vp, ctypes.c_int, P, P, vp]
         lib.la_decode_step_fm.restype = ctypes.c_int
+        lib.la_forward_token_decay.argtypes = [P, P, P, vp, vp, ctypes.c_int, P, P, vp, vp, vp]
+        lib.la_forward_token_decay.restype = ctypes.c_int
+        lib.la_decode_step_token_decay.argtypes = [vp, vp, P, P, P, vp, vp, ctypes.c_int, P, P,
+                                                   vp]
+        lib.la_decode_step_token_decay.restype = ctypes.c_int
         lib.la_status_string.argtypes = [ctypes.c_int]
         lib.la_status_string.restype = ctypes.c_char_p
         lib.la_get_last_device_status.argtypes = [vp]
@@ -229,6 +234,83 @@ def decode_step(mu, nu, q, k, v, decay_a=None, out=None, stream=None, feature_ma
                                       ctypes.byref(om) if om is not None else None,
                                       ctypes.byref(od), _stream_handle(stream))
         _check("la_decode_step_fm", st)
+    return out
+
+
+def _tok_ptrs(name_a, a, name_b, b, shape):
+    _need_cuda(name_a, a, torch.float32)
+    if tuple(a.shape) != tuple(shape):
+        raise ValueError(f"{name_a} must have the shape {tuple(shape)}")
+    bptr = None
+    if b is not None:
+        _need_cuda(name_b, b, torch.float32)
+        if tuple(b.shape) != tuple(shape):
+            raise ValueError(f"{name_b} must have the shape {tuple(shape)}")
+        bptr = b.data_ptr()
+    return a.data_ptr(), bptr
+
+
+def forward_token_decay(q, k, v, decay_a, weight_b=None, feature_map="elu1", omega=None,
+                        out=None, return_state=False, stream=None):
+    """la_forward_token_decay: causal forward with a per-token decay a [B,H,n]
+    fp32 and input weight b [B,H,n] fp32 (None: 1 − a).  Returns out, or
+    (out, μ, ν) with ``return_state``."""
+    out, fm, _, om, qd, kd, vd, od = _forward_args(q, k, v, None, feature_map, omega, out)
+    B, H, n, d = q.shape
+    aptr, bptr = _tok_ptrs("decay_a", decay_a, "weight_b", weight_b, (B, H, n))
+    mu_out = nu_out = None
+    if return_state:
+        dp = d if fm == LA_FM_ELU1 else omega.shape[1]
+        mu_out = torch.empty(B, H, dp, d, device=q.device, dtype=torch.float32)
+        nu_out = torch.empty(B, H, dp, device=q.device, dtype=torch.float32)
+    st = load().la_forward_token_decay(
+        ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), aptr, bptr, fm,
+        ctypes.byref(om) if om is not None else None, ctypes.byref(od),
+        mu_out.data_ptr() if return_state else None,
+        nu_out.data_ptr() if return_state else None, _stream_handle(stream))
+    _check("la_forward_token_decay", st)
+    if return_state:
+        return out, mu_out, nu_out
+    return out
+
+
+def decode_step_token_decay(mu, nu, q, k, v, decay_a, weight_b=None, out=None, stream=None,
+                            feature_map="elu1", omega=None):
+    """la_decode_step_token_decay: one step with this token's decay a [B,H]
+    and weight b [B,H] (None: 1 − a); state updated in place.  Returns out."""
+    _need_cuda("mu", mu, torch.float32)
+    _need_cuda("nu", nu, torch.float32)
+    for nm, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(nm, t)
+    if q.dim() == 3:
+        shape4 = (q.shape[0], q.shape[1], 1, q.shape[2])
+    elif q.dim() == 4:
+        shape4 = tuple(q.shape)
+    else:
+        raise ValueError("q must be [B,H,d] or [B,H,1,d]")
+    B, H, _, d = shape4
+    fm = _FM[feature_map] if isinstance(feature_map, str) else int(feature_map)
+    dp = d
+    om = None
+    if omega is not None:
+        _need_cuda("omega", omega)
+        if omega.dim() != 2:
+            raise ValueError("omega must be [d, m]")
+        dp = int(omega.shape[1])
+        om = LaTensor(omega.data_ptr(), _DT[omega.dtype], 1, 1, int(omega.shape[0]), dp)
+    if tuple(mu.shape) != (B, H, dp, d) or tuple(nu.shape) != (B, H, dp):
+        raise ValueError("mu must be [B,H,d',d] and nu [B,H,d']")
+    aptr, bptr = _tok_ptrs("decay_a", decay_a, "weight_b", weight_b, (B, H))
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda("out", out)
+    qd, kd, vd = (_desc(t, shape4) for t in (q, k, v))
+    od = _desc(out, shape4)
+    st = load().la_decode_step_token_decay(mu.data_ptr(), nu.data_ptr(), ctypes.byref(qd),
+                                           ctypes.byref(kd), ctypes.byref(vd), aptr, bptr, fm,
+                                           ctypes.byref(om) if om is not None else None,
+                                           ctypes.byref(od), _stream_handle(stream))
+    _check("la_decode_step_token_decay", st)
     return out
 
 

@@ -105,6 +105,9 @@ la_status validate_forward(const la_tensor* q, const la_tensor* k, const la_tens
   a->v = v->data;
   a->out = out->data;
   a->decay = decay_a;
+  a->tok_decay = nullptr;
+  a->tok_weight = nullptr;
+  a->ws_ld = nullptr;
   a->omega = omega ? omega->data : nullptr;
   a->B = q->B;
   a->H = q->H;
@@ -193,6 +196,9 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
   size_t ws_floats = 0;
   if (need_ws) ws_floats += (size_t)BH * plan.nseg * (state_elems + a.dp);
   if (need_tot) ws_floats += (size_t)BH * (state_elems + a.dp);
+  // per-token decay: the log2 decay of every segment, beside its aggregate
+  const bool need_ld = a.tok_decay != nullptr && plan.nseg > 1;
+  if (need_ld) ws_floats += (size_t)BH * plan.nseg;
   float* ws = nullptr;
   if (ws_floats) {
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_floats * sizeof(float), stream);
@@ -209,6 +215,7 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
     tot_state = ws + (size_t)BH * plan.nseg * (state_elems + a.dp);
     tot_z = tot_state + (size_t)BH * state_elems;
   }
+  if (need_ld) a.ws_ld = ws + (size_t)BH * plan.nseg * (state_elems + a.dp);
   cudaError_t e = dispatch_forward(a, pp, stream, ws_state, ws_z, tot_state, tot_z);
   if (ws) {
     cudaError_t f = cudaFreeAsync(ws, stream);
@@ -299,51 +306,104 @@ la_status la_forward_with_state(const la_tensor* q, const la_tensor* k, const la
   return la::run_forward(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
-la_status la_decode_step_fm(float* mu, float* nu, const la_tensor* q, const la_tensor* k,
-                            const la_tensor* v, const float* decay_a, la_feature_map feature_map,
-                            const la_tensor* omega, la_tensor* out, la_stream stream) {
+la_status la_forward_token_decay(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                                 const float* decay_a, const float* weight_b,
+                                 la_feature_map feature_map, const la_tensor* omega,
+                                 la_tensor* out, float* mu_out, float* nu_out, la_stream stream) {
+  la::FwdArgs a;
+  la_status st = la::validate_forward(q, k, v, nullptr, feature_map, omega, 1, out, &a);
+  if (st != LA_OK) return st;
+  if (q->B * q->H * q->n > 0 && !decay_a) return LA_ERR_INVALID_ARG;
+  if (decay_a && (reinterpret_cast<uintptr_t>(decay_a) & 3u)) return LA_ERR_INVALID_ARG;
+  if (weight_b && (reinterpret_cast<uintptr_t>(weight_b) & 3u)) return LA_ERR_INVALID_ARG;
+  if ((mu_out == nullptr) != (nu_out == nullptr)) return LA_ERR_INVALID_ARG;
+  if (mu_out && (!la::aligned16(mu_out) || !la::aligned16(nu_out))) return LA_ERR_INVALID_ARG;
+  a.tok_decay = decay_a;
+  a.tok_weight = weight_b;
+  a.mu_out = mu_out;
+  a.nu_out = nu_out;
+  return la::run_forward(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+namespace la {
+namespace {
+
+// Checks shared by the decode entry points; fills everything in `a` but the
+// decay fields.
+la_status validate_decode(float* mu, float* nu, const la_tensor* q, const la_tensor* k,
+                          const la_tensor* v, la_feature_map feature_map, const la_tensor* omega,
+                          la_tensor* out, DecodeArgs* a) {
   if (!mu || !nu || !q || !k || !v || !out) return LA_ERR_INVALID_ARG;
-  if (!la::valid_dtype(q->dtype) || k->dtype != q->dtype || v->dtype != q->dtype ||
+  if (!valid_dtype(q->dtype) || k->dtype != q->dtype || v->dtype != q->dtype ||
       out->dtype != q->dtype)
     return LA_ERR_INVALID_ARG;
-  if (!la::same_shape(q, k) || !la::same_shape(q, v) || !la::same_shape(q, out))
-    return LA_ERR_INVALID_ARG;
+  if (!same_shape(q, k) || !same_shape(q, v) || !same_shape(q, out)) return LA_ERR_INVALID_ARG;
   if (q->B < 1 || q->H < 1 || q->n != 1) return LA_ERR_INVALID_ARG;
   if (q->B * q->H > ((int64_t)1 << 31) - 1) return LA_ERR_UNSUPPORTED;
-  if (!la::supported_width(q->d)) return LA_ERR_UNSUPPORTED;
+  if (!supported_width(q->d)) return LA_ERR_UNSUPPORTED;
   if (!q->data || !k->data || !v->data || !out->data) return LA_ERR_INVALID_ARG;
-  if (!la::aligned16(mu) || !la::aligned16(nu) || !la::aligned16(q->data) ||
-      !la::aligned16(k->data) || !la::aligned16(v->data) || !la::aligned16(out->data))
+  if (!aligned16(mu) || !aligned16(nu) || !aligned16(q->data) || !aligned16(k->data) ||
+      !aligned16(v->data) || !aligned16(out->data))
     return LA_ERR_INVALID_ARG;
-  if (decay_a && (reinterpret_cast<uintptr_t>(decay_a) & 3u)) return LA_ERR_INVALID_ARG;
   int m = 0;
   if (feature_map == LA_FM_PERFORMER) {
     if (!omega || !omega->data) return LA_ERR_INVALID_ARG;
     if (omega->dtype != q->dtype || omega->B != 1 || omega->H != 1 || omega->n != q->d)
       return LA_ERR_INVALID_ARG;
-    if (!la::aligned16(omega->data)) return LA_ERR_INVALID_ARG;
-    if (!la::supported_features(omega->d)) return LA_ERR_UNSUPPORTED;
+    if (!aligned16(omega->data)) return LA_ERR_INVALID_ARG;
+    if (!supported_features(omega->d)) return LA_ERR_UNSUPPORTED;
     m = (int)omega->d;
   } else if (feature_map == LA_FM_ELU1) {
     if (omega) return LA_ERR_INVALID_ARG;
   } else {
     return LA_ERR_INVALID_ARG;
   }
+  a->mu = mu;
+  a->nu = nu;
+  a->q = q->data;
+  a->k = k->data;
+  a->v = v->data;
+  a->out = out->data;
+  a->decay = nullptr;
+  a->weight = nullptr;
+  a->per_token = false;
+  a->omega = omega ? omega->data : nullptr;
+  a->B = q->B;
+  a->H = q->H;
+  a->d = (int)q->d;
+  a->m = m;
+  a->bf16 = q->dtype == LA_BF16;
+  a->performer = feature_map == LA_FM_PERFORMER;
+  return LA_OK;
+}
+
+}  // namespace
+}  // namespace la
+
+la_status la_decode_step_token_decay(float* mu, float* nu, const la_tensor* q,
+                                     const la_tensor* k, const la_tensor* v,
+                                     const float* decay_a, const float* weight_b,
+                                     la_feature_map feature_map, const la_tensor* omega,
+                                     la_tensor* out, la_stream stream) {
   la::DecodeArgs a;
-  a.mu = mu;
-  a.nu = nu;
-  a.q = q->data;
-  a.k = k->data;
-  a.v = v->data;
-  a.out = out->data;
+  la_status st = la::validate_decode(mu, nu, q, k, v, feature_map, omega, out, &a);
+  if (st != LA_OK) return st;
+  if (!decay_a || (reinterpret_cast<uintptr_t>(decay_a) & 3u)) return LA_ERR_INVALID_ARG;
+  if (weight_b && (reinterpret_cast<uintptr_t>(weight_b) & 3u)) return LA_ERR_INVALID_ARG;
   a.decay = decay_a;
-  a.omega = omega ? omega->data : nullptr;
-  a.B = q->B;
-  a.H = q->H;
-  a.d = (int)q->d;
-  a.m = m;
-  a.bf16 = q->dtype == LA_BF16;
-  a.performer = feature_map == LA_FM_PERFORMER;
+  a.weight = weight_b;
+  a.per_token = true;
+  return la::to_status(la::decode_step(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+la_status la_decode_step_fm(float* mu, float* nu, const la_tensor* q, const la_tensor* k,
+                            const la_tensor* v, const float* decay_a, la_feature_map feature_map,
+                            const la_tensor* omega, la_tensor* out, la_stream stream) {
+  la::DecodeArgs a;
+  la_status st = la::validate_decode(mu, nu, q, k, v, feature_map, omega, out, &a);
+  if (st != LA_OK) return st;
+  if (decay_a && (reinterpret_cast<uintptr_t>(decay_a) & 3u)) return LA_ERR_INVALID_ARG;
+  a.decay = decay_a;
   return la::to_status(la::decode_step(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

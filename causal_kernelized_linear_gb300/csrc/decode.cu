@@ -1,6 +1,9 @@
 // Recurrent decode step ("Efficient Transformers II" §2.2, eq (10)–(11) and
 // the causal readout of eq (9)) for B·H independent heads.  elu+1 map (d' = d):
 //   k' = φ(k), q' = φ(q);  μ ← a·μ + w·k'ᵀv;  ν ← a·ν + w·k';  o = q'μ / q'ν.
+// The decay a is the head's (w = 1 − a, or 1 when a = 1), or this token's own
+// a and weight w = b (default 1 − a) — eq (4) of the same page with a and b
+// indexed by the token.
 //
 // The step is bound by HBM: every head streams its d×d fp32 μ in and out once
 // (128 KiB of traffic at d = 128) against ~5·d² flops.  One CTA per head; each
@@ -18,6 +21,25 @@ namespace {
 
 constexpr int kDecThreads = 256;
 
+// Where a step's decay and new-token weight come from: per head (a [H], or
+// none for a = 1) or per token (a [B·H] and b [B·H] or none for b = 1 − a).
+struct StepDecay {
+  const float* a;
+  const float* b;
+  int64_t H;
+  bool per_token;
+};
+
+__device__ __forceinline__ void step_decay(const StepDecay& sd, int64_t bh, float& a, float& w) {
+  if (sd.per_token) {
+    a = sd.a[bh];
+    w = sd.b ? sd.b[bh] : 1.f - a;
+  } else {
+    a = sd.a ? sd.a[bh % sd.H] : 1.f;
+    w = new_token_weight(a);
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ float load_elem(const T* p, int64_t i) { return to_f32(p[i]); }
 
@@ -25,7 +47,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kDecThreads)
 decode_step_kernel(float* __restrict__ mu, float* __restrict__ nu, const T* __restrict__ q,
                    const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ out,
-                   const float* __restrict__ decay, int64_t H) {
+                   const StepDecay sd) {
   constexpr int CG = D / 4;                 // float4 column groups per row
   constexpr int RG = kDecThreads / CG;      // row groups
   constexpr int RPT = D / RG;               // rows per thread
@@ -45,8 +67,8 @@ decode_step_kernel(float* __restrict__ mu, float* __restrict__ nu, const T* __re
 #pragma unroll
   for (int r = 0; r < RPT; ++r) m[r] = __ldcs(mrow + (int64_t)(rg + r * RG) * CG + cg);
 
-  const float a = decay ? decay[bh % H] : 1.f;
-  const float w = new_token_weight(a);
+  float a, w;
+  step_decay(sd, bh, a, w);
   for (int i = tid; i < D; i += kDecThreads) {
     qf[i] = elu1(load_elem(q, bh * D + i));
     kf[i] = elu1(load_elem(k, bh * D + i));
@@ -123,7 +145,7 @@ template <typename T, int D, int M>
 __global__ void __launch_bounds__((PerfDecodeCfg<T, D, M>::NT))
 decode_performer_kernel(float* __restrict__ mu, float* __restrict__ nu, const T* __restrict__ q,
                         const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ out,
-                        const float* __restrict__ decay, const T* __restrict__ omega, int64_t H) {
+                        const StepDecay sd, const T* __restrict__ omega) {
   using Cfg = PerfDecodeCfg<T, D, M>;
   constexpr int NT = Cfg::NT, CG = Cfg::CG, RG = Cfg::RG, RPT = Cfg::RPT;
   __shared__ float xq[D], xk[D], vv[D];
@@ -142,8 +164,8 @@ decode_performer_kernel(float* __restrict__ mu, float* __restrict__ nu, const T*
 #pragma unroll
   for (int r = 0; r < RPT; ++r) m[r] = __ldcs(mrow + (int64_t)(rg + r * RG) * CG + cg);
 
-  const float a = decay ? decay[bh % H] : 1.f;
-  const float w = new_token_weight(a);
+  float a, w;
+  step_decay(sd, bh, a, w);
   for (int i = tid; i < D; i += NT) {
     xq[i] = load_elem(q, bh * D + i);
     xk[i] = load_elem(k, bh * D + i);
@@ -222,13 +244,22 @@ decode_performer_kernel(float* __restrict__ mu, float* __restrict__ nu, const T*
   }
 }
 
+StepDecay step_decay_of(const DecodeArgs& a) {
+  StepDecay sd;
+  sd.a = a.decay;
+  sd.b = a.weight;
+  sd.H = a.H;
+  sd.per_token = a.per_token;
+  return sd;
+}
+
 template <typename T, int D, int M>
 cudaError_t launch_perf_decode(const DecodeArgs& a, cudaStream_t s) {
   using Cfg = PerfDecodeCfg<T, D, M>;
   decode_performer_kernel<T, D, M><<<(unsigned)(a.B * a.H), Cfg::NT, 0, s>>>(
       a.mu, a.nu, static_cast<const T*>(a.q), static_cast<const T*>(a.k),
-      static_cast<const T*>(a.v), static_cast<T*>(a.out), a.decay,
-      static_cast<const T*>(a.omega), a.H);
+      static_cast<const T*>(a.v), static_cast<T*>(a.out), step_decay_of(a),
+      static_cast<const T*>(a.omega));
   count_launches(1);
   return cudaGetLastError();
 }
@@ -253,13 +284,13 @@ cudaError_t run_decode(const DecodeArgs& a, cudaStream_t s) {
   T* o = static_cast<T*>(a.out);
   switch (a.d) {
     case 32:
-      decode_step_kernel<T, 32><<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, a.decay, a.H);
+      decode_step_kernel<T, 32><<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, step_decay_of(a));
       break;
     case 64:
-      decode_step_kernel<T, 64><<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, a.decay, a.H);
+      decode_step_kernel<T, 64><<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, step_decay_of(a));
       break;
     case 128:
-      decode_step_kernel<T, 128><<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, a.decay, a.H);
+      decode_step_kernel<T, 128><<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, step_decay_of(a));
       break;
     default:
       return cudaErrorInvalidValue;

@@ -13,6 +13,13 @@
 // for fp32 inputs, where the parity bound (1e-4) rules out bf16 tensor-core
 // operands.
 //
+// Per-token decay (the same page's eq (4), z_i = a·z_{i−1} + b·s_i, with a and
+// b indexed by the token): with L_t = Σ_{j≤t} log2 a_j over the chunk,
+//   a^{t−s} → 2^{L_t − L_s},  a^{t+1} → 2^{L_t},  a^{cs} → 2^{L_{cs−1}},
+// and the weight w of token s becomes b_s (1 − a_s unless given).  log2 a_j is
+// clamped at −64, so a_j = 0 attenuates the past by 2^{−64} instead of
+// erasing it.
+//
 // Long sequences are cut into segments (one CTA per (segment, head)).  Pass 1
 // computes each segment's own decayed aggregate, segment_scan turns them into
 // exclusive prefixes (the state entering each segment), pass 2 produces the
@@ -43,7 +50,9 @@ struct SimtCfg {
   static constexpr int oPW = oP + CS * CS;          // a^k, k = 0..CS
   static constexpr int oSQ = oPW + CS + 1;          // ½‖x‖² per row (Performer)
   static constexpr int oDEN = oSQ + CS;             // denominators [CS]
-  static constexpr int total = oDEN + CS;
+  static constexpr int oLC = oDEN + CS;             // per-token decay: L_t [CS]
+  static constexpr int oBW = oLC + CS;              // per-token decay: b_t [CS]
+  static constexpr int total = oBW + CS;
   static constexpr size_t bytes = size_t(total) * sizeof(float);
 };
 
@@ -106,12 +115,57 @@ __device__ void update_state(float* S, float* z, const float* kf, const float* v
   }
 }
 
+// Per-token decay of one chunk, computed by warp 0: Lc[t] = Σ_{j≤t} log2 a_j
+// (within the chunk, log2 clamped at −64; tokens t ≥ cs add 0, so Lc[CS−1]
+// is the chunk's total) and Bw[t] = b_t (0 for t ≥ cs).
+template <int CS>
+__device__ void tok_chunk_prep(const float* __restrict__ a, const float* __restrict__ b, int cs,
+                               float* Lc, float* Bw) {
+  static_assert(CS <= 32, "one warp per chunk");
+  if (threadIdx.x >= 32) return;
+  const int t = threadIdx.x;
+  const bool live = t < cs;
+  const float at = live ? a[t] : 1.f;
+  float lg = live ? fmaxf(log2f(at), -64.f) : 0.f;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float u = __shfl_up_sync(0xffffffffu, lg, o);
+    if (t >= o) lg += u;
+  }
+  if (t < CS) {
+    Lc[t] = lg;
+    Bw[t] = live ? (b ? b[t] : 1.f - at) : 0.f;
+  }
+}
+
+// Per-token form of update_state: μ ← 2^{L_{cs−1}} μ + Σ_s b_s·2^{L_{cs−1}−L_s} k'_sᵀ v_s.
+template <int D, int DP, int CS, int FS>
+__device__ void update_state_tok(float* S, float* z, const float* kf, const float* vv,
+                                 const float* Lc, const float* Bw, int cs) {
+  const float ltot = Lc[CS - 1];
+  const float acs = exp2f(ltot);
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) {
+    const int i = e / D, c = e % D;
+    float acc = 0.f;
+    for (int s = 0; s < cs; ++s) acc += (Bw[s] * exp2f(ltot - Lc[s])) * kf[s * FS + i] * vv[s * D + c];
+    S[e] = acs * S[e] + acc;
+  }
+  for (int i = threadIdx.x; i < DP; i += kThreads) {
+    float acc = 0.f;
+    for (int s = 0; s < cs; ++s) acc += (Bw[s] * exp2f(ltot - Lc[s])) * kf[s * FS + i];
+    z[i] = acs * z[i] + acc;
+  }
+}
+
 struct SimtParams {
   const void* q;
   const void* k;
   const void* v;
   void* out;
   const float* decay;
+  const float* tok_decay;   // [BH][n] or nullptr
+  const float* tok_weight;  // [BH][n] or nullptr
+  float* ws_ld;             // [BH][nseg] log2 decay of each segment (per-token decay)
   const void* omega;
   int64_t H, n, seg_len;
   int nseg;
@@ -123,8 +177,9 @@ struct SimtParams {
   float* fin_z;
 };
 
-// Pass 1: the decayed aggregate of one segment, starting from zero state.
-template <typename T, int D, int DP, bool PERF>
+// Pass 1: the decayed aggregate of one segment, starting from zero state
+// (and, with a per-token decay, the segment's total log2 decay).
+template <typename T, int D, int DP, bool PERF, bool TOK>
 __global__ void __launch_bounds__(kThreads)
 simt_segment_state(SimtParams p) {
   using C = SimtCfg<D, DP, PERF>;
@@ -137,6 +192,8 @@ simt_segment_state(SimtParams p) {
   float* xr = sm + C::oX;
   float* pw = sm + C::oPW;
   float* hs = sm + C::oSQ;
+  float* Lc = sm + C::oLC;
+  float* Bw = sm + C::oBW;
   const int g = blockIdx.x;
   const int64_t bh = blockIdx.y;
   const int64_t t_begin = (int64_t)g * p.seg_len;
@@ -149,23 +206,33 @@ simt_segment_state(SimtParams p) {
   const T* kb = static_cast<const T*>(p.k) + bh * p.n * D;
   const T* vb = static_cast<const T*>(p.v) + bh * p.n * D;
   const T* om = static_cast<const T*>(p.omega);
+  const float* ab = TOK ? p.tok_decay + bh * p.n : nullptr;
+  const float* bb = (TOK && p.tok_weight) ? p.tok_weight + bh * p.n : nullptr;
+  float seg_ld = 0.f;
   for (int64_t t0 = t_begin; t0 < t_end; t0 += CS) {
     const int cs = (int)min((int64_t)CS, t_end - t0);
     __syncthreads();
     load_features<T, D, DP, PERF, CS, FS>(kb + t0 * D, cs, kf, xr, hs, om);
     load_values<T, D, CS>(vb + t0 * D, cs, vv);
+    if (TOK) tok_chunk_prep<CS>(ab + t0, bb ? bb + t0 : nullptr, cs, Lc, Bw);
     __syncthreads();
-    update_state<D, DP, CS, FS>(S, z, kf, vv, pw, w, cs);
+    if (TOK) {
+      seg_ld += Lc[CS - 1];
+      update_state_tok<D, DP, CS, FS>(S, z, kf, vv, Lc, Bw, cs);
+    } else {
+      update_state<D, DP, CS, FS>(S, z, kf, vv, pw, w, cs);
+    }
   }
   __syncthreads();
   float* dS = p.ws_state + (bh * p.nseg + g) * (int64_t)(DP * D);
   float* dz = p.ws_z + (bh * p.nseg + g) * (int64_t)DP;
   for (int e = threadIdx.x; e < DP * D; e += kThreads) dS[e] = S[e];
   for (int i = threadIdx.x; i < DP; i += kThreads) dz[i] = z[i];
+  if (TOK && threadIdx.x == 0) p.ws_ld[bh * p.nseg + g] = seg_ld;
 }
 
 // Pass 2 (causal): outputs of one segment from the state entering it.
-template <typename T, int D, int DP, bool PERF>
+template <typename T, int D, int DP, bool PERF, bool TOK>
 __global__ void __launch_bounds__(kThreads)
 simt_causal_output(SimtParams p) {
   using C = SimtCfg<D, DP, PERF>;
@@ -181,6 +248,8 @@ simt_causal_output(SimtParams p) {
   float* pw = sm + C::oPW;
   float* hs = sm + C::oSQ;
   float* den = sm + C::oDEN;
+  float* Lc = sm + C::oLC;
+  float* Bw = sm + C::oBW;
   const int g = blockIdx.x;
   const int64_t bh = blockIdx.y;
   const int64_t t_begin = (int64_t)g * p.seg_len;
@@ -202,6 +271,8 @@ simt_causal_output(SimtParams p) {
   const T* vb = static_cast<const T*>(p.v) + bh * p.n * D;
   T* ob = static_cast<T*>(p.out) + bh * p.n * D;
   const T* om = static_cast<const T*>(p.omega);
+  const float* ab = TOK ? p.tok_decay + bh * p.n : nullptr;
+  const float* bb = (TOK && p.tok_weight) ? p.tok_weight + bh * p.n : nullptr;
   for (int64_t t0 = t_begin; t0 < t_end; t0 += CS) {
     const int cs = (int)min((int64_t)CS, t_end - t0);
     __syncthreads();
@@ -209,23 +280,26 @@ simt_causal_output(SimtParams p) {
     __syncthreads();
     load_features<T, D, DP, PERF, CS, FS>(qb + t0 * D, cs, qf, xr, hs, om);
     load_values<T, D, CS>(vb + t0 * D, cs, vv);
+    if (TOK) tok_chunk_prep<CS>(ab + t0, bb ? bb + t0 : nullptr, cs, Lc, Bw);
     __syncthreads();
     // masked, decayed weights P[t][s] = w·a^{t−s}(q'_t·k'_s), s ≤ t
+    // (per-token decay: b_s·2^{L_t − L_s}(q'_t·k'_s))
     for (int e = threadIdx.x; e < CS * CS; e += kThreads) {
       const int t = e / CS, s = e % CS;
       float acc = 0.f;
       if (s <= t) {
         for (int i = 0; i < DP; ++i) acc += qf[t * FS + i] * kf[s * FS + i];
-        acc *= w * pw[t - s];
+        acc *= TOK ? Bw[s] * exp2f(Lc[t] - Lc[s]) : w * pw[t - s];
       }
       P[e] = acc;
     }
     __syncthreads();
+    // decay of the entering state at token t: a^{t+1} (per-token: 2^{L_t})
     for (int t = threadIdx.x; t < CS; t += kThreads) {
       float intra = 0.f, inter = 0.f;
       for (int s = 0; s <= t; ++s) intra += P[t * CS + s];
       for (int i = 0; i < DP; ++i) inter += qf[t * FS + i] * z[i];
-      den[t] = intra + pw[t + 1] * inter;
+      den[t] = intra + (TOK ? exp2f(Lc[t]) : pw[t + 1]) * inter;
     }
     __syncthreads();
     for (int e = threadIdx.x; e < CS * D; e += kThreads) {
@@ -234,12 +308,13 @@ simt_causal_output(SimtParams p) {
         float intra = 0.f, inter = 0.f;
         for (int s = 0; s <= t; ++s) intra += P[t * CS + s] * vv[s * D + c];
         for (int i = 0; i < DP; ++i) inter += qf[t * FS + i] * S[i * D + c];
-        const float num = intra + pw[t + 1] * inter;
+        const float num = intra + (TOK ? exp2f(Lc[t]) : pw[t + 1]) * inter;
         ob[(t0 + t) * D + c] = from_f32<T>(num / den[t]);
       }
     }
     __syncthreads();
-    update_state<D, DP, CS, FS>(S, z, kf, vv, pw, w, cs);
+    if (TOK) update_state_tok<D, DP, CS, FS>(S, z, kf, vv, Lc, Bw, cs);
+    else update_state<D, DP, CS, FS>(S, z, kf, vv, pw, w, cs);
   }
   if (p.fin_state) {
     __syncthreads();
@@ -295,7 +370,7 @@ simt_noncausal_readout(SimtParams p) {
 __global__ void __launch_bounds__(256)
 segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z, int64_t H,
                     int nseg, int nagg, int64_t seg_len, int64_t n, int dpd, int dp,
-                    const float* decay) {
+                    const float* decay, const float* seg_ld) {
   constexpr int kBatch = 8;  // aggregates loaded together to keep loads in flight
   // launched as a programmatic dependent of the launch that wrote the
   // aggregates (tensor-core paths): let the next launch start, then wait for
@@ -327,7 +402,10 @@ segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z
       if (g < nseg) {
         base[g * stride] = acc;
         const int64_t len = min(seg_len, n - (int64_t)g * seg_len);
-        acc = (len == seg_len ? a_full : decay_pow(a, len)) * acc + agg[j];
+        // per-token decay: the segment's own total, written with its aggregate
+        const float fac = seg_ld ? (g < nagg ? exp2f(seg_ld[bh * nseg + g]) : 0.f)
+                                 : (len == seg_len ? a_full : decay_pow(a, len));
+        acc = fac * acc + agg[j];
       }
     }
   }
@@ -337,22 +415,24 @@ segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z
   }
 }
 
-template <typename T, int D, int DP, bool PERF>
-cudaError_t run_simt(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
-                     float* tot_state, float* tot_z, const SegmentPlan& plan) {
+template <typename T, int D, int DP, bool PERF, bool TOK>
+cudaError_t run_simt_impl(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                          float* tot_state, float* tot_z, const SegmentPlan& plan) {
   using C = SimtCfg<D, DP, PERF>;
   static_assert(C::bytes <= 227 * 1024, "SIMT chunk buffers exceed shared memory");
   const size_t smem = C::bytes;
   cudaError_t err;
-  err = cudaFuncSetAttribute(simt_segment_state<T, D, DP, PERF>,
+  err = cudaFuncSetAttribute(simt_segment_state<T, D, DP, PERF, TOK>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(simt_causal_output<T, D, DP, PERF>,
+  err = cudaFuncSetAttribute(simt_causal_output<T, D, DP, PERF, TOK>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(simt_noncausal_readout<T, D, DP, PERF>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
+  if (!TOK) {
+    err = cudaFuncSetAttribute(simt_noncausal_readout<T, D, DP, PERF>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
 
   SimtParams p{};
   p.q = a.q;
@@ -360,6 +440,9 @@ cudaError_t run_simt(const FwdArgs& a, cudaStream_t stream, float* ws_state, flo
   p.v = a.v;
   p.out = a.out;
   p.decay = a.decay;
+  p.tok_decay = a.tok_decay;
+  p.tok_weight = a.tok_weight;
+  p.ws_ld = a.ws_ld;
   p.omega = a.omega;
   p.H = a.H;
   p.n = a.n;
@@ -371,10 +454,10 @@ cudaError_t run_simt(const FwdArgs& a, cudaStream_t stream, float* ws_state, flo
   const dim3 grid((unsigned)plan.nseg, (unsigned)BH);
   const bool need_scan = !a.causal || plan.nseg > 1;
   if (need_scan) {
-    simt_segment_state<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
+    simt_segment_state<T, D, DP, PERF, TOK><<<grid, kThreads, smem, stream>>>(p);
     count_launches(1);
     err = segment_scan(ws_state, ws_z, tot_state, tot_z, BH, a.H, plan.nseg, plan.nseg,
-                       plan.seg_len, a.n, DP, D, a.decay, stream, false);
+                       plan.seg_len, a.n, DP, D, a.decay, TOK ? a.ws_ld : nullptr, stream, false);
     if (err != cudaSuccess) return err;
   }
   if (a.causal) {
@@ -382,15 +465,25 @@ cudaError_t run_simt(const FwdArgs& a, cudaStream_t stream, float* ws_state, flo
       p.fin_state = a.mu_out;
       p.fin_z = a.nu_out;
     }
-    simt_causal_output<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
+    simt_causal_output<T, D, DP, PERF, TOK><<<grid, kThreads, smem, stream>>>(p);
     count_launches(1);
-  } else {
+  } else if (!TOK) {
     p.tot_state = tot_state;
     p.tot_z = tot_z;
     simt_noncausal_readout<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
     count_launches(1);
+  } else {
+    return cudaErrorInvalidValue;   // the per-token decay is causal only
   }
   return cudaGetLastError();
+}
+
+template <typename T, int D, int DP, bool PERF>
+cudaError_t run_simt(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                     float* tot_state, float* tot_z, const SegmentPlan& plan) {
+  if (a.tok_decay)
+    return run_simt_impl<T, D, DP, PERF, true>(a, stream, ws_state, ws_z, tot_state, tot_z, plan);
+  return run_simt_impl<T, D, DP, PERF, false>(a, stream, ws_state, ws_z, tot_state, tot_z, plan);
 }
 
 template <typename T>
@@ -417,7 +510,8 @@ cudaError_t dispatch_simt(const FwdArgs& a, cudaStream_t s, float* ws, float* wz
 
 cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* tot_z,
                          int64_t BH, int64_t H, int nseg, int nagg, int64_t seg_len, int64_t n,
-                         int dp, int d, const float* decay, cudaStream_t stream, bool dependent) {
+                         int dp, int d, const float* decay, const float* seg_ld,
+                         cudaStream_t stream, bool dependent) {
   const int dpd = dp * d;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)BH, (unsigned)((dpd + dp + 255) / 256));
@@ -429,7 +523,7 @@ cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* 
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, segment_scan_kernel, ws_state, ws_z, tot_state, tot_z,
-                                     H, nseg, nagg, seg_len, n, dpd, dp, decay);
+                                     H, nseg, nagg, seg_len, n, dpd, dp, decay, seg_ld);
   count_launches(1);
   return e;
 }

@@ -23,6 +23,12 @@
 //       K'' = w·a^{cs−1−s}k'; P = (w·a^{t−s}) ⊙ Q'K'ᵀ with a table of w·a^k;
 //       num = P·V + Q''·S;  S ← a^{cs}S + K''ᵀV.
 // Each CTA picks the folding for its head's a.
+// Per-token decay (the same page's eq (4) with a and b indexed by the token):
+//   the general folding with L_t = Σ_{j≤t} log2 a_j over the chunk (log2
+//   clamped at −64):  Q'' = 2^{L_t}q' (TMEM),  K' = b_s·k',
+//   K'' = b_s·2^{L_{cs−1}−L_s}k',  P = 2^{L_t−L_s} ⊙ Q'K'ᵀ (computed per
+//   element), TMEM = 2^{L_{cs−1}}·S_c, and the segment aggregates carry
+//   their total log2 decay to the combine.
 //
 // One CTA per (segment, head), 16 warps:
 //   warp 0        TMA producer
@@ -139,6 +145,9 @@ struct Layout {
 struct TcParams {
   __nv_bfloat16* out;      // [BH, n, D]
   const float* decay;      // [H] or nullptr
+  const float* tok_decay;  // per-token decay [BH, n] or nullptr
+  const float* tok_weight; // per-token weight [BH, n] or nullptr (1 − a)
+  float* ws_ld;            // per-token decay: [BH][nseg] log2 decay of each segment
   int64_t H, n, seg_len;
   int nseg;
   float* ws_state;         // [BH][nseg][D*D]
@@ -180,7 +189,51 @@ struct Ctx {
   float a, w;
   float lg;    // log2 a (centered folding; 0 for a = 1)
   int R;       // centered folding: the TMEM state is rescaled every R chunks
+  const float* ta;   // per-token decay of this head (token 0 of the head), or nullptr
+  const float* tb;   // per-token weight of this head, or nullptr
 };
+
+// Per-token decay of chunk c, computed by one warp: lane j gets, for each
+// 32-token block i of the chunk, L[i] = Σ_{s ≤ 32i+j} log2 a_s (the running
+// sum from the chunk's first token, log2 clamped at −64; tokens past the
+// end add 0) and B[i] = b_{32i+j} (0 past the end); tot is the chunk's sum.
+struct TokChunk {
+  float L[4];
+  float B[4];
+  float tot;
+};
+
+__device__ __forceinline__ float pick4(const float (&v)[4], int i) {
+  return i == 0 ? v[0] : (i == 1 ? v[1] : (i == 2 ? v[2] : v[3]));
+}
+
+__device__ __forceinline__ TokChunk tok_chunk(const Ctx& x, int c, int lane) {
+  TokChunk t;
+  const int64_t t0 = x.t_begin + (int64_t)c * kC;
+  const int cs = (int)min((int64_t)kC, x.t_end - t0);
+  float av[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int s = 32 * i + lane;
+    const bool live = s < cs;
+    av[i] = live ? __ldg(x.ta + t0 + s) : 1.f;
+    t.B[i] = live ? (x.tb ? __ldg(x.tb + t0 + s) : 1.f - av[i]) : 0.f;
+  }
+  float run = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float v = fmaxf(log2f(av[i]), -64.f);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    t.L[i] = run + v;
+    run += __shfl_sync(0xffffffffu, v, 31);
+  }
+  t.tot = run;
+  return t;
+}
 
 // Centered folding, lazy rescaling: K'' of chunk c carries σ_c = a^{−128·(c mod R)}
 // (all chunks but the last are full), so that the state MMA can keep
@@ -405,21 +458,33 @@ __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, in
 // except for the general full kernel, which keeps K' = m·φ(k) in place and
 // writes K'' into its own tile.  φ is computed for every row so that no
 // per-element branch splits the warp.  Signals k_ready for the warp.
-template <int D, bool FULL, bool CEN>
+// Per-token decay: m = b_r, gs = b_r·2^{L_{cs−1} − L_r}; tok_out receives
+// (L_r, L_{cs−1}) of the chunk.
+template <int D, bool FULL, bool CEN, bool TOK>
 __device__ __forceinline__ bool phi_k_chunk(const Ctx& x, int c, int r, int j0, int j1, int lane,
-                                            float k_scale_cen) {
+                                            float k_scale_cen, float* tok_out) {
   using L = Layout<D, FULL, CEN>;
   uint64_t* bar = x.bar;
   int* st = x.status;
   volatile int* ab = x.abort_flag;
   const int ks = c % L::KST;
   const int cs = (int)min((int64_t)kC, x.t_end - (x.t_begin + (int64_t)c * kC));
+  TokChunk tk;
+  if (TOK) tk = tok_chunk(x, c, lane);   // its loads overlap the wait
   if (!warp_wait(&bar[B_KFULL0 + ks], (c / L::KST) & 1, st, ab)) return false;
   if (!L::K_IN_PLACE && c >= 1 && !warp_wait(&bar[B_KPEMPTY], (c - 1) & 1, st, ab)) return false;
   const bool live = r < cs;
-  const uint32_t m2 = live ? 0x3F803F80u : 0u;   // bf16 1.0 / 0.0 pairs
-  const uint32_t g2 =
-      live ? splat_bf16x2(CEN ? k_scale_cen * lazy_sigma(x, c) : x.pw[max(cs - 1 - r, 0)]) : 0u;
+  uint32_t m2, g2;
+  if (TOK) {
+    const float lr = pick4(tk.L, r >> 5), br = pick4(tk.B, r >> 5);
+    m2 = splat_bf16x2(br);
+    g2 = splat_bf16x2(br * exp2f(tk.tot - lr));
+    tok_out[0] = lr;
+    tok_out[1] = tk.tot;
+  } else {
+    m2 = live ? 0x3F803F80u : 0u;   // bf16 1.0 / 0.0 pairs
+    g2 = live ? splat_bf16x2(CEN ? k_scale_cen * lazy_sigma(x, c) : x.pw[max(cs - 1 - r, 0)]) : 0u;
+  }
   uint8_t* kt = x.sm + L::k_off(ks);
   uint8_t* kpp = x.sm + L::kpp_off(ks);
   // full launch: always 8 chunks (one 64-column half), fully unrolled so that
@@ -463,7 +528,7 @@ struct KSplit {
 };
 
 // Warps 4–7: masked P and the epilogue.  Thread r owns token row / TMEM lane r.
-template <int D, bool CEN>
+template <int D, bool CEN, bool TOK>
 __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int64_t p_n, int warp,
                                           int lane) {
   using Cfg = TcCfg<D>;
@@ -476,9 +541,13 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
   const int wq = warp - 4;                        // lane quarter
   const uint32_t lane_base = (uint32_t)wq * 32;
   for (int c = 0; c < x.nchunks; ++c) {
-    // ---- P: causal mask (and, general folding, the decay w·a^{t−s})
+    // ---- P: causal mask (and, general folding, the decay w·a^{t−s}; per-token
+    // decay: 2^{L_t − L_s}, L_s of block b taken from lane s − 32b)
+    TokChunk tk;
+    if (TOK) tk = tok_chunk(x, c, lane);
     if (!warp_wait(&bar[B_SCORES], c & 1, st, ab)) break;
     tc_fence_after();
+    const float l_t = TOK ? pick4(tk.L, wq) : 0.f;
     // 32-column blocks b: b > wq lies above the diagonal for the whole warp
     // (zeros, scores not read), b < wq below it (no mask), b == wq straddles it.
     // Loops over blocks and output columns stay rolled: the roles of this
@@ -506,6 +575,17 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
               const float p1 = (s0 + 1 <= r) ? __uint_as_float(sc[j + 1]) : 0.f;
               pk[j / 2] = pack_bf16x2(p0, p1);
             }
+          }
+        } else if (TOK) {
+          const float l_b = pick4(tk.L, b);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int s0 = b * 32 + j;
+            const float l0 = __shfl_sync(0xffffffffu, l_b, j);
+            const float l1 = __shfl_sync(0xffffffffu, l_b, j + 1);
+            const float p0 = (s0 <= r) ? ex2_f32(l_t - l0) * __uint_as_float(sc[j]) : 0.f;
+            const float p1 = (s0 + 1 <= r) ? ex2_f32(l_t - l1) * __uint_as_float(sc[j + 1]) : 0.f;
+            pk[j / 2] = pack_bf16x2(p0, p1);
           }
         } else {
           const float* wp = x.pw + (r - b * 32);   // wp[-j] = w·a^{r-(32b+j)}
@@ -578,7 +658,7 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
 //              σ ≤ 2^{32}.  a = 1: ρ = σ = 1 throughout.
 //   general:   TMEM = a^{cs}·S_c, so after the MMA v = S_{c+1}; the tile gets
 //              S_{c+1} and TMEM a^{cs'}·S_{c+1} for the next chunk (cs').
-template <int D, bool FULL, bool CEN>
+template <int D, bool FULL, bool CEN, bool TOK>
 __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int warp, int lane) {
   using Cfg = TcCfg<D>;
   using L = Layout<D, FULL, CEN>;
@@ -658,13 +738,22 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
 
   int kj0, kj1;
   KSplit<D, FULL>::range((warp - 8) / 4 + 2, kj0, kj1);
-  auto phi_k = [&](int c) { return phi_k_chunk<D, FULL, CEN>(x, c, r, kj0, kj1, lane, k_scale_cen); };
+  // per-token decay: (L_r, L_{cs−1}) of the chunk φ(K) last ran on, and the
+  // running log2 decay of the segment (state-only launch)
+  float tok[2] = {0.f, 0.f};
+  float seg_ld = 0.f;
+  auto phi_k = [&](int c) {
+    const bool r_ok = phi_k_chunk<D, FULL, CEN, TOK>(x, c, r, kj0, kj1, lane, k_scale_cen, tok);
+    if (TOK) seg_ld += tok[1];
+    return r_ok;
+  };
 
   // D = 128: these warps also compute φ(Q) for their half of the columns;
   // φ(Q) of the first chunk does not depend on the state, so it goes first
   constexpr bool DO_Q = FULL && Cfg::HALVES == 2;
-  const float a_row = CEN ? decay_pow_signed(a, r - 63) : decay_pow(a, r + 1);
+  float a_row = CEN ? decay_pow_signed(a, r - 63) : decay_pow(a, r + 1);
   bool ok = x.nchunks > 0 && phi_k(0);
+  if (TOK) a_row = exp2f(tok[0]);
   if (DO_Q && ok) ok = phi_q_half<D, CEN>(x, 0, half, r, lane, lane_base, a_row);
 
   // ---- initial state: S_in = Σ_{j<g} a^{L·(g−1−j)}·A_j over the aggregates
@@ -673,13 +762,16 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   if (ok) {
     const bool have_in = FULL && x.g > 0;
     if (have_in) grid_dependency_wait();
-    const float aL = have_in ? decay_pow(a, p.seg_len) : 0.f;
+    // segment j carries the state through it with aL (per-token decay: its
+    // own total 2^{ws_ld})
+    const float aL = (have_in && !TOK) ? decay_pow(a, p.seg_len) : 0.f;
     const int64_t agg0 = x.bh * p.nseg;
+    auto seg_fac = [&](int j) { return TOK ? exp2f(p.ws_ld[agg0 + j]) : aL; };
     float zin = 0.f;
     if (have_in && srow && half == 0)
-      for (int j = 0; j < x.g; ++j) zin = aL * zin + p.ws_z[(agg0 + j) * D + r];
+      for (int j = 0; j < x.g; ++j) zin = seg_fac(j) * zin + p.ws_z[(agg0 + j) * D + r];
     const float alpha0 = CEN ? decay_pow_signed(a, 64) : 1.f;
-    const float beta0 = CEN ? alpha0 : decay_pow(a, chunk_len(0));
+    const float beta0 = CEN ? alpha0 : (TOK ? exp2f(tok[1]) : decay_pow(a, chunk_len(0)));
     put_state([&](int hh, float* v) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = 0.f;
@@ -688,13 +780,14 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
 #pragma unroll 2
                   for (int j = 0; j < x.g; ++j) {
                     const float4* s4 = reinterpret_cast<const float4*>(src + j * (int64_t)(D * D));
+                    const float f = seg_fac(j);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                       const float4 t = s4[e];
-                      v[4 * e] = aL * v[4 * e] + t.x;
-                      v[4 * e + 1] = aL * v[4 * e + 1] + t.y;
-                      v[4 * e + 2] = aL * v[4 * e + 2] + t.z;
-                      v[4 * e + 3] = aL * v[4 * e + 3] + t.w;
+                      v[4 * e] = f * v[4 * e] + t.x;
+                      v[4 * e + 1] = f * v[4 * e + 1] + t.y;
+                      v[4 * e + 2] = f * v[4 * e + 2] + t.z;
+                      v[4 * e + 3] = f * v[4 * e + 3] + t.w;
                     }
                   }
                 }
@@ -723,7 +816,8 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
       to_tmem = renorm;
     } else {
       alpha = 1.f;
-      beta = last ? 1.f : decay_pow(a, chunk_len(c + 1));
+      // tok holds chunk c + 1's totals here (φ(K) of c + 1 ran above)
+      beta = last ? 1.f : (TOK ? exp2f(tok[1]) : decay_pow(a, chunk_len(c + 1)));
       gamma = 1.f;
       to_tmem = !last;
     }
@@ -749,13 +843,16 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
       mbar_arrive(&bar[B_DSEMPTY]);
       if (FULL && !last) mbar_arrive(&bar[B_SREADY]);
     }
+    if (TOK) a_row = exp2f(tok[0]);
     if (DO_Q && c + 1 < x.nchunks &&
         !phi_q_half<D, CEN>(x, c + 1, half, r, lane, lane_base, a_row))
       break;
   }
+  // state-only launch, per-token decay: the segment's total log2 decay
+  if (TOK && !FULL && ok && warp == 8 && lane == 0) p.ws_ld[x.bh * p.nseg + x.g] = seg_ld;
 }
 
-template <int D, bool FULL, bool CEN>
+template <int D, bool FULL, bool CEN, bool TOK>
 __device__ __forceinline__ void run_roles(const Ctx& x, const TcParams& p, const CUtensorMap* mq,
                                           const CUtensorMap* mk, const CUtensorMap* mv, int warp,
                                           int lane) {
@@ -767,27 +864,31 @@ __device__ __forceinline__ void run_roles(const Ctx& x, const TcParams& p, const
   } else if (warp == 2) {
     if (lane == 0) role_mma_state<D, FULL, CEN>(x);
   } else if (warp >= 4 && warp < 8 && FULL) {
-    role_rows<D, CEN>(x, p.out, p.n, warp, lane);
+    role_rows<D, CEN, TOK>(x, p.out, p.n, warp, lane);
   } else if (warp >= 8 && warp < 8 + 4 * Cfg::HALVES) {
-    role_state<D, FULL, CEN>(x, p, warp, lane);
+    role_state<D, FULL, CEN, TOK>(x, p, warp, lane);
   } else if (!FULL && warp >= 4) {
     // state-only launch: a share of φ(K) on the otherwise idle warpgroups
     const int r = (warp & 3) * 32 + lane;
     const float k_scale_cen = CEN ? x.w * decay_pow_signed(x.a, 63 - r) : 0.f;
     int j0, j1;
     KSplit<D, false>::range(warp / 4, j0, j1);
+    float tok[2];
     for (int c = 0; c < x.nchunks; ++c)
-      if (!phi_k_chunk<D, false, CEN>(x, c, r, j0, j1, lane, k_scale_cen)) break;
+      if (!phi_k_chunk<D, false, CEN, TOK>(x, c, r, j0, j1, lane, k_scale_cen, tok)) break;
   } else if (FULL && Cfg::HALVES == 1 && warp >= 12) {
     // D = 64: the fourth warpgroup computes φ(Q)
     const int r = (warp - 12) * 32 + lane;
     const float a_row = CEN ? decay_pow_signed(x.a, r - 63) : decay_pow(x.a, r + 1);
-    for (int c = 0; c < x.nchunks; ++c)
-      if (!phi_q_half<D, CEN>(x, c, 0, r, lane, (uint32_t)(warp - 12) * 32, a_row)) break;
+    for (int c = 0; c < x.nchunks; ++c) {
+      // per-token decay: Q'' = 2^{L_r}·φ(q) of this chunk
+      const float ar = TOK ? exp2f(pick4(tok_chunk(x, c, lane).L, r >> 5)) : a_row;
+      if (!phi_q_half<D, CEN>(x, c, 0, r, lane, (uint32_t)(warp - 12) * 32, ar)) break;
+    }
   }
 }
 
-template <int D, bool FULL>
+template <int D, bool FULL, bool TOK>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const TcParams p) {
@@ -818,7 +919,10 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   x.nchunks = (int)((x.t_end - x.t_begin + kC - 1) / kC);
   x.a = p.decay ? p.decay[x.bh % p.H] : 1.f;
   x.w = new_token_weight(x.a);
-  const bool cen = (x.a == 1.f) || (x.a >= kCenteredMinDecay);
+  x.ta = TOK ? p.tok_decay + x.bh * p.n : nullptr;
+  x.tb = (TOK && p.tok_weight) ? p.tok_weight + x.bh * p.n : nullptr;
+  // the per-token decay always takes the general folding
+  const bool cen = !TOK && ((x.a == 1.f) || (x.a >= kCenteredMinDecay));
   x.lg = (cen && x.a != 1.f) ? log2f(x.a) : 0.f;
   // largest R with 128·(R−1)·|log2 a| ≤ 32 − 128·|log2 a|, at least 1
   x.R = x.lg == 0.f ? (1 << 30) : max(1, (int)fminf(32.f / (128.f * -x.lg), 1e9f));
@@ -866,8 +970,9 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   tc_fence_after();
   x.tmem = *tmem_slot;
 
-  if (cen) run_roles<D, FULL, true>(x, p, &map_q, &map_k, &map_v, warp, lane);
-  else run_roles<D, FULL, false>(x, p, &map_q, &map_k, &map_v, warp, lane);
+  if (TOK) run_roles<D, FULL, false, true>(x, p, &map_q, &map_k, &map_v, warp, lane);
+  else if (cen) run_roles<D, FULL, true, false>(x, p, &map_q, &map_k, &map_v, warp, lane);
+  else run_roles<D, FULL, false, false>(x, p, &map_q, &map_k, &map_v, warp, lane);
 
   tc_fence_before();
   __syncthreads();
@@ -881,7 +986,7 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
 // ------------------------------------------------------------------ host side
 
-template <int D>
+template <int D, bool TOK>
 cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
                    const SegmentPlan& plan) {
   using Cfg = TcCfg<D>;
@@ -891,15 +996,18 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
   if ((e = tmap_rows(&mq, a.q, BH, a.n, D, kC)) != cudaSuccess) return e;
   if ((e = tmap_rows(&mk, a.k, BH, a.n, D, kC)) != cudaSuccess) return e;
   if ((e = tmap_rows(&mv, a.v, BH, a.n, D, kC)) != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc_forward_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg::SMEM_ALLOC);
+  e = cudaFuncSetAttribute(tc_forward_kernel<D, true, TOK>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc_forward_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg::SMEM_ALLOC);
+  e = cudaFuncSetAttribute(tc_forward_kernel<D, false, TOK>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   TcParams p{};
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.decay = a.decay;
+  p.tok_decay = a.tok_decay;
+  p.tok_weight = a.tok_weight;
+  p.ws_ld = a.ws_ld;
   p.H = a.H;
   p.n = a.n;
   p.seg_len = plan.seg_len;
@@ -913,7 +1021,7 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
   if (plan.nseg > 1) {
     // aggregates of segments 0 … nseg−2 (nothing follows the last one)
     const dim3 grid_state((unsigned)BH, (unsigned)(plan.nseg - 1));
-    tc_forward_kernel<D, false><<<grid_state, kThreadsTc, Cfg::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
+    tc_forward_kernel<D, false, TOK><<<grid_state, kThreadsTc, Cfg::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -930,7 +1038,7 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = plan.nseg > 1 ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, tc_forward_kernel<D, true>, mq, mk, mv, p);
+  e = cudaLaunchKernelEx(&cfg, tc_forward_kernel<D, true, TOK>, mq, mk, mv, p);
   count_launches(1);
   return e;
 }
@@ -947,8 +1055,13 @@ cudaError_t tc_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state, f
                        float* tot_state, float* tot_z, const SegmentPlan& plan) {
   (void)tot_state;   // causal only: the final state goes straight to a.mu_out
   (void)tot_z;
-  if (a.d == 128) return run_tc<128>(a, stream, ws_state, ws_z, plan);
-  if (a.d == 64) return run_tc<64>(a, stream, ws_state, ws_z, plan);
+  if (a.tok_decay) {
+    if (a.d == 128) return run_tc<128, true>(a, stream, ws_state, ws_z, plan);
+    if (a.d == 64) return run_tc<64, true>(a, stream, ws_state, ws_z, plan);
+    return cudaErrorInvalidValue;
+  }
+  if (a.d == 128) return run_tc<128, false>(a, stream, ws_state, ws_z, plan);
+  if (a.d == 64) return run_tc<64, false>(a, stream, ws_state, ws_z, plan);
   return cudaErrorInvalidValue;
 }
 

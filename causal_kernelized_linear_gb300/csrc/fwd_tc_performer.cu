@@ -823,7 +823,7 @@ cudaError_t run(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* w
       e = launch<DP, kState>(p, dim3(ubh, (unsigned)(plan.nseg - 1)), false, mq, mk, mv, mw, stream);
       if (e != cudaSuccess) return e;
       e = segment_scan(ws_state, ws_z, nullptr, nullptr, a.B * a.H, a.H, plan.nseg, plan.nseg - 1,
-                       plan.seg_len, a.n, DP, kD, nullptr, stream, true);
+                       plan.seg_len, a.n, DP, kD, nullptr, nullptr, stream, true);
       if (e != cudaSuccess) return e;
     }
     return launch<DP, kCausal>(p, dim3(ubh, (unsigned)plan.nseg), plan.nseg > 1, mq, mk, mv, mw,
@@ -833,7 +833,7 @@ cudaError_t run(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* w
   e = launch<DP, kState>(p, dim3(ubh, (unsigned)plan.nseg), false, mq, mk, mv, mw, stream);
   if (e != cudaSuccess) return e;
   e = segment_scan(ws_state, ws_z, tot_state, tot_z, a.B * a.H, a.H, plan.nseg, plan.nseg,
-                   plan.seg_len, a.n, DP, kD, nullptr, stream, true);
+                   plan.seg_len, a.n, DP, kD, nullptr, nullptr, stream, true);
   if (e != cudaSuccess) return e;
   return launch<DP, kReadout>(p, dim3(ubh, (unsigned)plan.nseg), true, mq, mk, mv, mw, stream);
 }
@@ -842,6 +842,7 @@ cudaError_t run(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* w
 
 bool tc_performer_supported(const FwdArgs& a) {
   return a.bf16 && a.performer && a.d == kD && (a.m == 128 || a.m == 256) && a.decay == nullptr &&
+         a.tok_decay == nullptr &&
          a.n >= kC;
 }
 

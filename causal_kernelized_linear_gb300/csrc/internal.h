@@ -18,6 +18,9 @@ struct FwdArgs {
   const void* v;
   void* out;
   const float* decay;   // device [H] or nullptr (a = 1)
+  const float* tok_decay;   // device [B,H,n] per-token decay, or nullptr
+  const float* tok_weight;  // device [B,H,n] per-token input weight, or nullptr (1 − a)
+  float* ws_ld;         // per-token decay, nseg > 1: [B·H][nseg] log2 decay of each segment
   const void* omega;    // device [d, m] (Performer) or nullptr
   int64_t B, H, n;
   int d;                // value / input width
@@ -39,7 +42,9 @@ struct DecodeArgs {
   const void* k;
   const void* v;
   void* out;
-  const float* decay;
+  const float* decay;   // [H] (or nullptr: a = 1), or [B·H] when per_token
+  const float* weight;  // per_token: new-token weights [B·H], or nullptr for 1 − a
+  bool per_token;
   const void* omega;    // Performer: [d, m]; else nullptr
   int64_t B, H;
   int d;
@@ -82,7 +87,10 @@ cudaError_t tmap_rows(CUtensorMap* m, const void* base, int64_t BH, int64_t n, i
 cudaError_t tmap_matrix(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows);
 
 // Exclusive decayed prefix over the per-segment aggregates of every head, in
-// place.  Only the first nagg aggregates are read (nagg = nseg − 1 when the
+// place.  Segment g's aggregate is carried past it with the factor
+// decay^{its length} (per-head decay), or 2^{seg_ld[bh·nseg + g]} when seg_ld
+// (the per-token decay's log2 total of each segment) is given.
+// Only the first nagg aggregates are read (nagg = nseg − 1 when the
 // last segment's aggregate was not computed: the exclusive prefixes do not
 // need it); the inclusive total (final state) is written when tot_state !=
 // nullptr and nagg == nseg.  `dependent` launches it as a programmatic
@@ -90,7 +98,8 @@ cudaError_t tmap_matrix(CUtensorMap* m, const void* base, int64_t rows, int64_t 
 // that wrote the aggregates); the launch after it may then start early too.
 cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* tot_z,
                          int64_t BH, int64_t H, int nseg, int nagg, int64_t seg_len, int64_t n,
-                         int dp, int d, const float* decay, cudaStream_t stream, bool dependent);
+                         int dp, int d, const float* decay, const float* seg_ld,
+                         cudaStream_t stream, bool dependent);
 
 // la_forward with a fixed workspace of ws_floats floats, fetched through
 // get_ws only when the plan needs it, instead of stream-ordered allocations

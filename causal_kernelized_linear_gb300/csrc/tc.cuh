@@ -431,6 +431,12 @@ __device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t a) {
   asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(d) : "r"(a));
   return d;
 }
+// 2^x in fp32 (hardware approximation, subnormal results flushed to zero).
+__device__ __forceinline__ float ex2_f32(float a) {
+  float d;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(d) : "f"(a));
+  return d;
+}
 // The same bf16 value in both lanes.
 __device__ __forceinline__ uint32_t splat_bf16x2(float x) { return pack_bf16x2(x, x); }
 

@@ -152,6 +152,51 @@ la_status la_decode_step_fm(float* mu, float* nu, const la_tensor* q, const la_t
                             const la_tensor* v, const float* decay_a, la_feature_map feature_map,
                             const la_tensor* omega, la_tensor* out, la_stream stream);
 
+/*
+ * la_forward_token_decay — causal forward with a decay and an input weight
+ * for every token: "Efficient Transformers II" eq (4), z_i = a·z_{i−1} + b·s_i,
+ * with a and b indexed by the token (the input-dependent, "selective" state
+ * update of the Mamba section of "Linear Attention Research 2026"), applied
+ * to the state of eq (7)–(8):
+ *   μ_i = a_i·μ_{i−1} + b_i·k'_iᵀv_i,  ν_i = a_i·ν_{i−1} + b_i·k'_iᵀ,
+ *   o_i = q'_i·μ_i / q'_i·ν_i  (token i included, zero initial state).
+ *   q, k, v, out, feature_map, omega  as la_forward (causal).
+ *   decay_a   device fp32 [B, H, n] (the layout of q without d), 4-byte
+ *             aligned, a_i ∈ [0, 1].  Required when B·H·n > 0.
+ *   weight_b  device fp32 [B, H, n], 4-byte aligned, b_i ≥ 0 — or NULL for
+ *             b_i = 1 − a_i (eq (10)–(11) per token; unlike la_forward there
+ *             is no special case at a_i = 1: such a token gets weight 0).
+ *   mu_out, nu_out  final state as in la_forward_with_state, or both NULL.
+ * Decays are applied as powers of two of per-chunk running sums of log2 a_i,
+ * with log2 a_i clamped at −64: a_i = 0 scales everything before token i by
+ * 2^−64 rather than removing it exactly.  Values of a outside [0, 1] or
+ * negative b give unspecified (finite-time, fault-free) results.
+ * bf16 inputs with elu+1 and d ∈ {64, 128} run on the tcgen05 path, all
+ * others on the fp32 CUDA-core path.
+ * Errors: as la_forward; LA_ERR_INVALID_ARG also for a missing or misaligned
+ * decay_a, a misaligned weight_b, or only one of mu_out / nu_out.
+ */
+la_status la_forward_token_decay(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                                 const float* decay_a, const float* weight_b,
+                                 la_feature_map feature_map, const la_tensor* omega,
+                                 la_tensor* out, float* mu_out, float* nu_out,
+                                 la_stream stream);
+
+/*
+ * la_decode_step_token_decay — one recurrent step with this token's own
+ * decay and weight (the step of la_forward_token_decay):
+ *   μ ← a·μ + b·k'ᵀv,  ν ← a·ν + b·k',  o = q'μ / q'ν,
+ *   decay_a   device fp32 [B, H], 4-byte aligned (required);
+ *   weight_b  device fp32 [B, H], or NULL for b = 1 − a.
+ * Everything else (state, shapes, feature maps, ownership, asynchrony,
+ * errors) is as for la_decode_step_fm.
+ */
+la_status la_decode_step_token_decay(float* mu, float* nu, const la_tensor* q,
+                                     const la_tensor* k, const la_tensor* v,
+                                     const float* decay_a, const float* weight_b,
+                                     la_feature_map feature_map, const la_tensor* omega,
+                                     la_tensor* out, la_stream stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* la_status_string(la_status status);
 

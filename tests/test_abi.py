@@ -137,6 +137,33 @@ def test_decode_fm_validation(lib):
     assert call(5, None) == B.LA_ERR_INVALID_ARG
 
 
+def test_token_decay_validation(lib):
+    ok = _t()
+    st0 = 0x40000
+
+    def fwd(a, b=None, mu=None, nu=None, q=ok):
+        return lib.la_forward_token_decay(ctypes.byref(q), ctypes.byref(ok), ctypes.byref(ok), a,
+                                          b, B.LA_FM_ELU1, None, ctypes.byref(ok), mu, nu, None)
+    assert fwd(None) == B.LA_ERR_INVALID_ARG                 # decay missing
+    assert fwd(0x20002) == B.LA_ERR_INVALID_ARG              # decay not 4-byte aligned
+    assert fwd(0x20000, 0x20001) == B.LA_ERR_INVALID_ARG     # weight not 4-byte aligned
+    assert fwd(0x20000, None, st0, None) == B.LA_ERR_INVALID_ARG   # only one state buffer
+    assert fwd(0x20000, None, st0 + 4, st0) == B.LA_ERR_INVALID_ARG
+    assert fwd(0x20000, q=_t(shape=(1, 2, 9, 64))) == B.LA_ERR_INVALID_ARG
+
+    q = _t(shape=(4, 2, 1, 64))
+
+    def dec(a, b=None, fm=B.LA_FM_ELU1, omega=None, qq=q):
+        return lib.la_decode_step_token_decay(
+            st0, st0, ctypes.byref(qq), ctypes.byref(qq), ctypes.byref(qq), a, b, fm,
+            ctypes.byref(omega) if omega is not None else None, ctypes.byref(qq), None)
+    assert dec(None) == B.LA_ERR_INVALID_ARG
+    assert dec(0x20001) == B.LA_ERR_INVALID_ARG
+    assert dec(0x20000, 0x20002) == B.LA_ERR_INVALID_ARG
+    assert dec(0x20000, fm=B.LA_FM_PERFORMER) == B.LA_ERR_INVALID_ARG
+    assert dec(0x20000, qq=_t(shape=(4, 2, 1, 96))) == B.LA_ERR_UNSUPPORTED
+
+
 def test_product_path_has_no_oracle_or_cpu_fallback():
     pkg = os.path.join(ROOT, "causal_kernelized_linear_gb300")
     for path in glob.glob(os.path.join(pkg, "**", "*"), recursive=True):

@@ -13,6 +13,7 @@ Research 2026", Performer and elu+1 sections); no public dataset is involved.
 """
 from __future__ import annotations
 
+import math
 from dataclasses import dataclass
 from typing import Optional, Tuple
 
@@ -80,6 +81,29 @@ PERFORMER_DECODE = DecodeWorkload("performer_decode_B256_H32_d64_m256", 256, 32,
 
 FORWARD_WORKLOADS = {w.name: w for w in (TINY_FP32, ELU1_DECAY, PERFORMER, LONG)}
 
+
+@dataclass(frozen=True)
+class TokenDecayWorkload:
+    """A forward workload whose decay varies by token (and carries an input
+    weight per token), drawn as in the selective state update of the Mamba
+    section of "Linear Attention Research 2026": a step Δ_t = softplus(z_t +
+    bias) from the input, a_t = exp(−A_h·Δ_t) with a per-head rate A_h, and the
+    input weight b_t = Δ_t."""
+    base: ForwardWorkload
+    rate: Tuple[float, float] = (1.0, 16.0)   # A_h log-uniform in this range
+    bias: float = -4.0
+    weight: bool = True                       # b_t = Δ_t; False: b_t = 1 − a_t
+    resets: float = 0.0                       # fraction of tokens with a_t = 0
+
+    @property
+    def name(self) -> str:
+        return "token_decay_" + self.base.name.split("_", 1)[1]
+
+
+# The long-sequence shape with a per-token decay and weight.
+TOKEN_DECAY_LONG = TokenDecayWorkload(ForwardWorkload("long_B1_H16_n65536_d128", 1, 16, 65536,
+                                                      128, "bf16", "elu1", seed=6))
+
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
 
 
@@ -136,3 +160,34 @@ def decode_step_inputs(w: DecodeWorkload, step: int, B: Optional[int] = None,
     k = torch.randn(B, H, w.d, generator=g) * w.qk_scale
     v = torch.randn(B, H, w.d, generator=g)
     return {"q": q.bfloat16(), "k": k.bfloat16(), "v": v.bfloat16()}
+
+
+def make_token_decay(B, H, n, seed, rate=(1.0, 16.0), bias=-4.0, weight=True, resets=0.0):
+    """Per-token decay a [B,H,n] fp32 and input weight b [B,H,n] fp32 (None
+    when ``weight`` is False): Δ = softplus(z + bias), z ~ N(0, 1); a = exp(−A_h·Δ)
+    with A_h log-uniform in ``rate``; b = Δ; a fraction ``resets`` of the
+    tokens (chosen uniformly) get a = 0.  Drawn in fp64 from their own
+    generator, then rounded to fp32."""
+    g = torch.Generator().manual_seed(int(seed) * 7919 + 104729)
+    lo, hi = rate
+    A = torch.exp(torch.rand(H, generator=g, dtype=torch.float64) * (math.log(hi) - math.log(lo))
+                  + math.log(lo))
+    z = torch.randn(B, H, n, generator=g, dtype=torch.float64)
+    delta = torch.nn.functional.softplus(z + bias)
+    a = torch.exp(-A[None, :, None] * delta)
+    if resets > 0.0:
+        a = torch.where(torch.rand(B, H, n, generator=g, dtype=torch.float64) < resets,
+                        torch.zeros_like(a), a)
+    return a.float(), (delta.float() if weight else None)
+
+
+def token_decay_inputs(w: TokenDecayWorkload, n: Optional[int] = None, B: Optional[int] = None,
+                       H: Optional[int] = None):
+    """q, k, v (as the base workload) plus the per-token a and b."""
+    x = forward_inputs(w.base, n=n, B=B, H=H)
+    a, b = make_token_decay(B or w.base.B, H or w.base.H, n or w.base.n, w.base.seed, w.rate,
+                            w.bias, w.weight, w.resets)
+    x["a"] = None
+    x["a_tok"] = a
+    x["b_tok"] = b
+    return x
