@@ -19,16 +19,17 @@
 //       Only Q'' (TMEM) and K'' (smem; the K-major view feeds Q''K''ᵀ, the
 //       MN-major view feeds K''ᵀV) are needed, so the raw Q/K tiles are
 //       released as soon as φ has read them.
-//   general (any a ∈ [0, 1]):  Q' (smem), Q'' = a^{t+1}q' (TMEM), K' (smem),
-//       K'' = w·a^{cs−1−s}k'; P = (w·a^{t−s}) ⊙ Q'K'ᵀ with a table of w·a^k;
-//       num = P·V + Q''·S;  S ← a^{cs}S + K''ᵀV.
+//   general (any a ∈ [0, 1]):  Q' = q' (TMEM), K' (smem), K'' = w·a^{cs−1−s}k';
+//       P = (w·a^{t−s}) ⊙ Q'K'ᵀ with a table of w·a^k; the product Q'·S is
+//       scaled by a^{t+1} row by row in fp32 before P·V accumulates onto it:
+//       num = P·V + a^{t+1}(Q'·S);  S ← a^{cs}S + K''ᵀV.
 // Each CTA picks the folding for its head's a.
 // Per-token decay (the same page's eq (4) with a and b indexed by the token):
 //   the general folding with L_t = Σ_{j≤t} log2 a_j over the chunk (log2
-//   clamped at −64):  Q'' = 2^{L_t}q' (TMEM),  K' = b_s·k',
-//   K'' = b_s·2^{L_{cs−1}−L_s}k',  P = 2^{L_t−L_s} ⊙ Q'K'ᵀ (computed per
-//   element), TMEM = 2^{L_{cs−1}}·S_c, and the segment aggregates carry
-//   their total log2 decay to the combine.
+//   clamped at −64):  K' = b_s·k',  K'' = b_s·2^{L_{cs−1}−L_s}k',
+//   P = 2^{L_t−L_s} ⊙ Q'K'ᵀ (computed per element), the row scale 2^{L_t},
+//   TMEM = 2^{L_{cs−1}}·S_c; the segment aggregates carry their total log2
+//   decay to the combine.
 //
 // One CTA per (segment, head), 16 warps:
 //   warp 0        TMA producer
@@ -121,6 +122,8 @@ static_assert(B_COUNT <= TcCfg<64>::NBAR, "barrier slots");
 // Roles of the seven tiles T0, T1, T2, KP, V0, V1 (and S) per kernel mode:
 //   centered, full:  Q stages T0, T1 | K stages T2, KP (φ(K) writes K'' in place) | V V0, V1
 //   general, full:   Q T0 | K stages T1, T2 (K' in place) | K'' in KP | V V0, V1
+// In both full modes the raw Q tile is released as soon as φ(Q) has read it
+// (the products read φ(Q) from TMEM).
 //   state-only:      K stages T0, T1, T2 (K'' in place) | V stages KP, V0, V1
 template <int D, bool FULL, bool CEN>
 struct Layout {
@@ -207,18 +210,39 @@ __device__ __forceinline__ float pick4(const float (&v)[4], int i) {
   return i == 0 ? v[0] : (i == 1 ? v[1] : (i == 2 ? v[2] : v[3]));
 }
 
-__device__ __forceinline__ TokChunk tok_chunk(const Ctx& x, int c, int lane) {
-  TokChunk t;
+// The raw a and b of one chunk for a warp (lane j: tokens 32i + j), loaded
+// one chunk ahead of their use so that their latency overlaps a chunk's work.
+struct TokPipe {
+  float a[4];
+  float b[4];
+  int c;        // the chunk they belong to, −1 for none
+};
+
+__device__ __forceinline__ void tok_load(const Ctx& x, int c, int lane, TokPipe& pp) {
   const int64_t t0 = x.t_begin + (int64_t)c * kC;
   const int cs = (int)min((int64_t)kC, x.t_end - t0);
-  float av[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int s = 32 * i + lane;
     const bool live = s < cs;
-    av[i] = live ? __ldg(x.ta + t0 + s) : 1.f;
-    t.B[i] = live ? (x.tb ? __ldg(x.tb + t0 + s) : 1.f - av[i]) : 0.f;
+    pp.a[i] = live ? __ldg(x.ta + t0 + s) : 1.f;
+    pp.b[i] = live ? (x.tb ? __ldg(x.tb + t0 + s) : 1.f - pp.a[i]) : 0.f;
   }
+  pp.c = c;
+}
+
+// Chunk c's decay from the pipe (loading it now if the pipe holds another
+// chunk), then the loads of chunk c + 1 are issued.
+__device__ __forceinline__ TokChunk tok_chunk(const Ctx& x, int c, int lane, TokPipe& pp) {
+  TokChunk t;
+  if (pp.c != c) tok_load(x, c, lane, pp);
+  float av[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    av[i] = pp.a[i];
+    t.B[i] = pp.b[i];
+  }
+  if (c + 1 < x.nchunks) tok_load(x, c + 1, lane, pp);
   float run = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -319,34 +343,24 @@ __device__ __forceinline__ void role_mma_out(const Ctx& x) {
   for (int c = 0; c < x.nchunks; ++c) {
     const int ks = c % L::KST, vs = c % L::VST;
     const uint32_t sK = x.sbase + L::k_off(ks);
-    const uint32_t sKP = x.sbase + L::kpp_off(ks);
     const uint32_t sV = x.sbase + L::v_off(vs);
-    // scores = Q''K''ᵀ (centered) or Q'K'ᵀ (general); P(c−1) in the same
-    // columns must have been consumed by P·V of chunk c−1
+    // scores = Q''K''ᵀ (centered; K'' in place of K) or Q'K'ᵀ (general; K'
+    // in place of K), A from TMEM; P(c−1) in the same columns must have been
+    // consumed by P·V of chunk c−1
     if (!mbar_wait(&bar[B_KREADY0 + ks], (c / L::KST) & 1, st, ab)) break;
     if (!mbar_wait(&bar[B_QREADY], c & 1, st, ab)) break;
     if (c >= 1 && !mbar_wait(&bar[B_NUMFULL], (c - 1) & 1, st, ab)) break;
     tc_fence_after();
-    if (CEN) {
-      const uint64_t dKP = smem_desc(sKP, 16, 1024, kSwizzle128B);
+    {
+      const uint64_t dK = smem_desc(sK, 16, 1024, kSwizzle128B);
 #pragma unroll
       for (int k = 0; k < KD; ++k)
         mma_ts(tmem + Cfg::TS, tmem + Cfg::TQ + k * 8,
-               desc_at(dKP, (k >> 2) * (kC * 128) + (k & 3) * 32), idS, k > 0);
+               desc_at(dK, (k >> 2) * (kC * 128) + (k & 3) * 32), idS, k > 0);
       mma_commit(&bar[B_SCORES]);
-    } else {
-      const uint64_t dQ = smem_desc(x.sbase + L::q_off(0), 16, 1024, kSwizzle128B);
-      const uint64_t dK = smem_desc(sK, 16, 1024, kSwizzle128B);
-#pragma unroll
-      for (int k = 0; k < KD; ++k) {
-        const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
-        mma_ss(tmem + Cfg::TS, desc_at(dQ, off), desc_at(dK, off), idS, k > 0);
-      }
-      mma_commit(&bar[B_SCORES]);
-      mma_commit(&bar[B_QEMPTY0]);
     }
     mma_commit(&bar[B_KEMPTY0 + ks]);
-    // num = Q''·S ; den = Q''·z
+    // num = Q''·S ; den = Q''·z (general: Q'·S, Q'·z, row-scaled by warps 4–7)
     if (!mbar_wait(&bar[B_SREADY], c & 1, st, ab)) break;
     if (c >= 1 && !mbar_wait(&bar[B_NUMEMPTY], (c - 1) & 1, st, ab)) break;
     tc_fence_after();
@@ -412,9 +426,9 @@ __device__ __forceinline__ void role_mma_state(const Ctx& x) {
 }
 
 // φ(Q) of chunk c for the 64 columns of half h of row r (TMEM lane r):
-// Q'' = a_row·φ(q) into TMEM; the general folding also writes Q' back in
-// place for the scores MMA.  Signals q_ready (the scores MMA may start).
-// Returns false if a wait gave up.
+// Q'' = a_row·φ(q) into TMEM (centered; Q' = φ(q) in the general folding),
+// then the raw Q tile is released.  Signals q_ready (the scores MMA may
+// start).  Returns false if a wait gave up.
 template <int D, bool CEN>
 __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, int lane,
                                            uint32_t lane_base, float a_row) {
@@ -426,29 +440,26 @@ __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, in
   const int qs = c % L::QST;
   if (!warp_wait(&bar[B_QFULL0 + qs], (c / L::QST) & 1, st, ab)) return false;
   if (c >= 1 && !warp_wait(&bar[B_QPEMPTY], (c - 1) & 1, st, ab)) return false;
-  uint8_t* qt = x.sm + L::q_off(qs);
+  const uint8_t* qt = x.sm + L::q_off(qs);
   const uint32_t a2 = splat_bf16x2(a_row);
   uint32_t packed[32];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    uint4* qp = reinterpret_cast<uint4*>(qt + sw_chunk(kC, r, h, j));
-    uint4 u = *qp;
+    uint4 u = *reinterpret_cast<const uint4*>(qt + sw_chunk(kC, r, h, j));
     u.x = elu1_bf16x2(u.x); u.y = elu1_bf16x2(u.y);
     u.z = elu1_bf16x2(u.z); u.w = elu1_bf16x2(u.w);
-    if (!CEN) *qp = u;
-    packed[j * 4 + 0] = mul_bf16x2(u.x, a2);
-    packed[j * 4 + 1] = mul_bf16x2(u.y, a2);
-    packed[j * 4 + 2] = mul_bf16x2(u.z, a2);
-    packed[j * 4 + 3] = mul_bf16x2(u.w, a2);
+    packed[j * 4 + 0] = CEN ? mul_bf16x2(u.x, a2) : u.x;
+    packed[j * 4 + 1] = CEN ? mul_bf16x2(u.y, a2) : u.y;
+    packed[j * 4 + 2] = CEN ? mul_bf16x2(u.z, a2) : u.z;
+    packed[j * 4 + 3] = CEN ? mul_bf16x2(u.w, a2) : u.w;
   }
   tmem_st32(tmem_addr(x.tmem, lane_base, Cfg::TQ + h * 32), packed);
   tmem_st_wait();
-  if (!CEN) fence_proxy_async_smem();            // Q' is read by the tensor core
   tc_fence_before();
   __syncwarp();
   if (lane == 0) {
     mbar_arrive(&bar[B_QREADY]);
-    if (CEN) mbar_arrive(&bar[B_QEMPTY0 + qs]);  // raw Q tile no longer needed
+    mbar_arrive(&bar[B_QEMPTY0 + qs]);   // raw Q tile no longer needed
   }
   return true;
 }
@@ -462,7 +473,7 @@ __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, in
 // (L_r, L_{cs−1}) of the chunk.
 template <int D, bool FULL, bool CEN, bool TOK>
 __device__ __forceinline__ bool phi_k_chunk(const Ctx& x, int c, int r, int j0, int j1, int lane,
-                                            float k_scale_cen, float* tok_out) {
+                                            float k_scale_cen, float* tok_out, TokPipe& pipe) {
   using L = Layout<D, FULL, CEN>;
   uint64_t* bar = x.bar;
   int* st = x.status;
@@ -470,7 +481,7 @@ __device__ __forceinline__ bool phi_k_chunk(const Ctx& x, int c, int r, int j0, 
   const int ks = c % L::KST;
   const int cs = (int)min((int64_t)kC, x.t_end - (x.t_begin + (int64_t)c * kC));
   TokChunk tk;
-  if (TOK) tk = tok_chunk(x, c, lane);   // its loads overlap the wait
+  if (TOK) tk = tok_chunk(x, c, lane, pipe);
   if (!warp_wait(&bar[B_KFULL0 + ks], (c / L::KST) & 1, st, ab)) return false;
   if (!L::K_IN_PLACE && c >= 1 && !warp_wait(&bar[B_KPEMPTY], (c - 1) & 1, st, ab)) return false;
   const bool live = r < cs;
@@ -540,11 +551,14 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
   const int r = (warp - 4) * 32 + lane;
   const int wq = warp - 4;                        // lane quarter
   const uint32_t lane_base = (uint32_t)wq * 32;
+  const float f_row = CEN ? 1.f : decay_pow(x.a, r + 1);   // general: a^{t+1}
+  TokPipe pipe;
+  pipe.c = -1;
   for (int c = 0; c < x.nchunks; ++c) {
     // ---- P: causal mask (and, general folding, the decay w·a^{t−s}; per-token
     // decay: 2^{L_t − L_s}, L_s of block b taken from lane s − 32b)
     TokChunk tk;
-    if (TOK) tk = tok_chunk(x, c, lane);
+    if (TOK) tk = tok_chunk(x, c, lane, pipe);
     if (!warp_wait(&bar[B_SCORES], c & 1, st, ab)) break;
     tc_fence_after();
     const float l_t = TOK ? pick4(tk.L, wq) : 0.f;
@@ -577,15 +591,31 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
             }
           }
         } else if (TOK) {
-          const float l_b = pick4(tk.L, b);
+          const float l_b = pick4(tk.L, b);   // lane j: L of token 32b + j
+          if (b < wq) {
+            // below the diagonal: 2^{L_t − L_s} = 2^{L_t − L_e}·2^{L_e − L_s} with
+            // e the block's last token; both factors are ≤ 1
+            const float l_e = __shfl_sync(0xffffffffu, l_b, 31);
+            const float rf = ex2_f32(l_t - l_e);
+            const float cf = ex2_f32(l_e - l_b);
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const int s0 = b * 32 + j;
-            const float l0 = __shfl_sync(0xffffffffu, l_b, j);
-            const float l1 = __shfl_sync(0xffffffffu, l_b, j + 1);
-            const float p0 = (s0 <= r) ? ex2_f32(l_t - l0) * __uint_as_float(sc[j]) : 0.f;
-            const float p1 = (s0 + 1 <= r) ? ex2_f32(l_t - l1) * __uint_as_float(sc[j + 1]) : 0.f;
-            pk[j / 2] = pack_bf16x2(p0, p1);
+            for (int j = 0; j < 32; j += 2) {
+              const float c0 = __shfl_sync(0xffffffffu, cf, j);
+              const float c1 = __shfl_sync(0xffffffffu, cf, j + 1);
+              pk[j / 2] = pack_bf16x2(rf * c0 * __uint_as_float(sc[j]),
+                                      rf * c1 * __uint_as_float(sc[j + 1]));
+            }
+          } else {
+            // the diagonal block: one exponential per entry s ≤ t
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const int s0 = b * 32 + j;
+              const float l0 = __shfl_sync(0xffffffffu, l_b, j);
+              const float l1 = __shfl_sync(0xffffffffu, l_b, j + 1);
+              const float p0 = (s0 <= r) ? ex2_f32(l_t - l0) * __uint_as_float(sc[j]) : 0.f;
+              const float p1 = (s0 + 1 <= r) ? ex2_f32(l_t - l1) * __uint_as_float(sc[j + 1]) : 0.f;
+              pk[j / 2] = pack_bf16x2(p0, p1);
+            }
           }
         } else {
           const float* wp = x.pw + (r - b * 32);   // wp[-j] = w·a^{r-(32b+j)}
@@ -606,6 +636,29 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
         }
       }
       tmem_st16(tmem_addr(tmem, lane_base, Cfg::TS + b * 16), pk);
+    }
+    if (!CEN) {
+      // general folding: the row's Q'·S and Q'·z (complete once Q' is
+      // released) are scaled by a^{t+1} (per-token decay: 2^{L_t}) before
+      // P·V and P·1 accumulate onto them
+      if (!warp_wait(&bar[B_QPEMPTY], c & 1, st, ab)) break;
+      tc_fence_after();
+      const float f = TOK ? exp2f(l_t) : f_row;
+#pragma unroll 1
+      for (int j0 = 0; j0 < D; j0 += 32) {
+        uint32_t nv[32];
+        tmem_ld32(tmem_addr(tmem, lane_base, Cfg::TN + j0), nv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) nv[e] = __float_as_uint(f * __uint_as_float(nv[e]));
+        tmem_st32(tmem_addr(tmem, lane_base, Cfg::TN + j0), nv);
+      }
+      uint32_t dz = 0;
+      tmem_ld1(tmem_addr(tmem, lane_base, Cfg::TR), dz);
+      tmem_ld_wait();
+      dz = __float_as_uint(f * __uint_as_float(dz));
+      asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};"
+                   ::"r"(tmem_addr(tmem, lane_base, Cfg::TR)), "r"(dz) : "memory");
     }
     tmem_st_wait();
     tc_fence_before();
@@ -742,8 +795,11 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   // running log2 decay of the segment (state-only launch)
   float tok[2] = {0.f, 0.f};
   float seg_ld = 0.f;
+  TokPipe pipe;
+  pipe.c = -1;
   auto phi_k = [&](int c) {
-    const bool r_ok = phi_k_chunk<D, FULL, CEN, TOK>(x, c, r, kj0, kj1, lane, k_scale_cen, tok);
+    const bool r_ok =
+        phi_k_chunk<D, FULL, CEN, TOK>(x, c, r, kj0, kj1, lane, k_scale_cen, tok, pipe);
     if (TOK) seg_ld += tok[1];
     return r_ok;
   };
@@ -751,9 +807,8 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   // D = 128: these warps also compute φ(Q) for their half of the columns;
   // φ(Q) of the first chunk does not depend on the state, so it goes first
   constexpr bool DO_Q = FULL && Cfg::HALVES == 2;
-  float a_row = CEN ? decay_pow_signed(a, r - 63) : decay_pow(a, r + 1);
+  const float a_row = CEN ? decay_pow_signed(a, r - 63) : 1.f;   // general: Q' unscaled
   bool ok = x.nchunks > 0 && phi_k(0);
-  if (TOK) a_row = exp2f(tok[0]);
   if (DO_Q && ok) ok = phi_q_half<D, CEN>(x, 0, half, r, lane, lane_base, a_row);
 
   // ---- initial state: S_in = Σ_{j<g} a^{L·(g−1−j)}·A_j over the aggregates
@@ -843,7 +898,6 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
       mbar_arrive(&bar[B_DSEMPTY]);
       if (FULL && !last) mbar_arrive(&bar[B_SREADY]);
     }
-    if (TOK) a_row = exp2f(tok[0]);
     if (DO_Q && c + 1 < x.nchunks &&
         !phi_q_half<D, CEN>(x, c + 1, half, r, lane, lane_base, a_row))
       break;
@@ -874,17 +928,16 @@ __device__ __forceinline__ void run_roles(const Ctx& x, const TcParams& p, const
     int j0, j1;
     KSplit<D, false>::range(warp / 4, j0, j1);
     float tok[2];
+    TokPipe pipe;
+    pipe.c = -1;
     for (int c = 0; c < x.nchunks; ++c)
-      if (!phi_k_chunk<D, false, CEN, TOK>(x, c, r, j0, j1, lane, k_scale_cen, tok)) break;
+      if (!phi_k_chunk<D, false, CEN, TOK>(x, c, r, j0, j1, lane, k_scale_cen, tok, pipe)) break;
   } else if (FULL && Cfg::HALVES == 1 && warp >= 12) {
     // D = 64: the fourth warpgroup computes φ(Q)
     const int r = (warp - 12) * 32 + lane;
-    const float a_row = CEN ? decay_pow_signed(x.a, r - 63) : decay_pow(x.a, r + 1);
-    for (int c = 0; c < x.nchunks; ++c) {
-      // per-token decay: Q'' = 2^{L_r}·φ(q) of this chunk
-      const float ar = TOK ? exp2f(pick4(tok_chunk(x, c, lane).L, r >> 5)) : a_row;
-      if (!phi_q_half<D, CEN>(x, c, 0, r, lane, (uint32_t)(warp - 12) * 32, ar)) break;
-    }
+    const float a_row = CEN ? decay_pow_signed(x.a, r - 63) : 1.f;   // general: Q' unscaled
+    for (int c = 0; c < x.nchunks; ++c)
+      if (!phi_q_half<D, CEN>(x, c, 0, r, lane, (uint32_t)(warp - 12) * 32, a_row)) break;
   }
 }
 
@@ -938,8 +991,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (i >= B_KREADY0 && i <= B_KREADY2) cnt = KSplit<D, FULL>::ARRIVALS;
       // φ(Q) warps: 8 for D = 128 (the state warps), 4 for D = 64
       if (i == B_QREADY) cnt = 4 * Cfg::HALVES;
-      // centered: raw Q tiles are released by the φ(Q) warps
-      if ((i == B_QEMPTY0 || i == B_QEMPTY1) && cen) cnt = 4 * Cfg::HALVES;
+      // raw Q tiles are released by the φ(Q) warps
+      if (i == B_QEMPTY0 || i == B_QEMPTY1) cnt = 4 * Cfg::HALVES;
       mbar_init(&x.bar[i], cnt);
     }
     *x.abort_flag = 0;
