@@ -26,7 +26,10 @@ closed form and its m^{-1/2} convergence; ω = 0 and single-entry ω closed
 forms; the exported state against Σ_i a^{n−i}(1−a) k'_iᵀ v_i.  Per-token decay:
 the quadratic form with weights b_s·Π_{s<j≤t} a_j by brute force and in exact
 rationals, reduction to the per-head oracle for constant a, the reset at
-a_i = 0, a single weighted token, and the state closed form.
+a_i = 0, a single weighted token, and the state closed form.  Backward
+(reverse mode of the recurrence, gradients of Σ g·o): central finite
+differences, fp64 autograd of the brute-force quadratic form, and the a = 0
+closed form (tests/test_oracle_backward.py).
 """
 from __future__ import annotations
 
@@ -86,6 +89,9 @@ def _load():
                                                        dp, dp, dp, dp, dp, dp, dp, dp,
                                                        dp, dp, dp]
             lib.oracle_forward_token_decay.restype = ctypes.c_int
+            lib.oracle_backward.argtypes = [i64, i64, i64, i64, ctypes.c_int, i64,
+                                            dp, dp, dp, dp, dp, dp, dp, dp, dp, dp]
+            lib.oracle_backward.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -243,3 +249,29 @@ def decode_step_token_decay(mu, nu, q, k, v, decay_a, weight_b=None, feature_map
         None if b is None else b.reshape(B, H, 1),
         feature_map, omega, mu0=mu, nu0=nu, return_state=True)
     return out[:, :, 0, :], mu2, nu2
+
+
+def backward(q, k, v, g, decay_a=None, feature_map="elu1", omega=None):
+    """Gradients of L = Σ g·o of the causal forward, in fp64: returns
+    (dq, dk, dv [B, H, n, d], da [H] or None).  g: [B, H, n, d]; decay_a
+    [H] or None (a = 1, no da)."""
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(g)
+    B, H, n, d = q.shape
+    for name, t in (("k", k), ("v", v), ("g", g)):
+        if t.shape != q.shape:
+            raise ValueError(f"{name} must have the shape of q")
+    fm = _fm(feature_map)
+    omega = _f64(omega)
+    if fm == FM_PERFORMER and omega is None:
+        raise ValueError("the Performer map needs omega [d, m]")
+    m = omega.shape[1] if fm == FM_PERFORMER else 0
+    a = _f64(decay_a)
+    dq = np.empty_like(q)
+    dk = np.empty_like(q)
+    dv = np.empty_like(q)
+    da = np.empty(H, dtype=np.float64) if a is not None else None
+    rc = _load().oracle_backward(B, H, n, d, fm, m, _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                                 _ptr(omega), _ptr(g), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da))
+    if rc != 0:
+        raise ValueError(f"oracle_backward rejected its arguments (rc={rc})")
+    return dq, dk, dv, da

@@ -304,3 +304,190 @@ int oracle_forward_token_decay(int64_t B, int64_t H, int64_t n, int64_t d, int f
   }
   return failed ? 2 : 0;
 }
+
+/* dφ for one row: given x ∈ R^d, φ(x) ∈ R^{d'} (already computed) and the
+ * gradient gf ∈ R^{d'} with respect to φ(x), writes the gradient gx ∈ R^d
+ * with respect to x:
+ *   elu+1:      ∂φ_c/∂x_c = 1 for x_c > 0, e^{x_c} otherwise (d' = d);
+ *   Performer:  ∂φ_i/∂x = φ_i·(ω_i − x), so gx = Σ_i gf_i φ_i (ω_i − x). */
+static void phi_row_grad(int fm, const double* x, int64_t d, const double* omega, int64_t m,
+                         const double* f, const double* gf, double* gx) {
+  if (fm == OR_FM_ELU1) {
+    for (int64_t c = 0; c < d; ++c) gx[c] = gf[c] * (x[c] > 0.0 ? 1.0 : exp(x[c]));
+  } else {
+    double tot = 0.0;
+    for (int64_t i = 0; i < m; ++i) tot += gf[i] * f[i];
+    for (int64_t c = 0; c < d; ++c) {
+      double acc = 0.0;
+      for (int64_t i = 0; i < m; ++i) acc += gf[i] * f[i] * omega[c * m + i];
+      gx[c] = acc - tot * x[c];
+    }
+  }
+}
+
+/*
+ * Reverse-mode gradient of L = Σ_j g_j·o_j for one causal head of the
+ * recurrence in one_head ([ET-II] eq (7)–(11) with the readout after eq (9)).
+ * With ĝ_j = g_j / den_j and ρ_j = −(g_j·o_j) / den_j (o_j = num_j / den_j),
+ * the adjoints of μ_j, ν_j obey M_j = q'_jᵀĝ_j + a·M_{j+1}, N_j = ρ_j q'_j +
+ * a·N_{j+1}, and
+ *   ∂q'_j = ĝ_j μ_jᵀ + ρ_j ν_j,   ∂k'_j = w (M_j v_jᵀ + N_j),   ∂v_j = w k'_j M_j,
+ *   ∂a    = Σ_j ⟨M_j, μ_{j−1} + w'·k'_jᵀv_j⟩ + ⟨N_j, ν_{j−1} + w'·k'_j⟩,
+ * w' = dw/da = −1 (0 when a = 1, where w = 1); then ∂q, ∂k by the chain
+ * rule through φ.  The states μ_j, ν_j are recomputed block by block from
+ * checkpoints taken every `blk` tokens in a first forward sweep.
+ */
+static int one_head_backward(int64_t n, int64_t d, int64_t dp, int fm, int64_t m,
+                             const double* q, const double* k, const double* v, const double* g,
+                             double a, const double* omega, double* dq, double* dk, double* dv,
+                             double* da_out) {
+  const int64_t blk = 64;
+  const int64_t nblk = (n + blk - 1) / blk;
+  const double w = (a == 1.0) ? 1.0 : (1.0 - a);
+  const double wprime = (a == 1.0) ? 0.0 : -1.0;
+  const size_t sd = (size_t)(dp * d);
+  double* ck_mu = (double*)calloc((size_t)(nblk > 0 ? nblk : 1) * sd, sizeof(double));
+  double* ck_nu = (double*)calloc((size_t)(nblk > 0 ? nblk : 1) * (size_t)dp, sizeof(double));
+  double* mu = (double*)calloc((size_t)(blk + 1) * sd, sizeof(double));    /* μ_{j−1}, μ_j, … of a block */
+  double* nu = (double*)calloc((size_t)(blk + 1) * (size_t)dp, sizeof(double));
+  double* kf = (double*)malloc((size_t)(blk * dp) * sizeof(double));
+  double* qf = (double*)malloc((size_t)(blk * dp) * sizeof(double));
+  double* M = (double*)calloc(sd, sizeof(double));
+  double* N = (double*)calloc((size_t)dp, sizeof(double));
+  double* gq = (double*)malloc((size_t)dp * sizeof(double));
+  double* gk = (double*)malloc((size_t)dp * sizeof(double));
+  if (!ck_mu || !ck_nu || !mu || !nu || !kf || !qf || !M || !N || !gq || !gk) {
+    free(ck_mu); free(ck_nu); free(mu); free(nu); free(kf); free(qf); free(M); free(N);
+    free(gq); free(gk);
+    return 2;
+  }
+  /* forward sweep: checkpoint the state entering every block */
+  {
+    double* cmu = mu;   /* running state */
+    double* cnu = nu;
+    for (int64_t j = 0; j < n; ++j) {
+      if (j % blk == 0) {
+        memcpy(ck_mu + (j / blk) * sd, cmu, sd * sizeof(double));
+        memcpy(ck_nu + (j / blk) * dp, cnu, (size_t)dp * sizeof(double));
+      }
+      phi_row(fm, k + j * d, d, omega, m, kf);
+      for (int64_t i = 0; i < dp; ++i) {
+        for (int64_t c = 0; c < d; ++c) cmu[i * d + c] = a * cmu[i * d + c] + w * kf[i] * v[j * d + c];
+        cnu[i] = a * cnu[i] + w * kf[i];
+      }
+    }
+  }
+  double da = 0.0;
+  for (int64_t b = nblk - 1; b >= 0; --b) {
+    const int64_t j0 = b * blk;
+    const int64_t len = (n - j0 < blk) ? n - j0 : blk;
+    /* recompute the block: mu[r] = μ_{j0+r−1} (r = 0 … len) */
+    memcpy(mu, ck_mu + b * sd, sd * sizeof(double));
+    memcpy(nu, ck_nu + b * dp, (size_t)dp * sizeof(double));
+    for (int64_t r = 0; r < len; ++r) {
+      const int64_t j = j0 + r;
+      phi_row(fm, k + j * d, d, omega, m, kf + r * dp);
+      phi_row(fm, q + j * d, d, omega, m, qf + r * dp);
+      const double* pm = mu + r * sd;
+      double* nm = mu + (r + 1) * sd;
+      for (int64_t i = 0; i < dp; ++i) {
+        for (int64_t c = 0; c < d; ++c)
+          nm[i * d + c] = a * pm[i * d + c] + w * kf[r * dp + i] * v[j * d + c];
+        nu[(r + 1) * dp + i] = a * nu[r * dp + i] + w * kf[r * dp + i];
+      }
+    }
+    for (int64_t r = len - 1; r >= 0; --r) {
+      const int64_t j = j0 + r;
+      const double* muj = mu + (r + 1) * sd;     /* μ_j */
+      const double* nuj = nu + (r + 1) * dp;
+      const double* mup = mu + r * sd;           /* μ_{j−1} */
+      const double* nup = nu + r * dp;
+      const double* qj = qf + r * dp;
+      const double* kj = kf + r * dp;
+      const double* vj = v + j * d;
+      const double* gj = g + j * d;
+      /* readout of token j */
+      double den = 0.0;
+      for (int64_t i = 0; i < dp; ++i) den += qj[i] * nuj[i];
+      double go = 0.0;
+      for (int64_t c = 0; c < d; ++c) {
+        double num = 0.0;
+        for (int64_t i = 0; i < dp; ++i) num += qj[i] * muj[i * d + c];
+        go += gj[c] * (num / den);
+      }
+      const double rho = -go / den;
+      /* adjoints M_j = q'ᵀĝ + a·M_{j+1}, N_j = ρ q' + a·N_{j+1} */
+      for (int64_t i = 0; i < dp; ++i) {
+        for (int64_t c = 0; c < d; ++c) M[i * d + c] = a * M[i * d + c] + qj[i] * (gj[c] / den);
+        N[i] = a * N[i] + rho * qj[i];
+      }
+      /* ∂q'_j = ĝ μ_jᵀ + ρ ν_j */
+      for (int64_t i = 0; i < dp; ++i) {
+        double acc = rho * nuj[i];
+        for (int64_t c = 0; c < d; ++c) acc += (gj[c] / den) * muj[i * d + c];
+        gq[i] = acc;
+      }
+      /* ∂k'_j = w (M v_j + N),  ∂v_j = w k'_j M */
+      for (int64_t i = 0; i < dp; ++i) {
+        double acc = N[i];
+        for (int64_t c = 0; c < d; ++c) acc += M[i * d + c] * vj[c];
+        gk[i] = w * acc;
+      }
+      for (int64_t c = 0; c < d; ++c) {
+        double acc = 0.0;
+        for (int64_t i = 0; i < dp; ++i) acc += kj[i] * M[i * d + c];
+        dv[j * d + c] = w * acc;
+      }
+      /* ∂a: μ_j = a μ_{j−1} + w(a) k'ᵀv */
+      for (int64_t i = 0; i < dp; ++i) {
+        for (int64_t c = 0; c < d; ++c)
+          da += M[i * d + c] * (mup[i * d + c] + wprime * kj[i] * vj[c]);
+        da += N[i] * (nup[i] + wprime * kj[i]);
+      }
+      phi_row_grad(fm, q + j * d, d, omega, m, qj, gq, dq + j * d);
+      phi_row_grad(fm, k + j * d, d, omega, m, kj, gk, dk + j * d);
+    }
+  }
+  *da_out = da;
+  free(ck_mu); free(ck_nu); free(mu); free(nu); free(kf); free(qf); free(M); free(N);
+  free(gq); free(gk);
+  return 0;
+}
+
+/*
+ * Backward of the causal forward over B·H heads: the gradients of
+ * L = Σ g·o with respect to q, k, v [B,H,n,d] and to the per-head decay
+ * a [H] (summed over the batch; da may be NULL, and is written only when a
+ * is given).  g [B,H,n,d].  Returns 0, 1 on invalid arguments, 2 when out
+ * of memory.
+ */
+int oracle_backward(int64_t B, int64_t H, int64_t n, int64_t d, int fm, int64_t m,
+                    const double* q, const double* k, const double* v, const double* a,
+                    const double* omega, const double* g, double* dq, double* dk, double* dv,
+                    double* da) {
+  if (fm != OR_FM_ELU1 && fm != OR_FM_PERFORMER) return 1;
+  if (fm == OR_FM_PERFORMER && (omega == NULL || m <= 0)) return 1;
+  if (a != NULL) {
+    for (int64_t h = 0; h < H; ++h) {
+      if (!(a[h] >= 0.0 && a[h] <= 1.0)) return 1;
+    }
+  }
+  const int64_t dp = feature_dim(fm, d, m);
+  double* da_bh = (double*)calloc((size_t)(B * H > 0 ? B * H : 1), sizeof(double));
+  if (!da_bh) return 2;
+  int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bh = 0; bh < B * H; ++bh) {
+    const double ah = a ? a[bh % H] : 1.0;
+    if (one_head_backward(n, d, dp, fm, m, q + bh * n * d, k + bh * n * d, v + bh * n * d,
+                          g + bh * n * d, ah, omega, dq + bh * n * d, dk + bh * n * d,
+                          dv + bh * n * d, da_bh + bh) != 0)
+      failed = 1;
+  }
+  if (da && a) {
+    for (int64_t h = 0; h < H; ++h) da[h] = 0.0;
+    for (int64_t bh = 0; bh < B * H; ++bh) da[bh % H] += da_bh[bh];
+  }
+  free(da_bh);
+  return failed ? 2 : 0;
+}
