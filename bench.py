@@ -242,6 +242,27 @@ def bench_token_decay(cl, tw: W.TokenDecayWorkload, steps, warmup, stream):
             "launches_per_step": launches / steps, "tokens": w.B * w.n}
 
 
+def bench_backward(cl, w: W.ForwardWorkload, steps, warmup, stream):
+    """la_backward over the whole batch (∂q, ∂k, ∂v and ∂a of the causal
+    forward).  Algorithmic bytes: q, k, v, ∂o read and ∂q, ∂k, ∂v written."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = W.forward_inputs(w)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    gen = torch.Generator().manual_seed(w.seed + 1000)
+    go = torch.randn(w.B, w.H, w.n, w.d, generator=gen).to(W.torch_dtype(w.dtype)).to(dev)
+    dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
+
+    def step():
+        cl.backward(g["q"], g["k"], g["v"], go, g["a"], w.feature_map, g["omega"], dq=dq, dk=dk,
+                    dv=dv, stream=stream)
+
+    ms, launches = _time_steps(step, steps, warmup, stream, None, cl.launch_count)
+    esize = 2 if w.dtype == "bf16" else 4
+    nbytes = w.B * w.H * w.n * w.d * esize * 7
+    return {"ms": ms, "avg_ms": statistics.mean(ms), "bytes": nbytes,
+            "launches_per_step": launches / steps, "tokens": w.B * w.n}
+
+
 def bench_forward_e2e(cl, w, causal, inp, steps, warmup, stream):
     """Same forward through the public API with host buffers: every step copies
     q, k, v from pinned host memory, runs la_forward and copies o back."""
@@ -428,6 +449,15 @@ def run_ours(args, rank, world, dist):
             "decay": "per token: a = exp(-A_h*softplus(z-4)), b = softplus(z-4)",
             "l2": "inputs (776 MiB) larger than L2; no flush",
             "launches_per_step": r["launches_per_step"]})
+        for bw in (W.ELU1_DECAY, W.LONG):
+            r = bench_backward(cl, bw, 5 if bw is W.LONG else max(args.steps, 20), 3, stream)
+            secs = r["avg_ms"] / 1e3
+            gbs = r["bytes"] / secs / 1e9
+            secondary.append({
+                "workload": bw.name, "pass": "backward (dq, dk, dv, da; fp32 CUDA cores)",
+                "value": r["tokens"] / secs, "unit": "tokens/s", "ms_per_step": r["avg_ms"],
+                "gbs_alg": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "steps": len(r["ms"]),
+                "launches_per_step": r["launches_per_step"]})
         for dw in (W.DECODE, W.PERFORMER_DECODE):
             d = bench_decode(cl, dw, stream)
             secs = d["avg_ms"] / 1e3

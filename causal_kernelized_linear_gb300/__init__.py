@@ -11,17 +11,19 @@ Python face of liblinattn (C ABI in include/linattn.h).  The method
 * ``decode_step`` — one recurrent token for many heads, state updated in place;
 * ``forward_token_decay`` / ``decode_step_token_decay`` — the causal form with
   a decay a_i and input weight b_i per token ("Efficient Transformers II"
-  eq (4) with a, b indexed by the token): μ_i = a_i μ_{i−1} + b_i k'_iᵀv_i.
+  eq (4) with a, b indexed by the token): μ_i = a_i μ_{i−1} + b_i k'_iᵀv_i;
+* ``backward`` — ∂L/∂q, ∂L/∂k, ∂L/∂v and ∂L/∂a of the causal forward.
 
 All work runs in the library's CUDA kernels; PyTorch only allocates device
 memory and provides the stream.
 """
-from ._binding import (EXPORTED, LinAttnError, decode_step, decode_step_token_decay, forward,
+from ._binding import (EXPORTED, LinAttnError, backward, decode_step, decode_step_token_decay,
+                       forward,
                        forward_token_decay, forward_with_state, last_device_status,
                        launch_count, library_path, load, selftest_wait_timeout, status_string)
 from .build import build
 
-__all__ = ["forward", "forward_with_state", "decode_step", "forward_token_decay",
+__all__ = ["forward", "forward_with_state", "decode_step", "forward_token_decay", "backward",
            "decode_step_token_decay", "last_device_status", "status_string",
            "LinAttnError", "build", "load", "library_path", "launch_count",
            "selftest_wait_timeout", "EXPORTED"]

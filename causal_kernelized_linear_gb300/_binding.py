@@ -32,7 +32,8 @@ _DT = {torch.bfloat16: LA_BF16, torch.float32: LA_F32}
 
 EXPORTED = ("la_forward", "la_forward_with_state", "la_decode_step", "la_status_string",
             "la_get_last_device_status", "la_launch_count", "la_selftest_wait_timeout",
-            "la_decode_step_fm", "la_forward_token_decay", "la_decode_step_token_decay")
+            "la_decode_step_fm", "la_forward_token_decay", "la_decode_step_token_decay",
+            "la_backward")
 
 
 class LinAttnError(RuntimeError):
@@ -84,6 +85,8 @@ def load():
         lib.la_decode_step_token_decay.argtypes = [vp, vp, P, P, P, vp, vp, ctypes.c_int, P, P,
                                                    vp]
         lib.la_decode_step_token_decay.restype = ctypes.c_int
+        lib.la_backward.argtypes = [P, P, P, vp, ctypes.c_int, P, P, P, P, P, vp, vp]
+        lib.la_backward.restype = ctypes.c_int
         lib.la_status_string.argtypes = [ctypes.c_int]
         lib.la_status_string.restype = ctypes.c_char_p
         lib.la_get_last_device_status.argtypes = [vp]
@@ -312,6 +315,31 @@ def decode_step_token_decay(mu, nu, q, k, v, decay_a, weight_b=None, out=None, s
                                            ctypes.byref(od), _stream_handle(stream))
     _check("la_decode_step_token_decay", st)
     return out
+
+
+def backward(q, k, v, grad_out, decay_a=None, feature_map="elu1", omega=None, dq=None, dk=None,
+             dv=None, want_da=True, stream=None):
+    """la_backward: gradients of the causal forward.  Returns (dq, dk, dv, da)
+    with da [H] fp32 (None without a decay or when ``want_da`` is False)."""
+    _, fm, dptr, om, qd, kd, vd, _ = _forward_args(q, k, v, decay_a, feature_map, omega, None)
+    _need_cuda("grad_out", grad_out)
+    if grad_out.shape != q.shape or grad_out.dtype != q.dtype:
+        raise ValueError("grad_out must match q in shape and dtype")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for nm, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _need_cuda(nm, t)
+    da = None
+    if decay_a is not None and want_da:
+        da = torch.empty(q.shape[1], device=q.device, dtype=torch.float32)
+    gd, dqd, dkd, dvd = (_desc(t, t.shape) for t in (grad_out, dq, dk, dv))
+    st = load().la_backward(ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), dptr, fm,
+                            ctypes.byref(om) if om is not None else None, ctypes.byref(gd),
+                            ctypes.byref(dqd), ctypes.byref(dkd), ctypes.byref(dvd),
+                            da.data_ptr() if da is not None else None, _stream_handle(stream))
+    _check("la_backward", st)
+    return dq, dk, dv, da
 
 
 def last_device_status(stream=None) -> int:

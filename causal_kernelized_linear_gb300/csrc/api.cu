@@ -325,6 +325,67 @@ la_status la_forward_token_decay(const la_tensor* q, const la_tensor* k, const l
   return la::run_forward(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+la_status la_backward(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                      const float* decay_a, la_feature_map feature_map, const la_tensor* omega,
+                      const la_tensor* grad_out, la_tensor* dq, la_tensor* dk, la_tensor* dv,
+                      float* da, la_stream stream) {
+  la::FwdArgs f;
+  // q, k, v, ω and the decay are checked as for the causal forward (with dq
+  // standing in for the output)
+  la_status st = la::validate_forward(q, k, v, decay_a, feature_map, omega, 1, dq, &f);
+  if (st != LA_OK) return st;
+  if (!grad_out || !dk || !dv) return LA_ERR_INVALID_ARG;
+  for (const la_tensor* t : {grad_out, static_cast<const la_tensor*>(dk),
+                             static_cast<const la_tensor*>(dv)}) {
+    if (t->dtype != q->dtype || !la::same_shape(q, t)) return LA_ERR_INVALID_ARG;
+    if (f.B * f.H * f.n > 0 && (!t->data || !la::aligned16(t->data))) return LA_ERR_INVALID_ARG;
+  }
+  if (da && !decay_a) return LA_ERR_INVALID_ARG;   // ∂a needs a decay to differentiate
+  if (da && (reinterpret_cast<uintptr_t>(da) & 3u)) return LA_ERR_INVALID_ARG;
+  if (!la::backward_supported(f.d, f.m, f.performer)) return LA_ERR_UNSUPPORTED;
+  la::DeviceInfo di;
+  st = la::device_info(&di);
+  if (st != LA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (f.n == 0) {
+    if (da && cudaMemsetAsync(da, 0, (size_t)f.H * sizeof(float), s) != cudaSuccess)
+      return LA_ERR_CUDA;
+    return LA_OK;
+  }
+  la::BwdArgs b;
+  b.q = f.q;
+  b.k = f.k;
+  b.v = f.v;
+  b.g = grad_out->data;
+  b.dq = dq->data;
+  b.dk = dk->data;
+  b.dv = dv->data;
+  b.decay = decay_a;
+  b.da = da;
+  b.omega = f.omega;
+  b.B = f.B;
+  b.H = f.H;
+  b.n = f.n;
+  b.d = f.d;
+  b.m = f.m;
+  b.dp = f.dp;
+  b.bf16 = f.bf16;
+  b.performer = f.performer;
+  // CUDA-core kernels: 32-token chunks, two CTAs per SM
+  const la::SegmentPlan plan = la::plan_segments(f.B * f.H, f.n, di.num_sms, 32, 2);
+  const size_t ws_floats = la::backward_workspace_floats(b, plan);
+  float* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_floats * sizeof(float), s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? LA_ERR_OUT_OF_MEMORY : LA_ERR_CUDA;
+  }
+  e = la::backward(b, ws, plan, s);
+  cudaError_t fe = cudaFreeAsync(ws, s);
+  if (e == cudaSuccess) e = fe;
+  return la::to_status(e);
+}
+
 namespace la {
 namespace {
 

@@ -1,0 +1,685 @@
+// Backward of the causal forward on fp32 CUDA cores: the gradients of
+// L = Σ_t g_t·o_t with respect to q, k, v and the per-head decay a.
+//
+// Method ("Efficient Transformers II" §2.2, eq (7)–(11) with the causal readout
+// of eq (9)), per head, with q' = φ(q), k' = φ(k), x_ts = q'_t·k'_s,
+// W_ts = w·a^{t−s} (s ≤ t), o_t = num_t / den_t:
+//   ĝ_t = g_t / den_t,   ρ_t = −(g_t·o_t) / den_t,   e_ts = W_ts·(ĝ_t·v_s + ρ_t) = ∂L/∂x_ts
+//   ∂q'_t = Σ_{s≤t} e_ts k'_s            ∂k'_s = Σ_{t≥s} e_ts q'_t
+//   ∂v_s  = Σ_{t≥s} W_ts x_ts ĝ_t         ∂a    = Σ_{s<t} (t−s)·w·a^{t−s−1}·x_ts·(ĝ_t·v_s + ρ_t)
+// (the term of ∂a through w vanishes: o does not change when every weight is
+// scaled by the same w), then ∂q, ∂k through φ.  Chunked over CS tokens (local
+// t, s) the sums split into the chunk's own pairs and two running states:
+//   forward direction  S = Σ_{s<t0} w·a^{t0−1−s} k'_sᵀv_s (and z), the state of
+//     the forward, and S̃ = Σ_{s<t0} (t0−1−s)·w·a^{t0−1−s} k'_sᵀv_s (and z̃),
+//     its age-weighted twin:
+//       ∂q'_t += a^{t+1}(S ĝ_tᵀ + ρ_t z),
+//       ∂a    += a^t·q'_t·[(t+1)(S ĝ_tᵀ + ρ_t z) + S̃ ĝ_tᵀ + ρ_t z̃];
+//   reverse direction  M = Σ_{t>end} a^{t−end} q'_tᵀ ĝ_t, N = Σ_{t>end} a^{t−end} ρ_t q'_t
+//     (the adjoints of μ and ν at the chunk's last token `end`):
+//       ∂k'_s += w·a^{cs−1−s}(M v_s + N),   ∂v_s += w·a^{cs−1−s} k'_s M.
+// Launches: segment aggregates of (S, z, S̃, z̃), their scan, the ∂q pass (which
+// also stores den_t and ρ_t), segment aggregates of (M, N), their reverse scan,
+// the ∂k/∂v pass, and the per-head sum of ∂a.  One CTA per (segment, head).
+#include "common.cuh"
+#include "internal.h"
+#include "simt.cuh"
+
+namespace la {
+namespace {
+
+using simt::kThreads;
+using simt::load_features;
+using simt::load_values;
+
+template <int D, int DP, bool PERF>
+struct BwdCfg {
+  static constexpr int CS = (DP >= 256) ? 16 : 32;   // tokens per chunk
+  static constexpr int FS = DP + 1;                   // padded feature row stride
+  // shared memory (floats)
+  static constexpr int oS = 0;                  // S or M      [DP][D]
+  static constexpr int oST = oS + DP * D;       // S̃           [DP][D] (∂q pass and aggregates)
+  static constexpr int oZ = oST + DP * D;       // z or N      [DP]
+  static constexpr int oZT = oZ + DP;           // z̃           [DP]
+  static constexpr int oQF = oZT + DP;          // q'          [CS][FS]
+  static constexpr int oKF = oQF + CS * FS;     // k'          [CS][FS]
+  static constexpr int oV = oKF + CS * FS;      // v           [CS][D]
+  static constexpr int oG = oV + CS * D;        // g, then ĝ   [CS][D]
+  static constexpr int oXR = oG + CS * D;       // raw rows (Performer) [CS][D]
+  static constexpr int oXM = oXR + (PERF ? CS * D : 0);   // x_ts (s ≤ t)  [CS][CS]
+  static constexpr int oDM = oXM + CS * CS;     // e_ts        [CS][CS]
+  static constexpr int oPW = oDM + CS * CS;     // a^k, k = 0..CS
+  static constexpr int oAW = oPW + CS + 1;      // k·w·a^{k−1}, k = 0..CS
+  static constexpr int oSQ = oAW + CS + 1;      // ½‖x‖² (Performer) [CS]
+  static constexpr int oDEN = oSQ + CS;         // den_t       [CS]
+  static constexpr int oRHO = oDEN + CS;        // ρ_t         [CS]
+  static constexpr int oRED = oRHO + CS;        // block reduction [kThreads/32]
+  static constexpr int total = oRED + kThreads / 32;
+  static constexpr size_t bytes = size_t(total) * sizeof(float);
+};
+
+struct BwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* g;
+  void* dq;
+  void* dk;
+  void* dv;
+  const void* omega;
+  const float* decay;   // [H] or nullptr (a = 1)
+  int64_t H, n, seg_len;
+  int nseg;
+  bool want_da;
+  // workspace
+  float* fS;    // [BH][nseg][DP*D]  forward-direction aggregates → entering states
+  float* fz;    // [BH][nseg][DP]
+  float* fST;   // [BH][nseg][DP*D]  age-weighted twins
+  float* fzt;   // [BH][nseg][DP]
+  float* rM;    // [BH][nseg][DP*D]  reverse-direction aggregates → adjoints after each segment
+  float* rN;    // [BH][nseg][DP]
+  float* den;   // [BH][n]
+  float* rho;   // [BH][n]
+  float* dapart;  // [BH][nseg]
+};
+
+struct HeadDecay {
+  float a, w;
+};
+
+__device__ __forceinline__ HeadDecay head_decay(const BwdParams& p, int64_t bh) {
+  HeadDecay h;
+  h.a = p.decay ? p.decay[bh % p.H] : 1.f;
+  h.w = new_token_weight(h.a);
+  return h;
+}
+
+// a^k (k = 0..CS) and the ∂a pair weights k·w·a^{k−1} (k ≥ 1).
+template <int CS>
+__device__ void fill_tables(float a, float w, float* pw, float* aw) {
+  for (int k = threadIdx.x; k <= CS; k += kThreads) {
+    pw[k] = decay_pow(a, k);
+    aw[k] = k == 0 ? 0.f : (float)k * w * decay_pow(a, k - 1);
+  }
+}
+
+// Sum of one value per thread over the CTA (result valid in thread 0).
+__device__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kThreads / 32; ++i) t += red[i];
+  return t;
+}
+
+// x_ts = q'_t·k'_s for s ≤ t < cs, 0 elsewhere.
+template <int DP, int CS, int FS>
+__device__ void chunk_scores(const float* qf, const float* kf, int cs, float* xm) {
+  for (int e = threadIdx.x; e < CS * CS; e += kThreads) {
+    const int t = e / CS, s = e % CS;
+    float acc = 0.f;
+    if (s <= t && t < cs)
+      for (int i = 0; i < DP; ++i) acc += qf[t * FS + i] * kf[s * FS + i];
+    xm[e] = acc;
+  }
+}
+
+// Forward-direction state update over one chunk:
+//   S ← a^{cs}S + Σ_s w·a^{cs−1−s} k'_sᵀv_s,
+//   S̃ ← a^{cs}(S̃ + cs·S) + Σ_s (cs−1−s)·w·a^{cs−1−s} k'_sᵀv_s   (when tilde), z, z̃ likewise.
+template <int D, int DP, int CS, int FS>
+__device__ void fwd_state_update(float* S, float* ST, float* z, float* zt, const float* kf,
+                                 const float* vv, const float* pw, float w, int cs, bool tilde) {
+  const float acs = pw[cs];
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) {
+    const int i = e / D, c = e % D;
+    float acc = 0.f, acc_t = 0.f;
+    for (int s = 0; s < cs; ++s) {
+      const float kv = w * pw[cs - 1 - s] * kf[s * FS + i] * vv[s * D + c];
+      acc += kv;
+      acc_t += (float)(cs - 1 - s) * kv;
+    }
+    const float s_old = S[e];
+    S[e] = acs * s_old + acc;
+    if (tilde) ST[e] = acs * (ST[e] + (float)cs * s_old) + acc_t;
+  }
+  for (int i = threadIdx.x; i < DP; i += kThreads) {
+    float acc = 0.f, acc_t = 0.f;
+    for (int s = 0; s < cs; ++s) {
+      const float kk = w * pw[cs - 1 - s] * kf[s * FS + i];
+      acc += kk;
+      acc_t += (float)(cs - 1 - s) * kk;
+    }
+    const float z_old = z[i];
+    z[i] = acs * z_old + acc;
+    if (tilde) zt[i] = acs * (zt[i] + (float)cs * z_old) + acc_t;
+  }
+}
+
+// Reverse-direction adjoint update over one chunk (ĝ in gg, ρ in rho):
+//   M ← a^{cs}M + Σ_t a^{t+1} q'_tᵀ ĝ_t,   N ← a^{cs}N + Σ_t a^{t+1} ρ_t q'_t.
+template <int D, int DP, int CS, int FS>
+__device__ void adj_update(float* M, float* N, const float* qf, const float* gg, const float* rho,
+                           const float* pw, int cs) {
+  const float acs = pw[cs];
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) {
+    const int i = e / D, c = e % D;
+    float acc = 0.f;
+    for (int t = 0; t < cs; ++t) acc += pw[t + 1] * qf[t * FS + i] * gg[t * D + c];
+    M[e] = acs * M[e] + acc;
+  }
+  for (int i = threadIdx.x; i < DP; i += kThreads) {
+    float acc = 0.f;
+    for (int t = 0; t < cs; ++t) acc += pw[t + 1] * rho[t] * qf[t * FS + i];
+    N[i] = acs * N[i] + acc;
+  }
+}
+
+// Gradient through the Performer φ for rows [0, cs): on entry f holds
+// ∂x' ⊙ φ(x); since ∂φ_i/∂x = φ_i·(ω_i − x),
+//   ∂x_c = Σ_i (∂x'_i φ_i) ω_{c,i} − (Σ_i ∂x'_i φ_i)·x_c,
+// written to global memory.  (elu+1 needs no pass of its own: φ' = 1 for
+// x > 0 and e^x = φ(x) otherwise, i.e. min(φ(x), 1).)
+template <typename T, int D, int DP, int CS, int FS>
+__device__ void phi_backward_perf(const float* f, const T* __restrict__ x,
+                                  const T* __restrict__ omega, int cs, float* tot, T* out) {
+  for (int t = threadIdx.x; t < CS; t += kThreads) {
+    float s = 0.f;
+    for (int i = 0; i < DP; ++i) s += f[t * FS + i];
+    tot[t] = s;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < CS * D; e += kThreads) {
+    const int t = e / D, c = e % D;
+    if (t < cs) {
+      float acc = 0.f;
+      for (int i = 0; i < DP; ++i) acc += f[t * FS + i] * to_f32(omega[c * DP + i]);
+      out[(int64_t)t * D + c] = from_f32<T>(acc - tot[t] * to_f32(x[(int64_t)t * D + c]));
+    }
+  }
+}
+
+// ---------------------------------------------------------------- kernels
+
+// Forward-direction aggregates of one segment from zero state: (S, z) and,
+// when ∂a is wanted, (S̃, z̃).
+template <typename T, int D, int DP, bool PERF>
+__global__ void __launch_bounds__(kThreads) bwd_fwd_aggregate(BwdParams p) {
+  using C = BwdCfg<D, DP, PERF>;
+  constexpr int CS = C::CS, FS = C::FS;
+  extern __shared__ float sm[];
+  float *S = sm + C::oS, *ST = sm + C::oST, *z = sm + C::oZ, *zt = sm + C::oZT;
+  float *kf = sm + C::oKF, *vv = sm + C::oV, *xr = sm + C::oXR, *pw = sm + C::oPW;
+  float *aw = sm + C::oAW, *hs = sm + C::oSQ;
+  const int g = blockIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int64_t t_begin = (int64_t)g * p.seg_len, t_end = min(p.n, t_begin + p.seg_len);
+  const HeadDecay hd = head_decay(p, bh);
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) S[e] = ST[e] = 0.f;
+  for (int i = threadIdx.x; i < DP; i += kThreads) z[i] = zt[i] = 0.f;
+  fill_tables<CS>(hd.a, hd.w, pw, aw);
+  const T* kb = static_cast<const T*>(p.k) + bh * p.n * D;
+  const T* vb = static_cast<const T*>(p.v) + bh * p.n * D;
+  const T* om = static_cast<const T*>(p.omega);
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += CS) {
+    const int cs = (int)min((int64_t)CS, t_end - t0);
+    __syncthreads();
+    load_features<T, D, DP, PERF, CS, FS>(kb + t0 * D, cs, kf, xr, hs, om);
+    load_values<T, D, CS>(vb + t0 * D, cs, vv);
+    __syncthreads();
+    fwd_state_update<D, DP, CS, FS>(S, ST, z, zt, kf, vv, pw, hd.w, cs, p.want_da);
+  }
+  __syncthreads();
+  const int64_t o = bh * p.nseg + g;
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) {
+    p.fS[o * (DP * D) + e] = S[e];
+    if (p.want_da) p.fST[o * (DP * D) + e] = ST[e];
+  }
+  for (int i = threadIdx.x; i < DP; i += kThreads) {
+    p.fz[o * DP + i] = z[i];
+    if (p.want_da) p.fzt[o * DP + i] = zt[i];
+  }
+}
+
+// ∂q pass: outputs' normalizers and ρ, ∂q, and this segment's share of ∂a.
+template <typename T, int D, int DP, bool PERF>
+__global__ void __launch_bounds__(kThreads) bwd_dq_pass(BwdParams p) {
+  using C = BwdCfg<D, DP, PERF>;
+  constexpr int CS = C::CS, FS = C::FS;
+  extern __shared__ float sm[];
+  float *S = sm + C::oS, *ST = sm + C::oST, *z = sm + C::oZ, *zt = sm + C::oZT;
+  float *qf = sm + C::oQF, *kf = sm + C::oKF, *vv = sm + C::oV, *gg = sm + C::oG;
+  float *xr = sm + C::oXR, *xm = sm + C::oXM, *dm = sm + C::oDM, *pw = sm + C::oPW;
+  float *aw = sm + C::oAW, *hs = sm + C::oSQ, *den = sm + C::oDEN, *rho = sm + C::oRHO;
+  float* red = sm + C::oRED;
+  const int g = blockIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int64_t t_begin = (int64_t)g * p.seg_len, t_end = min(p.n, t_begin + p.seg_len);
+  const HeadDecay hd = head_decay(p, bh);
+  const float w = hd.w;
+  if (p.nseg > 1) {
+    const int64_t o = bh * p.nseg + g;
+    for (int e = threadIdx.x; e < DP * D; e += kThreads) {
+      S[e] = p.fS[o * (DP * D) + e];
+      ST[e] = p.want_da ? p.fST[o * (DP * D) + e] : 0.f;
+    }
+    for (int i = threadIdx.x; i < DP; i += kThreads) {
+      z[i] = p.fz[o * DP + i];
+      zt[i] = p.want_da ? p.fzt[o * DP + i] : 0.f;
+    }
+  } else {
+    for (int e = threadIdx.x; e < DP * D; e += kThreads) S[e] = ST[e] = 0.f;
+    for (int i = threadIdx.x; i < DP; i += kThreads) z[i] = zt[i] = 0.f;
+  }
+  fill_tables<CS>(hd.a, w, pw, aw);
+  const T* qb = static_cast<const T*>(p.q) + bh * p.n * D;
+  const T* kb = static_cast<const T*>(p.k) + bh * p.n * D;
+  const T* vb = static_cast<const T*>(p.v) + bh * p.n * D;
+  const T* gb = static_cast<const T*>(p.g) + bh * p.n * D;
+  T* dqb = static_cast<T*>(p.dq) + bh * p.n * D;
+  const T* om = static_cast<const T*>(p.omega);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float da_acc = 0.f;
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += CS) {
+    const int cs = (int)min((int64_t)CS, t_end - t0);
+    __syncthreads();
+    load_features<T, D, DP, PERF, CS, FS>(kb + t0 * D, cs, kf, xr, hs, om);
+    __syncthreads();
+    load_features<T, D, DP, PERF, CS, FS>(qb + t0 * D, cs, qf, xr, hs, om);
+    load_values<T, D, CS>(vb + t0 * D, cs, vv);
+    load_values<T, D, CS>(gb + t0 * D, cs, gg);
+    __syncthreads();
+    chunk_scores<DP, CS, FS>(qf, kf, cs, xm);
+    __syncthreads();
+    // den_t = Σ_s W_ts x_ts + a^{t+1} q'_t·z
+    for (int t = threadIdx.x; t < CS; t += kThreads) {
+      float intra = 0.f, inter = 0.f;
+      if (t < cs) {
+        for (int s = 0; s <= t; ++s) intra += w * pw[t - s] * xm[t * CS + s];
+        for (int i = 0; i < DP; ++i) inter += qf[t * FS + i] * z[i];
+      }
+      den[t] = intra + pw[t + 1] * inter;
+    }
+    __syncthreads();
+    // ρ_t = −(g_t·o_t)/den_t, one warp per token
+    for (int t = warp; t < CS; t += kThreads / 32) {
+      float go = 0.f;
+      if (t < cs) {
+        for (int c = lane; c < D; c += 32) {
+          float num = 0.f, inter = 0.f;
+          for (int s = 0; s <= t; ++s) num += w * pw[t - s] * xm[t * CS + s] * vv[s * D + c];
+          for (int i = 0; i < DP; ++i) inter += qf[t * FS + i] * S[i * D + c];
+          go += gg[t * D + c] * (num + pw[t + 1] * inter);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) go += __shfl_xor_sync(0xffffffffu, go, o);
+      if (lane == 0) rho[t] = t < cs ? -go / (den[t] * den[t]) : 0.f;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < CS * D; e += kThreads) {
+      const int t = e / D;
+      gg[e] = t < cs ? gg[e] / den[t] : 0.f;   // ĝ
+    }
+    for (int t = threadIdx.x; t < cs; t += kThreads) {
+      p.den[bh * p.n + t0 + t] = den[t];
+      p.rho[bh * p.n + t0 + t] = rho[t];
+    }
+    __syncthreads();
+    // e_ts = W_ts (ĝ_t·v_s + ρ_t) (= ∂L/∂x_ts); pairs s < t add
+    // (t−s)·w·a^{t−s−1}·x_ts·(ĝ_t·v_s + ρ_t) to ∂a
+    for (int e = threadIdx.x; e < CS * CS; e += kThreads) {
+      const int t = e / CS, s = e % CS;
+      float val = 0.f;
+      if (s <= t && t < cs) {
+        float gv = 0.f;
+        for (int c = 0; c < D; ++c) gv += gg[t * D + c] * vv[s * D + c];
+        val = w * pw[t - s] * (gv + rho[t]);
+        if (s < t) da_acc += aw[t - s] * xm[e] * (gv + rho[t]);
+      }
+      dm[e] = val;
+    }
+    __syncthreads();
+    // ∂q'_t = Σ_s e_ts k'_s + a^{t+1} u_t,  u_t = S ĝ_tᵀ + ρ_t z;
+    // ∂a += a^t q'_t·[(t+1) u_t + S̃ ĝ_tᵀ + ρ_t z̃]
+    for (int e = threadIdx.x; e < CS * DP; e += kThreads) {
+      const int t = e / DP, i = e % DP;
+      if (t < cs) {
+        float intra = 0.f;
+        for (int s = 0; s <= t; ++s) intra += dm[t * CS + s] * kf[s * FS + i];
+        float u = rho[t] * z[i], ut = rho[t] * zt[i];
+        for (int c = 0; c < D; ++c) {
+          u += S[i * D + c] * gg[t * D + c];
+          if (p.want_da) ut += ST[i * D + c] * gg[t * D + c];
+        }
+        const float dqp = intra + pw[t + 1] * u;
+        const float phq = qf[t * FS + i];
+        if (p.want_da) da_acc += pw[t] * phq * ((float)(t + 1) * u + ut);
+        // through φ: elu+1 directly; Performer keeps ∂q' ⊙ φ(q) in q''s slot
+        // (only this thread reads this element in this loop)
+        if (PERF) qf[t * FS + i] = dqp * phq;
+        else dqb[(t0 + t) * D + i] = from_f32<T>(dqp * fminf(phq, 1.f));
+      }
+    }
+    __syncthreads();
+    if (PERF) phi_backward_perf<T, D, DP, CS, FS>(qf, qb + t0 * D, om, cs, hs, dqb + t0 * D);
+    __syncthreads();
+    fwd_state_update<D, DP, CS, FS>(S, ST, z, zt, kf, vv, pw, w, cs, p.want_da);
+  }
+  const float da_blk = block_sum(da_acc, red);
+  if (threadIdx.x == 0) p.dapart[bh * p.nseg + g] = da_blk;
+}
+
+// Reverse-direction aggregates of one segment from zero: (M, N) at the
+// boundary before the segment's first token.
+template <typename T, int D, int DP, bool PERF>
+__global__ void __launch_bounds__(kThreads) bwd_rev_aggregate(BwdParams p) {
+  using C = BwdCfg<D, DP, PERF>;
+  constexpr int CS = C::CS, FS = C::FS;
+  extern __shared__ float sm[];
+  float *M = sm + C::oS, *N = sm + C::oZ, *qf = sm + C::oQF, *gg = sm + C::oG;
+  float *xr = sm + C::oXR, *pw = sm + C::oPW, *aw = sm + C::oAW, *hs = sm + C::oSQ;
+  float *den = sm + C::oDEN, *rho = sm + C::oRHO;
+  const int g = blockIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int64_t t_begin = (int64_t)g * p.seg_len, t_end = min(p.n, t_begin + p.seg_len);
+  const HeadDecay hd = head_decay(p, bh);
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) M[e] = 0.f;
+  for (int i = threadIdx.x; i < DP; i += kThreads) N[i] = 0.f;
+  fill_tables<CS>(hd.a, hd.w, pw, aw);
+  const T* qb = static_cast<const T*>(p.q) + bh * p.n * D;
+  const T* gb = static_cast<const T*>(p.g) + bh * p.n * D;
+  const T* om = static_cast<const T*>(p.omega);
+  const int64_t nch = (t_end - t_begin + CS - 1) / CS;
+  for (int64_t ch = nch - 1; ch >= 0; --ch) {
+    const int64_t t0 = t_begin + ch * CS;
+    const int cs = (int)min((int64_t)CS, t_end - t0);
+    __syncthreads();
+    load_features<T, D, DP, PERF, CS, FS>(qb + t0 * D, cs, qf, xr, hs, om);
+    load_values<T, D, CS>(gb + t0 * D, cs, gg);
+    for (int t = threadIdx.x; t < CS; t += kThreads) {
+      den[t] = t < cs ? p.den[bh * p.n + t0 + t] : 1.f;
+      rho[t] = t < cs ? p.rho[bh * p.n + t0 + t] : 0.f;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < CS * D; e += kThreads) gg[e] = gg[e] / den[e / D];
+    __syncthreads();
+    adj_update<D, DP, CS, FS>(M, N, qf, gg, rho, pw, cs);
+  }
+  __syncthreads();
+  const int64_t o = bh * p.nseg + g;
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) p.rM[o * (DP * D) + e] = M[e];
+  for (int i = threadIdx.x; i < DP; i += kThreads) p.rN[o * DP + i] = N[i];
+}
+
+// ∂k/∂v pass: chunks of the segment in reverse order, from the adjoint after
+// the segment.
+template <typename T, int D, int DP, bool PERF>
+__global__ void __launch_bounds__(kThreads) bwd_dkdv_pass(BwdParams p) {
+  using C = BwdCfg<D, DP, PERF>;
+  constexpr int CS = C::CS, FS = C::FS;
+  extern __shared__ float sm[];
+  float *M = sm + C::oS, *N = sm + C::oZ, *qf = sm + C::oQF, *kf = sm + C::oKF;
+  float *vv = sm + C::oV, *gg = sm + C::oG, *xr = sm + C::oXR, *xm = sm + C::oXM;
+  float *dm = sm + C::oDM, *pw = sm + C::oPW, *aw = sm + C::oAW, *hs = sm + C::oSQ;
+  float *den = sm + C::oDEN, *rho = sm + C::oRHO;
+  const int g = blockIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int64_t t_begin = (int64_t)g * p.seg_len, t_end = min(p.n, t_begin + p.seg_len);
+  const HeadDecay hd = head_decay(p, bh);
+  const float w = hd.w;
+  if (p.nseg > 1) {
+    const int64_t o = bh * p.nseg + g;
+    for (int e = threadIdx.x; e < DP * D; e += kThreads) M[e] = p.rM[o * (DP * D) + e];
+    for (int i = threadIdx.x; i < DP; i += kThreads) N[i] = p.rN[o * DP + i];
+  } else {
+    for (int e = threadIdx.x; e < DP * D; e += kThreads) M[e] = 0.f;
+    for (int i = threadIdx.x; i < DP; i += kThreads) N[i] = 0.f;
+  }
+  fill_tables<CS>(hd.a, w, pw, aw);
+  const T* qb = static_cast<const T*>(p.q) + bh * p.n * D;
+  const T* kb = static_cast<const T*>(p.k) + bh * p.n * D;
+  const T* vb = static_cast<const T*>(p.v) + bh * p.n * D;
+  const T* gb = static_cast<const T*>(p.g) + bh * p.n * D;
+  T* dkb = static_cast<T*>(p.dk) + bh * p.n * D;
+  T* dvb = static_cast<T*>(p.dv) + bh * p.n * D;
+  const T* om = static_cast<const T*>(p.omega);
+  const int64_t nch = (t_end - t_begin + CS - 1) / CS;
+  for (int64_t ch = nch - 1; ch >= 0; --ch) {
+    const int64_t t0 = t_begin + ch * CS;
+    const int cs = (int)min((int64_t)CS, t_end - t0);
+    __syncthreads();
+    load_features<T, D, DP, PERF, CS, FS>(kb + t0 * D, cs, kf, xr, hs, om);
+    __syncthreads();
+    load_features<T, D, DP, PERF, CS, FS>(qb + t0 * D, cs, qf, xr, hs, om);
+    load_values<T, D, CS>(vb + t0 * D, cs, vv);
+    load_values<T, D, CS>(gb + t0 * D, cs, gg);
+    for (int t = threadIdx.x; t < CS; t += kThreads) {
+      den[t] = t < cs ? p.den[bh * p.n + t0 + t] : 1.f;
+      rho[t] = t < cs ? p.rho[bh * p.n + t0 + t] : 0.f;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < CS * D; e += kThreads) gg[e] = gg[e] / den[e / D];   // ĝ
+    chunk_scores<DP, CS, FS>(qf, kf, cs, xm);
+    __syncthreads();
+    // W_ts x_ts (in place) and e_ts = W_ts (ĝ_t·v_s + ρ_t)
+    for (int e = threadIdx.x; e < CS * CS; e += kThreads) {
+      const int t = e / CS, s = e % CS;
+      float wx = 0.f, val = 0.f;
+      if (s <= t && t < cs) {
+        float gv = 0.f;
+        for (int c = 0; c < D; ++c) gv += gg[t * D + c] * vv[s * D + c];
+        wx = w * pw[t - s] * xm[e];
+        val = w * pw[t - s] * (gv + rho[t]);
+      }
+      xm[e] = wx;
+      dm[e] = val;
+    }
+    __syncthreads();
+    // ∂v_s = Σ_{t≥s} W_ts x_ts ĝ_t + w·a^{cs−1−s} k'_s M
+    for (int e = threadIdx.x; e < CS * D; e += kThreads) {
+      const int s = e / D, c = e % D;
+      if (s < cs) {
+        float acc = 0.f, fut = 0.f;
+        for (int t = s; t < cs; ++t) acc += xm[t * CS + s] * gg[t * D + c];
+        for (int i = 0; i < DP; ++i) fut += kf[s * FS + i] * M[i * D + c];
+        dvb[(t0 + s) * D + c] = from_f32<T>(acc + w * pw[cs - 1 - s] * fut);
+      }
+    }
+    __syncthreads();
+    // ∂k'_s = Σ_{t≥s} e_ts q'_t + w·a^{cs−1−s}(M v_s + N), written over k'
+    // (after ∂v has read it) as ∂k' ⊙ φ(k) for the Performer chain rule
+    for (int e = threadIdx.x; e < CS * DP; e += kThreads) {
+      const int s = e / DP, i = e % DP;
+      if (s < cs) {
+        float acc = 0.f, fut = N[i];
+        for (int t = s; t < cs; ++t) acc += dm[t * CS + s] * qf[t * FS + i];
+        for (int c = 0; c < D; ++c) fut += M[i * D + c] * vv[s * D + c];
+        const float dkp = acc + w * pw[cs - 1 - s] * fut;
+        if (PERF) {
+          kf[s * FS + i] = dkp * kf[s * FS + i];
+        } else {
+          dkb[(t0 + s) * D + i] = from_f32<T>(dkp * fminf(kf[s * FS + i], 1.f));
+        }
+      }
+    }
+    __syncthreads();
+    if (PERF) phi_backward_perf<T, D, DP, CS, FS>(kf, kb + t0 * D, om, cs, hs, dkb + t0 * D);
+    __syncthreads();
+    adj_update<D, DP, CS, FS>(M, N, qf, gg, rho, pw, cs);
+  }
+}
+
+// Forward-direction scan over the segment aggregates (in place → entering
+// states): after segment j, S ← a^{L_j}S + A_j and S̃ ← a^{L_j}(S̃ + L_j·S) + Ã_j.
+// Reverse-direction scan (in place → adjoint after each segment): walking
+// down, out[g] = acc, then acc ← A_g + a^{L_g}·acc.
+__global__ void __launch_bounds__(256)
+bwd_scan_kernel(float* fS, float* fz, float* fST, float* fzt, float* rM, float* rN, int64_t H,
+                int nseg, int64_t seg_len, int64_t n, int dpd, int dp, const float* decay,
+                bool want_da, bool reverse) {
+  const int64_t bh = blockIdx.x;
+  const int e = blockIdx.y * 256 + threadIdx.x;
+  if (e >= dpd + dp) return;
+  const float a = decay ? decay[bh % H] : 1.f;
+  auto seg_len_of = [&](int g) { return min(seg_len, n - (int64_t)g * seg_len); };
+  if (!reverse) {
+    float* b = e < dpd ? fS + bh * nseg * (int64_t)dpd + e : fz + bh * nseg * (int64_t)dp + (e - dpd);
+    float* bt = e < dpd ? fST + bh * nseg * (int64_t)dpd + e : fzt + bh * nseg * (int64_t)dp + (e - dpd);
+    const int64_t stride = e < dpd ? dpd : dp;
+    float acc = 0.f, acc_t = 0.f;
+    for (int g = 0; g < nseg; ++g) {
+      const float agg = b[g * stride];
+      const float agg_t = want_da ? bt[g * stride] : 0.f;
+      b[g * stride] = acc;
+      if (want_da) bt[g * stride] = acc_t;
+      const int64_t len = seg_len_of(g);
+      const float f = decay_pow(a, len);
+      acc_t = f * (acc_t + (float)len * acc) + agg_t;
+      acc = f * acc + agg;
+    }
+  } else {
+    float* b = e < dpd ? rM + bh * nseg * (int64_t)dpd + e : rN + bh * nseg * (int64_t)dp + (e - dpd);
+    const int64_t stride = e < dpd ? dpd : dp;
+    float acc = 0.f;
+    for (int g = nseg - 1; g >= 0; --g) {
+      const float agg = b[g * stride];
+      b[g * stride] = acc;
+      acc = agg + decay_pow(a, seg_len_of(g)) * acc;
+    }
+  }
+}
+
+// ∂a[h] = Σ over the batch and the segments of the per-CTA shares (fp64 sum).
+__global__ void bwd_da_reduce(const float* dapart, float* da, int64_t B, int64_t H, int nseg) {
+  const int64_t h = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (h >= H) return;
+  double s = 0.0;
+  for (int64_t b = 0; b < B; ++b)
+    for (int g = 0; g < nseg; ++g) s += (double)dapart[(b * H + h) * nseg + g];
+  da[h] = (float)s;
+}
+
+template <typename T, int D, int DP, bool PERF>
+cudaError_t run_bwd(const BwdArgs& a, const BwdParams& p0, cudaStream_t stream) {
+  using C = BwdCfg<D, DP, PERF>;
+  static_assert(C::bytes <= 227 * 1024, "backward chunk buffers exceed shared memory");
+  const int smem = (int)C::bytes;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(bwd_fwd_aggregate<T, D, DP, PERF>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(bwd_dq_pass<T, D, DP, PERF>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(bwd_rev_aggregate<T, D, DP, PERF>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(bwd_dkdv_pass<T, D, DP, PERF>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+    return e;
+  const BwdParams& p = p0;
+  const int64_t BH = a.B * a.H;
+  const dim3 grid((unsigned)p.nseg, (unsigned)BH);
+  const int dpd = DP * D;
+  const dim3 sgrid((unsigned)BH, (unsigned)((dpd + DP + 255) / 256));
+  if (p.nseg > 1) {
+    bwd_fwd_aggregate<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
+    bwd_scan_kernel<<<sgrid, 256, 0, stream>>>(p.fS, p.fz, p.fST, p.fzt, nullptr, nullptr, a.H,
+                                               p.nseg, p.seg_len, a.n, dpd, DP, a.decay,
+                                               p.want_da, false);
+    count_launches(2);
+  }
+  bwd_dq_pass<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
+  count_launches(1);
+  if (p.nseg > 1) {
+    bwd_rev_aggregate<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
+    bwd_scan_kernel<<<sgrid, 256, 0, stream>>>(nullptr, nullptr, nullptr, nullptr, p.rM, p.rN,
+                                               a.H, p.nseg, p.seg_len, a.n, dpd, DP, a.decay,
+                                               false, true);
+    count_launches(2);
+  }
+  bwd_dkdv_pass<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
+  count_launches(1);
+  if (p.want_da) {
+    bwd_da_reduce<<<(unsigned)((a.H + 127) / 128), 128, 0, stream>>>(p.dapart, a.da, a.B, a.H,
+                                                                     p.nseg);
+    count_launches(1);
+  }
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_bwd(const BwdArgs& a, const BwdParams& p, cudaStream_t s) {
+  if (!a.performer) {
+    switch (a.d) {
+      case 32: return run_bwd<T, 32, 32, false>(a, p, s);
+      case 64: return run_bwd<T, 64, 64, false>(a, p, s);
+      case 128: return run_bwd<T, 128, 128, false>(a, p, s);
+    }
+    return cudaErrorInvalidValue;
+  }
+#define LA_BWD_PERF(DD, MM) \
+  if (a.d == DD && a.m == MM) return run_bwd<T, DD, MM, true>(a, p, s);
+  LA_BWD_PERF(32, 64) LA_BWD_PERF(32, 128) LA_BWD_PERF(32, 256)
+  LA_BWD_PERF(64, 64) LA_BWD_PERF(64, 128) LA_BWD_PERF(64, 256)
+  LA_BWD_PERF(128, 64) LA_BWD_PERF(128, 128)
+#undef LA_BWD_PERF
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool backward_supported(int d, int m, bool performer) {
+  if (!performer) return d == 32 || d == 64 || d == 128;
+  return (d == 32 || d == 64 || d == 128) && (m == 64 || m == 128 || m == 256) && d * m <= 16384;
+}
+
+size_t backward_workspace_floats(const BwdArgs& a, const SegmentPlan& plan) {
+  const size_t BH = (size_t)(a.B * a.H);
+  const size_t dpd = (size_t)a.dp * a.d;
+  size_t f = 2 * BH * (size_t)a.n + BH * (size_t)plan.nseg;   // den, ρ, ∂a shares
+  if (plan.nseg > 1) f += BH * (size_t)plan.nseg * 3 * (dpd + a.dp);   // (S,z), (S̃,z̃), (M,N)
+  return f;
+}
+
+cudaError_t backward(const BwdArgs& a, float* ws, const SegmentPlan& plan, cudaStream_t stream) {
+  const size_t BH = (size_t)(a.B * a.H);
+  const size_t dpd = (size_t)a.dp * a.d;
+  BwdParams p{};
+  p.q = a.q;
+  p.k = a.k;
+  p.v = a.v;
+  p.g = a.g;
+  p.dq = a.dq;
+  p.dk = a.dk;
+  p.dv = a.dv;
+  p.omega = a.omega;
+  p.decay = a.decay;
+  p.H = a.H;
+  p.n = a.n;
+  p.seg_len = plan.seg_len;
+  p.nseg = plan.nseg;
+  p.want_da = a.da != nullptr;
+  float* cur = ws;
+  p.den = cur; cur += BH * (size_t)a.n;
+  p.rho = cur; cur += BH * (size_t)a.n;
+  p.dapart = cur; cur += BH * (size_t)plan.nseg;
+  if (plan.nseg > 1) {
+    const size_t ns = BH * (size_t)plan.nseg;
+    p.fS = cur; cur += ns * dpd;
+    p.fz = cur; cur += ns * a.dp;
+    p.fST = cur; cur += ns * dpd;
+    p.fzt = cur; cur += ns * a.dp;
+    p.rM = cur; cur += ns * dpd;
+    p.rN = cur; cur += ns * a.dp;
+  }
+  if (a.bf16) return dispatch_bwd<__nv_bfloat16>(a, p, stream);
+  return dispatch_bwd<float>(a, p, stream);
+}
+
+}  // namespace la

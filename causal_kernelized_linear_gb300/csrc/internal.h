@@ -53,6 +53,24 @@ struct DecodeArgs {
   bool performer;
 };
 
+// Everything the backward needs, already validated by the API layer.
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* g;        // ∂L/∂o [B,H,n,d]
+  void* dq;
+  void* dk;
+  void* dv;
+  const float* decay;   // [H] or nullptr (a = 1)
+  float* da;            // [H] or nullptr
+  const void* omega;
+  int64_t B, H, n;
+  int d, m, dp;
+  bool bf16;
+  bool performer;
+};
+
 // Segment plan shared by the forward paths: the sequence of every head is cut
 // into nseg segments of seg_len tokens (the last one ragged); per-segment
 // states are combined by segment_scan.
@@ -115,6 +133,11 @@ void count_launches(int k);
 
 // One CTA of bounded waits on a barrier nothing signals (la_selftest_wait_timeout).
 cudaError_t selftest_wait(int* status, uint64_t limit_ns, cudaStream_t stream);
+
+// Backward of the causal forward (fp32 CUDA cores): ∂q, ∂k, ∂v and ∂a.
+bool backward_supported(int d, int m, bool performer);
+size_t backward_workspace_floats(const BwdArgs& a, const SegmentPlan& plan);
+cudaError_t backward(const BwdArgs& a, float* ws, const SegmentPlan& plan, cudaStream_t stream);
 
 // Memory-bound recurrent decode step.
 cudaError_t decode_step(const DecodeArgs& a, cudaStream_t stream);

@@ -197,6 +197,34 @@ la_status la_decode_step_token_decay(float* mu, float* nu, const la_tensor* q,
                                      la_feature_map feature_map, const la_tensor* omega,
                                      la_tensor* out, la_stream stream);
 
+/*
+ * la_backward — gradients of the causal forward (la_forward with causal != 0)
+ * for training: given ∂L/∂o = grad_out, writes ∂L/∂q, ∂L/∂k, ∂L/∂v and,
+ * when da != NULL, ∂L/∂a for the per-head decay ("Efficient Transformers II"
+ * eq (7)–(11) and the causal readout after eq (9), differentiated; the pages
+ * train a "as usual").  With ĝ_j = g_j/den_j and ρ_j = −(g_j·o_j)/den_j:
+ *   ∂q'_j = Σ_{s≤j} w·a^{j−s}(ĝ_j·v_s + ρ_j) k'_s,
+ *   ∂k'_s = Σ_{j≥s} w·a^{j−s}(ĝ_j·v_s + ρ_j) q'_j,
+ *   ∂v_s  = Σ_{j≥s} w·a^{j−s}(q'_j·k'_s) ĝ_j,
+ *   ∂a    = Σ_{s<j} (j−s)·w·a^{j−s−1}(q'_j·k'_s)(ĝ_j·v_s + ρ_j)  (summed over the batch),
+ * then ∂q, ∂k through φ (elu+1: φ' = 1 for x > 0, e^x otherwise; Performer:
+ * ∂φ_i/∂x = φ_i·(ω_i − x)).  The forward's outputs and normalizers are
+ * recomputed; nothing from the forward call needs to be kept.
+ *   q, k, v, decay_a, feature_map, omega  as la_forward (causal).
+ *   grad_out      [B, H, n, d], same dtype as q.
+ *   dq, dk, dv    [B, H, n, d], same dtype as q, written in full.
+ *   da            device fp32 [H] or NULL; needs decay_a (INVALID_ARG otherwise).
+ *                 At a = 1 it is the derivative of the plain sums' extension
+ *                 a ↦ w(a)·a^{j−s} from below.
+ * Runs on fp32 CUDA cores (bf16 inputs are widened); d ∈ {32, 64, 128}, and
+ * for the Performer map d·m ≤ 16384 (else LA_ERR_UNSUPPORTED).  Temporary
+ * workspace as for la_forward (cudaMallocAsync on `stream`).
+ */
+la_status la_backward(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                      const float* decay_a, la_feature_map feature_map, const la_tensor* omega,
+                      const la_tensor* grad_out, la_tensor* dq, la_tensor* dk, la_tensor* dv,
+                      float* da, la_stream stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* la_status_string(la_status status);
 

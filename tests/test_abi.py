@@ -164,6 +164,28 @@ def test_token_decay_validation(lib):
     assert dec(0x20000, qq=_t(shape=(4, 2, 1, 96))) == B.LA_ERR_UNSUPPORTED
 
 
+def test_backward_validation(lib):
+    ok = _t()
+
+    def bwd(go=ok, dk=ok, da=None, decay=0x20000, fm=B.LA_FM_ELU1, omega=None, q=ok):
+        return lib.la_backward(ctypes.byref(q), ctypes.byref(ok), ctypes.byref(ok), decay, fm,
+                               ctypes.byref(omega) if omega else None,
+                               ctypes.byref(go) if go else None, ctypes.byref(ok),
+                               ctypes.byref(dk) if dk else None, ctypes.byref(ok), da, None)
+    assert bwd(go=None) == B.LA_ERR_INVALID_ARG                         # grad_out missing
+    assert bwd(dk=None) == B.LA_ERR_INVALID_ARG                         # dk missing
+    assert bwd(go=_t(shape=(1, 2, 9, 64))) == B.LA_ERR_INVALID_ARG      # shape mismatch
+    assert bwd(dk=_t(dtype=B.LA_F32)) == B.LA_ERR_INVALID_ARG           # dtype mismatch
+    assert bwd(go=_t(ptr=0x10008)) == B.LA_ERR_INVALID_ARG              # misaligned
+    assert bwd(da=0x30000, decay=None) == B.LA_ERR_INVALID_ARG          # ∂a without a decay
+    assert bwd(da=0x30002) == B.LA_ERR_INVALID_ARG                      # misaligned ∂a
+    w = _t(shape=(1, 2, 8, 128))
+    assert lib.la_backward(ctypes.byref(w), ctypes.byref(w), ctypes.byref(w), None,
+                           B.LA_FM_PERFORMER, ctypes.byref(_t(shape=(1, 1, 128, 256))),
+                           ctypes.byref(w), ctypes.byref(w), ctypes.byref(w), ctypes.byref(w),
+                           None, None) == B.LA_ERR_UNSUPPORTED             # d·m = 32768
+
+
 def test_product_path_has_no_oracle_or_cpu_fallback():
     pkg = os.path.join(ROOT, "causal_kernelized_linear_gb300")
     for path in glob.glob(os.path.join(pkg, "**", "*"), recursive=True):
