@@ -22,16 +22,18 @@ namespace {
 constexpr int kDecThreads = 256;
 
 // Where a step's decay and new-token weight come from: per head (a [H], or
-// none for a = 1) or per token (a [B·H] and b [B·H] or none for b = 1 − a).
+// none for a = 1) or, with TOKD, per token (a [B·H] and b [B·H] or none for
+// b = 1 − a).  TOKD is a template parameter so that the per-head kernels
+// carry no code of the per-token form.
 struct StepDecay {
   const float* a;
   const float* b;
   int64_t H;
-  bool per_token;
 };
 
+template <bool TOKD>
 __device__ __forceinline__ void step_decay(const StepDecay& sd, int64_t bh, float& a, float& w) {
-  if (sd.per_token) {
+  if (TOKD) {
     a = sd.a[bh];
     w = sd.b ? sd.b[bh] : 1.f - a;
   } else {
@@ -43,7 +45,7 @@ __device__ __forceinline__ void step_decay(const StepDecay& sd, int64_t bh, floa
 template <typename T>
 __device__ __forceinline__ float load_elem(const T* p, int64_t i) { return to_f32(p[i]); }
 
-template <typename T, int D>
+template <typename T, int D, bool TOKD>
 __global__ void __launch_bounds__(kDecThreads)
 decode_step_kernel(float* __restrict__ mu, float* __restrict__ nu, const T* __restrict__ q,
                    const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ out,
@@ -68,7 +70,7 @@ decode_step_kernel(float* __restrict__ mu, float* __restrict__ nu, const T* __re
   for (int r = 0; r < RPT; ++r) m[r] = __ldcs(mrow + (int64_t)(rg + r * RG) * CG + cg);
 
   float a, w;
-  step_decay(sd, bh, a, w);
+  step_decay<TOKD>(sd, bh, a, w);
   for (int i = tid; i < D; i += kDecThreads) {
     qf[i] = elu1(load_elem(q, bh * D + i));
     kf[i] = elu1(load_elem(k, bh * D + i));
@@ -141,7 +143,7 @@ struct PerfDecodeCfg {
   static_assert(RPT >= 1 && M % RG == 0 && RPT <= 16 && NT >= M, "Performer decode layout");
 };
 
-template <typename T, int D, int M>
+template <typename T, int D, int M, bool TOKD>
 __global__ void __launch_bounds__((PerfDecodeCfg<T, D, M>::NT))
 decode_performer_kernel(float* __restrict__ mu, float* __restrict__ nu, const T* __restrict__ q,
                         const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ out,
@@ -165,7 +167,7 @@ decode_performer_kernel(float* __restrict__ mu, float* __restrict__ nu, const T*
   for (int r = 0; r < RPT; ++r) m[r] = __ldcs(mrow + (int64_t)(rg + r * RG) * CG + cg);
 
   float a, w;
-  step_decay(sd, bh, a, w);
+  step_decay<TOKD>(sd, bh, a, w);
   for (int i = tid; i < D; i += NT) {
     xq[i] = load_elem(q, bh * D + i);
     xk[i] = load_elem(k, bh * D + i);
@@ -249,14 +251,15 @@ StepDecay step_decay_of(const DecodeArgs& a) {
   sd.a = a.decay;
   sd.b = a.weight;
   sd.H = a.H;
-  sd.per_token = a.per_token;
   return sd;
 }
 
 template <typename T, int D, int M>
 cudaError_t launch_perf_decode(const DecodeArgs& a, cudaStream_t s) {
   using Cfg = PerfDecodeCfg<T, D, M>;
-  decode_performer_kernel<T, D, M><<<(unsigned)(a.B * a.H), Cfg::NT, 0, s>>>(
+  auto kern = a.per_token ? decode_performer_kernel<T, D, M, true>
+                          : decode_performer_kernel<T, D, M, false>;
+  kern<<<(unsigned)(a.B * a.H), Cfg::NT, 0, s>>>(
       a.mu, a.nu, static_cast<const T*>(a.q), static_cast<const T*>(a.k),
       static_cast<const T*>(a.v), static_cast<T*>(a.out), step_decay_of(a),
       static_cast<const T*>(a.omega));
@@ -284,13 +287,16 @@ cudaError_t run_decode(const DecodeArgs& a, cudaStream_t s) {
   T* o = static_cast<T*>(a.out);
   switch (a.d) {
     case 32:
-      decode_step_kernel<T, 32><<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, step_decay_of(a));
+      (a.per_token ? decode_step_kernel<T, 32, true> : decode_step_kernel<T, 32, false>)
+          <<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, step_decay_of(a));
       break;
     case 64:
-      decode_step_kernel<T, 64><<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, step_decay_of(a));
+      (a.per_token ? decode_step_kernel<T, 64, true> : decode_step_kernel<T, 64, false>)
+          <<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, step_decay_of(a));
       break;
     case 128:
-      decode_step_kernel<T, 128><<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, step_decay_of(a));
+      (a.per_token ? decode_step_kernel<T, 128, true> : decode_step_kernel<T, 128, false>)
+          <<<grid, kDecThreads, 0, s>>>(a.mu, a.nu, q, k, v, o, step_decay_of(a));
       break;
     default:
       return cudaErrorInvalidValue;

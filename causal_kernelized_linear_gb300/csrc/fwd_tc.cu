@@ -259,6 +259,30 @@ __device__ __forceinline__ TokChunk tok_chunk(const Ctx& x, int c, int lane, Tok
   return t;
 }
 
+// Per-warp running state of the per-token decay, advanced by φ(K) chunk by
+// chunk: the load pipe, and for the chunk φ(K) last ran on L_r (this thread's
+// row), L_{cs−1} and L_63.  The centered folding (Q̃ = 2^{L_t − L_63}φ(q),
+// K̃ = σ·b_s·2^{L_63 − L_s}φ(k)) also keeps log2 ρ of that chunk and, for the
+// state update of the chunk before it, whether its TMEM state is renormalised
+// and by which factor.  With Δ_c = L_63(c+1) + L_{cs−1}(c) − L_63(c) (the decay
+// from token 63 of chunk c to token 63 of chunk c + 1), log2 ρ_{c+1} =
+// log2 ρ_c + Δ_c, reset to 0 (a renormalisation) once it falls below −32, so
+// that σ = 1/ρ never exceeds 2^32.
+struct TokTrack {
+  TokPipe pipe;
+  float lr, tot, mid;
+  float lrho;
+  bool renorm_prev;
+  float alpha_prev;
+};
+
+__device__ __forceinline__ void tok_track_init(TokTrack& tt) {
+  tt.pipe.c = -1;
+  tt.lr = tt.tot = tt.mid = tt.lrho = 0.f;
+  tt.renorm_prev = false;
+  tt.alpha_prev = 1.f;
+}
+
 // Centered folding, lazy rescaling: K'' of chunk c carries σ_c = a^{−128·(c mod R)}
 // (all chunks but the last are full), so that the state MMA can keep
 // accumulating onto the TMEM state for R chunks before it is rescaled.
@@ -469,11 +493,11 @@ __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, in
 // except for the general full kernel, which keeps K' = m·φ(k) in place and
 // writes K'' into its own tile.  φ is computed for every row so that no
 // per-element branch splits the warp.  Signals k_ready for the warp.
-// Per-token decay: m = b_r, gs = b_r·2^{L_{cs−1} − L_r}; tok_out receives
-// (L_r, L_{cs−1}) of the chunk.
+// Per-token decay: general folding m = b_r, gs = b_r·2^{L_{cs−1} − L_r};
+// centered folding gs = σ_c·b_r·2^{L_63 − L_r}; tt advances to this chunk.
 template <int D, bool FULL, bool CEN, bool TOK>
 __device__ __forceinline__ bool phi_k_chunk(const Ctx& x, int c, int r, int j0, int j1, int lane,
-                                            float k_scale_cen, float* tok_out, TokPipe& pipe) {
+                                            float k_scale_cen, TokTrack& tt) {
   using L = Layout<D, FULL, CEN>;
   uint64_t* bar = x.bar;
   int* st = x.status;
@@ -481,17 +505,33 @@ __device__ __forceinline__ bool phi_k_chunk(const Ctx& x, int c, int r, int j0, 
   const int ks = c % L::KST;
   const int cs = (int)min((int64_t)kC, x.t_end - (x.t_begin + (int64_t)c * kC));
   TokChunk tk;
-  if (TOK) tk = tok_chunk(x, c, lane, pipe);
+  if (TOK) tk = tok_chunk(x, c, lane, tt.pipe);
   if (!warp_wait(&bar[B_KFULL0 + ks], (c / L::KST) & 1, st, ab)) return false;
   if (!L::K_IN_PLACE && c >= 1 && !warp_wait(&bar[B_KPEMPTY], (c - 1) & 1, st, ab)) return false;
   const bool live = r < cs;
   uint32_t m2, g2;
   if (TOK) {
     const float lr = pick4(tk.L, r >> 5), br = pick4(tk.B, r >> 5);
-    m2 = splat_bf16x2(br);
-    g2 = splat_bf16x2(br * exp2f(tk.tot - lr));
-    tok_out[0] = lr;
-    tok_out[1] = tk.tot;
+    const float mid = __shfl_sync(0xffffffffu, tk.L[1], 31);   // L_63
+    if (CEN) {
+      if (c == 0) {
+        tt.lrho = 0.f;
+        tt.renorm_prev = false;
+      } else {
+        const float l = tt.lrho + (mid + tt.tot - tt.mid);
+        tt.renorm_prev = l < -32.f;
+        tt.alpha_prev = exp2f(l);
+        tt.lrho = tt.renorm_prev ? 0.f : l;
+      }
+      m2 = 0u;
+      g2 = splat_bf16x2(br * exp2f(mid - lr - tt.lrho));
+    } else {
+      m2 = splat_bf16x2(br);
+      g2 = splat_bf16x2(br * exp2f(tk.tot - lr));
+    }
+    tt.lr = lr;
+    tt.tot = tk.tot;
+    tt.mid = mid;
   } else {
     m2 = live ? 0x3F803F80u : 0u;   // bf16 1.0 / 0.0 pairs
     g2 = live ? splat_bf16x2(CEN ? k_scale_cen * lazy_sigma(x, c) : x.pw[max(cs - 1 - r, 0)]) : 0u;
@@ -558,10 +598,10 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
     // ---- P: causal mask (and, general folding, the decay w·a^{t−s}; per-token
     // decay: 2^{L_t − L_s}, L_s of block b taken from lane s − 32b)
     TokChunk tk;
-    if (TOK) tk = tok_chunk(x, c, lane, pipe);
+    if (TOK && !CEN) tk = tok_chunk(x, c, lane, pipe);
     if (!warp_wait(&bar[B_SCORES], c & 1, st, ab)) break;
     tc_fence_after();
-    const float l_t = TOK ? pick4(tk.L, wq) : 0.f;
+    const float l_t = (TOK && !CEN) ? pick4(tk.L, wq) : 0.f;
     // 32-column blocks b: b > wq lies above the diagonal for the whole warp
     // (zeros, scores not read), b < wq below it (no mask), b == wq straddles it.
     // Loops over blocks and output columns stay rolled: the roles of this
@@ -791,25 +831,26 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
 
   int kj0, kj1;
   KSplit<D, FULL>::range((warp - 8) / 4 + 2, kj0, kj1);
-  // per-token decay: (L_r, L_{cs−1}) of the chunk φ(K) last ran on, and the
+  // per-token decay: the running state of the chunks φ(K) has seen, and the
   // running log2 decay of the segment (state-only launch)
-  float tok[2] = {0.f, 0.f};
+  TokTrack tt;
+  tok_track_init(tt);
   float seg_ld = 0.f;
-  TokPipe pipe;
-  pipe.c = -1;
   auto phi_k = [&](int c) {
-    const bool r_ok =
-        phi_k_chunk<D, FULL, CEN, TOK>(x, c, r, kj0, kj1, lane, k_scale_cen, tok, pipe);
-    if (TOK) seg_ld += tok[1];
+    const bool r_ok = phi_k_chunk<D, FULL, CEN, TOK>(x, c, r, kj0, kj1, lane, k_scale_cen, tt);
+    if (TOK) seg_ld += tt.tot;
     return r_ok;
   };
 
   // D = 128: these warps also compute φ(Q) for their half of the columns;
-  // φ(Q) of the first chunk does not depend on the state, so it goes first
+  // φ(Q) of the first chunk does not depend on the state, so it goes first.
+  // Centered: Q'' = a^{t−63}φ(q) (per-token: 2^{L_t − L_63}, from the chunk
+  // φ(K) last ran on); general: Q' unscaled.
   constexpr bool DO_Q = FULL && Cfg::HALVES == 2;
-  const float a_row = CEN ? decay_pow_signed(a, r - 63) : 1.f;   // general: Q' unscaled
+  const float a_row_head = CEN ? decay_pow_signed(a, r - 63) : 1.f;
+  auto q_row_scale = [&]() { return (CEN && TOK) ? exp2f(tt.lr - tt.mid) : a_row_head; };
   bool ok = x.nchunks > 0 && phi_k(0);
-  if (DO_Q && ok) ok = phi_q_half<D, CEN>(x, 0, half, r, lane, lane_base, a_row);
+  if (DO_Q && ok) ok = phi_q_half<D, CEN>(x, 0, half, r, lane, lane_base, q_row_scale());
 
   // ---- initial state: S_in = Σ_{j<g} a^{L·(g−1−j)}·A_j over the aggregates
   // A_j of the earlier segments of this head (all of length L), written by
@@ -825,8 +866,10 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
     float zin = 0.f;
     if (have_in && srow && half == 0)
       for (int j = 0; j < x.g; ++j) zin = seg_fac(j) * zin + p.ws_z[(agg0 + j) * D + r];
-    const float alpha0 = CEN ? decay_pow_signed(a, 64) : 1.f;
-    const float beta0 = CEN ? alpha0 : (TOK ? exp2f(tok[1]) : decay_pow(a, chunk_len(0)));
+    // centered: tile and TMEM hold a^{64}·S_in (per-token: 2^{L_63}·S_in);
+    // general: tile S_in, TMEM a^{cs}·S_in (per-token: 2^{L_{cs−1}}·S_in)
+    const float alpha0 = CEN ? (TOK ? exp2f(tt.mid) : decay_pow_signed(a, 64)) : 1.f;
+    const float beta0 = CEN ? alpha0 : (TOK ? exp2f(tt.tot) : decay_pow(a, chunk_len(0)));
     put_state([&](int hh, float* v) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = 0.f;
@@ -864,15 +907,22 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
     tc_fence_after();
     float alpha, beta, gamma;
     bool to_tmem;
-    if (CEN) {
+    if (CEN && TOK) {
+      // tt describes chunk c + 1 here (φ(K) of c + 1 ran above), or chunk c
+      // when c is the last one
+      const bool renorm = !last && tt.renorm_prev;
+      alpha = beta = renorm ? tt.alpha_prev : 1.f;
+      gamma = exp2f(tt.tot - tt.mid + tt.lrho);   // 2^{L_{cs−1} − L_63}·ρ_c (last chunk)
+      to_tmem = renorm;
+    } else if (CEN) {
       const bool renorm = !last && (c + 1) % x.R == 0;
       alpha = beta = renorm ? exp2f(128.f * (float)x.R * x.lg) : 1.f;
       gamma = exp2f(x.lg * (float)(cs - 64 + 128 * (c % x.R)));   // a^{cs−64}·ρ_c
       to_tmem = renorm;
     } else {
       alpha = 1.f;
-      // tok holds chunk c + 1's totals here (φ(K) of c + 1 ran above)
-      beta = last ? 1.f : (TOK ? exp2f(tok[1]) : decay_pow(a, chunk_len(c + 1)));
+      // tt holds chunk c + 1's totals here (φ(K) of c + 1 ran above)
+      beta = last ? 1.f : (TOK ? exp2f(tt.tot) : decay_pow(a, chunk_len(c + 1)));
       gamma = 1.f;
       to_tmem = !last;
     }
@@ -899,7 +949,7 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
       if (FULL && !last) mbar_arrive(&bar[B_SREADY]);
     }
     if (DO_Q && c + 1 < x.nchunks &&
-        !phi_q_half<D, CEN>(x, c + 1, half, r, lane, lane_base, a_row))
+        !phi_q_half<D, CEN>(x, c + 1, half, r, lane, lane_base, q_row_scale()))
       break;
   }
   // state-only launch, per-token decay: the segment's total log2 decay
@@ -927,18 +977,66 @@ __device__ __forceinline__ void run_roles(const Ctx& x, const TcParams& p, const
     const float k_scale_cen = CEN ? x.w * decay_pow_signed(x.a, 63 - r) : 0.f;
     int j0, j1;
     KSplit<D, false>::range(warp / 4, j0, j1);
-    float tok[2];
-    TokPipe pipe;
-    pipe.c = -1;
+    TokTrack tt;
+    tok_track_init(tt);
     for (int c = 0; c < x.nchunks; ++c)
-      if (!phi_k_chunk<D, false, CEN, TOK>(x, c, r, j0, j1, lane, k_scale_cen, tok, pipe)) break;
+      if (!phi_k_chunk<D, false, CEN, TOK>(x, c, r, j0, j1, lane, k_scale_cen, tt)) break;
   } else if (FULL && Cfg::HALVES == 1 && warp >= 12) {
     // D = 64: the fourth warpgroup computes φ(Q)
     const int r = (warp - 12) * 32 + lane;
     const float a_row = CEN ? decay_pow_signed(x.a, r - 63) : 1.f;   // general: Q' unscaled
-    for (int c = 0; c < x.nchunks; ++c)
-      if (!phi_q_half<D, CEN>(x, c, 0, r, lane, (uint32_t)(warp - 12) * 32, a_row)) break;
+    TokPipe pipe;
+    pipe.c = -1;
+    for (int c = 0; c < x.nchunks; ++c) {
+      float ar = a_row;
+      if (CEN && TOK) {   // 2^{L_r − L_63} of this chunk
+        const TokChunk tk = tok_chunk(x, c, lane, pipe);
+        ar = exp2f(pick4(tk.L, r >> 5) - __shfl_sync(0xffffffffu, tk.L[1], 31));
+      }
+      if (!phi_q_half<D, CEN>(x, c, 0, r, lane, (uint32_t)(warp - 12) * 32, ar)) break;
+    }
   }
+}
+
+// Per-token decay: whether every chunk of this CTA's segment fits the
+// centered folding — each half of a chunk (tokens 1–63 and 64–127) spans at
+// most 2^64 of decay, so that 2^{±(L_t − L_63)} and σ ≤ 2^32 stay far inside
+// the bf16/fp32 range.  All threads take part (one warp per chunk, 64
+// chunks' loads in flight per round); the answer is the CTA's.
+__device__ bool tok_centered_ok(const Ctx& x, int warp, int lane) {
+  bool bad = false;
+  for (int c0 = warp; c0 < x.nchunks; c0 += 16 * 4) {
+    float av[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + 16 * j;
+      const int64_t t0 = x.t_begin + (int64_t)c * kC;
+      const int cs = c < x.nchunks ? (int)min((int64_t)kC, x.t_end - t0) : 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int s = 32 * i + lane;
+        av[j][i] = s < cs ? __ldg(x.ta + t0 + s) : 1.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int s = 32 * i + lane;
+        const float l = fmaxf(log2f(av[j][i]), -64.f);
+        if (s >= 64) s2 -= l;
+        else if (s >= 1) s1 -= l;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+      }
+      if (s1 > 64.f || s2 > 64.f) bad = true;
+    }
+  }
+  return __syncthreads_or(bad) == 0;
 }
 
 template <int D, bool FULL, bool TOK>
@@ -974,8 +1072,10 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   x.w = new_token_weight(x.a);
   x.ta = TOK ? p.tok_decay + x.bh * p.n : nullptr;
   x.tb = (TOK && p.tok_weight) ? p.tok_weight + x.bh * p.n : nullptr;
-  // the per-token decay always takes the general folding
-  const bool cen = !TOK && ((x.a == 1.f) || (x.a >= kCenteredMinDecay));
+  // the per-token decay takes the centered folding when the whole segment
+  // fits it, the general folding otherwise
+  const bool cen = TOK ? tok_centered_ok(x, warp, lane)
+                       : ((x.a == 1.f) || (x.a >= kCenteredMinDecay));
   x.lg = (cen && x.a != 1.f) ? log2f(x.a) : 0.f;
   // largest R with 128·(R−1)·|log2 a| ≤ 32 − 128·|log2 a|, at least 1
   x.R = x.lg == 0.f ? (1 << 30) : max(1, (int)fminf(32.f / (128.f * -x.lg), 1e9f));
@@ -1023,7 +1123,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   tc_fence_after();
   x.tmem = *tmem_slot;
 
-  if (TOK) run_roles<D, FULL, false, true>(x, p, &map_q, &map_k, &map_v, warp, lane);
+  if (TOK && cen) run_roles<D, FULL, true, true>(x, p, &map_q, &map_k, &map_v, warp, lane);
+  else if (TOK) run_roles<D, FULL, false, true>(x, p, &map_q, &map_k, &map_v, warp, lane);
   else if (cen) run_roles<D, FULL, true, false>(x, p, &map_q, &map_k, &map_v, warp, lane);
   else run_roles<D, FULL, false, false>(x, p, &map_q, &map_k, &map_v, warp, lane);
 
