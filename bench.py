@@ -567,6 +567,14 @@ def run_profile_case(case):
         for _ in range(3):
             cl.forward_token_decay(g["q"], g["k"], g["v"], g["a_tok"], g["b_tok"], "elu1", None,
                                    out=out)
+    elif case == "backward-small":
+        w = W.ELU1_DECAY                             # B4 H8 n2048 d64 (the workload itself)
+        inp = W.forward_inputs(w)
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        gen = torch.Generator().manual_seed(w.seed + 1000)
+        go = torch.randn(w.B, w.H, w.n, w.d, generator=gen).bfloat16().to(dev)
+        for _ in range(3):
+            cl.backward(g["q"], g["k"], g["v"], go, g["a"], "elu1")
     elif case == "decode-small":
         w = W.DECODE
         B = 64                                       # B64 H32 d128: 128 MiB of state
@@ -595,7 +603,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile-case", choices=["forward-long-small", "performer", "decode-small",
-                                               "performer-decode-small", "token-decay-small"],
+                                               "performer-decode-small", "token-decay-small",
+                                               "backward-small"],
                     default=None,
                     help="run a small seeded case for an ncu capture and exit")
     args = ap.parse_args()

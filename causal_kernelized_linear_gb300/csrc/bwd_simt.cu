@@ -36,16 +36,20 @@ template <int D, int DP, bool PERF>
 struct BwdCfg {
   static constexpr int CS = (DP >= 256) ? 16 : 32;   // tokens per chunk
   static constexpr int FS = DP + 1;                   // padded feature row stride
+  // padded row strides of the states and of v, g: loops whose lanes walk the
+  // rows of these arrays read them without bank conflicts
+  static constexpr int SD = D + 1;
+  static constexpr int VD = D + 1;
   // shared memory (floats)
-  static constexpr int oS = 0;                  // S or M      [DP][D]
-  static constexpr int oST = oS + DP * D;       // S̃           [DP][D] (∂q pass and aggregates)
-  static constexpr int oZ = oST + DP * D;       // z or N      [DP]
+  static constexpr int oS = 0;                  // S or M      [DP][SD]
+  static constexpr int oST = oS + DP * SD;      // S̃           [DP][SD] (∂q pass and aggregates)
+  static constexpr int oZ = oST + DP * SD;      // z or N      [DP]
   static constexpr int oZT = oZ + DP;           // z̃           [DP]
   static constexpr int oQF = oZT + DP;          // q'          [CS][FS]
   static constexpr int oKF = oQF + CS * FS;     // k'          [CS][FS]
-  static constexpr int oV = oKF + CS * FS;      // v           [CS][D]
-  static constexpr int oG = oV + CS * D;        // g, then ĝ   [CS][D]
-  static constexpr int oXR = oG + CS * D;       // raw rows (Performer) [CS][D]
+  static constexpr int oV = oKF + CS * FS;      // v           [CS][VD]
+  static constexpr int oG = oV + CS * VD;       // g, then ĝ   [CS][VD]
+  static constexpr int oXR = oG + CS * VD;      // raw rows (Performer) [CS][D]
   static constexpr int oXM = oXR + (PERF ? CS * D : 0);   // x_ts (s ≤ t)  [CS][CS]
   static constexpr int oDM = oXM + CS * CS;     // e_ts        [CS][CS]
   static constexpr int oPW = oDM + CS * CS;     // a^k, k = 0..CS
@@ -131,7 +135,7 @@ __device__ void chunk_scores(const float* qf, const float* kf, int cs, float* xm
 // Forward-direction state update over one chunk:
 //   S ← a^{cs}S + Σ_s w·a^{cs−1−s} k'_sᵀv_s,
 //   S̃ ← a^{cs}(S̃ + cs·S) + Σ_s (cs−1−s)·w·a^{cs−1−s} k'_sᵀv_s   (when tilde), z, z̃ likewise.
-template <int D, int DP, int CS, int FS>
+template <int D, int DP, int CS, int FS, int SD, int VD>
 __device__ void fwd_state_update(float* S, float* ST, float* z, float* zt, const float* kf,
                                  const float* vv, const float* pw, float w, int cs, bool tilde) {
   const float acs = pw[cs];
@@ -139,13 +143,14 @@ __device__ void fwd_state_update(float* S, float* ST, float* z, float* zt, const
     const int i = e / D, c = e % D;
     float acc = 0.f, acc_t = 0.f;
     for (int s = 0; s < cs; ++s) {
-      const float kv = w * pw[cs - 1 - s] * kf[s * FS + i] * vv[s * D + c];
+      const float kv = w * pw[cs - 1 - s] * kf[s * FS + i] * vv[s * VD + c];
       acc += kv;
       acc_t += (float)(cs - 1 - s) * kv;
     }
-    const float s_old = S[e];
-    S[e] = acs * s_old + acc;
-    if (tilde) ST[e] = acs * (ST[e] + (float)cs * s_old) + acc_t;
+    const int o = i * SD + c;
+    const float s_old = S[o];
+    S[o] = acs * s_old + acc;
+    if (tilde) ST[o] = acs * (ST[o] + (float)cs * s_old) + acc_t;
   }
   for (int i = threadIdx.x; i < DP; i += kThreads) {
     float acc = 0.f, acc_t = 0.f;
@@ -162,15 +167,15 @@ __device__ void fwd_state_update(float* S, float* ST, float* z, float* zt, const
 
 // Reverse-direction adjoint update over one chunk (ĝ in gg, ρ in rho):
 //   M ← a^{cs}M + Σ_t a^{t+1} q'_tᵀ ĝ_t,   N ← a^{cs}N + Σ_t a^{t+1} ρ_t q'_t.
-template <int D, int DP, int CS, int FS>
+template <int D, int DP, int CS, int FS, int SD, int VD>
 __device__ void adj_update(float* M, float* N, const float* qf, const float* gg, const float* rho,
                            const float* pw, int cs) {
   const float acs = pw[cs];
   for (int e = threadIdx.x; e < DP * D; e += kThreads) {
     const int i = e / D, c = e % D;
     float acc = 0.f;
-    for (int t = 0; t < cs; ++t) acc += pw[t + 1] * qf[t * FS + i] * gg[t * D + c];
-    M[e] = acs * M[e] + acc;
+    for (int t = 0; t < cs; ++t) acc += pw[t + 1] * qf[t * FS + i] * gg[t * VD + c];
+    M[i * SD + c] = acs * M[i * SD + c] + acc;
   }
   for (int i = threadIdx.x; i < DP; i += kThreads) {
     float acc = 0.f;
@@ -210,7 +215,7 @@ __device__ void phi_backward_perf(const float* f, const T* __restrict__ x,
 template <typename T, int D, int DP, bool PERF>
 __global__ void __launch_bounds__(kThreads) bwd_fwd_aggregate(BwdParams p) {
   using C = BwdCfg<D, DP, PERF>;
-  constexpr int CS = C::CS, FS = C::FS;
+  constexpr int CS = C::CS, FS = C::FS, SD = C::SD, VD = C::VD;
   extern __shared__ float sm[];
   float *S = sm + C::oS, *ST = sm + C::oST, *z = sm + C::oZ, *zt = sm + C::oZT;
   float *kf = sm + C::oKF, *vv = sm + C::oV, *xr = sm + C::oXR, *pw = sm + C::oPW;
@@ -219,7 +224,10 @@ __global__ void __launch_bounds__(kThreads) bwd_fwd_aggregate(BwdParams p) {
   const int64_t bh = blockIdx.y;
   const int64_t t_begin = (int64_t)g * p.seg_len, t_end = min(p.n, t_begin + p.seg_len);
   const HeadDecay hd = head_decay(p, bh);
-  for (int e = threadIdx.x; e < DP * D; e += kThreads) S[e] = ST[e] = 0.f;
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) {
+    const int o = (e / D) * SD + e % D;
+    S[o] = ST[o] = 0.f;
+  }
   for (int i = threadIdx.x; i < DP; i += kThreads) z[i] = zt[i] = 0.f;
   fill_tables<CS>(hd.a, hd.w, pw, aw);
   const T* kb = static_cast<const T*>(p.k) + bh * p.n * D;
@@ -229,15 +237,16 @@ __global__ void __launch_bounds__(kThreads) bwd_fwd_aggregate(BwdParams p) {
     const int cs = (int)min((int64_t)CS, t_end - t0);
     __syncthreads();
     load_features<T, D, DP, PERF, CS, FS>(kb + t0 * D, cs, kf, xr, hs, om);
-    load_values<T, D, CS>(vb + t0 * D, cs, vv);
+    load_values<T, D, CS, VD>(vb + t0 * D, cs, vv);
     __syncthreads();
-    fwd_state_update<D, DP, CS, FS>(S, ST, z, zt, kf, vv, pw, hd.w, cs, p.want_da);
+    fwd_state_update<D, DP, CS, FS, C::SD, C::VD>(S, ST, z, zt, kf, vv, pw, hd.w, cs, p.want_da);
   }
   __syncthreads();
   const int64_t o = bh * p.nseg + g;
   for (int e = threadIdx.x; e < DP * D; e += kThreads) {
-    p.fS[o * (DP * D) + e] = S[e];
-    if (p.want_da) p.fST[o * (DP * D) + e] = ST[e];
+    const int so = (e / D) * SD + e % D;
+    p.fS[o * (DP * D) + e] = S[so];
+    if (p.want_da) p.fST[o * (DP * D) + e] = ST[so];
   }
   for (int i = threadIdx.x; i < DP; i += kThreads) {
     p.fz[o * DP + i] = z[i];
@@ -249,7 +258,7 @@ __global__ void __launch_bounds__(kThreads) bwd_fwd_aggregate(BwdParams p) {
 template <typename T, int D, int DP, bool PERF>
 __global__ void __launch_bounds__(kThreads) bwd_dq_pass(BwdParams p) {
   using C = BwdCfg<D, DP, PERF>;
-  constexpr int CS = C::CS, FS = C::FS;
+  constexpr int CS = C::CS, FS = C::FS, SD = C::SD, VD = C::VD;
   extern __shared__ float sm[];
   float *S = sm + C::oS, *ST = sm + C::oST, *z = sm + C::oZ, *zt = sm + C::oZT;
   float *qf = sm + C::oQF, *kf = sm + C::oKF, *vv = sm + C::oV, *gg = sm + C::oG;
@@ -264,15 +273,19 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_pass(BwdParams p) {
   if (p.nseg > 1) {
     const int64_t o = bh * p.nseg + g;
     for (int e = threadIdx.x; e < DP * D; e += kThreads) {
-      S[e] = p.fS[o * (DP * D) + e];
-      ST[e] = p.want_da ? p.fST[o * (DP * D) + e] : 0.f;
+      const int so = (e / D) * SD + e % D;
+      S[so] = p.fS[o * (DP * D) + e];
+      ST[so] = p.want_da ? p.fST[o * (DP * D) + e] : 0.f;
     }
     for (int i = threadIdx.x; i < DP; i += kThreads) {
       z[i] = p.fz[o * DP + i];
       zt[i] = p.want_da ? p.fzt[o * DP + i] : 0.f;
     }
   } else {
-    for (int e = threadIdx.x; e < DP * D; e += kThreads) S[e] = ST[e] = 0.f;
+    for (int e = threadIdx.x; e < DP * D; e += kThreads) {
+    const int o = (e / D) * SD + e % D;
+    S[o] = ST[o] = 0.f;
+  }
     for (int i = threadIdx.x; i < DP; i += kThreads) z[i] = zt[i] = 0.f;
   }
   fill_tables<CS>(hd.a, w, pw, aw);
@@ -290,8 +303,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_pass(BwdParams p) {
     load_features<T, D, DP, PERF, CS, FS>(kb + t0 * D, cs, kf, xr, hs, om);
     __syncthreads();
     load_features<T, D, DP, PERF, CS, FS>(qb + t0 * D, cs, qf, xr, hs, om);
-    load_values<T, D, CS>(vb + t0 * D, cs, vv);
-    load_values<T, D, CS>(gb + t0 * D, cs, gg);
+    load_values<T, D, CS, VD>(vb + t0 * D, cs, vv);
+    load_values<T, D, CS, VD>(gb + t0 * D, cs, gg);
     __syncthreads();
     chunk_scores<DP, CS, FS>(qf, kf, cs, xm);
     __syncthreads();
@@ -311,9 +324,9 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_pass(BwdParams p) {
       if (t < cs) {
         for (int c = lane; c < D; c += 32) {
           float num = 0.f, inter = 0.f;
-          for (int s = 0; s <= t; ++s) num += w * pw[t - s] * xm[t * CS + s] * vv[s * D + c];
-          for (int i = 0; i < DP; ++i) inter += qf[t * FS + i] * S[i * D + c];
-          go += gg[t * D + c] * (num + pw[t + 1] * inter);
+          for (int s = 0; s <= t; ++s) num += w * pw[t - s] * xm[t * CS + s] * vv[s * VD + c];
+          for (int i = 0; i < DP; ++i) inter += qf[t * FS + i] * S[i * SD + c];
+          go += gg[t * VD + c] * (num + pw[t + 1] * inter);
         }
       }
 #pragma unroll
@@ -322,8 +335,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_pass(BwdParams p) {
     }
     __syncthreads();
     for (int e = threadIdx.x; e < CS * D; e += kThreads) {
-      const int t = e / D;
-      gg[e] = t < cs ? gg[e] / den[t] : 0.f;   // ĝ
+      const int t = e / D, o = t * VD + e % D;
+      gg[o] = t < cs ? gg[o] / den[t] : 0.f;   // ĝ
     }
     for (int t = threadIdx.x; t < cs; t += kThreads) {
       p.den[bh * p.n + t0 + t] = den[t];
@@ -337,7 +350,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_pass(BwdParams p) {
       float val = 0.f;
       if (s <= t && t < cs) {
         float gv = 0.f;
-        for (int c = 0; c < D; ++c) gv += gg[t * D + c] * vv[s * D + c];
+        for (int c = 0; c < D; ++c) gv += gg[t * VD + c] * vv[s * VD + c];
         val = w * pw[t - s] * (gv + rho[t]);
         if (s < t) da_acc += aw[t - s] * xm[e] * (gv + rho[t]);
       }
@@ -353,8 +366,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_pass(BwdParams p) {
         for (int s = 0; s <= t; ++s) intra += dm[t * CS + s] * kf[s * FS + i];
         float u = rho[t] * z[i], ut = rho[t] * zt[i];
         for (int c = 0; c < D; ++c) {
-          u += S[i * D + c] * gg[t * D + c];
-          if (p.want_da) ut += ST[i * D + c] * gg[t * D + c];
+          u += S[i * SD + c] * gg[t * VD + c];
+          if (p.want_da) ut += ST[i * SD + c] * gg[t * VD + c];
         }
         const float dqp = intra + pw[t + 1] * u;
         const float phq = qf[t * FS + i];
@@ -368,7 +381,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_pass(BwdParams p) {
     __syncthreads();
     if (PERF) phi_backward_perf<T, D, DP, CS, FS>(qf, qb + t0 * D, om, cs, hs, dqb + t0 * D);
     __syncthreads();
-    fwd_state_update<D, DP, CS, FS>(S, ST, z, zt, kf, vv, pw, w, cs, p.want_da);
+    fwd_state_update<D, DP, CS, FS, C::SD, C::VD>(S, ST, z, zt, kf, vv, pw, w, cs, p.want_da);
   }
   const float da_blk = block_sum(da_acc, red);
   if (threadIdx.x == 0) p.dapart[bh * p.nseg + g] = da_blk;
@@ -379,7 +392,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_pass(BwdParams p) {
 template <typename T, int D, int DP, bool PERF>
 __global__ void __launch_bounds__(kThreads) bwd_rev_aggregate(BwdParams p) {
   using C = BwdCfg<D, DP, PERF>;
-  constexpr int CS = C::CS, FS = C::FS;
+  constexpr int CS = C::CS, FS = C::FS, SD = C::SD, VD = C::VD;
   extern __shared__ float sm[];
   float *M = sm + C::oS, *N = sm + C::oZ, *qf = sm + C::oQF, *gg = sm + C::oG;
   float *xr = sm + C::oXR, *pw = sm + C::oPW, *aw = sm + C::oAW, *hs = sm + C::oSQ;
@@ -388,7 +401,7 @@ __global__ void __launch_bounds__(kThreads) bwd_rev_aggregate(BwdParams p) {
   const int64_t bh = blockIdx.y;
   const int64_t t_begin = (int64_t)g * p.seg_len, t_end = min(p.n, t_begin + p.seg_len);
   const HeadDecay hd = head_decay(p, bh);
-  for (int e = threadIdx.x; e < DP * D; e += kThreads) M[e] = 0.f;
+  for (int e = threadIdx.x; e < DP * D; e += kThreads) M[(e / D) * SD + e % D] = 0.f;
   for (int i = threadIdx.x; i < DP; i += kThreads) N[i] = 0.f;
   fill_tables<CS>(hd.a, hd.w, pw, aw);
   const T* qb = static_cast<const T*>(p.q) + bh * p.n * D;
@@ -400,19 +413,23 @@ __global__ void __launch_bounds__(kThreads) bwd_rev_aggregate(BwdParams p) {
     const int cs = (int)min((int64_t)CS, t_end - t0);
     __syncthreads();
     load_features<T, D, DP, PERF, CS, FS>(qb + t0 * D, cs, qf, xr, hs, om);
-    load_values<T, D, CS>(gb + t0 * D, cs, gg);
+    load_values<T, D, CS, VD>(gb + t0 * D, cs, gg);
     for (int t = threadIdx.x; t < CS; t += kThreads) {
       den[t] = t < cs ? p.den[bh * p.n + t0 + t] : 1.f;
       rho[t] = t < cs ? p.rho[bh * p.n + t0 + t] : 0.f;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < CS * D; e += kThreads) gg[e] = gg[e] / den[e / D];
+    for (int e = threadIdx.x; e < CS * D; e += kThreads) {
+      const int o = (e / D) * VD + e % D;
+      gg[o] = gg[o] / den[e / D];
+    }
     __syncthreads();
-    adj_update<D, DP, CS, FS>(M, N, qf, gg, rho, pw, cs);
+    adj_update<D, DP, CS, FS, C::SD, C::VD>(M, N, qf, gg, rho, pw, cs);
   }
   __syncthreads();
   const int64_t o = bh * p.nseg + g;
-  for (int e = threadIdx.x; e < DP * D; e += kThreads) p.rM[o * (DP * D) + e] = M[e];
+  for (int e = threadIdx.x; e < DP * D; e += kThreads)
+    p.rM[o * (DP * D) + e] = M[(e / D) * SD + e % D];
   for (int i = threadIdx.x; i < DP; i += kThreads) p.rN[o * DP + i] = N[i];
 }
 
@@ -421,7 +438,7 @@ __global__ void __launch_bounds__(kThreads) bwd_rev_aggregate(BwdParams p) {
 template <typename T, int D, int DP, bool PERF>
 __global__ void __launch_bounds__(kThreads) bwd_dkdv_pass(BwdParams p) {
   using C = BwdCfg<D, DP, PERF>;
-  constexpr int CS = C::CS, FS = C::FS;
+  constexpr int CS = C::CS, FS = C::FS, SD = C::SD, VD = C::VD;
   extern __shared__ float sm[];
   float *M = sm + C::oS, *N = sm + C::oZ, *qf = sm + C::oQF, *kf = sm + C::oKF;
   float *vv = sm + C::oV, *gg = sm + C::oG, *xr = sm + C::oXR, *xm = sm + C::oXM;
@@ -434,10 +451,11 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_pass(BwdParams p) {
   const float w = hd.w;
   if (p.nseg > 1) {
     const int64_t o = bh * p.nseg + g;
-    for (int e = threadIdx.x; e < DP * D; e += kThreads) M[e] = p.rM[o * (DP * D) + e];
+    for (int e = threadIdx.x; e < DP * D; e += kThreads)
+      M[(e / D) * SD + e % D] = p.rM[o * (DP * D) + e];
     for (int i = threadIdx.x; i < DP; i += kThreads) N[i] = p.rN[o * DP + i];
   } else {
-    for (int e = threadIdx.x; e < DP * D; e += kThreads) M[e] = 0.f;
+    for (int e = threadIdx.x; e < DP * D; e += kThreads) M[(e / D) * SD + e % D] = 0.f;
     for (int i = threadIdx.x; i < DP; i += kThreads) N[i] = 0.f;
   }
   fill_tables<CS>(hd.a, w, pw, aw);
@@ -456,14 +474,17 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_pass(BwdParams p) {
     load_features<T, D, DP, PERF, CS, FS>(kb + t0 * D, cs, kf, xr, hs, om);
     __syncthreads();
     load_features<T, D, DP, PERF, CS, FS>(qb + t0 * D, cs, qf, xr, hs, om);
-    load_values<T, D, CS>(vb + t0 * D, cs, vv);
-    load_values<T, D, CS>(gb + t0 * D, cs, gg);
+    load_values<T, D, CS, VD>(vb + t0 * D, cs, vv);
+    load_values<T, D, CS, VD>(gb + t0 * D, cs, gg);
     for (int t = threadIdx.x; t < CS; t += kThreads) {
       den[t] = t < cs ? p.den[bh * p.n + t0 + t] : 1.f;
       rho[t] = t < cs ? p.rho[bh * p.n + t0 + t] : 0.f;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < CS * D; e += kThreads) gg[e] = gg[e] / den[e / D];   // ĝ
+    for (int e = threadIdx.x; e < CS * D; e += kThreads) {   // ĝ
+      const int o = (e / D) * VD + e % D;
+      gg[o] = gg[o] / den[e / D];
+    }
     chunk_scores<DP, CS, FS>(qf, kf, cs, xm);
     __syncthreads();
     // W_ts x_ts (in place) and e_ts = W_ts (ĝ_t·v_s + ρ_t)
@@ -472,7 +493,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_pass(BwdParams p) {
       float wx = 0.f, val = 0.f;
       if (s <= t && t < cs) {
         float gv = 0.f;
-        for (int c = 0; c < D; ++c) gv += gg[t * D + c] * vv[s * D + c];
+        for (int c = 0; c < D; ++c) gv += gg[t * VD + c] * vv[s * VD + c];
         wx = w * pw[t - s] * xm[e];
         val = w * pw[t - s] * (gv + rho[t]);
       }
@@ -485,8 +506,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_pass(BwdParams p) {
       const int s = e / D, c = e % D;
       if (s < cs) {
         float acc = 0.f, fut = 0.f;
-        for (int t = s; t < cs; ++t) acc += xm[t * CS + s] * gg[t * D + c];
-        for (int i = 0; i < DP; ++i) fut += kf[s * FS + i] * M[i * D + c];
+        for (int t = s; t < cs; ++t) acc += xm[t * CS + s] * gg[t * VD + c];
+        for (int i = 0; i < DP; ++i) fut += kf[s * FS + i] * M[i * SD + c];
         dvb[(t0 + s) * D + c] = from_f32<T>(acc + w * pw[cs - 1 - s] * fut);
       }
     }
@@ -498,7 +519,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_pass(BwdParams p) {
       if (s < cs) {
         float acc = 0.f, fut = N[i];
         for (int t = s; t < cs; ++t) acc += dm[t * CS + s] * qf[t * FS + i];
-        for (int c = 0; c < D; ++c) fut += M[i * D + c] * vv[s * D + c];
+        for (int c = 0; c < D; ++c) fut += M[i * SD + c] * vv[s * VD + c];
         const float dkp = acc + w * pw[cs - 1 - s] * fut;
         if (PERF) {
           kf[s * FS + i] = dkp * kf[s * FS + i];
@@ -510,7 +531,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_pass(BwdParams p) {
     __syncthreads();
     if (PERF) phi_backward_perf<T, D, DP, CS, FS>(kf, kb + t0 * D, om, cs, hs, dkb + t0 * D);
     __syncthreads();
-    adj_update<D, DP, CS, FS>(M, N, qf, gg, rho, pw, cs);
+    adj_update<D, DP, CS, FS, C::SD, C::VD>(M, N, qf, gg, rho, pw, cs);
   }
 }
 
@@ -527,29 +548,48 @@ bwd_scan_kernel(float* fS, float* fz, float* fST, float* fzt, float* rM, float* 
   if (e >= dpd + dp) return;
   const float a = decay ? decay[bh % H] : 1.f;
   auto seg_len_of = [&](int g) { return min(seg_len, n - (int64_t)g * seg_len); };
+  constexpr int kBatch = 8;   // aggregates loaded together to keep loads in flight
   if (!reverse) {
     float* b = e < dpd ? fS + bh * nseg * (int64_t)dpd + e : fz + bh * nseg * (int64_t)dp + (e - dpd);
     float* bt = e < dpd ? fST + bh * nseg * (int64_t)dpd + e : fzt + bh * nseg * (int64_t)dp + (e - dpd);
     const int64_t stride = e < dpd ? dpd : dp;
     float acc = 0.f, acc_t = 0.f;
-    for (int g = 0; g < nseg; ++g) {
-      const float agg = b[g * stride];
-      const float agg_t = want_da ? bt[g * stride] : 0.f;
-      b[g * stride] = acc;
-      if (want_da) bt[g * stride] = acc_t;
-      const int64_t len = seg_len_of(g);
-      const float f = decay_pow(a, len);
-      acc_t = f * (acc_t + (float)len * acc) + agg_t;
-      acc = f * acc + agg;
+    for (int g0 = 0; g0 < nseg; g0 += kBatch) {
+      float agg[kBatch], agg_t[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        agg[j] = g0 + j < nseg ? b[(g0 + j) * stride] : 0.f;
+        agg_t[j] = (want_da && g0 + j < nseg) ? bt[(g0 + j) * stride] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int g = g0 + j;
+        if (g < nseg) {
+          b[g * stride] = acc;
+          if (want_da) bt[g * stride] = acc_t;
+          const int64_t len = seg_len_of(g);
+          const float f = decay_pow(a, len);
+          acc_t = f * (acc_t + (float)len * acc) + agg_t[j];
+          acc = f * acc + agg[j];
+        }
+      }
     }
   } else {
     float* b = e < dpd ? rM + bh * nseg * (int64_t)dpd + e : rN + bh * nseg * (int64_t)dp + (e - dpd);
     const int64_t stride = e < dpd ? dpd : dp;
     float acc = 0.f;
-    for (int g = nseg - 1; g >= 0; --g) {
-      const float agg = b[g * stride];
-      b[g * stride] = acc;
-      acc = agg + decay_pow(a, seg_len_of(g)) * acc;
+    for (int g1 = nseg - 1; g1 >= 0; g1 -= kBatch) {
+      float agg[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) agg[j] = g1 - j >= 0 ? b[(g1 - j) * stride] : 0.f;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int g = g1 - j;
+        if (g >= 0) {
+          b[g * stride] = acc;
+          acc = agg[j] + decay_pow(a, seg_len_of(g)) * acc;
+        }
+      }
     }
   }
 }

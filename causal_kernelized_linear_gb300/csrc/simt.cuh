@@ -42,11 +42,12 @@ __device__ void load_features(const T* __restrict__ x, int cs, float* f, float* 
   }
 }
 
-template <typename T, int D, int CS>
+// Rows [0, cs) of one head into vv with row stride VS (zero beyond cs).
+template <typename T, int D, int CS, int VS = D>
 __device__ void load_values(const T* __restrict__ v, int cs, float* vv) {
   for (int e = threadIdx.x; e < CS * D; e += kThreads) {
-    const int t = e / D;
-    vv[e] = (t < cs) ? to_f32(v[(int64_t)t * D + (e % D)]) : 0.f;
+    const int t = e / D, c = e % D;
+    vv[t * VS + c] = (t < cs) ? to_f32(v[(int64_t)t * D + c]) : 0.f;
   }
 }
 

@@ -97,3 +97,42 @@ def test_two_streams_concurrently(cuda_device):
                   TOL_BF16, "stream 1")
     assert_parity(ob, oracle.forward(b["q"], b["k"], b["v"], None, "performer", b["omega"], False),
                   TOL_BF16, "stream 2")
+
+
+def test_token_decay_forward_and_backward_in_graphs(cuda_device):
+    """la_forward_token_decay and la_backward, each captured into a graph
+    (stream-ordered workspace inside the capture) and replayed."""
+    n = 3000
+    x = W.make_forward_inputs(2, 4, n, 64, "bf16", "elu1", decay=(0.9, 0.999), seed=57)
+    a_tok, b_tok = W.make_token_decay(2, 4, n, seed=57)
+    gen = torch.Generator().manual_seed(58)
+    go = torch.randn(2, 4, n, 64, generator=gen).bfloat16()
+    g = to_cuda(x, cuda_device)
+    at, bt, god = a_tok.to(cuda_device), b_tok.to(cuda_device), go.to(cuda_device)
+    out = torch.empty_like(g["q"])
+    dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    # warm-up outside the capture
+    cl.forward_token_decay(g["q"], g["k"], g["v"], at, bt, out=out, stream=s)
+    cl.backward(g["q"], g["k"], g["v"], god, g["a"], dq=dq, dk=dk, dv=dv, want_da=False, stream=s)
+    s.synchronize()
+    g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=s):
+        cl.forward_token_decay(g["q"], g["k"], g["v"], at, bt, out=out, stream=s)
+    with torch.cuda.graph(g2, stream=s):
+        cl.backward(g["q"], g["k"], g["v"], god, g["a"], dq=dq, dk=dk, dv=dv, want_da=False,
+                    stream=s)
+    ref = oracle.forward_token_decay(x["q"], x["k"], x["v"], a_tok, b_tok, "elu1")
+    rq, rk, rv, _ = oracle.backward(x["q"], x["k"], x["v"], go, x["a"], "elu1")
+    for _ in range(2):
+        out.zero_()
+        dq.zero_()
+        g1.replay()
+        g2.replay()
+        torch.cuda.synchronize()
+        assert_parity(out, ref, TOL_BF16, "token decay graph replay")
+        assert_parity(dq, rq, TOL_BF16, "backward graph replay dq")
+        assert_parity(dk, rk, TOL_BF16, "backward graph replay dk")
+        assert_parity(dv, rv, TOL_BF16, "backward graph replay dv")
+    assert cl.last_device_status() == B.LA_OK
