@@ -196,7 +196,9 @@ struct Ctx {
   const float* tb;   // per-token weight of this head, or nullptr
 };
 
-// Per-token decay of chunk c, computed by one warp: lane j gets, for each
+// Per-token decay of chunk c, computed by one warp (hardware lg2/ex2
+// approximations: their relative error, ≈ 2^-22, is far below the bf16
+// rounding the factors get as tensor-core operands): lane j gets, for each
 // 32-token block i of the chunk, L[i] = Σ_{s ≤ 32i+j} log2 a_s (the running
 // sum from the chunk's first token, log2 clamped at −64; tokens past the
 // end add 0) and B[i] = b_{32i+j} (0 past the end); tot is the chunk's sum.
@@ -246,7 +248,7 @@ __device__ __forceinline__ TokChunk tok_chunk(const Ctx& x, int c, int lane, Tok
   float run = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float v = fmaxf(log2f(av[i]), -64.f);
+    float v = fmaxf(lg2_f32(av[i]), -64.f);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float u = __shfl_up_sync(0xffffffffu, v, o);
@@ -524,10 +526,10 @@ __device__ __forceinline__ bool phi_k_chunk(const Ctx& x, int c, int r, int j0, 
         tt.lrho = tt.renorm_prev ? 0.f : l;
       }
       m2 = 0u;
-      g2 = splat_bf16x2(br * exp2f(mid - lr - tt.lrho));
+      g2 = splat_bf16x2(br * ex2_f32(mid - lr - tt.lrho));
     } else {
       m2 = splat_bf16x2(br);
-      g2 = splat_bf16x2(br * exp2f(tk.tot - lr));
+      g2 = splat_bf16x2(br * ex2_f32(tk.tot - lr));
     }
     tt.lr = lr;
     tt.tot = tk.tot;
@@ -848,7 +850,7 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   // φ(K) last ran on); general: Q' unscaled.
   constexpr bool DO_Q = FULL && Cfg::HALVES == 2;
   const float a_row_head = CEN ? decay_pow_signed(a, r - 63) : 1.f;
-  auto q_row_scale = [&]() { return (CEN && TOK) ? exp2f(tt.lr - tt.mid) : a_row_head; };
+  auto q_row_scale = [&]() { return (CEN && TOK) ? ex2_f32(tt.lr - tt.mid) : a_row_head; };
   bool ok = x.nchunks > 0 && phi_k(0);
   if (DO_Q && ok) ok = phi_q_half<D, CEN>(x, 0, half, r, lane, lane_base, q_row_scale());
 
@@ -991,7 +993,7 @@ __device__ __forceinline__ void run_roles(const Ctx& x, const TcParams& p, const
       float ar = a_row;
       if (CEN && TOK) {   // 2^{L_r − L_63} of this chunk
         const TokChunk tk = tok_chunk(x, c, lane, pipe);
-        ar = exp2f(pick4(tk.L, r >> 5) - __shfl_sync(0xffffffffu, tk.L[1], 31));
+        ar = ex2_f32(pick4(tk.L, r >> 5) - __shfl_sync(0xffffffffu, tk.L[1], 31));
       }
       if (!phi_q_half<D, CEN>(x, c, 0, r, lane, (uint32_t)(warp - 12) * 32, ar)) break;
     }
@@ -1024,7 +1026,7 @@ __device__ bool tok_centered_ok(const Ctx& x, int warp, int lane) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int s = 32 * i + lane;
-        const float l = fmaxf(log2f(av[j][i]), -64.f);
+        const float l = fmaxf(lg2_f32(av[j][i]), -64.f);
         if (s >= 64) s2 -= l;
         else if (s >= 1) s1 -= l;
       }

@@ -437,6 +437,12 @@ __device__ __forceinline__ float ex2_f32(float a) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(d) : "f"(a));
   return d;
 }
+// log2 x in fp32 (hardware approximation; 0 and subnormal inputs give −inf).
+__device__ __forceinline__ float lg2_f32(float a) {
+  float d;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(d) : "f"(a));
+  return d;
+}
 // The same bf16 value in both lanes.
 __device__ __forceinline__ uint32_t splat_bf16x2(float x) { return pack_bf16x2(x, x); }
 
