@@ -371,16 +371,18 @@ la_status la_backward(const la_tensor* q, const la_tensor* k, const la_tensor* v
   b.dp = f.dp;
   b.bf16 = f.bf16;
   b.performer = f.performer;
-  // CUDA-core kernels: 32-token chunks, two CTAs per SM
+  // tensor-core kernels (bf16, elu+1, d ∈ {64, 128}): per-chunk states;
+  // CUDA-core kernels otherwise: 32-token chunks, two CTAs per SM
+  const bool tc = la::tc_backward_supported(b);
   const la::SegmentPlan plan = la::plan_segments(f.B * f.H, f.n, di.num_sms, 32, 2);
-  const size_t ws_floats = la::backward_workspace_floats(b, plan);
+  const size_t ws_floats = tc ? la::tc_backward_ws_floats(b) : la::backward_workspace_floats(b, plan);
   float* ws = nullptr;
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_floats * sizeof(float), s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorMemoryAllocation ? LA_ERR_OUT_OF_MEMORY : LA_ERR_CUDA;
   }
-  e = la::backward(b, ws, plan, s);
+  e = tc ? la::tc_backward(b, ws, di.num_sms, di.status, s) : la::backward(b, ws, plan, s);
   cudaError_t fe = cudaFreeAsync(ws, s);
   if (e == cudaSuccess) e = fe;
   return la::to_status(e);

@@ -674,6 +674,24 @@ cudaError_t dispatch_bwd(const BwdArgs& a, const BwdParams& p, cudaStream_t s) {
 
 }  // namespace
 
+cudaError_t backward_scan(float* S, float* z, float* M, float* N, int64_t BH, int64_t H,
+                          int nseg, int64_t seg_len, int64_t n, int dp, int d, const float* decay,
+                          bool reverse, cudaStream_t stream) {
+  const int dpd = dp * d;
+  const dim3 grid((unsigned)BH, (unsigned)((dpd + dp + 255) / 256));
+  bwd_scan_kernel<<<grid, 256, 0, stream>>>(S, z, nullptr, nullptr, M, N, H, nseg, seg_len, n, dpd,
+                                            dp, decay, false, reverse);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t backward_da_reduce(const float* parts, float* da, int64_t B, int64_t H, int nparts,
+                               cudaStream_t stream) {
+  bwd_da_reduce<<<(unsigned)((H + 127) / 128), 128, 0, stream>>>(parts, da, B, H, nparts);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 bool backward_supported(int d, int m, bool performer) {
   if (!performer) return d == 32 || d == 64 || d == 128;
   return (d == 32 || d == 64 || d == 128) && (m == 64 || m == 128 || m == 256) && d * m <= 16384;

@@ -1,0 +1,953 @@
+// Tensor-core (tcgen05 + TMA + TMEM) backward of the causal forward, elu+1
+// map, bf16 inputs, d = d' ∈ {64, 128}: the gradients of L = Σ_t g_t·o_t.
+//
+// Method ("Efficient Transformers II" §2.2, eq (7)–(11) with the causal
+// readout of eq (9), differentiated).  Per head, chunks of C = 128 tokens
+// (local t, s; cs valid), q' = φ(q), k' = φ(k), x_ts = q'_t·k'_s,
+// W_ts = w·a^{t−s} (s ≤ t), and for every chunk c
+//   S_c, z_c  the forward state entering the chunk (Σ_{s<t0} w·a^{t0−1−s} k'_sᵀv_s, …),
+//   M_c, N_c  the adjoint after the chunk (Σ_{t>t1} a^{t−t1} q'_tᵀĝ_t, Σ a^{t−t1} ρ_t q'_t),
+// with ĝ_t = g_t/den_t and ρ_t = −(g_t·o_t)/den_t:
+//   ∂q'_t = Σ_{s≤t} W_ts(ĝ_t·v_s + ρ_t) k'_s + a^{t+1}(S_c ĝ_t + ρ_t z_c)
+//   ∂v_s  = Σ_{t≥s} W_ts x_ts ĝ_t + w·a^{cs−1−s} k'_s M_c
+//   ∂k'_s = Σ_{t≥s} W_ts(ĝ_t·v_s + ρ_t) q'_t + w·a^{cs−1−s}(M_c v_s + N_c)
+// and ∂a = Σ_{s<t}(t−s)·w·a^{t−s−1}·x_ts(ĝ_t·v_s + ρ_t), counted chunk by chunk
+// over the token boundaries inside the chunk: pairs inside it, pairs from
+// before it into it (weight t − t0 + 1), pairs from it to after it (weight
+// t1 − s), and pairs across it (weight cs, the term cs·a^{cs−1}(⟨S_c, M_c⟩ +
+// ⟨z_c, N_c⟩)) — so no position-weighted state is needed.
+//
+// Passes (each CTA loops over (head, chunk) items; 128 threads, thread r =
+// token row r = TMEM lane r; one thread issues the MMAs and every product is
+// waited for before the rows use it):
+//   1. bt_state:  ΔS_c = K''ᵀV (K'' = w·a^{cs−1−s}φ(k)), Δz_c      → workspace
+//   2. scan:      S_c = exclusive decayed prefix of ΔS               (CUDA cores)
+//   3. bt_dq:     recompute o, den; ∂q; den, ρ; ΔM_c = Q''ᵀĜ (Q'' = a^{t+1}φ(q)), ΔN_c
+//   4. scan:      M_c = reverse exclusive decayed suffix of ΔM       (CUDA cores)
+//   5. bt_dkdv:   ∂k, ∂v
+//   6. ∂a:        sum of the per-chunk shares                       (CUDA cores)
+// Every wait is bounded in time; on expiry the kernel records LA_ERR_TIMEOUT
+// in the device status word and stops.
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+#include <cuda.h>
+
+#include <algorithm>
+
+namespace la {
+namespace {
+
+using namespace tc;
+
+constexpr int kCb = 128;          // tokens per chunk
+constexpr int kThreadsB = 128;    // one thread per token row / TMEM lane
+
+template <int D>
+struct BtCfg {
+  static constexpr int HALVES = D / 64;
+  static constexpr int TILE = kCb * D * 2;      // [128 × D] bf16, 128-byte swizzle
+  static constexpr int STILE = D * D * 2;       // [D' × D] bf16 state / adjoint tile
+  static constexpr int oQ = 0;
+  static constexpr int oK = oQ + TILE;
+  static constexpr int oV = oK + TILE;
+  static constexpr int oG = oV + TILE;
+  static constexpr int oS = oG + TILE;
+  static constexpr int oZ = oS + STILE;          // fp32 [D]: z_c or N_c
+  static constexpr int oRHO = oZ + D * 4;        // fp32 [128]
+  static constexpr int oDEN = oRHO + kCb * 4;    // fp32 [128]
+  static constexpr int oPW = oDEN + kCb * 4;     // fp32 a^k, k = 0..128
+  static constexpr int oAW = oPW + 132 * 4;      // fp32 k·w·a^{k−1}, k = 0..128
+  static constexpr int oRED = oAW + 132 * 4;     // fp32 [4] warp partials
+  static constexpr int oBAR = oRED + 16;         // mbarriers: TMA, MMA
+  static constexpr int oMISC = oBAR + 16;        // TMEM slot, abort flag
+  static constexpr int BYTES = oMISC + 16;
+  // + alignment slack; at least half of the SM's shared memory, so that one
+  // CTA (which holds all 512 TMEM columns) runs per SM
+  static constexpr int SMEM_ALLOC = (BYTES + 1024 > 118 * 1024) ? BYTES + 1024 : 118 * 1024;
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  static constexpr uint32_t TMEM_COLS = 512;
+};
+
+struct BtParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* g;
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const float* decay;   // [H] or nullptr
+  int64_t H, n;
+  int nch;              // chunks per head
+  int64_t items;        // B·H·nch
+  float* S;             // [BH][nch][D*D]: ΔS_c, then S_c
+  float* z;             // [BH][nch][D]
+  float* M;             // [BH][nch][D*D]: ΔM_c, then M_c
+  float* N;             // [BH][nch][D]
+  float* den;           // [BH][n]
+  float* rho;           // [BH][n]
+  float* dapart;        // [BH][2·nch]: ∂q pass shares, then ∂k/∂v pass shares
+  bool want_da;
+  int* status;
+};
+
+struct Bt {
+  uint8_t* sm;
+  uint32_t sbase;
+  uint64_t* bar;         // [0] TMA, [1] MMA
+  volatile int* abort_flag;
+  uint32_t tmem;
+  uint32_t tma_phase, mma_phase;
+  bool tma_pending;      // a tile load was issued and not yet waited for
+  int* status;
+};
+
+__device__ __forceinline__ void init_bt(Bt& x, uint8_t* smem_raw, int* status, int off_bar,
+                                        int off_misc) {
+  const uint32_t raw = smem_u32(smem_raw);
+  x.sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  x.sbase = smem_u32(x.sm);
+  x.bar = reinterpret_cast<uint64_t*>(x.sm + off_bar);
+  x.abort_flag = reinterpret_cast<volatile int*>(x.sm + off_misc + 4);
+  x.tma_phase = x.mma_phase = 0;
+  x.tma_pending = false;
+  x.status = status;
+}
+
+// All threads wait for the MMAs issued since the last wait; false on timeout.
+// The outcome is made the same for the whole CTA, so that every thread leaves
+// the item loop together (the loop body is full of CTA barriers).
+__device__ __forceinline__ bool wait_mma(Bt& x) {
+  const bool ok = warp_wait(&x.bar[1], x.mma_phase & 1, x.status, x.abort_flag);
+  ++x.mma_phase;
+  tc_fence_after();
+  return __syncthreads_and(ok) != 0;
+}
+
+// Thread 0 commits the MMAs it issued to the MMA barrier.
+__device__ __forceinline__ void commit_mma(Bt& x) {
+  if (threadIdx.x == 0) mma_commit(&x.bar[1]);
+}
+
+// Hand-off from the rows (TMEM and shared-memory writes) to the MMA issuer.
+__device__ __forceinline__ void rows_to_mma() {
+  tmem_st_wait();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+template <int D>
+__device__ __forceinline__ void load_tiles(Bt& x, const CUtensorMap* const* maps, const int* offs,
+                                           int ntiles, int t0, int bh) {
+  using Cfg = BtCfg<D>;
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&x.bar[0], ntiles * Cfg::TILE);
+    for (int i = 0; i < ntiles; ++i)
+      for (int h = 0; h < Cfg::HALVES; ++h)
+        tma_load_3d(x.sm + offs[i] + h * kCb * 128, maps[i], &x.bar[0], h * 64, t0, bh);
+  }
+  x.tma_pending = true;
+}
+
+__device__ __forceinline__ bool wait_tiles(Bt& x) {
+  const bool ok = warp_wait(&x.bar[0], x.tma_phase & 1, x.status, x.abort_flag);
+  const bool all = __syncthreads_and(ok) != 0;
+  if (all) {
+    ++x.tma_phase;
+    x.tma_pending = false;
+  }
+  return all;
+}
+
+// φ = elu+1 in place on row r of a [128 × D] tile; rows ≥ cs become 0 (the
+// tensor map reads zeros past n, and φ(0) = 1 must not enter the sums).
+template <int D>
+__device__ __forceinline__ void phi_row_inplace(uint8_t* tile, int r, bool live) {
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint4* p = reinterpret_cast<uint4*>(tile + sw_chunk(kCb, r, h, j));
+      uint4 u = *p;
+      if (live) {
+        u.x = elu1_bf16x2(u.x); u.y = elu1_bf16x2(u.y); u.z = elu1_bf16x2(u.z); u.w = elu1_bf16x2(u.w);
+      } else {
+        u = make_uint4(0u, 0u, 0u, 0u);
+      }
+      *p = u;
+    }
+}
+
+// 8 bf16 → 8 floats
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  f[0] = bf16lo_to_f32(u.x); f[1] = bf16hi_to_f32(u.x);
+  f[2] = bf16lo_to_f32(u.y); f[3] = bf16hi_to_f32(u.y);
+  f[4] = bf16lo_to_f32(u.z); f[5] = bf16hi_to_f32(u.z);
+  f[6] = bf16lo_to_f32(u.w); f[7] = bf16hi_to_f32(u.w);
+}
+
+// A [D' × D] fp32 matrix from global memory into the bf16 operand tile
+// (column blocks of [D' × 64], 128-byte swizzle): thread r < D converts row r.
+template <int D>
+__device__ __forceinline__ void load_state_tile(uint8_t* tile, const float* src, int r) {
+  if (r >= D) return;
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 a = *reinterpret_cast<const float4*>(src + r * D + h * 64 + j * 8);
+      const float4 b = *reinterpret_cast<const float4*>(src + r * D + h * 64 + j * 8 + 4);
+      const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      *reinterpret_cast<uint4*>(tile + sw_chunk(D, r, h, j)) = pack8(f);
+    }
+}
+
+// Per-head tables a^k and k·w·a^{k−1} (k = 0..128).
+__device__ __forceinline__ void head_tables(float a, float w, float* pw, float* aw) {
+  for (int k = threadIdx.x; k <= kCb; k += kThreadsB) {
+    pw[k] = decay_pow(a, k);
+    aw[k] = k == 0 ? 0.f : (float)k * w * decay_pow(a, k - 1);
+  }
+}
+
+// Sum over the CTA (valid in every thread).
+__device__ __forceinline__ float cta_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  return red[0] + red[1] + red[2] + red[3];
+}
+
+__device__ __forceinline__ void head_decay(const BtParams& p, int64_t bh, float& a, float& w) {
+  a = p.decay ? p.decay[bh % p.H] : 1.f;
+  w = new_token_weight(a);
+}
+
+template <int D>
+struct BtSetup {
+  using Cfg = BtCfg<D>;
+  __device__ static void run(Bt& x) {
+    if (threadIdx.x == 0) {
+      mbar_init(&x.bar[0], 1);
+      mbar_init(&x.bar[1], 1);
+      *x.abort_flag = 0;
+      fence_barrier_init();
+    }
+    if (threadIdx.x < 32) {
+      tmem_alloc(reinterpret_cast<uint32_t*>(x.sm + Cfg::oMISC), Cfg::TMEM_COLS);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    x.tmem = *reinterpret_cast<uint32_t*>(x.sm + Cfg::oMISC);
+  }
+  __device__ static void teardown(Bt& x) {
+    // nothing issued may still run when TMEM and shared memory are released
+    if (threadIdx.x == 0 && *x.abort_flag) {
+      if (x.tma_pending) mbar_wait_drain(&x.bar[0], x.tma_phase & 1);
+      mma_commit(&x.bar[1]);
+      mbar_wait_drain(&x.bar[1], x.mma_phase & 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      tc_fence_after();
+      tmem_dealloc(x.tmem, Cfg::TMEM_COLS);
+    }
+  }
+};
+
+// ------------------------------------------------------------------ pass 1
+
+// ΔS_c = K''ᵀV with K'' = w·a^{cs−1−s}φ(k) (rows ≥ cs zero), Δz_c = Σ_s K''_s.
+template <int D>
+__global__ void __launch_bounds__(kThreadsB, 1)
+bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                const BtParams p) {
+  using Cfg = BtCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  Bt x;
+  init_bt(x, smem_raw, p.status, Cfg::oBAR, Cfg::oMISC);
+  BtSetup<D>::run(x);
+  float* pw = reinterpret_cast<float*>(x.sm + Cfg::oPW);
+  float* aw = reinterpret_cast<float*>(x.sm + Cfg::oAW);
+  const int r = threadIdx.x, wq = r >> 5;
+  const uint32_t lane_base = (uint32_t)wq * 32;
+  const CUtensorMap* maps[2] = {&map_k, &map_v};
+  const int offs[2] = {Cfg::oK, Cfg::oV};
+  int64_t last_bh = -1;
+  for (int64_t item = blockIdx.x; item < p.items && !*x.abort_flag; item += gridDim.x) {
+    const int64_t bh = item / p.nch;
+    const int c = (int)(item % p.nch);
+    const int t0 = c * kCb;
+    const int cs = (int)min((int64_t)kCb, p.n - t0);
+    float a, w;
+    head_decay(p, bh, a, w);
+    __syncthreads();   // the previous item's tiles and tables are no longer read
+    load_tiles<D>(x, maps, offs, 2, t0, (int)bh);
+    if (bh != last_bh) head_tables(a, w, pw, aw);
+    last_bh = bh;
+    __syncthreads();
+    if (!wait_tiles(x)) break;
+    // K'' in place
+    {
+      uint8_t* kt = x.sm + Cfg::oK;
+      const bool live = r < cs;
+      const uint32_t g2 = live ? splat_bf16x2(w * pw[cs - 1 - r]) : 0u;
+#pragma unroll
+      for (int h = 0; h < Cfg::HALVES; ++h)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint4* pp = reinterpret_cast<uint4*>(kt + sw_chunk(kCb, r, h, j));
+          uint4 u = *pp;
+          u.x = mul_bf16x2(elu1_bf16x2(u.x), g2); u.y = mul_bf16x2(elu1_bf16x2(u.y), g2);
+          u.z = mul_bf16x2(elu1_bf16x2(u.z), g2); u.w = mul_bf16x2(elu1_bf16x2(u.w), g2);
+          *pp = u;
+        }
+    }
+    rows_to_mma();
+    if (threadIdx.x == 0) {
+      const uint64_t dA = smem_desc(x.sbase + Cfg::oK, (D == 128) ? kCb * 128 : 0, 1024, kSwizzle128B);
+      const uint64_t dB = smem_desc(x.sbase + Cfg::oV, kCb * 128, 1024, kSwizzle128B);
+      constexpr uint32_t id = idesc_bf16_f32(128, D, true, true);
+#pragma unroll
+      for (int k = 0; k < kCb / 16; ++k)
+        mma_ss(x.tmem, desc_at(dA, k * 2048), desc_at(dB, k * 2048), id, k > 0);
+    }
+    commit_mma(x);
+    // Δz on the CUDA cores meanwhile (thread i sums feature column i of K'')
+    if (r < D) {
+      const uint8_t* kt = x.sm + Cfg::oK;
+      const int h = r >> 6, j = (r & 63) >> 3, e = r & 7;
+      float acc = 0.f;
+      for (int s = 0; s < cs; ++s) {
+        const uint4 u = *reinterpret_cast<const uint4*>(kt + sw_chunk(kCb, s, h, j));
+        float f[8];
+        unpack8(u, f);
+        acc += f[e];
+      }
+      p.z[item * D + r] = acc;
+    }
+    if (!wait_mma(x)) break;
+    if (r < D) {
+#pragma unroll 1
+      for (int j0 = 0; j0 < D; j0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem_addr(x.tmem, lane_base, j0), v);
+        tmem_ld_wait();
+        float4* dst = reinterpret_cast<float4*>(p.S + (item * D + r) * (int64_t)D + j0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      }
+    }
+    tc_fence_before();
+  }
+  BtSetup<D>::teardown(x);
+}
+
+// ------------------------------------------------------------------ pass 3
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsB, 1)
+bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
+             const BtParams p) {
+  using Cfg = BtCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  Bt x;
+  init_bt(x, smem_raw, p.status, Cfg::oBAR, Cfg::oMISC);
+  BtSetup<D>::run(x);
+  float* zc = reinterpret_cast<float*>(x.sm + Cfg::oZ);
+  float* srho = reinterpret_cast<float*>(x.sm + Cfg::oRHO);
+  float* pw = reinterpret_cast<float*>(x.sm + Cfg::oPW);
+  float* aw = reinterpret_cast<float*>(x.sm + Cfg::oAW);
+  float* red = reinterpret_cast<float*>(x.sm + Cfg::oRED);
+  uint8_t* qt = x.sm + Cfg::oQ;
+  uint8_t* gt = x.sm + Cfg::oG;
+  const int r = threadIdx.x, wq = r >> 5;
+  const uint32_t lane_base = (uint32_t)wq * 32;
+  // TMEM columns: X [0,128) | P, later E (bf16) [128,192) | Y, later U, then ∂q'
+  // [192, 192+D) | PV, later ĜVᵀ, then ΔM [192+D, 320+D)
+  constexpr uint32_t RX = 0, RP = 128, RY = 192, RN = 192 + D;
+  const CUtensorMap* maps[4] = {&map_q, &map_k, &map_v, &map_g};
+  const int offs[4] = {Cfg::oQ, Cfg::oK, Cfg::oV, Cfg::oG};
+  int64_t last_bh = -1;
+  for (int64_t item = blockIdx.x; item < p.items && !*x.abort_flag; item += gridDim.x) {
+    const int64_t bh = item / p.nch;
+    const int c = (int)(item % p.nch);
+    const int t0 = c * kCb;
+    const int cs = (int)min((int64_t)kCb, p.n - t0);
+    const bool live = r < cs;
+    float a, w;
+    head_decay(p, bh, a, w);
+    __syncthreads();
+    load_tiles<D>(x, maps, offs, 4, t0, (int)bh);
+    load_state_tile<D>(x.sm + Cfg::oS, p.S + item * (int64_t)(D * D), r);
+    if (r < D) zc[r] = p.z[item * D + r];
+    if (bh != last_bh) head_tables(a, w, pw, aw);
+    last_bh = bh;
+    __syncthreads();
+    if (!wait_tiles(x)) break;
+    phi_row_inplace<D>(x.sm + Cfg::oQ, r, live);
+    phi_row_inplace<D>(x.sm + Cfg::oK, r, live);
+    rows_to_mma();
+    // X = Q'K'ᵀ, Y = Q'·S_c
+    if (threadIdx.x == 0) {
+      const uint64_t dQ = smem_desc(x.sbase + Cfg::oQ, 16, 1024, kSwizzle128B);
+      const uint64_t dK = smem_desc(x.sbase + Cfg::oK, 16, 1024, kSwizzle128B);
+      const uint64_t dS = smem_desc(x.sbase + Cfg::oS, D * 128, 1024, kSwizzle128B);
+      constexpr uint32_t idX = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idY = idesc_bf16_f32(128, D, false, true);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * (kCb * 128) + (k & 3) * 32;
+        mma_ss(x.tmem + RX, desc_at(dQ, off), desc_at(dK, off), idX, k > 0);
+        mma_ss(x.tmem + RY, desc_at(dQ, off), desc_at(dS, k * 2048), idY, k > 0);
+      }
+    }
+    commit_mma(x);
+    // q'_r·z_c meanwhile
+    float qz = 0.f;
+#pragma unroll
+    for (int h = 0; h < Cfg::HALVES; ++h)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4*>(qt + sw_chunk(kCb, r, h, j)), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qz += f[e] * zc[h * 64 + j * 8 + e];
+      }
+    if (!wait_mma(x)) break;
+    // ---- rows 1: P = W ⊙ X (bf16, for P·V), den
+    float den = 0.f;
+#pragma unroll 1
+    for (int b = 0; b < 4; ++b) {
+      uint32_t pk[16];
+      if (b > wq) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = 0u;
+      } else {
+        uint32_t sc[32];
+        tmem_ld32(tmem_addr(x.tmem, lane_base, RX + b * 32), sc);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const int s0 = b * 32 + j;
+          const float p0 = (s0 <= r) ? w * pw[r - s0] * __uint_as_float(sc[j]) : 0.f;
+          const float p1 = (s0 + 1 <= r) ? w * pw[r - s0 - 1] * __uint_as_float(sc[j + 1]) : 0.f;
+          den += p0 + p1;
+          pk[j / 2] = pack_bf16x2(p0, p1);
+        }
+      }
+      tmem_st16(tmem_addr(x.tmem, lane_base, RP + b * 16), pk);
+    }
+    den += pw[r + 1] * qz;
+    rows_to_mma();
+    if (threadIdx.x == 0) {
+      const uint64_t dV = smem_desc(x.sbase + Cfg::oV, kCb * 128, 1024, kSwizzle128B);
+      constexpr uint32_t idN = idesc_bf16_f32(128, D, false, true);
+#pragma unroll
+      for (int k = 0; k < kCb / 16; ++k)
+        mma_ts(x.tmem + RN, x.tmem + RP + k * 8, desc_at(dV, k * 2048), idN, k > 0);
+    }
+    commit_mma(x);
+    if (!wait_mma(x)) break;
+    // ---- rows 2: o = (P·V + a^{t+1} Y)/den, ρ, ĝ (written over g)
+    const float inv_den = live ? 1.f / den : 0.f;
+    float go = 0.f;
+#pragma unroll 1
+    for (int j0 = 0; j0 < D; j0 += 32) {
+      uint32_t nv[32], yv[32];
+      tmem_ld32(tmem_addr(x.tmem, lane_base, RN + j0), nv);
+      tmem_ld32(tmem_addr(x.tmem, lane_base, RY + j0), yv);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        const int h = (j0 + q8 * 8) >> 6, j = ((j0 + q8 * 8) & 63) >> 3;
+        float gf[8];
+        unpack8(*reinterpret_cast<const uint4*>(gt + sw_chunk(kCb, r, h, j)), gf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float o = (__uint_as_float(nv[q8 * 8 + e]) + pw[r + 1] * __uint_as_float(yv[q8 * 8 + e])) * inv_den;
+          go += gf[e] * o;
+        }
+      }
+    }
+    const float rho = -go * inv_den;
+    srho[r] = rho;
+#pragma unroll
+    for (int h = 0; h < Cfg::HALVES; ++h)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint4* pp = reinterpret_cast<uint4*>(gt + sw_chunk(kCb, r, h, j));
+        float f[8];
+        unpack8(*pp, f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] *= inv_den;
+        *pp = pack8(f);
+      }
+    if (live) {
+      p.den[bh * p.n + t0 + r] = den;
+      p.rho[bh * p.n + t0 + r] = rho;
+    }
+    rows_to_mma();
+    // ĜVᵀ, U = Ĝ·S_cᵀ
+    if (threadIdx.x == 0) {
+      const uint64_t dG = smem_desc(x.sbase + Cfg::oG, 16, 1024, kSwizzle128B);
+      const uint64_t dVk = smem_desc(x.sbase + Cfg::oV, 16, 1024, kSwizzle128B);
+      const uint64_t dSk = smem_desc(x.sbase + Cfg::oS, 16, 1024, kSwizzle128B);
+      constexpr uint32_t idGV = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idU = idesc_bf16_f32(128, D, false, false);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * (kCb * 128) + (k & 3) * 32;
+        const uint32_t offS = (k >> 2) * (D * 128) + (k & 3) * 32;
+        mma_ss(x.tmem + RN, desc_at(dG, off), desc_at(dVk, off), idGV, k > 0);
+        mma_ss(x.tmem + RY, desc_at(dG, off), desc_at(dSk, offS), idU, k > 0);
+      }
+    }
+    commit_mma(x);
+    if (!wait_mma(x)) break;
+    // ---- rows 3: E = W ⊙ (ĜVᵀ + ρ) (bf16, for E·K'), ∂a shares; ∂q' starts
+    // as a^{t+1}·u_t, u_t = S_c ĝ_t + ρ_t z_c
+    float da = 0.f;
+#pragma unroll 1
+    for (int b = 0; b < 4; ++b) {
+      uint32_t pk[16];
+      if (b > wq) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = 0u;
+      } else {
+        uint32_t xv[32], gv[32];
+        tmem_ld32(tmem_addr(x.tmem, lane_base, RX + b * 32), xv);
+        tmem_ld32(tmem_addr(x.tmem, lane_base, RN + b * 32), gv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const int s0 = b * 32 + j;
+          float e2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int s = s0 + u;
+            const float f = __uint_as_float(gv[j + u]) + rho;
+            e2[u] = (s <= r && live) ? w * pw[r - s] * f : 0.f;
+            if (s < r && live) da += aw[r - s] * __uint_as_float(xv[j + u]) * f;
+          }
+          pk[j / 2] = pack_bf16x2(e2[0], e2[1]);
+        }
+      }
+      tmem_st16(tmem_addr(x.tmem, lane_base, RP + b * 16), pk);
+    }
+    float qu = 0.f;
+#pragma unroll 1
+    for (int j0 = 0; j0 < D; j0 += 32) {
+      uint32_t uv[32];
+      tmem_ld32(tmem_addr(x.tmem, lane_base, RY + j0), uv);
+      tmem_ld_wait();
+      float qf[32];
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        const int h = (j0 + q8 * 8) >> 6, j = ((j0 + q8 * 8) & 63) >> 3;
+        unpack8(*reinterpret_cast<const uint4*>(qt + sw_chunk(kCb, r, h, j)), qf + q8 * 8);
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float u = __uint_as_float(uv[e]) + rho * zc[j0 + e];
+        qu += qf[e] * u;
+        uv[e] = __float_as_uint(pw[r + 1] * u);
+      }
+      tmem_st32(tmem_addr(x.tmem, lane_base, RY + j0), uv);
+    }
+    if (live) da += (float)(r + 1) * pw[r] * qu;
+    rows_to_mma();
+    // ∂q' += E·K'
+    if (threadIdx.x == 0) {
+      const uint64_t dKm = smem_desc(x.sbase + Cfg::oK, kCb * 128, 1024, kSwizzle128B);
+      constexpr uint32_t idN = idesc_bf16_f32(128, D, false, true);
+#pragma unroll
+      for (int k = 0; k < kCb / 16; ++k)
+        mma_ts(x.tmem + RY, x.tmem + RP + k * 8, desc_at(dKm, k * 2048), idN, 1);
+    }
+    commit_mma(x);
+    // ΔN_i = Σ_t a^{t+1} ρ_t q'_ti meanwhile (thread i: feature column i)
+    if (r < D) {
+      const int h = r >> 6, j = (r & 63) >> 3, e = r & 7;
+      float acc = 0.f;
+      for (int t = 0; t < cs; ++t) {
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4*>(qt + sw_chunk(kCb, t, h, j)), f);
+        acc += pw[t + 1] * srho[t] * f[e];
+      }
+      p.N[item * D + r] = acc;
+    }
+    if (!wait_mma(x)) break;
+    // ---- rows 4: ∂q = ∂q' ⊙ min(φ(q), 1), then Q'' = a^{t+1}φ(q) in place
+    {
+      __nv_bfloat16* dst = p.dq + (bh * p.n + t0 + (live ? r : 0)) * D;
+#pragma unroll 1
+      for (int j0 = 0; j0 < D; j0 += 32) {
+        uint32_t dv[32];
+        tmem_ld32(tmem_addr(x.tmem, lane_base, RY + j0), dv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          const int h = (j0 + q8 * 8) >> 6, j = ((j0 + q8 * 8) & 63) >> 3;
+          float f[8];
+          unpack8(*reinterpret_cast<const uint4*>(qt + sw_chunk(kCb, r, h, j)), f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(dv[q8 * 8 + e]) * fminf(f[e], 1.f);
+          if (live) *reinterpret_cast<uint4*>(dst + j0 + q8 * 8) = pack8(f);
+        }
+      }
+    }
+    __syncthreads();   // every row's φ(q) has been read (ΔN, ∂q) before it is scaled
+    {
+      const uint32_t s2 = splat_bf16x2(pw[r + 1]);
+#pragma unroll
+      for (int h = 0; h < Cfg::HALVES; ++h)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint4* pp = reinterpret_cast<uint4*>(qt + sw_chunk(kCb, r, h, j));
+          uint4 u = *pp;
+          u.x = mul_bf16x2(u.x, s2); u.y = mul_bf16x2(u.y, s2);
+          u.z = mul_bf16x2(u.z, s2); u.w = mul_bf16x2(u.w, s2);
+          *pp = u;
+        }
+    }
+    rows_to_mma();
+    // ΔM = Q''ᵀĜ
+    if (threadIdx.x == 0) {
+      const uint64_t dA = smem_desc(x.sbase + Cfg::oQ, (D == 128) ? kCb * 128 : 0, 1024, kSwizzle128B);
+      const uint64_t dB = smem_desc(x.sbase + Cfg::oG, kCb * 128, 1024, kSwizzle128B);
+      constexpr uint32_t id = idesc_bf16_f32(128, D, true, true);
+#pragma unroll
+      for (int k = 0; k < kCb / 16; ++k)
+        mma_ss(x.tmem + RN, desc_at(dA, k * 2048), desc_at(dB, k * 2048), id, k > 0);
+    }
+    commit_mma(x);
+    if (!wait_mma(x)) break;
+    if (r < D) {
+#pragma unroll 1
+      for (int j0 = 0; j0 < D; j0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem_addr(x.tmem, lane_base, RN + j0), v);
+        tmem_ld_wait();
+        float4* dst = reinterpret_cast<float4*>(p.M + (item * D + r) * (int64_t)D + j0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      }
+    }
+    tc_fence_before();
+    if (p.want_da) {
+      const float s = cta_sum(da, red);
+      if (threadIdx.x == 0) p.dapart[bh * 2 * p.nch + c] = s;
+    }
+  }
+  BtSetup<D>::teardown(x);
+}
+
+// ------------------------------------------------------------------ pass 5
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsB, 1)
+bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
+               const BtParams p) {
+  using Cfg = BtCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  Bt x;
+  init_bt(x, smem_raw, p.status, Cfg::oBAR, Cfg::oMISC);
+  BtSetup<D>::run(x);
+  float* nc = reinterpret_cast<float*>(x.sm + Cfg::oZ);
+  float* srho = reinterpret_cast<float*>(x.sm + Cfg::oRHO);
+  float* sden = reinterpret_cast<float*>(x.sm + Cfg::oDEN);
+  float* pw = reinterpret_cast<float*>(x.sm + Cfg::oPW);
+  float* aw = reinterpret_cast<float*>(x.sm + Cfg::oAW);
+  float* red = reinterpret_cast<float*>(x.sm + Cfg::oRED);
+  uint8_t* kt = x.sm + Cfg::oK;
+  uint8_t* vt = x.sm + Cfg::oV;
+  uint8_t* gt = x.sm + Cfg::oG;
+  const int r = threadIdx.x, wq = r >> 5;
+  const uint32_t lane_base = (uint32_t)wq * 32;
+  // TMEM columns: Xᵀ, later K'M [0,128) | Pᵀ [128,192) | Eᵀ [192,256) (both
+  // later V·Mᵀ [128, 128+D)) | ∂v [256, 256+D) | ĜᵀV... ĜVᵀᵀ, later ∂k' [384, 512)
+  constexpr uint32_t RX = 0, RP = 128, RE = 192, RF = 128, RV = 256, RK = 384;
+  const CUtensorMap* maps[4] = {&map_q, &map_k, &map_v, &map_g};
+  const int offs[4] = {Cfg::oQ, Cfg::oK, Cfg::oV, Cfg::oG};
+  int64_t last_bh = -1;
+  for (int64_t item = blockIdx.x; item < p.items && !*x.abort_flag; item += gridDim.x) {
+    const int64_t bh = item / p.nch;
+    const int c = (int)(item % p.nch);
+    const int t0 = c * kCb;
+    const int cs = (int)min((int64_t)kCb, p.n - t0);
+    const bool live = r < cs;
+    float a, w;
+    head_decay(p, bh, a, w);
+    __syncthreads();
+    load_tiles<D>(x, maps, offs, 4, t0, (int)bh);
+    load_state_tile<D>(x.sm + Cfg::oS, p.M + item * (int64_t)(D * D), r);
+    if (r < D) nc[r] = p.N[item * D + r];
+    srho[r] = live ? p.rho[bh * p.n + t0 + r] : 0.f;
+    sden[r] = live ? p.den[bh * p.n + t0 + r] : 1.f;
+    if (bh != last_bh) head_tables(a, w, pw, aw);
+    last_bh = bh;
+    // ∂a share of the pairs across the chunk: cs·a^{cs−1}(⟨S_c, M_c⟩ + ⟨z_c, N_c⟩)
+    float da = 0.f;
+    if (p.want_da) {
+      const float* Sc = p.S + item * (int64_t)(D * D);
+      const float* Mc = p.M + item * (int64_t)(D * D);
+      float acc = 0.f;
+      for (int e = threadIdx.x * 4; e < D * D; e += kThreadsB * 4) {
+        const float4 s4 = *reinterpret_cast<const float4*>(Sc + e);
+        const float4 m4 = *reinterpret_cast<const float4*>(Mc + e);
+        acc += s4.x * m4.x + s4.y * m4.y + s4.z * m4.z + s4.w * m4.w;
+      }
+      if (r < D) acc += p.z[item * D + r] * p.N[item * D + r];
+      da = (float)cs * decay_pow(a, cs - 1) * acc;
+    }
+    __syncthreads();
+    if (!wait_tiles(x)) break;
+    phi_row_inplace<D>(x.sm + Cfg::oQ, r, live);
+    phi_row_inplace<D>(kt, r, live);
+    {   // ĝ = g / den in place
+      const float inv = live ? 1.f / sden[r] : 0.f;
+#pragma unroll
+      for (int h = 0; h < Cfg::HALVES; ++h)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint4* pp = reinterpret_cast<uint4*>(gt + sw_chunk(kCb, r, h, j));
+          float f[8];
+          unpack8(*pp, f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] *= inv;
+          *pp = pack8(f);
+        }
+    }
+    rows_to_mma();
+    // Xᵀ = K'Q'ᵀ, (ĜVᵀ)ᵀ = VĜᵀ
+    if (threadIdx.x == 0) {
+      const uint64_t dQ = smem_desc(x.sbase + Cfg::oQ, 16, 1024, kSwizzle128B);
+      const uint64_t dK = smem_desc(x.sbase + Cfg::oK, 16, 1024, kSwizzle128B);
+      const uint64_t dV = smem_desc(x.sbase + Cfg::oV, 16, 1024, kSwizzle128B);
+      const uint64_t dG = smem_desc(x.sbase + Cfg::oG, 16, 1024, kSwizzle128B);
+      constexpr uint32_t id = idesc_bf16_f32(128, 128, false, false);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * (kCb * 128) + (k & 3) * 32;
+        mma_ss(x.tmem + RX, desc_at(dK, off), desc_at(dQ, off), id, k > 0);
+        mma_ss(x.tmem + RK, desc_at(dV, off), desc_at(dG, off), id, k > 0);
+      }
+    }
+    commit_mma(x);
+    if (!wait_mma(x)) break;
+    // ---- rows 1 (thread s = r): Pᵀ_st = W_ts x_ts, Eᵀ_st = W_ts(ĝ_t·v_s + ρ_t), t ≥ s
+#pragma unroll 1
+    for (int b = 0; b < 4; ++b) {
+      uint32_t pk[16], ek[16];
+      if (b < wq) {   // every t of the block is before every s of the warp
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = ek[j] = 0u;
+      } else {
+        uint32_t xv[32], gv[32];
+        tmem_ld32(tmem_addr(x.tmem, lane_base, RX + b * 32), xv);
+        tmem_ld32(tmem_addr(x.tmem, lane_base, RK + b * 32), gv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          float p2[2], e2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int t = b * 32 + j + u;
+            const bool on = t >= r && t < cs;
+            const float wts = on ? w * pw[t - r] : 0.f;
+            p2[u] = wts * __uint_as_float(xv[j + u]);
+            e2[u] = wts * (__uint_as_float(gv[j + u]) + srho[t]);
+          }
+          pk[j / 2] = pack_bf16x2(p2[0], p2[1]);
+          ek[j / 2] = pack_bf16x2(e2[0], e2[1]);
+        }
+      }
+      tmem_st16(tmem_addr(x.tmem, lane_base, RP + b * 16), pk);
+      tmem_st16(tmem_addr(x.tmem, lane_base, RE + b * 16), ek);
+    }
+    rows_to_mma();
+    // ∂v = PᵀĜ, ∂k' = EᵀQ'
+    if (threadIdx.x == 0) {
+      const uint64_t dGm = smem_desc(x.sbase + Cfg::oG, kCb * 128, 1024, kSwizzle128B);
+      const uint64_t dQm = smem_desc(x.sbase + Cfg::oQ, kCb * 128, 1024, kSwizzle128B);
+      constexpr uint32_t idN = idesc_bf16_f32(128, D, false, true);
+#pragma unroll
+      for (int k = 0; k < kCb / 16; ++k) {
+        mma_ts(x.tmem + RV, x.tmem + RP + k * 8, desc_at(dGm, k * 2048), idN, k > 0);
+        mma_ts(x.tmem + RK, x.tmem + RE + k * 8, desc_at(dQm, k * 2048), idN, k > 0);
+      }
+    }
+    commit_mma(x);
+    if (!wait_mma(x)) break;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // K'·M_c, V·M_cᵀ (into the columns of Xᵀ, Pᵀ and Eᵀ, all consumed)
+    if (threadIdx.x == 0) {
+      const uint64_t dK = smem_desc(x.sbase + Cfg::oK, 16, 1024, kSwizzle128B);
+      const uint64_t dV = smem_desc(x.sbase + Cfg::oV, 16, 1024, kSwizzle128B);
+      const uint64_t dMm = smem_desc(x.sbase + Cfg::oS, D * 128, 1024, kSwizzle128B);
+      const uint64_t dMk = smem_desc(x.sbase + Cfg::oS, 16, 1024, kSwizzle128B);
+      constexpr uint32_t idMN = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t idKK = idesc_bf16_f32(128, D, false, false);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * (kCb * 128) + (k & 3) * 32;
+        const uint32_t offS = (k >> 2) * (D * 128) + (k & 3) * 32;
+        mma_ss(x.tmem + RX, desc_at(dK, off), desc_at(dMm, k * 2048), idMN, k > 0);
+        mma_ss(x.tmem + RF, desc_at(dV, off), desc_at(dMk, offS), idKK, k > 0);
+      }
+    }
+    commit_mma(x);
+    if (!wait_mma(x)) break;
+    // ---- rows 2: ∂v_s = (PᵀĜ)_s + w·a^{cs−1−s}(K'M)_s;
+    // ∂k'_s = (EᵀQ')_s + w·a^{cs−1−s}((VMᵀ)_s + N); ∂a share (t1 − s)·w·a^{t1−s−1}·k'_s·((VMᵀ)_s + N).
+    // The TMEM loads are warp-collective, so every row takes part; only the
+    // stores are limited to the valid rows.
+    {
+      const float fut = live ? w * pw[cs - 1 - r] : 0.f;
+      __nv_bfloat16* dvr = p.dv + (bh * p.n + t0 + (live ? r : 0)) * D;
+      __nv_bfloat16* dkr = p.dk + (bh * p.n + t0 + (live ? r : 0)) * D;
+      float kfut = 0.f;
+#pragma unroll 1
+      for (int j0 = 0; j0 < D; j0 += 32) {
+        uint32_t va[32], vb[32];
+        tmem_ld32(tmem_addr(x.tmem, lane_base, RV + j0), va);
+        tmem_ld32(tmem_addr(x.tmem, lane_base, RX + j0), vb);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            f[e] = __uint_as_float(va[q8 * 8 + e]) + fut * __uint_as_float(vb[q8 * 8 + e]);
+          if (live) *reinterpret_cast<uint4*>(dvr + j0 + q8 * 8) = pack8(f);
+        }
+        tmem_ld32(tmem_addr(x.tmem, lane_base, RK + j0), va);
+        tmem_ld32(tmem_addr(x.tmem, lane_base, RF + j0), vb);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          const int h = (j0 + q8 * 8) >> 6, j = ((j0 + q8 * 8) & 63) >> 3;
+          float kf[8], f[8];
+          unpack8(*reinterpret_cast<const uint4*>(kt + sw_chunk(kCb, r, h, j)), kf);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float m = __uint_as_float(vb[q8 * 8 + e]) + nc[j0 + q8 * 8 + e];
+            kfut += kf[e] * m;
+            f[e] = (__uint_as_float(va[q8 * 8 + e]) + fut * m) * fminf(kf[e], 1.f);
+          }
+          if (live) *reinterpret_cast<uint4*>(dkr + j0 + q8 * 8) = pack8(f);
+        }
+      }
+      if (live) da += aw[cs - 1 - r] * kfut;
+    }
+    tc_fence_before();
+    if (p.want_da) {
+      const float s = cta_sum(da, red);
+      if (threadIdx.x == 0) p.dapart[bh * 2 * p.nch + p.nch + c] = s;
+    }
+  }
+  BtSetup<D>::teardown(x);
+}
+
+template <int D>
+cudaError_t run_bt(const BwdArgs& a, float* ws, int num_sms, int* status, cudaStream_t stream) {
+  using Cfg = BtCfg<D>;
+  cudaError_t e;
+  const int64_t BH = a.B * a.H;
+  const int nch = (int)((a.n + kCb - 1) / kCb);
+  BtParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.k = static_cast<const __nv_bfloat16*>(a.k);
+  p.g = static_cast<const __nv_bfloat16*>(a.g);
+  p.dq = static_cast<__nv_bfloat16*>(a.dq);
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.decay = a.decay;
+  p.H = a.H;
+  p.n = a.n;
+  p.nch = nch;
+  p.items = BH * nch;
+  p.want_da = a.da != nullptr;
+  p.status = status;
+  const size_t ns = (size_t)BH * nch;
+  float* cur = ws;
+  p.S = cur; cur += ns * D * D;
+  p.z = cur; cur += ns * D;
+  p.M = cur; cur += ns * D * D;
+  p.N = cur; cur += ns * D;
+  p.den = cur; cur += (size_t)BH * a.n;
+  p.rho = cur; cur += (size_t)BH * a.n;
+  p.dapart = cur;
+  CUtensorMap mq, mk, mv, mg;
+  if ((e = tmap_rows(&mq, a.q, BH, a.n, D, kCb)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mk, a.k, BH, a.n, D, kCb)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mv, a.v, BH, a.n, D, kCb)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mg, a.g, BH, a.n, D, kCb)) != cudaSuccess) return e;
+  const int smem = Cfg::SMEM_ALLOC;
+  if ((e = cudaFuncSetAttribute(bt_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(bt_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(bt_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem)) != cudaSuccess)
+    return e;
+  const unsigned grid = (unsigned)std::min<int64_t>(p.items, (int64_t)num_sms);
+  bt_state_kernel<D><<<grid, kThreadsB, smem, stream>>>(mk, mv, p);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = backward_scan(p.S, p.z, nullptr, nullptr, BH, a.H, nch, kCb, a.n, D, D, a.decay, false,
+                         stream)) != cudaSuccess)
+    return e;
+  bt_dq_kernel<D><<<grid, kThreadsB, smem, stream>>>(mq, mk, mv, mg, p);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = backward_scan(nullptr, nullptr, p.M, p.N, BH, a.H, nch, kCb, a.n, D, D, a.decay, true,
+                         stream)) != cudaSuccess)
+    return e;
+  bt_dkdv_kernel<D><<<grid, kThreadsB, smem, stream>>>(mq, mk, mv, mg, p);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (p.want_da) return backward_da_reduce(p.dapart, a.da, a.B, a.H, 2 * nch, stream);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+bool tc_backward_supported(const BwdArgs& a) {
+  return a.bf16 && !a.performer && (a.d == 64 || a.d == 128) && a.n >= 1;
+}
+
+size_t tc_backward_ws_floats(const BwdArgs& a) {
+  const size_t BH = (size_t)(a.B * a.H);
+  const size_t nch = (size_t)((a.n + kCb - 1) / kCb);
+  const size_t D = (size_t)a.d;
+  return BH * nch * 2 * (D * D + D) + 2 * BH * (size_t)a.n + 2 * BH * nch;
+}
+
+cudaError_t tc_backward(const BwdArgs& a, float* ws, int num_sms, int* status,
+                        cudaStream_t stream) {
+  if (a.d == 128) return run_bt<128>(a, ws, num_sms, status, stream);
+  if (a.d == 64) return run_bt<64>(a, ws, num_sms, status, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace la

@@ -160,18 +160,6 @@ struct TcParams {
   int* status;
 };
 
-// φ(x) = elu(x) + 1 on a pair of bf16 values in packed bf16 arithmetic,
-// without a branch: max(x, 0) + 2^(min(x, 0)·log2 e) (x + 1 for x > 0 since
-// 2^0 = 1 exactly; e^x otherwise).  The result is bf16 (the precision the
-// tensor-core operand is rounded to anyway); the bf16 rounding of the
-// exponent argument and of log2 e adds an error of at most 1.3 % for
-// x ≥ −3 (3 % for x ≥ −6), on the small e^x branch only — the x + 1 branch
-// is rounded once, as before.
-__device__ __forceinline__ uint32_t elu1_bf16x2(uint32_t x) {
-  constexpr uint32_t kLog2e = 0x3FB93FB9u;   // bf16(log2 e) = 1.4453125, both lanes
-  const uint32_t e = ex2_bf16x2(mul_bf16x2(min_bf16x2(x, 0u), kLog2e));
-  return add_bf16x2(max_bf16x2(x, 0u), e);
-}
 
 // a^e for integer e of either sign (a > 0, or e ≥ 0).
 __device__ __forceinline__ float decay_pow_signed(float a, int e) {

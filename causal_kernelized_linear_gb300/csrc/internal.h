@@ -139,6 +139,23 @@ bool backward_supported(int d, int m, bool performer);
 size_t backward_workspace_floats(const BwdArgs& a, const SegmentPlan& plan);
 cudaError_t backward(const BwdArgs& a, float* ws, const SegmentPlan& plan, cudaStream_t stream);
 
+// Scans of the backward over consecutive blocks (segments or chunks) of
+// seg_len tokens, in place: forward (S, z) → the state entering each block;
+// reverse (M, N) → the adjoint after each block.  Only the pointers of the
+// chosen direction are used.
+cudaError_t backward_scan(float* S, float* z, float* M, float* N, int64_t BH, int64_t H,
+                          int nseg, int64_t seg_len, int64_t n, int dp, int d, const float* decay,
+                          bool reverse, cudaStream_t stream);
+// ∂a[h] = Σ over b and the nparts per-(b, h) partial sums (fp64 accumulation).
+cudaError_t backward_da_reduce(const float* parts, float* da, int64_t B, int64_t H, int nparts,
+                               cudaStream_t stream);
+
+// Tensor-core backward (bf16, elu+1, d ∈ {64, 128}): chunk states, the ∂q
+// pass and the ∂k/∂v pass on tcgen05; workspace of tc_backward_ws_floats.
+bool tc_backward_supported(const BwdArgs& a);
+size_t tc_backward_ws_floats(const BwdArgs& a);
+cudaError_t tc_backward(const BwdArgs& a, float* ws, int num_sms, int* status, cudaStream_t stream);
+
 // Memory-bound recurrent decode step.
 cudaError_t decode_step(const DecodeArgs& a, cudaStream_t stream);
 

@@ -216,9 +216,12 @@ la_status la_decode_step_token_decay(float* mu, float* nu, const la_tensor* q,
  *   da            device fp32 [H] or NULL; needs decay_a (INVALID_ARG otherwise).
  *                 At a = 1 it is the derivative of the plain sums' extension
  *                 a ↦ w(a)·a^{j−s} from below.
- * Runs on fp32 CUDA cores (bf16 inputs are widened); d ∈ {32, 64, 128}, and
- * for the Performer map d·m ≤ 16384 (else LA_ERR_UNSUPPORTED).  Temporary
- * workspace as for la_forward (cudaMallocAsync on `stream`).
+ * bf16 inputs with elu+1 and d ∈ {64, 128} run on tcgen05 tensor cores
+ * (per-chunk forward states and adjoints are kept in the workspace: about
+ * 2·(d² + d)·4 bytes per 128 tokens per head, plus 8 bytes per token); all
+ * other cases run on fp32 CUDA cores.  d ∈ {32, 64, 128}, and for the
+ * Performer map d·m ≤ 16384 (else LA_ERR_UNSUPPORTED).  Temporary workspace
+ * as for la_forward (cudaMallocAsync on `stream`).
  */
 la_status la_backward(const la_tensor* q, const la_tensor* k, const la_tensor* v,
                       const float* decay_a, la_feature_map feature_map, const la_tensor* omega,

@@ -82,6 +82,13 @@ CASES = [
     ("bf16", 128, "elu1", 0, (0.95, 0.9999), 1500),
     ("bf16", 32, "elu1", 0, None, 31),
     ("bf16", 64, "performer", 256, (0.9, 0.99), 700),
+    # tensor-core backward (bf16, elu+1, d ∈ {64, 128}): one partial chunk,
+    # exact multiples of 128, ragged tails, a = 0, a = 1 and no decay
+    ("bf16", 128, "elu1", 0, None, 77),
+    ("bf16", 64, "elu1", 0, (0.0, 0.0), 300),
+    ("bf16", 64, "elu1", 0, (1.0, 1.0), 256),
+    ("bf16", 128, "elu1", 0, (0.3, 0.9), 640),
+    ("bf16", 64, "elu1", 0, (0.5, 0.99), 129),
 ]
 
 
