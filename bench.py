@@ -575,6 +575,14 @@ def run_profile_case(case):
         go = torch.randn(w.B, w.H, w.n, w.d, generator=gen).bfloat16().to(dev)
         for _ in range(3):
             cl.backward(g["q"], g["k"], g["v"], go, g["a"], "elu1")
+    elif case == "backward-long-small":
+        w = W.LONG
+        inp = W.forward_inputs(w, n=16384)          # B1 H16 n16384 d128: 64 MiB per tensor
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        gen = torch.Generator().manual_seed(w.seed + 1000)
+        go = torch.randn(w.B, w.H, 16384, w.d, generator=gen).bfloat16().to(dev)
+        for _ in range(3):
+            cl.backward(g["q"], g["k"], g["v"], go, g["a"], "elu1")
     elif case == "decode-small":
         w = W.DECODE
         B = 64                                       # B64 H32 d128: 128 MiB of state
@@ -604,7 +612,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile-case", choices=["forward-long-small", "performer", "decode-small",
                                                "performer-decode-small", "token-decay-small",
-                                               "backward-small"],
+                                               "backward-small", "backward-long-small"],
                     default=None,
                     help="run a small seeded case for an ncu capture and exit")
     args = ap.parse_args()

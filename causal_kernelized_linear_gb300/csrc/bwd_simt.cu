@@ -547,7 +547,12 @@ bwd_scan_kernel(float* fS, float* fz, float* fST, float* fzt, float* rM, float* 
   const int e = blockIdx.y * 256 + threadIdx.x;
   if (e >= dpd + dp) return;
   const float a = decay ? decay[bh % H] : 1.f;
+  const float a_full = decay_pow(a, seg_len);   // every block but the last is full
   auto seg_len_of = [&](int g) { return min(seg_len, n - (int64_t)g * seg_len); };
+  auto fac_of = [&](int g) {
+    const int64_t len = seg_len_of(g);
+    return len == seg_len ? a_full : decay_pow(a, len);
+  };
   constexpr int kBatch = 8;   // aggregates loaded together to keep loads in flight
   if (!reverse) {
     float* b = e < dpd ? fS + bh * nseg * (int64_t)dpd + e : fz + bh * nseg * (int64_t)dp + (e - dpd);
@@ -568,7 +573,7 @@ bwd_scan_kernel(float* fS, float* fz, float* fST, float* fzt, float* rM, float* 
           b[g * stride] = acc;
           if (want_da) bt[g * stride] = acc_t;
           const int64_t len = seg_len_of(g);
-          const float f = decay_pow(a, len);
+          const float f = fac_of(g);
           acc_t = f * (acc_t + (float)len * acc) + agg_t[j];
           acc = f * acc + agg[j];
         }
@@ -587,21 +592,33 @@ bwd_scan_kernel(float* fS, float* fz, float* fST, float* fzt, float* rM, float* 
         const int g = g1 - j;
         if (g >= 0) {
           b[g * stride] = acc;
-          acc = agg[j] + decay_pow(a, seg_len_of(g)) * acc;
+          acc = agg[j] + fac_of(g) * acc;
         }
       }
     }
   }
 }
 
-// ∂a[h] = Σ over the batch and the segments of the per-CTA shares (fp64 sum).
-__global__ void bwd_da_reduce(const float* dapart, float* da, int64_t B, int64_t H, int nseg) {
-  const int64_t h = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (h >= H) return;
+// ∂a[h] = Σ over the batch and the segments (or chunks) of the per-CTA
+// shares: one block per head, fp64 partial sums per thread, then a fixed-order
+// tree over the block (deterministic).
+__global__ void __launch_bounds__(256)
+bwd_da_reduce(const float* dapart, float* da, int64_t B, int64_t H, int nseg) {
+  __shared__ double red[256];
+  const int64_t h = blockIdx.x;
   double s = 0.0;
-  for (int64_t b = 0; b < B; ++b)
-    for (int g = 0; g < nseg; ++g) s += (double)dapart[(b * H + h) * nseg + g];
-  da[h] = (float)s;
+  const int64_t per_b = nseg;
+  for (int64_t i = threadIdx.x; i < B * per_b; i += 256) {
+    const int64_t b = i / per_b, g = i % per_b;
+    s += (double)dapart[(b * H + h) * nseg + g];
+  }
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) da[h] = (float)red[0];
 }
 
 template <typename T, int D, int DP, bool PERF>
@@ -646,8 +663,7 @@ cudaError_t run_bwd(const BwdArgs& a, const BwdParams& p0, cudaStream_t stream) 
   bwd_dkdv_pass<T, D, DP, PERF><<<grid, kThreads, smem, stream>>>(p);
   count_launches(1);
   if (p.want_da) {
-    bwd_da_reduce<<<(unsigned)((a.H + 127) / 128), 128, 0, stream>>>(p.dapart, a.da, a.B, a.H,
-                                                                     p.nseg);
+    bwd_da_reduce<<<(unsigned)a.H, 256, 0, stream>>>(p.dapart, a.da, a.B, a.H, p.nseg);
     count_launches(1);
   }
   return cudaGetLastError();
@@ -687,7 +703,7 @@ cudaError_t backward_scan(float* S, float* z, float* M, float* N, int64_t BH, in
 
 cudaError_t backward_da_reduce(const float* parts, float* da, int64_t B, int64_t H, int nparts,
                                cudaStream_t stream) {
-  bwd_da_reduce<<<(unsigned)((H + 127) / 128), 128, 0, stream>>>(parts, da, B, H, nparts);
+  bwd_da_reduce<<<(unsigned)H, 256, 0, stream>>>(parts, da, B, H, nparts);
   count_launches(1);
   return cudaGetLastError();
 }

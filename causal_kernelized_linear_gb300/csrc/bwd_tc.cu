@@ -21,7 +21,7 @@
 // token row r = TMEM lane r; one thread issues the MMAs and every product is
 // waited for before the rows use it):
 //   1. bt_state:  ΔS_c = K''ᵀV (K'' = w·a^{cs−1−s}φ(k)), Δz_c      → workspace
-//   2. scan:      S_c = exclusive decayed prefix of ΔS               (CUDA cores)
+//   2. scan:      S_c = exclusive decayed prefix of ΔS               (CUDA cores, float4)
 //   3. bt_dq:     recompute o, den; ∂q; den, ρ; ΔM_c = Q''ᵀĜ (Q'' = a^{t+1}φ(q)), ΔN_c
 //   4. scan:      M_c = reverse exclusive decayed suffix of ΔM       (CUDA cores)
 //   5. bt_dkdv:   ∂k, ∂v
@@ -150,6 +150,18 @@ __device__ __forceinline__ void load_tiles(Bt& x, const CUtensorMap* const* maps
         tma_load_3d(x.sm + offs[i] + h * kCb * 128, maps[i], &x.bar[0], h * 64, t0, bh);
   }
   x.tma_pending = true;
+}
+
+// The tiles of the CTA's next item into L2 (no completion to wait for), so
+// that its loads do not start from DRAM.
+template <int D>
+__device__ __forceinline__ void prefetch_next(const CUtensorMap* const* maps, int ntiles,
+                                              int64_t next, const BtParams& p) {
+  if (threadIdx.x != 0 || next >= p.items) return;
+  const int bh = (int)(next / p.nch);
+  const int t0 = (int)(next % p.nch) * kCb;
+  for (int i = 0; i < ntiles; ++i)
+    for (int h = 0; h < D / 64; ++h) tma_prefetch_l2_3d(maps[i], h * 64, t0, bh);
 }
 
 __device__ __forceinline__ bool wait_tiles(Bt& x) {
@@ -291,6 +303,7 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     head_decay(p, bh, a, w);
     __syncthreads();   // the previous item's tiles and tables are no longer read
     load_tiles<D>(x, maps, offs, 2, t0, (int)bh);
+    prefetch_next<D>(maps, 2, item + gridDim.x, p);
     if (bh != last_bh) head_tables(a, w, pw, aw);
     last_bh = bh;
     __syncthreads();
@@ -390,6 +403,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     head_decay(p, bh, a, w);
     __syncthreads();
     load_tiles<D>(x, maps, offs, 4, t0, (int)bh);
+    prefetch_next<D>(maps, 4, item + gridDim.x, p);
     load_state_tile<D>(x.sm + Cfg::oS, p.S + item * (int64_t)(D * D), r);
     if (r < D) zc[r] = p.z[item * D + r];
     if (bh != last_bh) head_tables(a, w, pw, aw);
@@ -695,6 +709,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     head_decay(p, bh, a, w);
     __syncthreads();
     load_tiles<D>(x, maps, offs, 4, t0, (int)bh);
+    prefetch_next<D>(maps, 4, item + gridDim.x, p);
     load_state_tile<D>(x.sm + Cfg::oS, p.M + item * (int64_t)(D * D), r);
     if (r < D) nc[r] = p.N[item * D + r];
     srho[r] = live ? p.rho[bh * p.n + t0 + r] : 0.f;
@@ -866,6 +881,55 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   BtSetup<D>::teardown(x);
 }
 
+// The chunk scans, in place, four consecutive state elements per thread:
+// forward (S, z): out[c] = acc, acc ← a^{cs_c}·acc + ΔS_c (the state entering
+// chunk c); reverse (M, N): walking down, out[c] = acc, acc ← ΔM_c +
+// a^{cs_c}·acc (the adjoint after chunk c).  The next 8 chunks' values are
+// loaded before the current 8 results are stored, so that loads stay in
+// flight.
+__global__ void __launch_bounds__(256)
+bt_chunk_scan(float* __restrict__ S, float* __restrict__ z, int64_t H, int nch, int64_t n, int dpd,
+              int dp, const float* __restrict__ decay, bool reverse) {
+  const int64_t bh = blockIdx.x;
+  const int e4 = (blockIdx.y * 256 + threadIdx.x) * 4;
+  if (e4 >= dpd + dp) return;
+  const float a = decay ? decay[bh % H] : 1.f;
+  const float a_full = decay_pow(a, kCb);
+  float* base = e4 < dpd ? S + bh * nch * (int64_t)dpd + e4 : z + bh * nch * (int64_t)dp + (e4 - dpd);
+  const int64_t stride = e4 < dpd ? dpd : dp;
+  constexpr int kB = 8;
+  auto idx = [&](int i) { return reverse ? nch - 1 - i : i; };   // i-th chunk visited
+  auto fac = [&](int c) {
+    const int64_t len = min((int64_t)kCb, n - (int64_t)c * kCb);
+    return len == kCb ? a_full : decay_pow(a, len);
+  };
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 cur[kB], nxt[kB];
+#pragma unroll
+  for (int j = 0; j < kB; ++j)
+    cur[j] = j < nch ? *reinterpret_cast<const float4*>(base + idx(j) * stride)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = 0; i0 < nch; i0 += kB) {
+#pragma unroll
+    for (int j = 0; j < kB; ++j)
+      nxt[j] = i0 + kB + j < nch ? *reinterpret_cast<const float4*>(base + idx(i0 + kB + j) * stride)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int i = i0 + j;
+      if (i < nch) {
+        const int c = idx(i);
+        *reinterpret_cast<float4*>(base + c * stride) = acc;
+        const float f = fac(c);
+        acc = make_float4(f * acc.x + cur[j].x, f * acc.y + cur[j].y, f * acc.z + cur[j].z,
+                          f * acc.w + cur[j].w);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) cur[j] = nxt[j];
+  }
+}
+
 template <int D>
 cudaError_t run_bt(const BwdArgs& a, float* ws, int num_sms, int* status, cudaStream_t stream) {
   using Cfg = BtCfg<D>;
@@ -914,15 +978,16 @@ cudaError_t run_bt(const BwdArgs& a, float* ws, int num_sms, int* status, cudaSt
   bt_state_kernel<D><<<grid, kThreadsB, smem, stream>>>(mk, mv, p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = backward_scan(p.S, p.z, nullptr, nullptr, BH, a.H, nch, kCb, a.n, D, D, a.decay, false,
-                         stream)) != cudaSuccess)
-    return e;
+  const dim3 sgrid((unsigned)BH, (unsigned)((D * D + D) / 4 + 255) / 256);
+  bt_chunk_scan<<<sgrid, 256, 0, stream>>>(p.S, p.z, a.H, nch, a.n, D * D, D, a.decay, false);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   bt_dq_kernel<D><<<grid, kThreadsB, smem, stream>>>(mq, mk, mv, mg, p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = backward_scan(nullptr, nullptr, p.M, p.N, BH, a.H, nch, kCb, a.n, D, D, a.decay, true,
-                         stream)) != cudaSuccess)
-    return e;
+  bt_chunk_scan<<<sgrid, 256, 0, stream>>>(p.M, p.N, a.H, nch, a.n, D * D, D, a.decay, true);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   bt_dkdv_kernel<D><<<grid, kThreadsB, smem, stream>>>(mq, mk, mv, mg, p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
