@@ -67,6 +67,12 @@ struct BtCfg {
   // CTA (which holds all 512 TMEM columns) runs per SM
   static constexpr int SMEM_ALLOC = (BYTES + 1024 > 118 * 1024) ? BYTES + 1024 : 118 * 1024;
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  // staging areas laid over tiles that are free when they are used: fp32
+  // [D' × (D + 4)] from oQ; bf16 ∂v and ∂k rows of 2D + 16 bytes from oV
+  static_assert((D + 4) * D * 4 <= oG, "fp32 staging over the Q, K and V tiles");
+  static_assert(oV + 2 * kCb * (2 * D + 16) <= oZ, "∂v/∂k staging over the V, G and S tiles");
+  static_assert(oK + kCb * (2 * D + 16) <= oG, "∂q staging over the K and V tiles");
+  static_assert((kThreadsB / (D / 8)) * D * 4 <= STILE, "column-sum scratch in the S tile");
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -202,19 +208,128 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
 }
 
 // A [D' × D] fp32 matrix from global memory into the bf16 operand tile
-// (column blocks of [D' × 64], 128-byte swizzle): thread r < D converts row r.
-template <int D>
-__device__ __forceinline__ void load_state_tile(uint8_t* tile, const float* src, int r) {
-  if (r >= D) return;
+// (column blocks of [D' × 64], 128-byte swizzle).  Consecutive threads take
+// consecutive float4s, so every warp load is one contiguous 512-byte run.
+// With DOT, `other` (same shape) is read alongside and the thread's share of
+// the inner product ⟨src, other⟩ is returned.
+template <int D, bool DOT>
+__device__ __forceinline__ float load_state_tile(uint8_t* tile, const float* __restrict__ src,
+                                                 const float* __restrict__ other) {
+  constexpr int PER = D * D / 4 / kThreadsB;   // float4s per thread: 32 (d 128) or 8 (d 64)
+  constexpr int BATCH = 8;
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+  const float4* o4 = reinterpret_cast<const float4*>(other);
+  float dot = 0.f;
+#pragma unroll 1
+  for (int i0 = 0; i0 < PER; i0 += BATCH) {
+    float4 v[BATCH], u[BATCH];
 #pragma unroll
-  for (int h = 0; h < D / 64; ++h)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float4 a = *reinterpret_cast<const float4*>(src + r * D + h * 64 + j * 8);
-      const float4 b = *reinterpret_cast<const float4*>(src + r * D + h * 64 + j * 8 + 4);
-      const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      *reinterpret_cast<uint4*>(tile + sw_chunk(D, r, h, j)) = pack8(f);
+    for (int i = 0; i < BATCH; ++i) {
+      v[i] = s4[(i0 + i) * kThreadsB + threadIdx.x];
+      if (DOT) u[i] = o4[(i0 + i) * kThreadsB + threadIdx.x];
     }
+#pragma unroll
+    for (int i = 0; i < BATCH; ++i) {
+      const int e = ((i0 + i) * kThreadsB + threadIdx.x) * 4;
+      const int row = e / D, col = e % D;
+      const uint2 b = make_uint2(pack_bf16x2(v[i].x, v[i].y), pack_bf16x2(v[i].z, v[i].w));
+      *reinterpret_cast<uint2*>(tile + sw_chunk(D, row, col >> 6, (col & 63) >> 3) + (col & 7) * 2) = b;
+      if (DOT) dot += v[i].x * u[i].x + v[i].y * u[i].y + v[i].z * u[i].z + v[i].w * u[i].w;
+    }
+  }
+  return dot;
+}
+
+// The fp32 [D' × D] accumulator in TMEM (lane = row, columns col0..col0+D)
+// to a contiguous row-major matrix in global memory.  Rows go through
+// shared memory (`stage`, (D + 4)·D floats; the padding spreads a warp's
+// 16-byte writes over all banks) so that the global stores are coalesced.
+// Every thread of the CTA calls it (it holds a CTA barrier).
+template <int D>
+__device__ __forceinline__ void store_tmem_matrix(uint32_t tmem, uint32_t col0, float* stage,
+                                                  float* __restrict__ dst) {
+  constexpr int SR = D + 4;
+  const int r = threadIdx.x;
+  if (r < D) {
+    const uint32_t lane_base = (uint32_t)(r >> 5) * 32;
+#pragma unroll 1
+    for (int j0 = 0; j0 < D; j0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem_addr(tmem, lane_base, col0 + j0), v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4*>(stage + r * SR + j0 + 4 * q) =
+            make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                        __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+    }
+  }
+  __syncthreads();
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll 8
+  for (int e = threadIdx.x; e < D * D / 4; e += kThreadsB) {
+    const int row = e / (D / 4), c4 = e % (D / 4);
+    d4[e] = *reinterpret_cast<const float4*>(stage + row * SR + c4 * 4);
+  }
+}
+
+// Weighted column sums of a [128 × D] bf16 tile (rows = tokens, 128-byte
+// swizzle): out[i] = Σ_s wt(s)·T[s][i].  Thread t sums the 8 columns of chunk
+// t mod (D/8) over one group of rows, so its loads and adds are independent;
+// the group partials meet in `scratch` (128·8 floats).  Every thread of the
+// CTA calls it (it holds a CTA barrier).
+template <int D, typename Wt>
+__device__ __forceinline__ void tile_colsum(const uint8_t* tile, Wt wt, float* scratch,
+                                            float* __restrict__ out) {
+  constexpr int NCH = D / 8;                 // 16-byte chunks per row
+  constexpr int NG = kThreadsB / NCH;        // row groups
+  constexpr int RPG = kCb / NG;              // rows per group
+  const int ch = threadIdx.x % NCH, grp = threadIdx.x / NCH;
+  const int h = ch >> 3, j = ch & 7;
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int i = 0; i < RPG; ++i) {
+    const int s = grp * RPG + i;
+    float f[8];
+    unpack8(*reinterpret_cast<const uint4*>(tile + sw_chunk(kCb, s, h, j)), f);
+    const float ws = wt(s);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += ws * f[e];
+  }
+  float4* sc = reinterpret_cast<float4*>(scratch + grp * D + ch * 8);
+  sc[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  sc[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float s = 0.f;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) s += scratch[g * D + threadIdx.x];
+    out[threadIdx.x] = s;
+  }
+}
+
+// Stages one bf16 row of 8-element chunks for a coalesced store: row r of a
+// [128 × D] matrix at `stage` with a row stride of 2·D + 16 bytes.
+template <int D>
+__device__ __forceinline__ void stage_chunk(uint8_t* stage, int r, int col, const float (&f)[8]) {
+  *reinterpret_cast<uint4*>(stage + r * (2 * D + 16) + col * 2) = pack8(f);
+}
+
+// The staged rows [0, cs) of a [128 × D] bf16 matrix to global rows
+// dst[0..cs) (row-major, D elements each), 16 bytes per thread and step.
+template <int D>
+__device__ __forceinline__ void store_staged_rows(const uint8_t* stage, __nv_bfloat16* __restrict__ dst,
+                                                  int cs) {
+  constexpr int NCH = D / 8;
+#pragma unroll 4
+  for (int e = threadIdx.x; e < kCb * NCH; e += kThreadsB) {
+    const int row = e / NCH, c = e % NCH;
+    if (row < cs)
+      *reinterpret_cast<uint4*>(dst + (int64_t)row * D + c * 8) =
+          *reinterpret_cast<const uint4*>(stage + row * (2 * D + 16) + c * 16);
+  }
 }
 
 // Per-head tables a^k and k·w·a^{k−1} (k = 0..128).
@@ -289,8 +404,7 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   BtSetup<D>::run(x);
   float* pw = reinterpret_cast<float*>(x.sm + Cfg::oPW);
   float* aw = reinterpret_cast<float*>(x.sm + Cfg::oAW);
-  const int r = threadIdx.x, wq = r >> 5;
-  const uint32_t lane_base = (uint32_t)wq * 32;
+  const int r = threadIdx.x;
   const CUtensorMap* maps[2] = {&map_k, &map_v};
   const int offs[2] = {Cfg::oK, Cfg::oV};
   int64_t last_bh = -1;
@@ -334,34 +448,15 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         mma_ss(x.tmem, desc_at(dA, k * 2048), desc_at(dB, k * 2048), id, k > 0);
     }
     commit_mma(x);
-    // Δz on the CUDA cores meanwhile (thread i sums feature column i of K'')
-    if (r < D) {
-      const uint8_t* kt = x.sm + Cfg::oK;
-      const int h = r >> 6, j = (r & 63) >> 3, e = r & 7;
-      float acc = 0.f;
-      for (int s = 0; s < cs; ++s) {
-        const uint4 u = *reinterpret_cast<const uint4*>(kt + sw_chunk(kCb, s, h, j));
-        float f[8];
-        unpack8(u, f);
-        acc += f[e];
-      }
-      p.z[item * D + r] = acc;
-    }
+    // Δz on the CUDA cores meanwhile (rows ≥ cs of K'' are zero)
+    tile_colsum<D>(x.sm + Cfg::oK, [](int) { return 1.f; },
+                   reinterpret_cast<float*>(x.sm + Cfg::oS), p.z + item * D);
     if (!wait_mma(x)) break;
-    if (r < D) {
-#pragma unroll 1
-      for (int j0 = 0; j0 < D; j0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem_addr(x.tmem, lane_base, j0), v);
-        tmem_ld_wait();
-        float4* dst = reinterpret_cast<float4*>(p.S + (item * D + r) * (int64_t)D + j0);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-      }
-    }
+    // ΔS through the free Q/K/V tiles
+    store_tmem_matrix<D>(x.tmem, 0, reinterpret_cast<float*>(x.sm + Cfg::oQ),
+                         p.S + item * (int64_t)(D * D));
     tc_fence_before();
+    fence_proxy_async_smem();   // generic accesses before the next item's TMA writes
   }
   BtSetup<D>::teardown(x);
 }
@@ -404,7 +499,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     __syncthreads();
     load_tiles<D>(x, maps, offs, 4, t0, (int)bh);
     prefetch_next<D>(maps, 4, item + gridDim.x, p);
-    load_state_tile<D>(x.sm + Cfg::oS, p.S + item * (int64_t)(D * D), r);
+    load_state_tile<D, false>(x.sm + Cfg::oS, p.S + item * (int64_t)(D * D), nullptr);
     if (r < D) zc[r] = p.z[item * D + r];
     if (bh != last_bh) head_tables(a, w, pw, aw);
     last_bh = bh;
@@ -591,38 +686,31 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         mma_ts(x.tmem + RY, x.tmem + RP + k * 8, desc_at(dKm, k * 2048), idN, 1);
     }
     commit_mma(x);
-    // ΔN_i = Σ_t a^{t+1} ρ_t q'_ti meanwhile (thread i: feature column i)
-    if (r < D) {
-      const int h = r >> 6, j = (r & 63) >> 3, e = r & 7;
-      float acc = 0.f;
-      for (int t = 0; t < cs; ++t) {
-        float f[8];
-        unpack8(*reinterpret_cast<const uint4*>(qt + sw_chunk(kCb, t, h, j)), f);
-        acc += pw[t + 1] * srho[t] * f[e];
-      }
-      p.N[item * D + r] = acc;
-    }
+    // ΔN_i = Σ_t a^{t+1} ρ_t q'_ti meanwhile (rows ≥ cs of Q' and ρ are zero;
+    // the S_c tile is free since Ĝ·S_cᵀ completed)
+    tile_colsum<D>(qt, [&](int t) { return pw[t + 1] * srho[t]; },
+                   reinterpret_cast<float*>(x.sm + Cfg::oS), p.N + item * D);
     if (!wait_mma(x)) break;
-    // ---- rows 4: ∂q = ∂q' ⊙ min(φ(q), 1), then Q'' = a^{t+1}φ(q) in place
-    {
-      __nv_bfloat16* dst = p.dq + (bh * p.n + t0 + (live ? r : 0)) * D;
+    // ---- rows 4: ∂q = ∂q' ⊙ min(φ(q), 1), staged in the free K/V tiles; then
+    // Q'' = a^{t+1}φ(q) in place
+    uint8_t* dq_stage = x.sm + Cfg::oK;
 #pragma unroll 1
-      for (int j0 = 0; j0 < D; j0 += 32) {
-        uint32_t dv[32];
-        tmem_ld32(tmem_addr(x.tmem, lane_base, RY + j0), dv);
-        tmem_ld_wait();
+    for (int j0 = 0; j0 < D; j0 += 32) {
+      uint32_t dv[32];
+      tmem_ld32(tmem_addr(x.tmem, lane_base, RY + j0), dv);
+      tmem_ld_wait();
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          const int h = (j0 + q8 * 8) >> 6, j = ((j0 + q8 * 8) & 63) >> 3;
-          float f[8];
-          unpack8(*reinterpret_cast<const uint4*>(qt + sw_chunk(kCb, r, h, j)), f);
+      for (int q8 = 0; q8 < 4; ++q8) {
+        const int h = (j0 + q8 * 8) >> 6, j = ((j0 + q8 * 8) & 63) >> 3;
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4*>(qt + sw_chunk(kCb, r, h, j)), f);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(dv[q8 * 8 + e]) * fminf(f[e], 1.f);
-          if (live) *reinterpret_cast<uint4*>(dst + j0 + q8 * 8) = pack8(f);
-        }
+        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(dv[q8 * 8 + e]) * fminf(f[e], 1.f);
+        stage_chunk<D>(dq_stage, r, j0 + q8 * 8, f);
       }
     }
     __syncthreads();   // every row's φ(q) has been read (ΔN, ∂q) before it is scaled
+    store_staged_rows<D>(dq_stage, p.dq + (bh * p.n + t0) * D, cs);
     {
       const uint32_t s2 = splat_bf16x2(pw[r + 1]);
 #pragma unroll
@@ -648,20 +736,11 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     }
     commit_mma(x);
     if (!wait_mma(x)) break;
-    if (r < D) {
-#pragma unroll 1
-      for (int j0 = 0; j0 < D; j0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem_addr(x.tmem, lane_base, RN + j0), v);
-        tmem_ld_wait();
-        float4* dst = reinterpret_cast<float4*>(p.M + (item * D + r) * (int64_t)D + j0);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-      }
-    }
+    // ΔM through the free Q/K/V tiles
+    store_tmem_matrix<D>(x.tmem, RN, reinterpret_cast<float*>(x.sm + Cfg::oQ),
+                         p.M + item * (int64_t)(D * D));
     tc_fence_before();
+    fence_proxy_async_smem();   // generic accesses before the next item's TMA writes
     if (p.want_da) {
       const float s = cta_sum(da, red);
       if (threadIdx.x == 0) p.dapart[bh * 2 * p.nch + c] = s;
@@ -710,26 +789,24 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     __syncthreads();
     load_tiles<D>(x, maps, offs, 4, t0, (int)bh);
     prefetch_next<D>(maps, 4, item + gridDim.x, p);
-    load_state_tile<D>(x.sm + Cfg::oS, p.M + item * (int64_t)(D * D), r);
+    // M_c into the operand tile; with ∂a, the share of the pairs across the
+    // chunk, cs·a^{cs−1}(⟨S_c, M_c⟩ + ⟨z_c, N_c⟩), from the same loads
+    float da = 0.f;
+    {
+      const float* Mc = p.M + item * (int64_t)(D * D);
+      if (p.want_da) {
+        float acc = load_state_tile<D, true>(x.sm + Cfg::oS, Mc, p.S + item * (int64_t)(D * D));
+        if (r < D) acc += p.z[item * D + r] * p.N[item * D + r];
+        da = (float)cs * decay_pow(a, cs - 1) * acc;
+      } else {
+        load_state_tile<D, false>(x.sm + Cfg::oS, Mc, nullptr);
+      }
+    }
     if (r < D) nc[r] = p.N[item * D + r];
     srho[r] = live ? p.rho[bh * p.n + t0 + r] : 0.f;
     sden[r] = live ? p.den[bh * p.n + t0 + r] : 1.f;
     if (bh != last_bh) head_tables(a, w, pw, aw);
     last_bh = bh;
-    // ∂a share of the pairs across the chunk: cs·a^{cs−1}(⟨S_c, M_c⟩ + ⟨z_c, N_c⟩)
-    float da = 0.f;
-    if (p.want_da) {
-      const float* Sc = p.S + item * (int64_t)(D * D);
-      const float* Mc = p.M + item * (int64_t)(D * D);
-      float acc = 0.f;
-      for (int e = threadIdx.x * 4; e < D * D; e += kThreadsB * 4) {
-        const float4 s4 = *reinterpret_cast<const float4*>(Sc + e);
-        const float4 m4 = *reinterpret_cast<const float4*>(Mc + e);
-        acc += s4.x * m4.x + s4.y * m4.y + s4.z * m4.z + s4.w * m4.w;
-      }
-      if (r < D) acc += p.z[item * D + r] * p.N[item * D + r];
-      da = (float)cs * decay_pow(a, cs - 1) * acc;
-    }
     __syncthreads();
     if (!wait_tiles(x)) break;
     phi_row_inplace<D>(x.sm + Cfg::oQ, r, live);
@@ -833,11 +910,12 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     // ---- rows 2: ∂v_s = (PᵀĜ)_s + w·a^{cs−1−s}(K'M)_s;
     // ∂k'_s = (EᵀQ')_s + w·a^{cs−1−s}((VMᵀ)_s + N); ∂a share (t1 − s)·w·a^{t1−s−1}·k'_s·((VMᵀ)_s + N).
     // The TMEM loads are warp-collective, so every row takes part; only the
-    // stores are limited to the valid rows.
+    // valid rows are stored.  ∂v and ∂k are staged in the free V/G/S tiles
+    // (the K tile is still read here) and stored coalesced.
+    uint8_t* dv_stage = x.sm + Cfg::oV;
+    uint8_t* dk_stage = x.sm + Cfg::oV + kCb * (2 * D + 16);
     {
       const float fut = live ? w * pw[cs - 1 - r] : 0.f;
-      __nv_bfloat16* dvr = p.dv + (bh * p.n + t0 + (live ? r : 0)) * D;
-      __nv_bfloat16* dkr = p.dk + (bh * p.n + t0 + (live ? r : 0)) * D;
       float kfut = 0.f;
 #pragma unroll 1
       for (int j0 = 0; j0 < D; j0 += 32) {
@@ -851,7 +929,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             f[e] = __uint_as_float(va[q8 * 8 + e]) + fut * __uint_as_float(vb[q8 * 8 + e]);
-          if (live) *reinterpret_cast<uint4*>(dvr + j0 + q8 * 8) = pack8(f);
+          stage_chunk<D>(dv_stage, r, j0 + q8 * 8, f);
         }
         tmem_ld32(tmem_addr(x.tmem, lane_base, RK + j0), va);
         tmem_ld32(tmem_addr(x.tmem, lane_base, RF + j0), vb);
@@ -867,12 +945,16 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
             kfut += kf[e] * m;
             f[e] = (__uint_as_float(va[q8 * 8 + e]) + fut * m) * fminf(kf[e], 1.f);
           }
-          if (live) *reinterpret_cast<uint4*>(dkr + j0 + q8 * 8) = pack8(f);
+          stage_chunk<D>(dk_stage, r, j0 + q8 * 8, f);
         }
       }
       if (live) da += aw[cs - 1 - r] * kfut;
     }
     tc_fence_before();
+    __syncthreads();
+    store_staged_rows<D>(dv_stage, p.dv + (bh * p.n + t0) * D, cs);
+    store_staged_rows<D>(dk_stage, p.dk + (bh * p.n + t0) * D, cs);
+    fence_proxy_async_smem();   // generic accesses before the next item's TMA writes
     if (p.want_da) {
       const float s = cta_sum(da, red);
       if (threadIdx.x == 0) p.dapart[bh * 2 * p.nch + p.nch + c] = s;
