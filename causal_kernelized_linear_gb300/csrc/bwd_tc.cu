@@ -21,11 +21,15 @@
 // token row r = TMEM lane r; one thread issues the MMAs and every product is
 // waited for before the rows use it):
 //   1. bt_state:  ΔS_c = K''ᵀV (K'' = w·a^{cs−1−s}φ(k)), Δz_c      → workspace
-//   2. scan:      S_c = exclusive decayed prefix of ΔS               (CUDA cores, float4)
+//   2. scan:      S_c = exclusive decayed prefix of ΔS, in fp32 and as the
+//                 bf16 operand tile of pass 3                        (CUDA cores, float4)
 //   3. bt_dq:     recompute o, den; ∂q; den, ρ; ΔM_c = Q''ᵀĜ (Q'' = a^{t+1}φ(q)), ΔN_c
-//   4. scan:      M_c = reverse exclusive decayed suffix of ΔM       (CUDA cores)
+//   4. scan:      M_c = reverse exclusive decayed suffix of ΔM, as the bf16
+//                 operand tile of pass 5; the ∂a share across each chunk
 //   5. bt_dkdv:   ∂k, ∂v
 //   6. ∂a:        sum of the per-chunk shares                       (CUDA cores)
+// The [128 × D] tiles arrive by TMA (tensor maps over the [B·H, n, D] rows) and
+// the operand tiles of S_c and M_c by bulk copies, on one barrier per item.
 // Every wait is bounded in time; on expiry the kernel records LA_ERR_TIMEOUT
 // in the device status word and stops.
 #include "common.cuh"
@@ -91,9 +95,13 @@ struct BtParams {
   float* z;             // [BH][nch][D]
   float* M;             // [BH][nch][D*D]: ΔM_c, then M_c
   float* N;             // [BH][nch][D]
+  const __nv_bfloat16* St;   // [BH][nch] bf16 operand tiles of S_c
+  const __nv_bfloat16* Mt;   // [BH][nch] bf16 operand tiles of M_c
   float* den;           // [BH][n]
   float* rho;           // [BH][n]
-  float* dapart;        // [BH][2·nch]: ∂q pass shares, then ∂k/∂v pass shares
+  float* dapart;        // [BH][da_parts]: the ∂q pass shares (one per chunk), the
+                        // ∂k/∂v pass shares, then the reverse scan's warp shares
+  int da_parts;
   bool want_da;
   int* status;
 };
@@ -145,15 +153,29 @@ __device__ __forceinline__ void rows_to_mma() {
   tc_fence_after();
 }
 
+// Contiguous global → shared copy on the TMA barrier (both addresses 16-byte
+// aligned, bytes a multiple of 16); the caller has added the bytes to the
+// barrier's expected transaction count.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// The item's [128 × D] tiles, plus (when `state` is given) its bf16 [D' × D]
+// operand tile, all on the TMA barrier.
 template <int D>
-__device__ __forceinline__ void load_tiles(Bt& x, const CUtensorMap* const* maps, const int* offs,
-                                           int ntiles, int t0, int bh) {
+__device__ __forceinline__ void load_item(Bt& x, const CUtensorMap* const* maps, const int* offs,
+                                          int ntiles, int t0, int bh, const __nv_bfloat16* state) {
   using Cfg = BtCfg<D>;
   if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&x.bar[0], ntiles * Cfg::TILE);
+    mbar_arrive_expect_tx(&x.bar[0], ntiles * Cfg::TILE + (state ? Cfg::STILE : 0));
     for (int i = 0; i < ntiles; ++i)
       for (int h = 0; h < Cfg::HALVES; ++h)
         tma_load_3d(x.sm + offs[i] + h * kCb * 128, maps[i], &x.bar[0], h * 64, t0, bh);
+    if (state) bulk_load(x.sm + Cfg::oS, state, Cfg::STILE, &x.bar[0]);
   }
   x.tma_pending = true;
 }
@@ -205,39 +227,6 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
   f[2] = bf16lo_to_f32(u.y); f[3] = bf16hi_to_f32(u.y);
   f[4] = bf16lo_to_f32(u.z); f[5] = bf16hi_to_f32(u.z);
   f[6] = bf16lo_to_f32(u.w); f[7] = bf16hi_to_f32(u.w);
-}
-
-// A [D' × D] fp32 matrix from global memory into the bf16 operand tile
-// (column blocks of [D' × 64], 128-byte swizzle).  Consecutive threads take
-// consecutive float4s, so every warp load is one contiguous 512-byte run.
-// With DOT, `other` (same shape) is read alongside and the thread's share of
-// the inner product ⟨src, other⟩ is returned.
-template <int D, bool DOT>
-__device__ __forceinline__ float load_state_tile(uint8_t* tile, const float* __restrict__ src,
-                                                 const float* __restrict__ other) {
-  constexpr int PER = D * D / 4 / kThreadsB;   // float4s per thread: 32 (d 128) or 8 (d 64)
-  constexpr int BATCH = 8;
-  const float4* s4 = reinterpret_cast<const float4*>(src);
-  const float4* o4 = reinterpret_cast<const float4*>(other);
-  float dot = 0.f;
-#pragma unroll 1
-  for (int i0 = 0; i0 < PER; i0 += BATCH) {
-    float4 v[BATCH], u[BATCH];
-#pragma unroll
-    for (int i = 0; i < BATCH; ++i) {
-      v[i] = s4[(i0 + i) * kThreadsB + threadIdx.x];
-      if (DOT) u[i] = o4[(i0 + i) * kThreadsB + threadIdx.x];
-    }
-#pragma unroll
-    for (int i = 0; i < BATCH; ++i) {
-      const int e = ((i0 + i) * kThreadsB + threadIdx.x) * 4;
-      const int row = e / D, col = e % D;
-      const uint2 b = make_uint2(pack_bf16x2(v[i].x, v[i].y), pack_bf16x2(v[i].z, v[i].w));
-      *reinterpret_cast<uint2*>(tile + sw_chunk(D, row, col >> 6, (col & 63) >> 3) + (col & 7) * 2) = b;
-      if (DOT) dot += v[i].x * u[i].x + v[i].y * u[i].y + v[i].z * u[i].z + v[i].w * u[i].w;
-    }
-  }
-  return dot;
 }
 
 // The fp32 [D' × D] accumulator in TMEM (lane = row, columns col0..col0+D)
@@ -416,7 +405,7 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     float a, w;
     head_decay(p, bh, a, w);
     __syncthreads();   // the previous item's tiles and tables are no longer read
-    load_tiles<D>(x, maps, offs, 2, t0, (int)bh);
+    load_item<D>(x, maps, offs, 2, t0, (int)bh, nullptr);
     prefetch_next<D>(maps, 2, item + gridDim.x, p);
     if (bh != last_bh) head_tables(a, w, pw, aw);
     last_bh = bh;
@@ -497,9 +486,8 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     float a, w;
     head_decay(p, bh, a, w);
     __syncthreads();
-    load_tiles<D>(x, maps, offs, 4, t0, (int)bh);
+    load_item<D>(x, maps, offs, 4, t0, (int)bh, p.St + item * (int64_t)(D * D));
     prefetch_next<D>(maps, 4, item + gridDim.x, p);
-    load_state_tile<D, false>(x.sm + Cfg::oS, p.S + item * (int64_t)(D * D), nullptr);
     if (r < D) zc[r] = p.z[item * D + r];
     if (bh != last_bh) head_tables(a, w, pw, aw);
     last_bh = bh;
@@ -743,7 +731,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     fence_proxy_async_smem();   // generic accesses before the next item's TMA writes
     if (p.want_da) {
       const float s = cta_sum(da, red);
-      if (threadIdx.x == 0) p.dapart[bh * 2 * p.nch + c] = s;
+      if (threadIdx.x == 0) p.dapart[bh * p.da_parts + c] = s;
     }
   }
   BtSetup<D>::teardown(x);
@@ -787,21 +775,10 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     float a, w;
     head_decay(p, bh, a, w);
     __syncthreads();
-    load_tiles<D>(x, maps, offs, 4, t0, (int)bh);
+    load_item<D>(x, maps, offs, 4, t0, (int)bh, p.Mt + item * (int64_t)(D * D));
     prefetch_next<D>(maps, 4, item + gridDim.x, p);
-    // M_c into the operand tile; with ∂a, the share of the pairs across the
-    // chunk, cs·a^{cs−1}(⟨S_c, M_c⟩ + ⟨z_c, N_c⟩), from the same loads
+    // (the share of the pairs across the chunk comes from the reverse scan)
     float da = 0.f;
-    {
-      const float* Mc = p.M + item * (int64_t)(D * D);
-      if (p.want_da) {
-        float acc = load_state_tile<D, true>(x.sm + Cfg::oS, Mc, p.S + item * (int64_t)(D * D));
-        if (r < D) acc += p.z[item * D + r] * p.N[item * D + r];
-        da = (float)cs * decay_pow(a, cs - 1) * acc;
-      } else {
-        load_state_tile<D, false>(x.sm + Cfg::oS, Mc, nullptr);
-      }
-    }
     if (r < D) nc[r] = p.N[item * D + r];
     srho[r] = live ? p.rho[bh * p.n + t0 + r] : 0.f;
     sden[r] = live ? p.den[bh * p.n + t0 + r] : 1.f;
@@ -957,58 +934,106 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     fence_proxy_async_smem();   // generic accesses before the next item's TMA writes
     if (p.want_da) {
       const float s = cta_sum(da, red);
-      if (threadIdx.x == 0) p.dapart[bh * 2 * p.nch + p.nch + c] = s;
+      if (threadIdx.x == 0) p.dapart[bh * p.da_parts + p.nch + c] = s;
     }
   }
   BtSetup<D>::teardown(x);
 }
 
-// The chunk scans, in place, four consecutive state elements per thread:
-// forward (S, z): out[c] = acc, acc ← a^{cs_c}·acc + ΔS_c (the state entering
-// chunk c); reverse (M, N): walking down, out[c] = acc, acc ← ΔM_c +
-// a^{cs_c}·acc (the adjoint after chunk c).  The next 8 chunks' values are
-// loaded before the current 8 results are stored, so that loads stay in
-// flight.
-__global__ void __launch_bounds__(256)
-bt_chunk_scan(float* __restrict__ S, float* __restrict__ z, int64_t H, int nch, int64_t n, int dpd,
-              int dp, const float* __restrict__ decay, bool reverse) {
+// The chunk scans, four consecutive state elements per thread (the matrix
+// part [D' × D], then the vector part [D']):
+//   forward (S, z): out[c] = acc, acc ← a^{cs_c}·acc + ΔS_c — the state
+//     entering chunk c, written in place in fp32 and, for the matrix part,
+//     as the bf16 operand tile of the ∂q pass;
+//   reverse (M, N): walking down, out[c] = acc, acc ← ΔM_c + a^{cs_c}·acc —
+//     the adjoint after chunk c; the matrix part goes only to its bf16
+//     operand tile (for the ∂k/∂v pass), the vector part N_c stays fp32 in
+//     place.  With ∂a, every thread also sums its part of the pairs across
+//     the chunks, Σ_c cs_c·a^{cs_c−1}(⟨S_c, M_c⟩ + ⟨z_c, N_c⟩), from the fp32
+//     S_c and z_c of the forward scan; each warp stores one total in da_out.
+// The operand tile is [D' × 64]-column blocks with the 128-byte swizzle, the
+// layout the tensor-core passes copy into shared memory as is.  The next
+// chunks' values are loaded before the current results are stored, so that
+// loads stay in flight.
+template <int D, bool REV>
+__global__ void __launch_bounds__(256, 2)
+bt_chunk_scan(float* __restrict__ S, float* __restrict__ z, __nv_bfloat16* __restrict__ tiles,
+              const float* __restrict__ fS, const float* __restrict__ fz, float* __restrict__ da_out,
+              int da_parts, int64_t H, int nch, int64_t n, const float* __restrict__ decay) {
+  constexpr int DPD = D * D;
   const int64_t bh = blockIdx.x;
   const int e4 = (blockIdx.y * 256 + threadIdx.x) * 4;
-  if (e4 >= dpd + dp) return;
+  const bool valid = e4 < DPD + D;              // whole warps are valid or not, except for d = 64
+  const bool mat = e4 < DPD;
   const float a = decay ? decay[bh % H] : 1.f;
   const float a_full = decay_pow(a, kCb);
-  float* base = e4 < dpd ? S + bh * nch * (int64_t)dpd + e4 : z + bh * nch * (int64_t)dp + (e4 - dpd);
-  const int64_t stride = e4 < dpd ? dpd : dp;
-  constexpr int kB = 8;
-  auto idx = [&](int i) { return reverse ? nch - 1 - i : i; };   // i-th chunk visited
+  const int64_t off = mat ? bh * nch * (int64_t)DPD + e4 : bh * nch * (int64_t)D + (e4 - DPD);
+  float* base = (mat ? S : z) + off;
+  const float* fbase = (REV && da_out) ? (mat ? fS : fz) + off : nullptr;
+  const int64_t stride = mat ? DPD : D;
+  // byte offset of this thread's four elements inside an operand tile
+  const int row = e4 / D, col = e4 % D;
+  const uint32_t toff = mat ? sw_chunk(D, row, col >> 6, (col & 63) >> 3) + (col & 7) * 2 : 0u;
+  uint8_t* tbase = reinterpret_cast<uint8_t*>(tiles + bh * nch * (int64_t)DPD) + toff;
+  const int slot = blockIdx.y * 8 + (threadIdx.x >> 5);
+  constexpr int kB = REV ? 4 : 8;   // chunks in flight (the reverse scan loads two streams)
+  auto idx = [&](int i) { return REV ? nch - 1 - i : i; };   // i-th chunk visited
+  auto clen = [&](int c) { return (int)min((int64_t)kCb, n - (int64_t)c * kCb); };
   auto fac = [&](int c) {
-    const int64_t len = min((int64_t)kCb, n - (int64_t)c * kCb);
+    const int len = clen(c);
     return len == kCb ? a_full : decay_pow(a, len);
   };
+  auto ld = [&](const float* b, int i) {
+    return (valid && i < nch) ? *reinterpret_cast<const float4*>(b + idx(i) * stride)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  const float wfull = (float)kCb * decay_pow(a, kCb - 1);
+  float da_acc = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 cur[kB], nxt[kB];
+  float4 cur[kB], nxt[kB], fcur[kB], fnxt[kB];
 #pragma unroll
-  for (int j = 0; j < kB; ++j)
-    cur[j] = j < nch ? *reinterpret_cast<const float4*>(base + idx(j) * stride)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < kB; ++j) {
+    cur[j] = ld(base, j);
+    if (fbase) fcur[j] = ld(fbase, j);
+  }
   for (int i0 = 0; i0 < nch; i0 += kB) {
 #pragma unroll
-    for (int j = 0; j < kB; ++j)
-      nxt[j] = i0 + kB + j < nch ? *reinterpret_cast<const float4*>(base + idx(i0 + kB + j) * stride)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < kB; ++j) {
+      nxt[j] = ld(base, i0 + kB + j);
+      if (fbase) fnxt[j] = ld(fbase, i0 + kB + j);
+    }
 #pragma unroll
     for (int j = 0; j < kB; ++j) {
       const int i = i0 + j;
       if (i < nch) {
         const int c = idx(i);
-        *reinterpret_cast<float4*>(base + c * stride) = acc;
+        if (valid) {
+          if (!REV || !mat) *reinterpret_cast<float4*>(base + c * stride) = acc;
+          if (mat)
+            *reinterpret_cast<uint2*>(tbase + c * (int64_t)DPD * 2) =
+                make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+        }
+        if (fbase) {
+          const int len = clen(c);
+          const float w_c = len == kCb ? wfull : (float)len * decay_pow(a, len - 1);
+          da_acc += w_c * (acc.x * fcur[j].x + acc.y * fcur[j].y + acc.z * fcur[j].z +
+                           acc.w * fcur[j].w);
+        }
         const float f = fac(c);
         acc = make_float4(f * acc.x + cur[j].x, f * acc.y + cur[j].y, f * acc.z + cur[j].z,
                           f * acc.w + cur[j].w);
       }
     }
 #pragma unroll
-    for (int j = 0; j < kB; ++j) cur[j] = nxt[j];
+    for (int j = 0; j < kB; ++j) {
+      cur[j] = nxt[j];
+      if (fbase) fcur[j] = fnxt[j];
+    }
+  }
+  if (fbase) {   // warp-uniform: every lane takes part
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) da_acc += __shfl_xor_sync(0xffffffffu, da_acc, o);
+    if ((threadIdx.x & 31) == 0) da_out[bh * (int64_t)da_parts + slot] = da_acc;
   }
 }
 
@@ -1033,14 +1058,20 @@ cudaError_t run_bt(const BwdArgs& a, float* ws, int num_sms, int* status, cudaSt
   p.want_da = a.da != nullptr;
   p.status = status;
   const size_t ns = (size_t)BH * nch;
+  const dim3 sgrid((unsigned)BH, (unsigned)((D * D + D) / 4 + 255) / 256);
   float* cur = ws;
   p.S = cur; cur += ns * D * D;
   p.z = cur; cur += ns * D;
   p.M = cur; cur += ns * D * D;
   p.N = cur; cur += ns * D;
+  __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(cur); cur += ns * D * D / 2;
+  __nv_bfloat16* mt = reinterpret_cast<__nv_bfloat16*>(cur); cur += ns * D * D / 2;
+  p.St = st;
+  p.Mt = mt;
   p.den = cur; cur += (size_t)BH * a.n;
   p.rho = cur; cur += (size_t)BH * a.n;
   p.dapart = cur;
+  p.da_parts = 2 * nch + (int)sgrid.y * 8;
   CUtensorMap mq, mk, mv, mg;
   if ((e = tmap_rows(&mq, a.q, BH, a.n, D, kCb)) != cudaSuccess) return e;
   if ((e = tmap_rows(&mk, a.k, BH, a.n, D, kCb)) != cudaSuccess) return e;
@@ -1060,20 +1091,22 @@ cudaError_t run_bt(const BwdArgs& a, float* ws, int num_sms, int* status, cudaSt
   bt_state_kernel<D><<<grid, kThreadsB, smem, stream>>>(mk, mv, p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const dim3 sgrid((unsigned)BH, (unsigned)((D * D + D) / 4 + 255) / 256);
-  bt_chunk_scan<<<sgrid, 256, 0, stream>>>(p.S, p.z, a.H, nch, a.n, D * D, D, a.decay, false);
+  bt_chunk_scan<D, false><<<sgrid, 256, 0, stream>>>(p.S, p.z, st, nullptr, nullptr, nullptr, 0, a.H,
+                                                     nch, a.n, a.decay);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   bt_dq_kernel<D><<<grid, kThreadsB, smem, stream>>>(mq, mk, mv, mg, p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bt_chunk_scan<<<sgrid, 256, 0, stream>>>(p.M, p.N, a.H, nch, a.n, D * D, D, a.decay, true);
+  bt_chunk_scan<D, true><<<sgrid, 256, 0, stream>>>(p.M, p.N, mt, p.S, p.z,
+                                                    p.want_da ? p.dapart + 2 * nch : nullptr, p.da_parts,
+                                                    a.H, nch, a.n, a.decay);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   bt_dkdv_kernel<D><<<grid, kThreadsB, smem, stream>>>(mq, mk, mv, mg, p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (p.want_da) return backward_da_reduce(p.dapart, a.da, a.B, a.H, 2 * nch, stream);
+  if (p.want_da) return backward_da_reduce(p.dapart, a.da, a.B, a.H, p.da_parts, stream);
   return cudaSuccess;
 }
 
@@ -1087,7 +1120,8 @@ size_t tc_backward_ws_floats(const BwdArgs& a) {
   const size_t BH = (size_t)(a.B * a.H);
   const size_t nch = (size_t)((a.n + kCb - 1) / kCb);
   const size_t D = (size_t)a.d;
-  return BH * nch * 2 * (D * D + D) + 2 * BH * (size_t)a.n + 2 * BH * nch;
+  const size_t scan_warps = 8 * (((D * D + D) / 4 + 255) / 256);
+  return BH * nch * (3 * D * D + 2 * D) + 2 * BH * (size_t)a.n + BH * (2 * nch + scan_warps);
 }
 
 cudaError_t tc_backward(const BwdArgs& a, float* ws, int num_sms, int* status,
