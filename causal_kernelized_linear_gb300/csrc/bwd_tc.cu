@@ -58,7 +58,13 @@ struct BtCfg {
   static constexpr int oV = oK + TILE;
   static constexpr int oG = oV + TILE;
   static constexpr int oS = oG + TILE;
-  static constexpr int oZ = oS + STILE;          // fp32 [D]: z_c or N_c
+  // staging for coalesced stores, apart from the tiles (which the next item's
+  // loads may already be filling): half an fp32 [D' × D] matrix with rows
+  // padded to D/2 + 4, or a bf16 [128 × D] matrix with rows padded to 2D + 16 bytes
+  static constexpr int oST = oS + STILE;
+  static constexpr int STG_F32 = (D / 2 + 4) * D * 4;
+  static constexpr int STG_BF16 = kCb * (2 * D + 16);
+  static constexpr int oZ = oST + (STG_F32 > STG_BF16 ? STG_F32 : STG_BF16);   // fp32 [D]: z_c or N_c
   static constexpr int oRHO = oZ + D * 4;        // fp32 [128]
   static constexpr int oDEN = oRHO + kCb * 4;    // fp32 [128]
   static constexpr int oPW = oDEN + kCb * 4;     // fp32 a^k, k = 0..128
@@ -71,12 +77,8 @@ struct BtCfg {
   // CTA (which holds all 512 TMEM columns) runs per SM
   static constexpr int SMEM_ALLOC = (BYTES + 1024 > 118 * 1024) ? BYTES + 1024 : 118 * 1024;
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-  // staging areas laid over tiles that are free when they are used: fp32
-  // [D' × (D + 4)] from oQ; bf16 ∂v and ∂k rows of 2D + 16 bytes from oV
-  static_assert((D + 4) * D * 4 <= oG, "fp32 staging over the Q, K and V tiles");
-  static_assert(oV + 2 * kCb * (2 * D + 16) <= oZ, "∂v/∂k staging over the V, G and S tiles");
-  static_assert(oK + kCb * (2 * D + 16) <= oG, "∂q staging over the K and V tiles");
   static_assert((kThreadsB / (D / 8)) * D * 4 <= STILE, "column-sum scratch in the S tile");
+  static_assert(oZ % 16 == 0, "bulk-copy destination alignment");
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -164,20 +166,24 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// The item's [128 × D] tiles, plus (when `state` is given) its bf16 [D' × D]
-// operand tile, all on the TMA barrier.
-template <int D>
-__device__ __forceinline__ void load_item(Bt& x, const CUtensorMap* const* maps, const int* offs,
-                                          int ntiles, int t0, int bh, const __nv_bfloat16* state) {
-  using Cfg = BtCfg<D>;
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&x.bar[0], ntiles * Cfg::TILE + (state ? Cfg::STILE : 0));
-    for (int i = 0; i < ntiles; ++i)
-      for (int h = 0; h < Cfg::HALVES; ++h)
-        tma_load_3d(x.sm + offs[i] + h * kCb * 128, maps[i], &x.bar[0], h * 64, t0, bh);
-    if (state) bulk_load(x.sm + Cfg::oS, state, Cfg::STILE, &x.bar[0]);
-  }
+// Thread 0 arms the TMA barrier for the next `bytes` of copies (issued
+// before or after this call's copies complete, within the same phase).
+__device__ __forceinline__ void arm_tiles(Bt& x, uint32_t bytes) {
+  if (threadIdx.x == 0) mbar_arrive_expect_tx(&x.bar[0], bytes);
   x.tma_pending = true;
+}
+
+// Thread 0 loads the [128 × D] rows t0.. of head bh into the tile at `off`.
+template <int D>
+__device__ __forceinline__ void tile_load(Bt& x, const CUtensorMap* map, int off, int t0, int bh) {
+  if (threadIdx.x == 0)
+    for (int h = 0; h < D / 64; ++h)
+      tma_load_3d(x.sm + off + h * kCb * 128, map, &x.bar[0], h * 64, t0, bh);
+}
+
+// Thread 0 copies `bytes` contiguous bytes to shared memory at `off`.
+__device__ __forceinline__ void bulk_to(Bt& x, int off, const void* src, uint32_t bytes) {
+  if (threadIdx.x == 0) bulk_load(x.sm + off, src, bytes, &x.bar[0]);
 }
 
 // The tiles of the CTA's next item into L2 (no completion to wait for), so
@@ -202,23 +208,29 @@ __device__ __forceinline__ bool wait_tiles(Bt& x) {
   return all;
 }
 
+// Applies f to every 16-byte chunk (8 bf16) of row r of a [128 × D] tile
+// (128-byte swizzle), in place.  The whole row is loaded before anything is
+// stored, so the loads are not held back behind the stores of the same row.
+template <int D, typename F>
+__device__ __forceinline__ void row_map(uint8_t* tile, int r, F f) {
+  constexpr int NC = D / 8;
+  uint4 u[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) u[c] = *reinterpret_cast<const uint4*>(tile + sw_chunk(kCb, r, c >> 3, c & 7));
+#pragma unroll
+  for (int c = 0; c < NC; ++c) u[c] = f(u[c]);
+#pragma unroll
+  for (int c = 0; c < NC; ++c) *reinterpret_cast<uint4*>(tile + sw_chunk(kCb, r, c >> 3, c & 7)) = u[c];
+}
+
 // φ = elu+1 in place on row r of a [128 × D] tile; rows ≥ cs become 0 (the
 // tensor map reads zeros past n, and φ(0) = 1 must not enter the sums).
 template <int D>
 __device__ __forceinline__ void phi_row_inplace(uint8_t* tile, int r, bool live) {
-#pragma unroll
-  for (int h = 0; h < D / 64; ++h)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint4* p = reinterpret_cast<uint4*>(tile + sw_chunk(kCb, r, h, j));
-      uint4 u = *p;
-      if (live) {
-        u.x = elu1_bf16x2(u.x); u.y = elu1_bf16x2(u.y); u.z = elu1_bf16x2(u.z); u.w = elu1_bf16x2(u.w);
-      } else {
-        u = make_uint4(0u, 0u, 0u, 0u);
-      }
-      *p = u;
-    }
+  row_map<D>(tile, r, [live](uint4 u) {
+    if (!live) return make_uint4(0u, 0u, 0u, 0u);
+    return make_uint4(elu1_bf16x2(u.x), elu1_bf16x2(u.y), elu1_bf16x2(u.z), elu1_bf16x2(u.w));
+  });
 }
 
 // 8 bf16 → 8 floats
@@ -229,36 +241,53 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
   f[6] = bf16lo_to_f32(u.w); f[7] = bf16hi_to_f32(u.w);
 }
 
+// Row r of a [128 × D] tile scaled by s in place, in fp32 with one rounding.
+template <int D>
+__device__ __forceinline__ void scale_row_inplace(uint8_t* tile, int r, float sc) {
+  row_map<D>(tile, r, [sc](uint4 u) {
+    float f[8];
+    unpack8(u, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] *= sc;
+    return pack8(f);
+  });
+}
+
 // The fp32 [D' × D] accumulator in TMEM (lane = row, columns col0..col0+D)
-// to a contiguous row-major matrix in global memory.  Rows go through
-// shared memory (`stage`, (D + 4)·D floats; the padding spreads a warp's
-// 16-byte writes over all banks) so that the global stores are coalesced.
-// Every thread of the CTA calls it (it holds a CTA barrier).
+// to a contiguous row-major matrix in global memory, in two rounds of D/2
+// columns.  Rows go through shared memory (`stage`, (D/2 + 4)·D floats; the
+// padding spreads a warp's 16-byte writes over all banks) so that the global
+// stores are coalesced.  Every thread of the CTA calls it (it holds CTA
+// barriers).
 template <int D>
 __device__ __forceinline__ void store_tmem_matrix(uint32_t tmem, uint32_t col0, float* stage,
                                                   float* __restrict__ dst) {
-  constexpr int SR = D + 4;
+  constexpr int HC = D / 2, SR = HC + 4;
   const int r = threadIdx.x;
-  if (r < D) {
-    const uint32_t lane_base = (uint32_t)(r >> 5) * 32;
-#pragma unroll 1
-    for (int j0 = 0; j0 < D; j0 += 32) {
-      uint32_t v[32];
-      tmem_ld32(tmem_addr(tmem, lane_base, col0 + j0), v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<float4*>(stage + r * SR + j0 + 4 * q) =
-            make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                        __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-    }
-  }
-  __syncthreads();
   float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    if (r < D) {
+      const uint32_t lane_base = (uint32_t)(r >> 5) * 32;
+#pragma unroll 1
+      for (int j0 = 0; j0 < HC; j0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem_addr(tmem, lane_base, col0 + hh * HC + j0), v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(stage + r * SR + j0 + 4 * q) =
+              make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                          __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      }
+    }
+    __syncthreads();
 #pragma unroll 8
-  for (int e = threadIdx.x; e < D * D / 4; e += kThreadsB) {
-    const int row = e / (D / 4), c4 = e % (D / 4);
-    d4[e] = *reinterpret_cast<const float4*>(stage + row * SR + c4 * 4);
+    for (int e = threadIdx.x; e < D * HC / 4; e += kThreadsB) {
+      const int row = e / (HC / 4), c4 = e % (HC / 4);
+      d4[row * (D / 4) + hh * (HC / 4) + c4] = *reinterpret_cast<const float4*>(stage + row * SR + c4 * 4);
+    }
+    __syncthreads();
   }
 }
 
@@ -395,7 +424,16 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   float* aw = reinterpret_cast<float*>(x.sm + Cfg::oAW);
   const int r = threadIdx.x;
   const CUtensorMap* maps[2] = {&map_k, &map_v};
-  const int offs[2] = {Cfg::oK, Cfg::oV};
+  // the K and V tiles of item `it` (issued while the previous item finishes)
+  auto issue = [&](int64_t it) {
+    if (it >= p.items) return;
+    const int ibh = (int)(it / p.nch), it0 = (int)(it % p.nch) * kCb;
+    arm_tiles(x, 2 * Cfg::TILE);
+    tile_load<D>(x, &map_k, Cfg::oK, it0, ibh);
+    tile_load<D>(x, &map_v, Cfg::oV, it0, ibh);
+    prefetch_next<D>(maps, 2, it + gridDim.x, p);
+  };
+  issue(blockIdx.x);
   int64_t last_bh = -1;
   for (int64_t item = blockIdx.x; item < p.items && !*x.abort_flag; item += gridDim.x) {
     const int64_t bh = item / p.nch;
@@ -404,9 +442,7 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     const int cs = (int)min((int64_t)kCb, p.n - t0);
     float a, w;
     head_decay(p, bh, a, w);
-    __syncthreads();   // the previous item's tiles and tables are no longer read
-    load_item<D>(x, maps, offs, 2, t0, (int)bh, nullptr);
-    prefetch_next<D>(maps, 2, item + gridDim.x, p);
+    __syncthreads();   // the previous item's tables are no longer read
     if (bh != last_bh) head_tables(a, w, pw, aw);
     last_bh = bh;
     __syncthreads();
@@ -416,16 +452,10 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       uint8_t* kt = x.sm + Cfg::oK;
       const bool live = r < cs;
       const uint32_t g2 = live ? splat_bf16x2(w * pw[cs - 1 - r]) : 0u;
-#pragma unroll
-      for (int h = 0; h < Cfg::HALVES; ++h)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint4* pp = reinterpret_cast<uint4*>(kt + sw_chunk(kCb, r, h, j));
-          uint4 u = *pp;
-          u.x = mul_bf16x2(elu1_bf16x2(u.x), g2); u.y = mul_bf16x2(elu1_bf16x2(u.y), g2);
-          u.z = mul_bf16x2(elu1_bf16x2(u.z), g2); u.w = mul_bf16x2(elu1_bf16x2(u.w), g2);
-          *pp = u;
-        }
+      row_map<D>(kt, r, [g2](uint4 u) {
+        return make_uint4(mul_bf16x2(elu1_bf16x2(u.x), g2), mul_bf16x2(elu1_bf16x2(u.y), g2),
+                          mul_bf16x2(elu1_bf16x2(u.z), g2), mul_bf16x2(elu1_bf16x2(u.w), g2));
+      });
     }
     rows_to_mma();
     if (threadIdx.x == 0) {
@@ -441,11 +471,10 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     tile_colsum<D>(x.sm + Cfg::oK, [](int) { return 1.f; },
                    reinterpret_cast<float*>(x.sm + Cfg::oS), p.z + item * D);
     if (!wait_mma(x)) break;
-    // ΔS through the free Q/K/V tiles
-    store_tmem_matrix<D>(x.tmem, 0, reinterpret_cast<float*>(x.sm + Cfg::oQ),
+    issue(item + gridDim.x);   // K'' and V are consumed
+    store_tmem_matrix<D>(x.tmem, 0, reinterpret_cast<float*>(x.sm + Cfg::oST),
                          p.S + item * (int64_t)(D * D));
     tc_fence_before();
-    fence_proxy_async_smem();   // generic accesses before the next item's TMA writes
   }
   BtSetup<D>::teardown(x);
 }
@@ -475,7 +504,21 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
   // [192, 192+D) | PV, later ĜVᵀ, then ΔM [192+D, 320+D)
   constexpr uint32_t RX = 0, RP = 128, RY = 192, RN = 192 + D;
   const CUtensorMap* maps[4] = {&map_q, &map_k, &map_v, &map_g};
-  const int offs[4] = {Cfg::oQ, Cfg::oK, Cfg::oV, Cfg::oG};
+  // the Q, K, V, ∂o tiles, the S_c operand tile and z_c of item `it` (issued
+  // while the previous item finishes)
+  auto issue = [&](int64_t it) {
+    if (it >= p.items) return;
+    const int ibh = (int)(it / p.nch), it0 = (int)(it % p.nch) * kCb;
+    arm_tiles(x, 4 * Cfg::TILE + Cfg::STILE + D * 4);
+    tile_load<D>(x, &map_q, Cfg::oQ, it0, ibh);
+    tile_load<D>(x, &map_k, Cfg::oK, it0, ibh);
+    tile_load<D>(x, &map_v, Cfg::oV, it0, ibh);
+    tile_load<D>(x, &map_g, Cfg::oG, it0, ibh);
+    bulk_to(x, Cfg::oS, p.St + it * (int64_t)(D * D), Cfg::STILE);
+    bulk_to(x, Cfg::oZ, p.z + it * D, D * 4);
+    prefetch_next<D>(maps, 4, it + gridDim.x, p);
+  };
+  issue(blockIdx.x);
   int64_t last_bh = -1;
   for (int64_t item = blockIdx.x; item < p.items && !*x.abort_flag; item += gridDim.x) {
     const int64_t bh = item / p.nch;
@@ -485,10 +528,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     const bool live = r < cs;
     float a, w;
     head_decay(p, bh, a, w);
-    __syncthreads();
-    load_item<D>(x, maps, offs, 4, t0, (int)bh, p.St + item * (int64_t)(D * D));
-    prefetch_next<D>(maps, 4, item + gridDim.x, p);
-    if (r < D) zc[r] = p.z[item * D + r];
+    __syncthreads();   // the previous item's tables are no longer read
     if (bh != last_bh) head_tables(a, w, pw, aw);
     last_bh = bh;
     __syncthreads();
@@ -580,17 +620,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     }
     const float rho = -go * inv_den;
     srho[r] = rho;
-#pragma unroll
-    for (int h = 0; h < Cfg::HALVES; ++h)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint4* pp = reinterpret_cast<uint4*>(gt + sw_chunk(kCb, r, h, j));
-        float f[8];
-        unpack8(*pp, f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] *= inv_den;
-        *pp = pack8(f);
-      }
+    scale_row_inplace<D>(gt, r, inv_den);
     if (live) {
       p.den[bh * p.n + t0 + r] = den;
       p.rho[bh * p.n + t0 + r] = rho;
@@ -679,9 +709,8 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     tile_colsum<D>(qt, [&](int t) { return pw[t + 1] * srho[t]; },
                    reinterpret_cast<float*>(x.sm + Cfg::oS), p.N + item * D);
     if (!wait_mma(x)) break;
-    // ---- rows 4: ∂q = ∂q' ⊙ min(φ(q), 1), staged in the free K/V tiles; then
-    // Q'' = a^{t+1}φ(q) in place
-    uint8_t* dq_stage = x.sm + Cfg::oK;
+    // ---- rows 4: ∂q = ∂q' ⊙ min(φ(q), 1), staged; then Q'' = a^{t+1}φ(q) in place
+    uint8_t* dq_stage = x.sm + Cfg::oST;
 #pragma unroll 1
     for (int j0 = 0; j0 < D; j0 += 32) {
       uint32_t dv[32];
@@ -701,16 +730,10 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     store_staged_rows<D>(dq_stage, p.dq + (bh * p.n + t0) * D, cs);
     {
       const uint32_t s2 = splat_bf16x2(pw[r + 1]);
-#pragma unroll
-      for (int h = 0; h < Cfg::HALVES; ++h)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint4* pp = reinterpret_cast<uint4*>(qt + sw_chunk(kCb, r, h, j));
-          uint4 u = *pp;
-          u.x = mul_bf16x2(u.x, s2); u.y = mul_bf16x2(u.y, s2);
-          u.z = mul_bf16x2(u.z, s2); u.w = mul_bf16x2(u.w, s2);
-          *pp = u;
-        }
+      row_map<D>(qt, r, [s2](uint4 u) {
+        return make_uint4(mul_bf16x2(u.x, s2), mul_bf16x2(u.y, s2), mul_bf16x2(u.z, s2),
+                          mul_bf16x2(u.w, s2));
+      });
     }
     rows_to_mma();
     // ΔM = Q''ᵀĜ
@@ -724,11 +747,10 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     }
     commit_mma(x);
     if (!wait_mma(x)) break;
-    // ΔM through the free Q/K/V tiles
-    store_tmem_matrix<D>(x.tmem, RN, reinterpret_cast<float*>(x.sm + Cfg::oQ),
+    issue(item + gridDim.x);   // every tile, z_c and the scratch are consumed
+    store_tmem_matrix<D>(x.tmem, RN, reinterpret_cast<float*>(x.sm + Cfg::oST),
                          p.M + item * (int64_t)(D * D));
     tc_fence_before();
-    fence_proxy_async_smem();   // generic accesses before the next item's TMA writes
     if (p.want_da) {
       const float s = cta_sum(da, red);
       if (threadIdx.x == 0) p.dapart[bh * p.da_parts + c] = s;
@@ -756,7 +778,6 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   float* aw = reinterpret_cast<float*>(x.sm + Cfg::oAW);
   float* red = reinterpret_cast<float*>(x.sm + Cfg::oRED);
   uint8_t* kt = x.sm + Cfg::oK;
-  uint8_t* vt = x.sm + Cfg::oV;
   uint8_t* gt = x.sm + Cfg::oG;
   const int r = threadIdx.x, wq = r >> 5;
   const uint32_t lane_base = (uint32_t)wq * 32;
@@ -764,7 +785,36 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   // later V·Mᵀ [128, 128+D)) | ∂v [256, 256+D) | ĜᵀV... ĜVᵀᵀ, later ∂k' [384, 512)
   constexpr uint32_t RX = 0, RP = 128, RE = 192, RF = 128, RV = 256, RK = 384;
   const CUtensorMap* maps[4] = {&map_q, &map_k, &map_v, &map_g};
-  const int offs[4] = {Cfg::oQ, Cfg::oK, Cfg::oV, Cfg::oG};
+  // item `it`'s inputs, issued while the previous item finishes: first the
+  // Q, V, ∂o tiles and the M_c operand tile, then (once the K tile and N_c
+  // have been read) the K tile and N_c; ρ and den of its rows into registers
+  auto issue_a = [&](int64_t it) {
+    if (it >= p.items) return;
+    const int ibh = (int)(it / p.nch), it0 = (int)(it % p.nch) * kCb;
+    arm_tiles(x, 4 * Cfg::TILE + Cfg::STILE + D * 4);
+    tile_load<D>(x, &map_q, Cfg::oQ, it0, ibh);
+    tile_load<D>(x, &map_v, Cfg::oV, it0, ibh);
+    tile_load<D>(x, &map_g, Cfg::oG, it0, ibh);
+    bulk_to(x, Cfg::oS, p.Mt + it * (int64_t)(D * D), Cfg::STILE);
+  };
+  auto issue_b = [&](int64_t it) {
+    if (it >= p.items) return;
+    const int ibh = (int)(it / p.nch), it0 = (int)(it % p.nch) * kCb;
+    tile_load<D>(x, &map_k, Cfg::oK, it0, ibh);
+    bulk_to(x, Cfg::oZ, p.N + it * D, D * 4);
+    prefetch_next<D>(maps, 4, it + gridDim.x, p);
+  };
+  float rho_n = 0.f, den_n = 1.f;
+  auto rows_of = [&](int64_t it) {
+    if (it >= p.items) return;
+    const int64_t ibh = it / p.nch, it0 = (it % p.nch) * kCb;
+    const bool l = r < min((int64_t)kCb, p.n - it0);
+    rho_n = l ? p.rho[ibh * p.n + it0 + r] : 0.f;
+    den_n = l ? p.den[ibh * p.n + it0 + r] : 1.f;
+  };
+  issue_a(blockIdx.x);
+  issue_b(blockIdx.x);
+  rows_of(blockIdx.x);
   int64_t last_bh = -1;
   for (int64_t item = blockIdx.x; item < p.items && !*x.abort_flag; item += gridDim.x) {
     const int64_t bh = item / p.nch;
@@ -774,14 +824,11 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     const bool live = r < cs;
     float a, w;
     head_decay(p, bh, a, w);
-    __syncthreads();
-    load_item<D>(x, maps, offs, 4, t0, (int)bh, p.Mt + item * (int64_t)(D * D));
-    prefetch_next<D>(maps, 4, item + gridDim.x, p);
+    __syncthreads();   // the previous item's tables are no longer read
     // (the share of the pairs across the chunk comes from the reverse scan)
     float da = 0.f;
-    if (r < D) nc[r] = p.N[item * D + r];
-    srho[r] = live ? p.rho[bh * p.n + t0 + r] : 0.f;
-    sden[r] = live ? p.den[bh * p.n + t0 + r] : 1.f;
+    srho[r] = rho_n;
+    sden[r] = den_n;
     if (bh != last_bh) head_tables(a, w, pw, aw);
     last_bh = bh;
     __syncthreads();
@@ -790,17 +837,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     phi_row_inplace<D>(kt, r, live);
     {   // ĝ = g / den in place
       const float inv = live ? 1.f / sden[r] : 0.f;
-#pragma unroll
-      for (int h = 0; h < Cfg::HALVES; ++h)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint4* pp = reinterpret_cast<uint4*>(gt + sw_chunk(kCb, r, h, j));
-          float f[8];
-          unpack8(*pp, f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] *= inv;
-          *pp = pack8(f);
-        }
+      scale_row_inplace<D>(gt, r, inv);
     }
     rows_to_mma();
     // Xᵀ = K'Q'ᵀ, (ĜVᵀ)ᵀ = VĜᵀ
@@ -884,30 +921,38 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     }
     commit_mma(x);
     if (!wait_mma(x)) break;
+    issue_a(item + gridDim.x);   // Q, V, ∂o and M_c are consumed
+    rows_of(item + gridDim.x);
     // ---- rows 2: ∂v_s = (PᵀĜ)_s + w·a^{cs−1−s}(K'M)_s;
     // ∂k'_s = (EᵀQ')_s + w·a^{cs−1−s}((VMᵀ)_s + N); ∂a share (t1 − s)·w·a^{t1−s−1}·k'_s·((VMᵀ)_s + N).
     // The TMEM loads are warp-collective, so every row takes part; only the
-    // valid rows are stored.  ∂v and ∂k are staged in the free V/G/S tiles
-    // (the K tile is still read here) and stored coalesced.
-    uint8_t* dv_stage = x.sm + Cfg::oV;
-    uint8_t* dk_stage = x.sm + Cfg::oV + kCb * (2 * D + 16);
+    // valid rows are stored.  ∂v, then ∂k, go through the staging area and
+    // are stored coalesced.
+    uint8_t* stage = x.sm + Cfg::oST;
+    const float fut = live ? w * pw[cs - 1 - r] : 0.f;
+#pragma unroll 1
+    for (int j0 = 0; j0 < D; j0 += 32) {
+      uint32_t va[32], vb[32];
+      tmem_ld32(tmem_addr(x.tmem, lane_base, RV + j0), va);
+      tmem_ld32(tmem_addr(x.tmem, lane_base, RX + j0), vb);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          f[e] = __uint_as_float(va[q8 * 8 + e]) + fut * __uint_as_float(vb[q8 * 8 + e]);
+        stage_chunk<D>(stage, r, j0 + q8 * 8, f);
+      }
+    }
+    __syncthreads();
+    store_staged_rows<D>(stage, p.dv + (bh * p.n + t0) * D, cs);
+    __syncthreads();
     {
-      const float fut = live ? w * pw[cs - 1 - r] : 0.f;
       float kfut = 0.f;
 #pragma unroll 1
       for (int j0 = 0; j0 < D; j0 += 32) {
         uint32_t va[32], vb[32];
-        tmem_ld32(tmem_addr(x.tmem, lane_base, RV + j0), va);
-        tmem_ld32(tmem_addr(x.tmem, lane_base, RX + j0), vb);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            f[e] = __uint_as_float(va[q8 * 8 + e]) + fut * __uint_as_float(vb[q8 * 8 + e]);
-          stage_chunk<D>(dv_stage, r, j0 + q8 * 8, f);
-        }
         tmem_ld32(tmem_addr(x.tmem, lane_base, RK + j0), va);
         tmem_ld32(tmem_addr(x.tmem, lane_base, RF + j0), vb);
         tmem_ld_wait();
@@ -922,16 +967,15 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
             kfut += kf[e] * m;
             f[e] = (__uint_as_float(va[q8 * 8 + e]) + fut * m) * fminf(kf[e], 1.f);
           }
-          stage_chunk<D>(dk_stage, r, j0 + q8 * 8, f);
+          stage_chunk<D>(stage, r, j0 + q8 * 8, f);
         }
       }
       if (live) da += aw[cs - 1 - r] * kfut;
     }
     tc_fence_before();
     __syncthreads();
-    store_staged_rows<D>(dv_stage, p.dv + (bh * p.n + t0) * D, cs);
-    store_staged_rows<D>(dk_stage, p.dk + (bh * p.n + t0) * D, cs);
-    fence_proxy_async_smem();   // generic accesses before the next item's TMA writes
+    issue_b(item + gridDim.x);   // the K tile and N_c are consumed
+    store_staged_rows<D>(stage, p.dk + (bh * p.n + t0) * D, cs);
     if (p.want_da) {
       const float s = cta_sum(da, red);
       if (threadIdx.x == 0) p.dapart[bh * p.da_parts + p.nch + c] = s;
