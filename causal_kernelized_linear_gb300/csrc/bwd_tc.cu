@@ -17,9 +17,10 @@
 // t1 − s), and pairs across it (weight cs, the term cs·a^{cs−1}(⟨S_c, M_c⟩ +
 // ⟨z_c, N_c⟩)) — so no position-weighted state is needed.
 //
-// Passes (each CTA loops over (head, chunk) items; 128 threads, thread r =
-// token row r = TMEM lane r; one thread issues the MMAs and every product is
-// waited for before the rows use it):
+// Passes (each CTA loops over a contiguous range of (head, chunk) items; 128
+// threads, thread r = token row r = TMEM lane r; one thread issues the MMAs
+// and every product is waited for before the rows use it; the next item's
+// loads are issued as soon as the current item's tiles are consumed):
 //   1. bt_state:  ΔS_c = K''ᵀV (K'' = w·a^{cs−1−s}φ(k)), Δz_c      → workspace
 //   2. scan:      S_c = exclusive decayed prefix of ΔS, in fp32 and as the
 //                 bf16 operand tile of pass 3                        (CUDA cores, float4)
@@ -186,16 +187,12 @@ __device__ __forceinline__ void bulk_to(Bt& x, int off, const void* src, uint32_
   if (threadIdx.x == 0) bulk_load(x.sm + off, src, bytes, &x.bar[0]);
 }
 
-// The tiles of the CTA's next item into L2 (no completion to wait for), so
-// that its loads do not start from DRAM.
-template <int D>
-__device__ __forceinline__ void prefetch_next(const CUtensorMap* const* maps, int ntiles,
-                                              int64_t next, const BtParams& p) {
-  if (threadIdx.x != 0 || next >= p.items) return;
-  const int bh = (int)(next / p.nch);
-  const int t0 = (int)(next % p.nch) * kCb;
-  for (int i = 0; i < ntiles; ++i)
-    for (int h = 0; h < D / 64; ++h) tma_prefetch_l2_3d(maps[i], h * 64, t0, bh);
+// The CTA's items: a contiguous range, so that consecutive items mostly share
+// a head (and its decay tables).
+__device__ __forceinline__ void item_range(int64_t items, int64_t& ib, int64_t& ie) {
+  const int64_t per = (items + gridDim.x - 1) / gridDim.x;
+  ib = min(items, (int64_t)blockIdx.x * per);
+  ie = min(items, ib + per);
 }
 
 __device__ __forceinline__ bool wait_tiles(Bt& x) {
@@ -423,27 +420,29 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   float* pw = reinterpret_cast<float*>(x.sm + Cfg::oPW);
   float* aw = reinterpret_cast<float*>(x.sm + Cfg::oAW);
   const int r = threadIdx.x;
-  const CUtensorMap* maps[2] = {&map_k, &map_v};
+  int64_t ib, ie;
+  item_range(p.items, ib, ie);
   // the K and V tiles of item `it` (issued while the previous item finishes)
   auto issue = [&](int64_t it) {
-    if (it >= p.items) return;
+    if (it >= ie) return;
     const int ibh = (int)(it / p.nch), it0 = (int)(it % p.nch) * kCb;
     arm_tiles(x, 2 * Cfg::TILE);
     tile_load<D>(x, &map_k, Cfg::oK, it0, ibh);
     tile_load<D>(x, &map_v, Cfg::oV, it0, ibh);
-    prefetch_next<D>(maps, 2, it + gridDim.x, p);
   };
-  issue(blockIdx.x);
+  issue(ib);
   int64_t last_bh = -1;
-  for (int64_t item = blockIdx.x; item < p.items && !*x.abort_flag; item += gridDim.x) {
+  float a = 1.f, w = 1.f;   // the decay of head last_bh and its new-token weight
+  for (int64_t item = ib; item < ie && !*x.abort_flag; ++item) {
     const int64_t bh = item / p.nch;
     const int c = (int)(item % p.nch);
     const int t0 = c * kCb;
     const int cs = (int)min((int64_t)kCb, p.n - t0);
-    float a, w;
-    head_decay(p, bh, a, w);
     __syncthreads();   // the previous item's tables are no longer read
-    if (bh != last_bh) head_tables(a, w, pw, aw);
+    if (bh != last_bh) {
+      head_decay(p, bh, a, w);
+      head_tables(a, w, pw, aw);
+    }
     last_bh = bh;
     __syncthreads();
     if (!wait_tiles(x)) break;
@@ -471,7 +470,7 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     tile_colsum<D>(x.sm + Cfg::oK, [](int) { return 1.f; },
                    reinterpret_cast<float*>(x.sm + Cfg::oS), p.z + item * D);
     if (!wait_mma(x)) break;
-    issue(item + gridDim.x);   // K'' and V are consumed
+    issue(item + 1);   // K'' and V are consumed
     store_tmem_matrix<D>(x.tmem, 0, reinterpret_cast<float*>(x.sm + Cfg::oST),
                          p.S + item * (int64_t)(D * D));
     tc_fence_before();
@@ -503,11 +502,12 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
   // TMEM columns: X [0,128) | P, later E (bf16) [128,192) | Y, later U, then ∂q'
   // [192, 192+D) | PV, later ĜVᵀ, then ΔM [192+D, 320+D)
   constexpr uint32_t RX = 0, RP = 128, RY = 192, RN = 192 + D;
-  const CUtensorMap* maps[4] = {&map_q, &map_k, &map_v, &map_g};
+  int64_t ib, ie;
+  item_range(p.items, ib, ie);
   // the Q, K, V, ∂o tiles, the S_c operand tile and z_c of item `it` (issued
   // while the previous item finishes)
   auto issue = [&](int64_t it) {
-    if (it >= p.items) return;
+    if (it >= ie) return;
     const int ibh = (int)(it / p.nch), it0 = (int)(it % p.nch) * kCb;
     arm_tiles(x, 4 * Cfg::TILE + Cfg::STILE + D * 4);
     tile_load<D>(x, &map_q, Cfg::oQ, it0, ibh);
@@ -516,20 +516,21 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     tile_load<D>(x, &map_g, Cfg::oG, it0, ibh);
     bulk_to(x, Cfg::oS, p.St + it * (int64_t)(D * D), Cfg::STILE);
     bulk_to(x, Cfg::oZ, p.z + it * D, D * 4);
-    prefetch_next<D>(maps, 4, it + gridDim.x, p);
   };
-  issue(blockIdx.x);
+  issue(ib);
   int64_t last_bh = -1;
-  for (int64_t item = blockIdx.x; item < p.items && !*x.abort_flag; item += gridDim.x) {
+  float a = 1.f, w = 1.f;   // the decay of head last_bh and its new-token weight
+  for (int64_t item = ib; item < ie && !*x.abort_flag; ++item) {
     const int64_t bh = item / p.nch;
     const int c = (int)(item % p.nch);
     const int t0 = c * kCb;
     const int cs = (int)min((int64_t)kCb, p.n - t0);
     const bool live = r < cs;
-    float a, w;
-    head_decay(p, bh, a, w);
     __syncthreads();   // the previous item's tables are no longer read
-    if (bh != last_bh) head_tables(a, w, pw, aw);
+    if (bh != last_bh) {
+      head_decay(p, bh, a, w);
+      head_tables(a, w, pw, aw);
+    }
     last_bh = bh;
     __syncthreads();
     if (!wait_tiles(x)) break;
@@ -747,7 +748,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     }
     commit_mma(x);
     if (!wait_mma(x)) break;
-    issue(item + gridDim.x);   // every tile, z_c and the scratch are consumed
+    issue(item + 1);   // every tile, z_c and the scratch are consumed
     store_tmem_matrix<D>(x.tmem, RN, reinterpret_cast<float*>(x.sm + Cfg::oST),
                          p.M + item * (int64_t)(D * D));
     tc_fence_before();
@@ -784,12 +785,13 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   // TMEM columns: Xᵀ, later K'M [0,128) | Pᵀ [128,192) | Eᵀ [192,256) (both
   // later V·Mᵀ [128, 128+D)) | ∂v [256, 256+D) | ĜᵀV... ĜVᵀᵀ, later ∂k' [384, 512)
   constexpr uint32_t RX = 0, RP = 128, RE = 192, RF = 128, RV = 256, RK = 384;
-  const CUtensorMap* maps[4] = {&map_q, &map_k, &map_v, &map_g};
+  int64_t ib, ie;
+  item_range(p.items, ib, ie);
   // item `it`'s inputs, issued while the previous item finishes: first the
   // Q, V, ∂o tiles and the M_c operand tile, then (once the K tile and N_c
   // have been read) the K tile and N_c; ρ and den of its rows into registers
   auto issue_a = [&](int64_t it) {
-    if (it >= p.items) return;
+    if (it >= ie) return;
     const int ibh = (int)(it / p.nch), it0 = (int)(it % p.nch) * kCb;
     arm_tiles(x, 4 * Cfg::TILE + Cfg::STILE + D * 4);
     tile_load<D>(x, &map_q, Cfg::oQ, it0, ibh);
@@ -798,38 +800,39 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     bulk_to(x, Cfg::oS, p.Mt + it * (int64_t)(D * D), Cfg::STILE);
   };
   auto issue_b = [&](int64_t it) {
-    if (it >= p.items) return;
+    if (it >= ie) return;
     const int ibh = (int)(it / p.nch), it0 = (int)(it % p.nch) * kCb;
     tile_load<D>(x, &map_k, Cfg::oK, it0, ibh);
     bulk_to(x, Cfg::oZ, p.N + it * D, D * 4);
-    prefetch_next<D>(maps, 4, it + gridDim.x, p);
   };
   float rho_n = 0.f, den_n = 1.f;
   auto rows_of = [&](int64_t it) {
-    if (it >= p.items) return;
+    if (it >= ie) return;
     const int64_t ibh = it / p.nch, it0 = (it % p.nch) * kCb;
     const bool l = r < min((int64_t)kCb, p.n - it0);
     rho_n = l ? p.rho[ibh * p.n + it0 + r] : 0.f;
     den_n = l ? p.den[ibh * p.n + it0 + r] : 1.f;
   };
-  issue_a(blockIdx.x);
-  issue_b(blockIdx.x);
-  rows_of(blockIdx.x);
+  issue_a(ib);
+  issue_b(ib);
+  rows_of(ib);
   int64_t last_bh = -1;
-  for (int64_t item = blockIdx.x; item < p.items && !*x.abort_flag; item += gridDim.x) {
+  float a = 1.f, w = 1.f;   // the decay of head last_bh and its new-token weight
+  for (int64_t item = ib; item < ie && !*x.abort_flag; ++item) {
     const int64_t bh = item / p.nch;
     const int c = (int)(item % p.nch);
     const int t0 = c * kCb;
     const int cs = (int)min((int64_t)kCb, p.n - t0);
     const bool live = r < cs;
-    float a, w;
-    head_decay(p, bh, a, w);
     __syncthreads();   // the previous item's tables are no longer read
     // (the share of the pairs across the chunk comes from the reverse scan)
     float da = 0.f;
     srho[r] = rho_n;
     sden[r] = den_n;
-    if (bh != last_bh) head_tables(a, w, pw, aw);
+    if (bh != last_bh) {
+      head_decay(p, bh, a, w);
+      head_tables(a, w, pw, aw);
+    }
     last_bh = bh;
     __syncthreads();
     if (!wait_tiles(x)) break;
@@ -921,8 +924,8 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     }
     commit_mma(x);
     if (!wait_mma(x)) break;
-    issue_a(item + gridDim.x);   // Q, V, ∂o and M_c are consumed
-    rows_of(item + gridDim.x);
+    issue_a(item + 1);   // Q, V, ∂o and M_c are consumed
+    rows_of(item + 1);
     // ---- rows 2: ∂v_s = (PᵀĜ)_s + w·a^{cs−1−s}(K'M)_s;
     // ∂k'_s = (EᵀQ')_s + w·a^{cs−1−s}((VMᵀ)_s + N); ∂a share (t1 − s)·w·a^{t1−s−1}·k'_s·((VMᵀ)_s + N).
     // The TMEM loads are warp-collective, so every row takes part; only the
@@ -974,7 +977,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     }
     tc_fence_before();
     __syncthreads();
-    issue_b(item + gridDim.x);   // the K tile and N_c are consumed
+    issue_b(item + 1);   // the K tile and N_c are consumed
     store_staged_rows<D>(stage, p.dk + (bh * p.n + t0) * D, cs);
     if (p.want_da) {
       const float s = cta_sum(da, red);
