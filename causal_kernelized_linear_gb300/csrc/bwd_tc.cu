@@ -96,8 +96,8 @@ struct BtParams {
   int64_t items;        // B·H·nch
   float* S;             // [BH][nch][D*D]: ΔS_c, then S_c
   float* z;             // [BH][nch][D]
-  float* M;             // [BH][nch][D*D]: ΔM_c, then M_c
-  float* N;             // [BH][nch][D]
+  float* M;             // [BH][nch][D*D]: ΔM_c (M_c itself only as its bf16 tile)
+  float* N;             // [BH][nch][D]: ΔN_c, then N_c
   const __nv_bfloat16* St;   // [BH][nch] bf16 operand tiles of S_c
   const __nv_bfloat16* Mt;   // [BH][nch] bf16 operand tiles of M_c
   float* den;           // [BH][n]
@@ -167,8 +167,8 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// Thread 0 arms the TMA barrier for the next `bytes` of copies (issued
-// before or after this call's copies complete, within the same phase).
+// Thread 0 arms the TMA barrier with the byte count of one item's copies;
+// the copies may be issued later, within the same barrier phase.
 __device__ __forceinline__ void arm_tiles(Bt& x, uint32_t bytes) {
   if (threadIdx.x == 0) mbar_arrive_expect_tx(&x.bar[0], bytes);
   x.tma_pending = true;
@@ -238,7 +238,7 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
   f[6] = bf16lo_to_f32(u.w); f[7] = bf16hi_to_f32(u.w);
 }
 
-// Row r of a [128 × D] tile scaled by s in place, in fp32 with one rounding.
+// Row r of a [128 × D] tile scaled by sc in place, in fp32 with one rounding.
 template <int D>
 __device__ __forceinline__ void scale_row_inplace(uint8_t* tile, int r, float sc) {
   row_map<D>(tile, r, [sc](uint4 u) {
