@@ -78,3 +78,21 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_profile_summaries_run_committed_files_only():
+    # every command a summary under profiles/ prints is bench.py with one of
+    # its own profile cases (no scratch scripts)
+    import glob
+    import re
+    choices = set()
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    m = re.search(r'"--profile-case",\s*choices=\[(.*?)\]', src, re.S)
+    assert m, "bench.py defines --profile-case choices"
+    choices = set(re.findall(r'"([a-z0-9-]+)"', m.group(1)))
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        text = open(path, encoding="utf-8").read()
+        for script in re.findall(r"python\s+(\S+\.py)", text):
+            assert script == "bench.py", (path, script)
+        for case in re.findall(r"--profile-case\s+([a-z0-9-]+)", text):
+            assert case in choices, (path, case)
