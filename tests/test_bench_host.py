@@ -1,8 +1,10 @@
 """Host-side logic of bench.py, on the CPU: the algorithmic work behind the
 roofline, the staleness check of the recorded DRAM traffic, and the JSON
 line of the reference arm (the fp64 oracle timed on the host)."""
+import glob
 import json
 import os
+import re
 import subprocess
 import sys
 
@@ -83,9 +85,6 @@ def test_reference_arm_prints_one_contract_line():
 def test_profile_summaries_run_committed_files_only():
     # every command a summary under profiles/ prints is bench.py with one of
     # its own profile cases (no scratch scripts)
-    import glob
-    import re
-    choices = set()
     src = open(os.path.join(ROOT, "bench.py")).read()
     m = re.search(r'"--profile-case",\s*choices=\[(.*?)\]', src, re.S)
     assert m, "bench.py defines --profile-case choices"
