@@ -168,17 +168,26 @@ def _time_steps(fn, steps, warmup, stream, flush=None, counter=None):
 
 
 def _max_over_ranks(x, dist):
+    """The largest x over all ranks (x itself without a process group)."""
     if dist is None:
         return x
-    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], device=dev, dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _job_rate(units_per_rank, seconds, world, dist):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time."""
+    return units_per_rank * world / _max_over_ranks(seconds, dist)
 
 
 def _barrier(dist):
     if dist is not None:
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 # ----------------------------------------------------------------------------- workloads
@@ -438,9 +447,8 @@ def run_ours(args, rank, world, dist):
     _barrier(dist)
     clocks = sampler.stop() if sampler else None
 
-    step_s = sum(main["ms"]) / 1e3
-    step_s = _max_over_ranks(step_s, dist)
-    value = w.B * w.n * args.steps * world / step_s
+    step_s = _max_over_ranks(sum(main["ms"]) / 1e3, dist)
+    value = _job_rate(w.B * w.n * args.steps, step_s, world, None)
     ms_per_step = 1e3 * step_s / args.steps
     tflops = main["flops"] / (ms_per_step / 1e3) / 1e12
     achieved = main["bytes"] / (main["avg_ms"] / 1e3) / 1e9
@@ -451,7 +459,7 @@ def run_ours(args, rank, world, dist):
     e2e = None
     if "e2e" in main:
         e_s = _max_over_ranks(sum(main["e2e"]["ms"]) / 1e3, dist)
-        e2e = {"value": w.B * w.n * args.steps * world / e_s, "unit": "tokens/s",
+        e2e = {"value": _job_rate(w.B * w.n * args.steps, e_s, world, None), "unit": "tokens/s",
                "h2d_bytes_per_step": main["e2e"]["h2d"], "d2h_bytes_per_step": main["e2e"]["d2h"],
                "pipelining": main["e2e"]["overlap"],
                "ms_per_step": 1e3 * e_s / args.steps}
