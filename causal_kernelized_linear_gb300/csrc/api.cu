@@ -54,6 +54,40 @@ la_status device_info(DeviceInfo* out) {
   return LA_OK;
 }
 
+// Workspace memory: stream-ordered allocations from one pool per device owned
+// by the library.  The pool keeps what it has reserved (unlimited release
+// threshold), so repeated calls reuse the same device memory instead of
+// mapping and unmapping it at every synchronisation; the reservation is the
+// largest workspace that calls had in flight at once, held until exit.
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+cudaError_t ws_alloc(void** p, size_t bytes, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_pool[dev]) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t np;
+      if ((e = cudaMemPoolCreate(&np, &props)) != cudaSuccess) return e;
+      uint64_t keep = UINT64_MAX;
+      if ((e = cudaMemPoolSetAttribute(np, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+        cudaMemPoolDestroy(np);
+        return e;
+      }
+      g_pool[dev] = np;
+    }
+    pool = g_pool[dev];
+  }
+  return cudaMallocFromPoolAsync(p, bytes, pool, s);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool valid_dtype(la_dtype t) { return t == LA_BF16 || t == LA_F32; }
@@ -201,7 +235,7 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
   if (need_ld) ws_floats += (size_t)BH * plan.nseg;
   float* ws = nullptr;
   if (ws_floats) {
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_floats * sizeof(float), stream);
+    cudaError_t e = ws_alloc(reinterpret_cast<void**>(&ws), ws_floats * sizeof(float), stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return e == cudaErrorMemoryAllocation ? LA_ERR_OUT_OF_MEMORY : LA_ERR_CUDA;
@@ -377,7 +411,7 @@ la_status la_backward(const la_tensor* q, const la_tensor* k, const la_tensor* v
   const la::SegmentPlan plan = la::plan_segments(f.B * f.H, f.n, di.num_sms, 32, 2);
   const size_t ws_floats = tc ? la::tc_backward_ws_floats(b) : la::backward_workspace_floats(b, plan);
   float* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_floats * sizeof(float), s);
+  cudaError_t e = la::ws_alloc(reinterpret_cast<void**>(&ws), ws_floats * sizeof(float), s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorMemoryAllocation ? LA_ERR_OUT_OF_MEMORY : LA_ERR_CUDA;

@@ -2,8 +2,8 @@
 // memory while they run — for example code running inside an allocator
 // callback, under a memory-pool policy that forbids new allocations, or on a
 // stream being captured where an allocation would break the capture's rules.
-// The per-segment states that la_forward takes with cudaMallocAsync live
-// here in one fixed, file-scope device array instead.
+// The per-segment states that la_forward takes from its stream-ordered pool
+// live here in one fixed, file-scope device array instead.
 #include "linattn.h"
 
 #include "internal.h"

@@ -31,7 +31,10 @@
  *     Arguments are validated on the host before anything is queued: a call
  *     that returns an error queued no kernel and wrote nothing.
  *   - Temporary device workspace (per-segment states of long sequences) is
- *     taken with cudaMallocAsync / cudaFreeAsync on `stream`.
+ *     taken stream-ordered on `stream` (cudaMallocFromPoolAsync /
+ *     cudaFreeAsync) from a memory pool the library creates per device; the
+ *     pool keeps its reservation (the largest workspace in flight at once)
+ *     until the process exits, so repeated calls do not map memory again.
  *   - The library keeps per-device state only for cached device attributes,
  *     the device status word and cached kernel attributes.
  */
@@ -221,7 +224,7 @@ la_status la_decode_step_token_decay(float* mu, float* nu, const la_tensor* q,
  * 2·(d² + d)·4 bytes per 128 tokens per head, plus 8 bytes per token); all
  * other cases run on fp32 CUDA cores.  d ∈ {32, 64, 128}, and for the
  * Performer map d·m ≤ 16384 (else LA_ERR_UNSUPPORTED).  Temporary workspace
- * as for la_forward (cudaMallocAsync on `stream`).
+ * as for la_forward (stream-ordered, from the library's pool).
  */
 la_status la_backward(const la_tensor* q, const la_tensor* k, const la_tensor* v,
                       const float* decay_a, la_feature_map feature_map, const la_tensor* omega,
@@ -244,8 +247,8 @@ la_status la_get_last_device_status(la_stream stream);
  * memory during the call: code running inside an allocator or out-of-memory
  * handler, under a memory pool whose policy forbids growth, or in a setting
  * where cudaMalloc / cudaMallocAsync would deadlock or be refused.  It
- * allocates nothing: the per-segment states that la_forward takes with
- * cudaMallocAsync live in a fixed scratch array of 4 Mi floats (16 MiB),
+ * allocates nothing: the per-segment states that la_forward takes from
+ * its stream-ordered pool live in a fixed scratch array of 4 Mi floats (16 MiB),
  * which every GPU that loads the library holds until the process exits.
  * The method is the same as la_forward; the pages have no counterpart of
  * this entry point, it only changes where the temporary states live.

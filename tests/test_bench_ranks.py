@@ -24,7 +24,9 @@ out = {"rank": rank, "world": world,
        "max": bench._max_over_ranks(secs, dist),
        "rate": bench._job_rate(100.0, secs, world, dist)}
 bench._barrier(dist)
-print("RESULT " + json.dumps(out), flush=True)
+# one file per rank: lines the two ranks print to one pipe can interleave
+with open(os.path.join(sys.argv[2], f"rank{rank}.json"), "w") as f:
+    json.dump(out, f)
 dist.destroy_process_group()
 '''
 
@@ -40,11 +42,12 @@ def test_two_gloo_ranks_agree_on_the_slowest_time(tmp_path):
     script = tmp_path / "ranks.py"
     script.write_text(RANK_SCRIPT)
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
-           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), str(script), ROOT]
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), str(script), ROOT,
+           str(tmp_path)]
     env = dict(os.environ, OMP_NUM_THREADS="1")
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=220, env=env, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-3000:]
-    res = [json.loads(l.split("RESULT ", 1)[1]) for l in r.stdout.splitlines() if "RESULT " in l]
+    res = [json.loads((tmp_path / f"rank{i}.json").read_text()) for i in (0, 1)]
     assert sorted(x["rank"] for x in res) == [0, 1]
     for x in res:
         assert x["world"] == 2
