@@ -1,7 +1,6 @@
 // la_forward_noalloc: the forward for callers that cannot allocate device
 // memory while they run — for example code running inside an allocator
-// callback, under a memory-pool policy that forbids new allocations, or on a
-// stream being captured where an allocation would break the capture's rules.
+// callback, or under a memory-pool policy that forbids new allocations.
 // The per-segment states that la_forward takes from its stream-ordered pool
 // live here in one fixed, file-scope device array instead.
 #include "linattn.h"

@@ -5,8 +5,8 @@ out-of-memory handlers, pools whose policy forbids growth); for them the
 library keeps the per-segment states of long sequences in one fixed scratch
 array instead of taking them with cudaMallocAsync.  These tests call that
 entry point directly with ctypes on caller-allocated inputs and outputs and
-check it against la_forward, twice in a row with different inputs so that
-stale scratch contents from the first call cannot leak into the second.
+check it against the fp64 oracle, twice in a row with different inputs so
+that stale scratch contents from the first call cannot leak into the second.
 This file is collected last on purpose.
 """
 import ctypes
@@ -16,6 +16,7 @@ import torch
 
 import causal_kernelized_linear_gb300 as cl
 from causal_kernelized_linear_gb300 import _binding as B
+import oracle
 import workloads as W
 from helpers import TOL_BF16, TOL_F32, assert_parity
 
@@ -63,11 +64,11 @@ def test_noalloc_matches_forward_twice(lib, cuda_device, case):
         inp = W.make_forward_inputs(Bn, H, n, d, dtype, fm, m, decay, seed=seed + n,
                                     qk_scale=(d ** -0.25 if fm == "performer" else 1.0))
         g = {k: (x.to(cuda_device) if isinstance(x, torch.Tensor) else x) for k, x in inp.items()}
-        ref = cl.forward(g["q"], g["k"], g["v"], g["a"], fm, g["omega"], causal)
         st, out = _noalloc(lib, g["q"], g["k"], g["v"], g["a"], fm, g["omega"], causal)
         torch.cuda.synchronize()
         assert st == B.LA_OK, cl.status_string(st)
-        assert_parity(out, ref.float(), tol, f"no-alloc call {call + 1}")
+        ref = oracle.forward(inp["q"], inp["k"], inp["v"], inp["a"], fm, inp["omega"], causal)
+        assert_parity(out, ref, tol, f"no-alloc call {call + 1}")
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(lib, cuda_device):
@@ -76,7 +77,17 @@ def test_noalloc_rejects_requests_beyond_its_scratch(lib, cuda_device):
     st, out = _noalloc(lib, q, q, q, None, "elu1", None, False)
     torch.cuda.synchronize()
     assert st == B.LA_ERR_UNSUPPORTED
-    # invalid arguments are still rejected before any device work
-    a = torch.full((8,), 0.5, device=cuda_device)
-    st, _ = _noalloc(lib, q, q, q, a, "elu1", None, False)
+    # requests that would fit the scratch are still validated first: a decay
+    # on a non-causal call (eq (6) has none), mismatched shapes, and a
+    # misaligned tensor are refused whatever their size
+    small = torch.randn(1, 2, 256, 64, device=cuda_device).bfloat16()
+    a = torch.full((2,), 0.5, device=cuda_device)
+    st, _ = _noalloc(lib, small, small, small, a, "elu1", None, False)
     assert st == B.LA_ERR_UNSUPPORTED
+    short = torch.randn(1, 2, 128, 64, device=cuda_device).bfloat16()
+    st, _ = _noalloc(lib, small, short, small, None, "elu1", None, True)
+    assert st == B.LA_ERR_INVALID_ARG
+    flat = torch.randn(1 * 2 * 256 * 64 + 1, device=cuda_device).bfloat16()
+    odd = flat[1:].view(1, 2, 256, 64)   # 2 bytes past a 16-byte boundary
+    st, _ = _noalloc(lib, odd, small, small, None, "elu1", None, True)
+    assert st == B.LA_ERR_INVALID_ARG
