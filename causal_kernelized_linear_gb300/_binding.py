@@ -33,7 +33,7 @@ _DT = {torch.bfloat16: LA_BF16, torch.float32: LA_F32}
 EXPORTED = ("la_forward", "la_forward_with_state", "la_decode_step", "la_status_string",
             "la_get_last_device_status", "la_launch_count", "la_selftest_wait_timeout",
             "la_decode_step_fm", "la_forward_token_decay", "la_decode_step_token_decay",
-            "la_backward")
+            "la_backward", "la_forward_from_state", "la_forward_state", "la_shard_entering_state")
 
 
 class LinAttnError(RuntimeError):
@@ -76,6 +76,16 @@ def load():
         lib.la_forward_with_state.argtypes = [P, P, P, vp, ctypes.c_int, P, ctypes.c_int, P,
                                               vp, vp, vp]
         lib.la_forward_with_state.restype = ctypes.c_int
+        lib.la_forward_from_state.argtypes = [P, P, P, vp, ctypes.c_int, P, vp, vp, P, vp, vp,
+                                              vp]
+        lib.la_forward_from_state.restype = ctypes.c_int
+        lib.la_forward_state.argtypes = [P, P, vp, ctypes.c_int, P, vp, vp, vp]
+        lib.la_forward_state.restype = ctypes.c_int
+        lib.la_shard_entering_state.argtypes = [vp, ctypes.c_int, ctypes.c_int,
+                                                ctypes.POINTER(ctypes.c_int64), vp, ctypes.c_int64,
+                                                ctypes.c_int64, ctypes.c_int, ctypes.c_int, vp, vp,
+                                                vp]
+        lib.la_shard_entering_state.restype = ctypes.c_int
         lib.la_decode_step.argtypes = [vp, vp, P, P, P, vp, P, vp]
         lib.la_decode_step.restype = ctypes.c_int
         lib.la_decode_step_fm.argtypes = [vp, vp, P, P, P, vp, ctypes.c_int, P, P, vp]
@@ -187,6 +197,80 @@ def forward_with_state(q, k, v, decay_a=None, feature_map="elu1", omega=None, ca
                                       nu_out.data_ptr(), _stream_handle(stream))
     _check("la_forward_with_state", st)
     return out, mu_out, nu_out
+
+
+def _state_pair(name, mu, nu, shape_mu, shape_nu):
+    _need_cuda(name + " μ", mu, torch.float32)
+    _need_cuda(name + " ν", nu, torch.float32)
+    if tuple(mu.shape) != shape_mu or tuple(nu.shape) != shape_nu:
+        raise ValueError(f"{name}: μ must be {list(shape_mu)} and ν {list(shape_nu)}")
+
+
+def forward_from_state(q, k, v, mu0, nu0, decay_a=None, feature_map="elu1", omega=None, out=None,
+                       return_state=False, stream=None):
+    """la_forward_from_state: the causal forward continued from (μ0 [B,H,d',d],
+    ν0 [B,H,d'] fp32).  Returns out, or (out, μ, ν) with ``return_state``."""
+    out, fm, dptr, om, qd, kd, vd, od = _forward_args(q, k, v, decay_a, feature_map, omega, out)
+    B, H, _, d = q.shape
+    dp = d if fm == LA_FM_ELU1 else omega.shape[1]
+    _state_pair("initial state", mu0, nu0, (B, H, dp, d), (B, H, dp))
+    mu_out = nu_out = None
+    if return_state:
+        mu_out = torch.empty(B, H, dp, d, device=q.device, dtype=torch.float32)
+        nu_out = torch.empty(B, H, dp, device=q.device, dtype=torch.float32)
+    st = load().la_forward_from_state(
+        ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), dptr, fm,
+        ctypes.byref(om) if om is not None else None, mu0.data_ptr(), nu0.data_ptr(),
+        ctypes.byref(od), mu_out.data_ptr() if return_state else None,
+        nu_out.data_ptr() if return_state else None, _stream_handle(stream))
+    _check("la_forward_from_state", st)
+    return (out, mu_out, nu_out) if return_state else out
+
+
+def forward_state(k, v, decay_a=None, feature_map="elu1", omega=None, mu_out=None, nu_out=None,
+                  stream=None):
+    """la_forward_state: the state (μ, ν) the causal recurrence reaches from zero
+    over k, v [B,H,n,d] (no outputs).  Returns (μ [B,H,d',d], ν [B,H,d'])."""
+    _, fm, dptr, om, _, kd, vd, _ = _forward_args(k, k, v, decay_a, feature_map, omega, k)
+    B, H, _, d = k.shape
+    dp = d if fm == LA_FM_ELU1 else omega.shape[1]
+    if mu_out is None:
+        mu_out = torch.empty(B, H, dp, d, device=k.device, dtype=torch.float32)
+    if nu_out is None:
+        nu_out = torch.empty(B, H, dp, device=k.device, dtype=torch.float32)
+    _state_pair("state", mu_out, nu_out, (B, H, dp, d), (B, H, dp))
+    st = load().la_forward_state(ctypes.byref(kd), ctypes.byref(vd), dptr, fm,
+                                 ctypes.byref(om) if om is not None else None, mu_out.data_ptr(),
+                                 nu_out.data_ptr(), _stream_handle(stream))
+    _check("la_forward_state", st)
+    return mu_out, nu_out
+
+
+def shard_entering_state(gathered, rank, shard_len, B, H, dp, d, decay_a=None, mu_in=None,
+                         nu_in=None, stream=None):
+    """la_shard_entering_state: ``gathered`` fp32 [nshards, B·H·d'·d + B·H·d']
+    (each row a shard's μ then ν), ``shard_len`` the tokens of every shard.
+    Returns the state (μ [B,H,d',d], ν [B,H,d']) entering shard ``rank``."""
+    _need_cuda("gathered", gathered, torch.float32)
+    nshards = len(shard_len)
+    if gathered.dim() != 2 or gathered.shape[0] != nshards or \
+            gathered.shape[1] != B * H * (dp * d + dp):
+        raise ValueError("gathered must be [nshards, B·H·d'·d + B·H·d']")
+    dptr = None
+    if decay_a is not None:
+        _need_cuda("decay_a", decay_a, torch.float32)
+        dptr = decay_a.data_ptr()
+    if mu_in is None:
+        mu_in = torch.empty(B, H, dp, d, device=gathered.device, dtype=torch.float32)
+    if nu_in is None:
+        nu_in = torch.empty(B, H, dp, device=gathered.device, dtype=torch.float32)
+    _state_pair("entering state", mu_in, nu_in, (B, H, dp, d), (B, H, dp))
+    lens = (ctypes.c_int64 * nshards)(*[int(x) for x in shard_len])
+    st = load().la_shard_entering_state(gathered.data_ptr(), nshards, int(rank), lens, dptr,
+                                        int(B), int(H), int(dp), int(d), mu_in.data_ptr(),
+                                        nu_in.data_ptr(), _stream_handle(stream))
+    _check("la_shard_entering_state", st)
+    return mu_in, nu_in
 
 
 def decode_step(mu, nu, q, k, v, decay_a=None, out=None, stream=None, feature_map="elu1",

@@ -154,7 +154,15 @@ la_status validate_forward(const la_tensor* q, const la_tensor* k, const la_tens
   a->causal = causal != 0;
   a->mu_out = nullptr;
   a->nu_out = nullptr;
+  a->init_state = nullptr;
+  a->init_z = nullptr;
   return LA_OK;
+}
+
+// [p, p + bytes) and [q, q + bytes2) share a byte
+bool overlaps(const void* p, size_t bytes, const void* q, size_t bytes2) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), b0 = reinterpret_cast<uintptr_t>(q);
+  return a0 < b0 + bytes2 && b0 < a0 + bytes;
 }
 
 // Cut every head into segments so that all CTAs fit in one wave
@@ -214,7 +222,17 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
   const int64_t BH = a.B * a.H;
   const size_t state_elems = (size_t)a.dp * a.d;
   if (a.n == 0) {
-    // empty sequence: nothing to write but the (zero) state
+    // empty sequence: nothing to write but the state, which is the initial
+    // one (zero when none is given)
+    if (a.init_state) {
+      if (a.mu_out && cudaMemcpyAsync(a.mu_out, a.init_state, BH * state_elems * sizeof(float),
+                                      cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+        return LA_ERR_CUDA;
+      if (a.nu_out && cudaMemcpyAsync(a.nu_out, a.init_z, BH * a.dp * sizeof(float),
+                                      cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+        return LA_ERR_CUDA;
+      return LA_OK;
+    }
     if (a.mu_out && cudaMemsetAsync(a.mu_out, 0, BH * state_elems * sizeof(float), stream) != cudaSuccess)
       return LA_ERR_CUDA;
     if (a.nu_out && cudaMemsetAsync(a.nu_out, 0, BH * a.dp * sizeof(float), stream) != cudaSuccess)
@@ -255,6 +273,44 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
     cudaError_t f = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess) e = f;
   }
+  return to_status(e);
+}
+
+// The final state from zero without the outputs: the aggregate of every
+// segment, then their decayed sum (the scan's total) into mu_out / nu_out.
+la_status run_state(FwdArgs& a, cudaStream_t stream) {
+  DeviceInfo di;
+  la_status st = device_info(&di);
+  if (st != LA_OK) return st;
+  a.status = di.status;
+  a.num_sms = di.num_sms;
+  const int64_t BH = a.B * a.H;
+  const size_t state_elems = (size_t)a.dp * a.d;
+  if (a.n == 0) {
+    if (cudaMemsetAsync(a.mu_out, 0, BH * state_elems * sizeof(float), stream) != cudaSuccess ||
+        cudaMemsetAsync(a.nu_out, 0, BH * a.dp * sizeof(float), stream) != cudaSuccess)
+      return LA_ERR_CUDA;
+    return LA_OK;
+  }
+  const PathPlan pp = choose_path(a);
+  const SegmentPlan& plan = pp.plan;
+  float* ws = nullptr;
+  const size_t ws_floats = (size_t)BH * plan.nseg * (state_elems + a.dp);
+  cudaError_t e = ws_alloc(reinterpret_cast<void**>(&ws), ws_floats * sizeof(float), stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? LA_ERR_OUT_OF_MEMORY : LA_ERR_CUDA;
+  }
+  float* ws_state = ws;
+  float* ws_z = ws + (size_t)BH * plan.nseg * state_elems;
+  if (pp.tensor_cores && a.performer) e = tc_performer_state_only(a, stream, ws_state, ws_z, plan);
+  else if (pp.tensor_cores) e = tc_state_only(a, stream, ws_state, ws_z, plan);
+  else e = simt_state_only(a, stream, ws_state, ws_z, plan);
+  if (e == cudaSuccess)
+    e = segment_scan(ws_state, ws_z, a.mu_out, a.nu_out, BH, a.H, plan.nseg, plan.nseg,
+                     plan.seg_len, a.n, a.dp, a.d, a.decay, nullptr, stream, false);
+  const cudaError_t f = cudaFreeAsync(ws, stream);
+  if (e == cudaSuccess) e = f;
   return to_status(e);
 }
 
@@ -324,6 +380,49 @@ la_status la_forward(const la_tensor* q, const la_tensor* k, const la_tensor* v,
   la_status st = la::validate_forward(q, k, v, decay_a, feature_map, omega, causal, out, &a);
   if (st != LA_OK) return st;
   return la::run_forward(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+la_status la_forward_from_state(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                                const float* decay_a, la_feature_map feature_map,
+                                const la_tensor* omega, const float* mu0, const float* nu0,
+                                la_tensor* out, float* mu_out, float* nu_out, la_stream stream) {
+  la::FwdArgs a;
+  la_status st = la::validate_forward(q, k, v, decay_a, feature_map, omega, 1, out, &a);
+  if (st != LA_OK) return st;
+  if ((mu0 == nullptr) != (nu0 == nullptr) || (mu_out == nullptr) != (nu_out == nullptr))
+    return LA_ERR_INVALID_ARG;
+  const size_t BH = (size_t)(a.B * a.H);
+  const size_t sbytes = BH * (size_t)a.dp * a.d * sizeof(float);
+  const size_t zbytes = BH * (size_t)a.dp * sizeof(float);
+  if (mu0 && (!la::aligned16(mu0) || !la::aligned16(nu0))) return LA_ERR_INVALID_ARG;
+  if (mu_out && (!la::aligned16(mu_out) || !la::aligned16(nu_out))) return LA_ERR_INVALID_ARG;
+  if (mu0 && mu_out &&
+      (la::overlaps(mu0, sbytes, mu_out, sbytes) || la::overlaps(mu0, sbytes, nu_out, zbytes) ||
+       la::overlaps(nu0, zbytes, mu_out, sbytes) || la::overlaps(nu0, zbytes, nu_out, zbytes)))
+    return LA_ERR_INVALID_ARG;
+  a.init_state = mu0;
+  a.init_z = nu0;
+  a.mu_out = mu_out;
+  a.nu_out = nu_out;
+  return la::run_forward(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+la_status la_forward_state(const la_tensor* k, const la_tensor* v, const float* decay_a,
+                           la_feature_map feature_map, const la_tensor* omega, float* mu_out,
+                           float* nu_out, la_stream stream) {
+  if (!k || !v) return LA_ERR_INVALID_ARG;
+  // the checks of la_forward, with k standing in for q and for the output
+  la_tensor kk = *k;
+  la::FwdArgs a;
+  la_status st = la::validate_forward(&kk, k, v, decay_a, feature_map, omega, 1, &kk, &a);
+  if (st != LA_OK) return st;
+  if (!mu_out || !nu_out || !la::aligned16(mu_out) || !la::aligned16(nu_out))
+    return LA_ERR_INVALID_ARG;
+  a.q = nullptr;
+  a.out = nullptr;
+  a.mu_out = mu_out;
+  a.nu_out = nu_out;
+  return la::run_state(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 la_status la_forward_with_state(const la_tensor* q, const la_tensor* k, const la_tensor* v,

@@ -133,6 +133,8 @@ struct SimtParams {
   int nseg;
   float* ws_state;   // [BH][nseg][DP*D]
   float* ws_z;       // [BH][nseg][DP]
+  const float* init_state;   // causal: state entering token 0 [BH][DP*D], or nullptr
+  const float* init_z;       // [BH][DP]
   const float* tot_state;  // non-causal: [BH][DP*D]
   const float* tot_z;
   float* fin_state;  // causal single-segment: final state out (or nullptr)
@@ -218,9 +220,18 @@ simt_causal_output(SimtParams p) {
   const int64_t t_end = min(p.n, t_begin + p.seg_len);
   const float a = p.decay ? p.decay[bh % p.H] : 1.f;
   const float w = new_token_weight(a);
+  // the state entering the segment: its exclusive prefix from the scan
+  // (which starts from the initial state), or the initial state itself
+  const float* sS = nullptr;
+  const float* sz = nullptr;
   if (p.nseg > 1) {
-    const float* sS = p.ws_state + (bh * p.nseg + g) * (int64_t)(DP * D);
-    const float* sz = p.ws_z + (bh * p.nseg + g) * (int64_t)DP;
+    sS = p.ws_state + (bh * p.nseg + g) * (int64_t)(DP * D);
+    sz = p.ws_z + (bh * p.nseg + g) * (int64_t)DP;
+  } else if (p.init_state) {
+    sS = p.init_state + bh * (int64_t)(DP * D);
+    sz = p.init_z + bh * (int64_t)DP;
+  }
+  if (sS) {
     for (int e = threadIdx.x; e < DP * D; e += kThreads) S[e] = sS[e];
     for (int i = threadIdx.x; i < DP; i += kThreads) z[i] = sz[i];
   } else {
@@ -332,7 +343,8 @@ simt_noncausal_readout(SimtParams p) {
 __global__ void __launch_bounds__(256)
 segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z, int64_t H,
                     int nseg, int nagg, int64_t seg_len, int64_t n, int dpd, int dp,
-                    const float* decay, const float* seg_ld) {
+                    const float* decay, const float* seg_ld, const float* init_state,
+                    const float* init_z) {
   constexpr int kBatch = 8;  // aggregates loaded together to keep loads in flight
   // launched as a programmatic dependent of the launch that wrote the
   // aggregates (tensor-core paths): let the next launch start, then wait for
@@ -354,6 +366,7 @@ segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z
     stride = dp;
   }
   float acc = 0.f;  // state entering segment g
+  if (init_state) acc = e < dpd ? init_state[bh * dpd + e] : init_z[bh * dp + (e - dpd)];
   for (int g0 = 0; g0 < nseg; g0 += kBatch) {
     float agg[kBatch];
 #pragma unroll
@@ -412,6 +425,8 @@ cudaError_t run_simt_impl(const FwdArgs& a, cudaStream_t stream, float* ws_state
   p.nseg = plan.nseg;
   p.ws_state = ws_state;
   p.ws_z = ws_z;
+  p.init_state = a.init_state;
+  p.init_z = a.init_z;
   const int64_t BH = a.B * a.H;
   const dim3 grid((unsigned)plan.nseg, (unsigned)BH);
   const bool need_scan = !a.causal || plan.nseg > 1;
@@ -419,7 +434,8 @@ cudaError_t run_simt_impl(const FwdArgs& a, cudaStream_t stream, float* ws_state
     simt_segment_state<T, D, DP, PERF, TOK><<<grid, kThreads, smem, stream>>>(p);
     count_launches(1);
     err = segment_scan(ws_state, ws_z, tot_state, tot_z, BH, a.H, plan.nseg, plan.nseg,
-                       plan.seg_len, a.n, DP, D, a.decay, TOK ? a.ws_ld : nullptr, stream, false);
+                       plan.seg_len, a.n, DP, D, a.decay, TOK ? a.ws_ld : nullptr, stream, false,
+                       a.causal ? a.init_state : nullptr, a.causal ? a.init_z : nullptr);
     if (err != cudaSuccess) return err;
   }
   if (a.causal) {
@@ -473,7 +489,8 @@ cudaError_t dispatch_simt(const FwdArgs& a, cudaStream_t s, float* ws, float* wz
 cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* tot_z,
                          int64_t BH, int64_t H, int nseg, int nagg, int64_t seg_len, int64_t n,
                          int dp, int d, const float* decay, const float* seg_ld,
-                         cudaStream_t stream, bool dependent) {
+                         cudaStream_t stream, bool dependent, const float* init_state,
+                         const float* init_z) {
   const int dpd = dp * d;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)BH, (unsigned)((dpd + dp + 255) / 256));
@@ -485,9 +502,65 @@ cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* 
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, segment_scan_kernel, ws_state, ws_z, tot_state, tot_z,
-                                     H, nseg, nagg, seg_len, n, dpd, dp, decay, seg_ld);
+                                     H, nseg, nagg, seg_len, n, dpd, dp, decay, seg_ld,
+                                     init_state, init_z);
   count_launches(1);
   return e;
+}
+
+namespace {
+
+template <typename T, int D, int DP, bool PERF>
+cudaError_t run_simt_state(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                           const SegmentPlan& plan) {
+  using C = SimtCfg<D, DP, PERF>;
+  const size_t smem = C::bytes;
+  cudaError_t err = cudaFuncSetAttribute(simt_segment_state<T, D, DP, PERF, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  SimtParams p{};
+  p.k = a.k;
+  p.v = a.v;
+  p.decay = a.decay;
+  p.omega = a.omega;
+  p.H = a.H;
+  p.n = a.n;
+  p.seg_len = plan.seg_len;
+  p.nseg = plan.nseg;
+  p.ws_state = ws_state;
+  p.ws_z = ws_z;
+  const dim3 grid((unsigned)plan.nseg, (unsigned)(a.B * a.H));
+  simt_segment_state<T, D, DP, PERF, false><<<grid, kThreads, smem, stream>>>(p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_simt_state(const FwdArgs& a, cudaStream_t s, float* ws, float* wz,
+                                const SegmentPlan& pl) {
+  if (!a.performer) {
+    switch (a.d) {
+      case 32: return run_simt_state<T, 32, 32, false>(a, s, ws, wz, pl);
+      case 64: return run_simt_state<T, 64, 64, false>(a, s, ws, wz, pl);
+      case 128: return run_simt_state<T, 128, 128, false>(a, s, ws, wz, pl);
+    }
+    return cudaErrorInvalidValue;
+  }
+#define LA_PERF_CASE(DD, MM) \
+  if (a.d == DD && a.m == MM) return run_simt_state<T, DD, MM, true>(a, s, ws, wz, pl);
+  LA_PERF_CASE(32, 64) LA_PERF_CASE(32, 128) LA_PERF_CASE(32, 256)
+  LA_PERF_CASE(64, 64) LA_PERF_CASE(64, 128) LA_PERF_CASE(64, 256)
+  LA_PERF_CASE(128, 64) LA_PERF_CASE(128, 128) LA_PERF_CASE(128, 256)
+#undef LA_PERF_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t simt_state_only(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                            const SegmentPlan& plan) {
+  if (a.bf16) return dispatch_simt_state<__nv_bfloat16>(a, stream, ws_state, ws_z, plan);
+  return dispatch_simt_state<float>(a, stream, ws_state, ws_z, plan);
 }
 
 cudaError_t simt_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,

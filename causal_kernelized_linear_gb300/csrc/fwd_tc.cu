@@ -157,6 +157,8 @@ struct TcParams {
   float* ws_z;             // [BH][nseg][D]
   float* fin_state;        // final state (single-segment full launch) or nullptr
   float* fin_z;
+  const float* init_state; // state entering token 0 [BH][D*D], or nullptr (zero)
+  const float* init_z;     // [BH][D]
   int* status;
 };
 
@@ -842,11 +844,13 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   bool ok = x.nchunks > 0 && phi_k(0);
   if (DO_Q && ok) ok = phi_q_half<D, CEN>(x, 0, half, r, lane, lane_base, q_row_scale());
 
-  // ---- initial state: S_in = Σ_{j<g} a^{L·(g−1−j)}·A_j over the aggregates
-  // A_j of the earlier segments of this head (all of length L), written by
-  // the state-only launch that precedes this one — zero for the first segment
+  // ---- initial state: S_in = a^{L·g}·S_0 + Σ_{j<g} a^{L·(g−1−j)}·A_j over
+  // the caller's initial state S_0 (zero when none is given) and the
+  // aggregates A_j of the earlier segments of this head (all of length L),
+  // written by the state-only launch that precedes this one; in Horner form,
+  // S ← S_0, then S ← a^L·S + A_j for j = 0 … g−1
   if (ok) {
-    const bool have_in = FULL && x.g > 0;
+    const bool have_in = FULL && (x.g > 0 || p.init_state != nullptr);
     if (have_in) grid_dependency_wait();
     // segment j carries the state through it with aL (per-token decay: its
     // own total 2^{ws_ld})
@@ -854,8 +858,10 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
     const int64_t agg0 = x.bh * p.nseg;
     auto seg_fac = [&](int j) { return TOK ? exp2f(p.ws_ld[agg0 + j]) : aL; };
     float zin = 0.f;
-    if (have_in && srow && half == 0)
+    if (have_in && srow && half == 0) {
+      if (p.init_state) zin = p.init_z[x.bh * D + r];
       for (int j = 0; j < x.g; ++j) zin = seg_fac(j) * zin + p.ws_z[(agg0 + j) * D + r];
+    }
     // centered: tile and TMEM hold a^{64}·S_in (per-token: 2^{L_63}·S_in);
     // general: tile S_in, TMEM a^{cs}·S_in (per-token: 2^{L_{cs−1}}·S_in)
     const float alpha0 = CEN ? (TOK ? exp2f(tt.mid) : decay_pow_signed(a, 64)) : 1.f;
@@ -863,6 +869,18 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
     put_state([&](int hh, float* v) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = 0.f;
+                if (have_in && srow && p.init_state) {
+                  const float4* s4 = reinterpret_cast<const float4*>(
+                      p.init_state + x.bh * (int64_t)(D * D) + r * D + half * 64 + hh * 32);
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) {
+                    const float4 t = s4[e];
+                    v[4 * e] = t.x;
+                    v[4 * e + 1] = t.y;
+                    v[4 * e + 2] = t.z;
+                    v[4 * e + 3] = t.w;
+                  }
+                }
                 if (have_in && srow) {
                   const float* src = p.ws_state + agg0 * (int64_t)(D * D) + r * D + half * 64 + hh * 32;
 #pragma unroll 2
@@ -1162,6 +1180,8 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
   // the last segment's CTA of the full launch writes the final state
   p.fin_state = a.mu_out;
   p.fin_z = a.nu_out;
+  p.init_state = a.init_state;
+  p.init_z = a.init_z;
   if (plan.nseg > 1) {
     // aggregates of segments 0 … nseg−2 (nothing follows the last one)
     const dim3 grid_state((unsigned)BH, (unsigned)(plan.nseg - 1));
@@ -1187,6 +1207,36 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
   return e;
 }
 
+// The aggregate of every segment (the state-only launch over all of them).
+template <int D>
+cudaError_t run_tc_state(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                         const SegmentPlan& plan) {
+  using Cfg = TcCfg<D>;
+  cudaError_t e;
+  const int64_t BH = a.B * a.H;
+  CUtensorMap mq, mk, mv;
+  // the state-only launch never reads q; its map describes k
+  if ((e = tmap_rows(&mq, a.k, BH, a.n, D, kC)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mk, a.k, BH, a.n, D, kC)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mv, a.v, BH, a.n, D, kC)) != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc_forward_kernel<D, false, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  TcParams p{};
+  p.decay = a.decay;
+  p.H = a.H;
+  p.n = a.n;
+  p.seg_len = plan.seg_len;
+  p.nseg = plan.nseg;
+  p.ws_state = ws_state;
+  p.ws_z = ws_z;
+  p.status = a.status;
+  const dim3 grid((unsigned)BH, (unsigned)plan.nseg);
+  tc_forward_kernel<D, false, false><<<grid, kThreadsTc, Cfg::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool tc_forward_supported(const FwdArgs& a) {
@@ -1194,6 +1244,13 @@ bool tc_forward_supported(const FwdArgs& a) {
 }
 
 int64_t tc_segment_granule() { return kC; }
+
+cudaError_t tc_state_only(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                          const SegmentPlan& plan) {
+  if (a.d == 128) return run_tc_state<128>(a, stream, ws_state, ws_z, plan);
+  if (a.d == 64) return run_tc_state<64>(a, stream, ws_state, ws_z, plan);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t tc_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
                        float* tot_state, float* tot_z, const SegmentPlan& plan) {

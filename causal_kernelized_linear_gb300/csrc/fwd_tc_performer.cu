@@ -2,9 +2,10 @@
 // attention with the Performer positive random feature map, bf16 inputs,
 // fp32 state, d = 64, m ∈ {128, 256} features, no decay (a = 1).
 //
-// Method ("Efficient Transformers II" §2.1: φ(x) = exp(xω − ½‖x‖²)/√m;
-// "Efficient Transformers I" eq (6)–(9): the running sums μ, ν and the
-// causal readout o_j = q'_j·μ_j / q'_j·ν_j).  Per head and 128-token chunk
+// Method ("Linear Attention Research 2026", Performer random features:
+// φ(x) = exp(xω − ½‖x‖²)/√m; "Efficient Transformers II" §2.2 eq (6)–(9):
+// the running sums μ, ν, the causal readout o_j = q'_j·μ_j / q'_j·ν_j and the
+// non-causal D⁻¹(Q'(K'ᵀV)) of eq (6)).  Per head and 128-token chunk
 // (local t, s; cs valid rows) with state (S, z) at the chunk start:
 //   U = X·ω (the projection, on the tensor core, X = the raw q or k rows)
 //   φ(x)_i = 2^(u_i·log2 e − ½‖x‖²·log2 e − ½·log2 m)       (fp32 exponent)
@@ -126,6 +127,8 @@ struct PParams {
   float* tot_z;
   float* fin_state;        // causal: final state [BH][DP·64] or nullptr
   float* fin_z;
+  const float* init_state; // causal: state entering token 0 [BH][DP·64], or nullptr (zero)
+  const float* init_z;     // [BH][DP]
   float half_log2m;        // ½·log2 m
   int* status;
 };
@@ -519,13 +522,18 @@ __device__ __forceinline__ void role_rows(const PCtx& x, const PParams& p, int w
   };
 
   // ---- initial state: the prefix of the aggregates before this segment
-  // (causal, from the scan), the total (readout), or zero (state)
+  // (causal, from the scan, which starts from the caller's initial state),
+  // the caller's initial state (causal, first segment), the total
+  // (readout), or zero (state)
   {
     const float* srcS = nullptr;
     const float* srcZ = nullptr;
     if (MODE == kCausal && x.g > 0) {
       srcS = p.ws_state + (agg0 + x.g) * (int64_t)(DP * kD);
       srcZ = p.ws_z + (agg0 + x.g) * DP;
+    } else if (MODE == kCausal && p.init_state) {
+      srcS = p.init_state + x.bh * (int64_t)(DP * kD);
+      srcZ = p.init_z + x.bh * DP;
     } else if (MODE == kReadout) {
       srcS = p.tot_state + x.bh * (int64_t)(DP * kD);
       srcZ = p.tot_z + x.bh * DP;
@@ -813,6 +821,8 @@ cudaError_t run(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* w
   p.tot_z = tot_z;
   p.fin_state = a.mu_out;
   p.fin_z = a.nu_out;
+  p.init_state = a.causal ? a.init_state : nullptr;
+  p.init_z = a.causal ? a.init_z : nullptr;
   p.half_log2m = 0.5f * log2f((float)DP);
   p.status = a.status;
   const unsigned ubh = (unsigned)BH;
@@ -823,7 +833,8 @@ cudaError_t run(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* w
       e = launch<DP, kState>(p, dim3(ubh, (unsigned)(plan.nseg - 1)), false, mq, mk, mv, mw, stream);
       if (e != cudaSuccess) return e;
       e = segment_scan(ws_state, ws_z, nullptr, nullptr, a.B * a.H, a.H, plan.nseg, plan.nseg - 1,
-                       plan.seg_len, a.n, DP, kD, nullptr, nullptr, stream, true);
+                       plan.seg_len, a.n, DP, kD, nullptr, nullptr, stream, true, p.init_state,
+                       p.init_z);
       if (e != cudaSuccess) return e;
     }
     return launch<DP, kCausal>(p, dim3(ubh, (unsigned)plan.nseg), plan.nseg > 1, mq, mk, mv, mw,
@@ -838,12 +849,43 @@ cudaError_t run(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* w
   return launch<DP, kReadout>(p, dim3(ubh, (unsigned)plan.nseg), true, mq, mk, mv, mw, stream);
 }
 
+// The aggregate of every segment (the state launch over all of them).
+template <int DP>
+cudaError_t run_state(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                      const SegmentPlan& plan) {
+  const int64_t BH = a.B * a.H;
+  CUtensorMap mq, mk, mv, mw;
+  cudaError_t e;
+  // the state launch never reads q; its map describes k
+  if ((e = tmap_rows(&mq, a.k, BH, a.n, kD, kC)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mk, a.k, BH, a.n, kD, kC)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mv, a.v, BH, a.n, kD, kC)) != cudaSuccess) return e;
+  if ((e = tmap_matrix(&mw, a.omega, kD, DP, 64)) != cudaSuccess) return e;
+  PParams p{};
+  p.n = a.n;
+  p.seg_len = plan.seg_len;
+  p.nseg = plan.nseg;
+  p.ws_state = ws_state;
+  p.ws_z = ws_z;
+  p.half_log2m = 0.5f * log2f((float)DP);
+  p.status = a.status;
+  return launch<DP, kState>(p, dim3((unsigned)BH, (unsigned)plan.nseg), false, mq, mk, mv, mw,
+                            stream);
+}
+
 }  // namespace
 
 bool tc_performer_supported(const FwdArgs& a) {
   return a.bf16 && a.performer && a.d == kD && (a.m == 128 || a.m == 256) && a.decay == nullptr &&
          a.tok_decay == nullptr &&
          a.n >= kC;
+}
+
+cudaError_t tc_performer_state_only(const FwdArgs& a, cudaStream_t stream, float* ws_state,
+                                    float* ws_z, const SegmentPlan& plan) {
+  if (a.m == 256) return run_state<256>(a, stream, ws_state, ws_z, plan);
+  if (a.m == 128) return run_state<128>(a, stream, ws_state, ws_z, plan);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t tc_performer_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state,

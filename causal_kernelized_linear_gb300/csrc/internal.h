@@ -31,6 +31,8 @@ struct FwdArgs {
   bool causal;
   float* mu_out;        // optional final state [B,H,dp,d]
   float* nu_out;        // optional final state [B,H,dp]
+  const float* init_state;  // causal: state entering token 0 [B,H,dp,d], or nullptr (zero)
+  const float* init_z;      // [B,H,dp] (given together with init_state)
   int* status;          // device status word (bounded waits report here)
   int num_sms;
 };
@@ -84,6 +86,15 @@ cudaError_t simt_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state,
                          float* ws_z, float* tot_state, float* tot_z,
                          const SegmentPlan& plan);
 
+// The aggregate (the state reached from zero) of every segment of the plan,
+// into ws_state / ws_z [BH][nseg]: the state-only kernels of each family.
+cudaError_t simt_state_only(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                            const SegmentPlan& plan);
+cudaError_t tc_state_only(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
+                          const SegmentPlan& plan);
+cudaError_t tc_performer_state_only(const FwdArgs& a, cudaStream_t stream, float* ws_state,
+                                    float* ws_z, const SegmentPlan& plan);
+
 // tcgen05/TMA chunked forward (bf16, elu+1, causal, d ∈ {64, 128}, n ≥ 128).
 bool tc_forward_supported(const FwdArgs& a);
 int64_t tc_segment_granule();
@@ -111,13 +122,15 @@ cudaError_t tmap_matrix(CUtensorMap* m, const void* base, int64_t rows, int64_t 
 // Only the first nagg aggregates are read (nagg = nseg − 1 when the
 // last segment's aggregate was not computed: the exclusive prefixes do not
 // need it); the inclusive total (final state) is written when tot_state !=
-// nullptr and nagg == nseg.  `dependent` launches it as a programmatic
+// nullptr and nagg == nseg.  init_state / init_z ([BH][dp·d], [BH][dp], or
+// nullptr for zero) is the state entering segment 0.  `dependent` launches it as a programmatic
 // dependent of the preceding launch (which must be this library's kernel
 // that wrote the aggregates); the launch after it may then start early too.
 cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* tot_z,
                          int64_t BH, int64_t H, int nseg, int nagg, int64_t seg_len, int64_t n,
                          int dp, int d, const float* decay, const float* seg_ld,
-                         cudaStream_t stream, bool dependent);
+                         cudaStream_t stream, bool dependent, const float* init_state = nullptr,
+                         const float* init_z = nullptr);
 
 // la_forward with a fixed workspace of ws_floats floats, fetched through
 // get_ws only when the plan needs it, instead of stream-ordered allocations

@@ -123,6 +123,63 @@ la_status la_forward_with_state(const la_tensor* q, const la_tensor* k,
                                 float* nu_out, la_stream stream);
 
 /*
+ * la_forward_from_state — the causal forward of la_forward continued from a
+ * given state: the recurrence of eq (7)–(11) ("Efficient Transformers II"
+ * §2.2) starts from μ_{−1} = mu0, ν_{−1} = nu0 instead of zero, so that
+ * o_j = q'_j·μ_j / q'_j·ν_j with μ_j = a·μ_{j−1} + (1 − a)·k'_jᵀv_j (a = 1:
+ * the plain sums).  Running a sequence as two calls, the second from the
+ * first one's final state, gives the same outputs as one call.
+ *   mu0, nu0        device fp32 [B, H, d', d] and [B, H, d'], 16-byte
+ *                   aligned; both NULL for the zero state.
+ *   mu_out, nu_out  final state as in la_forward_with_state, or both NULL.
+ *                   Must not overlap mu0 / nu0.
+ * Other arguments and errors as la_forward with causal != 0 (one NULL of a
+ * pair, misalignment or overlap → LA_ERR_INVALID_ARG).  n = 0 copies the
+ * initial state to the final one.
+ */
+la_status la_forward_from_state(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                                const float* decay_a, la_feature_map feature_map,
+                                const la_tensor* omega, const float* mu0, const float* nu0,
+                                la_tensor* out, float* mu_out, float* nu_out, la_stream stream);
+
+/*
+ * la_forward_state — the state (μ_n, ν_n) that the recurrence of eq (7)–(11)
+ * reaches from zero over the whole sequence, without the outputs (no q, no
+ * o): for a = 1 these are the sums Σ_j k'_jᵀv_j and Σ_j k'_jᵀ of eq (6).
+ *   k, v            [B, H, n, d] as in la_forward.
+ *   mu_out, nu_out  device fp32 [B, H, d', d] and [B, H, d'], 16-byte
+ *                   aligned, written in full (zero for n = 0).
+ * Other arguments and errors as la_forward with causal != 0.
+ */
+la_status la_forward_state(const la_tensor* k, const la_tensor* v, const float* decay_a,
+                           la_feature_map feature_map, const la_tensor* omega, float* mu_out,
+                           float* nu_out, la_stream stream);
+
+/*
+ * la_shard_entering_state — the exchange step of a causal sequence split
+ * into consecutive shards (one per device): eq (10)–(11) unrolled over shard
+ * j, whose aggregate A_j (la_forward_state of its L_j tokens) and length
+ * are known to every device, give the state entering shard `rank`:
+ *   S_in(rank) = Σ_{j<rank} a^{L_{j+1} + … + L_{rank−1}}·A_j
+ * (ν likewise; a = 1 without a decay).  la_forward_from_state of the shard
+ * from S_in then equals la_forward of the whole sequence on those tokens.
+ *   gathered   device fp32, nshards consecutive blocks, block j = shard j's
+ *              μ [B, H, d', d] followed by its ν [B, H, d']; 4-byte aligned.
+ *   nshards    1 … 256; rank in [0, nshards).
+ *   shard_len  host int64 [nshards], tokens per shard (≥ 0).
+ *   decay_a    device [H] fp32, or NULL for a = 1.
+ *   B, H, dp, d  the state's shape (dp = d' = d for elu+1, m for Performer).
+ *   mu_in, nu_in  device fp32 [B, H, d', d] and [B, H, d'], written in full
+ *              (zero for rank 0).
+ * Errors: LA_ERR_INVALID_ARG (null pointer, bad count, rank or length,
+ * misalignment), LA_ERR_UNSUPPORTED (more than 256 shards), LA_ERR_CUDA.
+ */
+la_status la_shard_entering_state(const float* gathered, int nshards, int rank,
+                                  const int64_t* shard_len, const float* decay_a, int64_t B,
+                                  int64_t H, int dp, int d, float* mu_in, float* nu_in,
+                                  la_stream stream);
+
+/*
  * la_decode_step — one recurrent step for B·H heads ("Efficient Transformers
  * II" eq (10)–(11) followed by the causal readout of eq (9)), elu+1 map:
  *   k' = φ(k), μ ← a·μ + w·k'ᵀv, ν ← a·ν + w·k', o = q'μ / q'ν,
@@ -261,7 +318,7 @@ la_status la_get_last_device_status(la_stream stream);
  *   LA_ERR_UNSUPPORTED and queues nothing.  Causal requests that fit in one
  *   segment per head use no scratch at all.
  *   The first call on a device looks up the scratch array's device address
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   (cudaGetSymbolAddress) once; later calls reuse it.
  *   Every call overwrites the part of the scratch it uses and nothing needs
  *   to be zeroed, but all calls share the one array: calls that overlap on
  *   the GPU (e.g. on two streams) race on it and give wrong results.

@@ -105,6 +105,43 @@ def test_forward_with_state_needs_state_buffers(lib):
     assert st == B.LA_ERR_INVALID_ARG
 
 
+def test_state_entry_points_validate_before_any_launch(lib):
+    ok = _t()
+    P = ctypes.byref
+    fs = lib.la_forward_from_state
+    # an initial state must come as a pair, 16-byte aligned
+    assert fs(P(ok), P(ok), P(ok), None, 0, None, 0x40000, None, P(ok), None, None,
+              None) == B.LA_ERR_INVALID_ARG
+    assert fs(P(ok), P(ok), P(ok), None, 0, None, 0x40004, 0x50000, P(ok), None, None,
+              None) == B.LA_ERR_INVALID_ARG
+    # so must the final state; and it may not overlap the initial one
+    assert fs(P(ok), P(ok), P(ok), None, 0, None, 0x40000, 0x50000, P(ok), 0x60000, None,
+              None) == B.LA_ERR_INVALID_ARG
+    assert fs(P(ok), P(ok), P(ok), None, 0, None, 0x40000, 0x50000, P(ok), 0x40100, 0x70000,
+              None) == B.LA_ERR_INVALID_ARG
+    # the checks of la_forward still apply
+    assert fs(P(ok), P(_t(shape=(1, 2, 9, 64))), P(ok), None, 0, None, None, None, P(ok), None,
+              None, None) == B.LA_ERR_INVALID_ARG
+    st = lib.la_forward_state
+    assert st(None, P(ok), None, 0, None, 0x40000, 0x50000, None) == B.LA_ERR_INVALID_ARG
+    assert st(P(ok), P(ok), None, 0, None, None, 0x50000, None) == B.LA_ERR_INVALID_ARG
+    assert st(P(ok), P(ok), None, 0, None, 0x40008, 0x50000, None) == B.LA_ERR_INVALID_ARG
+    assert st(P(ok), P(_t(dtype=B.LA_F32)), None, 0, None, 0x40000, 0x50000,
+              None) == B.LA_ERR_INVALID_ARG
+    se = lib.la_shard_entering_state
+    lens = (ctypes.c_int64 * 3)(5, 6, 7)
+    assert se(0x40000, 3, 3, lens, None, 1, 2, 8, 8, 0x50000, 0x60000,
+              None) == B.LA_ERR_INVALID_ARG                      # rank past the last shard
+    assert se(None, 3, 1, lens, None, 1, 2, 8, 8, 0x50000, 0x60000,
+              None) == B.LA_ERR_INVALID_ARG
+    bad = (ctypes.c_int64 * 3)(5, -1, 7)
+    assert se(0x40000, 3, 1, bad, None, 1, 2, 8, 8, 0x50000, 0x60000,
+              None) == B.LA_ERR_INVALID_ARG                      # negative length
+    many = (ctypes.c_int64 * 300)()
+    assert se(0x40000, 300, 1, many, None, 1, 2, 8, 8, 0x50000, 0x60000,
+              None) == B.LA_ERR_UNSUPPORTED
+
+
 def test_decode_validation(lib):
     q = _t(shape=(4, 2, 1, 128))
     ok_state = 0x40000
