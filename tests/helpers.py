@@ -1,6 +1,9 @@
 """Shared helpers for the parity tests (test code only)."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -25,6 +28,12 @@ def head_rel_err(got, ref):
 def assert_parity(got, ref, tol, what=""):
     err = head_rel_err(got, ref)
     worst = float(err.max()) if err.size else 0.0
+    log = os.environ.get("LA_PARITY_LOG")
+    if log:
+        # one JSON line per check: the worst head's error and its bar
+        with open(log, "a") as f:
+            f.write(json.dumps({"check": what, "worst_head_err": worst, "tol": tol,
+                                "heads": int(err.size)}) + "\n")
     assert np.all(np.isfinite(err)), f"{what}: non-finite error"
     assert worst <= tol, f"{what}: worst head error {worst:.3e} > {tol:.1e}"
     return worst

@@ -101,9 +101,39 @@ def test_decode_workload_sampled_heads(cuda_device):
     assert_parity(sub(nu.cpu()).unsqueeze(-1), ref_nu[..., None], TOL_BF16, "final nu")
 
 
+def test_decode_workload_all_heads_at_checked_steps(cuda_device):
+    """Full-size decode, every one of the 8192 heads at steps 1, 2, 3, 512 and
+    1024: before a checked step the GPU's own state is widened to fp64 and the
+    oracle takes the same step from it, so the step's output and new state are
+    checked for all heads (the sampled-heads test above follows the whole
+    trajectory).  One step from the same state leaves only fp32 rounding in
+    the new state, so its bar is the fp32 one."""
+    w = W.DECODE
+    pre = W.decode_prefill_inputs(w)
+    g = to_cuda(pre, cuda_device)
+    _, mu, nu = cl.forward_with_state(g["q"], g["k"], g["v"], g["a"], "elu1")
+    out = torch.empty(w.B, w.H, w.d, device=cuda_device, dtype=torch.bfloat16)
+    checked = {0, 1, 2, 511, w.steps - 1}
+    for step in range(w.steps):
+        st = W.decode_step_inputs(w, step)
+        gs = to_cuda(st, cuda_device)
+        if step in checked:
+            torch.cuda.synchronize()
+            mu0, nu0 = mu.cpu(), nu.cpu()
+        cl.decode_step(mu, nu, gs["q"], gs["k"], gs["v"], g["a"], out=out)
+        if step in checked:
+            ref_o, ref_mu, ref_nu = oracle.decode_step(mu0, nu0, st["q"], st["k"], st["v"],
+                                                       pre["a"])
+            torch.cuda.synchronize()
+            # o is stored in bf16: its rounding is the bf16 bar
+            assert_parity(out.cpu(), ref_o, TOL_BF16, f"decode all heads, step {step + 1}: o")
+            assert_parity(mu.cpu(), ref_mu, TOL_F32, f"decode all heads, step {step + 1}: mu")
+            assert_parity(nu.cpu(), ref_nu, TOL_F32, f"decode all heads, step {step + 1}: nu")
+
+
 def test_performer_decode_workload_sampled_heads(cuda_device):
     """Full-size Performer decode (B=256, H=32, d=64, m=256): 512-token prefill
-    through la_forward_with_state, then 256 steps of la_decode_step_fm; the
+    through la_forward_with_state, then all 1024 steps of la_decode_step_fm; the
     oracle follows 32 seeded-random heads through the prefill and every step."""
     w = W.PERFORMER_DECODE
     pre = W.decode_prefill_inputs(w)
@@ -120,21 +150,21 @@ def test_performer_decode_workload_sampled_heads(cuda_device):
     a_sub = pre["a"][torch.from_numpy(hsel)]
     _, ref_mu, ref_nu = oracle.forward(sub(pre["q"]), sub(pre["k"]), sub(pre["v"]), a_sub,
                                        "performer", pre["omega"], return_state=True)
-    assert_parity(sub(mu.cpu()), ref_mu, TOL_BF16, "prefill state mu")
+    assert_parity(sub(mu.cpu()), ref_mu, TOL_BF16, "performer prefill state mu")
     out = torch.empty(w.B, w.H, w.d, device=cuda_device, dtype=torch.bfloat16)
-    for step in range(256):
+    for step in range(w.steps):
         st = W.decode_step_inputs(w, step)
         gs = to_cuda(st, cuda_device)
         cl.decode_step(mu, nu, gs["q"], gs["k"], gs["v"], g["a"], out=out,
                        feature_map="performer", omega=g["omega"])
         ref_o, ref_mu, ref_nu = oracle.decode_step(ref_mu, ref_nu, sub(st["q"]), sub(st["k"]),
                                                    sub(st["v"]), a_sub, "performer", pre["omega"])
-        if step in (0, 1, 2, 127) or step % 64 == 63:
+        if step in (0, 1, 2, 127, 511) or step % 64 == 63:
             assert_parity(sub(out.cpu()).unsqueeze(2), ref_o[:, :, None], TOL_BF16,
                           f"performer decode step {step}")
     torch.cuda.synchronize()
-    assert_parity(sub(mu.cpu()), ref_mu, TOL_BF16, "final mu")
-    assert_parity(sub(nu.cpu()).unsqueeze(-1), ref_nu[..., None], TOL_BF16, "final nu")
+    assert_parity(sub(mu.cpu()), ref_mu, TOL_BF16, "performer final mu")
+    assert_parity(sub(nu.cpu()).unsqueeze(-1), ref_nu[..., None], TOL_BF16, "performer final nu")
 
 
 # --- sweeps over shapes, maps, decays, ragged lengths --------------------------------------
