@@ -6,7 +6,8 @@ a ~ U[0.95, 0.9999], fp32 state) — the n ≥ 16K configuration at which the
 forward metric is quoted.  A step is one la_forward over the whole batch.
 Secondary lines (same JSON object, key "secondary") time the other
 workloads: elu+1 with decay at n=2048, Performer (m=256) causal and
-non-causal, the long shape with a per-token decay and input weight, and the
+non-causal, non-causal elu+1 (eq (6)) at the n=2048 and the long shape, the
+long shape with a per-token decay and input weight, the backward, and the
 recurrent decode step (B=256, H=32, d=128; and Performer, d=64, m=256).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -482,7 +483,8 @@ def run_ours(args, rank, world, dist):
     secondary = []
     if not args.no_secondary:
         for sw, causal, flush in ((W.ELU1_DECAY, True, True), (W.PERFORMER, False, True),
-                                  (W.PERFORMER, True, True)):
+                                  (W.PERFORMER, True, True), (W.ELU1_NONCAUSAL, False, True),
+                                  (W.LONG_NONCAUSAL, False, False)):
             r = bench_forward(cl, sw, causal, max(args.steps, 20), max(args.warmup, 3), stream,
                               flush_l2=flush, peaks=peaks)
             secs = r["avg_ms"] / 1e3
@@ -492,7 +494,8 @@ def run_ours(args, rank, world, dist):
                 "workload": sw.name, "causal": causal, "value": sw.B * sw.n / secs,
                 "unit": "tokens/s", "ms_per_step": r["avg_ms"], "tflops_alg": fl,
                 "frac_bf16_peak": fl / peaks["bf16_tflops"], "gbs_alg": gbs,
-                "frac_hbm": gbs / peaks["hbm_gbs"], "l2": "flushed between steps",
+                "frac_hbm": gbs / peaks["hbm_gbs"],
+                "l2": "flushed between steps" if flush else "inputs (805 MiB) larger than L2",
                 "launches_per_step": r["launches_per_step"]})
         tw = W.TOKEN_DECAY_LONG
         r = bench_token_decay(cl, tw, max(args.steps, 20), max(args.warmup, 3), stream)
@@ -560,6 +563,20 @@ def run_profile_case(case):
     if case == "forward-long-small":
         w = W.LONG
         inp = W.forward_inputs(w, n=32768)          # B1 H16 n32768 d128: 512 MiB of q, k, v, o
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        out = torch.empty_like(g["q"])
+        for _ in range(3):
+            cl.forward(g["q"], g["k"], g["v"], g["a"], "elu1", None, True, out=out)
+    elif case == "noncausal-long-small":
+        w = W.LONG_NONCAUSAL
+        inp = W.forward_inputs(w, n=32768)          # B1 H16 n32768 d128: 512 MiB of q, k, v, o
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        out = torch.empty_like(g["q"])
+        for _ in range(3):
+            cl.forward(g["q"], g["k"], g["v"], None, "elu1", None, False, out=out)
+    elif case == "elu1-decay":
+        w = W.ELU1_DECAY                             # B4 H8 n2048 d64 (the workload itself)
+        inp = W.forward_inputs(w)
         g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
         out = torch.empty_like(g["q"])
         for _ in range(3):
@@ -634,6 +651,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile-case", choices=["forward-long-small", "performer", "decode-small",
+                                               "noncausal-long-small", "elu1-decay",
                                                "performer-decode-small", "token-decay-small",
                                                "backward-small", "backward-long-small"],
                     default=None,

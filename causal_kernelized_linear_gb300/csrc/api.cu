@@ -197,7 +197,7 @@ struct PathPlan {
 
 PathPlan choose_path(const FwdArgs& a) {
   PathPlan pp;
-  pp.tensor_cores = tc_forward_supported(a) || tc_performer_supported(a);
+  pp.tensor_cores = tc_forward_supported(a) || tc_performer_supported(a) || tc_readout_supported(a);
   // tcgen05 path: one 512-thread CTA per SM, 128-token chunks; CUDA-core
   // path: two CTAs per SM, 32-token chunks
   pp.granule = pp.tensor_cores ? tc_segment_granule() : 32;
@@ -209,6 +209,8 @@ cudaError_t dispatch_forward(const FwdArgs& a, const PathPlan& pp, cudaStream_t 
                              float* ws_state, float* ws_z, float* tot_state, float* tot_z) {
   if (pp.tensor_cores && a.performer)
     return tc_performer_forward(a, stream, ws_state, ws_z, tot_state, tot_z, pp.plan);
+  if (pp.tensor_cores && !a.causal)
+    return tc_noncausal_forward(a, stream, ws_state, ws_z, tot_state, tot_z, pp.plan);
   if (pp.tensor_cores) return tc_forward(a, stream, ws_state, ws_z, tot_state, tot_z, pp.plan);
   return simt_forward(a, stream, ws_state, ws_z, tot_state, tot_z, pp.plan);
 }

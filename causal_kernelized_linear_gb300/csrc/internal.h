@@ -101,6 +101,14 @@ int64_t tc_segment_granule();
 cudaError_t tc_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* ws_z,
                        float* tot_state, float* tot_z, const SegmentPlan& plan);
 
+// tcgen05/TMA non-causal forward with the elu+1 map (bf16, d ∈ {64, 128},
+// n ≥ 128): the state-only launch over all segments, the scan's total (into
+// tot_state / tot_z), then the readout o = q'·S / q'·z.
+bool tc_readout_supported(const FwdArgs& a);
+cudaError_t tc_noncausal_forward(const FwdArgs& a, cudaStream_t stream, float* ws_state,
+                                 float* ws_z, float* tot_state, float* tot_z,
+                                 const SegmentPlan& plan);
+
 // tcgen05/TMA chunked forward with the Performer feature map (bf16, d = 64,
 // m ∈ {128, 256}, no decay, n ≥ 128; causal and non-causal).
 bool tc_performer_supported(const FwdArgs& a);

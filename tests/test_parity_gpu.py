@@ -197,12 +197,39 @@ CASES = [
     ("bf16", 64, "performer", 128, None, 4097, True),
     ("bf16", 64, "performer", 128, None, 300, False),
     ("bf16", 64, "performer", 256, None, 6000, False),
+    # tensor-core non-causal elu+1 (bf16, d ∈ {64, 128}, n ≥ 128): state-only
+    # launch over all segments, the scan's total, the tensor-core readout
+    ("bf16", 64, "elu1", 0, None, 128, False),
+    ("bf16", 128, "elu1", 0, None, 129, False),
+    ("bf16", 128, "elu1", 0, None, 1000, False),
+    ("bf16", 64, "elu1", 0, None, 4097, False),
+    ("bf16", 128, "elu1", 0, None, 20000, False),
     ("f32", 32, "elu1", 0, (0.9, 0.999), 1111, True),
     ("f32", 64, "elu1", 0, None, 517, False),
     ("f32", 128, "elu1", 0, (0.0, 1.0), 129, True),
     ("f32", 64, "performer", 128, None, 130, True),
     ("f32", 32, "performer", 64, None, 70, False),
 ]
+
+
+def test_noncausal_elu1_many_heads_one_segment(cuda_device):
+    # 160 heads: one segment per head, the readout's CTA count set by the heads
+    for d in (64, 128):
+        inp = W.make_forward_inputs(2, 80, 700, d, "bf16", "elu1", 0, None, seed=d + 1)
+        out = _run(inp, "elu1", False, cuda_device)
+        assert_parity(out, _ref(inp, "elu1", False), TOL_BF16, f"non-causal d={d}, 160 heads")
+
+
+def test_noncausal_elu1_exports_the_totals(cuda_device):
+    inp = W.make_forward_inputs(1, 4, 3000, 128, "bf16", "elu1", 0, None, seed=31)
+    g = to_cuda(inp, cuda_device)
+    out, mu, nu = cl.forward_with_state(g["q"], g["k"], g["v"], None, "elu1", None, False)
+    torch.cuda.synchronize()
+    ref, rmu, rnu = oracle.forward(inp["q"], inp["k"], inp["v"], None, "elu1", None, False,
+                                   return_state=True)
+    assert_parity(out, ref, TOL_BF16, "non-causal o")
+    assert_parity(mu, rmu, TOL_BF16, "non-causal μ_n")
+    assert_parity(nu, rnu, TOL_BF16, "non-causal ν_n")
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(str(x) for x in c))

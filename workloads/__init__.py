@@ -79,6 +79,13 @@ PERFORMER_DECODE = DecodeWorkload("performer_decode_B256_H32_d64_m256", 256, 32,
                                   steps=1024, decay=(0.9, 0.999), seed=5, feature_map="performer",
                                   m=256, qk_scale=64 ** -0.25)
 
+# Non-causal elu+1 (eq (6) has no decay): the shapes of the elu+1 decay
+# workload and of the long workload, each head reading out its totals.
+ELU1_NONCAUSAL = ForwardWorkload("elu1_noncausal_B4_H8_n2048_d64", 4, 8, 2048, 64, "bf16", "elu1",
+                                 seed=8, modes=("noncausal",))
+LONG_NONCAUSAL = ForwardWorkload("long_noncausal_B1_H16_n65536_d128", 1, 16, 65536, 128, "bf16",
+                                 "elu1", seed=9, modes=("noncausal",))
+
 FORWARD_WORKLOADS = {w.name: w for w in (TINY_FP32, ELU1_DECAY, PERFORMER, LONG)}
 
 
