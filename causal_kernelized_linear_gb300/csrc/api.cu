@@ -243,12 +243,15 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
   }
   const PathPlan pp = choose_path(a);
   const SegmentPlan& plan = pp.plan;
-  const bool need_ws = !a.causal || plan.nseg > 1;
+  // state slots per head: one per segment; the causal elu+1 tensor-core path
+  // keeps an initial state in one more, ahead of the segments' aggregates
+  const int slots = plan.nseg + ((a.init_state && tc_forward_supported(a)) ? 1 : 0);
+  const bool need_ws = !a.causal || slots > 1;
   // the inclusive total is an input of the non-causal readout; the causal
   // paths write the final state only when the caller asks for it
   const bool need_tot = !a.causal && (a.mu_out == nullptr);
   size_t ws_floats = 0;
-  if (need_ws) ws_floats += (size_t)BH * plan.nseg * (state_elems + a.dp);
+  if (need_ws) ws_floats += (size_t)BH * slots * (state_elems + a.dp);
   if (need_tot) ws_floats += (size_t)BH * (state_elems + a.dp);
   // per-token decay: the log2 decay of every segment, beside its aggregate
   const bool need_ld = a.tok_decay != nullptr && plan.nseg > 1;
@@ -262,14 +265,14 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
     }
   }
   float* ws_state = ws;
-  float* ws_z = ws ? ws + (size_t)BH * plan.nseg * state_elems : nullptr;
+  float* ws_z = ws ? ws + (size_t)BH * slots * state_elems : nullptr;
   float* tot_state = a.mu_out;
   float* tot_z = a.nu_out;
   if (need_tot) {
-    tot_state = ws + (size_t)BH * plan.nseg * (state_elems + a.dp);
+    tot_state = ws + (size_t)BH * slots * (state_elems + a.dp);
     tot_z = tot_state + (size_t)BH * state_elems;
   }
-  if (need_ld) a.ws_ld = ws + (size_t)BH * plan.nseg * (state_elems + a.dp);
+  if (need_ld) a.ws_ld = ws + (size_t)BH * slots * (state_elems + a.dp);
   cudaError_t e = dispatch_forward(a, pp, stream, ws_state, ws_z, tot_state, tot_z);
   if (ws) {
     cudaError_t f = cudaFreeAsync(ws, stream);

@@ -157,8 +157,9 @@ struct TcParams {
   float* ws_z;             // [BH][nseg][D]
   float* fin_state;        // final state (single-segment full launch) or nullptr
   float* fin_z;
-  const float* init_state; // state entering token 0 [BH][D*D], or nullptr (zero)
-  const float* init_z;     // [BH][D]
+  int init_slot;           // 1: slot 0 of every head's aggregates holds the state
+                           // entering token 0, segment g's aggregate is in slot
+                           // g + 1 (nseg + 1 slots per head); 0: no initial state
   int* status;
 };
 
@@ -767,8 +768,9 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   float* out_S = nullptr;
   float* out_z = nullptr;
   if (!FULL) {
-    out_S = p.ws_state + (x.bh * p.nseg + x.g) * (int64_t)(D * D);
-    out_z = p.ws_z + (x.bh * p.nseg + x.g) * (int64_t)D;
+    const int64_t slot = x.bh * (p.nseg + p.init_slot) + x.g + p.init_slot;
+    out_S = p.ws_state + slot * (int64_t)(D * D);
+    out_z = p.ws_z + slot * (int64_t)D;
   } else if (p.fin_state && x.g == p.nseg - 1) {
     out_S = p.fin_state + x.bh * (int64_t)(D * D);
     out_z = p.fin_z + x.bh * (int64_t)D;
@@ -847,21 +849,21 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   // ---- initial state: S_in = a^{L·g}·S_0 + Σ_{j<g} a^{L·(g−1−j)}·A_j over
   // the caller's initial state S_0 (zero when none is given) and the
   // aggregates A_j of the earlier segments of this head (all of length L),
-  // written by the state-only launch that precedes this one; in Horner form,
-  // S ← S_0, then S ← a^L·S + A_j for j = 0 … g−1
+  // written by the state-only launch that precedes this one.  In Horner
+  // form over the head's slots (S_0 first when given, then A_0, A_1, …):
+  // S ← 0, then S ← a^L·S + slot_j for the nin slots before this segment
   if (ok) {
-    const bool have_in = FULL && (x.g > 0 || p.init_state != nullptr);
+    const int nin = x.g + p.init_slot;
+    const bool have_in = FULL && nin > 0;
     if (have_in) grid_dependency_wait();
     // segment j carries the state through it with aL (per-token decay: its
     // own total 2^{ws_ld})
     const float aL = (have_in && !TOK) ? decay_pow(a, p.seg_len) : 0.f;
-    const int64_t agg0 = x.bh * p.nseg;
+    const int64_t agg0 = x.bh * (p.nseg + p.init_slot);
     auto seg_fac = [&](int j) { return TOK ? exp2f(p.ws_ld[agg0 + j]) : aL; };
     float zin = 0.f;
-    if (have_in && srow && half == 0) {
-      if (p.init_state) zin = p.init_z[x.bh * D + r];
-      for (int j = 0; j < x.g; ++j) zin = seg_fac(j) * zin + p.ws_z[(agg0 + j) * D + r];
-    }
+    if (have_in && srow && half == 0)
+      for (int j = 0; j < nin; ++j) zin = seg_fac(j) * zin + p.ws_z[(agg0 + j) * D + r];
     // centered: tile and TMEM hold a^{64}·S_in (per-token: 2^{L_63}·S_in);
     // general: tile S_in, TMEM a^{cs}·S_in (per-token: 2^{L_{cs−1}}·S_in)
     const float alpha0 = CEN ? (TOK ? exp2f(tt.mid) : decay_pow_signed(a, 64)) : 1.f;
@@ -869,22 +871,10 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
     put_state([&](int hh, float* v) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = 0.f;
-                if (have_in && srow && p.init_state) {
-                  const float4* s4 = reinterpret_cast<const float4*>(
-                      p.init_state + x.bh * (int64_t)(D * D) + r * D + half * 64 + hh * 32);
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) {
-                    const float4 t = s4[e];
-                    v[4 * e] = t.x;
-                    v[4 * e + 1] = t.y;
-                    v[4 * e + 2] = t.z;
-                    v[4 * e + 3] = t.w;
-                  }
-                }
                 if (have_in && srow) {
                   const float* src = p.ws_state + agg0 * (int64_t)(D * D) + r * D + half * 64 + hh * 32;
 #pragma unroll 2
-                  for (int j = 0; j < x.g; ++j) {
+                  for (int j = 0; j < nin; ++j) {
                     const float4* s4 = reinterpret_cast<const float4*>(src + j * (int64_t)(D * D));
                     const float f = seg_fac(j);
 #pragma unroll
@@ -1180,8 +1170,18 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
   // the last segment's CTA of the full launch writes the final state
   p.fin_state = a.mu_out;
   p.fin_z = a.nu_out;
-  p.init_state = a.init_state;
-  p.init_z = a.init_z;
+  p.init_slot = a.init_state ? 1 : 0;
+  if (a.init_state) {
+    // the initial state into slot 0 of every head's aggregates
+    const size_t nslot = (size_t)plan.nseg + 1;
+    e = cudaMemcpy2DAsync(ws_state, nslot * D * D * sizeof(float), a.init_state,
+                          (size_t)D * D * sizeof(float), (size_t)D * D * sizeof(float), (size_t)BH,
+                          cudaMemcpyDeviceToDevice, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpy2DAsync(ws_z, nslot * D * sizeof(float), a.init_z, (size_t)D * sizeof(float),
+                          (size_t)D * sizeof(float), (size_t)BH, cudaMemcpyDeviceToDevice, stream);
+    if (e != cudaSuccess) return e;
+  }
   if (plan.nseg > 1) {
     // aggregates of segments 0 … nseg−2 (nothing follows the last one)
     const dim3 grid_state((unsigned)BH, (unsigned)(plan.nseg - 1));
