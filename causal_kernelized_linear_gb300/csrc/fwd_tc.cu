@@ -114,7 +114,8 @@ enum {
   B_KFULL0, B_KFULL1, B_KFULL2, B_KEMPTY0, B_KEMPTY1, B_KEMPTY2,
   B_VFULL0, B_VFULL1, B_VFULL2, B_VEMPTY0, B_VEMPTY1, B_VEMPTY2,
   B_KREADY0, B_KREADY1, B_KREADY2,   // one per K stage: φ(K) may run a chunk ahead
-  B_QREADY, B_KPEMPTY, B_SREADY, B_SEMPTY, B_SCORES, B_PREADY, B_NUMFULL, B_NUMEMPTY,
+  B_QREADY0, B_QREADY1,              // one per Q stage: Q'' (centered) or Q' (general) ready
+  B_KPEMPTY, B_SREADY, B_SEMPTY, B_SCORES, B_PREADY, B_NUMFULL, B_NUMEMPTY,
   B_DSFULL, B_DSEMPTY, B_QPEMPTY, B_MMADONE, B_COUNT
 };
 static_assert(B_COUNT <= TcCfg<64>::NBAR, "barrier slots");
@@ -358,22 +359,30 @@ __device__ __forceinline__ void role_mma_out(const Ctx& x) {
   int* st = x.status;
   volatile int* ab = x.abort_flag;
   for (int c = 0; c < x.nchunks; ++c) {
-    const int ks = c % L::KST, vs = c % L::VST;
+    const int ks = c % L::KST, vs = c % L::VST, qs = c % L::QST;
     const uint32_t sK = x.sbase + L::k_off(ks);
     const uint32_t sV = x.sbase + L::v_off(vs);
+    // K-step k of a K-major [128 × D] operand tile (64-column atoms)
+    auto kstep = [](int k) { return (uint32_t)((k >> 2) * (kC * 128) + (k & 3) * 32); };
+    // centered: Q'' in place of the raw Q tile (A from shared memory);
+    // general: Q' in TMEM
+    const uint64_t dQ = smem_desc(x.sbase + L::q_off(qs), 16, 1024, kSwizzle128B);
     // scores = Q''K''ᵀ (centered; K'' in place of K) or Q'K'ᵀ (general; K'
-    // in place of K), A from TMEM; P(c−1) in the same columns must have been
-    // consumed by P·V of chunk c−1
+    // in place of K); P(c−1) in the same columns must have been consumed by
+    // P·V of chunk c−1
     if (!mbar_wait(&bar[B_KREADY0 + ks], (c / L::KST) & 1, st, ab)) break;
-    if (!mbar_wait(&bar[B_QREADY], c & 1, st, ab)) break;
+    if (!mbar_wait(&bar[B_QREADY0 + qs], (c / L::QST) & 1, st, ab)) break;
     if (c >= 1 && !mbar_wait(&bar[B_NUMFULL], (c - 1) & 1, st, ab)) break;
     tc_fence_after();
     {
       const uint64_t dK = smem_desc(sK, 16, 1024, kSwizzle128B);
 #pragma unroll
-      for (int k = 0; k < KD; ++k)
-        mma_ts(tmem + Cfg::TS, tmem + Cfg::TQ + k * 8,
-               desc_at(dK, (k >> 2) * (kC * 128) + (k & 3) * 32), idS, k > 0);
+      for (int k = 0; k < KD; ++k) {
+        if constexpr (CEN)
+          mma_ss(tmem + Cfg::TS, desc_at(dQ, kstep(k)), desc_at(dK, kstep(k)), idS, k > 0);
+        else
+          mma_ts(tmem + Cfg::TS, tmem + Cfg::TQ + k * 8, desc_at(dK, kstep(k)), idS, k > 0);
+      }
       mma_commit(&bar[B_SCORES]);
     }
     mma_commit(&bar[B_KEMPTY0 + ks]);
@@ -383,11 +392,17 @@ __device__ __forceinline__ void role_mma_out(const Ctx& x) {
     tc_fence_after();
 #pragma unroll
     for (int k = 0; k < KD; ++k) {
-      mma_ts(tmem + Cfg::TN, tmem + Cfg::TQ + k * 8, desc_at(dS, k * 2048), idN, k > 0);
-      mma_ts(tmem + Cfg::TR, tmem + Cfg::TQ + k * 8, desc_at(dZ, k * 32), idR, k > 0);
+      if constexpr (CEN) {
+        mma_ss(tmem + Cfg::TN, desc_at(dQ, kstep(k)), desc_at(dS, k * 2048), idN, k > 0);
+        mma_ss(tmem + Cfg::TR, desc_at(dQ, kstep(k)), desc_at(dZ, k * 32), idR, k > 0);
+      } else {
+        mma_ts(tmem + Cfg::TN, tmem + Cfg::TQ + k * 8, desc_at(dS, k * 2048), idN, k > 0);
+        mma_ts(tmem + Cfg::TR, tmem + Cfg::TQ + k * 8, desc_at(dZ, k * 32), idR, k > 0);
+      }
     }
     mma_commit(&bar[B_SEMPTY]);
-    mma_commit(&bar[B_QPEMPTY]);
+    // Q'' (its stage) or Q' (its TMEM columns) read by both of its products
+    mma_commit(&bar[CEN ? B_QEMPTY0 + qs : B_QPEMPTY]);
     // num += P·V ; den += P·1
     if (!mbar_wait(&bar[B_PREADY], c & 1, st, ab)) break;
     if (!mbar_wait(&bar[B_VFULL0 + vs], (c / L::VST) & 1, st, ab)) break;
@@ -456,9 +471,28 @@ __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, in
   volatile int* ab = x.abort_flag;
   const int qs = c % L::QST;
   if (!warp_wait(&bar[B_QFULL0 + qs], (c / L::QST) & 1, st, ab)) return false;
+  const uint32_t a2 = splat_bf16x2(a_row);
+  if constexpr (CEN) {
+    // Q'' in place of the raw tile (the A operand of the scores and of Q''·S);
+    // the output MMAs release the stage, so φ(Q) may run a stage ahead
+    uint8_t* qw = x.sm + L::q_off(qs);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint4* p4 = reinterpret_cast<uint4*>(qw + sw_chunk(kC, r, h, j));
+      uint4 u = *p4;
+      u.x = mul_bf16x2(elu1_bf16x2(u.x), a2);
+      u.y = mul_bf16x2(elu1_bf16x2(u.y), a2);
+      u.z = mul_bf16x2(elu1_bf16x2(u.z), a2);
+      u.w = mul_bf16x2(elu1_bf16x2(u.w), a2);
+      *p4 = u;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_QREADY0 + qs]);
+    return true;
+  }
   if (c >= 1 && !warp_wait(&bar[B_QPEMPTY], (c - 1) & 1, st, ab)) return false;
   const uint8_t* qt = x.sm + L::q_off(qs);
-  const uint32_t a2 = splat_bf16x2(a_row);
   uint32_t packed[32];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -475,7 +509,7 @@ __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, in
   tc_fence_before();
   __syncwarp();
   if (lane == 0) {
-    mbar_arrive(&bar[B_QREADY]);
+    mbar_arrive(&bar[B_QREADY0 + qs]);
     mbar_arrive(&bar[B_QEMPTY0 + qs]);   // raw Q tile no longer needed
   }
   return true;
@@ -897,6 +931,11 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
 
   for (int c = 0; ok && c < x.nchunks; ++c) {
     if (c + 1 < x.nchunks && !phi_k(c + 1)) break;
+    // centered: Q'' of the next chunk goes to its own stage, so it needs no
+    // product of this chunk and is formed before the state update
+    if (CEN && DO_Q && c + 1 < x.nchunks &&
+        !phi_q_half<D, CEN>(x, c + 1, half, r, lane, lane_base, q_row_scale()))
+      break;
     // ---- state update from the accumulated TMEM value v
     const int cs = chunk_len(c);
     const bool last = c + 1 == x.nchunks;
@@ -946,7 +985,7 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
       mbar_arrive(&bar[B_DSEMPTY]);
       if (FULL && !last) mbar_arrive(&bar[B_SREADY]);
     }
-    if (DO_Q && c + 1 < x.nchunks &&
+    if (!CEN && DO_Q && c + 1 < x.nchunks &&
         !phi_q_half<D, CEN>(x, c + 1, half, r, lane, lane_base, q_row_scale()))
       break;
   }
@@ -1088,9 +1127,10 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (i == B_SREADY || i == B_DSEMPTY) cnt = 4 * Cfg::HALVES;
       if (i >= B_KREADY0 && i <= B_KREADY2) cnt = KSplit<D, FULL>::ARRIVALS;
       // φ(Q) warps: 8 for D = 128 (the state warps), 4 for D = 64
-      if (i == B_QREADY) cnt = 4 * Cfg::HALVES;
-      // raw Q tiles are released by the φ(Q) warps
-      if (i == B_QEMPTY0 || i == B_QEMPTY1) cnt = 4 * Cfg::HALVES;
+      if (i == B_QREADY0 || i == B_QREADY1) cnt = 4 * Cfg::HALVES;
+      // Q stages are released by the φ(Q) warps (general: Q' goes to TMEM),
+      // or by the output MMAs that read Q'' in place (centered)
+      if (i == B_QEMPTY0 || i == B_QEMPTY1) cnt = (FULL && cen) ? 1 : 4 * Cfg::HALVES;
       mbar_init(&x.bar[i], cnt);
     }
     *x.abort_flag = 0;
