@@ -342,7 +342,7 @@ __device__ __forceinline__ void role_producer(const Ctx& x, const CUtensorMap* m
 // num += P·V and den += P·1.  State chain (warp 2): ΔS = K''ᵀV, Δz = K''ᵀ1.
 // Tiles read by both chains (K'' in the centered folding, V) are released
 // by a commit from each.
-template <int D, bool CEN>
+template <int D, bool CEN, bool QIP>
 __device__ __forceinline__ void role_mma_out(const Ctx& x) {
   using Cfg = TcCfg<D>;
   using L = Layout<D, true, CEN>;
@@ -364,8 +364,8 @@ __device__ __forceinline__ void role_mma_out(const Ctx& x) {
     const uint32_t sV = x.sbase + L::v_off(vs);
     // K-step k of a K-major [128 × D] operand tile (64-column atoms)
     auto kstep = [](int k) { return (uint32_t)((k >> 2) * (kC * 128) + (k & 3) * 32); };
-    // centered: Q'' in place of the raw Q tile (A from shared memory);
-    // general: Q' in TMEM
+    // QIP: Q'' in place of the raw Q tile (A from shared memory); otherwise
+    // Q'' (Q') in TMEM
     const uint64_t dQ = smem_desc(x.sbase + L::q_off(qs), 16, 1024, kSwizzle128B);
     // scores = Q''K''ᵀ (centered; K'' in place of K) or Q'K'ᵀ (general; K'
     // in place of K); P(c−1) in the same columns must have been consumed by
@@ -378,7 +378,7 @@ __device__ __forceinline__ void role_mma_out(const Ctx& x) {
       const uint64_t dK = smem_desc(sK, 16, 1024, kSwizzle128B);
 #pragma unroll
       for (int k = 0; k < KD; ++k) {
-        if constexpr (CEN)
+        if constexpr (QIP)
           mma_ss(tmem + Cfg::TS, desc_at(dQ, kstep(k)), desc_at(dK, kstep(k)), idS, k > 0);
         else
           mma_ts(tmem + Cfg::TS, tmem + Cfg::TQ + k * 8, desc_at(dK, kstep(k)), idS, k > 0);
@@ -392,7 +392,7 @@ __device__ __forceinline__ void role_mma_out(const Ctx& x) {
     tc_fence_after();
 #pragma unroll
     for (int k = 0; k < KD; ++k) {
-      if constexpr (CEN) {
+      if constexpr (QIP) {
         mma_ss(tmem + Cfg::TN, desc_at(dQ, kstep(k)), desc_at(dS, k * 2048), idN, k > 0);
         mma_ss(tmem + Cfg::TR, desc_at(dQ, kstep(k)), desc_at(dZ, k * 32), idR, k > 0);
       } else {
@@ -402,7 +402,7 @@ __device__ __forceinline__ void role_mma_out(const Ctx& x) {
     }
     mma_commit(&bar[B_SEMPTY]);
     // Q'' (its stage) or Q' (its TMEM columns) read by both of its products
-    mma_commit(&bar[CEN ? B_QEMPTY0 + qs : B_QPEMPTY]);
+    mma_commit(&bar[QIP ? B_QEMPTY0 + qs : B_QPEMPTY]);
     // num += P·V ; den += P·1
     if (!mbar_wait(&bar[B_PREADY], c & 1, st, ab)) break;
     if (!mbar_wait(&bar[B_VFULL0 + vs], (c / L::VST) & 1, st, ab)) break;
@@ -458,10 +458,12 @@ __device__ __forceinline__ void role_mma_state(const Ctx& x) {
 }
 
 // φ(Q) of chunk c for the 64 columns of half h of row r (TMEM lane r):
-// Q'' = a_row·φ(q) into TMEM (centered; Q' = φ(q) in the general folding),
-// then the raw Q tile is released.  Signals q_ready (the scores MMA may
-// start).  Returns false if a wait gave up.
-template <int D, bool CEN>
+// Q'' = a_row·φ(q) (centered; Q' = φ(q) in the general folding).  QIP
+// (per-head decay, centered): Q'' replaces the raw q tile in its stage,
+// which the output MMAs release; otherwise Q'' (Q') goes to TMEM and the
+// raw tile is released at once.  Signals the stage's q_ready (the scores MMA
+// may start).  Returns false if a wait gave up.
+template <int D, bool CEN, bool QIP>
 __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, int lane,
                                            uint32_t lane_base, float a_row) {
   using Cfg = TcCfg<D>;
@@ -472,7 +474,7 @@ __device__ __forceinline__ bool phi_q_half(const Ctx& x, int c, int h, int r, in
   const int qs = c % L::QST;
   if (!warp_wait(&bar[B_QFULL0 + qs], (c / L::QST) & 1, st, ab)) return false;
   const uint32_t a2 = splat_bf16x2(a_row);
-  if constexpr (CEN) {
+  if constexpr (QIP) {
     // Q'' in place of the raw tile (the A operand of the scores and of Q''·S);
     // the output MMAs release the stage, so φ(Q) may run a stage ahead
     uint8_t* qw = x.sm + L::q_off(qs);
@@ -878,7 +880,7 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   const float a_row_head = CEN ? decay_pow_signed(a, r - 63) : 1.f;
   auto q_row_scale = [&]() { return (CEN && TOK) ? ex2_f32(tt.lr - tt.mid) : a_row_head; };
   bool ok = x.nchunks > 0 && phi_k(0);
-  if (DO_Q && ok) ok = phi_q_half<D, CEN>(x, 0, half, r, lane, lane_base, q_row_scale());
+  if (DO_Q && ok) ok = phi_q_half<D, CEN, CEN && !TOK>(x, 0, half, r, lane, lane_base, q_row_scale());
 
   // ---- initial state: S_in = a^{L·g}·S_0 + Σ_{j<g} a^{L·(g−1−j)}·A_j over
   // the caller's initial state S_0 (zero when none is given) and the
@@ -931,10 +933,11 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
 
   for (int c = 0; ok && c < x.nchunks; ++c) {
     if (c + 1 < x.nchunks && !phi_k(c + 1)) break;
-    // centered: Q'' of the next chunk goes to its own stage, so it needs no
-    // product of this chunk and is formed before the state update
-    if (CEN && DO_Q && c + 1 < x.nchunks &&
-        !phi_q_half<D, CEN>(x, c + 1, half, r, lane, lane_base, q_row_scale()))
+    // centered, per-head decay: Q'' of the next chunk goes to its own stage,
+    // so it needs no product of this chunk and is formed before the state
+    // update (with a per-token decay Q'' stays in TMEM: measured faster)
+    if (CEN && !TOK && DO_Q && c + 1 < x.nchunks &&
+        !phi_q_half<D, CEN, CEN && !TOK>(x, c + 1, half, r, lane, lane_base, q_row_scale()))
       break;
     // ---- state update from the accumulated TMEM value v
     const int cs = chunk_len(c);
@@ -985,8 +988,8 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
       mbar_arrive(&bar[B_DSEMPTY]);
       if (FULL && !last) mbar_arrive(&bar[B_SREADY]);
     }
-    if (!CEN && DO_Q && c + 1 < x.nchunks &&
-        !phi_q_half<D, CEN>(x, c + 1, half, r, lane, lane_base, q_row_scale()))
+    if (!(CEN && !TOK) && DO_Q && c + 1 < x.nchunks &&
+        !phi_q_half<D, CEN, CEN && !TOK>(x, c + 1, half, r, lane, lane_base, q_row_scale()))
       break;
   }
   // state-only launch, per-token decay: the segment's total log2 decay
@@ -1001,7 +1004,7 @@ __device__ __forceinline__ void run_roles(const Ctx& x, const TcParams& p, const
   if (warp == 0) {
     if (lane == 0) role_producer<D, FULL, CEN>(x, mq, mk, mv);
   } else if (warp == 1) {
-    if (FULL && lane == 0) role_mma_out<D, CEN>(x);
+    if (FULL && lane == 0) role_mma_out<D, CEN, CEN && !TOK>(x);
   } else if (warp == 2) {
     if (lane == 0) role_mma_state<D, FULL, CEN>(x);
   } else if (warp >= 4 && warp < 8 && FULL) {
@@ -1030,7 +1033,7 @@ __device__ __forceinline__ void run_roles(const Ctx& x, const TcParams& p, const
         const TokChunk tk = tok_chunk(x, c, lane, pipe);
         ar = ex2_f32(pick4(tk.L, r >> 5) - __shfl_sync(0xffffffffu, tk.L[1], 31));
       }
-      if (!phi_q_half<D, CEN>(x, c, 0, r, lane, (uint32_t)(warp - 12) * 32, ar)) break;
+      if (!phi_q_half<D, CEN, CEN && !TOK>(x, c, 0, r, lane, (uint32_t)(warp - 12) * 32, ar)) break;
     }
   }
 }
@@ -1128,9 +1131,9 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (i >= B_KREADY0 && i <= B_KREADY2) cnt = KSplit<D, FULL>::ARRIVALS;
       // φ(Q) warps: 8 for D = 128 (the state warps), 4 for D = 64
       if (i == B_QREADY0 || i == B_QREADY1) cnt = 4 * Cfg::HALVES;
-      // Q stages are released by the φ(Q) warps (general: Q' goes to TMEM),
-      // or by the output MMAs that read Q'' in place (centered)
-      if (i == B_QEMPTY0 || i == B_QEMPTY1) cnt = (FULL && cen) ? 1 : 4 * Cfg::HALVES;
+      // Q stages are released by the φ(Q) warps (Q'' or Q' goes to TMEM),
+      // or by the output MMAs that read Q'' in place (centered, per-head decay)
+      if (i == B_QEMPTY0 || i == B_QEMPTY1) cnt = (FULL && cen && !TOK) ? 1 : 4 * Cfg::HALVES;
       mbar_init(&x.bar[i], cnt);
     }
     *x.abort_flag = 0;
