@@ -146,7 +146,7 @@ __device__ __forceinline__ void role_phi(const RCtx& x, int warp, int lane) {
   const int r = ((warp - 8) & 3) * 32 + lane;
   constexpr int NJ = D / 16;          // 16-byte chunks of a row per column half
   const int j0 = half * NJ;
-  const float* z = reinterpret_cast<const float*>(x.sm + Cfg::oZ);
+  const uint32_t zbase = x.sbase + Cfg::oZ;
   float* den = reinterpret_cast<float*>(x.sm + Cfg::oDEN);
   for (int c = 0; c < x.nchunks; ++c) {
     const int s = c % Cfg::NQ;
@@ -163,15 +163,17 @@ __device__ __forceinline__ void role_phi(const RCtx& x, int warp, int lane) {
       u.z = elu1_bf16x2(u.z);
       u.w = elu1_bf16x2(u.w);
       *reinterpret_cast<uint4*>(qt + off) = u;
-      const float* zc = z + jj * 8;
-      acc = fmaf(bf16lo_to_f32(u.x), zc[0], acc);
-      acc = fmaf(bf16hi_to_f32(u.x), zc[1], acc);
-      acc = fmaf(bf16lo_to_f32(u.y), zc[2], acc);
-      acc = fmaf(bf16hi_to_f32(u.y), zc[3], acc);
-      acc = fmaf(bf16lo_to_f32(u.z), zc[4], acc);
-      acc = fmaf(bf16hi_to_f32(u.z), zc[5], acc);
-      acc = fmaf(bf16lo_to_f32(u.w), zc[6], acc);
-      acc = fmaf(bf16hi_to_f32(u.w), zc[7], acc);
+      // z[8jj … 8jj+7]: the same address in every lane (a broadcast)
+      const float4 z0 = lds128f(zbase + jj * 32);
+      const float4 z1 = lds128f(zbase + jj * 32 + 16);
+      acc = fmaf(bf16lo_to_f32(u.x), z0.x, acc);
+      acc = fmaf(bf16hi_to_f32(u.x), z0.y, acc);
+      acc = fmaf(bf16lo_to_f32(u.y), z0.z, acc);
+      acc = fmaf(bf16hi_to_f32(u.y), z0.w, acc);
+      acc = fmaf(bf16lo_to_f32(u.z), z1.x, acc);
+      acc = fmaf(bf16hi_to_f32(u.z), z1.y, acc);
+      acc = fmaf(bf16lo_to_f32(u.w), z1.z, acc);
+      acc = fmaf(bf16hi_to_f32(u.w), z1.w, acc);
     }
     den[(s * 2 + half) * kC + r] = acc;
     fence_proxy_async_smem();   // Q' is read by the tensor core
