@@ -230,6 +230,41 @@ def bench_forward(cl, w, causal, steps, warmup, stream, flush_l2, peaks, want_e2
     return res
 
 
+def bench_shard_rank(cl, w: W.ForwardWorkload, nshards, steps, warmup, stream):
+    """One rank's work in the sequence-sharded causal forward of workload w
+    split into nshards equal shards, on this GPU: the aggregate of its shard
+    (la_forward_state), the state entering it from the gathered aggregates of
+    all shards (la_shard_entering_state) and its outputs from that state
+    (la_forward_from_state).  The all-gathers between the steps are not
+    timed (one GPU).  The last rank is timed (its entering state combines
+    every earlier shard)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    L = w.n // nshards
+    inp = W.forward_inputs(w)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    r = nshards - 1
+    q, k, v = (g[x][:, :, r * L:(r + 1) * L].contiguous() for x in ("q", "k", "v"))
+    dp = w.dprime
+    gathered = torch.zeros(nshards, w.B * w.H * (dp * w.d + dp), device=dev, dtype=torch.float32)
+    mu_a = gathered[r, :w.B * w.H * dp * w.d].view(w.B, w.H, dp, w.d)
+    nu_a = gathered[r, w.B * w.H * dp * w.d:].view(w.B, w.H, dp)
+    out = torch.empty_like(q)
+
+    def step():
+        cl.forward_state(k, v, g["a"], w.feature_map, g["omega"], mu_out=mu_a, nu_out=nu_a,
+                         stream=stream)
+        mu_in, nu_in = cl.shard_entering_state(gathered, r, [L] * nshards, w.B, w.H, dp, w.d,
+                                               g["a"], stream=stream)
+        cl.forward_from_state(q, k, v, mu_in, nu_in, g["a"], w.feature_map, g["omega"], out=out,
+                              stream=stream)
+
+    ms, launches = _time_steps(step, steps, warmup, stream, None, cl.launch_count)
+    avg_ms = statistics.mean(ms)
+    nbytes = w.B * w.H * L * w.d * 2 * 4
+    return {"ms": ms, "avg_ms": avg_ms, "tokens": w.B * L, "bytes": nbytes,
+            "launches_per_step": launches / steps}
+
+
 def bench_token_decay(cl, tw: W.TokenDecayWorkload, steps, warmup, stream):
     """la_forward_token_decay over the whole batch: per-token a and b [B,H,n]
     fp32.  Algorithmic bytes: q, k, v read and o written (bf16) plus a and b
@@ -519,6 +554,16 @@ def run_ours(args, rank, world, dist):
                 "value": r["tokens"] / secs, "unit": "tokens/s", "ms_per_step": r["avg_ms"],
                 "gbs_alg": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "steps": len(r["ms"]),
                 "launches_per_step": r["launches_per_step"]})
+        r = bench_shard_rank(cl, W.LONG, 2, max(args.steps, 20), max(args.warmup, 3), stream)
+        secs = r["avg_ms"] / 1e3
+        gbs = r["bytes"] / secs / 1e9
+        secondary.append({
+            "workload": W.LONG.name, "pass": "sequence-sharded forward, one rank of 2 (n/2 tokens): "
+            "state pass, entering state, forward from it; all-gathers not included (one GPU)",
+            "value": r["tokens"] / secs, "unit": "tokens/s (this rank)", "ms_per_step": r["avg_ms"],
+            "gbs_alg": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+            "l2": "inputs (403 MiB) larger than L2; no flush",
+            "launches_per_step": r["launches_per_step"]})
         for dw in (W.DECODE, W.PERFORMER_DECODE):
             d = bench_decode(cl, dw, stream)
             secs = d["avg_ms"] / 1e3
