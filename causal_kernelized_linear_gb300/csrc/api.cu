@@ -6,8 +6,12 @@
 
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
 #include <cstdint>
 #include <mutex>
 
@@ -18,6 +22,23 @@ std::atomic<uint64_t> g_launches{0};
 }  // namespace
 
 void count_launches(int k) { g_launches.fetch_add((uint64_t)k, std::memory_order_relaxed); }
+
+namespace {
+bool nvtx_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("LA_NVTX");
+    return e != nullptr && *e != '\0' && std::strcmp(e, "0") != 0;
+  }();
+  return on;
+}
+}  // namespace
+
+ApiRange::ApiRange(const char* name) : on_(nvtx_enabled()) {
+  if (on_) nvtxRangePushA(name);
+}
+ApiRange::~ApiRange() {
+  if (on_) nvtxRangePop();
+}
 
 namespace {
 
@@ -381,6 +402,7 @@ extern "C" {
 la_status la_forward(const la_tensor* q, const la_tensor* k, const la_tensor* v,
                      const float* decay_a, la_feature_map feature_map,
                      const la_tensor* omega, int causal, la_tensor* out, la_stream stream) {
+  la::ApiRange range_("la_forward");
   la::FwdArgs a;
   la_status st = la::validate_forward(q, k, v, decay_a, feature_map, omega, causal, out, &a);
   if (st != LA_OK) return st;
@@ -391,6 +413,7 @@ la_status la_forward_from_state(const la_tensor* q, const la_tensor* k, const la
                                 const float* decay_a, la_feature_map feature_map,
                                 const la_tensor* omega, const float* mu0, const float* nu0,
                                 la_tensor* out, float* mu_out, float* nu_out, la_stream stream) {
+  la::ApiRange range_("la_forward_from_state");
   la::FwdArgs a;
   la_status st = la::validate_forward(q, k, v, decay_a, feature_map, omega, 1, out, &a);
   if (st != LA_OK) return st;
@@ -415,6 +438,7 @@ la_status la_forward_from_state(const la_tensor* q, const la_tensor* k, const la
 la_status la_forward_state(const la_tensor* k, const la_tensor* v, const float* decay_a,
                            la_feature_map feature_map, const la_tensor* omega, float* mu_out,
                            float* nu_out, la_stream stream) {
+  la::ApiRange range_("la_forward_state");
   if (!k || !v) return LA_ERR_INVALID_ARG;
   // the checks of la_forward, with k standing in for q and for the output
   la_tensor kk = *k;
@@ -434,6 +458,7 @@ la_status la_forward_with_state(const la_tensor* q, const la_tensor* k, const la
                                 const float* decay_a, la_feature_map feature_map,
                                 const la_tensor* omega, int causal, la_tensor* out,
                                 float* mu_out, float* nu_out, la_stream stream) {
+  la::ApiRange range_("la_forward_with_state");
   la::FwdArgs a;
   la_status st = la::validate_forward(q, k, v, decay_a, feature_map, omega, causal, out, &a);
   if (st != LA_OK) return st;
@@ -448,6 +473,7 @@ la_status la_forward_token_decay(const la_tensor* q, const la_tensor* k, const l
                                  const float* decay_a, const float* weight_b,
                                  la_feature_map feature_map, const la_tensor* omega,
                                  la_tensor* out, float* mu_out, float* nu_out, la_stream stream) {
+  la::ApiRange range_("la_forward_token_decay");
   la::FwdArgs a;
   la_status st = la::validate_forward(q, k, v, nullptr, feature_map, omega, 1, out, &a);
   if (st != LA_OK) return st;
@@ -467,6 +493,7 @@ la_status la_backward(const la_tensor* q, const la_tensor* k, const la_tensor* v
                       const float* decay_a, la_feature_map feature_map, const la_tensor* omega,
                       const la_tensor* grad_out, la_tensor* dq, la_tensor* dk, la_tensor* dv,
                       float* da, la_stream stream) {
+  la::ApiRange range_("la_backward");
   la::FwdArgs f;
   // q, k, v, ω and the decay are checked as for the causal forward (with dq
   // standing in for the output)
@@ -586,6 +613,7 @@ la_status la_decode_step_token_decay(float* mu, float* nu, const la_tensor* q,
                                      const float* decay_a, const float* weight_b,
                                      la_feature_map feature_map, const la_tensor* omega,
                                      la_tensor* out, la_stream stream) {
+  la::ApiRange range_("la_decode_step_token_decay");
   la::DecodeArgs a;
   la_status st = la::validate_decode(mu, nu, q, k, v, feature_map, omega, out, &a);
   if (st != LA_OK) return st;
@@ -600,6 +628,7 @@ la_status la_decode_step_token_decay(float* mu, float* nu, const la_tensor* q,
 la_status la_decode_step_fm(float* mu, float* nu, const la_tensor* q, const la_tensor* k,
                             const la_tensor* v, const float* decay_a, la_feature_map feature_map,
                             const la_tensor* omega, la_tensor* out, la_stream stream) {
+  la::ApiRange range_("la_decode_step_fm");
   la::DecodeArgs a;
   la_status st = la::validate_decode(mu, nu, q, k, v, feature_map, omega, out, &a);
   if (st != LA_OK) return st;
@@ -611,6 +640,7 @@ la_status la_decode_step_fm(float* mu, float* nu, const la_tensor* q, const la_t
 la_status la_decode_step(float* mu, float* nu, const la_tensor* q, const la_tensor* k,
                          const la_tensor* v, const float* decay_a, la_tensor* out,
                          la_stream stream) {
+  la::ApiRange range_("la_decode_step");
   return la_decode_step_fm(mu, nu, q, k, v, decay_a, LA_FM_ELU1, nullptr, out, stream);
 }
 
@@ -629,6 +659,7 @@ const char* la_status_string(la_status status) {
 uint64_t la_launch_count(void) { return la::g_launches.load(std::memory_order_relaxed); }
 
 la_status la_selftest_wait_timeout(uint64_t limit_ns, la_stream stream) {
+  la::ApiRange range_("la_selftest_wait_timeout");
   if (limit_ns < 1000ull || limit_ns > 100000000ull) return LA_ERR_INVALID_ARG;
   la::DeviceInfo di;
   la_status st = la::device_info(&di);
@@ -637,6 +668,7 @@ la_status la_selftest_wait_timeout(uint64_t limit_ns, la_stream stream) {
 }
 
 la_status la_get_last_device_status(la_stream stream) {
+  la::ApiRange range_("la_get_last_device_status");
   la::DeviceInfo di;
   la_status st = la::device_info(&di);
   if (st != LA_OK) return st;

@@ -152,6 +152,21 @@ la_status forward_in_workspace(const la_tensor* q, const la_tensor* k, const la_
 // Records `k` kernel launches in the process-wide launch counter.
 void count_launches(int k);
 
+// An NVTX range named after a C entry point for the lifetime of the object,
+// when the environment variable LA_NVTX is set to a non-zero value (read
+// once); otherwise nothing.  Profilers that record NVTX show each call's
+// host-side span and the kernels it queued inside it.
+class ApiRange {
+ public:
+  explicit ApiRange(const char* name);
+  ~ApiRange();
+  ApiRange(const ApiRange&) = delete;
+  ApiRange& operator=(const ApiRange&) = delete;
+
+ private:
+  bool on_;
+};
+
 // One CTA of bounded waits on a barrier nothing signals (la_selftest_wait_timeout).
 cudaError_t selftest_wait(int* status, uint64_t limit_ns, cudaStream_t stream);
 

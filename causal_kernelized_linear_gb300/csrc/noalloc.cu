@@ -47,6 +47,7 @@ extern "C" la_status la_forward_noalloc(const la_tensor* q, const la_tensor* k,
                                         const la_tensor* v, const float* decay_a,
                                         la_feature_map feature_map, const la_tensor* omega,
                                         int causal, la_tensor* out, la_stream stream) {
+  la::ApiRange range_("la_forward_noalloc");
   return la::forward_in_workspace(q, k, v, decay_a, feature_map, omega, causal, out,
                                   scratch_on_current_device, kScratchFloats,
                                   reinterpret_cast<cudaStream_t>(stream));

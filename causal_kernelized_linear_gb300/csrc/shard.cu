@@ -44,6 +44,7 @@ la_status la_shard_entering_state(const float* gathered, int nshards, int rank,
                                   const int64_t* shard_len, const float* decay_a, int64_t B,
                                   int64_t H, int dp, int d, float* mu_in, float* nu_in,
                                   la_stream stream) {
+  la::ApiRange range_("la_shard_entering_state");
   if (!gathered || !shard_len || !mu_in || !nu_in) return LA_ERR_INVALID_ARG;
   if (nshards < 1 || rank < 0 || rank >= nshards || B < 1 || H < 1 || dp < 1 || d < 1)
     return LA_ERR_INVALID_ARG;

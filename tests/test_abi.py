@@ -233,3 +233,24 @@ def test_product_path_has_no_oracle_or_cpu_fallback():
         text = open(path, encoding="utf-8").read()
         assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), path
         assert "linattn_oracle" not in text and "liboracle" not in text, path
+
+
+def test_nvtx_ranges_do_not_change_results_of_host_checks(tmp_path):
+    # LA_NVTX=1 wraps every entry point in an NVTX range (read once per
+    # process, so a child process); without a profiler attached the calls
+    # behave as before
+    import subprocess
+    import sys
+    code = (
+        "import ctypes, causal_kernelized_linear_gb300 as cl\n"
+        "from causal_kernelized_linear_gb300 import _binding as B\n"
+        "lib = cl.load()\n"
+        "t = B.LaTensor(0x10000, B.LA_BF16, 1, 2, 8, 64)\n"
+        "print(lib.la_forward(None, ctypes.byref(t), ctypes.byref(t), None, 0, None, 1,"
+        " ctypes.byref(t), None))\n"
+        "print(lib.la_selftest_wait_timeout(999, None))\n")
+    env = dict(__import__("os").environ, LA_NVTX="1")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.split() == [str(B.LA_ERR_INVALID_ARG), str(B.LA_ERR_INVALID_ARG)]
