@@ -367,6 +367,31 @@ def bench_forward_e2e(cl, w, causal, inp, steps, warmup, stream):
             "overlap": "q, k, v and o copies on four streams overlap compute; two device buffer sets"}
 
 
+def bench_forward_host(cl, w, causal, inp, steps, warmup, stream):
+    """The same forward through la_forward_host: q, k, v in pinned host memory
+    go in and o comes back inside one library call per step (the library
+    cuts the sequence into pieces whose copies overlap the compute of the
+    others).  One event pair spans the timed calls."""
+    pin = {k: (x.pin_memory() if isinstance(x, torch.Tensor) else x) for k, x in inp.items()}
+    out = torch.empty_like(inp["q"]).pin_memory()
+
+    def step():
+        cl.forward_host(pin["q"], pin["k"], pin["v"], pin["a"], w.feature_map, pin["omega"],
+                        causal, out=out, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
 def bench_decode(cl, w: W.DecodeWorkload, stream, steps=None, distinct=32):
     """Prefill through la_forward_with_state, then `steps` decode steps (one
     launch each); per-step q, k, v cycle over `distinct` pre-generated sets."""
@@ -514,6 +539,13 @@ def run_ours(args, rank, world, dist):
                "h2d_bytes_per_step": main["e2e"]["h2d"], "d2h_bytes_per_step": main["e2e"]["d2h"],
                "pipelining": main["e2e"]["overlap"],
                "ms_per_step": 1e3 * e_s / args.steps}
+        # the same through the library's host-buffer entry point
+        h_ms = bench_forward_host(cl, w, True, W.forward_inputs(w), args.steps, args.warmup,
+                                  stream)
+        e2e["host_api"] = {"call": "la_forward_host", "value": w.B * w.n / (h_ms / 1e3),
+                           "unit": "tokens/s", "ms_per_step": h_ms,
+                           "h2d_bytes_per_step": main["e2e"]["h2d"],
+                           "d2h_bytes_per_step": main["e2e"]["d2h"]}
 
     secondary = []
     if not args.no_secondary:

@@ -7,6 +7,8 @@ Python face of liblinattn (C ABI in include/linattn.h).  The method
 * ``forward`` — o_j = q'_j·μ_j / q'_j·ν_j with μ_j = a·μ_{j−1} + (1−a)·k'_jᵀv_j,
   ν_j = a·ν_{j−1} + (1−a)·k'_jᵀ (plain sums for a = 1), or the non-causal
   D⁻¹(Q'(K'ᵀV)) of eq (6);
+* ``forward_host`` — the same on page-locked host buffers (the library copies them
+  in and out, overlapping the copies of some heads with the compute of others);
 * ``forward_with_state`` — the same, also returning the final (μ, ν);
 * ``forward_from_state`` — the causal form continued from a given (μ, ν);
 * ``forward_state`` — the (μ, ν) the causal recurrence reaches from zero,
@@ -24,13 +26,13 @@ All work runs in the library's CUDA kernels; PyTorch only allocates device
 memory and provides the stream.
 """
 from ._binding import (EXPORTED, LinAttnError, backward, decode_step, decode_step_token_decay,
-                       forward, forward_from_state, forward_state,
+                       forward, forward_from_state, forward_host, forward_state,
                        forward_token_decay, forward_with_state, last_device_status,
                        launch_count, library_path, load, selftest_wait_timeout,
                        shard_entering_state, status_string)
 from .build import build
 
-__all__ = ["forward", "forward_with_state", "forward_from_state", "forward_state",
+__all__ = ["forward", "forward_host", "forward_with_state", "forward_from_state", "forward_state",
            "shard_entering_state", "decode_step", "forward_token_decay", "backward",
            "decode_step_token_decay", "last_device_status", "status_string",
            "LinAttnError", "build", "load", "library_path", "launch_count",

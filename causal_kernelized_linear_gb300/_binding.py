@@ -33,7 +33,8 @@ _DT = {torch.bfloat16: LA_BF16, torch.float32: LA_F32}
 EXPORTED = ("la_forward", "la_forward_with_state", "la_decode_step", "la_status_string",
             "la_get_last_device_status", "la_launch_count", "la_selftest_wait_timeout",
             "la_decode_step_fm", "la_forward_token_decay", "la_decode_step_token_decay",
-            "la_backward", "la_forward_from_state", "la_forward_state", "la_shard_entering_state")
+            "la_backward", "la_forward_from_state", "la_forward_state", "la_shard_entering_state",
+            "la_forward_host")
 
 
 class LinAttnError(RuntimeError):
@@ -76,6 +77,8 @@ def load():
         lib.la_forward_with_state.argtypes = [P, P, P, vp, ctypes.c_int, P, ctypes.c_int, P,
                                               vp, vp, vp]
         lib.la_forward_with_state.restype = ctypes.c_int
+        lib.la_forward_host.argtypes = [P, P, P, vp, ctypes.c_int, P, ctypes.c_int, P, vp]
+        lib.la_forward_host.restype = ctypes.c_int
         lib.la_forward_from_state.argtypes = [P, P, P, vp, ctypes.c_int, P, vp, vp, P, vp, vp,
                                               vp]
         lib.la_forward_from_state.restype = ctypes.c_int
@@ -197,6 +200,48 @@ def forward_with_state(q, k, v, decay_a=None, feature_map="elu1", omega=None, ca
                                       nu_out.data_ptr(), _stream_handle(stream))
     _check("la_forward_with_state", st)
     return out, mu_out, nu_out
+
+
+def _need_pinned(name: str, t: torch.Tensor, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cpu" or not t.is_pinned():
+        raise ValueError(f"{name} must be a page-locked (pinned) CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+
+
+def forward_host(q, k, v, decay_a=None, feature_map="elu1", omega=None, causal=True, out=None,
+                 stream=None):
+    """la_forward_host: q, k, v [B,H,n,d] in pinned host memory (and decay_a [H],
+    omega [d, m] pinned too); the library copies them to the device, runs the
+    forward and copies o back into ``out`` (pinned, allocated when None),
+    overlapping the copies of some heads with the compute of others.  The
+    call is asynchronous on ``stream``: synchronise before reading ``out``."""
+    for nm, t in (("q", q), ("k", k), ("v", v)):
+        _need_pinned(nm, t)
+    if q.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, n, d]")
+    if out is None:
+        out = torch.empty_like(q).pin_memory()
+    _need_pinned("out", out)
+    fm = _FM[feature_map] if isinstance(feature_map, str) else int(feature_map)
+    dptr = None
+    if decay_a is not None:
+        _need_pinned("decay_a", decay_a, torch.float32)
+        dptr = decay_a.data_ptr()
+    om = None
+    if omega is not None:
+        _need_pinned("omega", omega)
+        om = _desc(omega, (1, 1, omega.shape[0], omega.shape[1]))
+    qd, kd, vd, od = (_desc(t, t.shape) for t in (q, k, v, out))
+    st = load().la_forward_host(ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), dptr, fm,
+                                ctypes.byref(om) if om is not None else None, int(bool(causal)),
+                                ctypes.byref(od), _stream_handle(stream))
+    _check("la_forward_host", st)
+    return out
 
 
 def _state_pair(name, mu, nu, shape_mu, shape_nu):

@@ -340,6 +340,201 @@ la_status run_state(FwdArgs& a, cudaStream_t stream) {
   return to_status(e);
 }
 
+// Copy streams of the host-buffer forward (one per input tensor and one for
+// the output), per device, created on first use and kept until exit.
+struct HostStreams {
+  cudaStream_t in[3] = {nullptr, nullptr, nullptr};
+  cudaStream_t out = nullptr;
+};
+HostStreams g_hs[kMaxDevices];
+
+cudaError_t host_streams(HostStreams* hs) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_hs[dev].out) {
+    HostStreams n;
+    cudaStream_t* all[4] = {&n.in[0], &n.in[1], &n.in[2], &n.out};
+    for (int i = 0; i < 4; ++i) {
+      if ((e = cudaStreamCreateWithFlags(all[i], cudaStreamNonBlocking)) != cudaSuccess) {
+        for (int j = 0; j < i; ++j) cudaStreamDestroy(*all[j]);
+        return e;
+      }
+    }
+    g_hs[dev] = n;
+  }
+  *hs = g_hs[dev];
+  return cudaSuccess;
+}
+
+// Page-locked host memory (cudaHostAlloc / cudaHostRegister).
+bool pinned_host(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost;
+}
+
+// la_forward on page-locked host buffers (validated into `a`, whose data
+// pointers are host pointers), in up to eight pieces whose copies overlap
+// the compute of the others:
+//   causal, n ≥ 2048: pieces along the sequence; piece g's rows of q, k, v
+//     go to dense device staging (one strided copy per tensor), its forward
+//     continues from the state piece g − 1 ended with (la_forward_from_state's
+//     path), and its rows of o go back with one strided copy;
+//   otherwise: groups of heads along B (or H when B = 1), each a forward of
+//     its own.
+// The q, k, v copies run on three copy-in streams and start at once (the
+// staging is taken on the first of them, so they need not wait for the work
+// already on `stream`); each piece's compute waits for its copies on
+// `stream`, its output copy waits for its compute on the copy-out stream,
+// and `stream` resumes after the last output copy, where the staging goes
+// back to the pool.
+la_status run_forward_host(FwdArgs& a, const float* decay_host, const void* omega_host,
+                           size_t omega_bytes, cudaStream_t stream) {
+  HostStreams hs;
+  if (host_streams(&hs) != cudaSuccess) return LA_ERR_CUDA;
+  const size_t esize = a.bf16 ? 2 : 4;
+  const int64_t BH = a.B * a.H;
+  const size_t row_bytes = (size_t)a.d * esize;
+  const size_t tensor_bytes = (size_t)BH * a.n * row_bytes;
+  const size_t decay_bytes = decay_host ? (size_t)a.H * sizeof(float) : 0;
+  const bool by_seq = a.causal && a.n >= 2048;
+  const size_t state_floats = (size_t)BH * ((size_t)a.dp * a.d + a.dp);
+  auto round16 = [](size_t x) { return (x + 15) & ~(size_t)15; };
+  const size_t states_bytes = by_seq ? 2 * round16(state_floats * sizeof(float)) : 0;
+  const size_t total =
+      4 * round16(tensor_bytes) + round16(omega_bytes) + round16(decay_bytes) + states_bytes;
+  char* stg = nullptr;
+  cudaError_t e = ws_alloc(reinterpret_cast<void**>(&stg), total, hs.in[0]);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? LA_ERR_OUT_OF_MEMORY : LA_ERR_CUDA;
+  }
+  char* dbuf[4];   // q, k, v, o staging
+  for (int i = 0; i < 4; ++i) dbuf[i] = stg + i * round16(tensor_bytes);
+  char* domega = stg + 4 * round16(tensor_bytes);
+  float* ddecay = reinterpret_cast<float*>(domega + round16(omega_bytes));
+  float* dstate[2];
+  dstate[0] = reinterpret_cast<float*>(reinterpret_cast<char*>(ddecay) + round16(decay_bytes));
+  dstate[1] = reinterpret_cast<float*>(reinterpret_cast<char*>(dstate[0]) +
+                                       round16(state_floats * sizeof(float)));
+  const char* hin[3] = {static_cast<const char*>(a.q), static_cast<const char*>(a.k),
+                        static_cast<const char*>(a.v)};
+  char* hout = static_cast<char*>(a.out);
+  la_status st = LA_OK;
+  auto ok = [&](cudaError_t r) {
+    if (r != cudaSuccess && st == LA_OK) st = LA_ERR_CUDA;
+    return r == cudaSuccess;
+  };
+  if (omega_bytes) ok(cudaMemcpyAsync(domega, omega_host, omega_bytes, cudaMemcpyHostToDevice, hs.in[0]));
+  if (decay_bytes) ok(cudaMemcpyAsync(ddecay, decay_host, decay_bytes, cudaMemcpyHostToDevice, hs.in[0]));
+  // the other copy-in streams may use the staging once it is allocated
+  cudaEvent_t ev_alloc = nullptr;
+  if (ok(cudaEventCreateWithFlags(&ev_alloc, cudaEventDisableTiming))) {
+    ok(cudaEventRecord(ev_alloc, hs.in[0]));
+    ok(cudaStreamWaitEvent(hs.in[1], ev_alloc, 0));
+    ok(cudaStreamWaitEvent(hs.in[2], ev_alloc, 0));
+    cudaEventDestroy(ev_alloc);
+  }
+  // pieces: rows [t0, t1) of every head (by_seq), or heads [u0, u1)
+  const int64_t outer = by_seq ? a.n : (a.B > 1 ? a.B : a.H);
+  int64_t npieces = by_seq ? std::min<int64_t>(8, a.n / 1024) : std::min<int64_t>(outer, 8);
+  int64_t piece_len = (outer + npieces - 1) / npieces;
+  if (by_seq) piece_len = (piece_len + 127) / 128 * 128;
+  npieces = (outer + piece_len - 1) / piece_len;
+  const size_t unit_bytes = by_seq ? row_bytes : (a.B > 1 ? (size_t)a.H : 1) * a.n * row_bytes;
+  for (int64_t gi = 0; gi < npieces && st == LA_OK; ++gi) {
+    const int64_t u0 = gi * piece_len, u1 = std::min(outer, u0 + piece_len);
+    cudaEvent_t ev_in[3] = {nullptr, nullptr, nullptr}, ev_comp = nullptr;
+    bool made = ok(cudaEventCreateWithFlags(&ev_comp, cudaEventDisableTiming));
+    for (int i = 0; i < 3 && made; ++i) made = ok(cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming));
+    if (!made) {
+      for (int i = 0; i < 3; ++i)
+        if (ev_in[i]) cudaEventDestroy(ev_in[i]);
+      if (ev_comp) cudaEventDestroy(ev_comp);
+      break;
+    }
+    // dense staging of the piece: [BH][u1 − u0 rows] (by_seq) or its heads
+    const size_t off = by_seq ? (size_t)BH * u0 * row_bytes : (size_t)u0 * unit_bytes;
+    const size_t width = (size_t)(u1 - u0) * unit_bytes;
+    for (int i = 0; i < 3; ++i) {
+      if (by_seq)
+        ok(cudaMemcpy2DAsync(dbuf[i] + off, width, hin[i] + (size_t)u0 * row_bytes,
+                             (size_t)a.n * row_bytes, width, (size_t)BH, cudaMemcpyHostToDevice,
+                             hs.in[i]));
+      else
+        ok(cudaMemcpyAsync(dbuf[i] + off, hin[i] + off, width, cudaMemcpyHostToDevice, hs.in[i]));
+      ok(cudaEventRecord(ev_in[i], hs.in[i]));
+      ok(cudaStreamWaitEvent(stream, ev_in[i], 0));
+    }
+    if (st == LA_OK) {
+      FwdArgs g = a;
+      g.q = dbuf[0] + off;
+      g.k = dbuf[1] + off;
+      g.v = dbuf[2] + off;
+      g.out = dbuf[3] + off;
+      g.omega = omega_bytes ? domega : nullptr;
+      g.decay = decay_bytes ? ddecay : nullptr;
+      g.mu_out = nullptr;
+      g.nu_out = nullptr;
+      g.init_state = nullptr;
+      g.init_z = nullptr;
+      if (by_seq) {
+        g.n = u1 - u0;
+        // the state piece gi − 1 ended with, into piece gi; every piece but
+        // the last leaves its own in the other buffer
+        const size_t zoff = (size_t)BH * a.dp * a.d;
+        if (gi > 0) {
+          g.init_state = dstate[(gi - 1) & 1];
+          g.init_z = dstate[(gi - 1) & 1] + zoff;
+        }
+        if (gi + 1 < npieces) {
+          g.mu_out = dstate[gi & 1];
+          g.nu_out = dstate[gi & 1] + zoff;
+        }
+      } else if (a.B > 1) {
+        g.B = u1 - u0;
+      } else {
+        g.H = u1 - u0;
+        g.decay = decay_bytes ? ddecay + u0 : nullptr;
+      }
+      const la_status fs = run_forward(g, stream);
+      if (fs != LA_OK) st = fs;
+    }
+    ok(cudaEventRecord(ev_comp, stream));
+    ok(cudaStreamWaitEvent(hs.out, ev_comp, 0));
+    if (by_seq)
+      ok(cudaMemcpy2DAsync(hout + (size_t)u0 * row_bytes, (size_t)a.n * row_bytes, dbuf[3] + off,
+                           width, width, (size_t)BH, cudaMemcpyDeviceToHost, hs.out));
+    else
+      ok(cudaMemcpyAsync(hout + off, dbuf[3] + off, width, cudaMemcpyDeviceToHost, hs.out));
+    for (int i = 0; i < 3; ++i) cudaEventDestroy(ev_in[i]);
+    cudaEventDestroy(ev_comp);
+  }
+  // the caller's stream resumes after the last copy out; the staging goes
+  // back to the pool after every use of it
+  cudaEvent_t ev_done = nullptr;
+  bool waited = false;
+  if (cudaEventCreateWithFlags(&ev_done, cudaEventDisableTiming) == cudaSuccess) {
+    waited = cudaEventRecord(ev_done, hs.out) == cudaSuccess &&
+             cudaStreamWaitEvent(stream, ev_done, 0) == cudaSuccess;
+    cudaEventDestroy(ev_done);
+  }
+  if (!waited) {
+    // order the release behind the copy streams the slow way
+    cudaStreamSynchronize(hs.out);
+    for (int i = 0; i < 3; ++i) cudaStreamSynchronize(hs.in[i]);
+    st = LA_ERR_CUDA;
+  }
+  if (cudaFreeAsync(stg, stream) != cudaSuccess && st == LA_OK) st = LA_ERR_CUDA;
+  return st;
+}
+
 }  // namespace
 
 // Forward into a workspace of `ws_floats` floats obtained from `get_ws`
@@ -407,6 +602,24 @@ la_status la_forward(const la_tensor* q, const la_tensor* k, const la_tensor* v,
   la_status st = la::validate_forward(q, k, v, decay_a, feature_map, omega, causal, out, &a);
   if (st != LA_OK) return st;
   return la::run_forward(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+la_status la_forward_host(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                          const float* decay_a, la_feature_map feature_map, const la_tensor* omega,
+                          int causal, la_tensor* out, la_stream stream) {
+  la::ApiRange range_("la_forward_host");
+  la::FwdArgs a;
+  la_status st = la::validate_forward(q, k, v, decay_a, feature_map, omega, causal, out, &a);
+  if (st != LA_OK) return st;
+  if (a.B * a.H * a.n * a.d == 0) return LA_OK;
+  // every host array must be page-locked (the copies are asynchronous)
+  if (!la::pinned_host(a.q) || !la::pinned_host(a.k) || !la::pinned_host(a.v) ||
+      !la::pinned_host(a.out) || (decay_a && !la::pinned_host(decay_a)) ||
+      (a.omega && !la::pinned_host(a.omega)))
+    return LA_ERR_INVALID_ARG;
+  const size_t omega_bytes = a.omega ? (size_t)a.d * a.m * (a.bf16 ? 2 : 4) : 0;
+  return la::run_forward_host(a, decay_a, a.omega, omega_bytes,
+                              reinterpret_cast<cudaStream_t>(stream));
 }
 
 la_status la_forward_from_state(const la_tensor* q, const la_tensor* k, const la_tensor* v,

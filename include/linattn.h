@@ -123,6 +123,28 @@ la_status la_forward_with_state(const la_tensor* q, const la_tensor* k,
                                 float* nu_out, la_stream stream);
 
 /*
+ * la_forward_host — la_forward on host buffers: q, k, v, out (and decay_a
+ * [H], omega when given) are page-locked host memory (cudaHostAlloc or
+ * cudaHostRegister).  The library copies the inputs to device memory it
+ * takes from its pool, runs la_forward, and copies o back; the heads are cut
+ * into up to eight groups (along B, or along H when B = 1) so that the copies
+ * of one group overlap the compute of the others.  The call is asynchronous:
+ * the input copies may start as soon as it is made (on the library's own
+ * copy stream, so the inputs must already be in host memory, not still being
+ * written by device work), while the compute and the copy of o back are
+ * ordered after the work already queued on `stream`, which resumes after the
+ * last copy.  The host buffers must stay valid, and the inputs unchanged,
+ * until then (synchronise `stream` before reading out).  The method
+ * and the other arguments are those of la_forward ("Efficient Transformers
+ * II" eq (6)–(11)).
+ * Errors: those of la_forward; LA_ERR_INVALID_ARG also when a buffer is not
+ * page-locked host memory.
+ */
+la_status la_forward_host(const la_tensor* q, const la_tensor* k, const la_tensor* v,
+                          const float* decay_a, la_feature_map feature_map, const la_tensor* omega,
+                          int causal, la_tensor* out, la_stream stream);
+
+/*
  * la_forward_from_state — the causal forward of la_forward continued from a
  * given state: the recurrence of eq (7)–(11) ("Efficient Transformers II"
  * §2.2) starts from μ_{−1} = mu0, ν_{−1} = nu0 instead of zero, so that

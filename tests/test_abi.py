@@ -142,6 +142,22 @@ def test_state_entry_points_validate_before_any_launch(lib):
               None) == B.LA_ERR_UNSUPPORTED
 
 
+def test_forward_host_validates_before_any_copy(lib):
+    ok = _t()
+    P = ctypes.byref
+    # the checks of la_forward come first; then every buffer must be
+    # page-locked host memory (on a machine without a GPU nothing is)
+    assert lib.la_forward_host(None, P(ok), P(ok), None, 0, None, 1, P(ok), None) == \
+        B.LA_ERR_INVALID_ARG
+    assert lib.la_forward_host(P(ok), P(_t(shape=(1, 2, 9, 64))), P(ok), None, 0, None, 1, P(ok),
+                               None) == B.LA_ERR_INVALID_ARG
+    w = _t(shape=(1, 2, 8, 48))
+    assert lib.la_forward_host(P(w), P(w), P(w), None, 0, None, 1, P(w), None) == \
+        B.LA_ERR_UNSUPPORTED
+    assert lib.la_forward_host(P(ok), P(ok), P(ok), None, 0, None, 1, P(ok), None) == \
+        B.LA_ERR_INVALID_ARG
+
+
 def test_decode_validation(lib):
     q = _t(shape=(4, 2, 1, 128))
     ok_state = 0x40000
