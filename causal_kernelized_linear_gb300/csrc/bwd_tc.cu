@@ -17,13 +17,14 @@
 // t1 − s), and pairs across it (weight cs, the term cs·a^{cs−1}(⟨S_c, M_c⟩ +
 // ⟨z_c, N_c⟩)) — so no position-weighted state is needed.
 //
-// Passes (each CTA loops over a contiguous range of (head, chunk) items; 128
-// threads, thread r = token row r = TMEM lane r; one thread issues the MMAs
-// and every product is waited for before the rows use it; the next item's
-// loads are issued as soon as the current item's tiles are consumed):
+// Passes (each CTA loops over a contiguous range of (head, chunk) items; 256
+// threads, two per token row r = TMEM lane r, each on one half of the row's
+// columns; one thread issues the MMAs and every product is waited for before
+// the rows use it; the next item's loads are issued as soon as the current
+// item's tiles are consumed):
 //   1. bt_state:  ΔS_c = K''ᵀV (K'' = w·a^{cs−1−s}φ(k)), Δz_c      → workspace
-//   2. scan:      S_c = exclusive decayed prefix of ΔS, in fp32 and as the
-//                 bf16 operand tile of pass 3                        (CUDA cores, float4)
+//   2. scan:      S_c = exclusive decayed prefix of ΔS, as the bf16 operand
+//                 tile of pass 3 (z_c in fp32)                       (CUDA cores, float4)
 //   3. bt_dq:     recompute o, den; ∂q; den, ρ; ΔM_c = Q''ᵀĜ (Q'' = a^{t+1}φ(q)), ΔN_c
 //   4. scan:      M_c = reverse exclusive decayed suffix of ΔM, as the bf16
 //                 operand tile of pass 5; the ∂a share across each chunk
@@ -40,6 +41,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <type_traits>
 
 namespace la {
 namespace {
@@ -47,7 +49,7 @@ namespace {
 using namespace tc;
 
 constexpr int kCb = 128;          // tokens per chunk
-constexpr int kThreadsB = 128;    // one thread per token row / TMEM lane
+constexpr int kThreadsB = 256;    // two threads per token row / TMEM lane (one per column half)
 
 template <int D>
 struct BtCfg {
@@ -70,8 +72,9 @@ struct BtCfg {
   static constexpr int oDEN = oRHO + kCb * 4;    // fp32 [128]
   static constexpr int oPW = oDEN + kCb * 4;     // fp32 a^k, k = 0..128
   static constexpr int oAW = oPW + 132 * 4;      // fp32 k·w·a^{k−1}, k = 0..128
-  static constexpr int oRED = oAW + 132 * 4;     // fp32 [4] warp partials
-  static constexpr int oBAR = oRED + 16;         // mbarriers: TMA, MMA
+  static constexpr int oRED = oAW + 132 * 4;     // fp32 [8] warp partials
+  static constexpr int oXCH = oRED + 32;         // fp32 [2][128] row partials of the two column halves
+  static constexpr int oBAR = oXCH + 2 * kCb * 4;   // mbarriers: TMA, MMA
   static constexpr int oMISC = oBAR + 16;        // TMEM slot, abort flag
   static constexpr int BYTES = oMISC + 16;
   // + alignment slack; at least half of the SM's shared memory, so that one
@@ -94,7 +97,7 @@ struct BtParams {
   int64_t H, n;
   int nch;              // chunks per head
   int64_t items;        // B·H·nch
-  float* S;             // [BH][nch][D*D]: ΔS_c, then S_c
+  float* S;             // [BH][nch][D*D]: ΔS_c (S_c itself only as its bf16 tile)
   float* z;             // [BH][nch][D]
   float* M;             // [BH][nch][D*D]: ΔM_c (M_c itself only as its bf16 tile)
   float* N;             // [BH][nch][D]: ΔN_c, then N_c
@@ -205,26 +208,38 @@ __device__ __forceinline__ bool wait_tiles(Bt& x) {
   return all;
 }
 
-// Applies f to every 16-byte chunk (8 bf16) of row r of a [128 × D] tile
-// (128-byte swizzle), in place.  The whole row is loaded before anything is
-// stored, so the loads are not held back behind the stores of the same row.
-template <int D, typename F>
-__device__ __forceinline__ void row_map(uint8_t* tile, int r, F f) {
-  constexpr int NC = D / 8;
+// Applies f to the 16-byte chunks (8 bf16) [c0, c0 + NC) of row r of a
+// [128 × D] tile (128-byte swizzle), in place: the whole row (NC = D/8, c0 = 0)
+// or one column half (NC = D/16, c0 = 0 or D/16).  Every chunk is loaded
+// before anything is stored, so the loads are not held back behind the stores.
+template <int D, int NC = D / 8, typename F>
+__device__ __forceinline__ void row_map(uint8_t* tile, int r, int c0, F f) {
   uint4 u[NC];
 #pragma unroll
-  for (int c = 0; c < NC; ++c) u[c] = *reinterpret_cast<const uint4*>(tile + sw_chunk(kCb, r, c >> 3, c & 7));
+  for (int i = 0; i < NC; ++i) {
+    const int c = c0 + i;
+    u[i] = *reinterpret_cast<const uint4*>(tile + sw_chunk(kCb, r, c >> 3, c & 7));
+  }
 #pragma unroll
-  for (int c = 0; c < NC; ++c) u[c] = f(u[c]);
+  for (int i = 0; i < NC; ++i) u[i] = f(u[i]);
 #pragma unroll
-  for (int c = 0; c < NC; ++c) *reinterpret_cast<uint4*>(tile + sw_chunk(kCb, r, c >> 3, c & 7)) = u[c];
+  for (int i = 0; i < NC; ++i) {
+    const int c = c0 + i;
+    *reinterpret_cast<uint4*>(tile + sw_chunk(kCb, r, c >> 3, c & 7)) = u[i];
+  }
+}
+
+// Column half hp of row r of a [128 × D] tile.
+template <int D, typename F>
+__device__ __forceinline__ void half_row_map(uint8_t* tile, int r, int hp, F f) {
+  row_map<D, D / 16>(tile, r, hp * (D / 16), f);
 }
 
 // φ = elu+1 in place on row r of a [128 × D] tile; rows ≥ cs become 0 (the
 // tensor map reads zeros past n, and φ(0) = 1 must not enter the sums).
 template <int D>
 __device__ __forceinline__ void phi_row_inplace(uint8_t* tile, int r, bool live) {
-  row_map<D>(tile, r, [live](uint4 u) {
+  row_map<D>(tile, r, 0, [live](uint4 u) {
     if (!live) return make_uint4(0u, 0u, 0u, 0u);
     return make_uint4(elu1_bf16x2(u.x), elu1_bf16x2(u.y), elu1_bf16x2(u.z), elu1_bf16x2(u.w));
   });
@@ -238,10 +253,11 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
   f[6] = bf16lo_to_f32(u.w); f[7] = bf16hi_to_f32(u.w);
 }
 
-// Row r of a [128 × D] tile scaled by sc in place, in fp32 with one rounding.
+// Column half hp of row r of a [128 × D] tile scaled by sc in place, in fp32
+// with one rounding.
 template <int D>
-__device__ __forceinline__ void scale_row_inplace(uint8_t* tile, int r, float sc) {
-  row_map<D>(tile, r, [sc](uint4 u) {
+__device__ __forceinline__ void scale_half_row_inplace(uint8_t* tile, int r, int hp, float sc) {
+  half_row_map<D>(tile, r, hp, [sc](uint4 u) {
     float f[8];
     unpack8(u, f);
 #pragma unroll
@@ -254,20 +270,20 @@ __device__ __forceinline__ void scale_row_inplace(uint8_t* tile, int r, float sc
 // to a contiguous row-major matrix in global memory, in two rounds of D/2
 // columns.  Rows go through shared memory (`stage`, (D/2 + 4)·D floats; the
 // padding spreads a warp's 16-byte writes over all banks) so that the global
-// stores are coalesced.  Every thread of the CTA calls it (it holds CTA
-// barriers).
+// stores are coalesced; the two threads of a row read alternate 32-column
+// steps of TMEM.  Every thread of the CTA calls it (it holds CTA barriers).
 template <int D>
 __device__ __forceinline__ void store_tmem_matrix(uint32_t tmem, uint32_t col0, float* stage,
                                                   float* __restrict__ dst) {
   constexpr int HC = D / 2, SR = HC + 4;
-  const int r = threadIdx.x;
+  const int r = threadIdx.x & (kCb - 1), part = threadIdx.x / kCb;
   float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
     if (r < D) {
       const uint32_t lane_base = (uint32_t)(r >> 5) * 32;
 #pragma unroll 1
-      for (int j0 = 0; j0 < HC; j0 += 32) {
+      for (int j0 = part * 32; j0 < HC; j0 += 64) {
         uint32_t v[32];
         tmem_ld32(tmem_addr(tmem, lane_base, col0 + hh * HC + j0), v);
         tmem_ld_wait();
@@ -362,7 +378,10 @@ __device__ __forceinline__ float cta_sum(float v, float* red) {
   __syncthreads();
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
-  return red[0] + red[1] + red[2] + red[3];
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < kThreadsB / 32; ++i) t += red[i];
+  return t;
 }
 
 __device__ __forceinline__ void head_decay(const BtParams& p, int64_t bh, float& a, float& w) {
@@ -419,7 +438,7 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   BtSetup<D>::run(x);
   float* pw = reinterpret_cast<float*>(x.sm + Cfg::oPW);
   float* aw = reinterpret_cast<float*>(x.sm + Cfg::oAW);
-  const int r = threadIdx.x;
+  const int r = threadIdx.x & (kCb - 1), hp = threadIdx.x / kCb;   // row, column half
   int64_t ib, ie;
   item_range(p.items, ib, ie);
   // the K and V tiles of item `it` (issued while the previous item finishes)
@@ -451,7 +470,7 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
       uint8_t* kt = x.sm + Cfg::oK;
       const bool live = r < cs;
       const uint32_t g2 = live ? splat_bf16x2(w * pw[cs - 1 - r]) : 0u;
-      row_map<D>(kt, r, [g2](uint4 u) {
+      half_row_map<D>(kt, r, hp, [g2](uint4 u) {
         return make_uint4(mul_bf16x2(elu1_bf16x2(u.x), g2), mul_bf16x2(elu1_bf16x2(u.y), g2),
                           mul_bf16x2(elu1_bf16x2(u.z), g2), mul_bf16x2(elu1_bf16x2(u.w), g2));
       });
@@ -495,29 +514,42 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
   float* pw = reinterpret_cast<float*>(x.sm + Cfg::oPW);
   float* aw = reinterpret_cast<float*>(x.sm + Cfg::oAW);
   float* red = reinterpret_cast<float*>(x.sm + Cfg::oRED);
+  float* xch = reinterpret_cast<float*>(x.sm + Cfg::oXCH);
   uint8_t* qt = x.sm + Cfg::oQ;
   uint8_t* gt = x.sm + Cfg::oG;
-  const int r = threadIdx.x, wq = r >> 5;
+  // thread (r, hp): token row r = TMEM lane r, column half hp (the 32-column
+  // blocks hp, hp + 2 of the [128 × 128] score tiles; columns [hp·D/2,
+  // (hp + 1)·D/2) of the [128 × D] ones); row sums meet in xch
+  const int r = threadIdx.x & (kCb - 1), hp = threadIdx.x / kCb, wq = r >> 5;
   const uint32_t lane_base = (uint32_t)wq * 32;
+  constexpr int HB = D / 2;
   // TMEM columns: X [0,128) | P, later E (bf16) [128,192) | Y, later U, then ∂q'
   // [192, 192+D) | PV, later ĜVᵀ, then ΔM [192+D, 320+D)
   constexpr uint32_t RX = 0, RP = 128, RY = 192, RN = 192 + D;
   int64_t ib, ie;
   item_range(p.items, ib, ie);
-  // the Q, K, V, ∂o tiles, the S_c operand tile and z_c of item `it` (issued
-  // while the previous item finishes)
-  auto issue = [&](int64_t it) {
+  // the Q, K, V, ∂o tiles, the S_c operand tile and z_c of item `it`, issued
+  // while the previous item finishes, each as soon as its region is free: V
+  // (arming the barrier for all of them), then K, then the rest
+  auto issue_v = [&](int64_t it) {
+    if (it >= ie) return;
+    arm_tiles(x, 4 * Cfg::TILE + Cfg::STILE + D * 4);
+    tile_load<D>(x, &map_v, Cfg::oV, (int)(it % p.nch) * kCb, (int)(it / p.nch));
+  };
+  auto issue_k = [&](int64_t it) {
+    if (it < ie) tile_load<D>(x, &map_k, Cfg::oK, (int)(it % p.nch) * kCb, (int)(it / p.nch));
+  };
+  auto issue_rest = [&](int64_t it) {
     if (it >= ie) return;
     const int ibh = (int)(it / p.nch), it0 = (int)(it % p.nch) * kCb;
-    arm_tiles(x, 4 * Cfg::TILE + Cfg::STILE + D * 4);
     tile_load<D>(x, &map_q, Cfg::oQ, it0, ibh);
-    tile_load<D>(x, &map_k, Cfg::oK, it0, ibh);
-    tile_load<D>(x, &map_v, Cfg::oV, it0, ibh);
     tile_load<D>(x, &map_g, Cfg::oG, it0, ibh);
     bulk_to(x, Cfg::oS, p.St + it * (int64_t)(D * D), Cfg::STILE);
     bulk_to(x, Cfg::oZ, p.z + it * D, D * 4);
   };
-  issue(ib);
+  issue_v(ib);
+  issue_k(ib);
+  issue_rest(ib);
   int64_t last_bh = -1;
   float a = 1.f, w = 1.f;   // the decay of head last_bh and its new-token weight
   for (int64_t item = ib; item < ie && !*x.abort_flag; ++item) {
@@ -534,8 +566,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     last_bh = bh;
     __syncthreads();
     if (!wait_tiles(x)) break;
-    phi_row_inplace<D>(x.sm + Cfg::oQ, r, live);
-    phi_row_inplace<D>(x.sm + Cfg::oK, r, live);
+    phi_row_inplace<D>(x.sm + (hp ? Cfg::oK : Cfg::oQ), r, live);   // φ(Q) | φ(K)
     rows_to_mma();
     // X = Q'K'ᵀ, Y = Q'·S_c
     if (threadIdx.x == 0) {
@@ -552,22 +583,21 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
       }
     }
     commit_mma(x);
-    // q'_r·z_c meanwhile
+    // q'_r·z_c over the column half meanwhile
     float qz = 0.f;
 #pragma unroll
-    for (int h = 0; h < Cfg::HALVES; ++h)
+    for (int i = 0; i < D / 16; ++i) {
+      const int cc = hp * (D / 16) + i;   // 16-byte chunk of the row
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(qt + sw_chunk(kCb, r, cc >> 3, cc & 7)), f);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float f[8];
-        unpack8(*reinterpret_cast<const uint4*>(qt + sw_chunk(kCb, r, h, j)), f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qz += f[e] * zc[h * 64 + j * 8 + e];
-      }
+      for (int e = 0; e < 8; ++e) qz += f[e] * zc[cc * 8 + e];
+    }
     if (!wait_mma(x)) break;
     // ---- rows 1: P = W ⊙ X (bf16, for P·V), den
     float den = 0.f;
 #pragma unroll 1
-    for (int b = 0; b < 4; ++b) {
+    for (int b = hp; b < 4; b += 2) {
       uint32_t pk[16];
       if (b > wq) {
 #pragma unroll
@@ -587,8 +617,9 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
       }
       tmem_st16(tmem_addr(x.tmem, lane_base, RP + b * 16), pk);
     }
-    den += pw[r + 1] * qz;
+    xch[hp * kCb + r] = den + pw[r + 1] * qz;
     rows_to_mma();
+    den = xch[r] + xch[kCb + r];
     if (threadIdx.x == 0) {
       const uint64_t dV = smem_desc(x.sbase + Cfg::oV, kCb * 128, 1024, kSwizzle128B);
       constexpr uint32_t idN = idesc_bf16_f32(128, D, false, true);
@@ -602,7 +633,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     const float inv_den = live ? 1.f / den : 0.f;
     float go = 0.f;
 #pragma unroll 1
-    for (int j0 = 0; j0 < D; j0 += 32) {
+    for (int j0 = hp * HB; j0 < (hp + 1) * HB; j0 += 32) {
       uint32_t nv[32], yv[32];
       tmem_ld32(tmem_addr(x.tmem, lane_base, RN + j0), nv);
       tmem_ld32(tmem_addr(x.tmem, lane_base, RY + j0), yv);
@@ -619,14 +650,17 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         }
       }
     }
-    const float rho = -go * inv_den;
-    srho[r] = rho;
-    scale_row_inplace<D>(gt, r, inv_den);
-    if (live) {
-      p.den[bh * p.n + t0 + r] = den;
-      p.rho[bh * p.n + t0 + r] = rho;
-    }
+    xch[hp * kCb + r] = go;
+    scale_half_row_inplace<D>(gt, r, hp, inv_den);
     rows_to_mma();
+    const float rho = -(xch[r] + xch[kCb + r]) * inv_den;
+    if (hp == 0) {
+      srho[r] = rho;
+      if (live) {
+        p.den[bh * p.n + t0 + r] = den;
+        p.rho[bh * p.n + t0 + r] = rho;
+      }
+    }
     // ĜVᵀ, U = Ĝ·S_cᵀ
     if (threadIdx.x == 0) {
       const uint64_t dG = smem_desc(x.sbase + Cfg::oG, 16, 1024, kSwizzle128B);
@@ -644,11 +678,12 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     }
     commit_mma(x);
     if (!wait_mma(x)) break;
+    issue_v(item + 1);   // V is consumed
     // ---- rows 3: E = W ⊙ (ĜVᵀ + ρ) (bf16, for E·K'), ∂a shares; ∂q' starts
     // as a^{t+1}·u_t, u_t = S_c ĝ_t + ρ_t z_c
     float da = 0.f;
 #pragma unroll 1
-    for (int b = 0; b < 4; ++b) {
+    for (int b = hp; b < 4; b += 2) {
       uint32_t pk[16];
       if (b > wq) {
 #pragma unroll
@@ -676,7 +711,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     }
     float qu = 0.f;
 #pragma unroll 1
-    for (int j0 = 0; j0 < D; j0 += 32) {
+    for (int j0 = hp * HB; j0 < (hp + 1) * HB; j0 += 32) {
       uint32_t uv[32];
       tmem_ld32(tmem_addr(x.tmem, lane_base, RY + j0), uv);
       tmem_ld_wait();
@@ -710,10 +745,11 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     tile_colsum<D>(qt, [&](int t) { return pw[t + 1] * srho[t]; },
                    reinterpret_cast<float*>(x.sm + Cfg::oS), p.N + item * D);
     if (!wait_mma(x)) break;
+    issue_k(item + 1);   // K is consumed
     // ---- rows 4: ∂q = ∂q' ⊙ min(φ(q), 1), staged; then Q'' = a^{t+1}φ(q) in place
     uint8_t* dq_stage = x.sm + Cfg::oST;
 #pragma unroll 1
-    for (int j0 = 0; j0 < D; j0 += 32) {
+    for (int j0 = hp * HB; j0 < (hp + 1) * HB; j0 += 32) {
       uint32_t dv[32];
       tmem_ld32(tmem_addr(x.tmem, lane_base, RY + j0), dv);
       tmem_ld_wait();
@@ -731,7 +767,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     store_staged_rows<D>(dq_stage, p.dq + (bh * p.n + t0) * D, cs);
     {
       const uint32_t s2 = splat_bf16x2(pw[r + 1]);
-      row_map<D>(qt, r, [s2](uint4 u) {
+      half_row_map<D>(qt, r, hp, [s2](uint4 u) {
         return make_uint4(mul_bf16x2(u.x, s2), mul_bf16x2(u.y, s2), mul_bf16x2(u.z, s2),
                           mul_bf16x2(u.w, s2));
       });
@@ -748,7 +784,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     }
     commit_mma(x);
     if (!wait_mma(x)) break;
-    issue(item + 1);   // every tile, z_c and the scratch are consumed
+    issue_rest(item + 1);   // Q, ∂o, the S_c tile (and scratch) and z_c are consumed
     store_tmem_matrix<D>(x.tmem, RN, reinterpret_cast<float*>(x.sm + Cfg::oST),
                          p.M + item * (int64_t)(D * D));
     tc_fence_before();
@@ -780,8 +816,10 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   float* red = reinterpret_cast<float*>(x.sm + Cfg::oRED);
   uint8_t* kt = x.sm + Cfg::oK;
   uint8_t* gt = x.sm + Cfg::oG;
-  const int r = threadIdx.x, wq = r >> 5;
+  // thread (r, hp): row r = TMEM lane r, column half hp (as in the ∂q pass)
+  const int r = threadIdx.x & (kCb - 1), hp = threadIdx.x / kCb, wq = r >> 5;
   const uint32_t lane_base = (uint32_t)wq * 32;
+  constexpr int HB = D / 2;
   // TMEM columns: Xᵀ, later K'M [0,128) | Pᵀ [128,192) | Eᵀ [192,256) (both
   // later V·Mᵀ [128, 128+D)) | ∂v [256, 256+D) | ĜᵀV... ĜVᵀᵀ, later ∂k' [384, 512)
   constexpr uint32_t RX = 0, RP = 128, RE = 192, RF = 128, RV = 256, RK = 384;
@@ -827,8 +865,10 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     __syncthreads();   // the previous item's tables are no longer read
     // (the share of the pairs across the chunk comes from the reverse scan)
     float da = 0.f;
-    srho[r] = rho_n;
-    sden[r] = den_n;
+    if (hp == 0) {
+      srho[r] = rho_n;
+      sden[r] = den_n;
+    }
     if (bh != last_bh) {
       head_decay(p, bh, a, w);
       head_tables(a, w, pw, aw);
@@ -836,11 +876,10 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     last_bh = bh;
     __syncthreads();
     if (!wait_tiles(x)) break;
-    phi_row_inplace<D>(x.sm + Cfg::oQ, r, live);
-    phi_row_inplace<D>(kt, r, live);
+    phi_row_inplace<D>(hp ? kt : x.sm + Cfg::oQ, r, live);   // φ(Q) | φ(K)
     {   // ĝ = g / den in place
       const float inv = live ? 1.f / sden[r] : 0.f;
-      scale_row_inplace<D>(gt, r, inv);
+      scale_half_row_inplace<D>(gt, r, hp, inv);
     }
     rows_to_mma();
     // Xᵀ = K'Q'ᵀ, (ĜVᵀ)ᵀ = VĜᵀ
@@ -861,7 +900,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     if (!wait_mma(x)) break;
     // ---- rows 1 (thread s = r): Pᵀ_st = W_ts x_ts, Eᵀ_st = W_ts(ĝ_t·v_s + ρ_t), t ≥ s
 #pragma unroll 1
-    for (int b = 0; b < 4; ++b) {
+    for (int b = hp; b < 4; b += 2) {
       uint32_t pk[16], ek[16];
       if (b < wq) {   // every t of the block is before every s of the warp
 #pragma unroll
@@ -934,7 +973,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     uint8_t* stage = x.sm + Cfg::oST;
     const float fut = live ? w * pw[cs - 1 - r] : 0.f;
 #pragma unroll 1
-    for (int j0 = 0; j0 < D; j0 += 32) {
+    for (int j0 = hp * HB; j0 < (hp + 1) * HB; j0 += 32) {
       uint32_t va[32], vb[32];
       tmem_ld32(tmem_addr(x.tmem, lane_base, RV + j0), va);
       tmem_ld32(tmem_addr(x.tmem, lane_base, RX + j0), vb);
@@ -954,7 +993,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     {
       float kfut = 0.f;
 #pragma unroll 1
-      for (int j0 = 0; j0 < D; j0 += 32) {
+      for (int j0 = hp * HB; j0 < (hp + 1) * HB; j0 += 32) {
         uint32_t va[32], vb[32];
         tmem_ld32(tmem_addr(x.tmem, lane_base, RK + j0), va);
         tmem_ld32(tmem_addr(x.tmem, lane_base, RF + j0), vb);
@@ -990,14 +1029,14 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 // The chunk scans, four consecutive state elements per thread (the matrix
 // part [D' × D], then the vector part [D']):
 //   forward (S, z): out[c] = acc, acc ← a^{cs_c}·acc + ΔS_c — the state
-//     entering chunk c, written in place in fp32 and, for the matrix part,
-//     as the bf16 operand tile of the ∂q pass;
+//     entering chunk c; the matrix part goes only to its bf16 operand tile
+//     (for the ∂q pass), the vector part z_c stays fp32 in place;
 //   reverse (M, N): walking down, out[c] = acc, acc ← ΔM_c + a^{cs_c}·acc —
-//     the adjoint after chunk c; the matrix part goes only to its bf16
-//     operand tile (for the ∂k/∂v pass), the vector part N_c stays fp32 in
-//     place.  With ∂a, every thread also sums its part of the pairs across
-//     the chunks, Σ_c cs_c·a^{cs_c−1}(⟨S_c, M_c⟩ + ⟨z_c, N_c⟩), from the fp32
-//     S_c and z_c of the forward scan; each warp stores one total in da_out.
+//     the adjoint after chunk c, stored the same way (M_c as the operand tile
+//     of the ∂k/∂v pass, N_c in fp32).  With ∂a, every thread also sums its
+//     part of the pairs across the chunks, Σ_c cs_c·a^{cs_c−1}(⟨S_c, M_c⟩ +
+//     ⟨z_c, N_c⟩), with S_c read from its bf16 operand tile (the value the
+//     ∂q pass uses) and z_c in fp32; each warp stores one total in da_out.
 // The operand tile is [D' × 64]-column blocks with the 128-byte swizzle, the
 // layout the tensor-core passes copy into shared memory as is.  The next
 // chunks' values are loaded before the current results are stored, so that
@@ -1005,79 +1044,112 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 template <int D, bool REV>
 __global__ void __launch_bounds__(256, 2)
 bt_chunk_scan(float* __restrict__ S, float* __restrict__ z, __nv_bfloat16* __restrict__ tiles,
-              const float* __restrict__ fS, const float* __restrict__ fz, float* __restrict__ da_out,
+              const __nv_bfloat16* __restrict__ fS, const float* __restrict__ fz, float* __restrict__ da_out,
               int da_parts, int64_t H, int nch, int64_t n, const float* __restrict__ decay) {
   constexpr int DPD = D * D;
+  static_assert(DPD % 1024 == 0, "a block holds matrix elements only or vector elements only");
   const int64_t bh = blockIdx.x;
-  const int e4 = (blockIdx.y * 256 + threadIdx.x) * 4;
-  const bool valid = e4 < DPD + D;              // whole warps are valid or not, except for d = 64
-  const bool mat = e4 < DPD;
   const float a = decay ? decay[bh % H] : 1.f;
   const float a_full = decay_pow(a, kCb);
-  const int64_t off = mat ? bh * nch * (int64_t)DPD + e4 : bh * nch * (int64_t)D + (e4 - DPD);
-  float* base = (mat ? S : z) + off;
-  const float* fbase = (REV && da_out) ? (mat ? fS : fz) + off : nullptr;
-  const int64_t stride = mat ? DPD : D;
-  // byte offset of this thread's four elements inside an operand tile
-  const int row = e4 / D, col = e4 % D;
-  const uint32_t toff = mat ? sw_chunk(D, row, col >> 6, (col & 63) >> 3) + (col & 7) * 2 : 0u;
-  uint8_t* tbase = reinterpret_cast<uint8_t*>(tiles + bh * nch * (int64_t)DPD) + toff;
+  const float wfull = (float)kCb * decay_pow(a, kCb - 1);
+  const bool fwd_state = REV && da_out;
   const int slot = blockIdx.y * 8 + (threadIdx.x >> 5);
-  constexpr int kB = REV ? 4 : 8;   // chunks in flight (the reverse scan loads two streams)
   auto idx = [&](int i) { return REV ? nch - 1 - i : i; };   // i-th chunk visited
   auto clen = [&](int c) { return (int)min((int64_t)kCb, n - (int64_t)c * kCb); };
   auto fac = [&](int c) {
     const int len = clen(c);
     return len == kCb ? a_full : decay_pow(a, len);
   };
-  auto ld = [&](const float* b, int i) {
-    return (valid && i < nch) ? *reinterpret_cast<const float4*>(b + idx(i) * stride)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-  };
-  const float wfull = (float)kCb * decay_pow(a, kCb - 1);
-  float da_acc = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 cur[kB], nxt[kB], fcur[kB], fnxt[kB];
-#pragma unroll
-  for (int j = 0; j < kB; ++j) {
-    cur[j] = ld(base, j);
-    if (fbase) fcur[j] = ld(fbase, j);
-  }
-  for (int i0 = 0; i0 < nch; i0 += kB) {
+  // The scan of four consecutive elements: of the matrix part (MAT; every
+  // thread of the block) or of the vector part (the first D/4 threads of the
+  // last block).
+  auto run = [&](auto mat_tag) {
+    constexpr bool MAT = decltype(mat_tag)::value;
+    // the ∂a stream (S_c from its operand tile, z_c in fp32) is kept as raw
+    // bits and widened only where it is used, so that the prefetching loads
+    // do not wait for their data
+    using Raw = std::conditional_t<MAT, uint2, uint4>;
+    constexpr int kB = REV ? 6 : 8;   // chunks in flight (the reverse scan loads two streams)
+    const int e4 = (blockIdx.y * 256 + threadIdx.x) * 4 - (MAT ? 0 : DPD);
+    const bool valid = MAT || e4 < D;
+    const int64_t off = MAT ? bh * nch * (int64_t)DPD + e4 : bh * nch * (int64_t)D + e4;
+    float* base = (MAT ? S : z) + off;
+    constexpr int64_t stride = MAT ? DPD : D;
+    // byte offset of this thread's four elements inside an operand tile
+    const int row = e4 / D, col = e4 % D;
+    const uint32_t toff = MAT ? sw_chunk(D, row, col >> 6, (col & 63) >> 3) + (col & 7) * 2 : 0u;
+    uint8_t* tbase = reinterpret_cast<uint8_t*>(tiles + bh * nch * (int64_t)DPD) + toff;
+    const uint8_t* fbase = nullptr;
+    if (fwd_state)
+      fbase = MAT ? reinterpret_cast<const uint8_t*>(fS + bh * nch * (int64_t)DPD) + toff
+                  : reinterpret_cast<const uint8_t*>(fz + off);
+    auto ld = [&](int i) {
+      return (valid && i < nch) ? *reinterpret_cast<const float4*>(base + idx(i) * stride)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto ld_state = [&](int i) {
+      Raw u{};
+      if (valid && i < nch)
+        u = *reinterpret_cast<const Raw*>(fbase + idx(i) * stride * (MAT ? 2 : 4));
+      return u;
+    };
+    auto state_val = [](const Raw& u) {
+      if constexpr (MAT)
+        return make_float4(bf16lo_to_f32(u.x), bf16hi_to_f32(u.x), bf16lo_to_f32(u.y),
+                           bf16hi_to_f32(u.y));
+      else
+        return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                           __uint_as_float(u.w));
+    };
+    float da_acc = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 cur[kB], nxt[kB];
+    Raw fcur[kB], fnxt[kB];
 #pragma unroll
     for (int j = 0; j < kB; ++j) {
-      nxt[j] = ld(base, i0 + kB + j);
-      if (fbase) fnxt[j] = ld(fbase, i0 + kB + j);
+      cur[j] = ld(j);
+      if (fwd_state) fcur[j] = ld_state(j);
     }
+    for (int i0 = 0; i0 < nch; i0 += kB) {
 #pragma unroll
-    for (int j = 0; j < kB; ++j) {
-      const int i = i0 + j;
-      if (i < nch) {
-        const int c = idx(i);
-        if (valid) {
-          if (!REV || !mat) *reinterpret_cast<float4*>(base + c * stride) = acc;
-          if (mat)
-            *reinterpret_cast<uint2*>(tbase + c * (int64_t)DPD * 2) =
-                make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      for (int j = 0; j < kB; ++j) {
+        nxt[j] = ld(i0 + kB + j);
+        if (fwd_state) fnxt[j] = ld_state(i0 + kB + j);
+      }
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        const int i = i0 + j;
+        if (i < nch) {
+          const int c = idx(i);
+          if (valid) {
+            if (MAT)
+              *reinterpret_cast<uint2*>(tbase + c * (int64_t)DPD * 2) =
+                  make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+            else
+              *reinterpret_cast<float4*>(base + c * stride) = acc;
+          }
+          if (fwd_state) {
+            const int len = clen(c);
+            const float w_c = len == kCb ? wfull : (float)len * decay_pow(a, len - 1);
+            const float4 sv = state_val(fcur[j]);
+            da_acc += w_c * (acc.x * sv.x + acc.y * sv.y + acc.z * sv.z + acc.w * sv.w);
+          }
+          const float f = fac(c);
+          acc = make_float4(f * acc.x + cur[j].x, f * acc.y + cur[j].y, f * acc.z + cur[j].z,
+                            f * acc.w + cur[j].w);
         }
-        if (fbase) {
-          const int len = clen(c);
-          const float w_c = len == kCb ? wfull : (float)len * decay_pow(a, len - 1);
-          da_acc += w_c * (acc.x * fcur[j].x + acc.y * fcur[j].y + acc.z * fcur[j].z +
-                           acc.w * fcur[j].w);
-        }
-        const float f = fac(c);
-        acc = make_float4(f * acc.x + cur[j].x, f * acc.y + cur[j].y, f * acc.z + cur[j].z,
-                          f * acc.w + cur[j].w);
+      }
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        cur[j] = nxt[j];
+        if (fwd_state) fcur[j] = fnxt[j];
       }
     }
-#pragma unroll
-    for (int j = 0; j < kB; ++j) {
-      cur[j] = nxt[j];
-      if (fbase) fcur[j] = fnxt[j];
-    }
-  }
-  if (fbase) {   // warp-uniform: every lane takes part
+    return da_acc;
+  };
+  const bool mat_block = (blockIdx.y + 1) * 1024 <= DPD;
+  float da_acc = mat_block ? run(std::true_type{}) : run(std::false_type{});
+  if (fwd_state) {   // block-uniform: every lane takes part
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) da_acc += __shfl_xor_sync(0xffffffffu, da_acc, o);
     if ((threadIdx.x & 31) == 0) da_out[bh * (int64_t)da_parts + slot] = da_acc;
@@ -1145,7 +1217,7 @@ cudaError_t run_bt(const BwdArgs& a, float* ws, int num_sms, int* status, cudaSt
   bt_dq_kernel<D><<<grid, kThreadsB, smem, stream>>>(mq, mk, mv, mg, p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bt_chunk_scan<D, true><<<sgrid, 256, 0, stream>>>(p.M, p.N, mt, p.S, p.z,
+  bt_chunk_scan<D, true><<<sgrid, 256, 0, stream>>>(p.M, p.N, mt, st, p.z,
                                                     p.want_da ? p.dapart + 2 * nch : nullptr, p.da_parts,
                                                     a.H, nch, a.n, a.decay);
   count_launches(1);
