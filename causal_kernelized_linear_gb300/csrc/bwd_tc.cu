@@ -53,7 +53,6 @@ constexpr int kThreadsB = 256;    // two threads per token row / TMEM lane (one 
 
 template <int D>
 struct BtCfg {
-  static constexpr int HALVES = D / 64;
   static constexpr int TILE = kCb * D * 2;      // [128 × D] bf16, 128-byte swizzle
   static constexpr int STILE = D * D * 2;       // [D' × D] bf16 state / adjoint tile
   static constexpr int oQ = 0;
@@ -61,13 +60,14 @@ struct BtCfg {
   static constexpr int oV = oK + TILE;
   static constexpr int oG = oV + TILE;
   static constexpr int oS = oG + TILE;
-  // staging for coalesced stores, apart from the tiles (which the next item's
-  // loads may already be filling): half an fp32 [D' × D] matrix with rows
-  // padded to D/2 + 4, or a bf16 [128 × D] matrix with rows padded to 2D + 16 bytes
+  // staging for stores, apart from the tiles (which the next item's loads may
+  // already be filling): half an fp32 [D' × D] matrix with rows padded to
+  // D/2 + 4 (coalesced stores of the state pass), two fp32 [D × 32] boxes or
+  // one bf16 [128 × D] tile with the 128-byte swizzle (TMA stores)
   static constexpr int oST = oS + STILE;
   static constexpr int STG_F32 = (D / 2 + 4) * D * 4;
-  static constexpr int STG_BF16 = kCb * (2 * D + 16);
-  static constexpr int oZ = oST + (STG_F32 > STG_BF16 ? STG_F32 : STG_BF16);   // fp32 [D]: z_c or N_c
+  static constexpr int STG_TMA = TILE > 2 * D * 128 ? TILE : 2 * D * 128;
+  static constexpr int oZ = oST + (STG_F32 > STG_TMA ? STG_F32 : STG_TMA);   // fp32 [D]: z_c or N_c
   static constexpr int oRHO = oZ + D * 4;        // fp32 [128]
   static constexpr int oDEN = oRHO + kCb * 4;    // fp32 [128]
   static constexpr int oPW = oDEN + kCb * 4;     // fp32 a^k, k = 0..128
@@ -83,6 +83,7 @@ struct BtCfg {
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
   static_assert((kThreadsB / (D / 8)) * D * 4 <= STILE, "column-sum scratch in the S tile");
   static_assert(oZ % 16 == 0, "bulk-copy destination alignment");
+  static_assert(oST % 1024 == 0, "swizzled staging alignment");
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -304,6 +305,47 @@ __device__ __forceinline__ void store_tmem_matrix(uint32_t tmem, uint32_t col0, 
   }
 }
 
+// The fp32 [D' × D] accumulator in TMEM (lane = row, columns col0..col0+D)
+// to matrix `item` of `map` (fp32 [D × D] matrices, boxes of 32 columns × D
+// rows with the 128-byte swizzle): staged box by box in shared memory
+// (`stage`, two boxes, 1024-byte aligned) and written by TMA stores, two
+// boxes per round; the two threads of a row fill one box each.  Thread 0
+// issues and commits the stores; before a round reuses the stage it waits
+// for the previous round's reads.  Every thread of the CTA calls it (it
+// holds CTA barriers); the caller waits for the last round's reads before
+// the stage is written again.
+template <int D>
+__device__ __forceinline__ void store_tmem_matrix_tma(uint32_t tmem, uint32_t col0, uint8_t* stage,
+                                                      const CUtensorMap* map, int64_t item) {
+  constexpr int BOX = D * 128;                 // bytes of one [D × 32] fp32 box
+  constexpr int NBOX = D / 32;
+  const int r = threadIdx.x & (kCb - 1), part = threadIdx.x / kCb;
+#pragma unroll 1
+  for (int b0 = 0; b0 < NBOX; b0 += 2) {
+    if (b0 > 0) {
+      if (threadIdx.x == 0) tma_store_wait_read0();
+      __syncthreads();
+    }
+    if (r < D) {
+      uint32_t v[32];
+      tmem_ld32(tmem_addr(tmem, (uint32_t)(r >> 5) * 32, col0 + (b0 + part) * 32), v);
+      tmem_ld_wait();
+      uint8_t* box = stage + part * BOX;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(box + sw_chunk(D, r, 0, j)) =
+            make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      tma_store_3d(map, stage, b0 * 32, 0, (int)item);
+      tma_store_3d(map, stage + BOX, (b0 + 1) * 32, 0, (int)item);
+      tma_store_commit();
+    }
+  }
+}
+
 // Weighted column sums of a [128 × D] bf16 tile (rows = tokens, 128-byte
 // swizzle): out[i] = Σ_s wt(s)·T[s][i].  Thread t sums the 8 columns of chunk
 // t mod (D/8) over one group of rows, so its loads and adds are independent;
@@ -338,28 +380,6 @@ __device__ __forceinline__ void tile_colsum(const uint8_t* tile, Wt wt, float* s
 #pragma unroll
     for (int g = 0; g < NG; ++g) s += scratch[g * D + threadIdx.x];
     out[threadIdx.x] = s;
-  }
-}
-
-// Stages one bf16 row of 8-element chunks for a coalesced store: row r of a
-// [128 × D] matrix at `stage` with a row stride of 2·D + 16 bytes.
-template <int D>
-__device__ __forceinline__ void stage_chunk(uint8_t* stage, int r, int col, const float (&f)[8]) {
-  *reinterpret_cast<uint4*>(stage + r * (2 * D + 16) + col * 2) = pack8(f);
-}
-
-// The staged rows [0, cs) of a [128 × D] bf16 matrix to global rows
-// dst[0..cs) (row-major, D elements each), 16 bytes per thread and step.
-template <int D>
-__device__ __forceinline__ void store_staged_rows(const uint8_t* stage, __nv_bfloat16* __restrict__ dst,
-                                                  int cs) {
-  constexpr int NCH = D / 8;
-#pragma unroll 4
-  for (int e = threadIdx.x; e < kCb * NCH; e += kThreadsB) {
-    const int row = e / NCH, c = e % NCH;
-    if (row < cs)
-      *reinterpret_cast<uint4*>(dst + (int64_t)row * D + c * 8) =
-          *reinterpret_cast<const uint4*>(stage + row * (2 * D + 16) + c * 16);
   }
 }
 
@@ -503,6 +523,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1)
 bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
              const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
+             const __grid_constant__ CUtensorMap map_dq, const __grid_constant__ CUtensorMap map_dm,
              const BtParams p) {
   using Cfg = BtCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -709,9 +730,13 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
       }
       tmem_st16(tmem_addr(x.tmem, lane_base, RP + b * 16), pk);
     }
+    // ... and Q'' = a^{t+1}φ(q) in place, keeping min(φ(q), 1) of this
+    // thread's columns (bf16 pairs) for ∂q
     float qu = 0.f;
-#pragma unroll 1
-    for (int j0 = hp * HB; j0 < (hp + 1) * HB; j0 += 32) {
+    uint32_t qmask[HB / 2];
+#pragma unroll
+    for (int jj = 0; jj < HB / 32; ++jj) {
+      const int j0 = hp * HB + jj * 32;
       uint32_t uv[32];
       tmem_ld32(tmem_addr(x.tmem, lane_base, RY + j0), uv);
       tmem_ld_wait();
@@ -728,53 +753,32 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         uv[e] = __float_as_uint(pw[r + 1] * u);
       }
       tmem_st32(tmem_addr(x.tmem, lane_base, RY + j0), uv);
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        const int h = (j0 + q8 * 8) >> 6, j = ((j0 + q8 * 8) & 63) >> 3;
+        float m[8], sc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          m[e] = fminf(qf[q8 * 8 + e], 1.f);
+          sc[e] = pw[r + 1] * qf[q8 * 8 + e];
+        }
+        const uint4 mk = pack8(m);
+        qmask[jj * 16 + q8 * 4 + 0] = mk.x;
+        qmask[jj * 16 + q8 * 4 + 1] = mk.y;
+        qmask[jj * 16 + q8 * 4 + 2] = mk.z;
+        qmask[jj * 16 + q8 * 4 + 3] = mk.w;
+        *reinterpret_cast<uint4*>(qt + sw_chunk(kCb, r, h, j)) = pack8(sc);
+      }
     }
     if (live) da += (float)(r + 1) * pw[r] * qu;
     rows_to_mma();
-    // ∂q' += E·K'
+    // ∂q' += E·K'; ΔM = Q''ᵀĜ (over the columns of ĜVᵀ, read by rows 3)
     if (threadIdx.x == 0) {
       const uint64_t dKm = smem_desc(x.sbase + Cfg::oK, kCb * 128, 1024, kSwizzle128B);
       constexpr uint32_t idN = idesc_bf16_f32(128, D, false, true);
 #pragma unroll
       for (int k = 0; k < kCb / 16; ++k)
         mma_ts(x.tmem + RY, x.tmem + RP + k * 8, desc_at(dKm, k * 2048), idN, 1);
-    }
-    commit_mma(x);
-    // ΔN_i = Σ_t a^{t+1} ρ_t q'_ti meanwhile (rows ≥ cs of Q' and ρ are zero;
-    // the S_c tile is free since Ĝ·S_cᵀ completed)
-    tile_colsum<D>(qt, [&](int t) { return pw[t + 1] * srho[t]; },
-                   reinterpret_cast<float*>(x.sm + Cfg::oS), p.N + item * D);
-    if (!wait_mma(x)) break;
-    issue_k(item + 1);   // K is consumed
-    // ---- rows 4: ∂q = ∂q' ⊙ min(φ(q), 1), staged; then Q'' = a^{t+1}φ(q) in place
-    uint8_t* dq_stage = x.sm + Cfg::oST;
-#pragma unroll 1
-    for (int j0 = hp * HB; j0 < (hp + 1) * HB; j0 += 32) {
-      uint32_t dv[32];
-      tmem_ld32(tmem_addr(x.tmem, lane_base, RY + j0), dv);
-      tmem_ld_wait();
-#pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        const int h = (j0 + q8 * 8) >> 6, j = ((j0 + q8 * 8) & 63) >> 3;
-        float f[8];
-        unpack8(*reinterpret_cast<const uint4*>(qt + sw_chunk(kCb, r, h, j)), f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(dv[q8 * 8 + e]) * fminf(f[e], 1.f);
-        stage_chunk<D>(dq_stage, r, j0 + q8 * 8, f);
-      }
-    }
-    __syncthreads();   // every row's φ(q) has been read (ΔN, ∂q) before it is scaled
-    store_staged_rows<D>(dq_stage, p.dq + (bh * p.n + t0) * D, cs);
-    {
-      const uint32_t s2 = splat_bf16x2(pw[r + 1]);
-      half_row_map<D>(qt, r, hp, [s2](uint4 u) {
-        return make_uint4(mul_bf16x2(u.x, s2), mul_bf16x2(u.y, s2), mul_bf16x2(u.z, s2),
-                          mul_bf16x2(u.w, s2));
-      });
-    }
-    rows_to_mma();
-    // ΔM = Q''ᵀĜ
-    if (threadIdx.x == 0) {
       const uint64_t dA = smem_desc(x.sbase + Cfg::oQ, (D == 128) ? kCb * 128 : 0, 1024, kSwizzle128B);
       const uint64_t dB = smem_desc(x.sbase + Cfg::oG, kCb * 128, 1024, kSwizzle128B);
       constexpr uint32_t id = idesc_bf16_f32(128, D, true, true);
@@ -783,16 +787,54 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         mma_ss(x.tmem + RN, desc_at(dA, k * 2048), desc_at(dB, k * 2048), id, k > 0);
     }
     commit_mma(x);
+    // ΔN_i = Σ_t ρ_t q''_ti meanwhile (rows ≥ cs of Q'' and ρ are zero; the
+    // S_c tile is free since Ĝ·S_cᵀ completed)
+    tile_colsum<D>(qt, [&](int t) { return srho[t]; }, reinterpret_cast<float*>(x.sm + Cfg::oS),
+                   p.N + item * D);
+    if (threadIdx.x == 0) tma_store_wait_read0();   // the previous item's ΔM left the stage
     if (!wait_mma(x)) break;
-    issue_rest(item + 1);   // Q, ∂o, the S_c tile (and scratch) and z_c are consumed
-    store_tmem_matrix<D>(x.tmem, RN, reinterpret_cast<float*>(x.sm + Cfg::oST),
-                         p.M + item * (int64_t)(D * D));
+    issue_k(item + 1);      // every tile, z_c and the scratch are consumed
+    issue_rest(item + 1);
+    // ---- rows 4: ∂q = ∂q' ⊙ min(φ(q), 1), staged as a swizzled tile and stored
+    // by TMA (rows past n are not written)
+    uint8_t* dq_stage = x.sm + Cfg::oST;
+#pragma unroll
+    for (int jj = 0; jj < HB / 32; ++jj) {
+      const int j0 = hp * HB + jj * 32;
+      uint32_t dv[32];
+      tmem_ld32(tmem_addr(x.tmem, lane_base, RY + j0), dv);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        const int h = (j0 + q8 * 8) >> 6, j = ((j0 + q8 * 8) & 63) >> 3;
+        float f[8];
+        unpack8(make_uint4(qmask[jj * 16 + q8 * 4 + 0], qmask[jj * 16 + q8 * 4 + 1],
+                           qmask[jj * 16 + q8 * 4 + 2], qmask[jj * 16 + q8 * 4 + 3]),
+                f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] *= __uint_as_float(dv[q8 * 8 + e]);
+        *reinterpret_cast<uint4*>(dq_stage + sw_chunk(kCb, r, h, j)) = pack8(f);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();   // ∂q is staged
+    tc_fence_after();
+    if (threadIdx.x == 0) {
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h) tma_store_3d(&map_dq, dq_stage + h * kCb * 128, h * 64, t0, (int)bh);
+      tma_store_commit();
+      tma_store_wait_read0();   // the stage is reused for ΔM
+    }
+    __syncthreads();
+    store_tmem_matrix_tma<D>(x.tmem, RN, x.sm + Cfg::oST, &map_dm, item);
     tc_fence_before();
     if (p.want_da) {
       const float s = cta_sum(da, red);
       if (threadIdx.x == 0) p.dapart[bh * p.da_parts + c] = s;
     }
   }
+  if (threadIdx.x == 0) tma_store_wait0();   // ∂q and ΔM are in global memory
   BtSetup<D>::teardown(x);
 }
 
@@ -802,6 +844,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1)
 bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
+               const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
                const BtParams p) {
   using Cfg = BtCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -962,34 +1005,18 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
     }
     commit_mma(x);
+    if (threadIdx.x == 0) tma_store_wait_read0();   // the previous item's ∂v left the stage
     if (!wait_mma(x)) break;
     issue_a(item + 1);   // Q, V, ∂o and M_c are consumed
     rows_of(item + 1);
-    // ---- rows 2: ∂v_s = (PᵀĜ)_s + w·a^{cs−1−s}(K'M)_s;
-    // ∂k'_s = (EᵀQ')_s + w·a^{cs−1−s}((VMᵀ)_s + N); ∂a share (t1 − s)·w·a^{t1−s−1}·k'_s·((VMᵀ)_s + N).
-    // The TMEM loads are warp-collective, so every row takes part; only the
-    // valid rows are stored.  ∂v, then ∂k, go through the staging area and
-    // are stored coalesced.
+    // ---- rows 2: ∂k'_s = (EᵀQ')_s + w·a^{cs−1−s}((VMᵀ)_s + N); ∂a share
+    // (t1 − s)·w·a^{t1−s−1}·k'_s·((VMᵀ)_s + N); then ∂v_s = (PᵀĜ)_s +
+    // w·a^{cs−1−s}(K'M)_s.  ∂k goes first: it is the last reader of the K tile
+    // and N_c, whose next loads then start.  The TMEM loads are warp-collective,
+    // so every row takes part.  ∂k, then ∂v, are staged as swizzled tiles and
+    // stored by TMA (rows past n are not written).
     uint8_t* stage = x.sm + Cfg::oST;
     const float fut = live ? w * pw[cs - 1 - r] : 0.f;
-#pragma unroll 1
-    for (int j0 = hp * HB; j0 < (hp + 1) * HB; j0 += 32) {
-      uint32_t va[32], vb[32];
-      tmem_ld32(tmem_addr(x.tmem, lane_base, RV + j0), va);
-      tmem_ld32(tmem_addr(x.tmem, lane_base, RX + j0), vb);
-      tmem_ld_wait();
-#pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        float f[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          f[e] = __uint_as_float(va[q8 * 8 + e]) + fut * __uint_as_float(vb[q8 * 8 + e]);
-        stage_chunk<D>(stage, r, j0 + q8 * 8, f);
-      }
-    }
-    __syncthreads();
-    store_staged_rows<D>(stage, p.dv + (bh * p.n + t0) * D, cs);
-    __syncthreads();
     {
       float kfut = 0.f;
 #pragma unroll 1
@@ -1009,20 +1036,52 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
             kfut += kf[e] * m;
             f[e] = (__uint_as_float(va[q8 * 8 + e]) + fut * m) * fminf(kf[e], 1.f);
           }
-          stage_chunk<D>(stage, r, j0 + q8 * 8, f);
+          *reinterpret_cast<uint4*>(stage + sw_chunk(kCb, r, h, j)) = pack8(f);
         }
       }
       if (live) da += aw[cs - 1 - r] * kfut;
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     issue_b(item + 1);   // the K tile and N_c are consumed
-    store_staged_rows<D>(stage, p.dk + (bh * p.n + t0) * D, cs);
+    if (threadIdx.x == 0) {
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h) tma_store_3d(&map_dk, stage + h * kCb * 128, h * 64, t0, (int)bh);
+      tma_store_commit();
+      tma_store_wait_read0();   // the stage is reused for ∂v
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int j0 = hp * HB; j0 < (hp + 1) * HB; j0 += 32) {
+      uint32_t va[32], vb[32];
+      tmem_ld32(tmem_addr(x.tmem, lane_base, RV + j0), va);
+      tmem_ld32(tmem_addr(x.tmem, lane_base, RX + j0), vb);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        const int h = (j0 + q8 * 8) >> 6, j = ((j0 + q8 * 8) & 63) >> 3;
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          f[e] = __uint_as_float(va[q8 * 8 + e]) + fut * __uint_as_float(vb[q8 * 8 + e]);
+        *reinterpret_cast<uint4*>(stage + sw_chunk(kCb, r, h, j)) = pack8(f);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h) tma_store_3d(&map_dv, stage + h * kCb * 128, h * 64, t0, (int)bh);
+      tma_store_commit();
+    }
     if (p.want_da) {
       const float s = cta_sum(da, red);
       if (threadIdx.x == 0) p.dapart[bh * p.da_parts + p.nch + c] = s;
     }
   }
+  if (threadIdx.x == 0) tma_store_wait0();   // ∂k and ∂v are in global memory
   BtSetup<D>::teardown(x);
 }
 
@@ -1191,7 +1250,11 @@ cudaError_t run_bt(const BwdArgs& a, float* ws, int num_sms, int* status, cudaSt
   p.rho = cur; cur += (size_t)BH * a.n;
   p.dapart = cur;
   p.da_parts = 2 * nch + (int)sgrid.y * 8;
-  CUtensorMap mq, mk, mv, mg;
+  CUtensorMap mq, mk, mv, mg, mdq, mdk, mdv, mdm;
+  if ((e = tmap_rows(&mdq, a.dq, BH, a.n, D, kCb)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mdk, a.dk, BH, a.n, D, kCb)) != cudaSuccess) return e;
+  if ((e = tmap_rows(&mdv, a.dv, BH, a.n, D, kCb)) != cudaSuccess) return e;
+  if ((e = tmap_f32_mats(&mdm, p.M, (int64_t)ns, D)) != cudaSuccess) return e;
   if ((e = tmap_rows(&mq, a.q, BH, a.n, D, kCb)) != cudaSuccess) return e;
   if ((e = tmap_rows(&mk, a.k, BH, a.n, D, kCb)) != cudaSuccess) return e;
   if ((e = tmap_rows(&mv, a.v, BH, a.n, D, kCb)) != cudaSuccess) return e;
@@ -1214,7 +1277,7 @@ cudaError_t run_bt(const BwdArgs& a, float* ws, int num_sms, int* status, cudaSt
                                                      nch, a.n, a.decay);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bt_dq_kernel<D><<<grid, kThreadsB, smem, stream>>>(mq, mk, mv, mg, p);
+  bt_dq_kernel<D><<<grid, kThreadsB, smem, stream>>>(mq, mk, mv, mg, mdq, mdm, p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   bt_chunk_scan<D, true><<<sgrid, 256, 0, stream>>>(p.M, p.N, mt, st, p.z,
@@ -1222,7 +1285,7 @@ cudaError_t run_bt(const BwdArgs& a, float* ws, int num_sms, int* status, cudaSt
                                                     a.H, nch, a.n, a.decay);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bt_dkdv_kernel<D><<<grid, kThreadsB, smem, stream>>>(mq, mk, mv, mg, p);
+  bt_dkdv_kernel<D><<<grid, kThreadsB, smem, stream>>>(mq, mk, mv, mg, mdk, mdv, p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.want_da) return backward_da_reduce(p.dapart, a.da, a.B, a.H, p.da_parts, stream);

@@ -116,12 +116,15 @@ cudaError_t tc_performer_forward(const FwdArgs& a, cudaStream_t stream, float* w
                                  float* ws_z, float* tot_state, float* tot_z,
                                  const SegmentPlan& plan);
 
-// TMA tensor maps (bf16, 128-byte swizzle, boxes 64 elements wide):
-//   tmap_rows:   [BH, n, D] as a 3-D tensor, box 64 × rows × 1 (rows past n
-//                read as zero);
-//   tmap_matrix: a row-major [rows, cols] matrix, box 64 × box_rows.
+// TMA tensor maps (128-byte swizzle, boxes 128 bytes wide):
+//   tmap_rows:     bf16 [BH, n, D] as a 3-D tensor, box 64 × rows × 1 (rows
+//                  past n read as zero and are not written);
+//   tmap_matrix:   a bf16 row-major [rows, cols] matrix, box 64 × box_rows;
+//   tmap_f32_mats: `count` fp32 row-major [D × D] matrices, contiguous, as a
+//                  3-D tensor, box 32 × D × 1.
 cudaError_t tmap_rows(CUtensorMap* m, const void* base, int64_t BH, int64_t n, int D, int rows);
 cudaError_t tmap_matrix(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows);
+cudaError_t tmap_f32_mats(CUtensorMap* m, const void* base, int64_t count, int D);
 
 // Exclusive decayed prefix over the per-segment aggregates of every head, in
 // place.  Segment g's aggregate is carried past it with the factor
