@@ -254,19 +254,6 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
   f[6] = bf16lo_to_f32(u.w); f[7] = bf16hi_to_f32(u.w);
 }
 
-// Column half hp of row r of a [128 × D] tile scaled by sc in place, in fp32
-// with one rounding.
-template <int D>
-__device__ __forceinline__ void scale_half_row_inplace(uint8_t* tile, int r, int hp, float sc) {
-  half_row_map<D>(tile, r, hp, [sc](uint4 u) {
-    float f[8];
-    unpack8(u, f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] *= sc;
-    return pack8(f);
-  });
-}
-
 // The fp32 [D' × D] accumulator in TMEM (lane = row, columns col0..col0+D)
 // to a contiguous row-major matrix in global memory, in two rounds of D/2
 // columns.  Rows go through shared memory (`stage`, (D/2 + 4)·D floats; the
@@ -650,7 +637,9 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     }
     commit_mma(x);
     if (!wait_mma(x)) break;
-    // ---- rows 2: o = (P·V + a^{t+1} Y)/den, ρ, ĝ (written over g)
+    // ---- rows 2: o = (P·V + a^{t+1} Y)/den, ρ.  The ∂o tile stays as it is
+    // (exact bf16): the products below use it and the rows divide by den in
+    // fp32, so that ĝ = ∂o/den is never rounded to bf16
     const float inv_den = live ? 1.f / den : 0.f;
     float go = 0.f;
 #pragma unroll 1
@@ -672,17 +661,17 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
       }
     }
     xch[hp * kCb + r] = go;
-    scale_half_row_inplace<D>(gt, r, hp, inv_den);
     rows_to_mma();
-    const float rho = -(xch[r] + xch[kCb + r]) * inv_den;
+    const float go_r = xch[r] + xch[kCb + r];
+    const float rho = -go_r * inv_den;
     if (hp == 0) {
-      srho[r] = rho;
+      srho[r] = live ? -go_r : 0.f;   // ρ_t·den_t, the ΔN weight of Q'' (which carries 1/den_t)
       if (live) {
         p.den[bh * p.n + t0 + r] = den;
         p.rho[bh * p.n + t0 + r] = rho;
       }
     }
-    // ĜVᵀ, U = Ĝ·S_cᵀ
+    // ∂o·Vᵀ, ∂o·S_cᵀ (rows scaled by 1/den in rows 3)
     if (threadIdx.x == 0) {
       const uint64_t dG = smem_desc(x.sbase + Cfg::oG, 16, 1024, kSwizzle128B);
       const uint64_t dVk = smem_desc(x.sbase + Cfg::oV, 16, 1024, kSwizzle128B);
@@ -701,7 +690,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     if (!wait_mma(x)) break;
     issue_v(item + 1);   // V is consumed
     // ---- rows 3: E = W ⊙ (ĜVᵀ + ρ) (bf16, for E·K'), ∂a shares; ∂q' starts
-    // as a^{t+1}·u_t, u_t = S_c ĝ_t + ρ_t z_c
+    // as a^{t+1}·u_t, u_t = S_c ĝ_t + ρ_t z_c (ĜVᵀ = ∂o·Vᵀ/den, S_c ĝ = S_c∂o/den)
     float da = 0.f;
 #pragma unroll 1
     for (int b = hp; b < 4; b += 2) {
@@ -721,7 +710,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int s = s0 + u;
-            const float f = __uint_as_float(gv[j + u]) + rho;
+            const float f = __uint_as_float(gv[j + u]) * inv_den + rho;
             e2[u] = (s <= r && live) ? w * pw[r - s] * f : 0.f;
             if (s < r && live) da += aw[r - s] * __uint_as_float(xv[j + u]) * f;
           }
@@ -730,10 +719,11 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
       }
       tmem_st16(tmem_addr(x.tmem, lane_base, RP + b * 16), pk);
     }
-    // ... and Q'' = a^{t+1}φ(q) in place, keeping min(φ(q), 1) of this
-    // thread's columns (bf16 pairs) for ∂q
+    // ... and Q'' = a^{t+1}φ(q)/den in place (ΔM = Q''ᵀ∂o = Σ_t a^{t+1}q'_tᵀĝ_t),
+    // keeping min(φ(q), 1) of this thread's columns (bf16 pairs) for ∂q
     float qu = 0.f;
     uint32_t qmask[HB / 2];
+    const float q2s = pw[r + 1] * inv_den;
 #pragma unroll
     for (int jj = 0; jj < HB / 32; ++jj) {
       const int j0 = hp * HB + jj * 32;
@@ -748,7 +738,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
       }
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const float u = __uint_as_float(uv[e]) + rho * zc[j0 + e];
+        const float u = __uint_as_float(uv[e]) * inv_den + rho * zc[j0 + e];
         qu += qf[e] * u;
         uv[e] = __float_as_uint(pw[r + 1] * u);
       }
@@ -760,7 +750,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           m[e] = fminf(qf[q8 * 8 + e], 1.f);
-          sc[e] = pw[r + 1] * qf[q8 * 8 + e];
+          sc[e] = q2s * qf[q8 * 8 + e];
         }
         const uint4 mk = pack8(m);
         qmask[jj * 16 + q8 * 4 + 0] = mk.x;
@@ -772,7 +762,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     }
     if (live) da += (float)(r + 1) * pw[r] * qu;
     rows_to_mma();
-    // ∂q' += E·K'; ΔM = Q''ᵀĜ (over the columns of ĜVᵀ, read by rows 3)
+    // ∂q' += E·K'; ΔM = Q''ᵀ∂o (over the columns of ĜVᵀ, read by rows 3)
     if (threadIdx.x == 0) {
       const uint64_t dKm = smem_desc(x.sbase + Cfg::oK, kCb * 128, 1024, kSwizzle128B);
       constexpr uint32_t idN = idesc_bf16_f32(128, D, false, true);
@@ -787,8 +777,9 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         mma_ss(x.tmem + RN, desc_at(dA, k * 2048), desc_at(dB, k * 2048), id, k > 0);
     }
     commit_mma(x);
-    // ΔN_i = Σ_t ρ_t q''_ti meanwhile (rows ≥ cs of Q'' and ρ are zero; the
-    // S_c tile is free since Ĝ·S_cᵀ completed)
+    // ΔN_i = Σ_t a^{t+1} ρ_t q'_ti = Σ_t ρ_t den_t q''_ti meanwhile (rows ≥ cs
+    // of Q'' and of the weights are zero; the S_c tile is free since ∂o·S_cᵀ
+    // completed)
     tile_colsum<D>(qt, [&](int t) { return srho[t]; }, reinterpret_cast<float*>(x.sm + Cfg::oS),
                    p.N + item * D);
     if (threadIdx.x == 0) tma_store_wait_read0();   // the previous item's ΔM left the stage
@@ -853,7 +844,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   BtSetup<D>::run(x);
   float* nc = reinterpret_cast<float*>(x.sm + Cfg::oZ);
   float* srho = reinterpret_cast<float*>(x.sm + Cfg::oRHO);
-  float* sden = reinterpret_cast<float*>(x.sm + Cfg::oDEN);
+  float* sinv = reinterpret_cast<float*>(x.sm + Cfg::oDEN);   // 1/den_t (0 past the chunk)
   float* pw = reinterpret_cast<float*>(x.sm + Cfg::oPW);
   float* aw = reinterpret_cast<float*>(x.sm + Cfg::oAW);
   float* red = reinterpret_cast<float*>(x.sm + Cfg::oRED);
@@ -864,7 +855,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   const uint32_t lane_base = (uint32_t)wq * 32;
   constexpr int HB = D / 2;
   // TMEM columns: Xᵀ, later K'M [0,128) | Pᵀ [128,192) | Eᵀ [192,256) (both
-  // later V·Mᵀ [128, 128+D)) | ∂v [256, 256+D) | ĜᵀV... ĜVᵀᵀ, later ∂k' [384, 512)
+  // later V·Mᵀ [128, 128+D)) | ∂v [256, 256+D) | V∂oᵀ, later ∂k' [384, 512)
   constexpr uint32_t RX = 0, RP = 128, RE = 192, RF = 128, RV = 256, RK = 384;
   int64_t ib, ie;
   item_range(p.items, ib, ie);
@@ -910,7 +901,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     float da = 0.f;
     if (hp == 0) {
       srho[r] = rho_n;
-      sden[r] = den_n;
+      sinv[r] = live ? 1.f / den_n : 0.f;
     }
     if (bh != last_bh) {
       head_decay(p, bh, a, w);
@@ -919,13 +910,11 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     last_bh = bh;
     __syncthreads();
     if (!wait_tiles(x)) break;
-    phi_row_inplace<D>(hp ? kt : x.sm + Cfg::oQ, r, live);   // φ(Q) | φ(K)
-    {   // ĝ = g / den in place
-      const float inv = live ? 1.f / sden[r] : 0.f;
-      scale_half_row_inplace<D>(gt, r, hp, inv);
-    }
+    // φ(Q) | φ(K); the ∂o tile stays as it is (exact bf16): the products use
+    // it and the rows carry 1/den_t, so that ĝ = ∂o/den is never rounded
+    phi_row_inplace<D>(hp ? kt : x.sm + Cfg::oQ, r, live);
     rows_to_mma();
-    // Xᵀ = K'Q'ᵀ, (ĜVᵀ)ᵀ = VĜᵀ
+    // Xᵀ = K'Q'ᵀ, V∂oᵀ (column t of it is den_t·(ĜVᵀ)ᵀ)
     if (threadIdx.x == 0) {
       const uint64_t dQ = smem_desc(x.sbase + Cfg::oQ, 16, 1024, kSwizzle128B);
       const uint64_t dK = smem_desc(x.sbase + Cfg::oK, 16, 1024, kSwizzle128B);
@@ -941,7 +930,8 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     }
     commit_mma(x);
     if (!wait_mma(x)) break;
-    // ---- rows 1 (thread s = r): Pᵀ_st = W_ts x_ts, Eᵀ_st = W_ts(ĝ_t·v_s + ρ_t), t ≥ s
+    // ---- rows 1 (thread s = r): Pᵀ_st = W_ts x_ts/den_t (so that Pᵀ∂o = PᵀĜ),
+    // Eᵀ_st = W_ts(ĝ_t·v_s + ρ_t), ĝ_t·v_s = (V∂oᵀ)_st/den_t, t ≥ s
 #pragma unroll 1
     for (int b = hp; b < 4; b += 2) {
       uint32_t pk[16], ek[16];
@@ -961,8 +951,8 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
             const int t = b * 32 + j + u;
             const bool on = t >= r && t < cs;
             const float wts = on ? w * pw[t - r] : 0.f;
-            p2[u] = wts * __uint_as_float(xv[j + u]);
-            e2[u] = wts * (__uint_as_float(gv[j + u]) + srho[t]);
+            p2[u] = wts * sinv[t] * __uint_as_float(xv[j + u]);
+            e2[u] = wts * (__uint_as_float(gv[j + u]) * sinv[t] + srho[t]);
           }
           pk[j / 2] = pack_bf16x2(p2[0], p2[1]);
           ek[j / 2] = pack_bf16x2(e2[0], e2[1]);
@@ -972,7 +962,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       tmem_st16(tmem_addr(x.tmem, lane_base, RE + b * 16), ek);
     }
     rows_to_mma();
-    // ∂v = PᵀĜ, ∂k' = EᵀQ'
+    // ∂v = Pᵀ∂o (= PᵀĜ), ∂k' = EᵀQ'
     if (threadIdx.x == 0) {
       const uint64_t dGm = smem_desc(x.sbase + Cfg::oG, kCb * 128, 1024, kSwizzle128B);
       const uint64_t dQm = smem_desc(x.sbase + Cfg::oQ, kCb * 128, 1024, kSwizzle128B);

@@ -25,15 +25,20 @@ def head_rel_err(got, ref):
     return num / den
 
 
+def log_parity(what, worst, tol, heads):
+    """With LA_PARITY_LOG set, appends one JSON line per check: the worst
+    head's error and its bar."""
+    log = os.environ.get("LA_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"check": what, "worst_head_err": float(worst), "tol": tol,
+                                "heads": int(heads)}) + "\n")
+
+
 def assert_parity(got, ref, tol, what=""):
     err = head_rel_err(got, ref)
     worst = float(err.max()) if err.size else 0.0
-    log = os.environ.get("LA_PARITY_LOG")
-    if log:
-        # one JSON line per check: the worst head's error and its bar
-        with open(log, "a") as f:
-            f.write(json.dumps({"check": what, "worst_head_err": worst, "tol": tol,
-                                "heads": int(err.size)}) + "\n")
+    log_parity(what, worst, tol, err.size)
     assert np.all(np.isfinite(err)), f"{what}: non-finite error"
     assert worst <= tol, f"{what}: worst head error {worst:.3e} > {tol:.1e}"
     return worst

@@ -14,7 +14,7 @@ import torch
 import causal_kernelized_linear_gb300 as cl
 import oracle
 import workloads as W
-from helpers import TOL_BF16, TOL_F32, assert_parity, to_cuda
+from helpers import TOL_BF16, TOL_F32, assert_parity, log_parity, to_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -62,6 +62,7 @@ def _check(x, go, fm, got, tol, what, qk_zero=False):
         scale = max(np.abs(rda).max(), 1e-30)
         err = np.abs(da - rda).max() / scale
         tol_da = TOL_DA_F32 if tol == TOL_F32 else tol
+        log_parity(f"{what} da (all heads, normwise)", err, tol_da, rda.size)
         assert np.isfinite(err) and err <= tol_da, f"{what} da: {err:.3e} ({da} vs {rda})"
 
 
@@ -126,6 +127,7 @@ def test_backward_long_workload_sampled_heads(cuda_device):
         assert_parity(gt.cpu()[:, pick], rf, TOL_BF16, f"{w.name} {name}")
     rda = ref[3]
     err = np.abs(da.cpu().double().numpy()[pick] - rda).max() / np.abs(rda).max()
+    log_parity(f"{w.name} da (sampled heads, normwise)", err, TOL_BF16, rda.size)
     assert err <= TOL_BF16, (da.cpu()[pick], rda)
 
 
