@@ -303,7 +303,7 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
 }
 
 // The final state from zero without the outputs: the aggregate of every
-// segment, then their decayed sum (the scan's total) into mu_out / nu_out.
+// segment, then their decayed sum (segment_total) into mu_out / nu_out.
 la_status run_state(FwdArgs& a, cudaStream_t stream) {
   DeviceInfo di;
   la_status st = device_info(&di);
@@ -333,8 +333,8 @@ la_status run_state(FwdArgs& a, cudaStream_t stream) {
   else if (pp.tensor_cores) e = tc_state_only(a, stream, ws_state, ws_z, plan);
   else e = simt_state_only(a, stream, ws_state, ws_z, plan);
   if (e == cudaSuccess)
-    e = segment_scan(ws_state, ws_z, a.mu_out, a.nu_out, BH, a.H, plan.nseg, plan.nseg,
-                     plan.seg_len, a.n, a.dp, a.d, a.decay, nullptr, stream, false);
+    e = segment_total(ws_state, ws_z, a.mu_out, a.nu_out, BH, a.H, plan.nseg, plan.seg_len, a.n,
+                      a.dp, a.d, a.decay, nullptr, stream, false);
   const cudaError_t f = cudaFreeAsync(ws, stream);
   if (e == cudaSuccess) e = f;
   return to_status(e);

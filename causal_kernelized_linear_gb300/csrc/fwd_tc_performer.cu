@@ -840,11 +840,11 @@ cudaError_t run(const FwdArgs& a, cudaStream_t stream, float* ws_state, float* w
     return launch<DP, kCausal>(p, dim3(ubh, (unsigned)plan.nseg), plan.nseg > 1, mq, mk, mv, mw,
                                stream);
   }
-  // non-causal: all the aggregates, their total (the final state) by the scan
+  // non-causal: all the aggregates, then their total (the final state)
   e = launch<DP, kState>(p, dim3(ubh, (unsigned)plan.nseg), false, mq, mk, mv, mw, stream);
   if (e != cudaSuccess) return e;
-  e = segment_scan(ws_state, ws_z, tot_state, tot_z, a.B * a.H, a.H, plan.nseg, plan.nseg,
-                   plan.seg_len, a.n, DP, kD, nullptr, nullptr, stream, true);
+  e = segment_total(ws_state, ws_z, tot_state, tot_z, a.B * a.H, a.H, plan.nseg, plan.seg_len,
+                    a.n, DP, kD, nullptr, nullptr, stream, true);
   if (e != cudaSuccess) return e;
   return launch<DP, kReadout>(p, dim3(ubh, (unsigned)plan.nseg), true, mq, mk, mv, mw, stream);
 }

@@ -353,8 +353,8 @@ cudaError_t tc_noncausal_forward(const FwdArgs& a, cudaStream_t stream, float* w
   // the aggregate of every segment, their total, then the readout
   cudaError_t e = tc_state_only(a, stream, ws_state, ws_z, plan);
   if (e != cudaSuccess) return e;
-  e = segment_scan(ws_state, ws_z, tot_state, tot_z, a.B * a.H, a.H, plan.nseg, plan.nseg,
-                   plan.seg_len, a.n, a.d, a.d, nullptr, nullptr, stream, false);
+  e = segment_total(ws_state, ws_z, tot_state, tot_z, a.B * a.H, a.H, plan.nseg, plan.seg_len,
+                    a.n, a.d, a.d, nullptr, nullptr, stream, true);
   if (e != cudaSuccess) return e;
   if (a.d == 128) return run_readout<128>(a, tot_state, tot_z, plan, true, stream);
   if (a.d == 64) return run_readout<64>(a, tot_state, tot_z, plan, true, stream);

@@ -143,6 +143,16 @@ cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* 
                          cudaStream_t stream, bool dependent, const float* init_state = nullptr,
                          const float* init_z = nullptr);
 
+// The total of the same recurrence over all nseg aggregates of every head
+// (acc ← init, then acc ← a^{L_g}·acc + A_g) into tot_state / tot_z, without
+// the exclusive prefixes; the aggregates are left as they are.  float4
+// loads (the scalar segment_scan when a pointer is not 16-byte aligned).
+cudaError_t segment_total(float* ws_state, float* ws_z, float* tot_state, float* tot_z,
+                          int64_t BH, int64_t H, int nseg, int64_t seg_len, int64_t n, int dp, int d,
+                          const float* decay, const float* seg_ld, cudaStream_t stream,
+                          bool dependent, const float* init_state = nullptr,
+                          const float* init_z = nullptr);
+
 // la_forward with a fixed workspace of ws_floats floats, fetched through
 // get_ws only when the plan needs it, instead of stream-ordered allocations
 // (see la_forward_noalloc).
