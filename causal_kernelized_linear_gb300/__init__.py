@@ -25,15 +25,17 @@ Python face of liblinattn (C ABI in include/linattn.h).  The method
 All work runs in the library's CUDA kernels; PyTorch only allocates device
 memory and provides the stream.
 """
-from ._binding import (EXPORTED, LinAttnError, backward, decode_step, decode_step_token_decay,
-                       forward, forward_from_state, forward_host, forward_state,
-                       forward_token_decay, forward_with_state, last_device_status,
-                       launch_count, library_path, load, selftest_wait_timeout,
-                       shard_entering_state, status_string)
+from ._binding import (EXPORTED, LinAttnError, backward, debug_build, decode_step,
+                       decode_step_token_decay, forward, forward_from_state, forward_host,
+                       forward_state, forward_token_decay, forward_with_state, last_device_check,
+                       last_device_status, launch_count, library_path, load,
+                       selftest_device_check, selftest_wait_timeout, shard_entering_state,
+                       status_string)
 from .build import build
 
 __all__ = ["forward", "forward_host", "forward_with_state", "forward_from_state", "forward_state",
            "shard_entering_state", "decode_step", "forward_token_decay", "backward",
            "decode_step_token_decay", "last_device_status", "status_string",
            "LinAttnError", "build", "load", "library_path", "launch_count",
-           "selftest_wait_timeout", "EXPORTED"]
+           "selftest_wait_timeout", "debug_build", "last_device_check", "selftest_device_check",
+           "EXPORTED"]

@@ -21,6 +21,7 @@ LA_ERR_UNSUPPORTED = 2
 LA_ERR_CUDA = 3
 LA_ERR_TIMEOUT = 4
 LA_ERR_OUT_OF_MEMORY = 5
+LA_ERR_DEVICE_CHECK = 6
 
 LA_BF16 = 0
 LA_F32 = 1
@@ -34,7 +35,8 @@ EXPORTED = ("la_forward", "la_forward_with_state", "la_decode_step", "la_status_
             "la_get_last_device_status", "la_launch_count", "la_selftest_wait_timeout",
             "la_decode_step_fm", "la_forward_token_decay", "la_decode_step_token_decay",
             "la_backward", "la_forward_from_state", "la_forward_state", "la_shard_entering_state",
-            "la_forward_host")
+            "la_forward_host", "la_debug_build", "la_get_last_device_check",
+            "la_selftest_device_check")
 
 
 class LinAttnError(RuntimeError):
@@ -55,20 +57,27 @@ _lock = threading.Lock()
 _lib = None
 
 
+def debug_selected() -> bool:
+    """Whether this process uses the LA_DEBUG build (environment LA_DEBUG=1)."""
+    return os.environ.get("LA_DEBUG") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB_PATH
+    return _build.DEBUG_LIB_PATH if debug_selected() else _build.LIB_PATH
 
 
 def load():
-    """Load liblinattn.so (built in-tree by ``causal_kernelized_linear_gb300.build``)."""
+    """Load liblinattn.so (built in-tree by ``causal_kernelized_linear_gb300.build``;
+    with LA_DEBUG=1 in the environment, the LA_DEBUG build from ``build --debug``)."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB_PATH
+        path = library_path()
         if not os.path.exists(path):
+            flag = " --debug" if debug_selected() else ""
             raise RuntimeError(f"liblinattn.so is not built ({path}); run "
-                               "`python -m causal_kernelized_linear_gb300.build`")
+                               f"`python -m causal_kernelized_linear_gb300.build{flag}`")
         lib = ctypes.CDLL(path)
         P = ctypes.POINTER(LaTensor)
         vp = ctypes.c_void_p
@@ -108,6 +117,12 @@ def load():
         lib.la_launch_count.restype = ctypes.c_uint64
         lib.la_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
         lib.la_selftest_wait_timeout.restype = ctypes.c_int
+        lib.la_debug_build.argtypes = []
+        lib.la_debug_build.restype = ctypes.c_int
+        lib.la_get_last_device_check.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+        lib.la_get_last_device_check.restype = ctypes.c_int
+        lib.la_selftest_device_check.argtypes = [vp]
+        lib.la_selftest_device_check.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -482,6 +497,26 @@ def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     returned status is that of the launch (the timeout itself is reported by
     last_device_status)."""
     return int(load().la_selftest_wait_timeout(int(limit_ns), _stream_handle(stream)))
+
+
+def debug_build() -> bool:
+    """la_debug_build: whether the loaded library is the LA_DEBUG build."""
+    return bool(load().la_debug_build())
+
+
+def last_device_check(stream=None):
+    """la_get_last_device_check: synchronises the stream and returns (and
+    clears) the device status word with the site of a failed LA_DEBUG check:
+    (status, site)."""
+    site = ctypes.c_int(0)
+    st = int(load().la_get_last_device_check(_stream_handle(stream), ctypes.byref(site)))
+    return st, int(site.value)
+
+
+def selftest_device_check(stream=None) -> int:
+    """la_selftest_device_check: queue the LA_DEBUG check self-test kernel
+    (LA_ERR_UNSUPPORTED in the release build)."""
+    return int(load().la_selftest_device_check(_stream_handle(stream)))
 
 
 def launch_count() -> int:

@@ -20,6 +20,9 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liblinattn.so")
+# the LA_DEBUG build (device-side index checks), apart from the product library
+DEBUG_BUILD_DIR = os.path.join(PKG_DIR, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(DEBUG_BUILD_DIR, "liblinattn.so")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CXX_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
@@ -42,23 +45,31 @@ def _deps():
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(debug: bool = False) -> bool:
+    path = DEBUG_LIB_PATH if debug else LIB_PATH
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile every ``csrc/*.cu`` for sm_103a and link liblinattn.so."""
-    if not force and up_to_date():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
+          debug: bool = False) -> str:
+    """Compile every ``csrc/*.cu`` for sm_103a and link liblinattn.so; with
+    ``debug``, the LA_DEBUG build (kernels check their indices) in a folder
+    of its own."""
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    if not force and up_to_date(debug):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    if debug:
+        extra.append("-DLA_DEBUG")
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH_FLAGS, *CXX_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -72,15 +83,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         for obj, log in results:
             if log.strip():
                 print(f"== {os.path.basename(obj)}\n{log}", file=sys.stderr)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH_FLAGS, "-shared", "-cudart", "shared", "-o", tmp,
            *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_verbose="--ptxas-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_verbose="--ptxas-v" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -2,6 +2,7 @@
 // path selection, segment planning and workspace, device status word.
 #include "linattn.h"
 
+#include "common.cuh"
 #include "internal.h"
 
 #include <cuda_runtime.h>
@@ -42,15 +43,17 @@ ApiRange::~ApiRange() {
 
 namespace {
 
-// Per-device status word written by kernels whose bounded waits expire.
-__device__ int g_device_status;
+// Per-device status word: [0] the first error a kernel recorded (a bounded
+// wait that expired; in LA_DEBUG builds also a failed device-side check),
+// [1] the site number of a failed check.
+__device__ int g_device_status[2];
 
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
-  int* status = nullptr;  // device address of g_device_status
+  int* status = nullptr;  // device address of g_device_status[0]
 };
 
 std::mutex g_mu;
@@ -857,6 +860,8 @@ la_status la_decode_step(float* mu, float* nu, const la_tensor* q, const la_tens
   return la_decode_step_fm(mu, nu, q, k, v, decay_a, LA_FM_ELU1, nullptr, out, stream);
 }
 
+static_assert(la::kStatusDeviceCheck == LA_ERR_DEVICE_CHECK, "device check status code");
+
 const char* la_status_string(la_status status) {
   switch (status) {
     case LA_OK: return "LA_OK";
@@ -865,6 +870,7 @@ const char* la_status_string(la_status status) {
     case LA_ERR_CUDA: return "LA_ERR_CUDA";
     case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT";
     case LA_ERR_OUT_OF_MEMORY: return "LA_ERR_OUT_OF_MEMORY";
+    case LA_ERR_DEVICE_CHECK: return "LA_ERR_DEVICE_CHECK";
   }
   return "LA_ERR_UNKNOWN";
 }
@@ -880,23 +886,57 @@ la_status la_selftest_wait_timeout(uint64_t limit_ns, la_stream stream) {
   return la::to_status(la::selftest_wait(di.status, limit_ns, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-la_status la_get_last_device_status(la_stream stream) {
-  la::ApiRange range_("la_get_last_device_status");
+// Synchronises the stream, reads and clears the device status word; *site
+// gets the site of a failed device-side check (0 if none).
+static la_status read_device_status(la_stream stream, int* site) {
   la::DeviceInfo di;
   la_status st = la::device_info(&di);
   if (st != LA_OK) return st;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return LA_ERR_CUDA;
-  int word = 0;
-  if (cudaMemcpy(&word, di.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+  int word[2] = {0, 0};
+  if (cudaMemcpy(word, di.status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
     return LA_ERR_CUDA;
-  if (word != 0) {
-    const int zero = 0;
-    if (cudaMemcpy(di.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+  if (site) *site = word[0] == la::kStatusDeviceCheck ? word[1] : 0;
+  if (word[0] != 0 || word[1] != 0) {
+    const int zero[2] = {0, 0};
+    if (cudaMemcpy(di.status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
       return LA_ERR_CUDA;
-    return static_cast<la_status>(word);
   }
-  return LA_OK;
+  return static_cast<la_status>(word[0]);
+}
+
+la_status la_get_last_device_status(la_stream stream) {
+  la::ApiRange range_("la_get_last_device_status");
+  return read_device_status(stream, nullptr);
+}
+
+la_status la_get_last_device_check(la_stream stream, int* site) {
+  la::ApiRange range_("la_get_last_device_check");
+  if (!site) return LA_ERR_INVALID_ARG;
+  *site = 0;
+  return read_device_status(stream, site);
+}
+
+int la_debug_build(void) {
+#ifdef LA_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+la_status la_selftest_device_check(la_stream stream) {
+  la::ApiRange range_("la_selftest_device_check");
+#ifdef LA_DEBUG
+  la::DeviceInfo di;
+  la_status st = la::device_info(&di);
+  if (st != LA_OK) return st;
+  return la::to_status(la::selftest_check(di.status, reinterpret_cast<cudaStream_t>(stream)));
+#else
+  (void)stream;
+  return LA_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // extern "C"

@@ -450,7 +450,7 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
   item_range(p.items, ib, ie);
   // the K and V tiles of item `it` (issued while the previous item finishes)
   auto issue = [&](int64_t it) {
-    if (it >= ie) return;
+    if (it >= ie || !LA_DCHECK(p.status, it < p.items, 21)) return;
     const int ibh = (int)(it / p.nch), it0 = (int)(it % p.nch) * kCb;
     arm_tiles(x, 2 * Cfg::TILE);
     tile_load<D>(x, &map_k, Cfg::oK, it0, ibh);
@@ -540,7 +540,7 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
   // while the previous item finishes, each as soon as its region is free: V
   // (arming the barrier for all of them), then K, then the rest
   auto issue_v = [&](int64_t it) {
-    if (it >= ie) return;
+    if (it >= ie || !LA_DCHECK(p.status, it < p.items, 22)) return;
     arm_tiles(x, 4 * Cfg::TILE + Cfg::STILE + D * 4);
     tile_load<D>(x, &map_v, Cfg::oV, (int)(it % p.nch) * kCb, (int)(it / p.nch));
   };
@@ -811,7 +811,8 @@ bt_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     tc_fence_before();
     __syncthreads();   // ∂q is staged
     tc_fence_after();
-    if (threadIdx.x == 0) {
+    // stores start at a non-negative row of the tensor (rows past n are clipped)
+    if (threadIdx.x == 0 && LA_DCHECK(p.status, t0 >= 0 && t0 < p.n && bh * p.nch < p.items, 24)) {
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) tma_store_3d(&map_dq, dq_stage + h * kCb * 128, h * 64, t0, (int)bh);
       tma_store_commit();
@@ -863,7 +864,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   // Q, V, ∂o tiles and the M_c operand tile, then (once the K tile and N_c
   // have been read) the K tile and N_c; ρ and den of its rows into registers
   auto issue_a = [&](int64_t it) {
-    if (it >= ie) return;
+    if (it >= ie || !LA_DCHECK(p.status, it < p.items, 23)) return;
     const int ibh = (int)(it / p.nch), it0 = (int)(it % p.nch) * kCb;
     arm_tiles(x, 4 * Cfg::TILE + Cfg::STILE + D * 4);
     tile_load<D>(x, &map_q, Cfg::oQ, it0, ibh);
@@ -1035,7 +1036,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     tc_fence_before();
     __syncthreads();
     issue_b(item + 1);   // the K tile and N_c are consumed
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && LA_DCHECK(p.status, t0 >= 0 && t0 < p.n && bh * p.nch < p.items, 25)) {
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) tma_store_3d(&map_dk, stage + h * kCb * 128, h * 64, t0, (int)bh);
       tma_store_commit();
@@ -1061,7 +1062,7 @@ bt_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && LA_DCHECK(p.status, t0 >= 0 && t0 < p.n && bh * p.nch < p.items, 26)) {
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) tma_store_3d(&map_dv, stage + h * kCb * 128, h * 64, t0, (int)bh);
       tma_store_commit();

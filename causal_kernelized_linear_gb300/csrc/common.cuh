@@ -31,4 +31,24 @@ __device__ __forceinline__ float decay_pow(float a, int64_t k) {
   return k == 0 ? 1.f : powf(a, (float)k);
 }
 
+// Status code of a failed device-side check of the LA_DEBUG build (the same
+// value as LA_ERR_DEVICE_CHECK in the public header).
+constexpr int kStatusDeviceCheck = 6;
+
+// LA_DCHECK(status, cond, site) guards an index, offset or TMA coordinate the
+// kernel is about to use.  In an LA_DEBUG build it evaluates cond; when cond
+// is false it records kStatusDeviceCheck in status[0] and the site number in
+// status[1] (the first failure wins, and a recorded timeout is kept) and
+// yields false, so that the caller skips the access.  In the release build it
+// is `true` and cond is not evaluated.  Sites are numbered per kernel file.
+#ifdef LA_DEBUG
+__device__ __noinline__ inline bool dcheck_failed(int* status, int site) {
+  if (status && atomicCAS(status, 0, kStatusDeviceCheck) == 0) atomicExch(status + 1, site);
+  return false;
+}
+#define LA_DCHECK(status, cond, site) ((cond) || ::la::dcheck_failed((status), (site)))
+#else
+#define LA_DCHECK(status, cond, site) true
+#endif
+
 }  // namespace la

@@ -390,6 +390,54 @@ segment_scan_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z
   }
 }
 
+// segment_scan_kernel with four consecutive state elements per thread
+// (float4 loads and stores; dp a multiple of 4 and every pointer 16-byte
+// aligned).
+__global__ void __launch_bounds__(256)
+segment_scan4_kernel(float* ws_state, float* ws_z, float* tot_state, float* tot_z, int64_t H,
+                     int nseg, int nagg, int64_t seg_len, int64_t n, int dpd, int dp,
+                     const float* decay, const float* seg_ld, const float* init_state,
+                     const float* init_z) {
+  constexpr int kBatch = 8;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t bh = blockIdx.x;
+  const int e4 = (blockIdx.y * 256 + threadIdx.x) * 4;
+  if (e4 >= dpd + dp) return;
+  const bool mat = e4 < dpd;
+  float* base = mat ? ws_state + bh * nseg * (int64_t)dpd + e4 : ws_z + bh * nseg * (int64_t)dp + (e4 - dpd);
+  const int64_t stride = mat ? dpd : dp;
+  const float a = decay ? decay[bh % H] : 1.f;
+  const float a_full = decay_pow(a, seg_len);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);   // state entering segment g
+  if (init_state)
+    acc = mat ? *reinterpret_cast<const float4*>(init_state + bh * dpd + e4)
+              : *reinterpret_cast<const float4*>(init_z + bh * dp + (e4 - dpd));
+  for (int g0 = 0; g0 < nseg; g0 += kBatch) {
+    float4 agg[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      agg[j] = (g0 + j < nagg) ? *reinterpret_cast<const float4*>(base + (g0 + j) * stride)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int g = g0 + j;
+      if (g < nseg) {
+        *reinterpret_cast<float4*>(base + g * stride) = acc;
+        const int64_t len = min(seg_len, n - (int64_t)g * seg_len);
+        const float fac = seg_ld ? (g < nagg ? exp2f(seg_ld[bh * nseg + g]) : 0.f)
+                                 : (len == seg_len ? a_full : decay_pow(a, len));
+        acc = make_float4(fac * acc.x + agg[j].x, fac * acc.y + agg[j].y, fac * acc.z + agg[j].z,
+                          fac * acc.w + agg[j].w);
+      }
+    }
+  }
+  if (tot_state && nagg == nseg) {
+    if (mat) *reinterpret_cast<float4*>(tot_state + bh * dpd + e4) = acc;
+    else *reinterpret_cast<float4*>(tot_z + bh * dp + (e4 - dpd)) = acc;
+  }
+}
+
 // The total of every head's segment aggregates alone (no exclusive prefixes):
 // acc ← init, then acc ← fac_g·acc + A_g over the segments g, four
 // consecutive state elements per thread, all of a head's aggregates loaded
@@ -565,8 +613,11 @@ cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* 
                          cudaStream_t stream, bool dependent, const float* init_state,
                          const float* init_z) {
   const int dpd = dp * d;
+  auto a16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+  const bool vec = dp % 4 == 0 && a16(ws_state) && a16(ws_z) && a16(tot_state) && a16(tot_z) &&
+                   a16(init_state) && a16(init_z);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)BH, (unsigned)((dpd + dp + 255) / 256));
+  cfg.gridDim = dim3((unsigned)BH, (unsigned)(((vec ? (dpd + dp) / 4 : dpd + dp) + 255) / 256));
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -574,9 +625,9 @@ cudaError_t segment_scan(float* ws_state, float* ws_z, float* tot_state, float* 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, segment_scan_kernel, ws_state, ws_z, tot_state, tot_z,
-                                     H, nseg, nagg, seg_len, n, dpd, dp, decay, seg_ld,
-                                     init_state, init_z);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, vec ? segment_scan4_kernel : segment_scan_kernel,
+                                     ws_state, ws_z, tot_state, tot_z, H, nseg, nagg, seg_len, n,
+                                     dpd, dp, decay, seg_ld, init_state, init_z);
   count_launches(1);
   return e;
 }

@@ -295,6 +295,8 @@ __device__ __forceinline__ void role_producer(const Ctx& x, const CUtensorMap* m
   uint64_t* bar = x.bar;
   int last_q = -1, last_k = -1, last_v = -1;
   auto load = [&](const CUtensorMap* map, int off, uint64_t* b, int y) {
+    // the tile's first row lies in this CTA's token range
+    if (!LA_DCHECK(x.status, y >= x.t_begin && y < x.t_end, 11)) return;
     mbar_arrive_expect_tx(b, Cfg::TILE);
     for (int h = 0; h < Cfg::HALVES; ++h)
       tma_load_3d(x.sm + off + h * kC * 128, map, b, h * 64, y, (int)x.bh);
@@ -742,7 +744,7 @@ __device__ __forceinline__ void role_rows(const Ctx& x, __nv_bfloat16* out, int6
     tmem_ld_wait();
     const float inv_den = 1.f / __uint_as_float(den);
     const int64_t row = x.t_begin + (int64_t)c * kC + r;
-    const bool valid = row < x.t_end;
+    const bool valid = row < x.t_end && LA_DCHECK(x.status, x.t_end <= p_n, 12);
     uint4* orow = reinterpret_cast<uint4*>(out + (x.bh * p_n + (valid ? row : 0)) * D);
 #pragma unroll 1
     for (int j0 = 0; j0 < D; j0 += 32) {
@@ -805,8 +807,10 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   float* out_z = nullptr;
   if (!FULL) {
     const int64_t slot = x.bh * (p.nseg + p.init_slot) + x.g + p.init_slot;
-    out_S = p.ws_state + slot * (int64_t)(D * D);
-    out_z = p.ws_z + slot * (int64_t)D;
+    if (LA_DCHECK(x.status, x.bh < gridDim.x && x.g < p.nseg, 13)) {
+      out_S = p.ws_state + slot * (int64_t)(D * D);
+      out_z = p.ws_z + slot * (int64_t)D;
+    }
   } else if (p.fin_state && x.g == p.nseg - 1) {
     out_S = p.fin_state + x.bh * (int64_t)(D * D);
     out_z = p.fin_z + x.bh * (int64_t)D;
@@ -890,7 +894,7 @@ __device__ __forceinline__ void role_state(const Ctx& x, const TcParams& p, int 
   // S ← 0, then S ← a^L·S + slot_j for the nin slots before this segment
   if (ok) {
     const int nin = x.g + p.init_slot;
-    const bool have_in = FULL && nin > 0;
+    const bool have_in = FULL && nin > 0 && LA_DCHECK(x.status, x.g < p.nseg, 14);
     if (have_in) grid_dependency_wait();
     // segment j carries the state through it with aL (per-token decay: its
     // own total 2^{ws_ld})

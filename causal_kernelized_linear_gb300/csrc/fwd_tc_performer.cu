@@ -175,6 +175,8 @@ __device__ __forceinline__ void role_producer(const PCtx& x, const CUtensorMap* 
     const int u = stages == 2 ? (c >> 1) : c;          // use index of the stage
     if (c >= stages && !mbar_wait(&bar[empty + s], (u - 1) & 1, x.status, x.abort_flag))
       return false;
+    // the tile's first row lies in this CTA's token range
+    if (!LA_DCHECK(x.status, y >= x.t_begin && y < x.t_end, 41)) return false;
     mbar_arrive_expect_tx(&bar[full + s], Cfg::TILE);
     tma_load_3d(x.sm + (s ? off1 : off0), map, &bar[full + s], 0, y, (int)x.bh);
     last[which] = c;
@@ -655,7 +657,7 @@ __device__ __forceinline__ void role_rows(const PCtx& x, const PParams& p, int w
     const float qz = qzbuf[((c & 1) * 2) * kC + r] + qzbuf[((c & 1) * 2 + 1) * kC + r];
     const float inv_den = 1.f / (__uint_as_float(psum) + qz);
     const int64_t row = x.t_begin + (int64_t)c * kC + r;
-    const bool valid = row < x.t_end;
+    const bool valid = row < x.t_end && LA_DCHECK(x.status, x.t_end <= p.n, 42);
     uint4* orow = reinterpret_cast<uint4*>(p.out + (x.bh * p.n + (valid ? row : 0)) * kD);
 #pragma unroll 1
     for (int j0 = 0; j0 < kD; j0 += 32) {

@@ -96,8 +96,10 @@ __device__ __forceinline__ void role_producer(const RCtx& x, const CUtensorMap* 
     const int s = c % Cfg::NQ;
     const int u = c / Cfg::NQ;   // use of the stage
     if (u >= 1 && !mbar_wait(&bar[Bar::QEMPTY + s], (u - 1) & 1, x.status, x.abort_flag)) break;
-    mbar_arrive_expect_tx(&bar[Bar::QFULL + s], Cfg::TILE);
     const int y = (int)(x.t_begin + (int64_t)c * kC);
+    // the tile's first row lies in this CTA's token range
+    if (!LA_DCHECK(x.status, y >= x.t_begin && y < x.t_end, 31)) break;
+    mbar_arrive_expect_tx(&bar[Bar::QFULL + s], Cfg::TILE);
     for (int h = 0; h < Cfg::HALVES; ++h)
       tma_load_3d(x.sm + Cfg::oQ0 + s * Cfg::TILE + h * kC * 128, mq, &bar[Bar::QFULL + s], h * 64,
                   y, (int)x.bh);
@@ -220,7 +222,7 @@ __device__ __forceinline__ void role_epilogue(const RCtx& x, const RParams& p, i
       mbar_arrive(&bar[Bar::QEMPTY + s]);   // the den partials of this stage are read
     }
     const int64_t t = x.t_begin + (int64_t)c * kC + r;
-    if (t < x.t_end) {
+    if (t < x.t_end && LA_DCHECK(x.status, x.t_end <= p.n, 32)) {
       uint4* orow = reinterpret_cast<uint4*>(p.out + (x.bh * p.n + t) * D);
 #pragma unroll
       for (int q = 0; q < D / 8; ++q)

@@ -182,6 +182,8 @@ class ApiRange {
 
 // One CTA of bounded waits on a barrier nothing signals (la_selftest_wait_timeout).
 cudaError_t selftest_wait(int* status, uint64_t limit_ns, cudaStream_t stream);
+// One guarded access whose LA_DEBUG check fails (la_selftest_device_check).
+cudaError_t selftest_check(int* status, cudaStream_t stream);
 
 // Backward of the causal forward (fp32 CUDA cores): ∂q, ∂k, ∂v and ∂a.
 bool backward_supported(int d, int m, bool performer);

@@ -1,6 +1,9 @@
-// Self-test of the bounded-wait failure path (la_selftest_wait_timeout): one
-// CTA waits, with the waits of the tensor-core kernels, on an mbarrier that
-// nothing signals, and must give up with LA_ERR_TIMEOUT in the status word.
+// Self-tests of the failure paths: la_selftest_wait_timeout (one CTA waits,
+// with the waits of the tensor-core kernels, on an mbarrier that nothing
+// signals, and must give up with LA_ERR_TIMEOUT in the status word) and
+// la_selftest_device_check (a device-side check of the LA_DEBUG build that
+// fails and must record LA_ERR_DEVICE_CHECK without making the access).
+#include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
 
@@ -27,7 +30,26 @@ __global__ void __launch_bounds__(64, 1) selftest_wait_kernel(int* status, uint6
   if (warp == 1 && (threadIdx.x & 31) == 0) mbar_wait(&bar, 0, status, &abort_flag, limit_ns);
 }
 
+// One thread guards an access with an index one past a 4-element buffer.  In
+// an LA_DEBUG build the check fails, records LA_ERR_DEVICE_CHECK with site 90
+// and the access is skipped; the index is masked as well, so the access stays
+// inside the buffer in any build.
+__global__ void __launch_bounds__(32, 1) selftest_check_kernel(int* status, int i, int* sink) {
+  __shared__ int buf[4];
+  if (threadIdx.x == 0) {
+    buf[0] = buf[1] = buf[2] = buf[3] = 0;
+    if (LA_DCHECK(status, i >= 0 && i < 4, 90)) buf[i & 3] = 1;
+    if (sink) *sink = buf[0] + buf[1] + buf[2] + buf[3];
+  }
+}
+
 }  // namespace
+
+cudaError_t selftest_check(int* status, cudaStream_t stream) {
+  selftest_check_kernel<<<1, 32, 0, stream>>>(status, 4, nullptr);
+  count_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t selftest_wait(int* status, uint64_t limit_ns, cudaStream_t stream) {
   selftest_wait_kernel<<<1, 64, 0, stream>>>(status, limit_ns);

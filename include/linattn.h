@@ -48,14 +48,17 @@ extern "C" {
 #endif
 
 /* Status codes.  LA_ERR_CUDA carries a CUDA runtime error from a launch or an
- * allocation; LA_ERR_TIMEOUT reports a bounded device-side wait that gave up. */
+ * allocation; LA_ERR_TIMEOUT reports a bounded device-side wait that gave up;
+ * LA_ERR_DEVICE_CHECK exists only in the LA_DEBUG build of the library. */
 typedef enum {
   LA_OK = 0,
   LA_ERR_INVALID_ARG = 1,   /* null pointer, shape or dtype mismatch, misalignment */
   LA_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels implement */
   LA_ERR_CUDA = 3,          /* a CUDA runtime call failed */
   LA_ERR_TIMEOUT = 4,       /* a device-side bounded wait expired (see la_get_last_device_status) */
-  LA_ERR_OUT_OF_MEMORY = 5  /* workspace allocation failed */
+  LA_ERR_OUT_OF_MEMORY = 5, /* workspace allocation failed */
+  LA_ERR_DEVICE_CHECK = 6   /* LA_DEBUG build: a kernel's index check failed and the
+                               access was skipped (see la_get_last_device_check) */
 } la_status;
 
 typedef enum { LA_BF16 = 0, LA_F32 = 1 } la_dtype;
@@ -373,6 +376,47 @@ uint64_t la_launch_count(void);
  * fails, else LA_OK.  No counterpart on the pages.
  */
 la_status la_selftest_wait_timeout(uint64_t limit_ns, la_stream stream);
+
+/*
+ * The LA_DEBUG build.  Compiled with -DLA_DEBUG (`python -m
+ * causal_kernelized_linear_gb300.build --debug`, into a library of its own),
+ * the kernels check the indices, workspace slots and TMA coordinates they are
+ * about to use — that a tile's first row lies in the CTA's token range, that
+ * an output row lies inside the tensor, that a workspace slot belongs to the
+ * head, that a TMA store starts at a non-negative row.  A failed check
+ * records LA_ERR_DEVICE_CHECK and the check's site number in the device
+ * status word (the first error of either kind wins) and skips the access;
+ * nothing traps.  Kernels waiting on a skipped load then give up through
+ * their bounded waits.  The release build compiles the checks away and
+ * otherwise runs the same arithmetic, so both give identical results.
+ *
+ * la_debug_build — 1 in the LA_DEBUG build, 0 otherwise.  Never fails.
+ */
+int la_debug_build(void);
+
+/*
+ * la_get_last_device_check — la_get_last_device_status that also reports,
+ * in *site, the site number of the first failed check when the status is
+ * LA_ERR_DEVICE_CHECK (0 otherwise).  Synchronises `stream`, then clears the
+ * word.  Site numbers: 11–14 the tcgen05 elu+1 forward (tile rows, output
+ * rows, the aggregate slot, the entering-state slots), 21–26 the tcgen05
+ * backward (item ranges of the loads, rows of the ∂q, ∂k, ∂v stores), 31–32
+ * the non-causal readout, 41–42 the Performer forward, 90 the self-test.
+ * Errors: LA_ERR_INVALID_ARG (site is NULL), LA_ERR_CUDA.
+ */
+la_status la_get_last_device_check(la_stream stream, int* site);
+
+/*
+ * la_selftest_device_check — test hook for the LA_DEBUG checks.  Queues one
+ * small kernel whose guarded access has an index one past its 4-element
+ * shared-memory buffer: the check fails, records LA_ERR_DEVICE_CHECK with
+ * site 90 and the access is skipped (the index is also masked into the
+ * buffer, so no build can touch memory outside it).  A following
+ * la_get_last_device_check(stream, &site) returns LA_ERR_DEVICE_CHECK and
+ * site 90.  Returns LA_ERR_UNSUPPORTED in the release build (nothing
+ * queued), LA_ERR_CUDA if the launch fails, else LA_OK.
+ */
+la_status la_selftest_device_check(la_stream stream);
 
 #ifdef __cplusplus
 }

@@ -270,3 +270,34 @@ def test_nvtx_ranges_do_not_change_results_of_host_checks(tmp_path):
                        timeout=120)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.split() == [str(B.LA_ERR_INVALID_ARG), str(B.LA_ERR_INVALID_ARG)]
+
+
+def test_release_build_reports_itself_and_refuses_the_check_selftest(lib):
+    assert lib.la_debug_build() == 0
+    assert cl.status_string(B.LA_ERR_DEVICE_CHECK) == "LA_ERR_DEVICE_CHECK"
+    # the release build compiles the device-side checks away: the self-test
+    # is refused before anything is queued
+    assert lib.la_selftest_device_check(None) == B.LA_ERR_UNSUPPORTED
+    assert lib.la_get_last_device_check(None, None) == B.LA_ERR_INVALID_ARG
+
+
+@pytest.mark.timeout(600)
+def test_debug_build_compiles_and_exports_the_same_boundary(tmp_path):
+    # the LA_DEBUG library (kernels check their indices) builds from the same
+    # sources into a folder of its own and exports every declared symbol
+    import subprocess
+    import sys
+    import importlib
+    bld = importlib.import_module("causal_kernelized_linear_gb300.build")
+    path = bld.build(debug=True)
+    assert path == bld.DEBUG_LIB_PATH and os.path.exists(path)
+    code = (
+        "import ctypes, sys\n"
+        f"lib = ctypes.CDLL({path!r})\n"
+        f"names = {sorted(_declared_functions())!r}\n"
+        "missing = [n for n in names if not hasattr(lib, n)]\n"
+        "lib.la_debug_build.restype = ctypes.c_int\n"
+        "print(lib.la_debug_build(), len(missing))\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.split() == ["1", "0"], r.stdout
