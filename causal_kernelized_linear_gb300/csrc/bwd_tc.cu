@@ -60,14 +60,12 @@ struct BtCfg {
   static constexpr int oV = oK + TILE;
   static constexpr int oG = oV + TILE;
   static constexpr int oS = oG + TILE;
-  // staging for stores, apart from the tiles (which the next item's loads may
-  // already be filling): half an fp32 [D' × D] matrix with rows padded to
-  // D/2 + 4 (coalesced stores of the state pass), two fp32 [D × 32] boxes or
-  // one bf16 [128 × D] tile with the 128-byte swizzle (TMA stores)
+  // staging for the TMA stores, apart from the tiles (which the next item's
+  // loads may already be filling): two fp32 [D × 32] boxes or one bf16
+  // [128 × D] tile, with the 128-byte swizzle
   static constexpr int oST = oS + STILE;
-  static constexpr int STG_F32 = (D / 2 + 4) * D * 4;
   static constexpr int STG_TMA = TILE > 2 * D * 128 ? TILE : 2 * D * 128;
-  static constexpr int oZ = oST + (STG_F32 > STG_TMA ? STG_F32 : STG_TMA);   // fp32 [D]: z_c or N_c
+  static constexpr int oZ = oST + STG_TMA;       // fp32 [D]: z_c or N_c
   static constexpr int oRHO = oZ + D * 4;        // fp32 [128]
   static constexpr int oDEN = oRHO + kCb * 4;    // fp32 [128]
   static constexpr int oPW = oDEN + kCb * 4;     // fp32 a^k, k = 0..128
@@ -255,44 +253,6 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
 }
 
 // The fp32 [D' × D] accumulator in TMEM (lane = row, columns col0..col0+D)
-// to a contiguous row-major matrix in global memory, in two rounds of D/2
-// columns.  Rows go through shared memory (`stage`, (D/2 + 4)·D floats; the
-// padding spreads a warp's 16-byte writes over all banks) so that the global
-// stores are coalesced; the two threads of a row read alternate 32-column
-// steps of TMEM.  Every thread of the CTA calls it (it holds CTA barriers).
-template <int D>
-__device__ __forceinline__ void store_tmem_matrix(uint32_t tmem, uint32_t col0, float* stage,
-                                                  float* __restrict__ dst) {
-  constexpr int HC = D / 2, SR = HC + 4;
-  const int r = threadIdx.x & (kCb - 1), part = threadIdx.x / kCb;
-  float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {
-    if (r < D) {
-      const uint32_t lane_base = (uint32_t)(r >> 5) * 32;
-#pragma unroll 1
-      for (int j0 = part * 32; j0 < HC; j0 += 64) {
-        uint32_t v[32];
-        tmem_ld32(tmem_addr(tmem, lane_base, col0 + hh * HC + j0), v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float4*>(stage + r * SR + j0 + 4 * q) =
-              make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                          __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-      }
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int e = threadIdx.x; e < D * HC / 4; e += kThreadsB) {
-      const int row = e / (HC / 4), c4 = e % (HC / 4);
-      d4[row * (D / 4) + hh * (HC / 4) + c4] = *reinterpret_cast<const float4*>(stage + row * SR + c4 * 4);
-    }
-    __syncthreads();
-  }
-}
-
-// The fp32 [D' × D] accumulator in TMEM (lane = row, columns col0..col0+D)
 // to matrix `item` of `map` (fp32 [D × D] matrices, boxes of 32 columns × D
 // rows with the 128-byte swizzle): staged box by box in shared memory
 // (`stage`, two boxes, 1024-byte aligned) and written by TMA stores, two
@@ -437,7 +397,7 @@ struct BtSetup {
 template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1)
 bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                const BtParams p) {
+                const __grid_constant__ CUtensorMap map_ds, const BtParams p) {
   using Cfg = BtCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   Bt x;
@@ -495,12 +455,13 @@ bt_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     // Δz on the CUDA cores meanwhile (rows ≥ cs of K'' are zero)
     tile_colsum<D>(x.sm + Cfg::oK, [](int) { return 1.f; },
                    reinterpret_cast<float*>(x.sm + Cfg::oS), p.z + item * D);
+    if (threadIdx.x == 0) tma_store_wait_read0();   // the previous item's ΔS left the stage
     if (!wait_mma(x)) break;
     issue(item + 1);   // K'' and V are consumed
-    store_tmem_matrix<D>(x.tmem, 0, reinterpret_cast<float*>(x.sm + Cfg::oST),
-                         p.S + item * (int64_t)(D * D));
+    store_tmem_matrix_tma<D>(x.tmem, 0, x.sm + Cfg::oST, &map_ds, item);
     tc_fence_before();
   }
+  if (threadIdx.x == 0) tma_store_wait0();   // ΔS is in global memory
   BtSetup<D>::teardown(x);
 }
 
@@ -1241,7 +1202,8 @@ cudaError_t run_bt(const BwdArgs& a, float* ws, int num_sms, int* status, cudaSt
   p.rho = cur; cur += (size_t)BH * a.n;
   p.dapart = cur;
   p.da_parts = 2 * nch + (int)sgrid.y * 8;
-  CUtensorMap mq, mk, mv, mg, mdq, mdk, mdv, mdm;
+  CUtensorMap mq, mk, mv, mg, mdq, mdk, mdv, mdm, mds;
+  if ((e = tmap_f32_mats(&mds, p.S, (int64_t)ns, D)) != cudaSuccess) return e;
   if ((e = tmap_rows(&mdq, a.dq, BH, a.n, D, kCb)) != cudaSuccess) return e;
   if ((e = tmap_rows(&mdk, a.dk, BH, a.n, D, kCb)) != cudaSuccess) return e;
   if ((e = tmap_rows(&mdv, a.dv, BH, a.n, D, kCb)) != cudaSuccess) return e;
@@ -1261,7 +1223,7 @@ cudaError_t run_bt(const BwdArgs& a, float* ws, int num_sms, int* status, cudaSt
                                 smem)) != cudaSuccess)
     return e;
   const unsigned grid = (unsigned)std::min<int64_t>(p.items, (int64_t)num_sms);
-  bt_state_kernel<D><<<grid, kThreadsB, smem, stream>>>(mk, mv, p);
+  bt_state_kernel<D><<<grid, kThreadsB, smem, stream>>>(mk, mv, mds, p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   bt_chunk_scan<D, false><<<sgrid, 256, 0, stream>>>(p.S, p.z, st, nullptr, nullptr, nullptr, 0, a.H,
