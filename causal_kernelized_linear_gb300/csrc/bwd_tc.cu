@@ -20,20 +20,23 @@
 // Passes (each CTA loops over a contiguous range of (head, chunk) items; 256
 // threads, two per token row r = TMEM lane r, each on one half of the row's
 // columns; one thread issues the MMAs and every product is waited for before
-// the rows use it; the next item's loads are issued as soon as the current
-// item's tiles are consumed):
+// the rows use it; each of the next item's loads is issued as soon as its
+// region is consumed):
 //   1. bt_state:  ΔS_c = K''ᵀV (K'' = w·a^{cs−1−s}φ(k)), Δz_c      → workspace
 //   2. scan:      S_c = exclusive decayed prefix of ΔS, as the bf16 operand
 //                 tile of pass 3 (z_c in fp32)                       (CUDA cores, float4)
-//   3. bt_dq:     recompute o, den; ∂q; den, ρ; ΔM_c = Q''ᵀĜ (Q'' = a^{t+1}φ(q)), ΔN_c
+//   3. bt_dq:     recompute o, den; ∂q; den, ρ; ΔM_c = Q''ᵀ∂o (Q'' = a^{t+1}φ(q)/den), ΔN_c
 //   4. scan:      M_c = reverse exclusive decayed suffix of ΔM, as the bf16
 //                 operand tile of pass 5; the ∂a share across each chunk
 //   5. bt_dkdv:   ∂k, ∂v
 //   6. ∂a:        sum of the per-chunk shares                       (CUDA cores)
-// The [128 × D] tiles arrive by TMA (tensor maps over the [B·H, n, D] rows) and
-// the operand tiles of S_c and M_c by bulk copies, on one barrier per item.
-// Every wait is bounded in time; on expiry the kernel records LA_ERR_TIMEOUT
-// in the device status word and stops.
+// The products take the ∂o tile as loaded (exact bf16) and the rows apply
+// 1/den in fp32, so ĝ is never rounded to bf16.  The [128 × D] tiles arrive by
+// TMA (tensor maps over the [B·H, n, D] rows) and the operand tiles of S_c and
+// M_c by bulk copies, on one barrier per item; ∂q, ∂k, ∂v, ΔS_c and ΔM_c leave
+// by TMA stores from swizzled staging tiles.  Every wait is bounded in time;
+// on expiry the kernel records LA_ERR_TIMEOUT in the device status word and
+// stops.
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
