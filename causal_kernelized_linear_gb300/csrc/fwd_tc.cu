@@ -206,9 +206,13 @@ __device__ __forceinline__ float pick4(const float (&v)[4], int i) {
 
 // The raw a and b of one chunk for a warp (lane j: tokens 32i + j), loaded
 // one chunk ahead of their use so that their latency overlaps a chunk's work.
+// The loads are unconditional (tokens past the end read the chunk's last
+// token) and the values stay as loaded until tok_chunk uses them: masking or
+// defaulting them here would make each load wait for its data at once.
 struct TokPipe {
   float a[4];
-  float b[4];
+  float b[4];   // as loaded (unused without a weight array)
+  int cs;       // valid tokens of the chunk
   int c;        // the chunk they belong to, −1 for none
 };
 
@@ -217,11 +221,11 @@ __device__ __forceinline__ void tok_load(const Ctx& x, int c, int lane, TokPipe&
   const int cs = (int)min((int64_t)kC, x.t_end - t0);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int s = 32 * i + lane;
-    const bool live = s < cs;
-    pp.a[i] = live ? __ldg(x.ta + t0 + s) : 1.f;
-    pp.b[i] = live ? (x.tb ? __ldg(x.tb + t0 + s) : 1.f - pp.a[i]) : 0.f;
+    const int s = min(32 * i + lane, cs - 1);
+    pp.a[i] = __ldg(x.ta + t0 + s);
+    if (x.tb) pp.b[i] = __ldg(x.tb + t0 + s);
   }
+  pp.cs = cs;
   pp.c = c;
 }
 
@@ -233,8 +237,9 @@ __device__ __forceinline__ TokChunk tok_chunk(const Ctx& x, int c, int lane, Tok
   float av[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    av[i] = pp.a[i];
-    t.B[i] = pp.b[i];
+    const bool live = 32 * i + lane < pp.cs;   // past the end: a = 1, b = 0
+    av[i] = live ? pp.a[i] : 1.f;
+    t.B[i] = live ? (x.tb ? pp.b[i] : 1.f - pp.a[i]) : 0.f;
   }
   if (c + 1 < x.nchunks) tok_load(x, c + 1, lane, pp);
   float run = 0.f;
