@@ -166,6 +166,7 @@ la_status validate_forward(const la_tensor* q, const la_tensor* k, const la_tens
   a->tok_decay = nullptr;
   a->tok_weight = nullptr;
   a->ws_ld = nullptr;
+  a->ws_tok = nullptr;
   a->omega = omega ? omega->data : nullptr;
   a->B = q->B;
   a->H = q->H;
@@ -280,6 +281,10 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
   // per-token decay: the log2 decay of every segment, beside its aggregate
   const bool need_ld = a.tok_decay != nullptr && plan.nseg > 1;
   if (need_ld) ws_floats += (size_t)BH * plan.nseg;
+  // per-token decay on the tensor-core elu+1 path: the per-token chunk prefixes
+  const bool need_tok = a.tok_decay != nullptr && tc_forward_supported(a);
+  const size_t tok_at = ws_floats + (need_tok ? (4 - ws_floats % 4) % 4 : 0);   // 16-byte aligned
+  if (need_tok) ws_floats = tok_at + 2 * (size_t)BH * a.n;
   float* ws = nullptr;
   if (ws_floats) {
     cudaError_t e = ws_alloc(reinterpret_cast<void**>(&ws), ws_floats * sizeof(float), stream);
@@ -297,6 +302,7 @@ la_status run_forward(FwdArgs& a, cudaStream_t stream) {
     tot_z = tot_state + (size_t)BH * state_elems;
   }
   if (need_ld) a.ws_ld = ws + (size_t)BH * slots * (state_elems + a.dp);
+  if (need_tok) a.ws_tok = ws + tok_at;
   cudaError_t e = dispatch_forward(a, pp, stream, ws_state, ws_z, tot_state, tot_z);
   if (ws) {
     cudaError_t f = cudaFreeAsync(ws, stream);

@@ -152,6 +152,8 @@ struct TcParams {
   const float* tok_decay;  // per-token decay [BH, n] or nullptr
   const float* tok_weight; // per-token weight [BH, n] or nullptr (1 − a)
   float* ws_ld;            // per-token decay: [BH][nseg] log2 decay of each segment
+  const float* tok_L;      // per-token decay: [BH, n] log2 prefix of a within each chunk
+  const float* tok_B;      // per-token decay: [BH, n] weight b (or 1 − a)
   int64_t H, n, seg_len;
   int nseg;
   float* ws_state;         // [BH][nseg][D*D]
@@ -185,7 +187,8 @@ struct Ctx {
   float lg;    // log2 a (centered folding; 0 for a = 1)
   int R;       // centered folding: the TMEM state is rescaled every R chunks
   const float* ta;   // per-token decay of this head (token 0 of the head), or nullptr
-  const float* tb;   // per-token weight of this head, or nullptr
+  const float* tl;   // its chunk prefixes L (tok_prefix_kernel), or nullptr
+  const float* tw;   // its weights B (tok_prefix_kernel), or nullptr
 };
 
 // Per-token decay of chunk c, computed by one warp (hardware lg2/ex2
@@ -204,14 +207,14 @@ __device__ __forceinline__ float pick4(const float (&v)[4], int i) {
   return i == 0 ? v[0] : (i == 1 ? v[1] : (i == 2 ? v[2] : v[3]));
 }
 
-// The raw a and b of one chunk for a warp (lane j: tokens 32i + j), loaded
-// one chunk ahead of their use so that their latency overlaps a chunk's work.
-// The loads are unconditional (tokens past the end read the chunk's last
-// token) and the values stay as loaded until tok_chunk uses them: masking or
-// defaulting them here would make each load wait for its data at once.
+// The precomputed L and B of one chunk for a warp (lane j: tokens 32i + j),
+// loaded one chunk ahead of their use so that their latency overlaps a
+// chunk's work.  The loads are unconditional (tokens past the end read the
+// chunk's last token) and the values stay as loaded until tok_chunk uses
+// them: masking them here would make each load wait for its data at once.
 struct TokPipe {
-  float a[4];
-  float b[4];   // as loaded (unused without a weight array)
+  float L[4];
+  float B[4];
   int cs;       // valid tokens of the chunk
   int c;        // the chunk they belong to, −1 for none
 };
@@ -222,26 +225,53 @@ __device__ __forceinline__ void tok_load(const Ctx& x, int c, int lane, TokPipe&
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int s = min(32 * i + lane, cs - 1);
-    pp.a[i] = __ldg(x.ta + t0 + s);
-    if (x.tb) pp.b[i] = __ldg(x.tb + t0 + s);
+    pp.L[i] = __ldg(x.tl + t0 + s);
+    pp.B[i] = __ldg(x.tw + t0 + s);
   }
   pp.cs = cs;
   pp.c = c;
 }
 
 // Chunk c's decay from the pipe (loading it now if the pipe holds another
-// chunk), then the loads of chunk c + 1 are issued.
+// chunk), then the loads of chunk c + 1 are issued.  L past the end is the
+// last token's (those tokens add no decay), so the chunk total is lane 31's
+// value of the last block.
 __device__ __forceinline__ TokChunk tok_chunk(const Ctx& x, int c, int lane, TokPipe& pp) {
   TokChunk t;
   if (pp.c != c) tok_load(x, c, lane, pp);
-  float av[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const bool live = 32 * i + lane < pp.cs;   // past the end: a = 1, b = 0
-    av[i] = live ? pp.a[i] : 1.f;
-    t.B[i] = live ? (x.tb ? pp.b[i] : 1.f - pp.a[i]) : 0.f;
+    t.L[i] = pp.L[i];
+    t.B[i] = 32 * i + lane < pp.cs ? pp.B[i] : 0.f;
   }
+  t.tot = __shfl_sync(0xffffffffu, pp.L[3], 31);
   if (c + 1 < x.nchunks) tok_load(x, c + 1, lane, pp);
+  return t;
+}
+
+// The per-token decay of every 128-token chunk of every head, once before the
+// tensor-core launches (one warp per chunk): L_t = Σ_{s ≤ t} max(log2 a_s, −64)
+// from the chunk's first token (hardware lg2; its relative error, ≈ 2^-22, is
+// far below the bf16 rounding the factors get as tensor-core operands), and
+// B_t = b_t (1 − a_t without a weight array).  tok_load / tok_chunk read them.
+__global__ void __launch_bounds__(128)
+tok_prefix_kernel(const float* __restrict__ ta, const float* __restrict__ tb,
+                  float* __restrict__ L, float* __restrict__ B, int64_t n, int64_t nch,
+                  int64_t chunks) {
+  const int64_t wid = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= chunks) return;
+  const int64_t bh = wid / nch;
+  const int64_t t0 = (wid % nch) * kC;
+  const int cs = (int)min((int64_t)kC, n - t0);
+  const int64_t base = bh * n + t0;
+  float av[4], bv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int s = 32 * i + lane;
+    av[i] = s < cs ? ta[base + s] : 1.f;
+    bv[i] = s < cs ? (tb ? tb[base + s] : 1.f - av[i]) : 0.f;
+  }
   float run = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -251,11 +281,13 @@ __device__ __forceinline__ TokChunk tok_chunk(const Ctx& x, int c, int lane, Tok
       const float u = __shfl_up_sync(0xffffffffu, v, o);
       if (lane >= o) v += u;
     }
-    t.L[i] = run + v;
+    const int s = 32 * i + lane;
+    if (s < cs) {
+      L[base + s] = run + v;
+      B[base + s] = bv[i];
+    }
     run += __shfl_sync(0xffffffffu, v, 31);
   }
-  t.tot = run;
-  return t;
 }
 
 // Per-warp running state of the per-token decay, advanced by φ(K) chunk by
@@ -1120,7 +1152,8 @@ tc_forward_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   x.a = p.decay ? p.decay[x.bh % p.H] : 1.f;
   x.w = new_token_weight(x.a);
   x.ta = TOK ? p.tok_decay + x.bh * p.n : nullptr;
-  x.tb = (TOK && p.tok_weight) ? p.tok_weight + x.bh * p.n : nullptr;
+  x.tl = TOK ? p.tok_L + x.bh * p.n : nullptr;
+  x.tw = TOK ? p.tok_B + x.bh * p.n : nullptr;
   // the per-token decay takes the centered folding when the whole segment
   // fits it, the general folding otherwise
   const bool cen = TOK ? tok_centered_ok(x, warp, lane)
@@ -1212,6 +1245,8 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
   p.tok_decay = a.tok_decay;
   p.tok_weight = a.tok_weight;
   p.ws_ld = a.ws_ld;
+  p.tok_L = a.ws_tok;
+  p.tok_B = a.ws_tok ? a.ws_tok + (size_t)BH * a.n : nullptr;
   p.H = a.H;
   p.n = a.n;
   p.seg_len = plan.seg_len;
@@ -1233,6 +1268,15 @@ cudaError_t run_tc(const FwdArgs& a, cudaStream_t stream, float* ws_state, float
     e = cudaMemcpy2DAsync(ws_z, nslot * D * sizeof(float), a.init_z, (size_t)D * sizeof(float),
                           (size_t)D * sizeof(float), (size_t)BH, cudaMemcpyDeviceToDevice, stream);
     if (e != cudaSuccess) return e;
+  }
+  if (TOK) {
+    // the per-token chunk prefixes and weights, read by every role that needs them
+    if (!a.ws_tok) return cudaErrorInvalidValue;
+    const int64_t nch = (a.n + kC - 1) / kC, chunks = BH * nch;
+    tok_prefix_kernel<<<(unsigned)((chunks + 3) / 4), 128, 0, stream>>>(
+        a.tok_decay, a.tok_weight, a.ws_tok, a.ws_tok + (size_t)BH * a.n, a.n, nch, chunks);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (plan.nseg > 1) {
     // aggregates of segments 0 … nseg−2 (nothing follows the last one)

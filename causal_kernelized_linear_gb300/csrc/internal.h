@@ -21,6 +21,8 @@ struct FwdArgs {
   const float* tok_decay;   // device [B,H,n] per-token decay, or nullptr
   const float* tok_weight;  // device [B,H,n] per-token input weight, or nullptr (1 − a)
   float* ws_ld;         // per-token decay, nseg > 1: [B·H][nseg] log2 decay of each segment
+  float* ws_tok;        // per-token decay, tensor-core path: [2][B·H][n], the log2 prefix of
+                        // a within each 128-token chunk, then the weight b (or 1 − a)
   const void* omega;    // device [d, m] (Performer) or nullptr
   int64_t B, H, n;
   int d;                // value / input width
