@@ -414,9 +414,16 @@ __device__ __forceinline__ void role_phi(const PCtx& x, const PParams& p, int wa
       const float a0 = ex2_approx(fmaf(__uint_as_float(u[2 * j]), kLog2e, -off));
       const float a1 = ex2_approx(fmaf(__uint_as_float(u[2 * j + 1]), kLog2e, -off));
       pkd[j] = live ? pack_bf16x2(a0, a1) : 0u;
-      // with the bf16 values the tensor core sees in φ(Q)·S
-      if (!is_k)
-        qz += bf16lo_to_f32(pkd[j]) * zf[f0 + 2 * j] + bf16hi_to_f32(pkd[j]) * zf[f0 + 2 * j + 1];
+    }
+    if (!is_k) {
+      // q'·z with the bf16 values the tensor core sees in φ(Q)·S; z by 16-byte
+      // broadcast loads (f0 is a multiple of 64)
+#pragma unroll
+      for (int j4 = 0; j4 < 16; ++j4) {
+        const float4 z4 = *reinterpret_cast<const float4*>(zf + f0 + 4 * j4);
+        qz += bf16lo_to_f32(pkd[2 * j4]) * z4.x + bf16hi_to_f32(pkd[2 * j4]) * z4.y +
+              bf16lo_to_f32(pkd[2 * j4 + 1]) * z4.z + bf16hi_to_f32(pkd[2 * j4 + 1]) * z4.w;
+      }
     }
     if (is_k) {
       const uint32_t base = x.sbase + Cfg::oKP + (2 * f + half) * Cfg::TILE;
